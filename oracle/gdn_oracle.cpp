@@ -1,0 +1,380 @@
+// gdn_oracle.cpp -- TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, obviously correct CPU statement of the Gated DeltaNet
+// recurrence, forward and reverse-mode backward, token by token, in f64.  It
+// shares no code with the CUDA path: only tests/, the smoke check and the CPU
+// baseline leg of bench.py may load it.
+//
+// What it follows (lattice-inference 0.6.0, src/attention/gdn_backward.rs, as
+// shown on docs.rs):
+//   * module header "Forward recap": per value head h the key head is h / ratio;
+//     g = exp(-exp(a_log[h]) * softplus(alpha + dt_bias[h])); retrieval from the
+//     pre-decayed state kv_mem = S_{t-1}^T k_hat; delta = (v - g kv_mem) beta;
+//     S_t = g S_{t-1} + k_hat delta^T; o_t = scale S_t^T q_hat, scale = 1/sqrt(Dk).
+//   * gdn_forward_save, "L2-normalize q, k": q_hat = q / sqrt(|q|^2 + 1e-6) (the
+//     eps-stabilised denominator is the one used; the max-clamped norm is only
+//     saved there).
+//   * gdn_backward, section 4 "Per value-head recurrence backward", steps 4a-4h
+//     (o backward, state-update backward, delta backward, retrieval backward,
+//     gate backward, L2-norm backward, accumulation over the value heads that
+//     share a key head, sigmoid backward).  d_beta is formed without dividing by
+//     beta, as step 4c there does.
+// Readings where the page is silent (each is listed in the design doc):
+//   * S_0 and dS_T are inputs (zero when absent); dS_0 is returned.
+//   * d a_log[h] = sum over every token of every sequence of dl * l (dl/d a_log
+//     = l because l = -exp(a_log) softplus(x)); d dt_bias[h] = sum of d alpha.
+//   * softplus(x) = max(x, 0) + log1p(exp(-|x|)), the exact log(1 + e^x).
+//   * varlen: each sequence of cu_seqlens starts from its own S_0[n].
+//
+// Memory: the backward keeps a state checkpoint every `segment` tokens and
+// recomputes the states inside one segment before walking it in reverse.
+// Work is split over (sequence, key head) units on std::threads; the only
+// cross-unit sums (d a_log, d dt_bias) are reduced in sequence order after
+// the threads join, so results do not depend on the thread count.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+extern "C" {
+
+typedef struct {
+  int32_t Hk, Hv, Dk, Dv;
+  int32_t n_seqs;
+  int64_t total_tokens;
+  double scale;       // <= 0 selects 1/sqrt(Dk)
+  int32_t n_threads;  // <= 0 selects std::thread::hardware_concurrency()
+  int32_t segment;    // backward checkpoint interval in tokens; <= 0 selects 64
+} gdn_oracle_shape;
+
+typedef struct {
+  const double* q;        int64_t q_ld;      // [T, q_ld], key head kh at column kh*Dk
+  const double* k;        int64_t k_ld;      // [T, k_ld], key head kh at column kh*Dk
+  const double* v;        int64_t v_ld;      // [T, v_ld], value head h at column h*Dv
+  const double* alpha;    int64_t alpha_ld;  // [T, alpha_ld], column h
+  const double* beta_raw; int64_t beta_ld;   // [T, beta_ld], column h
+  const double* a_log;                       // [Hv]
+  const double* dt_bias;                     // [Hv]
+  const int32_t* cu_seqlens;                 // [n_seqs + 1]
+  const double* S0;                          // [n_seqs, Hv, Dk, Dv] or NULL (zero)
+} gdn_oracle_inputs;
+
+int gdn_oracle_forward(const gdn_oracle_shape* shape, const gdn_oracle_inputs* in,
+                       double* o, int64_t o_ld, double* S_T);
+// As gdn_oracle_forward, and also writes the state at the start of every
+// `chunk`-token chunk of every sequence: chunk_states[c, Hv, Dk, Dv] with the
+// chunks of sequence n numbered from chunk_offsets[n] (chunks never span two
+// sequences; the last chunk of a sequence may be short).
+int gdn_oracle_forward_states(const gdn_oracle_shape* shape, const gdn_oracle_inputs* in,
+                              double* o, int64_t o_ld, double* S_T, int32_t chunk,
+                              const int32_t* chunk_offsets, double* chunk_states);
+int gdn_oracle_backward(const gdn_oracle_shape* shape, const gdn_oracle_inputs* in,
+                        const double* dO, int64_t dO_ld, const double* dS_T,
+                        double* dq, int64_t dq_ld, double* dk, int64_t dk_ld,
+                        double* dv, int64_t dv_ld, double* dalpha, int64_t dalpha_ld,
+                        double* dbeta_raw, int64_t dbeta_ld, double* da_log,
+                        double* ddt_bias, double* dS0);
+int gdn_oracle_hardware_threads(void);
+
+}  // extern "C"
+
+namespace {
+
+double softplus(double x) { return std::max(x, 0.0) + std::log1p(std::exp(-std::fabs(x))); }
+double sigmoid(double x) { return 1.0 / (1.0 + std::exp(-x)); }
+
+struct Dims {
+  int Hk, Hv, Dk, Dv, r;
+  double scale;
+  int64_t DkDv() const { return (int64_t)Dk * Dv; }
+};
+
+// Gate quantities of value head h at token t.
+struct Gate {
+  double b;  // beta = sigmoid(beta_raw)
+  double x;  // alpha + dt_bias
+  double l;  // log g = -exp(a_log) softplus(x)
+  double g;  // decay
+};
+
+Gate gate_at(const gdn_oracle_inputs& in, int64_t t, int h) {
+  Gate G;
+  G.b = sigmoid(in.beta_raw[t * in.beta_ld + h]);
+  G.x = in.alpha[t * in.alpha_ld + h] + in.dt_bias[h];
+  G.l = -std::exp(in.a_log[h]) * softplus(G.x);
+  G.g = std::exp(G.l);
+  return G;
+}
+
+// xhat = x / sqrt(|x|^2 + 1e-6); returns the denominator.
+double l2_normalise(const double* x, int D, double* xhat) {
+  double ss = 0.0;
+  for (int i = 0; i < D; ++i) ss += x[i] * x[i];
+  const double n = std::sqrt(ss + 1e-6);
+  for (int i = 0; i < D; ++i) xhat[i] = x[i] / n;
+  return n;
+}
+
+// One forward token step of one value head.  S is Dk x Dv row-major and is
+// updated in place; kv (retrieval) and delta are returned for the caller.
+void token_step(const Dims& d, double* S, const double* khat, const double* v, const Gate& G,
+                double* kv, double* delta) {
+  for (int j = 0; j < d.Dv; ++j) kv[j] = 0.0;
+  for (int i = 0; i < d.Dk; ++i)
+    for (int j = 0; j < d.Dv; ++j) kv[j] += S[(int64_t)i * d.Dv + j] * khat[i];
+  for (int j = 0; j < d.Dv; ++j) delta[j] = G.b * (v[j] - G.g * kv[j]);
+  for (int i = 0; i < d.Dk; ++i)
+    for (int j = 0; j < d.Dv; ++j)
+      S[(int64_t)i * d.Dv + j] = G.g * S[(int64_t)i * d.Dv + j] + khat[i] * delta[j];
+}
+
+template <typename F>
+void run_units(int n_units, int n_threads, F&& fn) {
+  if (n_threads <= 0) n_threads = (int)std::max(1u, std::thread::hardware_concurrency());
+  n_threads = std::max(1, std::min(n_threads, n_units));
+  std::atomic<int> next{0};
+  auto worker = [&]() {
+    for (;;) {
+      const int u = next.fetch_add(1);
+      if (u >= n_units) return;
+      fn(u);
+    }
+  };
+  if (n_threads == 1) {
+    worker();
+    return;
+  }
+  std::vector<std::thread> pool;
+  for (int i = 0; i < n_threads; ++i) pool.emplace_back(worker);
+  for (auto& th : pool) th.join();
+}
+
+int check_shape(const gdn_oracle_shape* s, const gdn_oracle_inputs* in, Dims* d) {
+  if (!s || !in) return -1;
+  if (s->Hk <= 0 || s->Hv <= 0 || s->Dk <= 0 || s->Dv <= 0 || s->n_seqs < 0) return -1;
+  if (s->Hv % s->Hk != 0) return -1;
+  if (!in->cu_seqlens) return -1;
+  if (in->cu_seqlens[0] != 0 || in->cu_seqlens[s->n_seqs] != s->total_tokens) return -1;
+  for (int n = 0; n < s->n_seqs; ++n)
+    if (in->cu_seqlens[n + 1] < in->cu_seqlens[n]) return -1;
+  d->Hk = s->Hk;
+  d->Hv = s->Hv;
+  d->Dk = s->Dk;
+  d->Dv = s->Dv;
+  d->r = s->Hv / s->Hk;
+  d->scale = s->scale > 0.0 ? s->scale : 1.0 / std::sqrt((double)s->Dk);
+  return 0;
+}
+
+}  // namespace
+
+extern "C" int gdn_oracle_hardware_threads(void) {
+  return (int)std::max(1u, std::thread::hardware_concurrency());
+}
+
+extern "C" int gdn_oracle_forward(const gdn_oracle_shape* shape, const gdn_oracle_inputs* inp,
+                                  double* o, int64_t o_ld, double* S_T) {
+  return gdn_oracle_forward_states(shape, inp, o, o_ld, S_T, 0, nullptr, nullptr);
+}
+
+extern "C" int gdn_oracle_forward_states(const gdn_oracle_shape* shape,
+                                         const gdn_oracle_inputs* inp, double* o, int64_t o_ld,
+                                         double* S_T, int32_t chunk,
+                                         const int32_t* chunk_offsets, double* chunk_states) {
+  Dims d;
+  if (check_shape(shape, inp, &d) != 0 || !o) return -1;
+  if (chunk_states && (chunk <= 0 || !chunk_offsets)) return -1;
+  const gdn_oracle_inputs& in = *inp;
+  const int n_units = shape->n_seqs * d.Hk;
+  run_units(n_units, shape->n_threads, [&](int u) {
+    const int n = u / d.Hk, kh = u % d.Hk;
+    const int64_t t0 = in.cu_seqlens[n], t1 = in.cu_seqlens[n + 1];
+    std::vector<double> S((size_t)d.r * d.DkDv(), 0.0);
+    if (in.S0)
+      for (int hh = 0; hh < d.r; ++hh)
+        std::memcpy(&S[(size_t)hh * d.DkDv()], in.S0 + ((int64_t)n * d.Hv + kh * d.r + hh) * d.DkDv(),
+                    sizeof(double) * d.DkDv());
+    std::vector<double> qh(d.Dk), kh_(d.Dk), kv(d.Dv), delta(d.Dv);
+    for (int64_t t = t0; t < t1; ++t) {
+      if (chunk_states && (t - t0) % chunk == 0) {
+        const int64_t c = chunk_offsets[n] + (t - t0) / chunk;
+        for (int hh = 0; hh < d.r; ++hh)
+          std::memcpy(chunk_states + (c * d.Hv + kh * d.r + hh) * d.DkDv(), &S[(size_t)hh * d.DkDv()],
+                      sizeof(double) * d.DkDv());
+      }
+      l2_normalise(in.q + t * in.q_ld + (int64_t)kh * d.Dk, d.Dk, qh.data());
+      l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, kh_.data());
+      for (int hh = 0; hh < d.r; ++hh) {
+        const int h = kh * d.r + hh;
+        double* Sh = &S[(size_t)hh * d.DkDv()];
+        const Gate G = gate_at(in, t, h);
+        token_step(d, Sh, kh_.data(), in.v + t * in.v_ld + (int64_t)h * d.Dv, G, kv.data(),
+                   delta.data());
+        double* orow = o + t * o_ld + (int64_t)h * d.Dv;
+        for (int j = 0; j < d.Dv; ++j) orow[j] = 0.0;
+        for (int i = 0; i < d.Dk; ++i)
+          for (int j = 0; j < d.Dv; ++j) orow[j] += Sh[(int64_t)i * d.Dv + j] * qh[i];
+        for (int j = 0; j < d.Dv; ++j) orow[j] *= d.scale;
+      }
+    }
+    if (S_T)
+      for (int hh = 0; hh < d.r; ++hh)
+        std::memcpy(S_T + ((int64_t)n * d.Hv + kh * d.r + hh) * d.DkDv(), &S[(size_t)hh * d.DkDv()],
+                    sizeof(double) * d.DkDv());
+  });
+  return 0;
+}
+
+extern "C" int gdn_oracle_backward(const gdn_oracle_shape* shape, const gdn_oracle_inputs* inp,
+                                   const double* dO, int64_t dO_ld, const double* dS_T,
+                                   double* dq, int64_t dq_ld, double* dk, int64_t dk_ld,
+                                   double* dv, int64_t dv_ld, double* dalpha, int64_t dalpha_ld,
+                                   double* dbeta_raw, int64_t dbeta_ld, double* da_log,
+                                   double* ddt_bias, double* dS0) {
+  Dims d;
+  if (check_shape(shape, inp, &d) != 0) return -1;
+  if (!dO || !dq || !dk || !dv || !dalpha || !dbeta_raw || !da_log || !ddt_bias) return -1;
+  const gdn_oracle_inputs& in = *inp;
+  const int seg = shape->segment > 0 ? shape->segment : 64;
+  const int N = shape->n_seqs;
+  // Per (sequence, value head) partial sums of d a_log and d dt_bias.
+  std::vector<double> pa((size_t)std::max(N, 1) * d.Hv, 0.0), pd((size_t)std::max(N, 1) * d.Hv, 0.0);
+  const int n_units = N * d.Hk;
+  run_units(n_units, shape->n_threads, [&](int u) {
+    const int n = u / d.Hk, kh = u % d.Hk;
+    const int64_t t0 = in.cu_seqlens[n], t1 = in.cu_seqlens[n + 1];
+    const int64_t L = t1 - t0;
+    const int64_t n_seg = (L + seg - 1) / seg;
+    const size_t SZ = (size_t)d.DkDv();
+    // Checkpoints: state of each value head of the group before token t0 + s*seg.
+    std::vector<double> ck((size_t)std::max<int64_t>(n_seg, 1) * d.r * SZ, 0.0);
+    std::vector<double> S((size_t)d.r * SZ, 0.0);
+    if (in.S0)
+      for (int hh = 0; hh < d.r; ++hh)
+        std::memcpy(&S[hh * SZ], in.S0 + ((int64_t)n * d.Hv + kh * d.r + hh) * SZ, sizeof(double) * SZ);
+    std::vector<double> qh(d.Dk), khat(d.Dk), kv(d.Dv), delta(d.Dv);
+    for (int64_t t = t0; t < t1; ++t) {
+      if ((t - t0) % seg == 0)
+        std::memcpy(&ck[(size_t)((t - t0) / seg) * d.r * SZ], S.data(), sizeof(double) * d.r * SZ);
+      l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, khat.data());
+      for (int hh = 0; hh < d.r; ++hh) {
+        const int h = kh * d.r + hh;
+        token_step(d, &S[hh * SZ], khat.data(), in.v + t * in.v_ld + (int64_t)h * d.Dv,
+                   gate_at(in, t, h), kv.data(), delta.data());
+      }
+    }
+    // Adjoint of the state, one per value head of the group.
+    std::vector<double> dS((size_t)d.r * SZ, 0.0);
+    if (dS_T)
+      for (int hh = 0; hh < d.r; ++hh)
+        std::memcpy(&dS[hh * SZ], dS_T + ((int64_t)n * d.Hv + kh * d.r + hh) * SZ, sizeof(double) * SZ);
+    // States before each token of the current segment (plus the one after its end).
+    std::vector<double> Sbuf((size_t)(seg + 1) * d.r * SZ);
+    std::vector<double> S_t(SZ), dqh(d.Dk), dkh(d.Dk), ddelta(d.Dv), dkv(d.Dv);
+    std::vector<double> dq_acc(d.Dk), dk_acc(d.Dk);
+    for (int64_t s = n_seg - 1; s >= 0; --s) {
+      const int64_t ta = t0 + s * seg, tb = std::min<int64_t>(ta + seg, t1);
+      std::memcpy(&Sbuf[0], &ck[(size_t)s * d.r * SZ], sizeof(double) * d.r * SZ);
+      for (int64_t t = ta; t < tb; ++t) {
+        l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, khat.data());
+        double* nxt = &Sbuf[(size_t)(t - ta + 1) * d.r * SZ];
+        std::memcpy(nxt, &Sbuf[(size_t)(t - ta) * d.r * SZ], sizeof(double) * d.r * SZ);
+        for (int hh = 0; hh < d.r; ++hh) {
+          const int h = kh * d.r + hh;
+          token_step(d, nxt + hh * SZ, khat.data(), in.v + t * in.v_ld + (int64_t)h * d.Dv,
+                     gate_at(in, t, h), kv.data(), delta.data());
+        }
+      }
+      for (int64_t t = tb - 1; t >= ta; --t) {
+        const double nq = l2_normalise(in.q + t * in.q_ld + (int64_t)kh * d.Dk, d.Dk, qh.data());
+        const double nk = l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, khat.data());
+        std::fill(dq_acc.begin(), dq_acc.end(), 0.0);
+        std::fill(dk_acc.begin(), dk_acc.end(), 0.0);
+        for (int hh = 0; hh < d.r; ++hh) {
+          const int h = kh * d.r + hh;
+          const double* S_prev = &Sbuf[(size_t)(t - ta) * d.r * SZ + hh * SZ];
+          const double* vrow = in.v + t * in.v_ld + (int64_t)h * d.Dv;
+          const double* dOrow = dO + t * dO_ld + (int64_t)h * d.Dv;
+          double* dSh = &dS[hh * SZ];
+          const Gate G = gate_at(in, t, h);
+          // Recompute this token's forward quantities from the state before it.
+          std::memcpy(S_t.data(), S_prev, sizeof(double) * SZ);
+          token_step(d, S_t.data(), khat.data(), vrow, G, kv.data(), delta.data());
+          // 4a: o = scale S_t^T q_hat.
+          for (int i = 0; i < d.Dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < d.Dv; ++j) {
+              dSh[(int64_t)i * d.Dv + j] += d.scale * qh[i] * dOrow[j];
+              acc += S_t[(int64_t)i * d.Dv + j] * dOrow[j];
+            }
+            dqh[i] = d.scale * acc;
+          }
+          // 4b: S_t = g S_prev + k_hat delta^T.
+          double dg = 0.0;
+          std::fill(dkh.begin(), dkh.end(), 0.0);
+          std::fill(ddelta.begin(), ddelta.end(), 0.0);
+          for (int i = 0; i < d.Dk; ++i)
+            for (int j = 0; j < d.Dv; ++j) {
+              const double ds = dSh[(int64_t)i * d.Dv + j];
+              dg += S_prev[(int64_t)i * d.Dv + j] * ds;
+              dkh[i] += ds * delta[j];
+              ddelta[j] += ds * khat[i];
+            }
+          for (size_t e = 0; e < SZ; ++e) dSh[e] *= G.g;
+          // 4c: delta = beta (v - g kv).
+          double db = 0.0;
+          for (int j = 0; j < d.Dv; ++j) {
+            dv[t * dv_ld + (int64_t)h * d.Dv + j] = G.b * ddelta[j];
+            dkv[j] = -G.g * G.b * ddelta[j];
+            dg += -kv[j] * G.b * ddelta[j];
+            db += (vrow[j] - G.g * kv[j]) * ddelta[j];
+          }
+          // 4d: kv = S_prev^T k_hat.
+          for (int i = 0; i < d.Dk; ++i)
+            for (int j = 0; j < d.Dv; ++j) {
+              dSh[(int64_t)i * d.Dv + j] += khat[i] * dkv[j];
+              dkh[i] += S_prev[(int64_t)i * d.Dv + j] * dkv[j];
+            }
+          // 4e: g = exp(l), l = -exp(a_log) softplus(x), softplus' = sigmoid.
+          const double dl = dg * G.g;
+          const double da = dl * (-std::exp(in.a_log[h])) * sigmoid(G.x);
+          dalpha[t * dalpha_ld + h] = da;
+          pa[(size_t)n * d.Hv + h] += dl * G.l;
+          pd[(size_t)n * d.Hv + h] += da;
+          // 4f + 4g: L2-norm backward, summed over the value heads of this key head.
+          double dot_q = 0.0, dot_k = 0.0;
+          for (int i = 0; i < d.Dk; ++i) {
+            dot_q += dqh[i] * qh[i];
+            dot_k += dkh[i] * khat[i];
+          }
+          for (int i = 0; i < d.Dk; ++i) {
+            dq_acc[i] += (dqh[i] - qh[i] * dot_q) / nq;
+            dk_acc[i] += (dkh[i] - khat[i] * dot_k) / nk;
+          }
+          // 4h: beta = sigmoid(beta_raw).
+          dbeta_raw[t * dbeta_ld + h] = db * G.b * (1.0 - G.b);
+        }
+        for (int i = 0; i < d.Dk; ++i) {
+          dq[t * dq_ld + (int64_t)kh * d.Dk + i] = dq_acc[i];
+          dk[t * dk_ld + (int64_t)kh * d.Dk + i] = dk_acc[i];
+        }
+      }
+    }
+    if (dS0)
+      for (int hh = 0; hh < d.r; ++hh)
+        std::memcpy(dS0 + ((int64_t)n * d.Hv + kh * d.r + hh) * SZ, &dS[hh * SZ], sizeof(double) * SZ);
+  });
+  for (int h = 0; h < d.Hv; ++h) {
+    double a = 0.0, b = 0.0;
+    for (int n = 0; n < N; ++n) {
+      a += pa[(size_t)n * d.Hv + h];
+      b += pd[(size_t)n * d.Hv + h];
+    }
+    da_log[h] = a;
+    ddt_bias[h] = b;
+  }
+  return 0;
+}
