@@ -1,0 +1,219 @@
+"""Python binding of libgdn.so, the GB300 Gated DeltaNet library.
+
+Argument marshalling only: every step of the forward and backward runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.  The names
+mirror the C ABI in ``include/gdn.h``:
+
+    gdn_plan, gdn_saved_state_bytes, gdn_workspace_bytes,
+    gdn_forward, gdn_backward, gdn_read_device_status, gdn_status_string
+
+Tensors are passed as (data pointer, row stride); a 2-D tensor must have unit
+column stride, so q/k/v may be column slices of one packed projection.  There
+is no fallback: importing this package fails loudly when libgdn.so is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libgdn.so is not built (%s); run `python gated_deltanet_backward_gb300/build.py` "
+        "or __graft_entry__.build()" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+GDN_OK = 0
+GDN_DTYPE_F32 = 0
+GDN_DTYPE_BF16 = 1
+CHUNK = 64
+
+
+class gdn_shape(ctypes.Structure):
+    _fields_ = [("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32),
+                ("Dv", ctypes.c_int32), ("n_seqs", ctypes.c_int32),
+                ("total_chunks", ctypes.c_int32), ("total_tokens", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_SP = ctypes.POINTER(gdn_shape)
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+_lib.gdn_plan.argtypes = [_I32P, ctypes.c_int32, _I32P, _I32P]
+_lib.gdn_plan.restype = ctypes.c_int
+_lib.gdn_saved_state_bytes.argtypes = [_SP]
+_lib.gdn_saved_state_bytes.restype = _sz
+_lib.gdn_workspace_bytes.argtypes = [_SP, ctypes.c_int]
+_lib.gdn_workspace_bytes.restype = _sz
+# shape; q,k,v,alpha,beta_raw (+ld); a_log, dt_bias, cu, coff, S0; o (+ld); S_T, saved, ws,
+# ws bytes, stream
+_lib.gdn_forward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] +
+                             [_vp, _vp, _vp, _sz, _vp])
+_lib.gdn_forward.restype = ctypes.c_int
+# shape; q,k,v,alpha,beta_raw (+ld); a_log, dt_bias, cu, coff, S0; dO (+ld); dS_T, saved;
+# dq,dk,dv,dalpha,dbeta_raw (+ld); da_log, ddt_bias, dS0, ws, ws bytes, stream
+_lib.gdn_backward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] + [_vp, _vp] +
+                              [_vp, _i64] * 5 + [_vp, _vp, _vp, _vp, _sz, _vp])
+_lib.gdn_backward.restype = ctypes.c_int
+_lib.gdn_read_device_status.argtypes = [_vp, _vp]
+_lib.gdn_read_device_status.restype = ctypes.c_int
+_lib.gdn_status_string.argtypes = [ctypes.c_int]
+_lib.gdn_status_string.restype = ctypes.c_char_p
+
+EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_forward",
+            "gdn_backward", "gdn_read_device_status", "gdn_status_string")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (where, gdn_status_string(code), code))
+
+
+def gdn_status_string(code: int) -> str:
+    return _lib.gdn_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != GDN_OK:
+        raise GdnError(code, where)
+
+
+def gdn_plan(cu_seqlens_host) -> tuple:
+    """Host cu_seqlens -> (chunk_offsets int32 [n_seqs+1], total_chunks)."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens_host), dtype=np.int32)
+    n = len(cu) - 1
+    off = np.zeros(n + 1, dtype=np.int32)
+    tot = ctypes.c_int32(0)
+    _check(_lib.gdn_plan(cu.ctypes.data_as(_I32P), n, off.ctypes.data_as(_I32P),
+                         ctypes.byref(tot)), "gdn_plan")
+    return off, int(tot.value)
+
+
+def make_shape(Hk, Hv, Dk, Dv, n_seqs, total_chunks, total_tokens, dtype, scale=0.0) -> gdn_shape:
+    if not isinstance(dtype, int):
+        dtype = GDN_DTYPE_BF16 if str(dtype) in ("bf16", "torch.bfloat16") else GDN_DTYPE_F32
+    return gdn_shape(int(Hk), int(Hv), int(Dk), int(Dv), int(n_seqs), int(total_chunks),
+                     int(total_tokens), int(dtype), float(scale or 0.0))
+
+
+def gdn_saved_state_bytes(shape: gdn_shape) -> int:
+    return int(_lib.gdn_saved_state_bytes(ctypes.byref(shape)))
+
+
+def gdn_workspace_bytes(shape: gdn_shape, is_backward: bool) -> int:
+    return int(_lib.gdn_workspace_bytes(ctypes.byref(shape), 1 if is_backward else 0))
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return int(t.data_ptr())
+
+
+def _mat(t):
+    """(pointer, row stride in elements) of a 2-D tensor with unit column stride."""
+    if t is None:
+        return None, 0
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor, got shape %s" % (tuple(t.shape),))
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("columns must be contiguous (stride(1) == 1)")
+    return int(t.data_ptr()), int(t.stride(0))
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def gdn_forward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, chunk_offsets, S0,
+                o, S_T, saved_states, workspace, stream=None) -> None:
+    """Calls gdn_forward.  All tensors are CUDA tensors (S0 / S_T may be None)."""
+    args = [ctypes.byref(shape)]
+    for t in (q, k, v, alpha, beta_raw):
+        args += list(_mat(t))
+    args += [_ptr(a_log), _ptr(dt_bias), _ptr(cu_seqlens), _ptr(chunk_offsets), _ptr(S0)]
+    args += list(_mat(o))
+    args += [_ptr(S_T), _ptr(saved_states), _ptr(workspace),
+             int(workspace.numel() * workspace.element_size()), _stream(stream)]
+    _check(_lib.gdn_forward(*args), "gdn_forward")
+
+
+def gdn_backward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, chunk_offsets, S0,
+                 dO, dS_T, saved_states, dq, dk, dv, dalpha, dbeta_raw, da_log, ddt_bias, dS0,
+                 workspace, stream=None) -> None:
+    """Calls gdn_backward.  All tensors are CUDA tensors (S0, dS_T, dS0 may be None)."""
+    args = [ctypes.byref(shape)]
+    for t in (q, k, v, alpha, beta_raw):
+        args += list(_mat(t))
+    args += [_ptr(a_log), _ptr(dt_bias), _ptr(cu_seqlens), _ptr(chunk_offsets), _ptr(S0)]
+    args += list(_mat(dO))
+    args += [_ptr(dS_T), _ptr(saved_states)]
+    for t in (dq, dk, dv, dalpha, dbeta_raw):
+        args += list(_mat(t))
+    args += [_ptr(da_log), _ptr(ddt_bias), _ptr(dS0), _ptr(workspace),
+             int(workspace.numel() * workspace.element_size()), _stream(stream)]
+    _check(_lib.gdn_backward(*args), "gdn_backward")
+
+
+def gdn_read_device_status(workspace, stream=None) -> int:
+    return int(_lib.gdn_read_device_status(_ptr(workspace), _stream(stream)))
+
+
+@dataclass
+class Layer:
+    """Device buffers for one varlen batch: shape, plan, saved states, workspaces.
+
+    A convenience holder for callers of gdn_forward / gdn_backward; it only
+    allocates (through PyTorch) and forwards arguments.
+    """
+    shape: gdn_shape
+    cu_seqlens: object
+    chunk_offsets: object
+    saved_states: object
+    ws_fwd: object
+    ws_bwd: object
+
+    @classmethod
+    def create(cls, Hk, Hv, Dk, Dv, cu_seqlens_host, dtype, scale=0.0, device="cuda"):
+        import torch
+        off, nc = gdn_plan(cu_seqlens_host)
+        cu = np.asarray(cu_seqlens_host, dtype=np.int32)
+        shape = make_shape(Hk, Hv, Dk, Dv, len(cu) - 1, nc, int(cu[-1]), dtype, scale)
+        saved = torch.empty(max(4, gdn_saved_state_bytes(shape) // 4), dtype=torch.float32,
+                            device=device)
+        ws_f = torch.empty(max(256, gdn_workspace_bytes(shape, False)), dtype=torch.uint8,
+                           device=device)
+        ws_b = torch.empty(max(256, gdn_workspace_bytes(shape, True)), dtype=torch.uint8,
+                           device=device)
+        return cls(shape, torch.from_numpy(cu).to(device), torch.from_numpy(off).to(device),
+                   saved, ws_f, ws_b)
+
+    def forward(self, q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream=None):
+        gdn_forward(self.shape, q, k, v, alpha, beta_raw, a_log, dt_bias, self.cu_seqlens,
+                    self.chunk_offsets, S0, o, S_T, self.saved_states, self.ws_fwd, stream)
+
+    def backward(self, q, k, v, alpha, beta_raw, a_log, dt_bias, S0, dO, dS_T, dq, dk, dv,
+                 dalpha, dbeta_raw, da_log, ddt_bias, dS0, stream=None):
+        gdn_backward(self.shape, q, k, v, alpha, beta_raw, a_log, dt_bias, self.cu_seqlens,
+                     self.chunk_offsets, S0, dO, dS_T, self.saved_states, dq, dk, dv, dalpha,
+                     dbeta_raw, da_log, ddt_bias, dS0, self.ws_bwd, stream)
+
+
+__all__ = list(EXPORTED) + ["gdn_shape", "make_shape", "Layer", "GdnError", "LIB_PATH", "CHUNK",
+                            "GDN_DTYPE_F32", "GDN_DTYPE_BF16"]

@@ -1,0 +1,291 @@
+// gdn_api.cu -- the C ABI of libgdn.so: argument checks, workspace carving and
+// kernel launches.  See include/gdn.h for the contract of every entry point.
+#include <cmath>
+#include <cstring>
+
+#include "gdn_internal.cuh"
+
+using gdn::Params;
+using gdn::WsLayout;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool head_size_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+int check_shape(const gdn_shape* s) {
+  if (!s) return GDN_ERR_INVALID_ARG;
+  if (s->Hk <= 0 || s->Hv <= 0 || s->n_seqs < 0 || s->total_tokens < 0 || s->total_chunks < 0)
+    return GDN_ERR_INVALID_ARG;
+  if (s->Hv % s->Hk != 0) return GDN_ERR_INVALID_ARG;
+  if (!head_size_ok(s->Dk) || !head_size_ok(s->Dv)) return GDN_ERR_UNSUPPORTED;
+  if (s->dtype != GDN_DTYPE_F32 && s->dtype != GDN_DTYPE_BF16) return GDN_ERR_UNSUPPORTED;
+  if (!(s->scale >= 0.f) || std::isinf(s->scale)) return GDN_ERR_INVALID_ARG;
+  // a chunk holds at least one token, and every token lies in some chunk
+  if ((int64_t)s->total_chunks > s->total_tokens) return GDN_ERR_INVALID_ARG;
+  if ((int64_t)s->total_chunks * gdn::kChunk < s->total_tokens) return GDN_ERR_INVALID_ARG;
+  if (s->n_seqs == 0 && s->total_tokens != 0) return GDN_ERR_INVALID_ARG;
+  // grid limits of the per-chunk kernels
+  if (s->total_chunks > 0x3fffffff || s->Hv > 65535 || s->n_seqs > 0x3fffffff)
+    return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+// A dtype-typed matrix argument [total_tokens, ld] holding `width` used columns.
+int check_matrix(const void* p, int64_t ld, int64_t width, size_t esize, int64_t rows) {
+  if (rows == 0) return GDN_OK;
+  if (!p) return GDN_ERR_INVALID_ARG;
+  if (ld < width) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(p) || ((size_t)ld * esize) % 16 != 0) return GDN_ERR_MISALIGNED;
+  return GDN_OK;
+}
+
+// An fp32 per-head matrix [total_tokens, ld] (alpha, beta_raw and their grads).
+int check_gate_matrix(const void* p, int64_t ld, int64_t Hv, int64_t rows) {
+  if (rows == 0) return GDN_OK;
+  if (!p) return GDN_ERR_INVALID_ARG;
+  if (ld < Hv) return GDN_ERR_INVALID_ARG;
+  if (((uintptr_t)p & 3u) != 0) return GDN_ERR_MISALIGNED;
+  return GDN_OK;
+}
+
+int check_vec(const void* p, bool required) {
+  if (!p) return required ? GDN_ERR_INVALID_ARG : GDN_OK;
+  if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+  return GDN_OK;
+}
+
+#define GDN_TRY(x)                 \
+  do {                             \
+    const int _rc = (x);           \
+    if (_rc != GDN_OK) return _rc; \
+  } while (0)
+
+void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                 int64_t k_ld, const void* v, int64_t v_ld, const float* alpha, int64_t alpha_ld,
+                 const float* beta_raw, int64_t beta_ld, const float* a_log, const float* dt_bias,
+                 const int32_t* cu, const int32_t* coff, const float* S0, void* ws, bool bwd) {
+  std::memset(&p, 0, sizeof(p));
+  p.Hk = s->Hk;
+  p.Hv = s->Hv;
+  p.Dk = s->Dk;
+  p.Dv = s->Dv;
+  p.r = s->Hv / s->Hk;
+  p.n_seqs = s->n_seqs;
+  p.NC = s->total_chunks;
+  p.T = s->total_tokens;
+  p.scale = s->scale > 0.f ? s->scale : 1.0f / std::sqrt((float)s->Dk);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.q_ld = q_ld;
+  p.k_ld = k_ld;
+  p.v_ld = v_ld;
+  p.alpha = alpha;
+  p.beta_raw = beta_raw;
+  p.alpha_ld = alpha_ld;
+  p.beta_ld = beta_ld;
+  p.a_log = a_log;
+  p.dt_bias = dt_bias;
+  p.cu = cu;
+  p.coff = coff;
+  p.S0 = S0;
+  const WsLayout L = gdn::ws_layout(*s, bwd);
+  char* base = (char*)ws;
+  p.status = (gdn::DeviceStatus*)(base + L.status);
+  p.Qn = (float*)(base + L.Qn);
+  p.Kn = (float*)(base + L.Kn);
+  p.nq = (float*)(base + L.nq);
+  p.nk = (float*)(base + L.nk);
+  p.W = (float*)(base + L.W);
+  p.U = (float*)(base + L.U);
+  p.G = (float*)(base + L.G);
+  p.b = (float*)(base + L.b);
+  if (bwd) {
+    p.Tm = (float*)(base + L.Tm);
+    p.dS = (float*)(base + L.dS);
+    p.dD = (float*)(base + L.dD);
+    p.dQh = (float*)(base + L.dQh);
+    p.dKh = (float*)(base + L.dKh);
+    p.pa = (float*)(base + L.pa);
+    p.pd = (float*)(base + L.pd);
+  }
+}
+
+int check_inputs(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, int64_t k_ld,
+                 const void* v, int64_t v_ld, const float* alpha, int64_t alpha_ld,
+                 const float* beta_raw, int64_t beta_ld, const float* a_log,
+                 const float* dt_bias, const int32_t* cu, const int32_t* coff, const float* S0) {
+  const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
+  const int64_t T = s->total_tokens;
+  GDN_TRY(check_matrix(q, q_ld, (int64_t)s->Hk * s->Dk, es, T));
+  GDN_TRY(check_matrix(k, k_ld, (int64_t)s->Hk * s->Dk, es, T));
+  GDN_TRY(check_matrix(v, v_ld, (int64_t)s->Hv * s->Dv, es, T));
+  GDN_TRY(check_gate_matrix(alpha, alpha_ld, s->Hv, T));
+  GDN_TRY(check_gate_matrix(beta_raw, beta_ld, s->Hv, T));
+  GDN_TRY(check_vec(a_log, true));
+  GDN_TRY(check_vec(dt_bias, true));
+  if (!cu || !coff) return GDN_ERR_INVALID_ARG;
+  if (((uintptr_t)cu & 3u) || ((uintptr_t)coff & 3u)) return GDN_ERR_MISALIGNED;
+  GDN_TRY(check_vec(S0, false));
+  return GDN_OK;
+}
+
+int check_workspace(const gdn_shape* s, void* ws, size_t bytes, bool bwd) {
+  if (!ws) return GDN_ERR_WORKSPACE;
+  if (((uintptr_t)ws & 255u) != 0) return GDN_ERR_WORKSPACE;
+  if (bytes < gdn::ws_layout(*s, bwd).total) return GDN_ERR_WORKSPACE;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t* chunk_offsets_host,
+             int32_t* total_chunks) {
+  if (!cu_seqlens_host || !chunk_offsets_host || !total_chunks || n_seqs < 0)
+    return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens_host[0] != 0) return GDN_ERR_INVALID_ARG;
+  int64_t acc = 0;
+  chunk_offsets_host[0] = 0;
+  for (int32_t n = 0; n < n_seqs; ++n) {
+    const int64_t len = (int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n];
+    if (len < 0) return GDN_ERR_INVALID_ARG;
+    acc += (len + gdn::kChunk - 1) / gdn::kChunk;
+    if (acc > 0x3fffffff) return GDN_ERR_INVALID_ARG;
+    chunk_offsets_host[n + 1] = (int32_t)acc;
+  }
+  *total_chunks = (int32_t)acc;
+  return GDN_OK;
+}
+
+size_t gdn_saved_state_bytes(const gdn_shape* s) {
+  if (check_shape(s) != GDN_OK) return 0;
+  return (size_t)s->total_chunks * s->Hv * s->Dk * s->Dv * sizeof(float);
+}
+
+size_t gdn_workspace_bytes(const gdn_shape* s, int is_backward) {
+  if (check_shape(s) != GDN_OK) return 0;
+  return gdn::ws_layout(*s, is_backward != 0).total;
+}
+
+int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, int64_t k_ld,
+                const void* v, int64_t v_ld, const float* alpha, int64_t alpha_ld,
+                const float* beta_raw, int64_t beta_ld, const float* a_log,
+                const float* dt_bias, const int32_t* cu_seqlens, const int32_t* chunk_offsets,
+                const float* S0, void* o, int64_t o_ld, float* S_T, float* saved_states,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  GDN_TRY(check_shape(s));
+  GDN_TRY(check_inputs(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
+                       dt_bias, cu_seqlens, chunk_offsets, S0));
+  const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
+  GDN_TRY(check_matrix(o, o_ld, (int64_t)s->Hv * s->Dv, es, s->total_tokens));
+  GDN_TRY(check_vec(S_T, false));
+  GDN_TRY(check_vec(saved_states, s->total_chunks > 0));
+  GDN_TRY(check_workspace(s, workspace, workspace_bytes, false));
+  cudaStream_t st = (cudaStream_t)stream;
+  Params p;
+  fill_common(p, s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
+              dt_bias, cu_seqlens, chunk_offsets, S0, workspace, false);
+  p.o = o;
+  p.o_ld = o_ld;
+  p.S_T = S_T;
+  p.saved = saved_states;
+  if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return GDN_ERR_CUDA;
+  if (s->n_seqs > 0 && s->total_chunks == 0) {
+    // every sequence is empty: S_T = S_0
+    if (!S_T) return GDN_OK;
+    const size_t bytes = (size_t)s->n_seqs * s->Hv * s->Dk * s->Dv * sizeof(float);
+    const cudaError_t e = S0 ? cudaMemcpyAsync(S_T, S0, bytes, cudaMemcpyDeviceToDevice, st)
+                             : cudaMemsetAsync(S_T, 0, bytes, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
+  if (gdn::launch_forward(p, s->dtype == GDN_DTYPE_BF16, st) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, int64_t k_ld,
+                 const void* v, int64_t v_ld, const float* alpha, int64_t alpha_ld,
+                 const float* beta_raw, int64_t beta_ld, const float* a_log,
+                 const float* dt_bias, const int32_t* cu_seqlens, const int32_t* chunk_offsets,
+                 const float* S0, const void* dO, int64_t dO_ld, const float* dS_T,
+                 const float* saved_states, void* dq, int64_t dq_ld, void* dk, int64_t dk_ld,
+                 void* dv, int64_t dv_ld, float* dalpha, int64_t dalpha_ld, float* dbeta_raw,
+                 int64_t dbeta_ld, float* da_log, float* ddt_bias, float* dS0, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  GDN_TRY(check_shape(s));
+  GDN_TRY(check_inputs(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
+                       dt_bias, cu_seqlens, chunk_offsets, S0));
+  const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
+  const int64_t T = s->total_tokens;
+  GDN_TRY(check_matrix(dO, dO_ld, (int64_t)s->Hv * s->Dv, es, T));
+  GDN_TRY(check_vec(dS_T, false));
+  GDN_TRY(check_vec(saved_states, s->total_chunks > 0));
+  GDN_TRY(check_matrix(dq, dq_ld, (int64_t)s->Hk * s->Dk, es, T));
+  GDN_TRY(check_matrix(dk, dk_ld, (int64_t)s->Hk * s->Dk, es, T));
+  GDN_TRY(check_matrix(dv, dv_ld, (int64_t)s->Hv * s->Dv, es, T));
+  GDN_TRY(check_gate_matrix(dalpha, dalpha_ld, s->Hv, T));
+  GDN_TRY(check_gate_matrix(dbeta_raw, dbeta_ld, s->Hv, T));
+  GDN_TRY(check_vec(da_log, true));
+  GDN_TRY(check_vec(ddt_bias, true));
+  GDN_TRY(check_vec(dS0, false));
+  GDN_TRY(check_workspace(s, workspace, workspace_bytes, true));
+  cudaStream_t st = (cudaStream_t)stream;
+  Params p;
+  fill_common(p, s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
+              dt_bias, cu_seqlens, chunk_offsets, S0, workspace, true);
+  p.saved_in = saved_states;
+  p.dO = dO;
+  p.dO_ld = dO_ld;
+  p.dS_T = dS_T;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dq_ld = dq_ld;
+  p.dk_ld = dk_ld;
+  p.dv_ld = dv_ld;
+  p.dalpha = dalpha;
+  p.dbeta = dbeta_raw;
+  p.dalpha_ld = dalpha_ld;
+  p.dbeta_ld = dbeta_ld;
+  p.da_log = da_log;
+  p.ddt_bias = ddt_bias;
+  p.dS0 = dS0;
+  if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return GDN_ERR_CUDA;
+  if (s->total_chunks == 0 && s->n_seqs > 0 && dS0) {
+    const size_t bytes = (size_t)s->n_seqs * s->Hv * s->Dk * s->Dv * sizeof(float);
+    const cudaError_t e = dS_T ? cudaMemcpyAsync(dS0, dS_T, bytes, cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(dS0, 0, bytes, st);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  if (gdn::launch_backward(p, s->dtype == GDN_DTYPE_BF16, st) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+int gdn_read_device_status(const void* workspace, void* stream) {
+  if (!workspace) return GDN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  gdn::DeviceStatus h{};
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+  return h.code;
+}
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_DEVICE_BOUNDS: return "GDN_ERR_DEVICE_BOUNDS";
+    default: return "GDN_UNKNOWN_STATUS";
+  }
+}
+
+}  // extern "C"

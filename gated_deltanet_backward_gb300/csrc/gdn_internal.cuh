@@ -1,0 +1,147 @@
+// gdn_internal.cuh -- shared declarations of the GB300 Gated DeltaNet kernels.
+//
+// Chunked form of the recurrence (derived from lattice-inference 0.6.0,
+// gdn_backward.rs, module doc "Forward recap"; the pages name a chunked
+// implementation, chunk_wy_forward_impl / ChunkWy::backward on the "KDA
+// attention arm" work log, but do not write it out).  Per chunk of c <= 64
+// tokens and value head h, rows r, s of the chunk:
+//   l = log g, G = inclusive cumsum(l), E[r,s] = exp(G[r] - G[s]) (s <= r)
+//   A = diag(b) (E * K K^T) strictly lower, T = (I + A)^-1
+//   W = T diag(b e^G) K,  U = T diag(b) V,  Delta = U - W S
+//   O = scale (diag(e^G) Q S + (E * Q K^T, lower) Delta)
+//   S_next = e^{G[c-1]} S + K^T diag(e^{G[c-1] - G}) Delta
+// K, Q are the L2-normalised keys / queries of key head h / v_repeat.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;     // tokens per chunk
+constexpr int kThreads = 256;  // threads per CTA of every kernel
+
+// Device-side status word layout at the start of the workspace.
+struct DeviceStatus {
+  int32_t code;    // first gdn_status recorded by a kernel (0 = OK)
+  int32_t detail;  // kernel-specific detail (e.g. the chunk index)
+};
+
+// Byte offsets of the workspace regions (fp32 unless noted).
+struct WsLayout {
+  size_t status;  // DeviceStatus, 256 B
+  size_t Qn;      // [NC][Hk][C][Dk] normalised queries
+  size_t Kn;      // [NC][Hk][C][Dk] normalised keys
+  size_t nq;      // [NC][Hk][C] query norms sqrt(|q|^2 + 1e-6)
+  size_t nk;      // [NC][Hk][C] key norms
+  size_t W;       // [NC][Hv][C][Dk]
+  size_t U;       // [NC][Hv][C][Dv]
+  size_t Tm;      // [NC][Hv][C][C] (backward only)
+  size_t G;       // [NC][Hv][C] inclusive cumsum of log g
+  size_t b;       // [NC][Hv][C] beta
+  size_t dS;      // [NC][Hv][Dk][Dv] state adjoint at each chunk end (backward)
+  size_t dD;      // [NC][Hv][C][Dv] d Delta (backward)
+  size_t dQh;     // [NC][Hv][C][Dk] per-value-head d q_hat partials (backward)
+  size_t dKh;     // [NC][Hv][C][Dk] per-value-head d k_hat partials (backward)
+  size_t pa;      // [NC][Hv] per-chunk partial of d a_log (backward)
+  size_t pd;      // [NC][Hv] per-chunk partial of d dt_bias (backward)
+  size_t total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
+  WsLayout L{};
+  const size_t NC = (size_t)s.total_chunks, C = kChunk;
+  const size_t Hk = s.Hk, Hv = s.Hv, Dk = s.Dk, Dv = s.Dv;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.Qn = take(NC * Hk * C * Dk * 4);
+  L.Kn = take(NC * Hk * C * Dk * 4);
+  L.nq = take(NC * Hk * C * 4);
+  L.nk = take(NC * Hk * C * 4);
+  L.W = take(NC * Hv * C * Dk * 4);
+  L.U = take(NC * Hv * C * Dv * 4);
+  L.G = take(NC * Hv * C * 4);
+  L.b = take(NC * Hv * C * 4);
+  if (bwd) {
+    L.Tm = take(NC * Hv * C * C * 4);
+    L.dS = take(NC * Hv * Dk * Dv * 4);
+    L.dD = take(NC * Hv * C * Dv * 4);
+    L.dQh = take(NC * Hv * C * Dk * 4);
+    L.dKh = take(NC * Hv * C * Dk * 4);
+    L.pa = take(NC * Hv * 4);
+    L.pd = take(NC * Hv * 4);
+  }
+  L.total = off;
+  return L;
+}
+
+// Everything a kernel needs, passed by value.
+struct Params {
+  int Hk, Hv, Dk, Dv, r, n_seqs, NC;
+  int64_t T;
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  int64_t q_ld, k_ld, v_ld;
+  const float* alpha;
+  const float* beta_raw;
+  int64_t alpha_ld, beta_ld;
+  const float* a_log;
+  const float* dt_bias;
+  const int32_t* cu;
+  const int32_t* coff;
+  const float* S0;
+  void* o;
+  int64_t o_ld;
+  float* S_T;
+  float* saved;
+  const float* saved_in;
+  const void* dO;
+  int64_t dO_ld;
+  const float* dS_T;
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t dq_ld, dk_ld, dv_ld;
+  float* dalpha;
+  float* dbeta;
+  int64_t dalpha_ld, dbeta_ld;
+  float* da_log;
+  float* ddt_bias;
+  float* dS0;
+  DeviceStatus* status;
+  float* Qn;
+  float* Kn;
+  float* nq;
+  float* nk;
+  float* W;
+  float* U;
+  float* Tm;
+  float* G;
+  float* b;
+  float* dS;
+  float* dD;
+  float* dQh;
+  float* dKh;
+  float* pa;
+  float* pd;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t st);
+cudaError_t launch_forward(const Params& p, bool bf16, cudaStream_t st);
+cudaError_t launch_backward(const Params& p, bool bf16, cudaStream_t st);
+
+}  // namespace gdn

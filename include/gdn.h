@@ -1,0 +1,167 @@
+/*
+ * gdn.h -- C ABI of the GB300 Gated DeltaNet library (libgdn.so).
+ *
+ * The operation (lattice-inference 0.6.0, src/attention/gdn_backward.rs,
+ * module doc "Forward recap"): for every sequence of a varlen batch and every
+ * value head h, with key head kh = h / (Hv / Hk),
+ *
+ *   q_hat = q / sqrt(|q|^2 + 1e-6),  k_hat = k / sqrt(|k|^2 + 1e-6)   (key head kh)
+ *   beta  = sigmoid(beta_raw[t, h])
+ *   g     = exp(-exp(a_log[h]) * softplus(alpha[t, h] + dt_bias[h]))
+ *   kv    = S_{t-1}^T k_hat                 (retrieval from the pre-decayed state)
+ *   delta = beta * (v - g * kv)
+ *   S_t   = g * S_{t-1} + k_hat delta^T     (S is Dk x Dv, row-major)
+ *   o_t   = scale * S_t^T q_hat             (scale = 1/sqrt(Dk) unless given)
+ *
+ * The backward is its reverse-mode derivative (gdn_backward, section 4,
+ * steps 4a-4h), taking dO and dS_T and returning dq, dk, dv, d alpha,
+ * d beta_raw, d a_log, d dt_bias and dS_0.  dq/dk of a key head are the sums
+ * over the value heads that read it (the cross-head reduction of the llama.cpp
+ * PR "tests: delta-net backward at the shape the 27B emits (shared key heads,
+ * strided q/k)"), formed in a fixed order: results are bit-reproducible run to
+ * run.  q/k/v may be strided row views of one packed projection (same PR).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Tokens of all sequences are packed row after row; sequence n owns rows
+ *    [cu_seqlens[n], cu_seqlens[n+1]).  Each sequence starts from its own S_0.
+ *  - `*_ld` arguments are row strides in ELEMENTS (one row per token).  Inside a
+ *    row, head h occupies columns [h*D, (h+1)*D).
+ *  - q, k, v, o, dO, dq, dk, dv have the element type `shape->dtype` (fp32 or
+ *    bf16).  alpha, beta_raw, a_log, dt_bias, S_0, S_T, dS_T, dS_0, the saved
+ *    states and d alpha, d beta_raw, d a_log, d dt_bias are fp32.  State and
+ *    accumulation arithmetic is fp32.  bf16 outputs are rounded to nearest even.
+ *  - State tensors (S_0, S_T, dS_T, dS_0) are [n_seqs, Hv, Dk, Dv] fp32,
+ *    contiguous.  Saved states are [total_chunks, Hv, Dk, Dv] fp32: the state at
+ *    the START of each 64-token chunk (chunks never span two sequences; the last
+ *    chunk of a sequence may be short; the chunks of sequence n are numbered
+ *    from chunk_offsets[n]).
+ *  - Pointers marked "device" are CUDA device pointers; "host" ones are host
+ *    pointers.  The caller owns every buffer.  The library allocates nothing
+ *    and keeps no state between calls.  Outputs are overwritten, never
+ *    accumulated into.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and the call returns without synchronising.
+ *  - Every argument is checked on the host before anything is launched: on a
+ *    failed check the call returns a negative gdn_status and launches nothing.
+ *    Supported: Dk, Dv in {16, 32, 64, 128}; Hv a multiple of Hk; device
+ *    buffers 16-byte aligned; row strides of q, k, v, o, dO, dq, dk, dv whose
+ *    byte size is a multiple of 16; fp32 row strides of alpha, beta_raw,
+ *    d alpha, d beta_raw of at least Hv; workspace at least
+ *    gdn_workspace_bytes() and 256-byte aligned.
+ *  - Errors found on the device (a cu_seqlens / chunk_offsets pair that does
+ *    not match the shape, a bounded wait that ran out) do not trap: the kernels
+ *    record a status code in the workspace and skip the offending work.  Read it
+ *    with gdn_read_device_status().
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = -1,   /* null pointer, bad size, inconsistent cu_seqlens */
+  GDN_ERR_UNSUPPORTED = -2,   /* head size or dtype outside the supported set */
+  GDN_ERR_MISALIGNED = -3,    /* pointer or row stride breaks the alignment rules */
+  GDN_ERR_CUDA = -4,          /* a CUDA runtime call or a launch failed */
+  GDN_ERR_TIMEOUT = -5,       /* a bounded device-side wait ran out (device status) */
+  GDN_ERR_WORKSPACE = -6,     /* workspace too small or misaligned */
+  GDN_ERR_DEVICE_BOUNDS = -7  /* device-side check: chunk or token index out of range */
+} gdn_status;
+
+typedef enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
+
+typedef struct {
+  int32_t Hk;           /* key heads (q and k heads) */
+  int32_t Hv;           /* value heads; Hv % Hk == 0, v_repeat = Hv / Hk */
+  int32_t Dk;           /* key / query head size */
+  int32_t Dv;           /* value head size */
+  int32_t n_seqs;       /* sequences in the varlen batch (>= 0) */
+  int32_t total_chunks; /* sum over sequences of ceil(len / 64), from gdn_plan */
+  int64_t total_tokens; /* cu_seqlens[n_seqs] */
+  int32_t dtype;        /* gdn_dtype of q, k, v, o, dO, dq, dk, dv */
+  float scale;          /* output scale; 0 selects 1/sqrt(Dk) */
+} gdn_shape;
+
+/* Chunk planning (host only).  From host cu_seqlens[n_seqs+1] (non-decreasing,
+ * starting at 0) fills chunk_offsets_host[n_seqs+1] (chunk_offsets[n] = number
+ * of 64-token chunks of the sequences before n) and *total_chunks.  The caller
+ * copies both arrays to the device for gdn_forward / gdn_backward.
+ * Returns GDN_OK or GDN_ERR_INVALID_ARG. */
+int gdn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t* chunk_offsets_host,
+             int32_t* total_chunks);
+
+/* Bytes of the saved-state buffer: total_chunks * Hv * Dk * Dv * 4.
+ * Returns 0 for an invalid shape. */
+size_t gdn_saved_state_bytes(const gdn_shape* shape);
+
+/* Bytes of device scratch the forward (is_backward = 0) or the backward
+ * (is_backward = 1) needs.  Returns 0 for an invalid shape. */
+size_t gdn_workspace_bytes(const gdn_shape* shape, int is_backward);
+
+/* Forward.  Chunked (64-token) scan of the recurrence above.
+ *   q, k      device, [total_tokens, *_ld] dtype; key head kh at column kh*Dk
+ *   v         device, [total_tokens, v_ld] dtype; value head h at column h*Dv
+ *   alpha     device, [total_tokens, alpha_ld] fp32; column h
+ *   beta_raw  device, [total_tokens, beta_ld] fp32; column h (beta = sigmoid)
+ *   a_log, dt_bias  device, [Hv] fp32
+ *   cu_seqlens, chunk_offsets  device, [n_seqs+1] int32 (see gdn_plan)
+ *   S0        device, [n_seqs, Hv, Dk, Dv] fp32, or NULL for a zero state
+ *   o         device, [total_tokens, o_ld] dtype (written)
+ *   S_T       device, [n_seqs, Hv, Dk, Dv] fp32 final states, or NULL
+ *   saved_states device, gdn_saved_state_bytes() bytes (written; the backward
+ *             reads it)
+ *   workspace device scratch, gdn_workspace_bytes(shape, 0) bytes
+ * Returns a gdn_status. */
+int gdn_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
+                int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
+                const int32_t* chunk_offsets, const float* S0, void* o, int64_t o_ld,
+                float* S_T, float* saved_states, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/* Backward (reverse chunk walk with a dS carry).  Inputs as gdn_forward, plus
+ *   dO        device, [total_tokens, dO_ld] dtype: dL/do
+ *   dS_T      device, [n_seqs, Hv, Dk, Dv] fp32: dL/dS_T, or NULL for zero
+ *   saved_states device, as written by gdn_forward on the same inputs
+ * Outputs (all written, none accumulated):
+ *   dq, dk    device, [total_tokens, *_ld] dtype: dL/dq, dL/dk of the RAW
+ *             (un-normalised) q and k, summed over the value heads of each key head
+ *   dv        device, [total_tokens, dv_ld] dtype
+ *   dalpha    device, [total_tokens, dalpha_ld] fp32: dL/d alpha
+ *   dbeta_raw device, [total_tokens, dbeta_ld] fp32: dL/d beta_raw
+ *   da_log, ddt_bias device, [Hv] fp32, summed over every token of every sequence
+ *   dS0       device, [n_seqs, Hv, Dk, Dv] fp32: dL/dS_0, or NULL to skip
+ *   workspace device scratch, gdn_workspace_bytes(shape, 1) bytes
+ * Returns a gdn_status. */
+int gdn_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
+                 int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                 int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                 const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
+                 const int32_t* chunk_offsets, const float* S0, const void* dO, int64_t dO_ld,
+                 const float* dS_T, const float* saved_states, void* dq, int64_t dq_ld,
+                 void* dk, int64_t dk_ld, void* dv, int64_t dv_ld, float* dalpha,
+                 int64_t dalpha_ld, float* dbeta_raw, int64_t dbeta_ld, float* da_log,
+                 float* ddt_bias, float* dS0, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* Synchronises `stream` and returns the device-side status recorded in
+ * `workspace` by the last gdn_forward / gdn_backward that used it (GDN_OK, or
+ * the first device error), or GDN_ERR_CUDA if the stream itself failed. */
+int gdn_read_device_status(const void* workspace, void* stream);
+
+/* A static, human-readable name for a gdn_status value. */
+const char* gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

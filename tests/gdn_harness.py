@@ -1,0 +1,153 @@
+"""Test harness: runs the CUDA library and the CPU oracle on one seeded draw.
+
+Not collected by pytest (no ``test_`` prefix).  The CUDA side goes through the
+Python binding of the C ABI; the oracle side through ``oracle``.  Both consume
+the same ``workloads.Inputs`` arrays.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import workloads as W
+
+GRADS = ("dq", "dk", "dv", "dalpha", "dbeta_raw", "da_log", "ddt_bias", "dS0")
+TOL = {"f32": 1e-3, "bf16": 2e-2}
+
+
+def rel_err(gpu, ref) -> float:
+    """max|gpu - ref| / max|ref|; for an all-zero reference, max|gpu| itself."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.abs(ref).max() if ref.size else 0.0
+    if den == 0.0:
+        return float(np.abs(gpu).max()) if gpu.size else 0.0
+    return float(np.abs(gpu - ref).max() / den)
+
+
+class DeviceRun:
+    """Device copies of one draw plus every output of one forward + backward."""
+
+    def __init__(self, inp: W.Inputs, device="cuda", dense=False, run_backward=True):
+        import torch
+        import gated_deltanet_backward_gb300 as gdn
+        self.inp = inp
+        wl = inp.wl
+        self.tdtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        T, Hk, Hv, Dk, Dv = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv
+
+        def dev(a, dt=None):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device=device,
+                                                                dtype=dt or torch.float32)
+
+        if inp.qkv is not None and not dense:
+            self.qkv = dev(inp.qkv, self.tdtype)
+            self.q = self.qkv[:, : Hk * Dk]
+            self.k = self.qkv[:, Hk * Dk: 2 * Hk * Dk]
+            self.v = self.qkv[:, 2 * Hk * Dk:]
+        else:
+            self.q, self.k, self.v = (dev(x, self.tdtype) for x in (inp.q, inp.k, inp.v))
+        self.alpha, self.beta_raw = dev(inp.alpha), dev(inp.beta_raw)
+        self.a_log, self.dt_bias = dev(inp.a_log), dev(inp.dt_bias)
+        self.S0 = None if inp.S0 is None else dev(inp.S0)
+        self.dO = dev(inp.dO, self.tdtype)
+        self.dS_T = None if inp.dS_T is None else dev(inp.dS_T)
+        self.layer = gdn.Layer.create(Hk, Hv, Dk, Dv, inp.cu_seqlens, wl.dtype,
+                                      wl.scale_value(), device=device)
+        N = wl.n_seqs
+        self.o = torch.full((T, Hv * Dv), float("nan"), device=device, dtype=self.tdtype)
+        self.S_T = torch.full((N, Hv, Dk, Dv), float("nan"), device=device)
+        self.layer.forward(self.q, self.k, self.v, self.alpha, self.beta_raw, self.a_log,
+                           self.dt_bias, self.S0, self.o, self.S_T)
+        self.grads = None
+        if run_backward:
+            self.run_backward()
+
+    def run_backward(self):
+        import torch
+        wl = self.inp.wl
+        T, Hk, Hv, Dk, Dv, N = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv, wl.n_seqs
+        dev = self.o.device
+        nan = float("nan")
+        g = dict(dq=torch.full((T, Hk * Dk), nan, device=dev, dtype=self.tdtype),
+                 dk=torch.full((T, Hk * Dk), nan, device=dev, dtype=self.tdtype),
+                 dv=torch.full((T, Hv * Dv), nan, device=dev, dtype=self.tdtype),
+                 dalpha=torch.full((T, Hv), nan, device=dev),
+                 dbeta_raw=torch.full((T, Hv), nan, device=dev),
+                 da_log=torch.full((Hv,), nan, device=dev),
+                 ddt_bias=torch.full((Hv,), nan, device=dev),
+                 dS0=torch.full((N, Hv, Dk, Dv), nan, device=dev))
+        self.layer.backward(self.q, self.k, self.v, self.alpha, self.beta_raw, self.a_log,
+                            self.dt_bias, self.S0, self.dO, self.dS_T, g["dq"], g["dk"], g["dv"],
+                            g["dalpha"], g["dbeta_raw"], g["da_log"], g["ddt_bias"], g["dS0"])
+        self.grads = g
+        return g
+
+    def status(self, backward=False) -> int:
+        import gated_deltanet_backward_gb300 as gdn
+        return gdn.gdn_read_device_status(self.layer.ws_bwd if backward else self.layer.ws_fwd)
+
+    def host(self):
+        """All outputs as f64 numpy arrays."""
+        import torch
+        torch.cuda.synchronize()
+        out = dict(o=self.o.double().cpu().numpy(), S_T=self.S_T.double().cpu().numpy())
+        wl = self.inp.wl
+        nbytes = wl.total_chunks * wl.Hv * wl.Dk * wl.Dv
+        out["saved"] = self.layer.saved_states[:nbytes].double().cpu().numpy().reshape(
+            wl.total_chunks, wl.Hv, wl.Dk, wl.Dv)
+        if self.grads is not None:
+            for k, v in self.grads.items():
+                out[k] = v.double().cpu().numpy()
+        return out
+
+
+def head_group_inputs(inp: W.Inputs, kh: int) -> W.Inputs:
+    """The inputs of key head kh and its v_repeat value heads, as a stand-alone draw
+    (heads are independent, so the oracle can check one group of a large batch)."""
+    wl = inp.wl
+    r, Dk, Dv = wl.v_repeat, wl.Dk, wl.Dv
+    hs = slice(kh * r, (kh + 1) * r)
+    sub = W.replace(wl, Hk=1, Hv=r, name=wl.name + "_kh%d" % kh)
+    return W.Inputs(sub, inp.cu_seqlens, None,
+                    inp.q[:, kh * Dk:(kh + 1) * Dk], inp.k[:, kh * Dk:(kh + 1) * Dk],
+                    inp.v[:, kh * r * Dv:(kh + 1) * r * Dv], inp.alpha[:, hs], inp.beta_raw[:, hs],
+                    inp.a_log[hs], inp.dt_bias[hs], None if inp.S0 is None else inp.S0[:, hs],
+                    inp.dO[:, kh * r * Dv:(kh + 1) * r * Dv],
+                    None if inp.dS_T is None else inp.dS_T[:, hs])
+
+
+def head_group_outputs(out: dict, wl: W.Workload, kh: int) -> dict:
+    r, Dk, Dv = wl.v_repeat, wl.Dk, wl.Dv
+    hs = slice(kh * r, (kh + 1) * r)
+    vs = slice(kh * r * Dv, (kh + 1) * r * Dv)
+    ks = slice(kh * Dk, (kh + 1) * Dk)
+    sel = dict(o=out["o"][:, vs], S_T=out["S_T"][:, hs], saved=out["saved"][:, hs])
+    if "dq" in out:
+        sel.update(dq=out["dq"][:, ks], dk=out["dk"][:, ks], dv=out["dv"][:, vs],
+                   dalpha=out["dalpha"][:, hs], dbeta_raw=out["dbeta_raw"][:, hs],
+                   da_log=out["da_log"][hs], ddt_bias=out["ddt_bias"][hs], dS0=out["dS0"][:, hs])
+    return sel
+
+
+def oracle_outputs(inp: W.Inputs, backward=True, n_threads=0) -> dict:
+    wl = inp.wl
+    kw = dict(Hk=wl.Hk, Hv=wl.Hv, Dk=wl.Dk, Dv=wl.Dv, scale=wl.scale_value(),
+              n_threads=n_threads)
+    o, S_T, states = oracle.forward(inp.q, inp.k, inp.v, inp.alpha, inp.beta_raw, inp.a_log,
+                                    inp.dt_bias, inp.cu_seqlens, inp.S0, chunk=W.CHUNK, **kw)
+    out = dict(o=o, S_T=S_T, saved=states)
+    if backward:
+        out.update(oracle.backward(inp.q, inp.k, inp.v, inp.alpha, inp.beta_raw, inp.a_log,
+                                   inp.dt_bias, inp.cu_seqlens, inp.dO, inp.S0, inp.dS_T, **kw))
+    return out
+
+
+def compare(gpu: dict, ref: dict, tol: float, keys=None) -> dict:
+    keys = keys or [k for k in ref if k in gpu]
+    errs = {k: rel_err(gpu[k], ref[k]) for k in keys}
+    for k in keys:
+        assert np.all(np.isfinite(gpu[k])), "%s has non-finite values" % k
+    bad = {k: e for k, e in errs.items() if not e <= tol}
+    assert not bad, "tensors over tolerance %g: %s (all: %s)" % (tol, bad, errs)
+    return errs

@@ -1,0 +1,141 @@
+"""GPU parity: the CUDA path (through the C ABI) against the f64 CPU oracle.
+
+Bar per output tensor: max|gpu - oracle| / max|oracle| <= 1e-3 for fp32 inputs,
+<= 2e-2 for bf16 inputs (an all-zero oracle tensor requires max|gpu| <= 1e-30).
+Full-size workloads are checked on whole key-head groups (heads are independent,
+so one group's oracle run covers every token of every sequence for those heads,
+including the per-head sums d a_log / d dt_bias).
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from tests.gdn_harness import (DeviceRun, TOL, compare, head_group_inputs, head_group_outputs,
+                               oracle_outputs, rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def _check_full(inp, dense=False):
+    run = DeviceRun(inp, dense=dense)
+    gpu = run.host()
+    assert run.status() == 0 and run.status(backward=True) == 0
+    ref = oracle_outputs(inp)
+    return compare(gpu, ref, TOL[inp.wl.dtype]), run
+
+
+def test_tiny_fp32_workload():
+    """1 x 64 tokens, Hk = Hv = 2, D = 16, dense q/k/v, fp32."""
+    _check_full(W.generate(W.get("tiny_f32")), dense=True)
+
+
+def test_shared_key_heads_strided_fp32_workload():
+    """2 x 512 tokens, 4 key heads shared by 12 value heads, packed strided qkv, fp32."""
+    _check_full(W.generate(W.get("shared_kh_f32")))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(Hk=1, Hv=2, Dk=16, Dv=16, seqlens=(200,)),                  # ragged 4th chunk
+    dict(Hk=2, Hv=4, Dk=32, Dv=64, seqlens=(1, 65, 0, 130)),          # 1-token, empty, tails
+    dict(Hk=1, Hv=3, Dk=128, Dv=32, seqlens=(70, 63)),                # Dk != Dv, large Dk
+    dict(Hk=2, Hv=2, Dk=64, Dv=128, seqlens=(129,)),                  # Dv = 128, v_repeat 1
+], ids=["T200_D16", "empty_and_1tok", "Dk128_Dv32", "Dk64_Dv128"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_edge_shapes(kw, dtype):
+    wl = W.custom(dtype=dtype, seed=7, S0_std=0.3, dST_std=0.2, dt_bias_std=0.2, **kw)
+    _check_full(W.generate(wl))
+
+
+def test_l27b_bf16_workload_full():
+    """The 27B-shaped layer: 4096 tokens, Hk = 16, Hv = 48, D = 128, bf16 (every head)."""
+    _check_full(W.generate(W.get("l27b_bf16")))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,groups", [("l27b_batch_bf16", (0, 15)), ("varlen_bf16", (0, 9))])
+def test_full_size_batches_on_head_groups(name, groups):
+    """8 x 8192 tokens (Hv = 48) and the 16-sequence varlen batch (Hv = 32), run whole on
+    the GPU; the oracle checks two key-head groups over every token."""
+    inp = W.generate(W.get(name))
+    run = DeviceRun(inp)
+    gpu = run.host()
+    assert run.status() == 0 and run.status(backward=True) == 0
+    for kh in groups:
+        sub = head_group_inputs(inp, kh)
+        ref = oracle_outputs(sub)
+        compare(head_group_outputs(gpu, inp.wl, kh), ref, TOL["bf16"])
+
+
+def test_strided_and_dense_inputs_give_identical_bits():
+    inp = W.generate(W.custom(dtype="bf16", Hk=2, Hv=6, Dk=64, Dv=64, seqlens=(300, 77), seed=3,
+                              S0_std=0.1, dST_std=0.1))
+    a = DeviceRun(inp).host()
+    b = DeviceRun(inp, dense=True).host()
+    for key in a:
+        assert np.array_equal(a[key], b[key], equal_nan=False), key
+
+
+def test_backward_is_bit_reproducible():
+    import torch
+    inp = W.generate(W.custom(dtype="bf16", Hk=4, Hv=12, Dk=64, Dv=64, seqlens=(256, 190),
+                              seed=11, S0_std=0.1, dST_std=0.1))
+    run = DeviceRun(inp)
+    first = {k: v.clone() for k, v in run.grads.items()}
+    for _ in range(4):
+        again = run.run_backward()
+        for key in first:
+            assert torch.equal(again[key], first[key]), key
+
+
+def test_zero_upstream_gives_zero_gradients():
+    wl = W.custom(dtype="f32", Hk=2, Hv=4, Dk=32, Dv=32, seqlens=(100, 40), seed=5, S0_std=0.5)
+    inp = W.generate(wl)
+    inp.dO[:] = 0.0
+    run = DeviceRun(inp)
+    gpu = run.host()
+    for key in ("dq", "dk", "dv", "dalpha", "dbeta_raw", "da_log", "ddt_bias", "dS0"):
+        assert np.abs(gpu[key]).max() == 0.0, key
+
+
+def test_all_empty_sequences():
+    wl = W.custom(dtype="f32", Hk=1, Hv=2, Dk=16, Dv=16, seqlens=(0, 0), seed=2, S0_std=0.5,
+                  dST_std=0.5)
+    inp = W.generate(wl)
+    gpu = DeviceRun(inp).host()
+    assert np.array_equal(gpu["S_T"], inp.S0.astype(np.float64))
+    assert np.array_equal(gpu["dS0"], inp.dS_T.astype(np.float64))
+    assert np.abs(gpu["da_log"]).max() == 0.0 and np.abs(gpu["ddt_bias"]).max() == 0.0
+
+
+def test_device_check_rejects_inconsistent_offsets():
+    """chunk_offsets that disagree with cu_seqlens are caught by the kernels' own range
+    checks (which run before any access) and reported through the status word."""
+    import torch
+    import gated_deltanet_backward_gb300 as gdn
+    inp = W.generate(W.custom(dtype="f32", Hk=1, Hv=1, Dk=16, Dv=16, seqlens=(100, 100), seed=1))
+    run = DeviceRun(inp, run_backward=False)
+    assert run.status() == 0
+    bad = torch.tensor([0, 1, 4], dtype=torch.int32, device="cuda")   # seq 0 has 2 chunks
+    o = torch.zeros_like(run.o)
+    gdn.gdn_forward(run.layer.shape, run.q, run.k, run.v, run.alpha, run.beta_raw, run.a_log,
+                    run.dt_bias, run.layer.cu_seqlens, bad, None, o, None,
+                    run.layer.saved_states, run.layer.ws_fwd)
+    assert gdn.gdn_read_device_status(run.layer.ws_fwd) == -7
+
+
+def test_saved_states_and_final_state_against_oracle_fp32():
+    wl = W.custom(dtype="f32", Hk=2, Hv=4, Dk=32, Dv=16, seqlens=(150, 64, 3), seed=9,
+                  S0_std=0.5)
+    inp = W.generate(wl)
+    gpu = DeviceRun(inp, run_backward=False).host()
+    ref = oracle_outputs(inp, backward=False)
+    assert rel_err(gpu["saved"], ref["saved"]) < 1e-4
+    assert rel_err(gpu["S_T"], ref["S_T"]) < 1e-4
