@@ -139,9 +139,66 @@ int check_workspace(const gdn_shape* s, void* ws, size_t bytes, bool bwd) {
   return GDN_OK;
 }
 
+struct ProfileState {
+  void* const* events = nullptr;
+  int32_t* ids = nullptr;
+  int32_t n_pairs = 0;
+  int32_t count = 0;
+  bool on = false;
+};
+thread_local ProfileState g_profile;
+
 }  // namespace
 
+namespace gdn {
+
+void profile_pre(cudaStream_t st, int kernel_id) {
+  ProfileState& P = g_profile;
+  if (!P.on) return;
+  if (P.count < P.n_pairs) {
+    P.ids[P.count] = kernel_id;
+    cudaEventRecord((cudaEvent_t)P.events[2 * P.count], st);
+  }
+}
+
+void profile_post(cudaStream_t st) {
+  ProfileState& P = g_profile;
+  if (!P.on) return;
+  if (P.count < P.n_pairs) cudaEventRecord((cudaEvent_t)P.events[2 * P.count + 1], st);
+  ++P.count;
+}
+
+}  // namespace gdn
+
 extern "C" {
+
+int gdn_profile_begin(void* const* events, int32_t* kernel_ids, int32_t n_pairs) {
+  if (n_pairs < 0 || (n_pairs > 0 && (!events || !kernel_ids))) return GDN_ERR_INVALID_ARG;
+  g_profile.events = events;
+  g_profile.ids = kernel_ids;
+  g_profile.n_pairs = n_pairs;
+  g_profile.count = 0;
+  g_profile.on = true;
+  return GDN_OK;
+}
+
+int gdn_profile_end(void) {
+  const int n = g_profile.count;
+  g_profile = ProfileState();
+  return n;
+}
+
+const char* gdn_kernel_name(int32_t id) {
+  switch (id) {
+    case gdn::KID_PREP: return "gdn_prep";
+    case gdn::KID_FWD_STATE: return "gdn_fwd_state";
+    case gdn::KID_BWD_STATE: return "gdn_bwd_state";
+    case gdn::KID_BWD_GRADS: return "gdn_bwd_grads";
+    case gdn::KID_BWD_QK: return "gdn_bwd_qk";
+    case gdn::KID_BWD_GATES: return "gdn_bwd_gates";
+    default: return "?";
+  }
+}
 
 int gdn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t* chunk_offsets_host,
              int32_t* total_chunks) {

@@ -416,25 +416,35 @@ static cudaError_t launch_backward_t(const Params& p, cudaStream_t st) {
   const int DVS = p.Dv < 32 ? p.Dv : 32;
   size_t smem = sizeof(float) * ((size_t)p.Dk * DVS + (size_t)C * DVS + C * C + 3 * C);
   cudaFuncSetAttribute(k_bwd_state<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  profile_pre(st, KID_BWD_STATE);
   k_bwd_state<T><<<dim3(p.n_seqs, p.Hv, p.Dv / DVS), kThreads, smem, st>>>(p, DVS);
+  profile_post(st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int Dm = p.Dk > p.Dv ? p.Dk : p.Dv;
   smem = sizeof(float) * ((size_t)C * p.Dv + (size_t)C * p.Dk + (size_t)C * Dm + 6 * C * C +
                           6 * C + kThreads / 32);
   cudaFuncSetAttribute(k_bwd_grads<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  profile_pre(st, KID_BWD_GRADS);
   k_bwd_grads<T><<<dim3(p.NC, p.Hv), kThreads, smem, st>>>(p);
+  profile_post(st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  profile_pre(st, KID_BWD_QK);
   k_bwd_qk<T><<<dim3(p.NC, p.Hk), kThreads, 0, st>>>(p);
+  profile_post(st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  profile_pre(st, KID_BWD_GATES);
   k_bwd_gates<<<1, kThreads, 0, st>>>(p);
+  profile_post(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_backward(const Params& p, bool bf16, cudaStream_t st) {
   if (p.NC == 0) {
     // No tokens: gradients of the per-head parameters are zero, dS_0 = dS_T.
+    profile_pre(st, KID_BWD_GATES);
     k_bwd_gates<<<1, kThreads, 0, st>>>(p);
+    profile_post(st);
     return cudaGetLastError();
   }
   cudaError_t e = launch_prep(p, bf16, true, st);

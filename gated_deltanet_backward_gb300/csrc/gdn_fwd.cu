@@ -207,6 +207,7 @@ cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t s
   if (p.NC == 0) return cudaSuccess;
   const size_t smem = prep_smem(p);
   dim3 grid(p.NC, p.Hk);
+  profile_pre(st, KID_PREP);
   if (bf16) {
     cudaFuncSetAttribute(k_prep<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k_prep<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, write_T ? 1 : 0);
@@ -214,6 +215,7 @@ cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t s
     cudaFuncSetAttribute(k_prep<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k_prep<float><<<grid, kThreads, smem, st>>>(p, write_T ? 1 : 0);
   }
+  profile_post(st);
   return cudaGetLastError();
 }
 
@@ -224,6 +226,7 @@ cudaError_t launch_forward(const Params& p, bool bf16, cudaStream_t st) {
   const size_t smem = sizeof(float) * ((size_t)p.Dk * DVS + (size_t)kChunk * DVS +
                                        kChunk * kChunk + 3 * kChunk);
   dim3 grid(p.n_seqs, p.Hv, p.Dv / DVS);
+  profile_pre(st, KID_FWD_STATE);
   if (bf16) {
     cudaFuncSetAttribute(k_fwd_state<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k_fwd_state<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, DVS);
@@ -231,6 +234,7 @@ cudaError_t launch_forward(const Params& p, bool bf16, cudaStream_t st) {
     cudaFuncSetAttribute(k_fwd_state<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k_fwd_state<float><<<grid, kThreads, smem, st>>>(p, DVS);
   }
+  profile_post(st);
   return cudaGetLastError();
 }
 

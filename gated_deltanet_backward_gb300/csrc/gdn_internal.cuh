@@ -139,6 +139,22 @@ struct Params {
   float* pd;
 };
 
+// Kernel ids reported to the profiling hook (gdn_profile_begin).
+enum KernelId {
+  KID_PREP = 0,
+  KID_FWD_STATE = 1,
+  KID_BWD_STATE = 2,
+  KID_BWD_GRADS = 3,
+  KID_BWD_QK = 4,
+  KID_BWD_GATES = 5,
+  KID_COUNT = 6
+};
+
+// Bracket one launch with the caller's profiling events (no-op when none are
+// registered on this host thread).
+void profile_pre(cudaStream_t st, int kernel_id);
+void profile_post(cudaStream_t st);
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t st);
 cudaError_t launch_forward(const Params& p, bool bf16, cudaStream_t st);

@@ -160,6 +160,23 @@ int gdn_read_device_status(const void* workspace, void* stream);
 /* A static, human-readable name for a gdn_status value. */
 const char* gdn_status_string(int status);
 
+/* Profiling aid (changes no result).  Between gdn_profile_begin and
+ * gdn_profile_end, every kernel that gdn_forward / gdn_backward launch from the
+ * calling host thread is bracketed by two of the caller's CUDA events, recorded
+ * on the call's stream: launch i (counted from begin) records events[2*i] just
+ * before and events[2*i+1] just after itself and stores its kernel id in
+ * kernel_ids[i], for i < n_pairs.  `events` holds 2*n_pairs cudaEvent_t handles
+ * created by the caller (plain events, not disabled timing); the caller reads
+ * cudaEventElapsedTime(events[2i], events[2i+1]) after synchronising.  The
+ * registration is per host thread and holds pointers only.
+ * gdn_profile_begin returns GDN_OK or GDN_ERR_INVALID_ARG; gdn_profile_end
+ * returns the number of launches seen (which may exceed n_pairs). */
+int gdn_profile_begin(void* const* events, int32_t* kernel_ids, int32_t n_pairs);
+int gdn_profile_end(void);
+
+/* Name of a kernel id reported through gdn_profile_begin ("?" if unknown). */
+const char* gdn_kernel_name(int32_t kernel_id);
+
 #ifdef __cplusplus
 }
 #endif

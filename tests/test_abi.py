@@ -14,8 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def gdn():
-    from gated_deltanet_backward_gb300 import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__._builder().build()
     import gated_deltanet_backward_gb300 as g
     return g
 
