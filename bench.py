@@ -1,0 +1,470 @@
+"""Throughput of the Gated DeltaNet forward + backward on GB300.
+
+One step = gdn_forward followed by gdn_backward over one batch of the workload
+(default: the 27B-shaped layer, 1 x 4096 tokens, 16 key heads shared by 48 value
+heads, head size 128, bf16 q/k/v/o/dO, fp32 gates and state), inputs already
+resident in HBM.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
+events on the launch stream, with a 256 MB write between steps (flushes the
+129 MB L2) outside the events; barrier + synchronize around the timed loop;
+max over ranks.  The library's profiling hook times every kernel launch of the
+timed steps with CUDA events on the same stream, which gives the dominant
+kernel's average duration for the roofline entry.
+
+Multi-GPU: the work shards into independent (sequence, key-head group) units,
+so N ranks each run their own batch with no data-path collective ("weak"
+scaling); value = all ranks' tokens / the slowest rank's time.
+
+--impl reference times the CPU oracle (f64, token by token, all host cores) on a
+bounded sample of the same workload: the pages ship no runnable implementation.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "GDN fwd+bwd tokens/s (Hk16/Hv48, d128, bf16) and % of roofline on 1 GB300"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return dict(hbm_gbs=float(pk["hbm_gbs"]), bf16_tflops=float(pk["bf16_tflops"]),
+                    bf16_tflops_sustained=float(pk.get("bf16_tflops_sustained",
+                                                       pk["bf16_tflops"])),
+                    sm_max_mhz=float(pk.get("sm_max_mhz", 2070.0)), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                    sm_max_mhz=2070.0, source="fallback")
+
+
+def alu_fp32_tflops(sm_mhz):
+    """FP32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------
+# Algorithmic work model.  Path level: what the method must move / compute per
+# token (bf16 q/k/v/o/dO and their grads, fp32 gates, fp32 chunk-start states).
+# Kernel level: each kernel's compulsory reads and writes of its own inputs and
+# outputs (workspace intermediates of this decomposition included), and the
+# multiply-add work of its contractions (2 FLOP per MAC; triangular products
+# counted at half).
+# ----------------------------------------------------------------------------
+def path_model(wl: W.Workload):
+    es = 2 if wl.dtype == "bf16" else 4
+    T, N, NC = wl.total_tokens, wl.n_seqs, wl.total_chunks
+    Hk, Hv, Dk, Dv, C = wl.Hk, wl.Hv, wl.Dk, wl.Dv, W.CHUNK
+    r = Hv // Hk
+    qk = 2 * Hk * Dk * es
+    v = Hv * Dv * es
+    gates = 2 * Hv * 4
+    states = NC * Hv * Dk * Dv * 4
+    fwd = T * (qk + v + gates + v) + states
+    bwd = T * (qk + v + gates + v) + states + T * (qk + v + gates)
+    st = N * Hv * Dk * Dv * 4
+    fwd += st * ((wl.S0_std > 0) + 1)
+    bwd += st * ((wl.S0_std > 0) + (wl.dST_std > 0) + 1)
+    # chunked-method FLOPs per chunk and value head (Grams shared by the r heads)
+    gram = 2 * C * C * Dk / r
+    f_fwd = (gram + 2 * C * C * Dk + 2 * C * C * Dv + C ** 3 / 3 + 2 * C * Dk * Dv + gram +
+             2 * C * Dk * Dv + C * C * Dv + 2 * C * Dk * Dv)
+    f_bwd = (f_fwd - 2 * C * Dk * Dv - C * C * Dv  # recompute everything but O
+             + C * C * Dv + 2 * C * Dk * Dv + 4 * C * Dk * Dv  # dDelta, dS carry
+             + 2 * C * C * Dv + 4 * C * Dk * Dv + 4 * C * C * Dk  # dP, dQ, dK
+             + 4 * C * Dk * Dv + 2 * C * Dk * Dv  # (QS).dO, (K dS).Delta, dW
+             + 2 * C * C * (Dv + Dk) + 2 * C * C * (Dv + Dk) + 4 * C ** 3 + 4 * C * C * Dk)
+    flops = NC * Hv * (f_fwd + f_bwd)
+    return dict(bytes_fwd=fwd, bytes_bwd=bwd, bytes=fwd + bwd, flops=flops)
+
+
+def kernel_models(wl: W.Workload):
+    """kernel name -> (algorithmic bytes per launch, FLOPs per launch, compute unit)."""
+    es = 2 if wl.dtype == "bf16" else 4
+    NC, N = wl.total_chunks, wl.n_seqs
+    Hk, Hv, Dk, Dv, C = wl.Hk, wl.Hv, wl.Dk, wl.Dv, W.CHUNK
+    r = Hv // Hk
+    T = wl.total_tokens
+    f4 = 4
+    prep_b = (T * (2 * Hk * Dk * es + Hv * Dv * es + 2 * Hv * 4) +
+              NC * Hk * C * (2 * Dk + 2) * f4 + NC * Hv * C * (Dk + Dv + 2) * f4)
+    prep_f = NC * Hk * (2 * C * C * Dk + r * (C ** 3 / 3 + 2 * C * C * (Dk + Dv)))
+    fst_b = (NC * Hk * C * 2 * Dk * f4 + NC * Hv * C * (Dk + Dv + 1) * f4 + T * Hv * Dv * es +
+             NC * Hv * Dk * Dv * f4)
+    fst_f = NC * Hv * (6 * C * Dk * Dv + C * C * Dv) + NC * Hk * 2 * C * C * Dk
+    bst_b = (NC * Hk * C * 2 * Dk * f4 + NC * Hv * C * (Dk + 1) * f4 + T * Hv * Dv * es +
+             NC * Hv * (Dk * Dv + C * Dv) * f4)
+    bst_f = NC * Hv * (C * C * Dv + 6 * C * Dk * Dv) + NC * Hk * 2 * C * C * Dk
+    bgr_b = (NC * Hv * (2 * Dk * Dv + C * (Dk + 2 * Dv + C + 3)) * f4 +
+             NC * Hk * C * 2 * Dk * f4 + T * Hv * 2 * Dv * es + T * Hv * 4 +
+             NC * Hv * 2 * C * Dk * f4 + T * Hv * Dv * es + T * Hv * 2 * 4)
+    bgr_f = NC * Hv * (12 * C * Dk * Dv + 2 * C * C * (5 * Dk + 3 * Dv) + 4 * C ** 3)
+    bqk_b = NC * Hv * 2 * C * Dk * f4 + NC * Hk * C * 2 * (Dk + 1) * f4 + T * Hk * 2 * Dk * es
+    return {
+        "gdn_prep": (prep_b, prep_f, "alu"),
+        "gdn_fwd_state": (fst_b, fst_f, "alu"),
+        "gdn_bwd_state": (bst_b, bst_f, "alu"),
+        "gdn_bwd_grads": (bgr_b, bgr_f, "alu"),
+        "gdn_bwd_qk": (bqk_b, 0.0, "alu"),
+        "gdn_bwd_gates": (NC * Hv * 8 + Hv * 8, 0.0, "alu"),
+    }
+
+
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-i", str(index), "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in rows:
+            if len(row) < 9:
+                continue
+            try:
+                mhz.append(float(row[1]))
+                mx.append(float(row[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, row[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------------------
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import torch
+    import gated_deltanet_backward_gb300 as gdn
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wl = W.get(args.workload)
+    inp = W.generate(wl)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    T, Hk, Hv, Dk, Dv, N = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv, wl.n_seqs
+
+    def dev(a, dt=torch.float32):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device, dt)
+
+    qkv = dev(inp.qkv, tdt)
+    q, k, v = qkv[:, :Hk * Dk], qkv[:, Hk * Dk:2 * Hk * Dk], qkv[:, 2 * Hk * Dk:]
+    alpha, beta_raw = dev(inp.alpha), dev(inp.beta_raw)
+    a_log, dt_bias = dev(inp.a_log), dev(inp.dt_bias)
+    S0, dS_T, dO = dev(inp.S0), dev(inp.dS_T), dev(inp.dO, tdt)
+    layer = gdn.Layer.create(Hk, Hv, Dk, Dv, inp.cu_seqlens, wl.dtype, wl.scale_value(),
+                             device=device)
+    o = torch.empty(T, Hv * Dv, device=device, dtype=tdt)
+    S_T = torch.empty(N, Hv, Dk, Dv, device=device)
+    dq = torch.empty(T, Hk * Dk, device=device, dtype=tdt)
+    dk = torch.empty_like(dq)
+    dv = torch.empty(T, Hv * Dv, device=device, dtype=tdt)
+    dalpha = torch.empty(T, Hv, device=device)
+    dbeta = torch.empty(T, Hv, device=device)
+    da_log = torch.empty(Hv, device=device)
+    ddt = torch.empty(Hv, device=device)
+    dS0 = torch.empty(N, Hv, Dk, Dv, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fwd():
+        layer.forward(q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream)
+
+    def bwd():
+        layer.backward(q, k, v, alpha, beta_raw, a_log, dt_bias, S0, dO, dS_T, dq, dk, dv,
+                       dalpha, dbeta, da_log, ddt, dS0, stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+        flush.zero_()
+    torch.cuda.synchronize()
+    assert gdn.gdn_read_device_status(layer.ws_bwd) == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    prof = gdn.gdn_profile(max_launches=16 * K)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with prof:
+        for i in range(K):
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            bwd()
+            ev[i][2].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    f_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    b_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = sum(f_ms[i] + b_ms[i] for i in range(K)) / K
+    if world > 1:
+        t = torch.tensor([step_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * T / (step_ms * 1e-3)
+
+    # per-kernel durations from the profiling hook
+    per = {}
+    for name, ms in prof.launches():
+        per.setdefault(name, []).append(ms)
+    launches = prof.count
+    tot = sum(sum(v) for v in per.values())
+    kernels = {n: {"launches": len(v), "avg_us": 1e3 * sum(v) / len(v),
+                   "share": sum(v) / tot if tot else 0.0} for n, v in per.items()}
+    pk = _peaks()
+    models = kernel_models(wl)
+    dom = max(per, key=lambda n: sum(per[n]))
+    b, f, unit = models[dom]
+    avg_s = sum(per[dom]) / len(per[dom]) * 1e-3
+    peak_alu = alu_fp32_tflops(pk["sm_max_mhz"])
+    t_mem = b / (pk["hbm_gbs"] * 1e9)
+    t_cmp = f / (peak_alu * 1e12) if unit == "alu" else f / (pk["bf16_tflops"] * 1e12)
+    if t_cmp > t_mem:
+        roof = {"bound": unit, "achieved": f / avg_s / 1e12,
+                "peak": peak_alu if unit == "alu" else pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": b / avg_s / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["algorithmic_bytes"] = b
+    roof["algorithmic_flops"] = f
+    roof["peak_source"] = pk["source"] if roof["unit"] == "GB/s" or unit != "alu" else \
+        "derived: 152 SMs x 128 FP32 lanes x 2 x %.0f MHz" % pk["sm_max_mhz"]
+    pm = path_model(wl)
+    t_roof = max(pm["bytes"] / (pk["hbm_gbs"] * 1e9), pm["flops"] / (pk["bf16_tflops"] * 1e12))
+    path_roof = {"bytes_per_step": pm["bytes"], "flops_per_step": pm["flops"],
+                 "roofline_us": t_roof * 1e6, "roofline_tokens_per_s": T / t_roof,
+                 "frac": (T / (step_ms * 1e-3)) / (T / t_roof),
+                 "bound": "hbm" if pm["bytes"] / (pk["hbm_gbs"] * 1e9) >= pm["flops"] / (
+                     pk["bf16_tflops"] * 1e12) else "tensor"}
+
+    e2e = run_e2e(args, inp, layer, device, tdt, world) if not args.no_e2e else None
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "%s: %d x %d tokens, Hk=%d, Hv=%d, Dk=%d, Dv=%d, %s q/k/v/o/dO, "
+                               "fp32 gates/state" % (wl.name, N, T // max(N, 1), Hk, Hv, Dk, Dv,
+                                                      wl.dtype),
+                   "tokens_per_gpu": T, "io_dtype": wl.dtype, "compute": "fp32 CUDA-core FMA",
+                   "l2": "flushed: 256 MB write between timed steps",
+                   "parallelism": "independent batch per GPU" if world > 1 else "single GPU"},
+        "fwd_ms": sum(f_ms) / K, "bwd_ms": sum(b_ms) / K,
+        "roofline": roof, "path_roofline": path_roof, "kernels": kernels,
+        "gpu_launches": launches, "clocks": clocks, "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, inp, layer, device, tdt, world):
+    """Same metric through the public API with host buffers: every step copies its inputs
+    from pinned host memory to the device and reads the results back."""
+    import torch
+    wl = inp.wl
+    T, Hk, Hv, Dk, Dv, N = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv, wl.n_seqs
+
+    def pin(a, dt=torch.float32):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dt).pin_memory()
+
+    h_in = dict(qkv=pin(inp.qkv, tdt), alpha=pin(inp.alpha), beta_raw=pin(inp.beta_raw),
+                a_log=pin(inp.a_log), dt_bias=pin(inp.dt_bias), dO=pin(inp.dO, tdt),
+                S0=pin(inp.S0), dS_T=pin(inp.dS_T))
+    d_in = {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, device=device))
+            for k, v in h_in.items()}
+    outs = dict(o=(T, Hv * Dv, tdt), dq=(T, Hk * Dk, tdt), dk=(T, Hk * Dk, tdt),
+                dv=(T, Hv * Dv, tdt), dalpha=(T, Hv, torch.float32),
+                dbeta=(T, Hv, torch.float32), da_log=(Hv, None, torch.float32),
+                ddt=(Hv, None, torch.float32), S_T=(N, Hv * Dk * Dv, torch.float32),
+                dS0=(N, Hv * Dk * Dv, torch.float32))
+    d_out = {k: torch.empty(s[:2] if s[1] else (s[0],), dtype=s[2], device=device)
+             for k, s in outs.items()}
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in d_out.items()}
+    stream = torch.cuda.current_stream(device)
+    bytes_in = sum(v.numel() * v.element_size() for v in h_in.values() if v is not None)
+    bytes_out = sum(v.numel() * v.element_size() for v in h_out.values())
+
+    def step():
+        for key, h in h_in.items():
+            if h is not None:
+                d_in[key].copy_(h, non_blocking=True)
+        qkv = d_in["qkv"]
+        q, k, v = qkv[:, :Hk * Dk], qkv[:, Hk * Dk:2 * Hk * Dk], qkv[:, 2 * Hk * Dk:]
+        S0 = None if d_in["S0"] is None else d_in["S0"]
+        dS_T = None if d_in["dS_T"] is None else d_in["dS_T"]
+        layer.forward(q, k, v, d_in["alpha"], d_in["beta_raw"], d_in["a_log"], d_in["dt_bias"],
+                      S0, d_out["o"], d_out["S_T"].view(N, Hv, Dk, Dv), stream)
+        layer.backward(q, k, v, d_in["alpha"], d_in["beta_raw"], d_in["a_log"],
+                       d_in["dt_bias"], S0, d_in["dO"], dS_T, d_out["dq"], d_out["dk"],
+                       d_out["dv"], d_out["dalpha"], d_out["dbeta"], d_out["da_log"],
+                       d_out["ddt"], d_out["dS0"].view(N, Hv, Dk, Dv), stream)
+        for key, h in h_out.items():
+            h.copy_(d_out[key], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(bytes_in), "d2h_bytes_per_step": int(bytes_out)}
+
+
+def _oracle_step(inp, tokens):
+    import oracle
+    wl = inp.wl
+    cu = np.array([0, tokens], np.int32) if tokens < wl.total_tokens else inp.cu_seqlens
+    sl = slice(0, tokens)
+    S0 = inp.S0 if tokens >= wl.total_tokens else (None if inp.S0 is None else inp.S0[:1])
+    dS_T = inp.dS_T if tokens >= wl.total_tokens else (None if inp.dS_T is None else inp.dS_T[:1])
+    kw = dict(Hk=wl.Hk, Hv=wl.Hv, Dk=wl.Dk, Dv=wl.Dv, scale=wl.scale_value())
+    oracle.forward(inp.q[sl], inp.k[sl], inp.v[sl], inp.alpha[sl], inp.beta_raw[sl], inp.a_log,
+                   inp.dt_bias, cu, S0, **kw)
+    oracle.backward(inp.q[sl], inp.k[sl], inp.v[sl], inp.alpha[sl], inp.beta_raw[sl], inp.a_log,
+                    inp.dt_bias, cu, inp.dO[sl], S0, dS_T, **kw)
+
+
+def cpu_baseline(wl, inp, tokens):
+    import oracle
+    tokens = min(tokens, wl.total_tokens)
+    t0 = time.perf_counter()
+    _oracle_step(inp, tokens)
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": oracle.hardware_threads(),
+            "kind": "oracle",
+            "sample": "f64 token-by-token forward + backward of the first %d tokens of %s "
+                      "(all %d value heads), one pass, %.1f s" % (tokens, wl.name, wl.Hv, dt)}
+
+
+def run_reference(args):
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    import oracle
+    wl = W.get(args.workload)
+    inp = W.generate(wl)
+    tokens = min(args.ref_tokens, wl.total_tokens)
+    oracle.build()
+    for _ in range(args.warmup):
+        _oracle_step(inp, tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(inp, tokens)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = tokens / dt
+    sample = ("f64 token-by-token CPU oracle, forward + backward of the first %d tokens of %s "
+              "(all %d value heads) per step" % (tokens, wl.name, wl.Hv))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "tokens_per_step": tokens},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.hardware_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="l27b_bf16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-tokens", type=int, default=4096)
+    ap.add_argument("--ref-tokens", type=int, default=512)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

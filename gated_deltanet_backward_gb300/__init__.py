@@ -69,9 +69,16 @@ _lib.gdn_read_device_status.argtypes = [_vp, _vp]
 _lib.gdn_read_device_status.restype = ctypes.c_int
 _lib.gdn_status_string.argtypes = [ctypes.c_int]
 _lib.gdn_status_string.restype = ctypes.c_char_p
+_lib.gdn_profile_begin.argtypes = [ctypes.POINTER(ctypes.c_void_p), _I32P, ctypes.c_int32]
+_lib.gdn_profile_begin.restype = ctypes.c_int
+_lib.gdn_profile_end.argtypes = []
+_lib.gdn_profile_end.restype = ctypes.c_int
+_lib.gdn_kernel_name.argtypes = [ctypes.c_int32]
+_lib.gdn_kernel_name.restype = ctypes.c_char_p
 
 EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_forward",
-            "gdn_backward", "gdn_read_device_status", "gdn_status_string")
+            "gdn_backward", "gdn_read_device_status", "gdn_status_string", "gdn_profile_begin",
+            "gdn_profile_end", "gdn_kernel_name")
 
 
 class GdnError(RuntimeError):
@@ -127,6 +134,8 @@ def _mat(t):
         return None, 0
     if t.dim() != 2:
         raise ValueError("expected a 2-D tensor, got shape %s" % (tuple(t.shape),))
+    if t.numel() == 0:
+        return int(t.data_ptr()), max(int(t.stride(0)), int(t.shape[1]))
     if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError("columns must be contiguous (stride(1) == 1)")
     return int(t.data_ptr()), int(t.stride(0))
@@ -175,6 +184,40 @@ def gdn_read_device_status(workspace, stream=None) -> int:
     return int(_lib.gdn_read_device_status(_ptr(workspace), _stream(stream)))
 
 
+def gdn_kernel_name(kernel_id: int) -> str:
+    return _lib.gdn_kernel_name(int(kernel_id)).decode()
+
+
+class gdn_profile:
+    """Context manager around gdn_profile_begin / gdn_profile_end: brackets each kernel
+    the library launches from this thread with two torch.cuda.Event's (recorded by the
+    library on the launch's stream).  After exit and a synchronize, ``launches()`` gives
+    (kernel name, milliseconds) per launch and ``count`` the launches seen."""
+
+    def __init__(self, max_launches: int):
+        import torch
+        self.n = int(max_launches)
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * self.n)]
+        self._handles = (ctypes.c_void_p * (2 * self.n))(
+            *[ctypes.c_void_p(e.cuda_event) for e in self.events])
+        self._ids = np.zeros(max(1, self.n), dtype=np.int32)
+        self.count = 0
+
+    def __enter__(self):
+        _check(_lib.gdn_profile_begin(self._handles, self._ids.ctypes.data_as(_I32P), self.n),
+               "gdn_profile_begin")
+        return self
+
+    def __exit__(self, *exc):
+        self.count = int(_lib.gdn_profile_end())
+        return False
+
+    def launches(self):
+        m = min(self.count, self.n)
+        return [(gdn_kernel_name(self._ids[i]),
+                 self.events[2 * i].elapsed_time(self.events[2 * i + 1])) for i in range(m)]
+
+
 @dataclass
 class Layer:
     """Device buffers for one varlen batch: shape, plan, saved states, workspaces.
@@ -215,5 +258,5 @@ class Layer:
                      dbeta_raw, da_log, ddt_bias, dS0, self.ws_bwd, stream)
 
 
-__all__ = list(EXPORTED) + ["gdn_shape", "make_shape", "Layer", "GdnError", "LIB_PATH", "CHUNK",
+__all__ = list(EXPORTED) + ["gdn_profile", "gdn_shape", "make_shape", "Layer", "GdnError", "LIB_PATH", "CHUNK",
                             "GDN_DTYPE_F32", "GDN_DTYPE_BF16"]
