@@ -73,18 +73,26 @@ _lib.gdn_profile_begin.argtypes = [ctypes.POINTER(ctypes.c_void_p), _I32P, ctype
 _lib.gdn_profile_begin.restype = ctypes.c_int
 _lib.gdn_profile_end.argtypes = []
 _lib.gdn_profile_end.restype = ctypes.c_int
+_lib.gdn_last_error.argtypes = []
+_lib.gdn_last_error.restype = ctypes.c_char_p
 _lib.gdn_kernel_name.argtypes = [ctypes.c_int32]
 _lib.gdn_kernel_name.restype = ctypes.c_char_p
 
 EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_forward",
             "gdn_backward", "gdn_read_device_status", "gdn_status_string", "gdn_profile_begin",
-            "gdn_profile_end", "gdn_kernel_name")
+            "gdn_profile_end", "gdn_kernel_name", "gdn_last_error")
 
 
 class GdnError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__("%s failed: %s (%d)" % (where, gdn_status_string(code), code))
+        detail = gdn_last_error() if code == -4 else ""
+        super().__init__("%s failed: %s (%d)%s" % (where, gdn_status_string(code), code,
+                                                   (" -- " + detail) if detail else ""))
+
+
+def gdn_last_error() -> str:
+    return _lib.gdn_last_error().decode()
 
 
 def gdn_status_string(code: int) -> str:

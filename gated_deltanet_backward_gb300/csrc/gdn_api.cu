@@ -1,6 +1,7 @@
 // gdn_api.cu -- the C ABI of libgdn.so: argument checks, workspace carving and
 // kernel launches.  See include/gdn.h for the contract of every entry point.
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 
 #include "gdn_internal.cuh"
@@ -139,6 +140,15 @@ int check_workspace(const gdn_shape* s, void* ws, size_t bytes, bool bwd) {
   return GDN_OK;
 }
 
+thread_local char g_last_error[160] = "";
+
+// Records which CUDA call failed (see gdn_last_error) and returns GDN_ERR_CUDA.
+int cuda_fail(const char* what, cudaError_t e) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return GDN_ERR_CUDA;
+}
+
 struct ProfileState {
   void* const* events = nullptr;
   int32_t* ids = nullptr;
@@ -187,6 +197,8 @@ int gdn_profile_end(void) {
   g_profile = ProfileState();
   return n;
 }
+
+const char* gdn_last_error(void) { return g_last_error; }
 
 const char* gdn_kernel_name(int32_t id) {
   switch (id) {
@@ -250,16 +262,20 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
   p.o_ld = o_ld;
   p.S_T = S_T;
   p.saved = saved_states;
-  if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return GDN_ERR_CUDA;
+  (void)cudaGetLastError();  // report only errors of this call's own launches
+  g_last_error[0] = 0;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail("gdn_forward: clearing the status word", e);
   if (s->n_seqs > 0 && s->total_chunks == 0) {
     // every sequence is empty: S_T = S_0
     if (!S_T) return GDN_OK;
     const size_t bytes = (size_t)s->n_seqs * s->Hv * s->Dk * s->Dv * sizeof(float);
-    const cudaError_t e = S0 ? cudaMemcpyAsync(S_T, S0, bytes, cudaMemcpyDeviceToDevice, st)
-                             : cudaMemsetAsync(S_T, 0, bytes, st);
-    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    e = S0 ? cudaMemcpyAsync(S_T, S0, bytes, cudaMemcpyDeviceToDevice, st)
+           : cudaMemsetAsync(S_T, 0, bytes, st);
+    return e == cudaSuccess ? GDN_OK : cuda_fail("gdn_forward: S_T of empty sequences", e);
   }
-  if (gdn::launch_forward(p, s->dtype == GDN_DTYPE_BF16, st) != cudaSuccess) return GDN_ERR_CUDA;
+  e = gdn::launch_forward(p, s->dtype == GDN_DTYPE_BF16, st);
+  if (e != cudaSuccess) return cuda_fail("gdn_forward: kernel launch", e);
   return GDN_OK;
 }
 
@@ -310,14 +326,18 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
   p.da_log = da_log;
   p.ddt_bias = ddt_bias;
   p.dS0 = dS0;
-  if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return GDN_ERR_CUDA;
+  (void)cudaGetLastError();  // report only errors of this call's own launches
+  g_last_error[0] = 0;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail("gdn_backward: clearing the status word", e);
   if (s->total_chunks == 0 && s->n_seqs > 0 && dS0) {
     const size_t bytes = (size_t)s->n_seqs * s->Hv * s->Dk * s->Dv * sizeof(float);
-    const cudaError_t e = dS_T ? cudaMemcpyAsync(dS0, dS_T, bytes, cudaMemcpyDeviceToDevice, st)
-                               : cudaMemsetAsync(dS0, 0, bytes, st);
-    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    e = dS_T ? cudaMemcpyAsync(dS0, dS_T, bytes, cudaMemcpyDeviceToDevice, st)
+             : cudaMemsetAsync(dS0, 0, bytes, st);
+    if (e != cudaSuccess) return cuda_fail("gdn_backward: dS_0 of empty sequences", e);
   }
-  if (gdn::launch_backward(p, s->dtype == GDN_DTYPE_BF16, st) != cudaSuccess) return GDN_ERR_CUDA;
+  e = gdn::launch_backward(p, s->dtype == GDN_DTYPE_BF16, st);
+  if (e != cudaSuccess) return cuda_fail("gdn_backward: kernel launch", e);
   return GDN_OK;
 }
 
@@ -325,9 +345,10 @@ int gdn_read_device_status(const void* workspace, void* stream) {
   if (!workspace) return GDN_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   gdn::DeviceStatus h{};
-  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return GDN_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail("gdn_read_device_status: copy", e);
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail("gdn_read_device_status: synchronize", e);
   return h.code;
 }
 

@@ -1,0 +1,188 @@
+// umma.cuh -- Blackwell (sm_100 family) tensor-core building blocks in inline PTX:
+// TMEM allocation, tcgen05.mma (kind::f16, bf16 x bf16 -> fp32), tcgen05.commit
+// onto an mbarrier, tcgen05.ld of the fp32 accumulator, shared-memory matrix
+// descriptors for K-major operands in the 128-byte swizzled layout, and bounded
+// mbarrier waits.
+//
+// Operand tiles ("K-major SW128"): a tile of R rows (the M or N index) by K
+// columns of bf16 is stored as K/64 column blocks; block b holds columns
+// [64b, 64b+64) of every row, row r at byte r*128 of the block, and the 16-byte
+// chunk j of a row at chunk position j ^ (r % 8).  Blocks are R*128 bytes
+// apart and 1024-byte aligned.  This is the layout the MMA unit reads with a
+// descriptor of swizzle mode 128B, stride between 8-row groups 1024 bytes; a
+// K step of 16 elements inside a block advances the descriptor's start
+// address by 32 bytes.
+//
+// Accumulator (M = 128, cta_group::1): row i of D lives in TMEM lane i, column
+// j in TMEM column (base + j), one fp32 per cell.  Warp w of a CTA may read
+// lanes [32 (w % 4), 32 (w % 4) + 32).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gdn {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete.  Gives up after
+// `limit_ns` nanoseconds of wall time and returns false (the caller records
+// GDN_ERR_TIMEOUT and winds down); never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < (1u << 30); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// ------------------------------------------------------------------ fences
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (the tensor core reads operands through it).
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// -------------------------------------------------------------------- TMEM
+// Whole warp: allocates `ncols` TMEM columns (power of two, >= 32) and writes
+// the base address to *dst (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Whole warp: 16 consecutive fp32 columns of the warp's 32 lanes; thread t gets
+// lane (lane base + t).  Follow with tmem_ld_wait() before using the values.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------ descriptors
+// Shared-memory descriptor of a K-major, 128-byte-swizzled operand starting at
+// shared address `saddr` (the block base must be 1024-byte aligned; the start
+// may be offset by a multiple of 32 bytes inside the first 128-byte row for
+// K steps).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading-dimension byte offset (unused with SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: 8-row groups are 1024 B apart
+  d |= (uint64_t)1 << 46;              // descriptor version for sm_100 family
+  d |= (uint64_t)2 << 61;              // swizzle mode: 128B
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
+// both operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// One thread: D[tmem] (+)= A * B^T, single K=16 step.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One thread: arrive once on `bar` when every MMA this thread issued so far has
+// completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// Byte offset of element (row, k) in a K-major SW128 bf16 tile of `rows` rows.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int k, int rows) {
+  const uint32_t blk = (uint32_t)(k >> 6);
+  const uint32_t byte = (uint32_t)(k & 63) * 2u;
+  const uint32_t chunk = (byte >> 4) ^ (uint32_t)(row & 7);
+  return blk * (uint32_t)rows * 128u + (uint32_t)row * 128u + chunk * 16u + (byte & 15u);
+}
+
+// Issues D (+)= A[M x K] * B[N x K]^T over K (multiple of 16) from K-major SW128
+// tiles at shared addresses a_base (M rows) and b_base (N rows).
+__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_base, int M, uint32_t b_base,
+                                         int N, int K, uint32_t accumulate_first) {
+  const uint32_t idesc = idesc_bf16(M, N);
+  for (int kk = 0; kk < K; kk += 16) {
+    const uint32_t a = a_base + (uint32_t)(kk >> 6) * (uint32_t)M * 128u + (uint32_t)(kk & 63) * 2u;
+    const uint32_t b = b_base + (uint32_t)(kk >> 6) * (uint32_t)N * 128u + (uint32_t)(kk & 63) * 2u;
+    mma_bf16(d_tmem, desc_sw128(a), desc_sw128(b), idesc, (kk > 0) ? 1u : accumulate_first);
+  }
+}
+
+}  // namespace tc
+}  // namespace gdn

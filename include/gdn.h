@@ -160,6 +160,11 @@ int gdn_read_device_status(const void* workspace, void* stream);
 /* A static, human-readable name for a gdn_status value. */
 const char* gdn_status_string(int status);
 
+/* After a call of this host thread returned GDN_ERR_CUDA: which CUDA call
+ * failed and the CUDA error name; "" otherwise.  The string is owned by the
+ * library and stays valid until this thread's next gdn_forward / gdn_backward. */
+const char* gdn_last_error(void);
+
 /* Profiling aid (changes no result).  Between gdn_profile_begin and
  * gdn_profile_end, every kernel that gdn_forward / gdn_backward launch from the
  * calling host thread is bracketed by two of the caller's CUDA events, recorded
