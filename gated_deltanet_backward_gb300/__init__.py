@@ -206,6 +206,9 @@ class gdn_profile:
         import torch
         self.n = int(max_launches)
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * self.n)]
+        for e in self.events:   # torch creates the CUDA event on its first record
+            e.record()
+        torch.cuda.current_stream().synchronize()
         self._handles = (ctypes.c_void_p * (2 * self.n))(
             *[ctypes.c_void_p(e.cuda_event) for e in self.events])
         self._ids = np.zeros(max(1, self.n), dtype=np.int32)

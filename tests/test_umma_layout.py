@@ -1,0 +1,63 @@
+"""The tensor-core building blocks (csrc/umma.cuh) on the GPU, in isolation.
+
+A probe kernel (tests/cuda/umma_check.cu, test-only) issues one tcgen05.mma of
+kind::f16 (bf16 x bf16 -> fp32) from K-major 128-byte-swizzled shared-memory
+tiles and dumps every TMEM lane.  Checks: the instruction and shared-memory
+descriptors give D = A B^T; for M = 128 row i sits in lane i; the lane layout of
+M = 64 is recorded (rows 16w..16w+15 in lanes 32w..32w+15)."""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+@pytest.fixture(scope="module")
+def probe():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    src = os.path.join(HERE, "cuda", "umma_check.cu")
+    lib = os.path.join(HERE, "cuda", "libumma_check.so")
+    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2",
+                           "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-cudart", "shared",
+                           "-I", os.path.join(ROOT, "gated_deltanet_backward_gb300", "csrc"),
+                           src, "-o", lib])
+    L = ctypes.CDLL(lib)
+    L.umma_check.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    L.umma_check.restype = ctypes.c_int
+    return torch, L
+
+
+def _run(probe, M, N, K, seed=0):
+    torch, L = probe
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    dA, dB = A.cuda(), B.cuda()
+    out = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = L.umma_check(dA.data_ptr(), dB.data_ptr(), out.data_ptr(), M, N, K, st.data_ptr())
+    assert rc == 0 and int(st.item()) == 0
+    ref = (A.double() @ B.double().T).numpy()
+    return out.cpu().double().numpy(), ref
+
+
+@pytest.mark.parametrize("N,K", [(16, 16), (64, 64), (64, 128), (128, 128), (256, 64), (32, 96)])
+def test_m128_is_row_per_lane(probe, N, K):
+    got, ref = _run(probe, 128, N, K)
+    err = np.abs(got - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("N,K", [(64, 128), (128, 64)])
+def test_m64_lane_layout(probe, N, K):
+    got, ref = _run(probe, 64, N, K)
+    lanes = np.array([32 * (i // 16) + (i % 16) for i in range(64)])
+    err = np.abs(got[lanes] - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
