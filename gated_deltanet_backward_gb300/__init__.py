@@ -65,6 +65,10 @@ _lib.gdn_forward.restype = ctypes.c_int
 _lib.gdn_backward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] + [_vp, _vp] +
                               [_vp, _i64] * 5 + [_vp, _vp, _vp, _vp, _sz, _vp])
 _lib.gdn_backward.restype = ctypes.c_int
+# as gdn_forward without the workspace and its size
+_lib.gdn_forward_noalloc.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] +
+                                     [_vp, _vp, _vp])
+_lib.gdn_forward_noalloc.restype = ctypes.c_int
 _lib.gdn_read_device_status.argtypes = [_vp, _vp]
 _lib.gdn_read_device_status.restype = ctypes.c_int
 _lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -80,7 +84,7 @@ _lib.gdn_kernel_name.restype = ctypes.c_char_p
 
 EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_forward",
             "gdn_backward", "gdn_read_device_status", "gdn_status_string", "gdn_profile_begin",
-            "gdn_profile_end", "gdn_kernel_name", "gdn_last_error")
+            "gdn_profile_end", "gdn_kernel_name", "gdn_last_error", "gdn_forward_noalloc")
 
 
 class GdnError(RuntimeError):
@@ -186,6 +190,19 @@ def gdn_backward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, ch
     args += [_ptr(da_log), _ptr(ddt_bias), _ptr(dS0), _ptr(workspace),
              int(workspace.numel() * workspace.element_size()), _stream(stream)]
     _check(_lib.gdn_backward(*args), "gdn_backward")
+
+
+def gdn_forward_noalloc(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens,
+                        chunk_offsets, S0, o, S_T, saved_states, stream=None) -> None:
+    """Calls gdn_forward_noalloc: the forward using the library's built-in scratch array
+    instead of a caller workspace, for callers that cannot allocate device memory."""
+    args = [ctypes.byref(shape)]
+    for t in (q, k, v, alpha, beta_raw):
+        args += list(_mat(t))
+    args += [_ptr(a_log), _ptr(dt_bias), _ptr(cu_seqlens), _ptr(chunk_offsets), _ptr(S0)]
+    args += list(_mat(o))
+    args += [_ptr(S_T), _ptr(saved_states), _stream(stream)]
+    _check(_lib.gdn_forward_noalloc(*args), "gdn_forward_noalloc")
 
 
 def gdn_read_device_status(workspace, stream=None) -> int:

@@ -162,6 +162,10 @@ thread_local ProfileState g_profile;
 
 namespace gdn {
 
+// Lets other translation units of the library explain a failure through
+// gdn_last_error().
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
 void profile_pre(cudaStream_t st, int kernel_id) {
   ProfileState& P = g_profile;
   if (!P.on) return;

@@ -152,6 +152,39 @@ int gdn_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void
                  float* ddt_bias, float* dS0, void* workspace, size_t workspace_bytes,
                  void* stream);
 
+/* Size of the scratch array built into the library for gdn_forward_noalloc. */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* gdn_forward for callers that cannot allocate device memory (no counterpart on
+ * the pages this library implements; it is a convenience of this library).
+ * Some callers may not call cudaMalloc: code that runs under a device-memory
+ * budget fixed at start-up, plugin hosts that pass a kernel its inputs and
+ * outputs but no scratch, and paths that cannot accept the implicit device
+ * synchronisation of cudaMalloc / cudaFree.  This entry point takes the same
+ * arguments as gdn_forward minus the workspace and uses instead one scratch
+ * array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library, which
+ * every GPU that loads the library holds until the process exits.  It allocates
+ * nothing.
+ *  - Shapes whose gdn_workspace_bytes(shape, 0) exceeds GDN_NOALLOC_SCRATCH_BYTES
+ *    are rejected with GDN_ERR_WORKSPACE before anything is launched
+ *    (gdn_last_error() says why); use gdn_forward with a caller workspace.
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *    first call before any stream capture.
+ *  - All calls on a device share the one scratch array, which keeps the last
+ *    call's contents (each call clears what must start at zero).  Calls whose
+ *    work overlaps on the GPU (concurrent streams, or host threads) race on it:
+ *    serialise them.
+ *  - The device-side status of these calls is not readable through
+ *    gdn_read_device_status (the caller has no workspace pointer).
+ * Returns a gdn_status like gdn_forward. */
+int gdn_forward_noalloc(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
+                        int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                        int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                        const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
+                        const int32_t* chunk_offsets, const float* S0, void* o, int64_t o_ld,
+                        float* S_T, float* saved_states, void* stream);
+
 /* Synchronises `stream` and returns the device-side status recorded in
  * `workspace` by the last gdn_forward / gdn_backward that used it (GDN_OK, or
  * the first device error), or GDN_ERR_CUDA if the stream itself failed. */
