@@ -112,6 +112,19 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
     p.pa = (float*)(base + L.pa);
     p.pd = (float*)(base + L.pd);
   }
+  if (s->dtype == GDN_DTYPE_BF16) {
+    p.Qsw = (uint8_t*)(base + L.Qsw);
+    p.Ksw = (uint8_t*)(base + L.Ksw);
+    p.Ktsw = (uint8_t*)(base + L.Ktsw);
+    p.Wsw = (uint8_t*)(base + L.Wsw);
+    p.Psw = (uint8_t*)(base + L.Psw);
+    p.Utb = (__nv_bfloat16*)(base + L.Utb);
+    if (bwd) {
+      p.Wtsw = (uint8_t*)(base + L.Wtsw);
+      p.QKf = (float*)(base + L.QKf);
+      p.KKf = (float*)(base + L.KKf);
+    }
+  }
 }
 
 int check_inputs(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, int64_t k_ld,
@@ -212,6 +225,8 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_BWD_GRADS: return "gdn_bwd_grads";
     case gdn::KID_BWD_QK: return "gdn_bwd_qk";
     case gdn::KID_BWD_GATES: return "gdn_bwd_gates";
+    case gdn::KID_PREP_TC: return "gdn_prep_tc";
+    case gdn::KID_FWD_STATE_TC: return "gdn_fwd_state_tc";
     default: return "?";
   }
 }

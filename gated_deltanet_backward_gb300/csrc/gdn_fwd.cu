@@ -220,6 +220,12 @@ cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t s
 }
 
 cudaError_t launch_forward(const Params& p, bool bf16, cudaStream_t st) {
+  if (bf16) {
+    // bf16 inputs: tensor-core chunk preparation and state walk
+    cudaError_t e = launch_prep_tc(p, false, st);
+    if (e != cudaSuccess) return e;
+    return launch_fwd_state_tc(p, st);
+  }
   cudaError_t e = launch_prep(p, bf16, false, st);
   if (e != cudaSuccess || p.n_seqs == 0) return e;
   const int DVS = p.Dv < 32 ? p.Dv : 32;

@@ -49,8 +49,24 @@ struct WsLayout {
   size_t dKh;     // [NC][Hv][C][Dk] per-value-head d k_hat partials (backward)
   size_t pa;      // [NC][Hv] per-chunk partial of d a_log (backward)
   size_t pd;      // [NC][Hv] per-chunk partial of d dt_bias (backward)
+  // bf16 tensor-core path: operand tiles in the K-major 128B-swizzled layout
+  // (see umma.cuh), written by the chunk preparation, copied as-is by the
+  // state walks.
+  size_t Qsw;     // [NC][Hk] tile [C rows][Dk]   normalised queries
+  size_t Ksw;     // [NC][Hk] tile [C rows][Dk]   normalised keys
+  size_t Ktsw;    // [NC][Hk] tile [Dk rows][C]   normalised keys, transposed
+  size_t Wsw;     // [NC][Hv] tile [C rows][Dk]   W
+  size_t Wtsw;    // [NC][Hv] tile [Dk rows][C]   W^T (backward)
+  size_t Psw;     // [NC][Hv] tile [C rows][C]    P = E * (Q K^T), lower incl. diagonal
+  size_t Utb;     // [NC][Hv][Dv][C] bf16         U^T
+  size_t QKf;     // [NC][Hk][C][C] fp32          Q K^T (backward)
+  size_t KKf;     // [NC][Hk][C][C] fp32          K K^T (backward)
   size_t total;
 };
+
+// Bytes of the bf16 SW128 operand tiles (C = 64 rows or columns).
+inline size_t tile_CxD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
+inline size_t tile_DxC(int D) { return (size_t)D * 128; }
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -81,6 +97,19 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
     L.dKh = take(NC * Hv * C * Dk * 4);
     L.pa = take(NC * Hv * 4);
     L.pd = take(NC * Hv * 4);
+  }
+  if (s.dtype == GDN_DTYPE_BF16) {
+    L.Qsw = take(NC * Hk * tile_CxD(s.Dk));
+    L.Ksw = take(NC * Hk * tile_CxD(s.Dk));
+    L.Ktsw = take(NC * Hk * tile_DxC(s.Dk));
+    L.Wsw = take(NC * Hv * tile_CxD(s.Dk));
+    L.Psw = take(NC * Hv * tile_CxD(64));
+    L.Utb = take(NC * Hv * Dv * C * 2);
+    if (bwd) {
+      L.Wtsw = take(NC * Hv * tile_DxC(s.Dk));
+      L.QKf = take(NC * Hk * C * C * 4);
+      L.KKf = take(NC * Hk * C * C * 4);
+    }
   }
   L.total = off;
   return L;
@@ -137,6 +166,15 @@ struct Params {
   float* dKh;
   float* pa;
   float* pd;
+  uint8_t* Qsw;
+  uint8_t* Ksw;
+  uint8_t* Ktsw;
+  uint8_t* Wsw;
+  uint8_t* Wtsw;
+  uint8_t* Psw;
+  __nv_bfloat16* Utb;
+  float* QKf;
+  float* KKf;
 };
 
 // Kernel ids reported to the profiling hook (gdn_profile_begin).
@@ -147,13 +185,19 @@ enum KernelId {
   KID_BWD_GRADS = 3,
   KID_BWD_QK = 4,
   KID_BWD_GATES = 5,
-  KID_COUNT = 6
+  KID_PREP_TC = 6,
+  KID_FWD_STATE_TC = 7,
+  KID_COUNT = 8
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
 // registered on this host thread).
 void profile_pre(cudaStream_t st, int kernel_id);
 void profile_post(cudaStream_t st);
+
+// Tensor-core (bf16) launchers.
+cudaError_t launch_prep_tc(const Params& p, bool bwd, cudaStream_t st);
+cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st);
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t st);

@@ -1,0 +1,91 @@
+// gdn_tc.cuh -- CTA-level helpers for the tensor-core (tcgen05) kernels:
+// accumulator row ownership, epilogue column walks, staging of bf16 operand
+// tiles in the K-major 128B-swizzled layout, and MMA completion waits that all
+// threads agree on.
+#pragma once
+
+#include "gdn_device.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+// Accumulator row held by this thread's TMEM lane for an M-row MMA, or -1.
+// M = 128: warp w (mod 4) owns rows 32w..32w+31 (row = lane).  M = 64: rows
+// 16w..16w+15 sit in lanes 32w..32w+15 (checked by tests/test_umma_layout.py).
+__device__ __forceinline__ int acc_row(int M) {
+  const int w = (threadIdx.x >> 5) & 3, l = threadIdx.x & 31;
+  if (M == 128) return 32 * w + l;
+  return l < 16 ? 16 * w + l : -1;
+}
+__device__ __forceinline__ uint32_t lane_quarter() {
+  return (uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16;
+}
+
+// Walks the accumulator columns [0, N) in 16-column pieces; the two warps that
+// share a lane quarter (w and w + 4 of an 8-warp CTA) take alternate pieces.
+// f(row, col0, v[16]) runs for rows < valid.  Whole warps must call this.
+template <class F>
+__device__ __forceinline__ void acc_walk(uint32_t tmem, int M, int N, int valid, F f) {
+  const int half = (int)(threadIdx.x >> 7);  // 0 for warps 0-3, 1 for warps 4-7
+  const int row = acc_row(M);
+  for (int c = half * 16; c < N; c += 32) {
+    float v[16];
+    tc::tmem_ld16(tmem + lane_quarter() + (uint32_t)c, v);
+    tc::tmem_ld_wait();
+    if (row >= 0 && row < valid) f(row, c, v);
+  }
+}
+
+// Stages a bf16 K-major SW128 tile of rows x cols (cols a multiple of 8) from
+// f(r, c) -> float, 8 elements (one 16-byte store) per step.
+template <class F>
+__device__ __forceinline__ void stage_tile(uint8_t* tile, int rows, int cols, F f) {
+  const int cpr = cols >> 3;
+  for (int idx = threadIdx.x; idx < rows * cpr; idx += blockDim.x) {
+    const int r = idx / cpr, c8 = (idx - (idx / cpr) * cpr) << 3;
+    __align__(16) __nv_bfloat162 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __floats2bfloat162_rn(f(r, c8 + 2 * u), f(r, c8 + 2 * u + 1));
+    *(uint4*)(tile + tc::sw128_offset(r, c8, rows)) = *(const uint4*)v;
+  }
+}
+
+// Stores one bf16 element of a K-major SW128 tile.
+__device__ __forceinline__ void tile_put(uint8_t* tile, int rows, int r, int c, float x) {
+  *(__nv_bfloat16*)(tile + tc::sw128_offset(r, c, rows)) = __float2bfloat16_rn(x);
+}
+
+// Copies `bytes` (multiple of 16) between 16-byte-aligned buffers with the whole CTA.
+__device__ __forceinline__ void cta_copy16(void* dst, const void* src, uint32_t bytes) {
+  uint4* d = (uint4*)dst;
+  const uint4* s = (const uint4*)src;
+  for (uint32_t i = threadIdx.x; i < bytes / 16; i += blockDim.x) d[i] = s[i];
+}
+
+// Thread 0 issues MMAs through `issue()`, commits them onto `bar`, and every
+// thread waits.  Returns false on every thread if any thread's bounded wait ran
+// out (the status word then holds GDN_ERR_TIMEOUT).  Writers of the operand
+// tiles must have called tc::fence_async_smem() before this.
+template <class F>
+__device__ __forceinline__ bool mma_run(F issue, uint64_t* bar, uint32_t& phase,
+                                        DeviceStatus* status, int detail) {
+  tc::fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tc::fence_after_sync();
+    issue();
+    tc::mma_commit(bar);
+  }
+  const bool ok = tc::mbar_wait(bar, phase);
+  phase ^= 1u;
+  tc::fence_after_sync();
+  const int bad = __syncthreads_or(ok ? 0 : 1);
+  if (bad && threadIdx.x == 0) set_status(status, GDN_ERR_TIMEOUT, detail);
+  return bad == 0;
+}
+
+}  // namespace gdn

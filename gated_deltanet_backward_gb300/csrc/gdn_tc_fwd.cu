@@ -1,0 +1,541 @@
+// gdn_tc_fwd.cu -- tensor-core (tcgen05) forward for bf16 inputs.
+//
+// k_prep_tc       one CTA per (chunk, key head).  Normalises q, k (L2 with the
+//                 1e-6 eps inside the square root), forms [K;Q] K^T on the tensor
+//                 core (K K^T and Q K^T in one M = 128 MMA), then for each value
+//                 head of the group the gates, T = (I + A)^-1 (blocked forward
+//                 substitution in fp32), W^T = K^T diag(b e^G) T^T and
+//                 U^T = V^T diag(b) T^T on the tensor core, and P = E * (Q K^T).
+//                 Writes bf16 operand tiles (K-major, 128B-swizzled) that the
+//                 state walk copies straight into shared memory.
+// k_fwd_state_tc  one CTA per (sequence, value head).  Walks the chunks in order
+//                 with the state S^T held in registers (fp32) and as a bf16
+//                 operand tile; per chunk: X^T = S^T W^T and S^T Q^T (tcgen05),
+//                 Delta^T = U^T - X^T, then O^T = diag... P Delta and the state
+//                 update S^T <- e^{G_last} S^T + Delta^T diag(c) K (tcgen05).  The
+//                 next chunk's tiles are prefetched with the bulk-copy engine
+//                 while the current chunk computes.
+// Notation as in gdn_internal.cuh; every product is D = A B^T with A, B K-major.
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int C = kChunk;
+constexpr int RB = 3;  // value heads prepared together (triangular solves in parallel)
+
+__device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
+__device__ __forceinline__ size_t tileDC(int D) { return (size_t)D * 128; }
+
+// In-place inverse of (I + A) for nh strictly-lower 64x64 fp32 matrices A
+// (Tm[hh] holds A on entry, T = (I + A)^-1 on exit).  Diagonal 16x16 blocks by
+// forward substitution, then block rows 1..3: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
+__device__ void tri_inverse(float* Tm, int nh, float* Mt) {
+  const int tid = threadIdx.x;
+  // diagonal blocks
+  {
+    const int hh = tid / 64, blk = (tid / 16) & 3, j = tid & 15;
+    float* T = Tm + hh * C * C;
+    for (int rr = 0; rr < 16; ++rr) {
+      float val = 0.f;
+      if (hh < nh) {
+        const int R = blk * 16 + rr, J = blk * 16 + j;
+        if (j == rr) {
+          val = 1.f;
+        } else if (j < rr) {
+          float acc = 0.f;
+          for (int s = j; s < rr; ++s) acc = fmaf(T[R * C + blk * 16 + s], T[(blk * 16 + s) * C + J], acc);
+          val = -acc;
+        }
+      }
+      __syncthreads();
+      if (hh < nh) T[(blk * 16 + rr) * C + blk * 16 + j] = val;
+      __syncthreads();
+    }
+  }
+  // block rows
+  for (int bi = 1; bi < 4; ++bi) {
+    const int n_el = nh * bi * 256;
+    for (int idx = tid; idx < n_el; idx += blockDim.x) {
+      const int hh = idx / (bi * 256), rem = idx % (bi * 256), bj = rem / 256, e = rem % 256;
+      const int rr = e / 16, cc = e % 16;
+      const float* T = Tm + hh * C * C;
+      float acc = 0.f;
+      for (int kb = bj; kb < bi; ++kb)
+        for (int s = 0; s < 16; ++s)
+          acc = fmaf(T[(bi * 16 + rr) * C + kb * 16 + s], T[(kb * 16 + s) * C + bj * 16 + cc], acc);
+      Mt[(hh * 3 + bj) * 256 + e] = acc;
+    }
+    __syncthreads();
+    // T_ij = -T_ii M_ij, written over A_ij (no longer read: block row bi's M are done)
+    for (int idx = tid; idx < n_el; idx += blockDim.x) {
+      const int hh = idx / (bi * 256), rem = idx % (bi * 256), bj = rem / 256, e = rem % 256;
+      const int rr = e / 16, cc = e % 16;
+      float* T = Tm + hh * C * C;
+      float acc = 0.f;
+      for (int s = 0; s <= rr; ++s)
+        acc = fmaf(T[(bi * 16 + rr) * C + bi * 16 + s], Mt[(hh * 3 + bj) * 256 + s * 16 + cc], acc);
+      T[(bi * 16 + rr) * C + bj * 16 + cc] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int c = blockIdx.x, kh = blockIdx.y;
+  int n;
+  int64_t t0;
+  int len;
+  if (!chunk_info(p, c, &n, &t0, &len)) {
+    if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
+    return;
+  }
+  const int Dk = p.Dk, Dv = p.Dv;
+  const int MK = Dk < 64 ? 64 : Dk, MV = Dv < 64 ? 64 : Dv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t aqk_pitch = 128u * 128u;
+  uint8_t* tAQK = sm;                                   // [128][Dk]: rows 0-63 K, 64-127 Q
+  uint8_t* tKt = tAQK + tc::sw128_bytes(128, Dk);       // [MK][C]  K^T
+  uint8_t* tVt = tKt + MK * 128;                        // [MV][C]  V^T of one head
+  uint8_t* tTW = tVt + MV * 128;                        // [C][C]   T diag(b e^G)
+  uint8_t* tTB = tTW + 8192;                            // [C][C]   T diag(b)
+  uint8_t* tOW = tTB + 8192;                            // [C][Dk]  W (staging)
+  uint8_t* tOWt = tOW + tc::sw128_bytes(64, Dk);        // [Dk][C]  W^T (staging)
+  uint8_t* tOP = tOWt + Dk * 128;                       // [C][C]   P (staging)
+  float* KK = (float*)(tOP + 8192);                     // [C][C]
+  float* QK = KK + C * C;                               // [C][C]
+  float* Tm = QK + C * C;                               // [RB][C][C]
+  float* Mt = Tm + RB * C * C;                          // [RB][3][256]
+  float* gv = Mt + RB * 3 * 256;                        // [RB][C]
+  float* bv = gv + RB * C;                              // [RB][C]
+  float* wv = bv + RB * C;                              // [RB][C]
+  uint64_t* bar = (uint64_t*)(wv + RB * C);
+  uint32_t* tslot = (uint32_t*)(bar + 1);
+
+  // zero the transposed tiles (rows past Dk / Dv pad the M = 64 products)
+  for (int i = tid; i < MK * 128 / 16; i += kThreads) ((uint4*)tKt)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < MV * 128 / 16; i += kThreads) ((uint4*)tVt)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 256);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  uint32_t phase = 0;
+  bool ok = true;
+
+  // 1. L2-normalise q and k rows into the operand tiles.
+  const size_t ck = ((size_t)c * p.Hk + kh) * C;
+  for (int row = warp; row < 2 * C; row += kThreads / 32) {
+    const bool isq = row >= C;
+    const int t = row & (C - 1);
+    const __nv_bfloat16* src = (const __nv_bfloat16*)(isq ? p.q : p.k) +
+                               (t0 + t) * (isq ? p.q_ld : p.k_ld) + (int64_t)kh * Dk;
+    float x[4];
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = lane + 32 * u;
+      x[u] = (t < len && i < Dk) ? __bfloat162float(src[i]) : 0.f;
+      ss = fmaf(x[u], x[u], ss);
+    }
+    ss = warp_sum(ss);
+    const float nrm = sqrtf(ss + 1e-6f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = lane + 32 * u;
+      if (i < Dk) {
+        const float xh = x[u] / nrm;
+        tile_put(tAQK, 128, row, i, xh);
+        if (!isq) tile_put(tKt, MK, i, t, xh);
+        if (bwd) (isq ? p.Qn : p.Kn)[(ck + t) * Dk + i] = xh;
+      }
+    }
+    if (bwd && lane == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
+  }
+  tc::fence_async_smem();
+  // 2. [K; Q] K^T -> TMEM columns [0, 64): lanes 0-63 K K^T, lanes 64-127 Q K^T.
+  ok = mma_run([&] { tc::mma_tile_p(tmem, tc::smem_u32(tAQK), aqk_pitch, 128, tc::smem_u32(tAQK),
+                                     aqk_pitch, 64, Dk, 0u); },
+               bar, phase, p.status, c);
+  if (!ok) goto done;
+  acc_walk(tmem, 128, 64, 128, [&](int row, int col0, const float* v) {
+    float* dst = row < C ? KK + row * C : QK + (row - C) * C;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) dst[col0 + j] = v[j];
+    if (bwd) {
+      float* g = (row < C ? p.KKf + (ck + row) * C : p.QKf + (ck + row - C) * C) + col0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) g[j] = v[j];
+    }
+  });
+  // operand tiles of this key head to the workspace
+  {
+    const size_t tcd = tileCD(Dk);
+    uint8_t* gq = p.Qsw + ((size_t)c * p.Hk + kh) * tcd;
+    uint8_t* gk = p.Ksw + ((size_t)c * p.Hk + kh) * tcd;
+    for (int b = 0; b * 64 < Dk; ++b) {
+      cta_copy16(gk + b * 8192, tAQK + b * aqk_pitch, 8192);
+      cta_copy16(gq + b * 8192, tAQK + b * aqk_pitch + 8192, 8192);
+    }
+    cta_copy16(p.Ktsw + ((size_t)c * p.Hk + kh) * tileDC(Dk), tKt, Dk * 128);
+  }
+  __syncthreads();
+
+  for (int g0 = 0; g0 < p.r; g0 += RB) {
+    const int nh = (p.r - g0) < RB ? (p.r - g0) : RB;
+    // 3. gates of the nh value heads
+    if (tid < nh * C) {
+      const int hh = tid / C, t = tid % C, h = kh * p.r + g0 + hh;
+      float l = 0.f, b = 0.f;
+      if (t < len) {
+        b = sigmoid_f(p.beta_raw[(t0 + t) * p.beta_ld + h]);
+        const float x = p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
+        l = -expf(p.a_log[h]) * softplus_f(x);
+      }
+      gv[hh * C + t] = l;
+      bv[hh * C + t] = b;
+    }
+    __syncthreads();
+    if (warp < nh && lane < 32) {
+      // inclusive cumsum of 64 values, two per lane
+      float* x = gv + warp * C;
+      const float a = x[2 * lane], b2 = a + x[2 * lane + 1];
+      float run = b2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, run, o);
+        if (lane >= o) run += y;
+      }
+      x[2 * lane] = run - b2 + a;
+      x[2 * lane + 1] = run;
+    }
+    __syncthreads();
+    if (tid < nh * C) {
+      const int hh = tid / C, t = tid % C, h = kh * p.r + g0 + hh;
+      const size_t ch = (size_t)c * p.Hv + h;
+      wv[hh * C + t] = bv[hh * C + t] * expf(gv[hh * C + t]);
+      p.G[ch * C + t] = gv[hh * C + t];
+      p.b[ch * C + t] = bv[hh * C + t];
+    }
+    for (int idx = tid; idx < nh * C * C; idx += kThreads) {
+      const int hh = idx / (C * C), e = idx % (C * C), r = e / C, s = e % C;
+      Tm[idx] = s < r ? bv[hh * C + r] * expf(gv[hh * C + r] - gv[hh * C + s]) * KK[e] : 0.f;
+    }
+    __syncthreads();
+    // 4. T = (I + A)^-1 for the nh heads at once
+    tri_inverse(Tm, nh, Mt);
+    // 5. per head: W^T = K^T (T diag(w))^T, U^T = V^T (T diag(b))^T, P
+    for (int hh = 0; hh < nh; ++hh) {
+      const int h = kh * p.r + g0 + hh;
+      const size_t ch = (size_t)c * p.Hv + h;
+      const float* T = Tm + hh * C * C;
+      const float* w = wv + hh * C;
+      const float* bb = bv + hh * C;
+      const float* G = gv + hh * C;
+      stage_tile(tTW, C, C, [&](int r, int s) { return T[r * C + s] * w[s]; });
+      stage_tile(tTB, C, C, [&](int r, int s) { return T[r * C + s] * bb[s]; });
+      stage_tile(tOP, C, C, [&](int r, int s) {
+        return s <= r ? expf(G[r] - G[s]) * QK[r * C + s] : 0.f;
+      });
+      const __nv_bfloat16* Vs = (const __nv_bfloat16*)p.v + t0 * p.v_ld + (int64_t)h * Dv;
+      stage_tile(tVt, Dv, C, [&](int vv, int s) {
+        return s < len ? __bfloat162float(Vs[(int64_t)s * p.v_ld + vv]) : 0.f;
+      });
+      tc::fence_async_smem();
+      ok = mma_run([&] {
+        tc::mma_tile(tmem + 64, tc::smem_u32(tKt), MK, tc::smem_u32(tTW), C, C, 0u);
+        tc::mma_tile(tmem + 128, tc::smem_u32(tVt), MV, tc::smem_u32(tTB), C, C, 0u);
+      }, bar, phase, p.status, c);
+      if (!ok) goto done;
+      acc_walk(tmem + 64, MK, 64, Dk, [&](int k, int col0, const float* v) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          tile_put(tOW, C, col0 + j, k, v[j]);
+          if (bwd) {
+            tile_put(tOWt, Dk, k, col0 + j, v[j]);
+            p.W[(ch * C + col0 + j) * Dk + k] = v[j];
+          }
+        }
+      });
+      acc_walk(tmem + 128, MV, 64, Dv, [&](int vv, int col0, const float* v) {
+        __align__(16) __nv_bfloat162 pk[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pk[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+        uint4* dst = (uint4*)(p.Utb + (ch * Dv + vv) * C + col0);
+        dst[0] = ((const uint4*)pk)[0];
+        dst[1] = ((const uint4*)pk)[1];
+        if (bwd)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) p.U[(ch * C + col0 + j) * Dv + vv] = v[j];
+      });
+      if (bwd)
+        for (int i = tid; i < C * C; i += kThreads) p.Tm[ch * C * C + i] = T[i];
+      __syncthreads();
+      cta_copy16(p.Wsw + ch * tileCD(Dk), tOW, (uint32_t)tileCD(Dk));
+      cta_copy16(p.Psw + ch * tileCD(64), tOP, 8192);
+      if (bwd) cta_copy16(p.Wtsw + ch * tileDC(Dk), tOWt, Dk * 128);
+      __syncthreads();
+    }
+  }
+done:
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int n = blockIdx.x, h = blockIdx.y, kh = h / p.r;
+  int64_t s0, s1;
+  int c0, c1;
+  if (!seq_info(p, n, &s0, &s1, &c0, &c1)) {
+    if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, n);
+    return;
+  }
+  constexpr int NKC = (DK + 31) / 32;          // 16-column pieces of S^T per thread
+  const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
+  const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
+  const uint32_t bW = (uint32_t)tileCD(DK), bKt = (uint32_t)tileDC(DK), bP = 8192;
+  const uint32_t bU = (uint32_t)Dv * C * 2, bG = C * 4;
+  uint8_t* tSt = sm;                                  // [MV][DK]
+  uint8_t* buf0 = tSt + tc::sw128_bytes(MV, DK);
+  const uint32_t bufsz = bW * 2 + bKt + bP + ((bU + bG + 1023) & ~1023u);
+  uint8_t* tDt = buf0 + 2 * bufsz;                    // [MV][C] Delta^T
+  uint8_t* tDct = tDt + MV * 128;                     // [MV][C] Delta^T diag(c)
+  float* ev = (float*)(tDct + MV * 128);              // [C]
+  float* cv = ev + C;                                 // [C]
+  uint64_t* bars = (uint64_t*)(cv + C);               // mma, load0, load1
+  uint32_t* tslot = (uint32_t*)(bars + 3);
+  auto tW = [&](int b) { return buf0 + b * bufsz; };
+  auto tQ = [&](int b) { return buf0 + b * bufsz + bW; };
+  auto tKt = [&](int b) { return buf0 + b * bufsz + 2 * bW; };
+  auto tP = [&](int b) { return buf0 + b * bufsz + 2 * bW + bKt; };
+  auto sU = [&](int b) { return (const __nv_bfloat16*)(buf0 + b * bufsz + 2 * bW + bKt + bP); };
+  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + 2 * bW + bKt + bP + bU); };
+
+  for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) / 16); i += kThreads)
+    ((uint4*)tSt)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < MV * 128 * 2 / 16; i += kThreads) ((uint4*)tDt)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::mbar_init(&bars[2], 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 256);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tX = tmem, tO1 = tmem + 64, tS = tmem + 128;
+  uint32_t mphase = 0, lphase0 = 0, lphase1 = 0;
+  const int vrow = acc_row(MV);
+  const bool vok = vrow >= 0 && vrow < Dv;
+  const size_t SZ = (size_t)DK * Dv;
+
+  // state S^T (row v = this thread's lane, columns k of its 16-column pieces)
+  float S[NKC][16];
+#pragma unroll
+  for (int i = 0; i < NKC; ++i)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int k = half * 16 + 32 * i + j;
+      S[i][j] = (vok && k < DK && p.S0) ? p.S0[((size_t)n * p.Hv + h) * SZ + (size_t)k * Dv + vrow] : 0.f;
+    }
+#pragma unroll
+  for (int i = 0; i < NKC; ++i)
+    if (half * 16 + 32 * i < DK && vok)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tile_put(tSt, MV, vrow, half * 16 + 32 * i + j, S[i][j]);
+
+  auto issue_load = [&](int cc, int b) {
+    uint64_t* lb = &bars[1 + b];
+    const size_t chh = (size_t)cc * p.Hv + h, ckk = (size_t)cc * p.Hk + kh;
+    tc::mbar_arrive_expect_tx(lb, 2 * bW + bKt + bP + bU + bG);
+    tc::bulk_g2s(tW(b), p.Wsw + chh * bW, bW, lb);
+    tc::bulk_g2s(tQ(b), p.Qsw + ckk * bW, bW, lb);
+    tc::bulk_g2s(tKt(b), p.Ktsw + ckk * bKt, bKt, lb);
+    tc::bulk_g2s(tP(b), p.Psw + chh * bP, bP, lb);
+    tc::bulk_g2s((void*)sU(b), p.Utb + chh * Dv * C, bU, lb);
+    tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
+  };
+  if (tid == 0 && c1 > c0) issue_load(c0, 0);
+
+  bool ok = true;
+  for (int c = c0; c < c1 && ok; ++c) {
+    const int i = c - c0, b = i & 1;
+    const int64_t t0 = s0 + (int64_t)i * C;
+    const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
+    // chunk-start state
+    float* sv = p.saved + ((size_t)c * p.Hv + h) * SZ;
+    if (vok)
+#pragma unroll
+      for (int ii = 0; ii < NKC; ++ii)
+        if (half * 16 + 32 * ii < DK)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sv[(size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = S[ii][j];
+    // tiles of this chunk
+    const bool lok = tc::mbar_wait(&bars[1 + b], b ? lphase1 : lphase0);
+    if (b) lphase1 ^= 1u; else lphase0 ^= 1u;
+    if (__syncthreads_or(lok ? 0 : 1)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+      ok = false;
+      break;
+    }
+    if (tid == 0 && c + 1 < c1) {
+      tc::fence_async_smem();
+      issue_load(c + 1, b ^ 1);
+    }
+    const float* G = sG(b);
+    if (tid < C) {
+      ev[tid] = expf(G[tid]);
+      cv[tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
+    }
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tX, tc::smem_u32(tSt), MV, tc::smem_u32(tW(b)), C, DK, 0u);
+      tc::mma_tile(tO1, tc::smem_u32(tSt), MV, tc::smem_u32(tQ(b)), C, DK, 0u);
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    // Delta^T = U^T - X^T; keep S^T Q^T for the output
+    float o1[2][16];
+    const __nv_bfloat16* U = sU(b);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int col0 = half * 16 + 32 * q;
+      float x[16];
+      tc::tmem_ld16(tX + lane_quarter() + col0, x);
+      tc::tmem_ld16(tO1 + lane_quarter() + col0, o1[q]);
+      tc::tmem_ld_wait();
+      if (vok) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float d = __bfloat162float(U[vrow * C + col0 + j]) - x[j];
+          tile_put(tDt, MV, vrow, col0 + j, d);
+          tile_put(tDct, MV, vrow, col0 + j, d * cv[col0 + j]);
+        }
+      }
+    }
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tX, tc::smem_u32(tDt), MV, tc::smem_u32(tP(b)), C, C, 0u);
+      tc::mma_tile(tS, tc::smem_u32(tDct), MV, tc::smem_u32(tKt(b)), DK, C, 0u);
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    // O = scale (e^G Q S + P Delta): column r of O^T is token t0 + r
+    __nv_bfloat16* orow = (__nv_bfloat16*)p.o + t0 * p.o_ld + (int64_t)h * Dv;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int col0 = half * 16 + 32 * q;
+      float x[16];
+      tc::tmem_ld16(tX + lane_quarter() + col0, x);
+      tc::tmem_ld_wait();
+      if (vok)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = col0 + j;
+          if (r < len)
+            orow[(int64_t)r * p.o_ld + vrow] = __float2bfloat16_rn(p.scale * (ev[r] * o1[q][j] + x[j]));
+        }
+    }
+    // S^T <- e^{G_last} S^T + Delta^T diag(c) K
+    const float eC = expf(G[len - 1]);
+#pragma unroll
+    for (int ii = 0; ii < NKC; ++ii) {
+      const int col0 = half * 16 + 32 * ii;
+      if (col0 < DK) {
+        float x[16];
+        tc::tmem_ld16(tS + lane_quarter() + col0, x);
+        tc::tmem_ld_wait();
+        if (vok)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            S[ii][j] = fmaf(eC, S[ii][j], x[j]);
+            tile_put(tSt, MV, vrow, col0 + j, S[ii][j]);
+          }
+      }
+    }
+    tc::fence_async_smem();
+  }
+  if (ok && p.S_T && vok)
+#pragma unroll
+    for (int ii = 0; ii < NKC; ++ii)
+      if (half * 16 + 32 * ii < DK)
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          p.S_T[((size_t)n * p.Hv + h) * SZ + (size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = S[ii][j];
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+static size_t prep_tc_smem(const Params& p) {
+  const int Dk = p.Dk, Dv = p.Dv, MK = Dk < 64 ? 64 : Dk, MV = Dv < 64 ? 64 : Dv;
+  size_t b = tc::sw128_bytes(128, Dk) + (size_t)MK * 128 + (size_t)MV * 128 + 8192 * 2 +
+             tc::sw128_bytes(64, Dk) + (size_t)Dk * 128 + 8192;
+  b += sizeof(float) * ((size_t)2 * C * C + (size_t)RB * C * C + RB * 3 * 256 + 3 * RB * C);
+  return b + 64 + 1024;
+}
+
+template <int DK>
+static size_t fwd_state_tc_smem(const Params& p) {
+  const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
+  const size_t bW = tc::sw128_bytes(64, DK), bKt = (size_t)DK * 128, bP = 8192;
+  const size_t bU = (size_t)Dv * C * 2, bG = C * 4;
+  const size_t bufsz = bW * 2 + bKt + bP + ((bU + bG + 1023) & ~(size_t)1023);
+  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 2 * C * 4 + 64 + 1024;
+}
+
+cudaError_t launch_prep_tc(const Params& p, bool bwd, cudaStream_t st) {
+  if (p.NC == 0) return cudaSuccess;
+  const size_t smem = prep_tc_smem(p);
+  cudaFuncSetAttribute(k_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  profile_pre(st, KID_PREP_TC);
+  k_prep_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, bwd ? 1 : 0);
+  profile_post(st);
+  return cudaGetLastError();
+}
+
+template <int DK>
+static cudaError_t launch_fwd_state_tc_t(const Params& p, cudaStream_t st) {
+  const size_t smem = fwd_state_tc_smem<DK>(p);
+  cudaFuncSetAttribute(k_fwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  profile_pre(st, KID_FWD_STATE_TC);
+  k_fwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kThreads, smem, st>>>(p);
+  profile_post(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st) {
+  if (p.n_seqs == 0) return cudaSuccess;
+  switch (p.Dk) {
+    case 16: return launch_fwd_state_tc_t<16>(p, st);
+    case 32: return launch_fwd_state_tc_t<32>(p, st);
+    case 64: return launch_fwd_state_tc_t<64>(p, st);
+    default: return launch_fwd_state_tc_t<128>(p, st);
+  }
+}
+
+}  // namespace gdn

@@ -173,15 +173,41 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int k, int ro
 }
 
 // Issues D (+)= A[M x K] * B[N x K]^T over K (multiple of 16) from K-major SW128
-// tiles at shared addresses a_base (M rows) and b_base (N rows).
-__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_base, int M, uint32_t b_base,
-                                         int N, int K, uint32_t accumulate_first) {
+// tiles at shared addresses a_base (M rows) and b_base (N rows).  a_pitch /
+// b_pitch are the byte distances between consecutive 64-column blocks of each
+// tile (rows * 128 for a tile stored on its own).
+__device__ __forceinline__ void mma_tile_p(uint32_t d_tmem, uint32_t a_base, uint32_t a_pitch,
+                                           int M, uint32_t b_base, uint32_t b_pitch, int N,
+                                           int K, uint32_t accumulate_first) {
   const uint32_t idesc = idesc_bf16(M, N);
   for (int kk = 0; kk < K; kk += 16) {
-    const uint32_t a = a_base + (uint32_t)(kk >> 6) * (uint32_t)M * 128u + (uint32_t)(kk & 63) * 2u;
-    const uint32_t b = b_base + (uint32_t)(kk >> 6) * (uint32_t)N * 128u + (uint32_t)(kk & 63) * 2u;
+    const uint32_t a = a_base + (uint32_t)(kk >> 6) * a_pitch + (uint32_t)(kk & 63) * 2u;
+    const uint32_t b = b_base + (uint32_t)(kk >> 6) * b_pitch + (uint32_t)(kk & 63) * 2u;
     mma_bf16(d_tmem, desc_sw128(a), desc_sw128(b), idesc, (kk > 0) ? 1u : accumulate_first);
   }
+}
+__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_base, int M, uint32_t b_base,
+                                         int N, int K, uint32_t accumulate_first) {
+  mma_tile_p(d_tmem, a_base, (uint32_t)M * 128u, M, b_base, (uint32_t)N * 128u, N, K,
+             accumulate_first);
+}
+
+// Bytes of a K-major SW128 bf16 tile of `rows` rows and `cols` columns.
+__host__ __device__ __forceinline__ uint32_t sw128_bytes(int rows, int cols) {
+  return (uint32_t)((cols + 63) / 64) * (uint32_t)rows * 128u;
+}
+
+// ------------------------------------------------------------ bulk copies
+// One thread: copies `bytes` (multiple of 16; both addresses 16-byte aligned)
+// from global memory into shared memory with the bulk-copy engine; completion
+// is signalled on `bar` through its transaction count.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 }  // namespace tc
