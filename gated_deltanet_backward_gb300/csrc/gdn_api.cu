@@ -121,6 +121,8 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
     p.Utb = (__nv_bfloat16*)(base + L.Utb);
     if (bwd) {
       p.Wtsw = (uint8_t*)(base + L.Wtsw);
+      p.Qtsw = (uint8_t*)(base + L.Qtsw);
+      p.Ptsw = (uint8_t*)(base + L.Ptsw);
       p.QKf = (float*)(base + L.QKf);
       p.KKf = (float*)(base + L.KKf);
     }
@@ -227,6 +229,8 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_BWD_GATES: return "gdn_bwd_gates";
     case gdn::KID_PREP_TC: return "gdn_prep_tc";
     case gdn::KID_FWD_STATE_TC: return "gdn_fwd_state_tc";
+    case gdn::KID_BWD_STATE_TC: return "gdn_bwd_state_tc";
+    case gdn::KID_BWD_GRADS_TC: return "gdn_bwd_grads_tc";
     default: return "?";
   }
 }

@@ -447,9 +447,15 @@ cudaError_t launch_backward(const Params& p, bool bf16, cudaStream_t st) {
     profile_post(st);
     return cudaGetLastError();
   }
-  cudaError_t e = bf16 ? launch_prep_tc(p, true, st) : launch_prep(p, bf16, true, st);
+  if (bf16) {
+    // bf16 inputs: tensor-core preparation, reverse state walk and gradients
+    cudaError_t e = launch_prep_tc(p, true, st);
+    if (e != cudaSuccess) return e;
+    return launch_bwd_tc(p, st);
+  }
+  cudaError_t e = launch_prep(p, bf16, true, st);
   if (e != cudaSuccess) return e;
-  return bf16 ? launch_backward_t<__nv_bfloat16>(p, st) : launch_backward_t<float>(p, st);
+  return launch_backward_t<float>(p, st);
 }
 
 }  // namespace gdn

@@ -59,6 +59,8 @@ struct WsLayout {
   size_t Wtsw;    // [NC][Hv] tile [Dk rows][C]   W^T (backward)
   size_t Psw;     // [NC][Hv] tile [C rows][C]    P = E * (Q K^T), lower incl. diagonal
   size_t Utb;     // [NC][Hv][Dv][C] bf16         U^T
+  size_t Qtsw;    // [NC][Hk] tile [Dk rows][C]   normalised queries, transposed (backward)
+  size_t Ptsw;    // [NC][Hv] tile [C rows][C]    P^T (backward)
   size_t QKf;     // [NC][Hk][C][C] fp32          Q K^T (backward)
   size_t KKf;     // [NC][Hk][C][C] fp32          K K^T (backward)
   size_t total;
@@ -107,6 +109,8 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
     L.Utb = take(NC * Hv * Dv * C * 2);
     if (bwd) {
       L.Wtsw = take(NC * Hv * tile_DxC(s.Dk));
+      L.Qtsw = take(NC * Hk * tile_DxC(s.Dk));
+      L.Ptsw = take(NC * Hv * tile_CxD(64));
       L.QKf = take(NC * Hk * C * C * 4);
       L.KKf = take(NC * Hk * C * C * 4);
     }
@@ -171,7 +175,9 @@ struct Params {
   uint8_t* Ktsw;
   uint8_t* Wsw;
   uint8_t* Wtsw;
+  uint8_t* Qtsw;
   uint8_t* Psw;
+  uint8_t* Ptsw;
   __nv_bfloat16* Utb;
   float* QKf;
   float* KKf;
@@ -187,7 +193,9 @@ enum KernelId {
   KID_BWD_GATES = 5,
   KID_PREP_TC = 6,
   KID_FWD_STATE_TC = 7,
-  KID_COUNT = 8
+  KID_BWD_STATE_TC = 8,
+  KID_BWD_GRADS_TC = 9,
+  KID_COUNT = 10
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
@@ -198,6 +206,7 @@ void profile_post(cudaStream_t st);
 // Tensor-core (bf16) launchers.
 cudaError_t launch_prep_tc(const Params& p, bool bwd, cudaStream_t st);
 cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st);
+cudaError_t launch_bwd_tc(const Params& p, cudaStream_t st);
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t st);

@@ -54,6 +54,77 @@ __device__ __forceinline__ void stage_tile(uint8_t* tile, int rows, int cols, F 
   }
 }
 
+// Stages an fp32 row-major source M (R rows x Cc columns, row stride ld floats,
+// 16-byte aligned rows, Cc a multiple of 8) into a natural tile tn (R rows, Cc
+// columns) and / or a transposed tile tt (Cc rows, R columns; tt_rows = its row
+// count), each element multiplied by rs(r).  Rows r >= valid read as zero.
+template <class RS>
+__device__ __forceinline__ void stage_f32(const float* M, int R, int Cc, int64_t ld, int valid,
+                                          uint8_t* tn, uint8_t* tt, int tt_rows, RS rs) {
+  const int cpr = Cc >> 3;
+  for (int idx = threadIdx.x; idx < R * cpr; idx += blockDim.x) {
+    const int r = idx / cpr, c0 = (idx - (idx / cpr) * cpr) << 3;
+    float v[8];
+    if (r < valid) {
+      const float4 a = *(const float4*)(M + (int64_t)r * ld + c0);
+      const float4 b = *(const float4*)(M + (int64_t)r * ld + c0 + 4);
+      const float s = rs(r);
+      v[0] = a.x * s; v[1] = a.y * s; v[2] = a.z * s; v[3] = a.w * s;
+      v[4] = b.x * s; v[5] = b.y * s; v[6] = b.z * s; v[7] = b.w * s;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = 0.f;
+    }
+    if (tn) {
+      __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pk[u] = __floats2bfloat162_rn(v[2 * u], v[2 * u + 1]);
+      *(uint4*)(tn + tc::sw128_offset(r, c0, R)) = *(const uint4*)pk;
+    }
+    if (tt)
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + u, r, tt_rows)) = __float2bfloat16_rn(v[u]);
+  }
+}
+
+// As stage_f32 for a bf16 row-major source (row stride ld elements, 16-byte
+// aligned rows).  Two natural outputs may be produced: tn (unscaled) and tn2
+// (scaled by rs(r)); tt (transposed, unscaled).
+template <class RS>
+__device__ __forceinline__ void stage_bf16(const __nv_bfloat16* M, int R, int Cc, int64_t ld,
+                                           int valid, uint8_t* tn, int tn_rows, uint8_t* tn2,
+                                           uint8_t* tt, int tt_rows, RS rs) {
+  const int cpr = Cc >> 3;
+  for (int idx = threadIdx.x; idx < R * cpr; idx += blockDim.x) {
+    const int r = idx / cpr, c0 = (idx - (idx / cpr) * cpr) << 3;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (r < valid) raw = *(const uint4*)(M + (int64_t)r * ld + c0);
+    if (tn) *(uint4*)(tn + tc::sw128_offset(r, c0, tn_rows)) = raw;
+    if (tn2 || tt) {
+      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
+      const float s = tn2 ? rs(r) : 1.f;
+      if (tn2) {
+        __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          pk[u] = __floats2bfloat162_rn(__bfloat162float(e[2 * u]) * s,
+                                        __bfloat162float(e[2 * u + 1]) * s);
+        *(uint4*)(tn2 + tc::sw128_offset(r, c0, R)) = *(const uint4*)pk;
+      }
+      if (tt)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + u, r, tt_rows)) = e[u];
+    }
+  }
+}
+
+// Reads one bf16 element of a K-major SW128 tile as float.
+__device__ __forceinline__ float tile_get(const uint8_t* tile, int rows, int r, int c) {
+  return __bfloat162float(*(const __nv_bfloat16*)(tile + tc::sw128_offset(r, c, rows)));
+}
+
 // Stores one bf16 element of a K-major SW128 tile.
 __device__ __forceinline__ void tile_put(uint8_t* tile, int rows, int r, int c, float x) {
   *(__nv_bfloat16*)(tile + tc::sw128_offset(r, c, rows)) = __float2bfloat16_rn(x);

@@ -1,0 +1,750 @@
+// gdn_tc_bwd.cu -- tensor-core (tcgen05) backward for bf16 inputs.
+//
+// k_bwd_state_tc  one CTA per (sequence, value head): reverse walk over the chunks
+//                 with the state adjoint dS^T in registers (fp32) and as a bf16
+//                 operand tile.  Per chunk:
+//                   dDelta^T = scale (dO^T P) + diag-cols(c) (dS^T K^T)
+//                   dS^T    <- e^{G_last} dS^T + (scale e^G dO)^T Q - dDelta^T W
+//                 and it stores dS (chunk end) and dDelta for the gradient kernel.
+// k_bwd_grads_tc  one CTA per (chunk, key head), looping over the value heads of
+//                 the key head; dQ_hat and dK_hat of the key head accumulate in
+//                 TMEM across the heads (fixed order: bit-reproducible, no
+//                 atomics), then the L2-norm backward writes dq, dk.  Per head it
+//                 recomputes Delta = U - W S and forms every chunk-level
+//                 derivative of the WY form (see gdn_bwd.cu) with tcgen05 MMAs,
+//                 plus the gate / sigmoid epilogues.
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+namespace {
+constexpr int C = kChunk;
+__device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
+__device__ __forceinline__ size_t tileDC(int D) { return (size_t)D * 128; }
+}  // namespace
+
+// ---------------------------------------------------------------------------
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int n = blockIdx.x, h = blockIdx.y, kh = h / p.r;
+  int64_t s0, s1;
+  int c0, c1;
+  if (!seq_info(p, n, &s0, &s1, &c0, &c1)) {
+    if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, n);
+    return;
+  }
+  constexpr int NKC = (DK + 31) / 32;
+  const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
+  const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
+  const uint32_t bK = (uint32_t)tileCD(DK), bKt = (uint32_t)tileDC(DK), bP = 8192, bG = C * 4;
+  uint8_t* tdSt = sm;                                        // [MV][DK]
+  uint8_t* tdOt = tdSt + tc::sw128_bytes(MV, DK);            // [MV][C] dO^T
+  uint8_t* tdOet = tdOt + MV * 128;                          // [MV][C] (scale e^G dO)^T
+  uint8_t* tmDt = tdOet + MV * 128;                          // [MV][C] -dDelta^T
+  uint8_t* buf0 = tmDt + MV * 128;
+  const uint32_t bufsz = bK + bP + 2 * bKt + 1024;
+  float* ev = (float*)(buf0 + 2 * bufsz);
+  float* cv = ev + C;
+  uint64_t* bars = (uint64_t*)(cv + C);
+  uint32_t* tslot = (uint32_t*)(bars + 3);
+  auto tK = [&](int b) { return buf0 + b * bufsz; };
+  auto tPt = [&](int b) { return buf0 + b * bufsz + bK; };
+  auto tQt = [&](int b) { return buf0 + b * bufsz + bK + bP; };
+  auto tWt = [&](int b) { return buf0 + b * bufsz + bK + bP + bKt; };
+  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + bK + bP + 2 * bKt); };
+
+  for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) + 3 * MV * 128) / 16; i += kThreads)
+    ((uint4*)tdSt)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::mbar_init(&bars[2], 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 256);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tA1 = tmem, tA2 = tmem + 64, tA3 = tmem + 128;
+  uint32_t mphase = 0, lph[2] = {0, 0};
+  const int vrow = acc_row(MV);
+  const bool vok = vrow >= 0 && vrow < Dv;
+  const size_t SZ = (size_t)DK * Dv;
+
+  float dS[NKC][16];
+#pragma unroll
+  for (int i = 0; i < NKC; ++i)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int k = half * 16 + 32 * i + j;
+      dS[i][j] = (vok && k < DK && p.dS_T) ? p.dS_T[((size_t)n * p.Hv + h) * SZ + (size_t)k * Dv + vrow] : 0.f;
+    }
+#pragma unroll
+  for (int i = 0; i < NKC; ++i)
+    if (half * 16 + 32 * i < DK && vok)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tile_put(tdSt, MV, vrow, half * 16 + 32 * i + j, dS[i][j]);
+
+  auto issue_load = [&](int cc, int b) {
+    uint64_t* lb = &bars[1 + b];
+    const size_t chh = (size_t)cc * p.Hv + h, ckk = (size_t)cc * p.Hk + kh;
+    tc::mbar_arrive_expect_tx(lb, bK + bP + 2 * bKt + bG);
+    tc::bulk_g2s(tK(b), p.Ksw + ckk * bK, bK, lb);
+    tc::bulk_g2s(tPt(b), p.Ptsw + chh * bP, bP, lb);
+    tc::bulk_g2s(tQt(b), p.Qtsw + ckk * bKt, bKt, lb);
+    tc::bulk_g2s(tWt(b), p.Wtsw + chh * bKt, bKt, lb);
+    tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
+  };
+  if (tid == 0 && c1 > c0) issue_load(c1 - 1, 0);
+
+  bool ok = true;
+  for (int c = c1 - 1; c >= c0 && ok; --c) {
+    const int i = c1 - 1 - c, b = i & 1;
+    const int64_t t0 = s0 + (int64_t)(c - c0) * C;
+    const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
+    const size_t ch = (size_t)c * p.Hv + h;
+    // state adjoint at the end of this chunk, for the gradient kernel
+    float* dsv = p.dS + ch * SZ;
+    if (vok)
+#pragma unroll
+      for (int ii = 0; ii < NKC; ++ii)
+        if (half * 16 + 32 * ii < DK)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dsv[(size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = dS[ii][j];
+    const bool lok = tc::mbar_wait(&bars[1 + b], lph[b]);
+    lph[b] ^= 1u;
+    if (__syncthreads_or(lok ? 0 : 1)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+      ok = false;
+      break;
+    }
+    if (tid == 0 && c - 1 >= c0) {
+      tc::fence_async_smem();
+      issue_load(c - 1, b ^ 1);
+    }
+    const float* G = sG(b);
+    if (tid < C) {
+      ev[tid] = expf(G[tid]);
+      cv[tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
+    }
+    __syncthreads();
+    const __nv_bfloat16* dOc = (const __nv_bfloat16*)p.dO + t0 * p.dO_ld + (int64_t)h * Dv;
+    // dO^T and (scale e^G dO)^T: rows v, columns r
+    for (int idx = tid; idx < C * (Dv / 8); idx += kThreads) {
+      const int r = idx / (Dv / 8), v0 = (idx % (Dv / 8)) * 8;
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      if (r < len) raw = *(const uint4*)(dOc + (int64_t)r * p.dO_ld + v0);
+      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
+      const float sc = p.scale * ev[r];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        *(__nv_bfloat16*)(tdOt + tc::sw128_offset(v0 + u, r, MV)) = e[u];
+        tile_put(tdOet, MV, v0 + u, r, __bfloat162float(e[u]) * sc);
+      }
+    }
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tA1, tc::smem_u32(tdOt), MV, tc::smem_u32(tPt(b)), C, C, 0u);
+      tc::mma_tile(tA2, tc::smem_u32(tdSt), MV, tc::smem_u32(tK(b)), C, DK, 0u);
+      tc::mma_tile(tA3, tc::smem_u32(tdOet), MV, tc::smem_u32(tQt(b)), DK, C, 0u);
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    // dDelta^T = scale (P^T dO)^T + c (K dS)^T
+    float* dDg = p.dD + ch * C * Dv;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int col0 = half * 16 + 32 * q;
+      float a1[16], a2[16];
+      tc::tmem_ld16(tA1 + lane_quarter() + col0, a1);
+      tc::tmem_ld16(tA2 + lane_quarter() + col0, a2);
+      tc::tmem_ld_wait();
+      if (vok)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int s = col0 + j;
+          const float d = s < len ? p.scale * a1[j] + cv[s] * a2[j] : 0.f;
+          tile_put(tmDt, MV, vrow, s, -d);
+          dDg[(size_t)s * Dv + vrow] = d;
+        }
+    }
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tA3, tc::smem_u32(tmDt), MV, tc::smem_u32(tWt(b)), DK, C, 1u);
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    const float eC = expf(G[len - 1]);
+#pragma unroll
+    for (int ii = 0; ii < NKC; ++ii) {
+      const int col0 = half * 16 + 32 * ii;
+      if (col0 < DK) {
+        float x[16];
+        tc::tmem_ld16(tA3 + lane_quarter() + col0, x);
+        tc::tmem_ld_wait();
+        if (vok)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            dS[ii][j] = fmaf(eC, dS[ii][j], x[j]);
+            tile_put(tdSt, MV, vrow, col0 + j, dS[ii][j]);
+          }
+      }
+    }
+    tc::fence_async_smem();
+  }
+  if (ok && p.dS0 && vok)
+#pragma unroll
+    for (int ii = 0; ii < NKC; ++ii)
+      if (half * 16 + 32 * ii < DK)
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          p.dS0[((size_t)n * p.Hv + h) * SZ + (size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = dS[ii][j];
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory plan of k_bwd_grads_tc (bytes for Dk = Dv = 128; phases A-E of one
+// value head reuse the regions):
+//   R1 64K  A: S^T [Dv][Dk], S [Dk][Dv] | B: Delta, c*Delta, dW [C][D], dW^T [Dk][C]
+//           C-E: dPE, dPE^T, dT^T, Hs [C][C] (over Delta / c*Delta)
+//   R2 32K  A-B: [dO; dDelta] [128][Dv]   | B-E: fp32 [C][C] scratch
+//   R3 48K  A: W [C][Dk], scale e^G dO [C][Dv], U^T [Dv][C] | B: dS [Dk][Dv], P [C][C]
+//           C-E: dDelta^T [Dv][C], T^T, T, b e^G T^T, Y [C][C]
+//   R4 32K  B-C: V [C][Dv], e^G K [C][Dk]
+//   R5 32K  K^T, Q^T [Dk][C] of the key head (whole CTA)
+// TMEM (512 columns): dQ_hat @0, dK_hat @128 (M = 64 accumulators), scratch @256.
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int c = blockIdx.x, kh = blockIdx.y;
+  int n;
+  int64_t t0;
+  int len;
+  if (!chunk_info(p, c, &n, &t0, &len)) {
+    if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
+    return;
+  }
+  const int Dk = p.Dk, Dv = p.Dv;
+  const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
+  const uint32_t sCK = tc::sw128_bytes(C, Dk), sCV = tc::sw128_bytes(C, Dv);
+  const uint32_t sKC = (uint32_t)Dk * 128, sVC = (uint32_t)Dv * 128, sCC = 8192;
+  uint8_t* R1 = sm;
+  uint8_t* R2 = R1 + 65536;
+  uint8_t* R3 = R2 + 32768;
+  uint8_t* R4 = R3 + 49152;
+  uint8_t* R5 = R4 + 32768;
+  // R1
+  uint8_t* tSt = R1;                               // [Dv][Dk]
+  uint8_t* tS = R1 + tc::sw128_bytes(Dv, Dk);      // [Dk][Dv]
+  uint8_t* tDl = R1;                               // [C][Dv]
+  uint8_t* tDlc = R1 + 16384;                      // [C][Dv]
+  uint8_t* tdW = R1 + 32768;                       // [C][Dk]
+  uint8_t* tdWt = R1 + 49152;                      // [Dk][C]
+  uint8_t* tdPE = R1;                              // [C][C]
+  uint8_t* tdPEt = R1 + 8192;
+  uint8_t* tdTt = R1 + 16384;
+  uint8_t* tHs = R1 + 24576;
+  // R2
+  uint8_t* tA2 = R2;                               // [128][Dv]: rows 0-63 dO, 64-127 dDelta
+  float* X = (float*)R2;                           // [C][C] fp32 scratch
+  // R3
+  uint8_t* tW = R3;                                // [C][Dk]
+  uint8_t* tdOe = R3 + 16384;                      // [C][Dv]
+  __nv_bfloat16* sU = (__nv_bfloat16*)(R3 + 32768);// [Dv][C]
+  uint8_t* tdS = R3;                               // [Dk][Dv]
+  uint8_t* tP = R3 + 32768;                        // [C][C]
+  uint8_t* tdDt = R3;                              // [Dv][C]
+  uint8_t* tTt = R3 + 16384;
+  uint8_t* tT = R3 + 24576;
+  uint8_t* tTbe = R3 + 32768;
+  uint8_t* tY = R3 + 40960;
+  // R4
+  uint8_t* tV = R4;                                // [C][Dv]
+  uint8_t* tKe = R4 + 16384;                       // [C][Dk]
+  // R5
+  uint8_t* tKt = R5;                               // [Dk][C]
+  uint8_t* tQt = R5 + 16384;                       // [Dk][C]
+  float* vec = (float*)(R5 + 32768);
+  float* gv = vec;            // G
+  float* ev = gv + C;         // e^G
+  float* cv = ev + C;         // e^{G_last - G}
+  float* bv = cv + C;         // beta
+  float* dG = bv + C;         // dL/dG
+  float* db = dG + C;         // dL/d beta
+  float* part = db + C;       // [2][C] per-half partial row sums
+  float* red = part + 2 * C;  // [kThreads / 32]
+  uint64_t* bars = (uint64_t*)(red + 8);  // mma, load
+  uint32_t* tslot = (uint32_t*)(bars + 2);
+
+  if (tid == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tdQ = tmem, tdK = tmem + 128, tmp = tmem + 256;
+  uint32_t mphase = 0, lphase = 0;
+  const size_t ckk = (size_t)c * p.Hk + kh;
+  const float* Qn = p.Qn + ckk * C * Dk;
+  const float* Kn = p.Kn + ckk * C * Dk;
+  const float* KK = p.KKf + ckk * C * C;
+  const int row64 = acc_row(64);
+  const size_t SZ = (size_t)Dk * Dv;
+  bool ok = true;
+
+  // key-head tiles for the whole CTA
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bars[1], 2 * sKC);
+    tc::bulk_g2s(tKt, p.Ktsw + ckk * sKC, sKC, &bars[1]);
+    tc::bulk_g2s(tQt, p.Qtsw + ckk * sKC, sKC, &bars[1]);
+  }
+  {
+    const bool lok = tc::mbar_wait(&bars[1], lphase);
+    lphase ^= 1u;
+    if (__syncthreads_or(lok ? 0 : 1)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+      ok = false;
+    }
+  }
+
+  for (int hh = 0; hh < p.r && ok; ++hh) {
+    const int h = kh * p.r + hh;
+    const size_t ch = (size_t)c * p.Hv + h;
+    const uint32_t acc_first = hh > 0 ? 1u : 0u;
+    const float* S = p.saved_in + ch * SZ;
+    const float* dSg = p.dS + ch * SZ;
+    const float* dDg = p.dD + ch * C * Dv;
+    const float* Tg = p.Tm + ch * C * C;
+    const __nv_bfloat16* dOc = (const __nv_bfloat16*)p.dO + t0 * p.dO_ld + (int64_t)h * Dv;
+    const __nv_bfloat16* Vc = (const __nv_bfloat16*)p.v + t0 * p.v_ld + (int64_t)h * Dv;
+    if (tid < C) {
+      const float g = p.G[ch * C + tid];
+      gv[tid] = g;
+      bv[tid] = p.b[ch * C + tid];
+      dG[tid] = 0.f;
+      db[tid] = 0.f;
+    }
+    // W and U^T tiles of this head (bulk copies), overlapped with the staging below
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2);
+      tc::bulk_g2s(tW, p.Wsw + ch * sCK, sCK, &bars[1]);
+      tc::bulk_g2s(sU, p.Utb + ch * Dv * C, (uint32_t)Dv * C * 2, &bars[1]);
+    }
+    __syncthreads();
+    if (tid < C) {
+      ev[tid] = expf(gv[tid]);
+      cv[tid] = tid < len ? expf(gv[len - 1] - gv[tid]) : 0.f;
+    }
+    __syncthreads();
+    // ---- phase A: S, S^T, [dO; dDelta], scale e^G dO
+    stage_f32(S, Dk, Dv, Dv, Dk, tS, tSt, Dv, [](int) { return 1.f; });
+    stage_bf16(dOc, C, Dv, p.dO_ld, len, tA2, 128, tdOe, nullptr, 0,
+               [&](int r) { return p.scale * ev[r]; });
+    {
+      // rows 64..127 of the [dO; dDelta] tile
+      const int cpr = Dv / 8;
+      for (int idx = tid; idx < C * cpr; idx += kThreads) {
+        const int r = idx / cpr, c0 = (idx % cpr) * 8;
+        const float4 a = *(const float4*)(dDg + (size_t)r * Dv + c0);
+        const float4 bq = *(const float4*)(dDg + (size_t)r * Dv + c0 + 4);
+        __align__(16) __nv_bfloat162 pk[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
+                                              __floats2bfloat162_rn(bq.x, bq.y), __floats2bfloat162_rn(bq.z, bq.w)};
+        *(uint4*)(tA2 + tc::sw128_offset(64 + r, c0, 128)) = *(const uint4*)pk;
+      }
+    }
+    {
+      const bool lok = tc::mbar_wait(&bars[1], lphase);
+      lphase ^= 1u;
+      if (__syncthreads_or(lok ? 0 : 1)) {
+        if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+        ok = false;
+        break;
+      }
+    }
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tmp, tc::smem_u32(tW), 64, tc::smem_u32(tSt), Dv, Dk, 0u);           // W S
+      tc::mma_tile(tmp + 128, tc::smem_u32(tA2), 128, tc::smem_u32(tS), Dk, Dv, 0u);   // [dO;dD] S^T
+      tc::mma_tile(tdQ, tc::smem_u32(tdOe), 64, tc::smem_u32(tS), Dk, Dv, acc_first);  // dQ += s e^G dO S^T
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    // epilogue A: Delta = U - W S; dG += scale e^G (Q . dO S^T); dW = -dDelta S^T
+    part[tid & 127] = 0.f;
+    __syncthreads();
+    for (int q = half; q * 16 < Dv; q += 2) {
+      float x[16];
+      tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
+      tc::tmem_ld_wait();
+      if (row64 >= 0)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int v = q * 16 + j;
+          const float d = __bfloat162float(sU[v * C + row64]) - x[j];
+          tile_put(tDl, C, row64, v, d);
+          tile_put(tDlc, C, row64, v, d * cv[row64]);
+        }
+    }
+    {
+      const int row = acc_row(128);
+      float rs = 0.f;
+      for (int q = half; q * 16 < Dk; q += 2) {
+        float x[16];
+        tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
+        tc::tmem_ld_wait();
+        if (row < C) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) rs = fmaf(Qn[row * Dk + q * 16 + j], x[j], rs);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            tile_put(tdW, C, row - C, q * 16 + j, -x[j]);
+            tile_put(tdWt, Dk, q * 16 + j, row - C, -x[j]);
+          }
+        }
+      }
+      if (row < C) part[half * C + row] = rs;
+    }
+    __syncthreads();
+    if (tid < C) dG[tid] += p.scale * ev[tid] * (part[tid] + part[C + tid]);
+    // ---- phase B: dS, V, e^G K, P
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(&bars[1], sCC);
+      tc::bulk_g2s(tP, p.Psw + ch * sCC, sCC, &bars[1]);
+    }
+    stage_f32(dSg, Dk, Dv, Dv, Dk, tdS, nullptr, 0, [](int) { return 1.f; });
+    stage_bf16(Vc, C, Dv, p.v_ld, len, tV, C, nullptr, nullptr, 0, [](int) { return 1.f; });
+    stage_f32(Kn, C, Dk, Dk, C, tKe, nullptr, 0, [&](int r) { return ev[r]; });
+    {
+      float sds = 0.f;
+      for (size_t e = tid; e < SZ; e += kThreads) sds = fmaf(S[e], dSg[e], sds);
+      sds = warp_sum(sds);
+      if ((tid & 31) == 0) red[warp] = sds;
+    }
+    {
+      const bool lok = tc::mbar_wait(&bars[1], lphase);
+      lphase ^= 1u;
+      if (__syncthreads_or(lok ? 0 : 1)) {
+        if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+        ok = false;
+        break;
+      }
+    }
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tmp, tc::smem_u32(tDlc), 64, tc::smem_u32(tdS), Dk, Dv, 0u);        // c Delta dS^T
+      tc::mma_tile(tdK, tc::smem_u32(tDlc), 64, tc::smem_u32(tdS), Dk, Dv, acc_first); // dK +=
+      tc::mma_tile_p(tmp + 128, tc::smem_u32(tA2), 128u * 128u, 64, tc::smem_u32(tDl),
+                     (uint32_t)C * 128u, C, Dv, 0u);                                     // dO Delta^T
+      tc::mma_tile_p(tmp + 192, tc::smem_u32(tA2) + 64u * 128u, 128u * 128u, 64,
+                     tc::smem_u32(tV), (uint32_t)C * 128u, C, Dv, 0u);                  // dDelta V^T
+      tc::mma_tile(tmp + 192, tc::smem_u32(tdW), 64, tc::smem_u32(tKe), C, Dk, 1u);     // + dW (e^G K)^T
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    // epilogue B
+    {
+      float rs = 0.f;
+      for (int q = half; q * 16 < Dk; q += 2) {
+        float x[16];
+        tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
+        tc::tmem_ld_wait();
+        if (row64 >= 0)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) rs = fmaf(Kn[row64 * Dk + q * 16 + j], x[j], rs);
+      }
+      if (row64 >= 0) part[half * C + row64] = rs;  // c_s * dc_s
+    }
+    for (int q = half; q < 4; q += 2) {
+      float x[16], y[16];
+      tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
+      tc::tmem_ld16(tmp + 192 + lane_quarter() + q * 16, y);
+      tc::tmem_ld_wait();
+      if (row64 >= 0) {
+        const int r = row64;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int s = q * 16 + j;
+          const float dP = (s <= r && r < len) ? p.scale * x[j] : 0.f;
+          const float E = s <= r ? expf(gv[r] - gv[s]) : 0.f;
+          X[r * C + s] = dP * tile_get(tP, C, r, s);
+          tile_put(tdPE, C, r, s, dP * E);
+          tile_put(tdPEt, C, s, r, dP * E);
+          tile_put(tdTt, C, s, r, bv[s] * y[j]);   // dT[r][s] = b_s (...)
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < C) {
+      const int t = tid;
+      float rsum = 0.f, csum = 0.f;
+      for (int s = 0; s < C; ++s) rsum += X[t * C + s];
+      for (int r = 0; r < C; ++r) csum += X[r * C + t];
+      dG[t] += rsum - csum - (part[t] + part[C + t]);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float tot = 0.f, sc = 0.f;
+      for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
+      for (int s = 0; s < C; ++s) sc += part[s] + part[C + s];
+      dG[len - 1] += expf(gv[len - 1]) * tot + sc;
+    }
+    // ---- phase C: dDelta^T, T^T, T, b e^G T^T
+    stage_f32(dDg, C, Dv, Dv, C, nullptr, tdDt, Dv, [](int) { return 1.f; });
+    stage_f32(Tg, C, C, C, C, tT, tTt, C, [](int) { return 1.f; });
+    stage_f32(Tg, C, C, C, C, nullptr, tTbe, C, [&](int r) { return 1.f; });
+    __syncthreads();
+    // b e^G T^T: scale row s of tTbe (= column s of T) by b_s e^{G_s}
+    for (int idx = tid; idx < C * C; idx += kThreads) {
+      const int s = idx / C, r = idx % C;
+      tile_put(tTbe, C, s, r, tile_get(tTbe, C, s, r) * bv[s] * ev[s]);
+    }
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tdQ, tc::smem_u32(tdPE), 64, tc::smem_u32(tKt), Dk, C, 1u);      // dQ += dPE K
+      tc::mma_tile(tdK, tc::smem_u32(tdPEt), 64, tc::smem_u32(tQt), Dk, C, 1u);     // dK += dPE^T Q
+      tc::mma_tile(tmp, tc::smem_u32(tTt), 64, tc::smem_u32(tdDt), Dv, C, 0u);      // dBv = T^T dD
+      tc::mma_tile(tmp + 128, tc::smem_u32(tTt), 64, tc::smem_u32(tdTt), C, C, 0u); // Y = T^T dT
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    // epilogue C: dv = b dBv, db += rowsum(dBv * V), Y tile
+    {
+      __nv_bfloat16* dvc = (__nv_bfloat16*)p.dv + t0 * p.dv_ld + (int64_t)h * Dv;
+      float rs = 0.f;
+      for (int q = half; q * 16 < Dv; q += 2) {
+        float x[16];
+        tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
+        tc::tmem_ld_wait();
+        if (row64 >= 0 && row64 < len) {
+          const int s = row64;
+          __align__(16) __nv_bfloat162 pk[8];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) rs = fmaf(x[j], tile_get(tV, C, s, q * 16 + j), rs);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pk[j] = __floats2bfloat162_rn(bv[s] * x[2 * j], bv[s] * x[2 * j + 1]);
+          uint4* dst = (uint4*)(dvc + (int64_t)s * p.dv_ld + q * 16);
+          dst[0] = ((const uint4*)pk)[0];
+          dst[1] = ((const uint4*)pk)[1];
+        }
+      }
+      if (row64 >= 0) part[half * C + row64] = rs;
+      for (int q = half; q < 4; q += 2) {
+        float x[16];
+        tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
+        tc::tmem_ld_wait();
+        if (row64 >= 0)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) tile_put(tY, C, row64, q * 16 + j, x[j]);
+      }
+    }
+    __syncthreads();
+    if (tid < C) db[tid] += part[tid] + part[C + tid];
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tmp, tc::smem_u32(tTt), 64, tc::smem_u32(tdWt), Dk, C, 0u);    // dBk = T^T dW
+      tc::mma_tile(tdK, tc::smem_u32(tTbe), 64, tc::smem_u32(tdWt), Dk, C, 1u);   // dK += b e^G dBk
+      tc::mma_tile(tmp + 128, tc::smem_u32(tY), 64, tc::smem_u32(tT), C, C, 0u);  // Y T^T
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    // epilogue D: t_s = rowsum(dBk * K); dA = -(Y T^T) strictly lower
+    {
+      float rs = 0.f;
+      for (int q = half; q * 16 < Dk; q += 2) {
+        float x[16];
+        tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
+        tc::tmem_ld_wait();
+        if (row64 >= 0)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) rs = fmaf(Kn[row64 * Dk + q * 16 + j], x[j], rs);
+      }
+      if (row64 >= 0) part[half * C + row64] = rs;
+      for (int q = half; q < 4; q += 2) {
+        float x[16];
+        tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
+        tc::tmem_ld_wait();
+        if (row64 >= 0)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int s = q * 16 + j;
+            X[row64 * C + s] = s < row64 ? -x[j] : 0.f;
+          }
+      }
+    }
+    __syncthreads();
+    if (tid < C) {
+      const int t = tid;
+      const float ts = part[t] + part[C + t];
+      db[t] += ev[t] * ts;
+      dG[t] += bv[t] * ev[t] * ts;
+      // A[r][s] = b_r E_rs KK_rs (s < r): db_r += sum_s dA E KK, dG_r += sum_s dA*A, dG_s -= sum_r dA*A
+      float rdb = 0.f, ry = 0.f, cy = 0.f;
+      for (int s = 0; s < t; ++s) {
+        const float q = X[t * C + s] * expf(gv[t] - gv[s]) * KK[t * C + s];
+        rdb += q;
+        ry += q * bv[t];
+      }
+      for (int r = t + 1; r < C; ++r) cy += X[r * C + t] * expf(gv[r] - gv[t]) * KK[r * C + t] * bv[r];
+      db[t] += rdb;
+      dG[t] += ry - cy;
+    }
+    // H = dA * b_r E; Hs = H + H^T
+    for (int idx = tid; idx < C * C; idx += kThreads) {
+      const int s = idx / C, r = idx % C;
+      const float h1 = r < s ? X[s * C + r] * bv[s] * expf(gv[s] - gv[r]) : 0.f;
+      const float h2 = s < r ? X[r * C + s] * bv[r] * expf(gv[r] - gv[s]) : 0.f;
+      tile_put(tHs, C, s, r, h1 + h2);
+    }
+    tc::fence_async_smem();
+    ok = mma_run([&] {
+      tc::mma_tile(tdK, tc::smem_u32(tHs), 64, tc::smem_u32(tKt), Dk, C, 1u);     // dK += Hs K
+    }, &bars[0], mphase, p.status, c);
+    if (!ok) break;
+    // gate and sigmoid epilogues: dl = reverse cumsum of dG
+    if (tid == 0) {
+      float run = 0.f;
+      for (int t = C - 1; t >= 0; --t) {
+        run += (t < len) ? dG[t] : 0.f;
+        part[t] = run;
+      }
+    }
+    __syncthreads();
+    {
+      float pa = 0.f, pd = 0.f;
+      if (tid < len) {
+        const int t = tid;
+        const float x = p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
+        const float ea = expf(p.a_log[h]);
+        const float l = -ea * softplus_f(x);
+        const float dl = part[t];
+        const float da = dl * (-ea) * sigmoid_f(x);
+        p.dalpha[(t0 + t) * p.dalpha_ld + h] = da;
+        p.dbeta[(t0 + t) * p.dbeta_ld + h] = db[t] * bv[t] * (1.f - bv[t]);
+        pa = dl * l;
+        pd = da;
+      }
+      pa = warp_sum(pa);
+      pd = warp_sum(pd);
+      __syncthreads();
+      if (tid < C && (tid & 31) == 0) {
+        red[tid >> 5] = pa;
+        red[2 + (tid >> 5)] = pd;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        p.pa[ch] = red[0] + red[1];
+        p.pd[ch] = red[2] + red[3];
+      }
+      __syncthreads();
+    }
+  }
+  // dq, dk of the key head: L2-norm backward of the accumulated dQ_hat, dK_hat
+  if (ok) {
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t acc = which ? tdK : tdQ;
+      const float* xh = which ? Kn : Qn;
+      float dot = 0.f;
+      for (int q = half; q * 16 < Dk; q += 2) {
+        float x[16];
+        tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
+        tc::tmem_ld_wait();
+        if (row64 >= 0)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dot = fmaf(x[j], xh[row64 * Dk + q * 16 + j], dot);
+      }
+      if (row64 >= 0) part[half * C + row64] = dot;
+      __syncthreads();
+      const float* nrm = (which ? p.nk : p.nq) + ckk * C;
+      __nv_bfloat16* dst = (__nv_bfloat16*)(which ? p.dk : p.dq) +
+                           t0 * (which ? p.dk_ld : p.dq_ld) + (int64_t)kh * Dk;
+      const int64_t ld = which ? p.dk_ld : p.dq_ld;
+      for (int q = half; q * 16 < Dk; q += 2) {
+        float x[16];
+        tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
+        tc::tmem_ld_wait();
+        if (row64 >= 0 && row64 < len) {
+          const int r = row64;
+          const float d = part[r] + part[C + r], inv = 1.f / nrm[r];
+          __align__(16) __nv_bfloat162 pk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float a = (x[2 * j] - xh[r * Dk + q * 16 + 2 * j] * d) * inv;
+            const float b2 = (x[2 * j + 1] - xh[r * Dk + q * 16 + 2 * j + 1] * d) * inv;
+            pk[j] = __floats2bfloat162_rn(a, b2);
+          }
+          uint4* o = (uint4*)(dst + (int64_t)r * ld + q * 16);
+          o[0] = ((const uint4*)pk)[0];
+          o[1] = ((const uint4*)pk)[1];
+        }
+      }
+      __syncthreads();
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+__global__ void k_bwd_gates_tc(Params p) {
+  for (int h = threadIdx.x; h < p.Hv; h += blockDim.x) {
+    float a = 0.f, d = 0.f;
+    for (int c = 0; c < p.NC; ++c) {
+      a += p.pa[(size_t)c * p.Hv + h];
+      d += p.pd[(size_t)c * p.Hv + h];
+    }
+    p.da_log[h] = a;
+    p.ddt_bias[h] = d;
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int DK>
+static cudaError_t launch_bwd_state_tc_t(const Params& p, cudaStream_t st) {
+  const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
+  const size_t bK = tc::sw128_bytes(64, DK), bKt = (size_t)DK * 128;
+  const size_t bufsz = bK + 8192 + 2 * bKt + 1024;
+  const size_t smem = tc::sw128_bytes(MV, DK) + 3 * (size_t)MV * 128 + 2 * bufsz + 2 * C * 4 + 64 + 1024;
+  cudaFuncSetAttribute(k_bwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  profile_pre(st, KID_BWD_STATE_TC);
+  k_bwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kThreads, smem, st>>>(p);
+  profile_post(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_tc(const Params& p, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  if (p.n_seqs > 0) {
+    switch (p.Dk) {
+      case 16: e = launch_bwd_state_tc_t<16>(p, st); break;
+      case 32: e = launch_bwd_state_tc_t<32>(p, st); break;
+      case 64: e = launch_bwd_state_tc_t<64>(p, st); break;
+      default: e = launch_bwd_state_tc_t<128>(p, st); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  const size_t smem = 65536 + 32768 + 49152 + 32768 + 32768 + (size_t)(10 * C + 8) * 4 + 64 + 1024;
+  cudaFuncSetAttribute(k_bwd_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  profile_pre(st, KID_BWD_GRADS_TC);
+  k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p);
+  profile_post(st);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  profile_pre(st, KID_BWD_GATES);
+  k_bwd_gates_tc<<<1, kThreads, 0, st>>>(p);
+  profile_post(st);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

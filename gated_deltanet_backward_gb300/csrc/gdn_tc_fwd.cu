@@ -108,7 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
   uint8_t* tOW = tTB + 8192;                            // [C][Dk]  W (staging)
   uint8_t* tOWt = tOW + tc::sw128_bytes(64, Dk);        // [Dk][C]  W^T (staging)
   uint8_t* tOP = tOWt + Dk * 128;                       // [C][C]   P (staging)
-  float* KK = (float*)(tOP + 8192);                     // [C][C]
+  uint8_t* tOPt = tOP + 8192;                           // [C][C]   P^T (staging, backward)
+  uint8_t* tQt = tOW;  // [MK][C] Q^T (backward); shares tOW's space, used before the head loop
+  float* KK = (float*)(tOPt + 8192);                    // [C][C]
   float* QK = KK + C * C;                               // [C][C]
   float* Tm = QK + C * C;                               // [RB][C][C]
   float* Mt = Tm + RB * C * C;                          // [RB][3][256]
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
 
   // zero the transposed tiles (rows past Dk / Dv pad the M = 64 products)
   for (int i = tid; i < MK * 128 / 16; i += kThreads) ((uint4*)tKt)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < MK * 128 / 16; i += kThreads) ((uint4*)tQt)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < MV * 128 / 16; i += kThreads) ((uint4*)tVt)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     tc::mbar_init(bar, 1);
@@ -160,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
         const float xh = x[u] / nrm;
         tile_put(tAQK, 128, row, i, xh);
         if (!isq) tile_put(tKt, MK, i, t, xh);
+        else if (bwd) tile_put(tQt, MK, i, t, xh);
         if (bwd) (isq ? p.Qn : p.Kn)[(ck + t) * Dk + i] = xh;
       }
     }
@@ -191,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
       cta_copy16(gq + b * 8192, tAQK + b * aqk_pitch + 8192, 8192);
     }
     cta_copy16(p.Ktsw + ((size_t)c * p.Hk + kh) * tileDC(Dk), tKt, Dk * 128);
+    if (bwd) cta_copy16(p.Qtsw + ((size_t)c * p.Hk + kh) * tileDC(Dk), tQt, Dk * 128);
   }
   __syncthreads();
 
@@ -250,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
       stage_tile(tOP, C, C, [&](int r, int s) {
         return s <= r ? expf(G[r] - G[s]) * QK[r * C + s] : 0.f;
       });
+      if (bwd)
+        stage_tile(tOPt, C, C, [&](int s, int r) {
+          return s <= r ? expf(G[r] - G[s]) * QK[r * C + s] : 0.f;
+        });
       const __nv_bfloat16* Vs = (const __nv_bfloat16*)p.v + t0 * p.v_ld + (int64_t)h * Dv;
       stage_tile(tVt, Dv, C, [&](int vv, int s) {
         return s < len ? __bfloat162float(Vs[(int64_t)s * p.v_ld + vv]) : 0.f;
@@ -286,7 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
       __syncthreads();
       cta_copy16(p.Wsw + ch * tileCD(Dk), tOW, (uint32_t)tileCD(Dk));
       cta_copy16(p.Psw + ch * tileCD(64), tOP, 8192);
-      if (bwd) cta_copy16(p.Wtsw + ch * tileDC(Dk), tOWt, Dk * 128);
+      if (bwd) {
+        cta_copy16(p.Wtsw + ch * tileDC(Dk), tOWt, Dk * 128);
+        cta_copy16(p.Ptsw + ch * 8192, tOPt, 8192);
+      }
       __syncthreads();
     }
   }
@@ -494,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
 static size_t prep_tc_smem(const Params& p) {
   const int Dk = p.Dk, Dv = p.Dv, MK = Dk < 64 ? 64 : Dk, MV = Dv < 64 ? 64 : Dv;
   size_t b = tc::sw128_bytes(128, Dk) + (size_t)MK * 128 + (size_t)MV * 128 + 8192 * 2 +
-             tc::sw128_bytes(64, Dk) + (size_t)Dk * 128 + 8192;
+             tc::sw128_bytes(64, Dk) + (size_t)Dk * 128 + 8192 * 2;
   b += sizeof(float) * ((size_t)2 * C * C + (size_t)RB * C * C + RB * 3 * 256 + 3 * RB * C);
   return b + 64 + 1024;
 }
