@@ -118,7 +118,35 @@ def kernel_models(wl: W.Workload):
              NC * Hv * 2 * C * Dk * f4 + T * Hv * Dv * es + T * Hv * 2 * 4)
     bgr_f = NC * Hv * (12 * C * Dk * Dv + 2 * C * C * (5 * Dk + 3 * Dv) + 4 * C ** 3)
     bqk_b = NC * Hv * 2 * C * Dk * f4 + NC * Hk * C * 2 * (Dk + 1) * f4 + T * Hk * 2 * Dk * es
+    # tensor-core (bf16) kernels
+    sKC = (Dk + 63) // 64 * C * 128                  # bf16 [C][Dk] tile
+    sKt = Dk * 128                                   # bf16 [Dk][C] tile
+    tc_prep_b = (T * (2 * Hk * Dk * es + Hv * Dv * es + 2 * Hv * 4) + NC * Hk * 3 * sKC +
+                 NC * Hv * (sKC + C * C * 2 + Dv * C * 2 + 2 * C * 4))
+    tc_prep_f = (NC * Hk * 2 * 128 * C * Dk + NC * Hv * (2 * C * C * (Dk + Dv) + C ** 3 / 3 +
+                                                          C * C * 8))
+    tc_prep_bwd_b = tc_prep_b + (NC * Hk * (C * Dk * 8 + C * 8 + 2 * C * C * 4 + sKt) +
+                                 NC * Hv * (C * (Dk + Dv) * 4 + C * C * 4 + sKt + C * C * 2))
+    fst_tc_b = (NC * Hv * (sKC + C * C * 2 + Dv * C * 2 + C * 4) + NC * Hk * (sKC + sKt) +
+                T * Hv * Dv * es + NC * Hv * Dk * Dv * 4)
+    fst_tc_f = NC * Hv * (6 * C * Dk * Dv + 2 * C * C * Dv)
+    bst_tc_b = (NC * Hk * (sKC + sKt) + NC * Hv * (C * C * 2 + sKt + C * 4) + T * Hv * Dv * es +
+                NC * Hv * (Dk * Dv + C * Dv) * 4)
+    bst_tc_f = NC * Hv * (2 * C * C * Dv + 6 * C * Dk * Dv)
+    bgr_tc_b = (NC * Hv * (2 * Dk * Dv * 4 + 2 * C * Dv * 4 + sKC + Dv * C * 2 + C * C * 2 +
+                           2 * C * C * 4 + 3 * C * 4) + T * Hv * (2 * Dv * es + 4) +
+                NC * Hk * (2 * C * Dk * 4 + C * C * 4 + 2 * sKt + 2 * C * 4) +
+                T * Hk * 2 * Dk * es + T * Hv * (Dv * es + 8) + NC * Hv * 8)
+    bgr_tc_f = NC * Hv * (2 * C * Dk * Dv + 2 * 128 * Dk * Dv + 2 * C * Dk * Dv +
+                          4 * C * Dk * Dv + 2 * C * C * Dv + 2 * C * C * (Dv + Dk) +
+                          4 * C * C * Dk + 2 * C * C * Dv + 4 * C ** 3 + 4 * C * C * Dk +
+                          2 * C * C * Dk)
     return {
+        "gdn_prep_tc": (tc_prep_b, tc_prep_f, "tensor"),
+        "gdn_prep_tc_bwd": (tc_prep_bwd_b, tc_prep_f, "tensor"),
+        "gdn_fwd_state_tc": (fst_tc_b, fst_tc_f, "tensor"),
+        "gdn_bwd_state_tc": (bst_tc_b, bst_tc_f, "tensor"),
+        "gdn_bwd_grads_tc": (bgr_tc_b, bgr_tc_f, "tensor"),
         "gdn_prep": (prep_b, prep_f, "alu"),
         "gdn_fwd_state": (fst_b, fst_f, "alu"),
         "gdn_bwd_state": (bst_b, bst_f, "alu"),
@@ -126,6 +154,27 @@ def kernel_models(wl: W.Workload):
         "gdn_bwd_qk": (bqk_b, 0.0, "alu"),
         "gdn_bwd_gates": (NC * Hv * 8 + Hv * 8, 0.0, "alu"),
     }
+
+
+def kernel_roofline(b, f, unit, avg_s, pk):
+    """Roofline entry of one kernel: the roof (HBM bytes or FLOPs at the unit's peak)
+    that bounds its algorithmic work, and the achieved rate against it."""
+    peak_alu = alu_fp32_tflops(pk["sm_max_mhz"])
+    t_mem = b / (pk["hbm_gbs"] * 1e9)
+    peak_c = peak_alu if unit == "alu" else pk["bf16_tflops"]
+    t_cmp = f / (peak_c * 1e12)
+    if t_cmp > t_mem:
+        roof = {"bound": unit, "achieved": f / avg_s / 1e12, "peak": peak_c, "unit": "TFLOP/s"}
+        roof["peak_source"] = ("derived: 152 SMs x 128 FP32 lanes x 2 x %.0f MHz" %
+                               pk["sm_max_mhz"]) if unit == "alu" else pk["source"] + " bf16"
+    else:
+        roof = {"bound": "hbm", "achieved": b / avg_s / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "peak_source": pk["source"] + " HBM"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["algorithmic_bytes"] = b
+    roof["algorithmic_flops"] = f
+    return roof
 
 
 # ----------------------------------------------------------------------------
@@ -279,22 +328,12 @@ def run_ours(args):
     dom = max(per, key=lambda n: sum(per[n]))
     b, f, unit = models[dom]
     avg_s = sum(per[dom]) / len(per[dom]) * 1e-3
-    peak_alu = alu_fp32_tflops(pk["sm_max_mhz"])
-    t_mem = b / (pk["hbm_gbs"] * 1e9)
-    t_cmp = f / (peak_alu * 1e12) if unit == "alu" else f / (pk["bf16_tflops"] * 1e12)
-    if t_cmp > t_mem:
-        roof = {"bound": unit, "achieved": f / avg_s / 1e12,
-                "peak": peak_alu if unit == "alu" else pk["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": b / avg_s / 1e9, "peak": pk["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof = kernel_roofline(b, f, unit, avg_s, pk)
     roof["kernel"] = dom
-    roof["algorithmic_bytes"] = b
-    roof["algorithmic_flops"] = f
-    roof["peak_source"] = pk["source"] if roof["unit"] == "GB/s" or unit != "alu" else \
-        "derived: 152 SMs x 128 FP32 lanes x 2 x %.0f MHz" % pk["sm_max_mhz"]
+    for name in kernels:
+        kb, kf, ku = models[name]
+        r = kernel_roofline(kb, kf, ku, kernels[name]["avg_us"] * 1e-6, pk)
+        kernels[name].update(bound=r["bound"], frac=r["frac"])
     pm = path_model(wl)
     t_roof = max(pm["bytes"] / (pk["hbm_gbs"] * 1e9), pm["flops"] / (pk["bf16_tflops"] * 1e12))
     path_roof = {"bytes_per_step": pm["bytes"], "flops_per_step": pm["flops"],
@@ -308,11 +347,13 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": "%s: %d x %d tokens, Hk=%d, Hv=%d, Dk=%d, Dv=%d, %s q/k/v/o/dO, "
                                "fp32 gates/state" % (wl.name, N, T // max(N, 1), Hk, Hv, Dk, Dv,
                                                       wl.dtype),
-                   "tokens_per_gpu": T, "io_dtype": wl.dtype, "compute": "fp32 CUDA-core FMA",
+                   "tokens_per_gpu": T, "io_dtype": wl.dtype,
+                   "compute": ("tcgen05 bf16 MMA, fp32 accumulate and state" if wl.dtype == "bf16"
+                               else "fp32 CUDA-core FMA"),
                    "l2": "flushed: 256 MB write between timed steps",
                    "parallelism": "independent batch per GPU" if world > 1 else "single GPU"},
         "fwd_ms": sum(f_ms) / K, "bwd_ms": sum(b_ms) / K,

@@ -231,6 +231,7 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_FWD_STATE_TC: return "gdn_fwd_state_tc";
     case gdn::KID_BWD_STATE_TC: return "gdn_bwd_state_tc";
     case gdn::KID_BWD_GRADS_TC: return "gdn_bwd_grads_tc";
+    case gdn::KID_PREP_TC_BWD: return "gdn_prep_tc_bwd";
     default: return "?";
   }
 }

@@ -195,7 +195,8 @@ enum KernelId {
   KID_FWD_STATE_TC = 7,
   KID_BWD_STATE_TC = 8,
   KID_BWD_GRADS_TC = 9,
-  KID_COUNT = 10
+  KID_PREP_TC_BWD = 10,
+  KID_COUNT = 11
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are

@@ -524,7 +524,7 @@ cudaError_t launch_prep_tc(const Params& p, bool bwd, cudaStream_t st) {
   if (p.NC == 0) return cudaSuccess;
   const size_t smem = prep_tc_smem(p);
   cudaFuncSetAttribute(k_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  profile_pre(st, KID_PREP_TC);
+  profile_pre(st, bwd ? KID_PREP_TC_BWD : KID_PREP_TC);
   k_prep_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, bwd ? 1 : 0);
   profile_post(st);
   return cudaGetLastError();
