@@ -57,13 +57,16 @@ __device__ __forceinline__ void stage_tile(uint8_t* tile, int rows, int cols, F 
 // Stages an fp32 row-major source M (R rows x Cc columns, row stride ld floats,
 // 16-byte aligned rows, Cc a multiple of 8) into a natural tile tn (R rows, Cc
 // columns) and / or a transposed tile tt (Cc rows, R columns; tt_rows = its row
-// count), each element multiplied by rs(r).  Rows r >= valid read as zero.
-template <class RS>
+// count); element (r, c) is multiplied by rs(r) * cs(c).  Rows r >= valid read as
+// zero.  Consecutive threads take consecutive source rows, so that the
+// transposed writes of a warp land in one tile row (no bank conflicts) and the
+// natural 16-byte writes of 8 threads cover all 32 banks.
+template <class RS, class CS>
 __device__ __forceinline__ void stage_f32(const float* M, int R, int Cc, int64_t ld, int valid,
-                                          uint8_t* tn, uint8_t* tt, int tt_rows, RS rs) {
+                                          uint8_t* tn, uint8_t* tt, int tt_rows, RS rs, CS cs) {
   const int cpr = Cc >> 3;
   for (int idx = threadIdx.x; idx < R * cpr; idx += blockDim.x) {
-    const int r = idx / cpr, c0 = (idx - (idx / cpr) * cpr) << 3;
+    const int r = idx % R, c0 = (idx / R) << 3;
     float v[8];
     if (r < valid) {
       const float4 a = *(const float4*)(M + (int64_t)r * ld + c0);
@@ -71,6 +74,8 @@ __device__ __forceinline__ void stage_f32(const float* M, int R, int Cc, int64_t
       const float s = rs(r);
       v[0] = a.x * s; v[1] = a.y * s; v[2] = a.z * s; v[3] = a.w * s;
       v[4] = b.x * s; v[5] = b.y * s; v[6] = b.z * s; v[7] = b.w * s;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] *= cs(c0 + u);
     } else {
 #pragma unroll
       for (int u = 0; u < 8; ++u) v[u] = 0.f;
@@ -87,23 +92,26 @@ __device__ __forceinline__ void stage_f32(const float* M, int R, int Cc, int64_t
         *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + u, r, tt_rows)) = __float2bfloat16_rn(v[u]);
   }
 }
+struct One {
+  __device__ __forceinline__ float operator()(int) const { return 1.f; }
+};
 
 // As stage_f32 for a bf16 row-major source (row stride ld elements, 16-byte
-// aligned rows).  Two natural outputs may be produced: tn (unscaled) and tn2
-// (scaled by rs(r)); tt (transposed, unscaled).
+// aligned rows).  Outputs: tn (natural, unscaled, tn_rows rows), tn2 (natural,
+// scaled by rs(r), R rows), tt (transposed, scaled by rs(r), tt_rows rows).
 template <class RS>
 __device__ __forceinline__ void stage_bf16(const __nv_bfloat16* M, int R, int Cc, int64_t ld,
                                            int valid, uint8_t* tn, int tn_rows, uint8_t* tn2,
                                            uint8_t* tt, int tt_rows, RS rs) {
   const int cpr = Cc >> 3;
   for (int idx = threadIdx.x; idx < R * cpr; idx += blockDim.x) {
-    const int r = idx / cpr, c0 = (idx - (idx / cpr) * cpr) << 3;
+    const int r = idx % R, c0 = (idx / R) << 3;
     uint4 raw = make_uint4(0, 0, 0, 0);
     if (r < valid) raw = *(const uint4*)(M + (int64_t)r * ld + c0);
     if (tn) *(uint4*)(tn + tc::sw128_offset(r, c0, tn_rows)) = raw;
     if (tn2 || tt) {
       const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
-      const float s = tn2 ? rs(r) : 1.f;
+      const float s = rs(r);
       if (tn2) {
         __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
@@ -115,8 +123,32 @@ __device__ __forceinline__ void stage_bf16(const __nv_bfloat16* M, int R, int Cc
       if (tt)
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + u, r, tt_rows)) = e[u];
+          *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + u, r, tt_rows)) =
+              __float2bfloat16_rn(__bfloat162float(e[u]) * s);
     }
+  }
+}
+
+// Writes 16 consecutive elements v[0..15] of row r, columns c0..c0+15 (c0 a
+// multiple of 16), of a K-major SW128 bf16 tile with two 16-byte stores.
+__device__ __forceinline__ void tile_put16(uint8_t* tile, int rows, int r, int c0, const float* v) {
+  __align__(16) __nv_bfloat162 pk[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) pk[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+  *(uint4*)(tile + tc::sw128_offset(r, c0, rows)) = ((const uint4*)pk)[0];
+  *(uint4*)(tile + tc::sw128_offset(r, c0 + 8, rows)) = ((const uint4*)pk)[1];
+}
+
+// Reads 16 consecutive elements of row r, columns c0..c0+15, of a SW128 bf16 tile.
+__device__ __forceinline__ void tile_get16(const uint8_t* tile, int rows, int r, int c0, float* v) {
+  const uint4 a = *(const uint4*)(tile + tc::sw128_offset(r, c0, rows));
+  const uint4 b = *(const uint4*)(tile + tc::sw128_offset(r, c0 + 8, rows));
+  const __nv_bfloat16* ea = (const __nv_bfloat16*)&a;
+  const __nv_bfloat16* eb = (const __nv_bfloat16*)&b;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[j] = __bfloat162float(ea[j]);
+    v[8 + j] = __bfloat162float(eb[j]);
   }
 }
 

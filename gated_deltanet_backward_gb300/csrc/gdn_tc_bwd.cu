@@ -87,9 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
     }
 #pragma unroll
   for (int i = 0; i < NKC; ++i)
-    if (half * 16 + 32 * i < DK && vok)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) tile_put(tdSt, MV, vrow, half * 16 + 32 * i + j, dS[i][j]);
+    if (half * 16 + 32 * i < DK && vok) tile_put16(tdSt, MV, vrow, half * 16 + 32 * i, dS[i]);
 
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
@@ -136,18 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
     __syncthreads();
     const __nv_bfloat16* dOc = (const __nv_bfloat16*)p.dO + t0 * p.dO_ld + (int64_t)h * Dv;
     // dO^T and (scale e^G dO)^T: rows v, columns r
-    for (int idx = tid; idx < C * (Dv / 8); idx += kThreads) {
-      const int r = idx / (Dv / 8), v0 = (idx % (Dv / 8)) * 8;
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (r < len) raw = *(const uint4*)(dOc + (int64_t)r * p.dO_ld + v0);
-      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
-      const float sc = p.scale * ev[r];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        *(__nv_bfloat16*)(tdOt + tc::sw128_offset(v0 + u, r, MV)) = e[u];
-        tile_put(tdOet, MV, v0 + u, r, __bfloat162float(e[u]) * sc);
-      }
-    }
+    stage_bf16(dOc, C, Dv, p.dO_ld, len, nullptr, 0, nullptr, tdOt, MV, One());
+    stage_bf16(dOc, C, Dv, p.dO_ld, len, nullptr, 0, nullptr, tdOet, MV,
+               [&](int r) { return p.scale * ev[r]; });
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::mma_tile(tA1, tc::smem_u32(tdOt), MV, tc::smem_u32(tPt(b)), C, C, 0u);
@@ -164,14 +153,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
       tc::tmem_ld16(tA1 + lane_quarter() + col0, a1);
       tc::tmem_ld16(tA2 + lane_quarter() + col0, a2);
       tc::tmem_ld_wait();
-      if (vok)
+      if (vok) {
+        float md[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int s = col0 + j;
           const float d = s < len ? p.scale * a1[j] + cv[s] * a2[j] : 0.f;
-          tile_put(tmDt, MV, vrow, s, -d);
+          md[j] = -d;
           dDg[(size_t)s * Dv + vrow] = d;
         }
+        tile_put16(tmDt, MV, vrow, col0, md);
+      }
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
@@ -186,12 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
         float x[16];
         tc::tmem_ld16(tA3 + lane_quarter() + col0, x);
         tc::tmem_ld_wait();
-        if (vok)
+        if (vok) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            dS[ii][j] = fmaf(eC, dS[ii][j], x[j]);
-            tile_put(tdSt, MV, vrow, col0 + j, dS[ii][j]);
-          }
+          for (int j = 0; j < 16; ++j) dS[ii][j] = fmaf(eC, dS[ii][j], x[j]);
+          tile_put16(tdSt, MV, vrow, col0, dS[ii]);
+        }
       }
     }
     tc::fence_async_smem();
@@ -253,11 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
   uint8_t* tHs = R1 + 24576;
   // R2
   uint8_t* tA2 = R2;                               // [128][Dv]: rows 0-63 dO, 64-127 dDelta
-  float* X = (float*)R2;                           // [C][C] fp32 scratch
+  float* X = (float*)R2;                           // [C][C + 1] fp32 scratch (padded rows)
+  constexpr int XL = C + 1;
   // R3
   uint8_t* tW = R3;                                // [C][Dk]
   uint8_t* tdOe = R3 + 16384;                      // [C][Dv]
-  __nv_bfloat16* sU = (__nv_bfloat16*)(R3 + 32768);// [Dv][C]
+  uint8_t* sU = R3 + 32768;                        // [Dv][C] SW128 tile of U^T
   uint8_t* tdS = R3;                               // [Dk][Dv]
   uint8_t* tP = R3 + 32768;                        // [C][C]
   uint8_t* tdDt = R3;                              // [Dv][C]
@@ -351,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
     }
     __syncthreads();
     // ---- phase A: S, S^T, [dO; dDelta], scale e^G dO
-    stage_f32(S, Dk, Dv, Dv, Dk, tS, tSt, Dv, [](int) { return 1.f; });
+    stage_f32(S, Dk, Dv, Dv, Dk, tS, tSt, Dv, One(), One());
     stage_bf16(dOc, C, Dv, p.dO_ld, len, tA2, 128, tdOe, nullptr, 0,
                [&](int r) { return p.scale * ev[r]; });
     {
@@ -389,14 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
       float x[16];
       tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
       tc::tmem_ld_wait();
-      if (row64 >= 0)
+      if (row64 >= 0) {
+        float dc[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int v = q * 16 + j;
-          const float d = __bfloat162float(sU[v * C + row64]) - x[j];
-          tile_put(tDl, C, row64, v, d);
-          tile_put(tDlc, C, row64, v, d * cv[row64]);
+          x[j] = tile_get(sU, Dv, q * 16 + j, row64) - x[j];
+          dc[j] = x[j] * cv[row64];
         }
+        tile_put16(tDl, C, row64, q * 16, x);
+        tile_put16(tDlc, C, row64, q * 16, dc);
+      }
     }
     {
       const int row = acc_row(128);
@@ -411,9 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            tile_put(tdW, C, row - C, q * 16 + j, -x[j]);
-            tile_put(tdWt, Dk, q * 16 + j, row - C, -x[j]);
+            x[j] = -x[j];
+            tile_put(tdWt, Dk, q * 16 + j, row - C, x[j]);
           }
+          tile_put16(tdW, C, row - C, q * 16, x);
         }
       }
       if (row < C) part[half * C + row] = rs;
@@ -425,12 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
       tc::mbar_arrive_expect_tx(&bars[1], sCC);
       tc::bulk_g2s(tP, p.Psw + ch * sCC, sCC, &bars[1]);
     }
-    stage_f32(dSg, Dk, Dv, Dv, Dk, tdS, nullptr, 0, [](int) { return 1.f; });
-    stage_bf16(Vc, C, Dv, p.v_ld, len, tV, C, nullptr, nullptr, 0, [](int) { return 1.f; });
-    stage_f32(Kn, C, Dk, Dk, C, tKe, nullptr, 0, [&](int r) { return ev[r]; });
+    stage_f32(dSg, Dk, Dv, Dv, Dk, tdS, nullptr, 0, One(), One());
+    stage_bf16(Vc, C, Dv, p.v_ld, len, tV, C, nullptr, nullptr, 0, One());
+    stage_f32(Kn, C, Dk, Dk, C, tKe, nullptr, 0, [&](int r) { return ev[r]; }, One());
     {
       float sds = 0.f;
-      for (size_t e = tid; e < SZ; e += kThreads) sds = fmaf(S[e], dSg[e], sds);
+      const float4* S4 = (const float4*)S;
+      const float4* D4 = (const float4*)dSg;
+      for (size_t e = tid; e < SZ / 4; e += kThreads) {
+        const float4 a = S4[e], d = D4[e];
+        sds = fmaf(a.x, d.x, fmaf(a.y, d.y, fmaf(a.z, d.z, fmaf(a.w, d.w, sds))));
+      }
       sds = warp_sum(sds);
       if ((tid & 31) == 0) red[warp] = sds;
     }
@@ -474,24 +474,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
       tc::tmem_ld_wait();
       if (row64 >= 0) {
         const int r = row64;
+        float pv[16], pe[16];
+        tile_get16(tP, C, r, q * 16, pv);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int s = q * 16 + j;
           const float dP = (s <= r && r < len) ? p.scale * x[j] : 0.f;
           const float E = s <= r ? expf(gv[r] - gv[s]) : 0.f;
-          X[r * C + s] = dP * tile_get(tP, C, r, s);
-          tile_put(tdPE, C, r, s, dP * E);
-          tile_put(tdPEt, C, s, r, dP * E);
+          X[r * XL + s] = dP * pv[j];
+          pe[j] = dP * E;
+          tile_put(tdPEt, C, s, r, pe[j]);
           tile_put(tdTt, C, s, r, bv[s] * y[j]);   // dT[r][s] = b_s (...)
         }
+        tile_put16(tdPE, C, r, q * 16, pe);
       }
     }
     __syncthreads();
     if (tid < C) {
       const int t = tid;
       float rsum = 0.f, csum = 0.f;
-      for (int s = 0; s < C; ++s) rsum += X[t * C + s];
-      for (int r = 0; r < C; ++r) csum += X[r * C + t];
+      for (int s = 0; s < C; ++s) rsum += X[t * XL + s];
+      for (int r = 0; r < C; ++r) csum += X[r * XL + t];
       dG[t] += rsum - csum - (part[t] + part[C + t]);
     }
     __syncthreads();
@@ -502,15 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
       dG[len - 1] += expf(gv[len - 1]) * tot + sc;
     }
     // ---- phase C: dDelta^T, T^T, T, b e^G T^T
-    stage_f32(dDg, C, Dv, Dv, C, nullptr, tdDt, Dv, [](int) { return 1.f; });
-    stage_f32(Tg, C, C, C, C, tT, tTt, C, [](int) { return 1.f; });
-    stage_f32(Tg, C, C, C, C, nullptr, tTbe, C, [&](int r) { return 1.f; });
-    __syncthreads();
-    // b e^G T^T: scale row s of tTbe (= column s of T) by b_s e^{G_s}
-    for (int idx = tid; idx < C * C; idx += kThreads) {
-      const int s = idx / C, r = idx % C;
-      tile_put(tTbe, C, s, r, tile_get(tTbe, C, s, r) * bv[s] * ev[s]);
-    }
+    stage_f32(dDg, C, Dv, Dv, C, nullptr, tdDt, Dv, One(), One());
+    stage_f32(Tg, C, C, C, C, tT, tTt, C, One(), One());
+    // b e^G T^T: row s of the transposed tile (column s of T) scaled by b_s e^{G_s}
+    stage_f32(Tg, C, C, C, C, nullptr, tTbe, C, One(), [&](int s) { return bv[s] * ev[s]; });
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::mma_tile(tdQ, tc::smem_u32(tdPE), 64, tc::smem_u32(tKt), Dk, C, 1u);      // dQ += dPE K
@@ -545,9 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
         float x[16];
         tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
-        if (row64 >= 0)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) tile_put(tY, C, row64, q * 16 + j, x[j]);
+        if (row64 >= 0) tile_put16(tY, C, row64, q * 16, x);
       }
     }
     __syncthreads();
@@ -579,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int s = q * 16 + j;
-            X[row64 * C + s] = s < row64 ? -x[j] : 0.f;
+            X[row64 * XL + s] = s < row64 ? -x[j] : 0.f;
           }
       }
     }
@@ -592,19 +588,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
       // A[r][s] = b_r E_rs KK_rs (s < r): db_r += sum_s dA E KK, dG_r += sum_s dA*A, dG_s -= sum_r dA*A
       float rdb = 0.f, ry = 0.f, cy = 0.f;
       for (int s = 0; s < t; ++s) {
-        const float q = X[t * C + s] * expf(gv[t] - gv[s]) * KK[t * C + s];
+        const float q = X[t * XL + s] * expf(gv[t] - gv[s]) * KK[t * C + s];
         rdb += q;
         ry += q * bv[t];
       }
-      for (int r = t + 1; r < C; ++r) cy += X[r * C + t] * expf(gv[r] - gv[t]) * KK[r * C + t] * bv[r];
+      for (int r = t + 1; r < C; ++r) cy += X[r * XL + t] * expf(gv[r] - gv[t]) * KK[r * C + t] * bv[r];
       db[t] += rdb;
       dG[t] += ry - cy;
     }
     // H = dA * b_r E; Hs = H + H^T
     for (int idx = tid; idx < C * C; idx += kThreads) {
       const int s = idx / C, r = idx % C;
-      const float h1 = r < s ? X[s * C + r] * bv[s] * expf(gv[s] - gv[r]) : 0.f;
-      const float h2 = s < r ? X[r * C + s] * bv[r] * expf(gv[r] - gv[s]) : 0.f;
+      const float h1 = r < s ? X[s * XL + r] * bv[s] * expf(gv[s] - gv[r]) : 0.f;
+      const float h2 = s < r ? X[r * XL + s] * bv[r] * expf(gv[r] - gv[s]) : 0.f;
       tile_put(tHs, C, s, r, h1 + h2);
     }
     tc::fence_async_smem();

@@ -141,33 +141,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
 
   // 1. L2-normalise q and k rows into the operand tiles.
   const size_t ck = ((size_t)c * p.Hk + kh) * C;
-  for (int row = warp; row < 2 * C; row += kThreads / 32) {
-    const bool isq = row >= C;
-    const int t = row & (C - 1);
-    const __nv_bfloat16* src = (const __nv_bfloat16*)(isq ? p.q : p.k) +
-                               (t0 + t) * (isq ? p.q_ld : p.k_ld) + (int64_t)kh * Dk;
-    float x[4];
-    float ss = 0.f;
+  // each warp normalises rows warp, warp + 8, ..., loading 8 rows before reducing
+  for (int g = 0; g < 2; ++g) {
+    float x[8][4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = lane + 32 * u;
-      x[u] = (t < len && i < Dk) ? __bfloat162float(src[i]) : 0.f;
-      ss = fmaf(x[u], x[u], ss);
-    }
-    ss = warp_sum(ss);
-    const float nrm = sqrtf(ss + 1e-6f);
+    for (int rr = 0; rr < 8; ++rr) {
+      const int row = warp + 8 * (8 * g + rr);
+      const bool isq = row >= C;
+      const int t = row & (C - 1);
+      const __nv_bfloat16* src = (const __nv_bfloat16*)(isq ? p.q : p.k) +
+                                 (t0 + t) * (isq ? p.q_ld : p.k_ld) + (int64_t)kh * Dk;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = lane + 32 * u;
-      if (i < Dk) {
-        const float xh = x[u] / nrm;
-        tile_put(tAQK, 128, row, i, xh);
-        if (!isq) tile_put(tKt, MK, i, t, xh);
-        else if (bwd) tile_put(tQt, MK, i, t, xh);
-        if (bwd) (isq ? p.Qn : p.Kn)[(ck + t) * Dk + i] = xh;
+      for (int u = 0; u < 4; ++u) {
+        const int i = lane + 32 * u;
+        x[rr][u] = (t < len && i < Dk) ? __bfloat162float(src[i]) : 0.f;
       }
     }
-    if (bwd && lane == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      const int row = warp + 8 * (8 * g + rr);
+      const bool isq = row >= C;
+      const int t = row & (C - 1);
+      float ss = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ss = fmaf(x[rr][u], x[rr][u], ss);
+      ss = warp_sum(ss);
+      const float nrm = sqrtf(ss + 1e-6f);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = lane + 32 * u;
+        if (i < Dk) {
+          const float xh = x[rr][u] / nrm;
+          tile_put(tAQK, 128, row, i, xh);
+          if (!isq) tile_put(tKt, MK, i, t, xh);
+          else if (bwd) tile_put(tQt, MK, i, t, xh);
+          if (bwd) (isq ? p.Qn : p.Kn)[(ck + t) * Dk + i] = xh;
+        }
+      }
+      if (bwd && lane == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
+    }
   }
   tc::fence_async_smem();
   // 2. [K; Q] K^T -> TMEM columns [0, 64): lanes 0-63 K K^T, lanes 64-127 Q K^T.
@@ -179,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
     float* dst = row < C ? KK + row * C : QK + (row - C) * C;
 #pragma unroll
     for (int j = 0; j < 16; ++j) dst[col0 + j] = v[j];
-    if (bwd) {
-      float* g = (row < C ? p.KKf + (ck + row) * C : p.QKf + (ck + row - C) * C) + col0;
+    if (bwd && row < C) {
+      float* g = p.KKf + (ck + row) * C + col0;
 #pragma unroll
       for (int j = 0; j < 16; ++j) g[j] = v[j];
     }
@@ -260,9 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
           return s <= r ? expf(G[r] - G[s]) * QK[r * C + s] : 0.f;
         });
       const __nv_bfloat16* Vs = (const __nv_bfloat16*)p.v + t0 * p.v_ld + (int64_t)h * Dv;
-      stage_tile(tVt, Dv, C, [&](int vv, int s) {
-        return s < len ? __bfloat162float(Vs[(int64_t)s * p.v_ld + vv]) : 0.f;
-      });
+      stage_bf16(Vs, C, Dv, p.v_ld, len, nullptr, 0, nullptr, tVt, MV, One());
       tc::fence_async_smem();
       ok = mma_run([&] {
         tc::mma_tile(tmem + 64, tc::smem_u32(tKt), MK, tc::smem_u32(tTW), C, C, 0u);
@@ -271,24 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
       if (!ok) goto done;
       acc_walk(tmem + 64, MK, 64, Dk, [&](int k, int col0, const float* v) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          tile_put(tOW, C, col0 + j, k, v[j]);
-          if (bwd) {
-            tile_put(tOWt, Dk, k, col0 + j, v[j]);
-            p.W[(ch * C + col0 + j) * Dk + k] = v[j];
-          }
-        }
+        for (int j = 0; j < 16; ++j) tile_put(tOW, C, col0 + j, k, v[j]);
+        if (bwd) tile_put16(tOWt, Dk, k, col0, v);
       });
       acc_walk(tmem + 128, MV, 64, Dv, [&](int vv, int col0, const float* v) {
-        __align__(16) __nv_bfloat162 pk[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) pk[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-        uint4* dst = (uint4*)(p.Utb + (ch * Dv + vv) * C + col0);
-        dst[0] = ((const uint4*)pk)[0];
-        dst[1] = ((const uint4*)pk)[1];
-        if (bwd)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) p.U[(ch * C + col0 + j) * Dv + vv] = v[j];
+        // U^T as a [Dv][C] SW128 tile, so that row reads by the state walks are conflict-free
+        tile_put16((uint8_t*)(p.Utb + ch * Dv * C), Dv, vv, col0, v);
       });
       if (bwd)
         for (int i = tid; i < C * C; i += kThreads) p.Tm[ch * C * C + i] = T[i];
@@ -376,9 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     }
 #pragma unroll
   for (int i = 0; i < NKC; ++i)
-    if (half * 16 + 32 * i < DK && vok)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) tile_put(tSt, MV, vrow, half * 16 + 32 * i + j, S[i][j]);
+    if (half * 16 + 32 * i < DK && vok) tile_put16(tSt, MV, vrow, half * 16 + 32 * i, S[i]);
 
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
@@ -431,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     if (!ok) break;
     // Delta^T = U^T - X^T; keep S^T Q^T for the output
     float o1[2][16];
-    const __nv_bfloat16* U = sU(b);
+    const uint8_t* U = (const uint8_t*)sU(b);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int col0 = half * 16 + 32 * q;
@@ -440,12 +436,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
       tc::tmem_ld16(tO1 + lane_quarter() + col0, o1[q]);
       tc::tmem_ld_wait();
       if (vok) {
+        float u[16], dc[16];
+        tile_get16(U, Dv, vrow, col0, u);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float d = __bfloat162float(U[vrow * C + col0 + j]) - x[j];
-          tile_put(tDt, MV, vrow, col0 + j, d);
-          tile_put(tDct, MV, vrow, col0 + j, d * cv[col0 + j]);
+          x[j] = u[j] - x[j];
+          dc[j] = x[j] * cv[col0 + j];
         }
+        tile_put16(tDt, MV, vrow, col0, x);
+        tile_put16(tDct, MV, vrow, col0, dc);
       }
     }
     tc::fence_async_smem();
@@ -479,12 +478,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
         float x[16];
         tc::tmem_ld16(tS + lane_quarter() + col0, x);
         tc::tmem_ld_wait();
-        if (vok)
+        if (vok) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            S[ii][j] = fmaf(eC, S[ii][j], x[j]);
-            tile_put(tSt, MV, vrow, col0 + j, S[ii][j]);
-          }
+          for (int j = 0; j < 16; ++j) S[ii][j] = fmaf(eC, S[ii][j], x[j]);
+          tile_put16(tSt, MV, vrow, col0, S[ii]);
+        }
       }
     }
     tc::fence_async_smem();
