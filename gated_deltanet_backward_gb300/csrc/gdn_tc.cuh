@@ -64,32 +64,40 @@ __device__ __forceinline__ void stage_tile(uint8_t* tile, int rows, int cols, F 
 template <class RS, class CS>
 __device__ __forceinline__ void stage_f32(const float* M, int R, int Cc, int64_t ld, int valid,
                                           uint8_t* tn, uint8_t* tt, int tt_rows, RS rs, CS cs) {
-  const int cpr = Cc >> 3;
-  for (int idx = threadIdx.x; idx < R * cpr; idx += blockDim.x) {
-    const int r = idx % R, c0 = (idx / R) << 3;
-    float v[8];
-    if (r < valid) {
-      const float4 a = *(const float4*)(M + (int64_t)r * ld + c0);
-      const float4 b = *(const float4*)(M + (int64_t)r * ld + c0 + 4);
-      const float s = rs(r);
-      v[0] = a.x * s; v[1] = a.y * s; v[2] = a.z * s; v[3] = a.w * s;
-      v[4] = b.x * s; v[5] = b.y * s; v[6] = b.z * s; v[7] = b.w * s;
+  const int cpr = Cc >> 3, total = R * cpr;
+  // four items per thread per batch: all loads are issued before any store
+  for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
+    float4 a[4], b[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] *= cs(c0 + u);
-    } else {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = 0.f;
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * blockDim.x;
+      const int r = idx % R, c0 = (idx / R) << 3;
+      a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (idx < total && r < valid) {
+        a[u] = *(const float4*)(M + (int64_t)r * ld + c0);
+        b[u] = *(const float4*)(M + (int64_t)r * ld + c0 + 4);
+      }
     }
-    if (tn) {
-      __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) pk[u] = __floats2bfloat162_rn(v[2 * u], v[2 * u + 1]);
-      *(uint4*)(tn + tc::sw128_offset(r, c0, R)) = *(const uint4*)pk;
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx >= total) break;
+      const int r = idx % R, c0 = (idx / R) << 3;
+      const float s = r < valid ? rs(r) : 0.f;
+      float v[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] *= s * cs(c0 + e);
+      if (tn) {
+        __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[e] = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        *(uint4*)(tn + tc::sw128_offset(r, c0, R)) = *(const uint4*)pk;
+      }
+      if (tt)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + e, r, tt_rows)) = __float2bfloat16_rn(v[e]);
     }
-    if (tt)
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + u, r, tt_rows)) = __float2bfloat16_rn(v[u]);
   }
 }
 struct One {
@@ -103,28 +111,39 @@ template <class RS>
 __device__ __forceinline__ void stage_bf16(const __nv_bfloat16* M, int R, int Cc, int64_t ld,
                                            int valid, uint8_t* tn, int tn_rows, uint8_t* tn2,
                                            uint8_t* tt, int tt_rows, RS rs) {
-  const int cpr = Cc >> 3;
-  for (int idx = threadIdx.x; idx < R * cpr; idx += blockDim.x) {
-    const int r = idx % R, c0 = (idx / R) << 3;
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (r < valid) raw = *(const uint4*)(M + (int64_t)r * ld + c0);
-    if (tn) *(uint4*)(tn + tc::sw128_offset(r, c0, tn_rows)) = raw;
-    if (tn2 || tt) {
-      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
-      const float s = rs(r);
-      if (tn2) {
-        __align__(16) __nv_bfloat162 pk[4];
+  const int cpr = Cc >> 3, total = R * cpr;
+  for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
+    uint4 raw[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          pk[u] = __floats2bfloat162_rn(__bfloat162float(e[2 * u]) * s,
-                                        __bfloat162float(e[2 * u + 1]) * s);
-        *(uint4*)(tn2 + tc::sw128_offset(r, c0, R)) = *(const uint4*)pk;
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * blockDim.x;
+      const int r = idx % R, c0 = (idx / R) << 3;
+      raw[u] = make_uint4(0, 0, 0, 0);
+      if (idx < total && r < valid) raw[u] = *(const uint4*)(M + (int64_t)r * ld + c0);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx >= total) break;
+      const int r = idx % R, c0 = (idx / R) << 3;
+      if (tn) *(uint4*)(tn + tc::sw128_offset(r, c0, tn_rows)) = raw[u];
+      if (tn2 || tt) {
+        const __nv_bfloat16* e = (const __nv_bfloat16*)&raw[u];
+        const float s = rs(r);
+        if (tn2) {
+          __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            pk[q] = __floats2bfloat162_rn(__bfloat162float(e[2 * q]) * s,
+                                          __bfloat162float(e[2 * q + 1]) * s);
+          *(uint4*)(tn2 + tc::sw128_offset(r, c0, R)) = *(const uint4*)pk;
+        }
+        if (tt)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + q, r, tt_rows)) =
+                __float2bfloat16_rn(__bfloat162float(e[q]) * s);
       }
-      if (tt)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *(__nv_bfloat16*)(tt + tc::sw128_offset(c0 + u, r, tt_rows)) =
-              __float2bfloat16_rn(__bfloat162float(e[u]) * s);
     }
   }
 }

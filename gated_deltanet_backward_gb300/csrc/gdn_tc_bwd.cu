@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
   // R4
   uint8_t* tV = R4;                                // [C][Dv]
   uint8_t* tKe = R4 + 16384;                       // [C][Dk]
+  float* sKK = (float*)R4;                         // [C][C] fp32 K K^T (phase D)
   // R5
   uint8_t* tKt = R5;                               // [Dk][C]
   uint8_t* tQt = R5 + 16384;                       // [Dk][C]
@@ -548,6 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
     }
     __syncthreads();
     if (tid < C) db[tid] += part[tid] + part[C + tid];
+    // K K^T into shared memory (R4 is free once epilogue C has read V)
+    for (int i = tid; i < C * C / 4; i += kThreads) ((float4*)sKK)[i] = ((const float4*)KK)[i];
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::mma_tile(tmp, tc::smem_u32(tTt), 64, tc::smem_u32(tdWt), Dk, C, 0u);    // dBk = T^T dW
@@ -588,11 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
       // A[r][s] = b_r E_rs KK_rs (s < r): db_r += sum_s dA E KK, dG_r += sum_s dA*A, dG_s -= sum_r dA*A
       float rdb = 0.f, ry = 0.f, cy = 0.f;
       for (int s = 0; s < t; ++s) {
-        const float q = X[t * XL + s] * expf(gv[t] - gv[s]) * KK[t * C + s];
+        const float q = X[t * XL + s] * expf(gv[t] - gv[s]) * sKK[t * C + s];
         rdb += q;
         ry += q * bv[t];
       }
-      for (int r = t + 1; r < C; ++r) cy += X[r * XL + t] * expf(gv[r] - gv[t]) * KK[r * C + t] * bv[r];
+      for (int r = t + 1; r < C; ++r) cy += X[r * XL + t] * expf(gv[r] - gv[t]) * sKK[r * C + t] * bv[r];
       db[t] += rdb;
       dG[t] += ry - cy;
     }

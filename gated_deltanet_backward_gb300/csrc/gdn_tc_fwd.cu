@@ -33,26 +33,28 @@ __device__ __forceinline__ size_t tileDC(int D) { return (size_t)D * 128; }
 // forward substitution, then block rows 1..3: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
 __device__ void tri_inverse(float* Tm, int nh, float* Mt) {
   const int tid = threadIdx.x;
-  // diagonal blocks
+  // diagonal blocks: one warp per (head, block); lane j < 16 keeps column j of the
+  // block inverse in registers (forward substitution, no block-wide barriers)
   {
-    const int hh = tid / 64, blk = (tid / 16) & 3, j = tid & 15;
-    float* T = Tm + hh * C * C;
-    for (int rr = 0; rr < 16; ++rr) {
-      float val = 0.f;
-      if (hh < nh) {
-        const int R = blk * 16 + rr, J = blk * 16 + j;
-        if (j == rr) {
-          val = 1.f;
-        } else if (j < rr) {
-          float acc = 0.f;
-          for (int s = j; s < rr; ++s) acc = fmaf(T[R * C + blk * 16 + s], T[(blk * 16 + s) * C + J], acc);
-          val = -acc;
-        }
+    const int warp = tid >> 5, lane = tid & 31, j = lane & 15;
+    for (int unit = warp; unit < nh * 4; unit += blockDim.x / 32) {
+      const int hh = unit >> 2, blk = unit & 3;
+      float* T = Tm + hh * C * C + blk * 16 * C + blk * 16;   // block origin
+      float col[16];
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        float acc = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < rr; ++s2) acc = fmaf(T[rr * C + s2], col[s2], acc);
+        col[rr] = rr == j ? 1.f : (rr > j ? -acc : 0.f);
       }
-      __syncthreads();
-      if (hh < nh) T[(blk * 16 + rr) * C + blk * 16 + j] = val;
-      __syncthreads();
+      __syncwarp();
+      if (lane < 16)
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) T[rr * C + j] = col[rr];
+      __syncwarp();
     }
+    __syncthreads();
   }
   // block rows
   for (int bi = 1; bi < 4; ++bi) {
@@ -141,45 +143,69 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
 
   // 1. L2-normalise q and k rows into the operand tiles.
   const size_t ck = ((size_t)c * p.Hk + kh) * C;
-  // each warp normalises rows warp, warp + 8, ..., loading 8 rows before reducing
-  for (int g = 0; g < 2; ++g) {
-    float x[8][4];
+  // 16-byte loads: a row of Dk elements is Dk/8 consecutive threads; 8 (Dk = 128) row
+  // chunks per thread, all loaded before the sums of squares are reduced.
+  {
+    const int lpr = Dk / 8;                       // threads per row (2..16)
+    const int total = 2 * C * lpr;                 // chunks of the 128 rows
+    for (int base = 0; base < total; base += 8 * kThreads) {
+      uint4 raw[8];
 #pragma unroll
-    for (int rr = 0; rr < 8; ++rr) {
-      const int row = warp + 8 * (8 * g + rr);
-      const bool isq = row >= C;
-      const int t = row & (C - 1);
-      const __nv_bfloat16* src = (const __nv_bfloat16*)(isq ? p.q : p.k) +
-                                 (t0 + t) * (isq ? p.q_ld : p.k_ld) + (int64_t)kh * Dk;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = lane + 32 * u;
-        x[rr][u] = (t < len && i < Dk) ? __bfloat162float(src[i]) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int rr = 0; rr < 8; ++rr) {
-      const int row = warp + 8 * (8 * g + rr);
-      const bool isq = row >= C;
-      const int t = row & (C - 1);
-      float ss = 0.f;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) ss = fmaf(x[rr][u], x[rr][u], ss);
-      ss = warp_sum(ss);
-      const float nrm = sqrtf(ss + 1e-6f);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = lane + 32 * u;
-        if (i < Dk) {
-          const float xh = x[rr][u] / nrm;
-          tile_put(tAQK, 128, row, i, xh);
-          if (!isq) tile_put(tKt, MK, i, t, xh);
-          else if (bwd) tile_put(tQt, MK, i, t, xh);
-          if (bwd) (isq ? p.Qn : p.Kn)[(ck + t) * Dk + i] = xh;
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + u * kThreads + tid;
+        raw[u] = make_uint4(0, 0, 0, 0);
+        const int row = idx / lpr, c0 = (idx % lpr) * 8;
+        const int t = row & (C - 1);
+        if (idx < total && t < len) {
+          const bool isq = row >= C;
+          const __nv_bfloat16* src = (const __nv_bfloat16*)(isq ? p.q : p.k) +
+                                     (t0 + t) * (isq ? p.q_ld : p.k_ld) + (int64_t)kh * Dk;
+          raw[u] = *(const uint4*)(src + c0);
         }
       }
-      if (bwd && lane == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + u * kThreads + tid;
+        const int row = idx / lpr, c0 = (idx % lpr) * 8;
+        const __nv_bfloat16* e = (const __nv_bfloat16*)&raw[u];
+        float x[8], ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          x[q] = __bfloat162float(e[q]);
+          ss = fmaf(x[q], x[q], ss);
+        }
+        for (int o = lpr >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (idx < total) {
+          const bool isq = row >= C;
+          const int t = row & (C - 1);
+          const float nrm = sqrtf(ss + 1e-6f), inv = 1.f / nrm;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[q] = x[q] / nrm;
+          __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) pk[q] = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
+          *(uint4*)(tAQK + tc::sw128_offset(row, c0, 128)) = *(const uint4*)pk;
+          if (bwd) {
+            float* dst = (isq ? p.Qn : p.Kn) + (ck + t) * Dk + c0;
+            *(float4*)dst = make_float4(x[0], x[1], x[2], x[3]);
+            *(float4*)(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            if (c0 == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
+          }
+          (void)inv;
+        }
+      }
     }
+  }
+  __syncthreads();
+  // K^T (and Q^T) tiles from the natural rows: thread (k, chunk of 8 tokens)
+  for (int idx = tid; idx < (bwd ? 2 : 1) * Dk * (C / 8); idx += kThreads) {
+    const int which = idx / (Dk * (C / 8)), rem = idx % (Dk * (C / 8));
+    const int kk = rem % Dk, t8 = (rem / Dk) * 8;
+    __align__(16) __nv_bfloat16 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      v[q] = *(const __nv_bfloat16*)(tAQK + tc::sw128_offset(which * C + t8 + q, kk, 128));
+    *(uint4*)((which ? tQt : tKt) + tc::sw128_offset(kk, t8, MK)) = *(const uint4*)v;
   }
   tc::fence_async_smem();
   // 2. [K; Q] K^T -> TMEM columns [0, 64): lanes 0-63 K K^T, lanes 64-127 Q K^T.
