@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "gdn_internal.cuh"
 
@@ -177,6 +178,38 @@ thread_local ProfileState g_profile;
 
 namespace gdn {
 
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  });
+  return fn;
+}
+}  // namespace
+
+bool encode_tma_2d(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Lets other translation units of the library explain a failure through
 // gdn_last_error().
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
@@ -298,7 +331,18 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
            : cudaMemsetAsync(S_T, 0, bytes, st);
     return e == cudaSuccess ? GDN_OK : cuda_fail("gdn_forward: S_T of empty sequences", e);
   }
-  e = gdn::launch_forward(p, s->dtype == GDN_DTYPE_BF16, st);
+  gdn::TmaMaps maps;
+  const bool bf16 = s->dtype == GDN_DTYPE_BF16;
+  if (bf16 && s->total_tokens > 0) {
+    const int64_t T = s->total_tokens;
+    if (!gdn::encode_tma_2d(&maps.q, q, (int64_t)s->Hk * s->Dk, T, q_ld) ||
+        !gdn::encode_tma_2d(&maps.k, k, (int64_t)s->Hk * s->Dk, T, k_ld) ||
+        !gdn::encode_tma_2d(&maps.v, v, (int64_t)s->Hv * s->Dv, T, v_ld)) {
+      snprintf(g_last_error, sizeof(g_last_error), "gdn_forward: cuTensorMapEncodeTiled failed");
+      return GDN_ERR_CUDA;
+    }
+  }
+  e = gdn::launch_forward(p, bf16 ? &maps : nullptr, st);
   if (e != cudaSuccess) return cuda_fail("gdn_forward: kernel launch", e);
   return GDN_OK;
 }
@@ -360,7 +404,19 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
              : cudaMemsetAsync(dS0, 0, bytes, st);
     if (e != cudaSuccess) return cuda_fail("gdn_backward: dS_0 of empty sequences", e);
   }
-  e = gdn::launch_backward(p, s->dtype == GDN_DTYPE_BF16, st);
+  gdn::TmaMaps maps;
+  const bool bf16 = s->dtype == GDN_DTYPE_BF16;
+  if (bf16 && s->total_tokens > 0) {
+    const int64_t T = s->total_tokens;
+    if (!gdn::encode_tma_2d(&maps.q, q, (int64_t)s->Hk * s->Dk, T, q_ld) ||
+        !gdn::encode_tma_2d(&maps.k, k, (int64_t)s->Hk * s->Dk, T, k_ld) ||
+        !gdn::encode_tma_2d(&maps.v, v, (int64_t)s->Hv * s->Dv, T, v_ld) ||
+        !gdn::encode_tma_2d(&maps.dO, dO, (int64_t)s->Hv * s->Dv, T, dO_ld)) {
+      snprintf(g_last_error, sizeof(g_last_error), "gdn_backward: cuTensorMapEncodeTiled failed");
+      return GDN_ERR_CUDA;
+    }
+  }
+  e = gdn::launch_backward(p, bf16 ? &maps : nullptr, st);
   if (e != cudaSuccess) return cuda_fail("gdn_backward: kernel launch", e);
   return GDN_OK;
 }

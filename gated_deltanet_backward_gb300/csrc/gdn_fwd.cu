@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) k_fwd_state(Params p, int DVS) {
     float* sv = p.saved + ch * SZ;
     for (int idx = threadIdx.x; idx < Dk * DVS; idx += kThreads) {
       const int kk = idx / DVS, j = idx % DVS;
-      sv[(size_t)kk * Dv + v0 + j] = S[idx];
+      sv[(size_t)(v0 + j) * Dk + kk] = S[idx];   // saved transposed: [Dv][Dk]
     }
     if (threadIdx.x < C) gv[threadIdx.x] = p.G[ch * C + threadIdx.x];
     __syncthreads();
@@ -219,10 +219,11 @@ cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t s
   return cudaGetLastError();
 }
 
-cudaError_t launch_forward(const Params& p, bool bf16, cudaStream_t st) {
+cudaError_t launch_forward(const Params& p, const TmaMaps* maps, cudaStream_t st) {
+  const bool bf16 = maps != nullptr;
   if (bf16) {
     // bf16 inputs: tensor-core chunk preparation and state walk
-    cudaError_t e = launch_prep_tc(p, false, st);
+    cudaError_t e = launch_prep_tc(p, *maps, false, st);
     if (e != cudaSuccess) return e;
     return launch_fwd_state_tc(p, st);
   }

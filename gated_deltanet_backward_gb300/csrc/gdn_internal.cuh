@@ -13,6 +13,7 @@
 // K, Q are the L2-normalised keys / queries of key head h / v_repeat.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -204,14 +205,25 @@ enum KernelId {
 void profile_pre(cudaStream_t st, int kernel_id);
 void profile_post(cudaStream_t st);
 
+// TMA tensor maps of the bf16 row-major inputs: 2-D (columns, tokens), boxes of
+// 64 columns x 64 tokens, 128-byte swizzle (the K-major SW128 operand layout),
+// out-of-range rows and columns read as zero.
+struct TmaMaps {
+  CUtensorMap q, k, v, dO;
+};
+
+// Encodes `m` over a [rows, ld] bf16 matrix of which the first `cols` columns are
+// used.  Returns false if the driver rejects it.
+bool encode_tma_2d(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld);
+
 // Tensor-core (bf16) launchers.
-cudaError_t launch_prep_tc(const Params& p, bool bwd, cudaStream_t st);
+cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st);
 cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st);
-cudaError_t launch_bwd_tc(const Params& p, cudaStream_t st);
+cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st);
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t st);
-cudaError_t launch_forward(const Params& p, bool bf16, cudaStream_t st);
-cudaError_t launch_backward(const Params& p, bool bf16, cudaStream_t st);
+cudaError_t launch_forward(const Params& p, const TmaMaps* maps, cudaStream_t st);
+cudaError_t launch_backward(const Params& p, const TmaMaps* maps, cudaStream_t st);
 
 }  // namespace gdn

@@ -25,7 +25,8 @@ __device__ __forceinline__ size_t tileDC(int D) { return (size_t)D * 128; }
 
 // ---------------------------------------------------------------------------
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
+                                                               const __grid_constant__ TmaMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int n = blockIdx.x, h = blockIdx.y, kh = h / p.r;
@@ -39,23 +40,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
   const uint32_t bK = (uint32_t)tileCD(DK), bKt = (uint32_t)tileDC(DK), bP = 8192, bG = C * 4;
+  const int nbv = (Dv + 63) / 64;
+  const uint32_t bO = (uint32_t)nbv * 8192;                  // natural dO tile [C][Dv]
   uint8_t* tdSt = sm;                                        // [MV][DK]
   uint8_t* tdOt = tdSt + tc::sw128_bytes(MV, DK);            // [MV][C] dO^T
-  uint8_t* tdOet = tdOt + MV * 128;                          // [MV][C] (scale e^G dO)^T
-  uint8_t* tmDt = tdOet + MV * 128;                          // [MV][C] -dDelta^T
+  uint8_t* tmDt = tdOt + MV * 128;                           // [MV][C] -dDelta^T
   uint8_t* buf0 = tmDt + MV * 128;
-  const uint32_t bufsz = bK + bP + 2 * bKt + 1024;
+  const uint32_t bufsz = bO + bK + bP + 2 * bKt + 1024;
   float* ev = (float*)(buf0 + 2 * bufsz);
   float* cv = ev + C;
   uint64_t* bars = (uint64_t*)(cv + C);
   uint32_t* tslot = (uint32_t*)(bars + 3);
-  auto tK = [&](int b) { return buf0 + b * bufsz; };
-  auto tPt = [&](int b) { return buf0 + b * bufsz + bK; };
-  auto tQt = [&](int b) { return buf0 + b * bufsz + bK + bP; };
-  auto tWt = [&](int b) { return buf0 + b * bufsz + bK + bP + bKt; };
-  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + bK + bP + 2 * bKt); };
+  // per stage buffer: natural dO tile (TMA; reused for (scale e^G dO)^T), K, P^T, Q^T, W^T, G
+  auto sdO = [&](int b) { return buf0 + b * bufsz; };
+  auto tK = [&](int b) { return buf0 + b * bufsz + bO; };
+  auto tPt = [&](int b) { return buf0 + b * bufsz + bO + bK; };
+  auto tQt = [&](int b) { return buf0 + b * bufsz + bO + bK + bP; };
+  auto tWt = [&](int b) { return buf0 + b * bufsz + bO + bK + bP + bKt; };
+  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + bO + bK + bP + 2 * bKt); };
 
-  for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) + 3 * MV * 128) / 16; i += kThreads)
+  for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) + 2 * MV * 128) / 16; i += kThreads)
     ((uint4*)tdSt)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     tc::mbar_init(&bars[0], 1);
@@ -92,7 +96,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
     const size_t chh = (size_t)cc * p.Hv + h, ckk = (size_t)cc * p.Hk + kh;
-    tc::mbar_arrive_expect_tx(lb, bK + bP + 2 * bKt + bG);
+    tc::mbar_arrive_expect_tx(lb, bO + bK + bP + 2 * bKt + bG);
+    for (int b2 = 0; b2 < nbv; ++b2)
+      tc::tma_load_2d(sdO(b) + b2 * 8192, &maps.dO, h * Dv + 64 * b2,
+                      (int)(s0 + (int64_t)(cc - c0) * C), lb);
     tc::bulk_g2s(tK(b), p.Ksw + ckk * bK, bK, lb);
     tc::bulk_g2s(tPt(b), p.Ptsw + chh * bP, bP, lb);
     tc::bulk_g2s(tQt(b), p.Qtsw + ckk * bKt, bKt, lb);
@@ -132,11 +139,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
       cv[tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
     }
     __syncthreads();
-    const __nv_bfloat16* dOc = (const __nv_bfloat16*)p.dO + t0 * p.dO_ld + (int64_t)h * Dv;
-    // dO^T and (scale e^G dO)^T: rows v, columns r
-    stage_bf16(dOc, C, Dv, p.dO_ld, len, nullptr, 0, nullptr, tdOt, MV, One());
-    stage_bf16(dOc, C, Dv, p.dO_ld, len, nullptr, 0, nullptr, tdOet, MV,
-               [&](int r) { return p.scale * ev[r]; });
+    // dO^T (rows v, columns r) from the natural dO tile; rows past the chunk are zero
+    for (int idx = tid; idx < Dv * (C / 8); idx += kThreads) {
+      const int vv = idx % Dv, r8 = (idx / Dv) * 8;
+      __align__(16) __nv_bfloat16 e[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        e[q] = r8 + q < len ? *(const __nv_bfloat16*)(sdO(b) + tc::sw128_offset(r8 + q, vv, C))
+                            : __float2bfloat16(0.f);
+      *(uint4*)(tdOt + tc::sw128_offset(vv, r8, MV)) = *(const uint4*)e;
+    }
+    __syncthreads();
+    // (scale e^G dO)^T over the natural tile's space (no longer read)
+    uint8_t* tdOet = sdO(b);
+    for (int idx = tid; idx < Dv * (C / 8); idx += kThreads) {
+      const int vv = idx % Dv, r8 = (idx / Dv) * 8;
+      const uint4 raw = *(const uint4*)(tdOt + tc::sw128_offset(vv, r8, MV));
+      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
+      __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        pk[q] = __floats2bfloat162_rn(__bfloat162float(e[2 * q]) * p.scale * ev[r8 + 2 * q],
+                                      __bfloat162float(e[2 * q + 1]) * p.scale * ev[r8 + 2 * q + 1]);
+      *(uint4*)(tdOet + tc::sw128_offset(vv, r8, MV)) = *(const uint4*)pk;
+    }
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::mma_tile(tA1, tc::smem_u32(tdOt), MV, tc::smem_u32(tPt(b)), C, C, 0u);
@@ -211,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p) {
 //   R4 32K  B-C: V [C][Dv], e^G K [C][Dk]
 //   R5 32K  K^T, Q^T [Dk][C] of the key head (whole CTA)
 // TMEM (512 columns): dQ_hat @0, dK_hat @128 (M = 64 accumulators), scratch @256.
-__global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
+                                                               const __grid_constant__ TmaMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int c = blockIdx.x, kh = blockIdx.y;
@@ -322,8 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
     const float* dSg = p.dS + ch * SZ;
     const float* dDg = p.dD + ch * C * Dv;
     const float* Tg = p.Tm + ch * C * C;
-    const __nv_bfloat16* dOc = (const __nv_bfloat16*)p.dO + t0 * p.dO_ld + (int64_t)h * Dv;
-    const __nv_bfloat16* Vc = (const __nv_bfloat16*)p.v + t0 * p.v_ld + (int64_t)h * Dv;
     if (tid < C) {
       const float g = p.G[ch * C + tid];
       gv[tid] = g;
@@ -331,11 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
       dG[tid] = 0.f;
       db[tid] = 0.f;
     }
-    // W and U^T tiles of this head (bulk copies), overlapped with the staging below
+    // W and U^T tiles (bulk copies), dO rows into the [dO; dDelta] tile and V rows
+    // (TMA), overlapped with the staging below
     if (tid == 0) {
-      tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2);
+      const int nbv = (Dv + 63) / 64;
+      tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2 + 2u * nbv * 8192u);
       tc::bulk_g2s(tW, p.Wsw + ch * sCK, sCK, &bars[1]);
       tc::bulk_g2s(sU, p.Utb + ch * Dv * C, (uint32_t)Dv * C * 2, &bars[1]);
+      for (int b = 0; b < nbv; ++b) {
+        tc::tma_load_2d(tA2 + b * 16384, &maps.dO, h * Dv + 64 * b, (int)t0, &bars[1]);
+        tc::tma_load_2d(tV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bars[1]);
+      }
     }
     __syncthreads();
     if (tid < C) {
@@ -344,9 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
     }
     __syncthreads();
     // ---- phase A: S, S^T, [dO; dDelta], scale e^G dO
-    stage_f32(S, Dk, Dv, Dv, Dk, tS, tSt, Dv, One(), One());
-    stage_bf16(dOc, C, Dv, p.dO_ld, len, tA2, 128, tdOe, nullptr, 0,
-               [&](int r) { return p.scale * ev[r]; });
+    // saved S is stored transposed ([Dv][Dk]): natural rows give S^T, transposed give S
+    stage_f32(S, Dv, Dk, Dk, Dv, tSt, tS, Dk, One(), One());
     {
       // rows 64..127 of the [dO; dDelta] tile
       const int cpr = Dv / 8;
@@ -367,6 +397,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
         ok = false;
         break;
       }
+    }
+    // scale e^G dO (rows past the chunk zero) from the dO rows of the [dO; dDelta] tile
+    for (int idx = tid; idx < C * (Dv / 8); idx += kThreads) {
+      const int r = idx % C, c8 = (idx / C) * 8;
+      const uint4 raw = *(const uint4*)(tA2 + tc::sw128_offset(r, c8, 128));
+      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
+      const float sc = r < len ? p.scale * ev[r] : 0.f;
+      __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        pk[q] = __floats2bfloat162_rn(__bfloat162float(e[2 * q]) * sc, __bfloat162float(e[2 * q + 1]) * sc);
+      *(uint4*)(tdOe + tc::sw128_offset(r, c8, C)) = *(const uint4*)pk;
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
@@ -422,15 +464,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p) {
       tc::bulk_g2s(tP, p.Psw + ch * sCC, sCC, &bars[1]);
     }
     stage_f32(dSg, Dk, Dv, Dv, Dk, tdS, nullptr, 0, One(), One());
-    stage_bf16(Vc, C, Dv, p.v_ld, len, tV, C, nullptr, nullptr, 0, One());
     stage_f32(Kn, C, Dk, Dk, C, tKe, nullptr, 0, [&](int r) { return ev[r]; }, One());
     {
       float sds = 0.f;
-      const float4* S4 = (const float4*)S;
-      const float4* D4 = (const float4*)dSg;
-      for (size_t e = tid; e < SZ / 4; e += kThreads) {
-        const float4 a = S4[e], d = D4[e];
-        sds = fmaf(a.x, d.x, fmaf(a.y, d.y, fmaf(a.z, d.z, fmaf(a.w, d.w, sds))));
+      // <S, dS>: S^T rows (v) against dS columns
+      for (int e = tid; e < Dv * (Dk / 4); e += kThreads) {
+        const int v = e % Dv, k4 = (e / Dv) * 4;
+        const float4 a = *(const float4*)(S + (size_t)v * Dk + k4);
+        sds = fmaf(a.x, dSg[(size_t)k4 * Dv + v], sds);
+        sds = fmaf(a.y, dSg[(size_t)(k4 + 1) * Dv + v], sds);
+        sds = fmaf(a.z, dSg[(size_t)(k4 + 2) * Dv + v], sds);
+        sds = fmaf(a.w, dSg[(size_t)(k4 + 3) * Dv + v], sds);
       }
       sds = warp_sum(sds);
       if ((tid & 31) == 0) red[warp] = sds;
@@ -711,33 +755,34 @@ __global__ void k_bwd_gates_tc(Params p) {
 
 // ---------------------------------------------------------------------------
 template <int DK>
-static cudaError_t launch_bwd_state_tc_t(const Params& p, cudaStream_t st) {
+static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, cudaStream_t st) {
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const size_t bK = tc::sw128_bytes(64, DK), bKt = (size_t)DK * 128;
-  const size_t bufsz = bK + 8192 + 2 * bKt + 1024;
-  const size_t smem = tc::sw128_bytes(MV, DK) + 3 * (size_t)MV * 128 + 2 * bufsz + 2 * C * 4 + 64 + 1024;
+  const size_t bO = (size_t)((Dv + 63) / 64) * 8192;
+  const size_t bufsz = bO + bK + 8192 + 2 * bKt + 1024;
+  const size_t smem = tc::sw128_bytes(MV, DK) + 2 * (size_t)MV * 128 + 2 * bufsz + 2 * C * 4 + 64 + 1024;
   cudaFuncSetAttribute(k_bwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_BWD_STATE_TC);
-  k_bwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kThreads, smem, st>>>(p);
+  k_bwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kThreads, smem, st>>>(p, maps);
   profile_post(st);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_tc(const Params& p, cudaStream_t st) {
+cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   if (p.n_seqs > 0) {
     switch (p.Dk) {
-      case 16: e = launch_bwd_state_tc_t<16>(p, st); break;
-      case 32: e = launch_bwd_state_tc_t<32>(p, st); break;
-      case 64: e = launch_bwd_state_tc_t<64>(p, st); break;
-      default: e = launch_bwd_state_tc_t<128>(p, st); break;
+      case 16: e = launch_bwd_state_tc_t<16>(p, maps, st); break;
+      case 32: e = launch_bwd_state_tc_t<32>(p, maps, st); break;
+      case 64: e = launch_bwd_state_tc_t<64>(p, maps, st); break;
+      default: e = launch_bwd_state_tc_t<128>(p, maps, st); break;
     }
     if (e != cudaSuccess) return e;
   }
   const size_t smem = 65536 + 32768 + 49152 + 32768 + 32768 + (size_t)(10 * C + 8) * 4 + 64 + 1024;
   cudaFuncSetAttribute(k_bwd_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_BWD_GRADS_TC);
-  k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p);
+  k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, maps);
   profile_post(st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   profile_pre(st, KID_BWD_GATES);

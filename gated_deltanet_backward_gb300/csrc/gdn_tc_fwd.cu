@@ -87,7 +87,9 @@ __device__ void tri_inverse(float* Tm, int nh, float* Mt) {
 }  // namespace
 
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
+__global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
+                                                          const __grid_constant__ TmaMaps maps,
+                                                          int bwd) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int c = blockIdx.x, kh = blockIdx.y;
@@ -119,15 +121,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
   float* gv = Mt + RB * 3 * 256;                        // [RB][C]
   float* bv = gv + RB * C;                              // [RB][C]
   float* wv = bv + RB * C;                              // [RB][C]
-  uint64_t* bar = (uint64_t*)(wv + RB * C);
-  uint32_t* tslot = (uint32_t*)(bar + 1);
+  uint64_t* bar = (uint64_t*)(wv + RB * C);   // [0] MMA completion, [1] TMA loads
+  uint32_t* tslot = (uint32_t*)(bar + 2);
+  uint8_t* sV = (uint8_t*)KK;  // [C][Dv] natural V tile of one head (KK is free by then)
 
   // zero the transposed tiles (rows past Dk / Dv pad the M = 64 products)
   for (int i = tid; i < MK * 128 / 16; i += kThreads) ((uint4*)tKt)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < MK * 128 / 16; i += kThreads) ((uint4*)tQt)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < MV * 128 / 16; i += kThreads) ((uint4*)tVt)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
     tc::fence_mbar_init();
   }
   if (warp == 0) {
@@ -138,60 +142,61 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  uint32_t phase = 0;
+  uint32_t phase = 0, lphase = 0;
   bool ok = true;
+  const int nbk = (Dk + 63) / 64, nbv = (Dv + 63) / 64;
+  const size_t ck = ((size_t)c * p.Hk + kh) * C;
+  // raw k and q rows of the chunk: TMA boxes straight into the [K; Q] operand tile
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bar[1], 2u * nbk * 8192u);
+    for (int b = 0; b < nbk; ++b) {
+      tc::tma_load_2d(tAQK + b * aqk_pitch, &maps.k, kh * Dk + 64 * b, (int)t0, &bar[1]);
+      tc::tma_load_2d(tAQK + b * aqk_pitch + 8192, &maps.q, kh * Dk + 64 * b, (int)t0, &bar[1]);
+    }
+  }
+  {
+    const bool lok = tc::mbar_wait(&bar[1], lphase);
+    lphase ^= 1u;
+    if (__syncthreads_or(lok ? 0 : 1)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+      ok = false;
+    }
+  }
+  if (!ok) goto done;
 
   // 1. L2-normalise q and k rows into the operand tiles.
-  const size_t ck = ((size_t)c * p.Hk + kh) * C;
-  // 16-byte loads: a row of Dk elements is Dk/8 consecutive threads; 8 (Dk = 128) row
-  // chunks per thread, all loaded before the sums of squares are reduced.
+  // L2 normalisation in place: a row of Dk elements is Dk/8 consecutive threads
   {
-    const int lpr = Dk / 8;                       // threads per row (2..16)
-    const int total = 2 * C * lpr;                 // chunks of the 128 rows
-    for (int base = 0; base < total; base += 8 * kThreads) {
-      uint4 raw[8];
+    const int lpr = Dk / 8;
+    const int total = 2 * C * lpr;
+    for (int idx0 = 0; idx0 < total; idx0 += kThreads) {
+      const int idx = idx0 + tid;
+      const int row = idx / lpr, c0 = (idx % lpr) * 8;
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      if (idx < total) raw = *(const uint4*)(tAQK + tc::sw128_offset(row, c0, 128));
+      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
+      float x[8], ss = 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * kThreads + tid;
-        raw[u] = make_uint4(0, 0, 0, 0);
-        const int row = idx / lpr, c0 = (idx % lpr) * 8;
-        const int t = row & (C - 1);
-        if (idx < total && t < len) {
-          const bool isq = row >= C;
-          const __nv_bfloat16* src = (const __nv_bfloat16*)(isq ? p.q : p.k) +
-                                     (t0 + t) * (isq ? p.q_ld : p.k_ld) + (int64_t)kh * Dk;
-          raw[u] = *(const uint4*)(src + c0);
-        }
+      for (int q = 0; q < 8; ++q) {
+        x[q] = __bfloat162float(e[q]);
+        ss = fmaf(x[q], x[q], ss);
       }
+      for (int o = lpr >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (idx < total) {
+        const bool isq = row >= C;
+        const int t = row & (C - 1);
+        const float nrm = sqrtf(ss + 1e-6f);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * kThreads + tid;
-        const int row = idx / lpr, c0 = (idx % lpr) * 8;
-        const __nv_bfloat16* e = (const __nv_bfloat16*)&raw[u];
-        float x[8], ss = 0.f;
+        for (int q = 0; q < 8; ++q) x[q] = t < len ? x[q] / nrm : 0.f;
+        __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          x[q] = __bfloat162float(e[q]);
-          ss = fmaf(x[q], x[q], ss);
-        }
-        for (int o = lpr >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (idx < total) {
-          const bool isq = row >= C;
-          const int t = row & (C - 1);
-          const float nrm = sqrtf(ss + 1e-6f), inv = 1.f / nrm;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x[q] = x[q] / nrm;
-          __align__(16) __nv_bfloat162 pk[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) pk[q] = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
-          *(uint4*)(tAQK + tc::sw128_offset(row, c0, 128)) = *(const uint4*)pk;
-          if (bwd) {
-            float* dst = (isq ? p.Qn : p.Kn) + (ck + t) * Dk + c0;
-            *(float4*)dst = make_float4(x[0], x[1], x[2], x[3]);
-            *(float4*)(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
-            if (c0 == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
-          }
-          (void)inv;
+        for (int q = 0; q < 4; ++q) pk[q] = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
+        *(uint4*)(tAQK + tc::sw128_offset(row, c0, 128)) = *(const uint4*)pk;
+        if (bwd) {
+          float* dst = (isq ? p.Qn : p.Kn) + (ck + t) * Dk + c0;
+          *(float4*)dst = make_float4(x[0], x[1], x[2], x[3]);
+          *(float4*)(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+          if (c0 == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
         }
       }
     }
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
   // 2. [K; Q] K^T -> TMEM columns [0, 64): lanes 0-63 K K^T, lanes 64-127 Q K^T.
   ok = mma_run([&] { tc::mma_tile_p(tmem, tc::smem_u32(tAQK), aqk_pitch, 128, tc::smem_u32(tAQK),
                                      aqk_pitch, 64, Dk, 0u); },
-               bar, phase, p.status, c);
+               &bar[0], phase, p.status, c);
   if (!ok) goto done;
   acc_walk(tmem, 128, 64, 128, [&](int row, int col0, const float* v) {
     float* dst = row < C ? KK + row * C : QK + (row - C) * C;
@@ -285,6 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
       const int h = kh * p.r + g0 + hh;
       const size_t ch = (size_t)c * p.Hv + h;
       const float* T = Tm + hh * C * C;
+      if (tid == 0) {  // this head's V rows, landing while the T tiles are staged
+        tc::mbar_arrive_expect_tx(&bar[1], (uint32_t)nbv * 8192u);
+        for (int b = 0; b < nbv; ++b)
+          tc::tma_load_2d(sV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bar[1]);
+      }
       const float* w = wv + hh * C;
       const float* bb = bv + hh * C;
       const float* G = gv + hh * C;
@@ -297,13 +307,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p, int bwd) {
         stage_tile(tOPt, C, C, [&](int s, int r) {
           return s <= r ? expf(G[r] - G[s]) * QK[r * C + s] : 0.f;
         });
-      const __nv_bfloat16* Vs = (const __nv_bfloat16*)p.v + t0 * p.v_ld + (int64_t)h * Dv;
-      stage_bf16(Vs, C, Dv, p.v_ld, len, nullptr, 0, nullptr, tVt, MV, One());
+      {
+        const bool lok = tc::mbar_wait(&bar[1], lphase);
+        lphase ^= 1u;
+        if (__syncthreads_or(lok ? 0 : 1)) {
+          if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+          ok = false;
+          goto done;
+        }
+      }
+      // V^T (rows v, columns s) from the natural V tile; rows past the chunk are zero
+      for (int idx = tid; idx < Dv * (C / 8); idx += kThreads) {
+        const int vv = idx % Dv, s8 = (idx / Dv) * 8;
+        __align__(16) __nv_bfloat16 e[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          e[q] = s8 + q < len ? *(const __nv_bfloat16*)(sV + tc::sw128_offset(s8 + q, vv, C))
+                              : __float2bfloat16(0.f);
+        *(uint4*)(tVt + tc::sw128_offset(vv, s8, MV)) = *(const uint4*)e;
+      }
       tc::fence_async_smem();
       ok = mma_run([&] {
         tc::mma_tile(tmem + 64, tc::smem_u32(tKt), MK, tc::smem_u32(tTW), C, C, 0u);
         tc::mma_tile(tmem + 128, tc::smem_u32(tVt), MV, tc::smem_u32(tTB), C, C, 0u);
-      }, bar, phase, p.status, c);
+      }, &bar[0], phase, p.status, c);
       if (!ok) goto done;
       acc_walk(tmem + 64, MK, 64, Dk, [&](int k, int col0, const float* v) {
 #pragma unroll
@@ -420,14 +447,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     const int i = c - c0, b = i & 1;
     const int64_t t0 = s0 + (int64_t)i * C;
     const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
-    // chunk-start state
-    float* sv = p.saved + ((size_t)c * p.Hv + h) * SZ;
+    // chunk-start state, saved transposed ([Dv][Dk]): row v is this thread's
+    float* sv = p.saved + ((size_t)c * p.Hv + h) * SZ + (size_t)vrow * DK;
     if (vok)
 #pragma unroll
       for (int ii = 0; ii < NKC; ++ii)
         if (half * 16 + 32 * ii < DK)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[(size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = S[ii][j];
+          for (int j = 0; j < 16; j += 4)
+            *(float4*)(sv + half * 16 + 32 * ii + j) =
+                make_float4(S[ii][j], S[ii][j + 1], S[ii][j + 2], S[ii][j + 3]);
     // tiles of this chunk
     const bool lok = tc::mbar_wait(&bars[1 + b], b ? lphase1 : lphase0);
     if (b) lphase1 ^= 1u; else lphase0 ^= 1u;
@@ -479,8 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
       tc::mma_tile(tS, tc::smem_u32(tDct), MV, tc::smem_u32(tKt(b)), DK, C, 0u);
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
-    // O = scale (e^G Q S + P Delta): column r of O^T is token t0 + r
-    __nv_bfloat16* orow = (__nv_bfloat16*)p.o + t0 * p.o_ld + (int64_t)h * Dv;
+    // O = scale (e^G Q S + P Delta): column r of O^T is token t0 + r.  Staged as
+    // [C][Dv] rows in the (now free) Delta^T tile, then stored row by row.
+    __nv_bfloat16* sO = (__nv_bfloat16*)tDt;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int col0 = half * 16 + 32 * q;
@@ -489,11 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
       tc::tmem_ld_wait();
       if (vok)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = col0 + j;
-          if (r < len)
-            orow[(int64_t)r * p.o_ld + vrow] = __float2bfloat16_rn(p.scale * (ev[r] * o1[q][j] + x[j]));
-        }
+        for (int j = 0; j < 16; ++j)
+          sO[(col0 + j) * Dv + vrow] = __float2bfloat16_rn(p.scale * (ev[col0 + j] * o1[q][j] + x[j]));
+    }
+    __syncthreads();
+    {
+      __nv_bfloat16* orow = (__nv_bfloat16*)p.o + t0 * p.o_ld + (int64_t)h * Dv;
+      const int cpr = Dv / 8;
+      for (int idx = tid; idx < len * cpr; idx += kThreads) {
+        const int r = idx / cpr, c8 = (idx % cpr) * 8;
+        *(uint4*)(orow + (int64_t)r * p.o_ld + c8) = *(const uint4*)(sO + r * Dv + c8);
+      }
     }
     // S^T <- e^{G_last} S^T + Delta^T diag(c) K
     const float eC = expf(G[len - 1]);
@@ -544,12 +580,12 @@ static size_t fwd_state_tc_smem(const Params& p) {
   return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 2 * C * 4 + 64 + 1024;
 }
 
-cudaError_t launch_prep_tc(const Params& p, bool bwd, cudaStream_t st) {
+cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st) {
   if (p.NC == 0) return cudaSuccess;
   const size_t smem = prep_tc_smem(p);
   cudaFuncSetAttribute(k_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, bwd ? KID_PREP_TC_BWD : KID_PREP_TC);
-  k_prep_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, bwd ? 1 : 0);
+  k_prep_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, maps, bwd ? 1 : 0);
   profile_post(st);
   return cudaGetLastError();
 }

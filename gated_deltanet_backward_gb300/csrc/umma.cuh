@@ -197,6 +197,20 @@ __host__ __device__ __forceinline__ uint32_t sw128_bytes(int rows, int cols) {
   return (uint32_t)((cols + 63) / 64) * (uint32_t)rows * 128u;
 }
 
+// ------------------------------------------------------------ TMA tiles
+// One thread: loads the box at (x, y) (x = column, a multiple of 8 bf16; y =
+// row) of the 2-D tensor map into shared memory; completion is signalled on
+// `bar` through its transaction count.  The map lives in kernel-parameter
+// space (__grid_constant__).
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------ bulk copies
 // One thread: copies `bytes` (multiple of 16; both addresses 16-byte aligned)
 // from global memory into shared memory with the bulk-copy engine; completion
