@@ -96,24 +96,27 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
   const WsLayout L = gdn::ws_layout(*s, bwd);
   char* base = (char*)ws;
   p.status = (gdn::DeviceStatus*)(base + L.status);
-  p.Qn = (float*)(base + L.Qn);
-  p.Kn = (float*)(base + L.Kn);
   p.nq = (float*)(base + L.nq);
   p.nk = (float*)(base + L.nk);
-  p.W = (float*)(base + L.W);
-  p.U = (float*)(base + L.U);
   p.G = (float*)(base + L.G);
   p.b = (float*)(base + L.b);
   if (bwd) {
-    p.Tm = (float*)(base + L.Tm);
-    p.dS = (float*)(base + L.dS);
-    p.dD = (float*)(base + L.dD);
-    p.dQh = (float*)(base + L.dQh);
-    p.dKh = (float*)(base + L.dKh);
     p.pa = (float*)(base + L.pa);
     p.pd = (float*)(base + L.pd);
   }
-  if (s->dtype == GDN_DTYPE_BF16) {
+  if (s->dtype != GDN_DTYPE_BF16) {
+    p.Qn = (float*)(base + L.Qn);
+    p.Kn = (float*)(base + L.Kn);
+    p.W = (float*)(base + L.W);
+    p.U = (float*)(base + L.U);
+    if (bwd) {
+      p.Tm = (float*)(base + L.Tm);
+      p.dS = (float*)(base + L.dS);
+      p.dD = (float*)(base + L.dD);
+      p.dQh = (float*)(base + L.dQh);
+      p.dKh = (float*)(base + L.dKh);
+    }
+  } else {
     p.Qsw = (uint8_t*)(base + L.Qsw);
     p.Ksw = (uint8_t*)(base + L.Ksw);
     p.Ktsw = (uint8_t*)(base + L.Ktsw);
@@ -121,11 +124,14 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
     p.Psw = (uint8_t*)(base + L.Psw);
     p.Utb = (__nv_bfloat16*)(base + L.Utb);
     if (bwd) {
-      p.Wtsw = (uint8_t*)(base + L.Wtsw);
       p.Qtsw = (uint8_t*)(base + L.Qtsw);
+      p.Wtsw = (uint8_t*)(base + L.Wtsw);
       p.Ptsw = (uint8_t*)(base + L.Ptsw);
-      p.QKf = (float*)(base + L.QKf);
       p.KKf = (float*)(base + L.KKf);
+      p.Tb = (uint8_t*)(base + L.Tb);
+      p.dSb = (uint8_t*)(base + L.dSb);
+      p.dDb = (uint8_t*)(base + L.dDb);
+      p.dDtb = (uint8_t*)(base + L.dDtb);
     }
   }
 }

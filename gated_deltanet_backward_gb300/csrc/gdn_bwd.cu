@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
   float* red = db + C;          // [kThreads / 32] block reduction scratch
   const size_t ch = (size_t)c * p.Hv + h;
   const size_t SZ = (size_t)Dk * Dv;
-  const float* S = p.saved_in + ch * SZ;   // chunk-start state, stored transposed [Dv][Dk]
+  const float* S = p.saved_in + ch * SZ;
   const float* dSg = p.dS + ch * SZ;
   const float* Wc = p.W + ch * C * Dk;
   const float* Uc = p.U + ch * C * Dv;
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
   }
   // Delta = U - W S
   block_mm(C, Dv, Dk, [&](int i, int kk) { return Wc[i * Dk + kk]; },
-           [&](int kk, int j) { return S[(size_t)j * Dk + kk]; },
+           [&](int kk, int j) { return S[(size_t)kk * Dv + j]; },
            [&](int i, int j, float acc) { Dl[i * Dv + j] = Uc[i * Dv + j] - acc; });
   block_mm(C, C, Dk, [&](int i, int kk) { return Kc[i * Dk + kk]; },
            [&](int kk, int j) { return Kc[j * Dk + kk]; },
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
     const int r = idx / Dk, kk = idx % Dk;
     float a1 = 0.f, a2 = 0.f;
     if (r < len) {
-      for (int j = 0; j < Dv; ++j) a1 = fmaf(dO_at(r, j), S[(size_t)j * Dk + kk], a1);
+      for (int j = 0; j < Dv; ++j) a1 = fmaf(dO_at(r, j), S[(size_t)kk * Dv + j], a1);
       for (int s = 0; s <= r; ++s) a2 = fmaf(dP[r * C + s] * E[r * C + s], Kc[s * Dk + kk], a2);
     }
     dQh[idx] = p.scale * ev[r] * a1 + a2;
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
   }
   // Tmp = (Q S) * dO  ->  dG_r += scale e^{G_r} rowsum
   block_mm(C, Dv, Dk, [&](int i, int kk) { return Qc[i * Dk + kk]; },
-           [&](int kk, int j) { return S[(size_t)j * Dk + kk]; },
+           [&](int kk, int j) { return S[(size_t)kk * Dv + j]; },
            [&](int i, int j, float acc) { Tmp[i * Dv + j] = acc * dO_at(i, j); });
   __syncthreads();
   if (threadIdx.x < C) {
@@ -222,8 +222,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
            [&](int kk, int j) { return dSg[(size_t)kk * Dv + j]; },
            [&](int i, int j, float acc) { Tmp[i * Dv + j] = acc * Dl[i * Dv + j]; });
   float sds = 0.f;
-  for (size_t e = threadIdx.x; e < SZ; e += kThreads)  // saved S is [Dv][Dk]; dS is [Dk][Dv]
-    sds = fmaf(S[(e % Dv) * Dk + e / Dv], dSg[e], sds);
+  for (size_t e = threadIdx.x; e < SZ; e += kThreads) sds = fmaf(S[e], dSg[e], sds);
   sds = warp_sum(sds);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sds;
   __syncthreads();
@@ -244,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
   if (threadIdx.x < C) dG[threadIdx.x] -= X[threadIdx.x];
   // dW = -dDelta S^T
   block_mm(C, Dk, Dv, [&](int i, int j) { return dDc[i * Dv + j]; },
-           [&](int j, int kk) { return S[(size_t)j * Dk + kk]; },
+           [&](int j, int kk) { return S[(size_t)kk * Dv + j]; },
            [&](int i, int kk, float acc) { dW[i * Dk + kk] = -acc; });
   __syncthreads();
   // dT = dDelta (b V)^T + dW (b e^G K)^T, columns of valid rows only

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) k_fwd_state(Params p, int DVS) {
     float* sv = p.saved + ch * SZ;
     for (int idx = threadIdx.x; idx < Dk * DVS; idx += kThreads) {
       const int kk = idx / DVS, j = idx % DVS;
-      sv[(size_t)(v0 + j) * Dk + kk] = S[idx];   // saved transposed: [Dv][Dk]
+      sv[(size_t)kk * Dv + v0 + j] = S[idx];
     }
     if (threadIdx.x < C) gv[threadIdx.x] = p.G[ch * C + threadIdx.x];
     __syncthreads();

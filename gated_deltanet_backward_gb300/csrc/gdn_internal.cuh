@@ -32,44 +32,51 @@ struct DeviceStatus {
   int32_t detail;  // kernel-specific detail (e.g. the chunk index)
 };
 
-// Byte offsets of the workspace regions (fp32 unless noted).
+// Byte offsets of the workspace regions (fp32 unless noted; 0 = not allocated).
+// C = 64 tokens per chunk; NC chunks.  fp32 inputs use the CUDA-core kernels'
+// regions, bf16 inputs the tensor-core kernels' operand tiles (K-major,
+// 128B-swizzled bf16, see umma.cuh), written by one kernel and copied as-is into
+// shared memory by the next.
 struct WsLayout {
   size_t status;  // DeviceStatus, 256 B
-  size_t Qn;      // [NC][Hk][C][Dk] normalised queries
-  size_t Kn;      // [NC][Hk][C][Dk] normalised keys
   size_t nq;      // [NC][Hk][C] query norms sqrt(|q|^2 + 1e-6)
   size_t nk;      // [NC][Hk][C] key norms
-  size_t W;       // [NC][Hv][C][Dk]
-  size_t U;       // [NC][Hv][C][Dv]
-  size_t Tm;      // [NC][Hv][C][C] (backward only)
   size_t G;       // [NC][Hv][C] inclusive cumsum of log g
   size_t b;       // [NC][Hv][C] beta
+  size_t pa;      // [NC][Hv] per-chunk partial of d a_log (backward)
+  size_t pd;      // [NC][Hv] per-chunk partial of d dt_bias (backward)
+  // fp32 path
+  size_t Qn;      // [NC][Hk][C][Dk] normalised queries
+  size_t Kn;      // [NC][Hk][C][Dk] normalised keys
+  size_t W;       // [NC][Hv][C][Dk]
+  size_t U;       // [NC][Hv][C][Dv]
+  size_t Tm;      // [NC][Hv][C][C] (backward)
   size_t dS;      // [NC][Hv][Dk][Dv] state adjoint at each chunk end (backward)
   size_t dD;      // [NC][Hv][C][Dv] d Delta (backward)
   size_t dQh;     // [NC][Hv][C][Dk] per-value-head d q_hat partials (backward)
   size_t dKh;     // [NC][Hv][C][Dk] per-value-head d k_hat partials (backward)
-  size_t pa;      // [NC][Hv] per-chunk partial of d a_log (backward)
-  size_t pd;      // [NC][Hv] per-chunk partial of d dt_bias (backward)
-  // bf16 tensor-core path: operand tiles in the K-major 128B-swizzled layout
-  // (see umma.cuh), written by the chunk preparation, copied as-is by the
-  // state walks.
-  size_t Qsw;     // [NC][Hk] tile [C rows][Dk]   normalised queries
-  size_t Ksw;     // [NC][Hk] tile [C rows][Dk]   normalised keys
-  size_t Ktsw;    // [NC][Hk] tile [Dk rows][C]   normalised keys, transposed
-  size_t Wsw;     // [NC][Hv] tile [C rows][Dk]   W
-  size_t Wtsw;    // [NC][Hv] tile [Dk rows][C]   W^T (backward)
-  size_t Psw;     // [NC][Hv] tile [C rows][C]    P = E * (Q K^T), lower incl. diagonal
-  size_t Utb;     // [NC][Hv][Dv][C] bf16         U^T
-  size_t Qtsw;    // [NC][Hk] tile [Dk rows][C]   normalised queries, transposed (backward)
-  size_t Ptsw;    // [NC][Hv] tile [C rows][C]    P^T (backward)
-  size_t QKf;     // [NC][Hk][C][C] fp32          Q K^T (backward)
-  size_t KKf;     // [NC][Hk][C][C] fp32          K K^T (backward)
+  // bf16 path (tiles)
+  size_t Qsw;     // [NC][Hk] [C][Dk]   normalised queries
+  size_t Ksw;     // [NC][Hk] [C][Dk]   normalised keys
+  size_t Ktsw;    // [NC][Hk] [Dk][C]   K^T
+  size_t Qtsw;    // [NC][Hk] [Dk][C]   Q^T (backward)
+  size_t Wsw;     // [NC][Hv] [C][Dk]   W
+  size_t Wtsw;    // [NC][Hv] [Dk][C]   W^T (backward)
+  size_t Psw;     // [NC][Hv] [C][C]    P = E * (Q K^T), lower incl. diagonal
+  size_t Ptsw;    // [NC][Hv] [C][C]    P^T (backward)
+  size_t Utb;     // [NC][Hv] [Dv][C]   U^T
+  size_t KKf;     // [NC][Hk][C][C] fp32  K K^T (backward)
+  size_t Tb;      // [NC][Hv] 3 x [C][C]: T, T^T, diag(b e^G) T^T (backward)
+  size_t dSb;     // [NC][Hv] [Dk][Dv]  state adjoint at each chunk end (backward)
+  size_t dDb;     // [NC][Hv] [C][Dv]   d Delta (backward)
+  size_t dDtb;    // [NC][Hv] [Dv][C]   d Delta^T (backward)
   size_t total;
 };
 
 // Bytes of the bf16 SW128 operand tiles (C = 64 rows or columns).
 inline size_t tile_CxD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
 inline size_t tile_DxC(int D) { return (size_t)D * 128; }
+inline size_t tile_DxD(int R, int D) { return (size_t)((D + 63) / 64) * R * 128; }
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -84,24 +91,27 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
     return at;
   };
   L.status = take(256);
-  L.Qn = take(NC * Hk * C * Dk * 4);
-  L.Kn = take(NC * Hk * C * Dk * 4);
   L.nq = take(NC * Hk * C * 4);
   L.nk = take(NC * Hk * C * 4);
-  L.W = take(NC * Hv * C * Dk * 4);
-  L.U = take(NC * Hv * C * Dv * 4);
   L.G = take(NC * Hv * C * 4);
   L.b = take(NC * Hv * C * 4);
   if (bwd) {
-    L.Tm = take(NC * Hv * C * C * 4);
-    L.dS = take(NC * Hv * Dk * Dv * 4);
-    L.dD = take(NC * Hv * C * Dv * 4);
-    L.dQh = take(NC * Hv * C * Dk * 4);
-    L.dKh = take(NC * Hv * C * Dk * 4);
     L.pa = take(NC * Hv * 4);
     L.pd = take(NC * Hv * 4);
   }
-  if (s.dtype == GDN_DTYPE_BF16) {
+  if (s.dtype != GDN_DTYPE_BF16) {
+    L.Qn = take(NC * Hk * C * Dk * 4);
+    L.Kn = take(NC * Hk * C * Dk * 4);
+    L.W = take(NC * Hv * C * Dk * 4);
+    L.U = take(NC * Hv * C * Dv * 4);
+    if (bwd) {
+      L.Tm = take(NC * Hv * C * C * 4);
+      L.dS = take(NC * Hv * Dk * Dv * 4);
+      L.dD = take(NC * Hv * C * Dv * 4);
+      L.dQh = take(NC * Hv * C * Dk * 4);
+      L.dKh = take(NC * Hv * C * Dk * 4);
+    }
+  } else {
     L.Qsw = take(NC * Hk * tile_CxD(s.Dk));
     L.Ksw = take(NC * Hk * tile_CxD(s.Dk));
     L.Ktsw = take(NC * Hk * tile_DxC(s.Dk));
@@ -109,11 +119,14 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
     L.Psw = take(NC * Hv * tile_CxD(64));
     L.Utb = take(NC * Hv * Dv * C * 2);
     if (bwd) {
-      L.Wtsw = take(NC * Hv * tile_DxC(s.Dk));
       L.Qtsw = take(NC * Hk * tile_DxC(s.Dk));
+      L.Wtsw = take(NC * Hv * tile_DxC(s.Dk));
       L.Ptsw = take(NC * Hv * tile_CxD(64));
-      L.QKf = take(NC * Hk * C * C * 4);
       L.KKf = take(NC * Hk * C * C * 4);
+      L.Tb = take(NC * Hv * 3 * tile_CxD(64));
+      L.dSb = take(NC * Hv * tile_DxD(s.Dk, s.Dv));
+      L.dDb = take(NC * Hv * tile_CxD(s.Dv));
+      L.dDtb = take(NC * Hv * tile_DxC(s.Dv));
     }
   }
   L.total = off;
@@ -180,8 +193,11 @@ struct Params {
   uint8_t* Psw;
   uint8_t* Ptsw;
   __nv_bfloat16* Utb;
-  float* QKf;
   float* KKf;
+  uint8_t* Tb;
+  uint8_t* dSb;
+  uint8_t* dDb;
+  uint8_t* dDtb;
 };
 
 // Kernel ids reported to the profiling hook (gdn_profile_begin).

@@ -114,14 +114,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
     const int64_t t0 = s0 + (int64_t)(c - c0) * C;
     const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
     const size_t ch = (size_t)c * p.Hv + h;
-    // state adjoint at the end of this chunk, for the gradient kernel
-    float* dsv = p.dS + ch * SZ;
+    // state adjoint at the end of this chunk, as a bf16 [DK][Dv] operand tile for the
+    // gradient kernel (a warp's lanes write consecutive columns of one tile row)
+    uint8_t* dst_dS = p.dSb + ch * (size_t)tc::sw128_bytes(DK, Dv);
     if (vok)
 #pragma unroll
       for (int ii = 0; ii < NKC; ++ii)
         if (half * 16 + 32 * ii < DK)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dsv[(size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = dS[ii][j];
+          for (int j = 0; j < 16; ++j)
+            *(__nv_bfloat16*)(dst_dS + tc::sw128_offset(half * 16 + 32 * ii + j, vrow, DK)) =
+                __float2bfloat16_rn(dS[ii][j]);
     const bool lok = tc::mbar_wait(&bars[1 + b], lph[b]);
     lph[b] ^= 1u;
     if (__syncthreads_or(lok ? 0 : 1)) {
@@ -171,7 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // dDelta^T = scale (P^T dO)^T + c (K dS)^T
-    float* dDg = p.dD + ch * C * Dv;
+    // dDelta as bf16 tiles for the gradient kernel: natural [C][Dv] and transposed [Dv][C]
+    uint8_t* dst_dD = p.dDb + ch * (size_t)tc::sw128_bytes(C, Dv);
+    uint8_t* dst_dDt = p.dDtb + ch * (size_t)Dv * 128;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int col0 = half * 16 + 32 * q;
@@ -180,15 +185,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
       tc::tmem_ld16(tA2 + lane_quarter() + col0, a2);
       tc::tmem_ld_wait();
       if (vok) {
-        float md[16];
+        float d[16], md[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int s = col0 + j;
-          const float d = s < len ? p.scale * a1[j] + cv[s] * a2[j] : 0.f;
-          md[j] = -d;
-          dDg[(size_t)s * Dv + vrow] = d;
+          d[j] = s < len ? p.scale * a1[j] + cv[s] * a2[j] : 0.f;
+          md[j] = -d[j];
+          *(__nv_bfloat16*)(dst_dD + tc::sw128_offset(s, vrow, C)) = __float2bfloat16_rn(d[j]);
         }
         tile_put16(tmDt, MV, vrow, col0, md);
+        tile_put16(dst_dDt, Dv, vrow, col0, d);
       }
     }
     tc::fence_async_smem();
@@ -319,8 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   const uint32_t tdQ = tmem, tdK = tmem + 128, tmp = tmem + 256;
   uint32_t mphase = 0, lphase = 0;
   const size_t ckk = (size_t)c * p.Hk + kh;
-  const float* Qn = p.Qn + ckk * C * Dk;
-  const float* Kn = p.Kn + ckk * C * Dk;
   const float* KK = p.KKf + ckk * C * C;
   const int row64 = acc_row(64);
   const size_t SZ = (size_t)Dk * Dv;
@@ -346,9 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     const size_t ch = (size_t)c * p.Hv + h;
     const uint32_t acc_first = hh > 0 ? 1u : 0u;
     const float* S = p.saved_in + ch * SZ;
-    const float* dSg = p.dS + ch * SZ;
-    const float* dDg = p.dD + ch * C * Dv;
-    const float* Tg = p.Tm + ch * C * C;
     if (tid < C) {
       const float g = p.G[ch * C + tid];
       gv[tid] = g;
@@ -360,12 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     // (TMA), overlapped with the staging below
     if (tid == 0) {
       const int nbv = (Dv + 63) / 64;
-      tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2 + 2u * nbv * 8192u);
+      tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u);
       tc::bulk_g2s(tW, p.Wsw + ch * sCK, sCK, &bars[1]);
       tc::bulk_g2s(sU, p.Utb + ch * Dv * C, (uint32_t)Dv * C * 2, &bars[1]);
       for (int b = 0; b < nbv; ++b) {
         tc::tma_load_2d(tA2 + b * 16384, &maps.dO, h * Dv + 64 * b, (int)t0, &bars[1]);
         tc::tma_load_2d(tV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bars[1]);
+        tc::bulk_g2s(tA2 + b * 16384 + 8192, p.dDb + ch * sCV + b * 8192, 8192, &bars[1]);
       }
     }
     __syncthreads();
@@ -375,20 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     }
     __syncthreads();
     // ---- phase A: S, S^T, [dO; dDelta], scale e^G dO
-    // saved S is stored transposed ([Dv][Dk]): natural rows give S^T, transposed give S
-    stage_f32(S, Dv, Dk, Dk, Dv, tSt, tS, Dk, One(), One());
-    {
-      // rows 64..127 of the [dO; dDelta] tile
-      const int cpr = Dv / 8;
-      for (int idx = tid; idx < C * cpr; idx += kThreads) {
-        const int r = idx / cpr, c0 = (idx % cpr) * 8;
-        const float4 a = *(const float4*)(dDg + (size_t)r * Dv + c0);
-        const float4 bq = *(const float4*)(dDg + (size_t)r * Dv + c0 + 4);
-        __align__(16) __nv_bfloat162 pk[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
-                                              __floats2bfloat162_rn(bq.x, bq.y), __floats2bfloat162_rn(bq.z, bq.w)};
-        *(uint4*)(tA2 + tc::sw128_offset(64 + r, c0, 128)) = *(const uint4*)pk;
-      }
-    }
+    stage_f32(S, Dk, Dv, Dv, Dk, tS, tSt, Dv, One(), One());
     {
       const bool lok = tc::mbar_wait(&bars[1], lphase);
       lphase ^= 1u;
@@ -444,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         tc::tmem_ld_wait();
         if (row < C) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(Qn[row * Dk + q * 16 + j], x[j], rs);
+          for (int j = 0; j < 16; ++j) rs = fmaf(tile_get(tQt, Dk, q * 16 + j, row), x[j], rs);
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -458,26 +447,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     }
     __syncthreads();
     if (tid < C) dG[tid] += p.scale * ev[tid] * (part[tid] + part[C + tid]);
-    // ---- phase B: dS, V, e^G K, P
+    // ---- phase B: dS tile, P tile (bulk), e^G K from K^T, <S, dS>
     if (tid == 0) {
-      tc::mbar_arrive_expect_tx(&bars[1], sCC);
+      tc::mbar_arrive_expect_tx(&bars[1], sCC + tc::sw128_bytes(Dk, Dv));
       tc::bulk_g2s(tP, p.Psw + ch * sCC, sCC, &bars[1]);
+      tc::bulk_g2s(tdS, p.dSb + ch * tc::sw128_bytes(Dk, Dv), tc::sw128_bytes(Dk, Dv), &bars[1]);
     }
-    stage_f32(dSg, Dk, Dv, Dv, Dk, tdS, nullptr, 0, One(), One());
-    stage_f32(Kn, C, Dk, Dk, C, tKe, nullptr, 0, [&](int r) { return ev[r]; }, One());
-    {
-      float sds = 0.f;
-      // <S, dS>: S^T rows (v) against dS columns
-      for (int e = tid; e < Dv * (Dk / 4); e += kThreads) {
-        const int v = e % Dv, k4 = (e / Dv) * 4;
-        const float4 a = *(const float4*)(S + (size_t)v * Dk + k4);
-        sds = fmaf(a.x, dSg[(size_t)k4 * Dv + v], sds);
-        sds = fmaf(a.y, dSg[(size_t)(k4 + 1) * Dv + v], sds);
-        sds = fmaf(a.z, dSg[(size_t)(k4 + 2) * Dv + v], sds);
-        sds = fmaf(a.w, dSg[(size_t)(k4 + 3) * Dv + v], sds);
-      }
-      sds = warp_sum(sds);
-      if ((tid & 31) == 0) red[warp] = sds;
+    for (int idx = tid; idx < C * (Dk / 8); idx += kThreads) {
+      const int s = idx % C, k8 = (idx / C) * 8;
+      __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        pk[u] = __floats2bfloat162_rn(tile_get(tKt, Dk, k8 + 2 * u, s) * ev[s],
+                                      tile_get(tKt, Dk, k8 + 2 * u + 1, s) * ev[s]);
+      *(uint4*)(tKe + tc::sw128_offset(s, k8, C)) = *(const uint4*)pk;
     }
     {
       const bool lok = tc::mbar_wait(&bars[1], lphase);
@@ -487,6 +470,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         ok = false;
         break;
       }
+    }
+    {
+      // <S, dS> with S (fp32, L2-resident after phase A) and the dS tile
+      float sds = 0.f;
+      for (int idx = tid; idx < Dk * (Dv / 8); idx += kThreads) {
+        const int kk = idx % Dk, v8 = (idx / Dk) * 8;
+        const float4 a = *(const float4*)(S + (size_t)kk * Dv + v8);
+        const float4 b4 = *(const float4*)(S + (size_t)kk * Dv + v8 + 4);
+        const uint4 raw = *(const uint4*)(tdS + tc::sw128_offset(kk, v8, Dk));
+        const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
+        sds = fmaf(a.x, __bfloat162float(e[0]), sds);
+        sds = fmaf(a.y, __bfloat162float(e[1]), sds);
+        sds = fmaf(a.z, __bfloat162float(e[2]), sds);
+        sds = fmaf(a.w, __bfloat162float(e[3]), sds);
+        sds = fmaf(b4.x, __bfloat162float(e[4]), sds);
+        sds = fmaf(b4.y, __bfloat162float(e[5]), sds);
+        sds = fmaf(b4.z, __bfloat162float(e[6]), sds);
+        sds = fmaf(b4.w, __bfloat162float(e[7]), sds);
+      }
+      sds = warp_sum(sds);
+      if ((tid & 31) == 0) red[warp] = sds;
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         tc::tmem_ld_wait();
         if (row64 >= 0)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(Kn[row64 * Dk + q * 16 + j], x[j], rs);
+          for (int j = 0; j < 16; ++j) rs = fmaf(tile_get(tKt, Dk, q * 16 + j, row64), x[j], rs);
       }
       if (row64 >= 0) part[half * C + row64] = rs;  // c_s * dc_s
     }
@@ -550,10 +554,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
       dG[len - 1] += expf(gv[len - 1]) * tot + sc;
     }
     // ---- phase C: dDelta^T, T^T, T, b e^G T^T
-    stage_f32(dDg, C, Dv, Dv, C, nullptr, tdDt, Dv, One(), One());
-    stage_f32(Tg, C, C, C, C, tT, tTt, C, One(), One());
-    // b e^G T^T: row s of the transposed tile (column s of T) scaled by b_s e^{G_s}
-    stage_f32(Tg, C, C, C, C, nullptr, tTbe, C, One(), [&](int s) { return bv[s] * ev[s]; });
+    if (tid == 0) {
+      const uint8_t* tb = p.Tb + ch * 3 * sCC;
+      tc::mbar_arrive_expect_tx(&bars[1], sVC + 3 * sCC);
+      tc::bulk_g2s(tdDt, p.dDtb + ch * sVC, sVC, &bars[1]);
+      tc::bulk_g2s(tT, tb, sCC, &bars[1]);
+      tc::bulk_g2s(tTt, tb + sCC, sCC, &bars[1]);
+      tc::bulk_g2s(tTbe, tb + 2 * sCC, sCC, &bars[1]);
+    }
+    {
+      const bool lok = tc::mbar_wait(&bars[1], lphase);
+      lphase ^= 1u;
+      if (__syncthreads_or(lok ? 0 : 1)) {
+        if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+        ok = false;
+        break;
+      }
+    }
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::mma_tile(tdQ, tc::smem_u32(tdPE), 64, tc::smem_u32(tKt), Dk, C, 1u);      // dQ += dPE K
@@ -611,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         tc::tmem_ld_wait();
         if (row64 >= 0)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(Kn[row64 * Dk + q * 16 + j], x[j], rs);
+          for (int j = 0; j < 16; ++j) rs = fmaf(tile_get(tKt, Dk, q * 16 + j, row64), x[j], rs);
       }
       if (row64 >= 0) part[half * C + row64] = rs;
       for (int q = half; q < 4; q += 2) {
@@ -697,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   if (ok) {
     for (int which = 0; which < 2; ++which) {
       const uint32_t acc = which ? tdK : tdQ;
-      const float* xh = which ? Kn : Qn;
+      const uint8_t* xt = which ? tKt : tQt;   // x_hat^T tiles [Dk][C]
       float dot = 0.f;
       for (int q = half; q * 16 < Dk; q += 2) {
         float x[16];
@@ -705,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         tc::tmem_ld_wait();
         if (row64 >= 0)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dot = fmaf(x[j], xh[row64 * Dk + q * 16 + j], dot);
+          for (int j = 0; j < 16; ++j) dot = fmaf(x[j], tile_get(xt, Dk, q * 16 + j, row64), dot);
       }
       if (row64 >= 0) part[half * C + row64] = dot;
       __syncthreads();
@@ -723,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
           __align__(16) __nv_bfloat162 pk[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float a = (x[2 * j] - xh[r * Dk + q * 16 + 2 * j] * d) * inv;
-            const float b2 = (x[2 * j + 1] - xh[r * Dk + q * 16 + 2 * j + 1] * d) * inv;
+            const float a = (x[2 * j] - tile_get(xt, Dk, q * 16 + 2 * j, r) * d) * inv;
+            const float b2 = (x[2 * j + 1] - tile_get(xt, Dk, q * 16 + 2 * j + 1, r) * d) * inv;
             pk[j] = __floats2bfloat162_rn(a, b2);
           }
           uint4* o = (uint4*)(dst + (int64_t)r * ld + q * 16);

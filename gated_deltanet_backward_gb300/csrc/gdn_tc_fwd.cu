@@ -192,12 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
 #pragma unroll
         for (int q = 0; q < 4; ++q) pk[q] = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
         *(uint4*)(tAQK + tc::sw128_offset(row, c0, 128)) = *(const uint4*)pk;
-        if (bwd) {
-          float* dst = (isq ? p.Qn : p.Kn) + (ck + t) * Dk + c0;
-          *(float4*)dst = make_float4(x[0], x[1], x[2], x[3]);
-          *(float4*)(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
-          if (c0 == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
-        }
+        if (bwd && c0 == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
       }
     }
   }
@@ -341,8 +336,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
         // U^T as a [Dv][C] SW128 tile, so that row reads by the state walks are conflict-free
         tile_put16((uint8_t*)(p.Utb + ch * Dv * C), Dv, vv, col0, v);
       });
-      if (bwd)
-        for (int i = tid; i < C * C; i += kThreads) p.Tm[ch * C * C + i] = T[i];
+      if (bwd) {
+        // T, T^T and diag(b e^G) T^T as bf16 tiles, written straight to the workspace
+        uint8_t* tb = p.Tb + ch * 3 * 8192;
+        for (int idx = tid; idx < 3 * C * (C / 8); idx += kThreads) {
+          const int which = idx / (C * (C / 8)), rem = idx % (C * (C / 8));
+          const int row = rem % C, c8 = (rem / C) * 8;
+          __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float a, b2;
+            if (which == 0) {
+              a = T[row * C + c8 + 2 * u];
+              b2 = T[row * C + c8 + 2 * u + 1];
+            } else {
+              a = T[(c8 + 2 * u) * C + row];
+              b2 = T[(c8 + 2 * u + 1) * C + row];
+              if (which == 2) {
+                a *= w[row];
+                b2 *= w[row];
+              }
+            }
+            pk[u] = __floats2bfloat162_rn(a, b2);
+          }
+          *(uint4*)(tb + which * 8192 + tc::sw128_offset(row, c8, C)) = *(const uint4*)pk;
+        }
+      }
       __syncthreads();
       cta_copy16(p.Wsw + ch * tileCD(Dk), tOW, (uint32_t)tileCD(Dk));
       cta_copy16(p.Psw + ch * tileCD(64), tOP, 8192);
@@ -447,16 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     const int i = c - c0, b = i & 1;
     const int64_t t0 = s0 + (int64_t)i * C;
     const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
-    // chunk-start state, saved transposed ([Dv][Dk]): row v is this thread's
-    float* sv = p.saved + ((size_t)c * p.Hv + h) * SZ + (size_t)vrow * DK;
+    // chunk-start state: for each k, the warp's lanes write consecutive v (128-byte rows)
+    float* sv = p.saved + ((size_t)c * p.Hv + h) * SZ;
     if (vok)
 #pragma unroll
       for (int ii = 0; ii < NKC; ++ii)
         if (half * 16 + 32 * ii < DK)
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            *(float4*)(sv + half * 16 + 32 * ii + j) =
-                make_float4(S[ii][j], S[ii][j + 1], S[ii][j + 2], S[ii][j + 3]);
+          for (int j = 0; j < 16; ++j) sv[(size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = S[ii][j];
     // tiles of this chunk
     const bool lok = tc::mbar_wait(&bars[1 + b], b ? lphase1 : lphase0);
     if (b) lphase1 ^= 1u; else lphase0 ^= 1u;

@@ -32,9 +32,8 @@
  *    states and d alpha, d beta_raw, d a_log, d dt_bias are fp32.  State and
  *    accumulation arithmetic is fp32.  bf16 outputs are rounded to nearest even.
  *  - State tensors (S_0, S_T, dS_T, dS_0) are [n_seqs, Hv, Dk, Dv] fp32,
- *    contiguous.  Saved states are [total_chunks, Hv, Dv, Dk] fp32: the state at
- *    the START of each 64-token chunk, stored TRANSPOSED (S^T, so that each
- *    value column of S is contiguous; chunks never span two sequences; the last
+ *    contiguous.  Saved states are [total_chunks, Hv, Dk, Dv] fp32: the state at
+ *    the START of each 64-token chunk (chunks never span two sequences; the last
  *    chunk of a sequence may be short; the chunks of sequence n are numbered
  *    from chunk_offsets[n]).
  *  - Pointers marked "device" are CUDA device pointers; "host" ones are host

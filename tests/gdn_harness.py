@@ -94,9 +94,8 @@ class DeviceRun:
         out = dict(o=self.o.double().cpu().numpy(), S_T=self.S_T.double().cpu().numpy())
         wl = self.inp.wl
         nbytes = wl.total_chunks * wl.Hv * wl.Dk * wl.Dv
-        # the library stores chunk-start states transposed ([.., Dv, Dk]); compare as S
         out["saved"] = self.layer.saved_states[:nbytes].double().cpu().numpy().reshape(
-            wl.total_chunks, wl.Hv, wl.Dv, wl.Dk).transpose(0, 1, 3, 2)
+            wl.total_chunks, wl.Hv, wl.Dk, wl.Dv)
         if self.grads is not None:
             for k, v in self.grads.items():
                 out[k] = v.double().cpu().numpy()
