@@ -118,32 +118,40 @@ def kernel_models(wl: W.Workload):
              NC * Hv * 2 * C * Dk * f4 + T * Hv * Dv * es + T * Hv * 2 * 4)
     bgr_f = NC * Hv * (12 * C * Dk * Dv + 2 * C * C * (5 * Dk + 3 * Dv) + 4 * C ** 3)
     bqk_b = NC * Hv * 2 * C * Dk * f4 + NC * Hk * C * 2 * (Dk + 1) * f4 + T * Hk * 2 * Dk * es
-    # tensor-core (bf16) kernels
-    sKC = (Dk + 63) // 64 * C * 128                  # bf16 [C][Dk] tile
-    sKt = Dk * 128                                   # bf16 [Dk][C] tile
-    tc_prep_b = (T * (2 * Hk * Dk * es + Hv * Dv * es + 2 * Hv * 4) + NC * Hk * 3 * sKC +
-                 NC * Hv * (sKC + C * C * 2 + Dv * C * 2 + 2 * C * 4))
+    # tensor-core (bf16) kernels: every operand handed between kernels is a bf16
+    # 128B-swizzled tile; the bytes below are each kernel's reads plus writes of
+    # distinct data (a key-head tile read by its r value-head CTAs counts once)
+    sKC = (Dk + 63) // 64 * C * 128                  # [C][Dk] tile
+    sVC = (Dv + 63) // 64 * C * 128                  # [C][Dv] tile
+    sKt, sVt, sCC = Dk * 128, Dv * 128, C * C * 2    # [Dk][C], [Dv][C], [C][C] tiles
+    sDD = (Dv + 63) // 64 * Dk * 128                 # [Dk][Dv] tile
+    tok_in = T * (2 * Hk * Dk * es + Hv * Dv * es + 2 * Hv * 4)   # q, k, v, alpha, beta
+    tc_prep_b = (tok_in + NC * Hk * (2 * sKC + sKt) +
+                 NC * Hv * (2 * C * 4 + sVt + sKC + sCC))           # Q, K, K^T; G, b, U^T, W, P
     tc_prep_f = (NC * Hk * 2 * 128 * C * Dk + NC * Hv * (2 * C * C * (Dk + Dv) + C ** 3 / 3 +
                                                           C * C * 8))
-    tc_prep_bwd_b = tc_prep_b + (NC * Hk * (C * Dk * 8 + C * 8 + 2 * C * C * 4 + sKt) +
-                                 NC * Hv * (C * (Dk + Dv) * 4 + C * C * 4 + sKt + C * C * 2))
-    fst_tc_b = (NC * Hv * (sKC + C * C * 2 + Dv * C * 2 + C * 4) + NC * Hk * (sKC + sKt) +
-                T * Hv * Dv * es + NC * Hv * Dk * Dv * 4)
+    tc_prep_bwd_b = tc_prep_b + (NC * Hk * (2 * C * 4 + C * C * 4 + sKt) +   # norms, K K^T, Q^T
+                                 NC * Hv * (sKt + sCC + 3 * sCC))            # W^T, P^T, T tiles
+    st = N * Hv * Dk * Dv * 4
+    fst_st = st * ((wl.S0_std > 0) + 1)                             # S0 read, S_T written
+    bst_st = st * ((wl.dST_std > 0) + 1)                            # dS_T read, dS0 written
+    fst_tc_b = (NC * Hk * (sKC + sKt) + NC * Hv * (sKC + sCC + sVt + C * 4) +
+                T * Hv * Dv * es + NC * Hv * Dk * Dv * 4 + fst_st)  # ... o, saved states
     fst_tc_f = NC * Hv * (6 * C * Dk * Dv + 2 * C * C * Dv)
-    bst_tc_b = (NC * Hk * (sKC + sKt) + NC * Hv * (C * C * 2 + sKt + C * 4) + T * Hv * Dv * es +
-                NC * Hv * (Dk * Dv + C * Dv) * 4)
+    bst_tc_b = (NC * Hk * (sKC + sKt) + NC * Hv * (sCC + sKt + C * 4) + T * Hv * Dv * es +
+                NC * Hv * (sDD + sVC + sVt) + bst_st)               # ... dS, dDelta, dDelta^T
     bst_tc_f = NC * Hv * (2 * C * C * Dv + 6 * C * Dk * Dv)
-    bgr_tc_b = (NC * Hv * (2 * Dk * Dv * 4 + 2 * C * Dv * 4 + sKC + Dv * C * 2 + C * C * 2 +
-                           2 * C * C * 4 + 3 * C * 4) + T * Hv * (2 * Dv * es + 4) +
-                NC * Hk * (2 * C * Dk * 4 + C * C * 4 + 2 * sKt + 2 * C * 4) +
-                T * Hk * 2 * Dk * es + T * Hv * (Dv * es + 8) + NC * Hv * 8)
+    bgr_tc_b = (NC * Hk * (2 * sKt + C * C * 4 + 2 * C * 4) + T * Hk * 2 * Dk * es +
+                NC * Hv * (Dk * Dv * 4 + 2 * C * 4 + sKC + sVt + sVC + sCC + sDD + sVt +
+                           3 * sCC + 8) +
+                T * Hv * (2 * Dv * es + 4) + T * Hv * (Dv * es + 8))
     bgr_tc_f = NC * Hv * (2 * C * Dk * Dv + 2 * 128 * Dk * Dv + 2 * C * Dk * Dv +
                           4 * C * Dk * Dv + 2 * C * C * Dv + 2 * C * C * (Dv + Dk) +
                           4 * C * C * Dk + 2 * C * C * Dv + 4 * C ** 3 + 4 * C * C * Dk +
                           2 * C * C * Dk)
     return {
         "gdn_prep_tc": (tc_prep_b, tc_prep_f, "tensor"),
-        "gdn_prep_tc_bwd": (tc_prep_bwd_b, tc_prep_f, "tensor"),
+        "gdn_prep_tc_full": (tc_prep_bwd_b, tc_prep_f, "tensor"),
         "gdn_fwd_state_tc": (fst_tc_b, fst_tc_f, "tensor"),
         "gdn_bwd_state_tc": (bst_tc_b, bst_tc_f, "tensor"),
         "gdn_bwd_grads_tc": (bgr_tc_b, bgr_tc_f, "tensor"),
@@ -274,11 +282,11 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
 
     def fwd():
-        layer.forward(q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream)
+        layer.forward(q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream, train=True)
 
     def bwd():
         layer.backward(q, k, v, alpha, beta_raw, a_log, dt_bias, S0, dO, dS_T, dq, dk, dv,
-                       dalpha, dbeta, da_log, ddt, dS0, stream)
+                       dalpha, dbeta, da_log, ddt, dS0, stream, train=True)
 
     for _ in range(args.warmup):
         fwd()
@@ -355,6 +363,8 @@ def run_ours(args):
                    "compute": ("tcgen05 bf16 MMA, fp32 accumulate and state" if wl.dtype == "bf16"
                                else "fp32 CUDA-core FMA"),
                    "l2": "flushed: 256 MB write between timed steps",
+                   "step": "training step: the forward keeps its chunk operands for the "
+                           "backward (GDN_FLAG_KEEP_FOR_BACKWARD / GDN_FLAG_REUSE_FORWARD)",
                    "parallelism": "independent batch per GPU" if world > 1 else "single GPU"},
         "fwd_ms": sum(f_ms) / K, "bwd_ms": sum(b_ms) / K,
         "roofline": roof, "path_roofline": path_roof, "kernels": kernels,
@@ -404,11 +414,11 @@ def run_e2e(args, inp, layer, device, tdt, world):
         S0 = None if d_in["S0"] is None else d_in["S0"]
         dS_T = None if d_in["dS_T"] is None else d_in["dS_T"]
         layer.forward(q, k, v, d_in["alpha"], d_in["beta_raw"], d_in["a_log"], d_in["dt_bias"],
-                      S0, d_out["o"], d_out["S_T"].view(N, Hv, Dk, Dv), stream)
+                      S0, d_out["o"], d_out["S_T"].view(N, Hv, Dk, Dv), stream, train=True)
         layer.backward(q, k, v, d_in["alpha"], d_in["beta_raw"], d_in["a_log"],
                        d_in["dt_bias"], S0, d_in["dO"], dS_T, d_out["dq"], d_out["dk"],
                        d_out["dv"], d_out["dalpha"], d_out["dbeta"], d_out["da_log"],
-                       d_out["ddt"], d_out["dS0"].view(N, Hv, Dk, Dv), stream)
+                       d_out["ddt"], d_out["dS0"].view(N, Hv, Dk, Dv), stream, train=True)
         for key, h in h_out.items():
             h.copy_(d_out[key], non_blocking=True)
 

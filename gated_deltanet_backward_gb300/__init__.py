@@ -33,6 +33,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 GDN_OK = 0
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
+GDN_FLAG_KEEP_FOR_BACKWARD = 1
+GDN_FLAG_REUSE_FORWARD = 2
+GDN_ERR_NOT_KEPT = -8
 CHUNK = 64
 
 
@@ -56,16 +59,17 @@ _lib.gdn_saved_state_bytes.restype = _sz
 _lib.gdn_workspace_bytes.argtypes = [_SP, ctypes.c_int]
 _lib.gdn_workspace_bytes.restype = _sz
 # shape; q,k,v,alpha,beta_raw (+ld); a_log, dt_bias, cu, coff, S0; o (+ld); S_T, saved, ws,
-# ws bytes, stream
+# ws bytes, flags, stream
+_u32 = ctypes.c_uint32
 _lib.gdn_forward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] +
-                             [_vp, _vp, _vp, _sz, _vp])
+                             [_vp, _vp, _vp, _sz, _u32, _vp])
 _lib.gdn_forward.restype = ctypes.c_int
 # shape; q,k,v,alpha,beta_raw (+ld); a_log, dt_bias, cu, coff, S0; dO (+ld); dS_T, saved;
-# dq,dk,dv,dalpha,dbeta_raw (+ld); da_log, ddt_bias, dS0, ws, ws bytes, stream
+# dq,dk,dv,dalpha,dbeta_raw (+ld); da_log, ddt_bias, dS0, ws, ws bytes, flags, stream
 _lib.gdn_backward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] + [_vp, _vp] +
-                              [_vp, _i64] * 5 + [_vp, _vp, _vp, _vp, _sz, _vp])
+                              [_vp, _i64] * 5 + [_vp, _vp, _vp, _vp, _sz, _u32, _vp])
 _lib.gdn_backward.restype = ctypes.c_int
-# as gdn_forward without the workspace and its size
+# as gdn_forward without the workspace, its size and the flags
 _lib.gdn_forward_noalloc.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] +
                                      [_vp, _vp, _vp])
 _lib.gdn_forward_noalloc.restype = ctypes.c_int
@@ -163,22 +167,24 @@ def _stream(stream) -> Optional[int]:
 
 
 def gdn_forward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, chunk_offsets, S0,
-                o, S_T, saved_states, workspace, stream=None) -> None:
-    """Calls gdn_forward.  All tensors are CUDA tensors (S0 / S_T may be None)."""
+                o, S_T, saved_states, workspace, stream=None, flags=0) -> None:
+    """Calls gdn_forward.  All tensors are CUDA tensors (S0 / S_T may be None).
+    flags: 0 or GDN_FLAG_KEEP_FOR_BACKWARD (workspace then of the backward's size)."""
     args = [ctypes.byref(shape)]
     for t in (q, k, v, alpha, beta_raw):
         args += list(_mat(t))
     args += [_ptr(a_log), _ptr(dt_bias), _ptr(cu_seqlens), _ptr(chunk_offsets), _ptr(S0)]
     args += list(_mat(o))
     args += [_ptr(S_T), _ptr(saved_states), _ptr(workspace),
-             int(workspace.numel() * workspace.element_size()), _stream(stream)]
+             int(workspace.numel() * workspace.element_size()), int(flags), _stream(stream)]
     _check(_lib.gdn_forward(*args), "gdn_forward")
 
 
 def gdn_backward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, chunk_offsets, S0,
                  dO, dS_T, saved_states, dq, dk, dv, dalpha, dbeta_raw, da_log, ddt_bias, dS0,
-                 workspace, stream=None) -> None:
-    """Calls gdn_backward.  All tensors are CUDA tensors (S0, dS_T, dS0 may be None)."""
+                 workspace, stream=None, flags=0) -> None:
+    """Calls gdn_backward.  All tensors are CUDA tensors (S0, dS_T, dS0 may be None).
+    flags: 0 or GDN_FLAG_REUSE_FORWARD (workspace then the one a keeping forward used)."""
     args = [ctypes.byref(shape)]
     for t in (q, k, v, alpha, beta_raw):
         args += list(_mat(t))
@@ -188,7 +194,7 @@ def gdn_backward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, ch
     for t in (dq, dk, dv, dalpha, dbeta_raw):
         args += list(_mat(t))
     args += [_ptr(da_log), _ptr(ddt_bias), _ptr(dS0), _ptr(workspace),
-             int(workspace.numel() * workspace.element_size()), _stream(stream)]
+             int(workspace.numel() * workspace.element_size()), int(flags), _stream(stream)]
     _check(_lib.gdn_backward(*args), "gdn_backward")
 
 
@@ -251,7 +257,10 @@ class Layer:
     """Device buffers for one varlen batch: shape, plan, saved states, workspaces.
 
     A convenience holder for callers of gdn_forward / gdn_backward; it only
-    allocates (through PyTorch) and forwards arguments.
+    allocates (through PyTorch) and forwards arguments.  ``train=True`` runs the
+    pair as a training step: the forward keeps the backward's chunk operands in
+    the backward workspace (GDN_FLAG_KEEP_FOR_BACKWARD) and the backward reuses
+    them (GDN_FLAG_REUSE_FORWARD) instead of recomputing them.
     """
     shape: gdn_shape
     cu_seqlens: object
@@ -275,16 +284,21 @@ class Layer:
         return cls(shape, torch.from_numpy(cu).to(device), torch.from_numpy(off).to(device),
                    saved, ws_f, ws_b)
 
-    def forward(self, q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream=None):
+    def forward(self, q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream=None,
+                train=False):
         gdn_forward(self.shape, q, k, v, alpha, beta_raw, a_log, dt_bias, self.cu_seqlens,
-                    self.chunk_offsets, S0, o, S_T, self.saved_states, self.ws_fwd, stream)
+                    self.chunk_offsets, S0, o, S_T, self.saved_states,
+                    self.ws_bwd if train else self.ws_fwd, stream,
+                    GDN_FLAG_KEEP_FOR_BACKWARD if train else 0)
 
     def backward(self, q, k, v, alpha, beta_raw, a_log, dt_bias, S0, dO, dS_T, dq, dk, dv,
-                 dalpha, dbeta_raw, da_log, ddt_bias, dS0, stream=None):
+                 dalpha, dbeta_raw, da_log, ddt_bias, dS0, stream=None, train=False):
         gdn_backward(self.shape, q, k, v, alpha, beta_raw, a_log, dt_bias, self.cu_seqlens,
                      self.chunk_offsets, S0, dO, dS_T, self.saved_states, dq, dk, dv, dalpha,
-                     dbeta_raw, da_log, ddt_bias, dS0, self.ws_bwd, stream)
+                     dbeta_raw, da_log, ddt_bias, dS0, self.ws_bwd, stream,
+                     GDN_FLAG_REUSE_FORWARD if train else 0)
 
 
 __all__ = list(EXPORTED) + ["gdn_profile", "gdn_shape", "make_shape", "Layer", "GdnError", "LIB_PATH", "CHUNK",
-                            "GDN_DTYPE_F32", "GDN_DTYPE_BF16"]
+                            "GDN_DTYPE_F32", "GDN_DTYPE_BF16", "GDN_FLAG_KEEP_FOR_BACKWARD",
+                            "GDN_FLAG_REUSE_FORWARD", "GDN_ERR_NOT_KEPT"]

@@ -162,6 +162,21 @@ int check_workspace(const gdn_shape* s, void* ws, size_t bytes, bool bwd) {
   return GDN_OK;
 }
 
+// Tag of a shape (FNV-1a over its fields, never 0): a keeping forward stamps it
+// into the workspace's status block and a reusing backward compares it.
+uint32_t shape_tag(const gdn_shape* s) {
+  const int64_t f[9] = {s->Hk, s->Hv, s->Dk, s->Dv, s->n_seqs, s->total_chunks, s->total_tokens,
+                        s->dtype, 0};
+  uint32_t h = 2166136261u;
+  auto mix = [&](const void* data, size_t n) {
+    const unsigned char* b = (const unsigned char*)data;
+    for (size_t i = 0; i < n; ++i) h = (h ^ b[i]) * 16777619u;
+  };
+  mix(f, sizeof(int64_t) * 8);
+  mix(&s->scale, sizeof(float));
+  return h | 1u;
+}
+
 thread_local char g_last_error[160] = "";
 
 // Records which CUDA call failed (see gdn_last_error) and returns GDN_ERR_CUDA.
@@ -270,7 +285,7 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_FWD_STATE_TC: return "gdn_fwd_state_tc";
     case gdn::KID_BWD_STATE_TC: return "gdn_bwd_state_tc";
     case gdn::KID_BWD_GRADS_TC: return "gdn_bwd_grads_tc";
-    case gdn::KID_PREP_TC_BWD: return "gdn_prep_tc_bwd";
+    case gdn::KID_PREP_TC_FULL: return "gdn_prep_tc_full";
     default: return "?";
   }
 }
@@ -308,19 +323,25 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
                 const float* beta_raw, int64_t beta_ld, const float* a_log,
                 const float* dt_bias, const int32_t* cu_seqlens, const int32_t* chunk_offsets,
                 const float* S0, void* o, int64_t o_ld, float* S_T, float* saved_states,
-                void* workspace, size_t workspace_bytes, void* stream) {
+                void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
   GDN_TRY(check_shape(s));
+  if (flags & ~(uint32_t)GDN_FLAG_KEEP_FOR_BACKWARD) return GDN_ERR_INVALID_ARG;
+  const bool keep = (flags & GDN_FLAG_KEEP_FOR_BACKWARD) != 0;
   GDN_TRY(check_inputs(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
                        dt_bias, cu_seqlens, chunk_offsets, S0));
   const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
   GDN_TRY(check_matrix(o, o_ld, (int64_t)s->Hv * s->Dv, es, s->total_tokens));
   GDN_TRY(check_vec(S_T, false));
   GDN_TRY(check_vec(saved_states, s->total_chunks > 0));
-  GDN_TRY(check_workspace(s, workspace, workspace_bytes, false));
+  GDN_TRY(check_workspace(s, workspace, workspace_bytes, keep));
   cudaStream_t st = (cudaStream_t)stream;
   Params p;
+  // a keeping forward carves the backward's layout, whose forward regions sit
+  // at the same offsets as the backward will read them
   fill_common(p, s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
-              dt_bias, cu_seqlens, chunk_offsets, S0, workspace, false);
+              dt_bias, cu_seqlens, chunk_offsets, S0, workspace, keep);
+  p.keep = keep ? 1 : 0;
+  p.tag = shape_tag(s);
   p.o = o;
   p.o_ld = o_ld;
   p.S_T = S_T;
@@ -361,8 +382,9 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
                  const float* saved_states, void* dq, int64_t dq_ld, void* dk, int64_t dk_ld,
                  void* dv, int64_t dv_ld, float* dalpha, int64_t dalpha_ld, float* dbeta_raw,
                  int64_t dbeta_ld, float* da_log, float* ddt_bias, float* dS0, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+                 size_t workspace_bytes, uint32_t flags, void* stream) {
   GDN_TRY(check_shape(s));
+  if (flags & ~(uint32_t)GDN_FLAG_REUSE_FORWARD) return GDN_ERR_INVALID_ARG;
   GDN_TRY(check_inputs(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
                        dt_bias, cu_seqlens, chunk_offsets, S0));
   const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
@@ -400,9 +422,13 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
   p.da_log = da_log;
   p.ddt_bias = ddt_bias;
   p.dS0 = dS0;
+  // with no chunk there is nothing to reuse: the flag is then a no-op
+  p.reuse = (flags & GDN_FLAG_REUSE_FORWARD) != 0 && s->total_chunks > 0 ? 1 : 0;
+  p.tag = shape_tag(s);
   (void)cudaGetLastError();  // report only errors of this call's own launches
   g_last_error[0] = 0;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, st);
+  // a reusing backward keeps the forward's tag (it sits after the status word)
+  cudaError_t e = cudaMemsetAsync(workspace, 0, p.reuse ? sizeof(int32_t) * 2 : 256, st);
   if (e != cudaSuccess) return cuda_fail("gdn_backward: clearing the status word", e);
   if (s->total_chunks == 0 && s->n_seqs > 0 && dS0) {
     const size_t bytes = (size_t)s->n_seqs * s->Hv * s->Dk * s->Dv * sizeof(float);
@@ -448,6 +474,7 @@ const char* gdn_status_string(int status) {
     case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
     case GDN_ERR_DEVICE_BOUNDS: return "GDN_ERR_DEVICE_BOUNDS";
+    case GDN_ERR_NOT_KEPT: return "GDN_ERR_NOT_KEPT";
     default: return "GDN_UNKNOWN_STATUS";
   }
 }

@@ -17,6 +17,7 @@ namespace gdn {
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_bwd_state(Params p, int DVS) {
+  if (kept_operands_missing(p)) return;
   extern __shared__ __align__(16) float sm[];
   const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * DVS;
   const int kh = h / p.r, Dk = p.Dk, Dv = p.Dv, C = kChunk;
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_state(Params p, int DVS) {
 // the dQh / dKh workspace partials; k_bwd_qk sums them per key head.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
+  if (kept_operands_missing(p)) return;
   extern __shared__ __align__(16) float sm[];
   const int c = blockIdx.x, h = blockIdx.y, kh = h / p.r;
   int n;
@@ -359,6 +361,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
 // dx = (dx_hat - x_hat (x_hat . dx_hat)) / sqrt(|x|^2 + 1e-6).
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_bwd_qk(Params p) {
+  if (kept_operands_missing(p)) return;
   const int c = blockIdx.x, kh = blockIdx.y;
   int n;
   int64_t t0;
@@ -399,6 +402,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_qk(Params p) {
 }
 
 __global__ void k_bwd_gates(Params p) {
+  if (kept_operands_missing(p)) return;
   for (int h = threadIdx.x; h < p.Hv; h += blockDim.x) {
     float a = 0.f, d = 0.f;
     for (int c = 0; c < p.NC; ++c) {
@@ -450,12 +454,16 @@ cudaError_t launch_backward(const Params& p, const TmaMaps* maps, cudaStream_t s
   }
   if (bf16) {
     // bf16 inputs: tensor-core preparation, reverse state walk and gradients
-    cudaError_t e = launch_prep_tc(p, *maps, true, st);
-    if (e != cudaSuccess) return e;
+    if (!p.reuse) {
+      cudaError_t e = launch_prep_tc(p, *maps, true, st);
+      if (e != cudaSuccess) return e;
+    }
     return launch_bwd_tc(p, *maps, st);
   }
-  cudaError_t e = launch_prep(p, bf16, true, st);
-  if (e != cudaSuccess) return e;
+  if (!p.reuse) {
+    cudaError_t e = launch_prep(p, bf16, true, st);
+    if (e != cudaSuccess) return e;
+  }
   return launch_backward_t<float>(p, st);
 }
 

@@ -21,6 +21,20 @@ __device__ __forceinline__ void set_status(DeviceStatus* st, int code, int detai
   if (atomicCAS(&st->code, 0, code) == 0) st->detail = detail;
 }
 
+// A reusing backward whose workspace does not carry this shape's tag records
+// GDN_ERR_NOT_KEPT and does nothing.  Every backward kernel asks first.
+__device__ __forceinline__ bool kept_operands_missing(const Params& p) {
+  if (!p.reuse) return false;
+  if (*(volatile const uint32_t*)&p.status->tag == p.tag) return false;
+  if (threadIdx.x == 0) set_status(p.status, GDN_ERR_NOT_KEPT, 0);
+  return true;
+}
+
+// The first CTA of a keeping forward's preparation stamps the workspace.
+__device__ __forceinline__ void stamp_kept_operands(const Params& p) {
+  if (p.keep && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.status->tag = p.tag;
+}
+
 // softplus(x) = log(1 + e^x) in the overflow-free form max(x,0) + log1p(e^-|x|).
 __device__ __forceinline__ float softplus_f(float x) {
   return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));

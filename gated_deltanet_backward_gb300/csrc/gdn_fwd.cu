@@ -14,6 +14,7 @@ namespace gdn {
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_prep(Params p, int write_T) {
+  stamp_kept_operands(p);
   extern __shared__ __align__(16) float sm[];
   const int c = blockIdx.x, kh = blockIdx.y;
   int n;
@@ -223,11 +224,11 @@ cudaError_t launch_forward(const Params& p, const TmaMaps* maps, cudaStream_t st
   const bool bf16 = maps != nullptr;
   if (bf16) {
     // bf16 inputs: tensor-core chunk preparation and state walk
-    cudaError_t e = launch_prep_tc(p, *maps, false, st);
+    cudaError_t e = launch_prep_tc(p, *maps, p.keep != 0, st);
     if (e != cudaSuccess) return e;
     return launch_fwd_state_tc(p, st);
   }
-  cudaError_t e = launch_prep(p, bf16, false, st);
+  cudaError_t e = launch_prep(p, bf16, p.keep != 0, st);
   if (e != cudaSuccess || p.n_seqs == 0) return e;
   const int DVS = p.Dv < 32 ? p.Dv : 32;
   const size_t smem = sizeof(float) * ((size_t)p.Dk * DVS + (size_t)kChunk * DVS +

@@ -30,6 +30,7 @@ constexpr int kThreads = 256;  // threads per CTA of every kernel
 struct DeviceStatus {
   int32_t code;    // first gdn_status recorded by a kernel (0 = OK)
   int32_t detail;  // kernel-specific detail (e.g. the chunk index)
+  uint32_t tag;    // shape tag of a forward that kept the backward's operands (0 = none)
 };
 
 // Byte offsets of the workspace regions (fp32 unless noted; 0 = not allocated).
@@ -169,6 +170,9 @@ struct Params {
   float* ddt_bias;
   float* dS0;
   DeviceStatus* status;
+  uint32_t tag;  // shape tag (see shape_tag); written by a keeping forward, checked by a reusing backward
+  int keep;      // forward: leave the backward's chunk operands in the workspace
+  int reuse;     // backward: read them from the workspace instead of recomputing them
   float* Qn;
   float* Kn;
   float* nq;
@@ -212,7 +216,7 @@ enum KernelId {
   KID_FWD_STATE_TC = 7,
   KID_BWD_STATE_TC = 8,
   KID_BWD_GRADS_TC = 9,
-  KID_PREP_TC_BWD = 10,
+  KID_PREP_TC_FULL = 10,
   KID_COUNT = 11
 };
 

@@ -58,7 +58,7 @@ extern "C" int gdn_forward_noalloc(const gdn_shape* s, const void* q, int64_t q_
   if (need == 0)  // invalid shape: let the regular entry point name the problem
     return gdn_forward(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
                        dt_bias, cu_seqlens, chunk_offsets, S0, o, o_ld, S_T, saved_states,
-                       nullptr, 0, stream);
+                       nullptr, 0, 0u, stream);
   if (need > kScratchBytes) {
     gdn::set_last_error(
         "gdn_forward_noalloc: this shape needs more scratch than the built-in "
@@ -75,5 +75,5 @@ extern "C" int gdn_forward_noalloc(const gdn_shape* s, const void* q, int64_t q_
   // region is fully written before it is read.
   return gdn_forward(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
                      dt_bias, cu_seqlens, chunk_offsets, S0, o, o_ld, S_T, saved_states,
-                     scratch, kScratchBytes, stream);
+                     scratch, kScratchBytes, 0u, stream);
 }

@@ -27,6 +27,7 @@ __device__ __forceinline__ size_t tileDC(int D) { return (size_t)D * 128; }
 template <int DK>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
+  if (kept_operands_missing(p)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int n = blockIdx.x, h = blockIdx.y, kh = h / p.r;
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
 // TMEM (512 columns): dQ_hat @0, dK_hat @128 (M = 64 accumulators), scratch @256.
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
+  if (kept_operands_missing(p)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int c = blockIdx.x, kh = blockIdx.y;
@@ -759,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
 }
 
 __global__ void k_bwd_gates_tc(Params p) {
+  if (kept_operands_missing(p)) return;
   for (int h = threadIdx.x; h < p.Hv; h += blockDim.x) {
     float a = 0.f, d = 0.f;
     for (int c = 0; c < p.NC; ++c) {

@@ -90,6 +90,7 @@ __device__ void tri_inverse(float* Tm, int nh, float* Mt) {
 __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
                                                           const __grid_constant__ TmaMaps maps,
                                                           int bwd) {
+  stamp_kept_operands(p);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int c = blockIdx.x, kh = blockIdx.y;
@@ -601,7 +602,7 @@ cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaS
   if (p.NC == 0) return cudaSuccess;
   const size_t smem = prep_tc_smem(p);
   cudaFuncSetAttribute(k_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  profile_pre(st, bwd ? KID_PREP_TC_BWD : KID_PREP_TC);
+  profile_pre(st, bwd ? KID_PREP_TC_FULL : KID_PREP_TC);
   k_prep_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, maps, bwd ? 1 : 0);
   profile_post(st);
   return cudaGetLastError();

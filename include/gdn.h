@@ -72,10 +72,32 @@ typedef enum {
   GDN_ERR_CUDA = -4,          /* a CUDA runtime call or a launch failed */
   GDN_ERR_TIMEOUT = -5,       /* a bounded device-side wait ran out (device status) */
   GDN_ERR_WORKSPACE = -6,     /* workspace too small or misaligned */
-  GDN_ERR_DEVICE_BOUNDS = -7  /* device-side check: chunk or token index out of range */
+  GDN_ERR_DEVICE_BOUNDS = -7, /* device-side check: chunk or token index out of range */
+  GDN_ERR_NOT_KEPT = -8       /* GDN_FLAG_REUSE_FORWARD given a workspace that holds no
+                                 kept forward of this shape (device status) */
 } gdn_status;
 
 typedef enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
+
+/* Call flags (the `flags` argument of gdn_forward / gdn_backward).
+ *
+ * A training step runs the forward and then, on the same inputs, the backward.
+ * Both need the same per-chunk operands (normalised q/k tiles, the gates, the
+ * inverse T = (I + A)^-1 and W, U, P of each chunk and value head).  With
+ * GDN_FLAG_KEEP_FOR_BACKWARD the forward leaves them in its workspace, which
+ * must then be gdn_workspace_bytes(shape, 1) bytes, and stamps the workspace
+ * with a tag of the shape.  The backward, given that same workspace untouched
+ * in between and GDN_FLAG_REUSE_FORWARD, reads them instead of recomputing
+ * them.  Results are bit-identical to a backward without the flag.  A REUSE
+ * backward whose workspace carries no matching tag computes nothing and
+ * records GDN_ERR_NOT_KEPT as its device status; the host cannot see the tag
+ * without synchronising, so the call itself returns GDN_OK.  Keeping the
+ * operands for inputs that then change before the backward is the caller's
+ * error and is not detected. */
+typedef enum {
+  GDN_FLAG_KEEP_FOR_BACKWARD = 1, /* gdn_forward only */
+  GDN_FLAG_REUSE_FORWARD = 2      /* gdn_backward only */
+} gdn_flag;
 
 typedef struct {
   int32_t Hk;           /* key heads (q and k heads) */
@@ -118,6 +140,8 @@ size_t gdn_workspace_bytes(const gdn_shape* shape, int is_backward);
  *   saved_states device, gdn_saved_state_bytes() bytes (written; the backward
  *             reads it)
  *   workspace device scratch, gdn_workspace_bytes(shape, 0) bytes
+ *             (gdn_workspace_bytes(shape, 1) with GDN_FLAG_KEEP_FOR_BACKWARD)
+ *   flags     0 or GDN_FLAG_KEEP_FOR_BACKWARD
  * Returns a gdn_status. */
 int gdn_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
                 int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
@@ -125,7 +149,7 @@ int gdn_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void*
                 const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
                 const int32_t* chunk_offsets, const float* S0, void* o, int64_t o_ld,
                 float* S_T, float* saved_states, void* workspace, size_t workspace_bytes,
-                void* stream);
+                uint32_t flags, void* stream);
 
 /* Backward (reverse chunk walk with a dS carry).  Inputs as gdn_forward, plus
  *   dO        device, [total_tokens, dO_ld] dtype: dL/do
@@ -139,7 +163,9 @@ int gdn_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void*
  *   dbeta_raw device, [total_tokens, dbeta_ld] fp32: dL/d beta_raw
  *   da_log, ddt_bias device, [Hv] fp32, summed over every token of every sequence
  *   dS0       device, [n_seqs, Hv, Dk, Dv] fp32: dL/dS_0, or NULL to skip
- *   workspace device scratch, gdn_workspace_bytes(shape, 1) bytes
+ *   workspace device scratch, gdn_workspace_bytes(shape, 1) bytes; with
+ *             GDN_FLAG_REUSE_FORWARD, the workspace of the kept forward
+ *   flags     0 or GDN_FLAG_REUSE_FORWARD
  * Returns a gdn_status. */
 int gdn_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
                  int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
@@ -150,7 +176,7 @@ int gdn_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void
                  void* dk, int64_t dk_ld, void* dv, int64_t dv_ld, float* dalpha,
                  int64_t dalpha_ld, float* dbeta_raw, int64_t dbeta_ld, float* da_log,
                  float* ddt_bias, float* dS0, void* workspace, size_t workspace_bytes,
-                 void* stream);
+                 uint32_t flags, void* stream);
 
 /* Size of the scratch array built into the library for gdn_forward_noalloc. */
 #define GDN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
@@ -161,7 +187,8 @@ int gdn_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void
  * budget fixed at start-up, plugin hosts that pass a kernel its inputs and
  * outputs but no scratch, and paths that cannot accept the implicit device
  * synchronisation of cudaMalloc / cudaFree.  This entry point takes the same
- * arguments as gdn_forward minus the workspace and uses instead one scratch
+ * arguments as gdn_forward minus the workspace and the flags (it keeps nothing
+ * for a backward) and uses instead one scratch
  * array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library, which
  * every GPU that loads the library holds until the process exits.  It allocates
  * nothing.

@@ -26,9 +26,14 @@ def rel_err(gpu, ref) -> float:
 
 
 class DeviceRun:
-    """Device copies of one draw plus every output of one forward + backward."""
+    """Device copies of one draw plus every output of one forward + backward.
 
-    def __init__(self, inp: W.Inputs, device="cuda", dense=False, run_backward=True):
+    train=True (the default) runs the pair as a training step: the forward keeps
+    the backward's chunk operands and the backward reuses them; train=False has
+    each call compute everything itself."""
+
+    def __init__(self, inp: W.Inputs, device="cuda", dense=False, run_backward=True,
+                 train=True):
         import torch
         import gated_deltanet_backward_gb300 as gdn
         self.inp = inp
@@ -57,14 +62,18 @@ class DeviceRun:
         N = wl.n_seqs
         self.o = torch.full((T, Hv * Dv), float("nan"), device=device, dtype=self.tdtype)
         self.S_T = torch.full((N, Hv, Dk, Dv), float("nan"), device=device)
+        self.train = train
         self.layer.forward(self.q, self.k, self.v, self.alpha, self.beta_raw, self.a_log,
-                           self.dt_bias, self.S0, self.o, self.S_T)
+                           self.dt_bias, self.S0, self.o, self.S_T, train=train)
+        # a training step's backward shares the forward's workspace (and status word)
+        self.fwd_status = gdn.gdn_read_device_status(self.layer.ws_bwd) if train else None
         self.grads = None
         if run_backward:
             self.run_backward()
 
-    def run_backward(self):
+    def run_backward(self, train=None):
         import torch
+        train = self.train if train is None else train
         wl = self.inp.wl
         T, Hk, Hv, Dk, Dv, N = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv, wl.n_seqs
         dev = self.o.device
@@ -79,12 +88,15 @@ class DeviceRun:
                  dS0=torch.full((N, Hv, Dk, Dv), nan, device=dev))
         self.layer.backward(self.q, self.k, self.v, self.alpha, self.beta_raw, self.a_log,
                             self.dt_bias, self.S0, self.dO, self.dS_T, g["dq"], g["dk"], g["dv"],
-                            g["dalpha"], g["dbeta_raw"], g["da_log"], g["ddt_bias"], g["dS0"])
+                            g["dalpha"], g["dbeta_raw"], g["da_log"], g["ddt_bias"], g["dS0"],
+                            train=train)
         self.grads = g
         return g
 
     def status(self, backward=False) -> int:
         import gated_deltanet_backward_gb300 as gdn
+        if self.train and not backward:
+            return self.fwd_status
         return gdn.gdn_read_device_status(self.layer.ws_bwd if backward else self.layer.ws_fwd)
 
     def host(self):

@@ -70,14 +70,14 @@ def _fwd_args(gdn, shape, **over):
     a = dict(q=A, q_ld=shape.Hk * shape.Dk * 2 + shape.Hv * shape.Dv, k=A, k_ld=None, v=A,
              v_ld=None, alpha=A, alpha_ld=shape.Hv, beta=A, beta_ld=shape.Hv, a_log=A, dt=A,
              cu=A, coff=A, S0=None, o=A, o_ld=shape.Hv * shape.Dv, S_T=None, saved=A, ws=A,
-             ws_bytes=0, stream=None)
+             ws_bytes=0, flags=0, stream=None)
     a["k_ld"] = a["q_ld"]
     a["v_ld"] = a["q_ld"]
     a.update(over)
     return [ctypes.byref(shape), a["q"], a["q_ld"], a["k"], a["k_ld"], a["v"], a["v_ld"],
             a["alpha"], a["alpha_ld"], a["beta"], a["beta_ld"], a["a_log"], a["dt"], a["cu"],
             a["coff"], a["S0"], a["o"], a["o_ld"], a["S_T"], a["saved"], a["ws"], a["ws_bytes"],
-            a["stream"]]
+            a["flags"], a["stream"]]
 
 
 def test_forward_rejects_bad_arguments_before_launching(gdn):
@@ -102,11 +102,18 @@ def test_forward_rejects_bad_arguments_before_launching(gdn):
     s4 = gdn.make_shape(4, 6, 64, 64, 1, 2, 100, "f32")
     assert lib.gdn_forward(*_fwd_args(gdn, s4, ws_bytes=ws)) == -1
     assert lib.gdn_forward(None, *_fwd_args(gdn, s, ws_bytes=ws)[1:]) == -1
+    # unknown flags, a backward-only flag, and a keeping forward whose workspace has
+    # only the forward's size
+    assert lib.gdn_forward(*_fwd_args(gdn, s, ws_bytes=ws, flags=4)) == -1
+    assert lib.gdn_forward(*_fwd_args(gdn, s, ws_bytes=ws, flags=gdn.GDN_FLAG_REUSE_FORWARD)) == -1
+    assert lib.gdn_forward(*_fwd_args(gdn, s, ws_bytes=ws,
+                                      flags=gdn.GDN_FLAG_KEEP_FOR_BACKWARD)) == -6
 
 
 def test_status_strings(gdn):
     for code, name in [(0, "GDN_OK"), (-1, "GDN_ERR_INVALID_ARG"), (-5, "GDN_ERR_TIMEOUT"),
-                       (-7, "GDN_ERR_DEVICE_BOUNDS"), (99, "GDN_UNKNOWN_STATUS")]:
+                       (-7, "GDN_ERR_DEVICE_BOUNDS"), (-8, "GDN_ERR_NOT_KEPT"),
+                       (99, "GDN_UNKNOWN_STATUS")]:
         assert gdn.gdn_status_string(code) == name
 
 

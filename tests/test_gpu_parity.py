@@ -139,3 +139,45 @@ def test_saved_states_and_final_state_against_oracle_fp32():
     ref = oracle_outputs(inp, backward=False)
     assert rel_err(gpu["saved"], ref["saved"]) < 1e-4
     assert rel_err(gpu["S_T"], ref["S_T"]) < 1e-4
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_training_step_reuse_gives_the_bits_of_a_recomputing_backward(dtype):
+    """A forward that keeps the chunk operands plus a backward that reuses them
+    produce exactly the outputs of two calls that each compute everything."""
+    wl = W.custom(dtype=dtype, Hk=2, Hv=6, Dk=128 if dtype == "bf16" else 32,
+                  Dv=128 if dtype == "bf16" else 32, seqlens=(300, 0, 77, 64), seed=21,
+                  S0_std=0.1, dST_std=0.1, dt_bias_std=0.1)
+    inp = W.generate(wl)
+    kept, fresh = DeviceRun(inp, train=True), DeviceRun(inp, train=False)
+    assert kept.status() == 0 and kept.status(backward=True) == 0
+    assert fresh.status() == 0 and fresh.status(backward=True) == 0
+    a, b = kept.host(), fresh.host()
+    for key in b:
+        assert np.all(np.isfinite(a[key])), key
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_reuse_without_a_kept_forward_is_refused_on_the_device():
+    """A reusing backward whose workspace holds no kept forward of its shape records
+    GDN_ERR_NOT_KEPT and writes nothing; a proper training step afterwards works."""
+    import gated_deltanet_backward_gb300 as gdn
+    wl = W.custom(dtype="bf16", Hk=1, Hv=2, Dk=64, Dv=64, seqlens=(130, 40), seed=5)
+    inp = W.generate(wl)
+    # (1) the forward did not keep: its operands went to the forward workspace
+    run = DeviceRun(inp, run_backward=False, train=False)
+    run.layer.ws_bwd.zero_()
+    g = run.run_backward(train=True)
+    assert run.status(backward=True) == gdn.GDN_ERR_NOT_KEPT
+    assert all(bool(t.isnan().all()) for t in g.values())
+    # (2) the workspace was kept for another shape (a different output scale)
+    run = DeviceRun(inp, run_backward=False, train=True)
+    assert run.status() == 0
+    run.layer.shape.scale = 0.5
+    g = run.run_backward(train=True)
+    assert run.status(backward=True) == gdn.GDN_ERR_NOT_KEPT
+    assert all(bool(t.isnan().all()) for t in g.values())
+    # (3) the context is intact: a training step on the same draw matches the oracle
+    run = DeviceRun(inp, train=True)
+    assert run.status() == 0 and run.status(backward=True) == 0
+    compare(run.host(), oracle_outputs(inp), TOL["bf16"])
