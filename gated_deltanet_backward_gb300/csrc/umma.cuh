@@ -137,11 +137,26 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major, 128-byte-swizzled operand: the tile
+// is stored with one 128-byte row per K index holding 64 consecutive M (or N)
+// elements, 8 rows to a 1024-byte swizzle atom.  `mn_stride` is the byte
+// distance between consecutive 64-element MN blocks (leading-dimension byte
+// offset); consecutive 8-row K groups are 1024 B apart (stride byte offset).
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
-// both operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// shape M x N; a_mn / b_mn select MN-major (transposed) storage of A / B.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = false,
+                                                  bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // One thread: D[tmem] (+)= A * B^T, single K=16 step.
@@ -190,6 +205,29 @@ __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_base, int M
                                          int N, int K, uint32_t accumulate_first) {
   mma_tile_p(d_tmem, a_base, (uint32_t)M * 128u, M, b_base, (uint32_t)N * 128u, N, K,
              accumulate_first);
+}
+
+// As mma_tile_p with either operand optionally MN-major.  An MN-major operand
+// X (M or N = 64 or 128) is a SW128 tile stored as rows = K indices (its
+// K-major view transposed): element (mn, k) at sw128_offset(k, mn, x_rows),
+// with x_rows >= K the tile's row count; its 64-element MN blocks are
+// x_rows * 128 bytes apart, and a K step of 16 advances 16 rows (2048 bytes).
+// A K-major operand keeps the meaning of mma_tile_p (pitch between 64-column
+// blocks).
+__device__ __forceinline__ void mma_tile_x(uint32_t d_tmem, uint32_t a_base, bool a_mn,
+                                           uint32_t a_pitch, int M, uint32_t b_base, bool b_mn,
+                                           uint32_t b_pitch, int N, int K,
+                                           uint32_t accumulate_first) {
+  const uint32_t idesc = idesc_bf16(M, N, a_mn, b_mn);
+  for (int kk = 0; kk < K; kk += 16) {
+    const uint64_t da =
+        a_mn ? desc_sw128_mn(a_base + (uint32_t)kk * 128u, a_pitch)
+             : desc_sw128(a_base + (uint32_t)(kk >> 6) * a_pitch + (uint32_t)(kk & 63) * 2u);
+    const uint64_t db =
+        b_mn ? desc_sw128_mn(b_base + (uint32_t)kk * 128u, b_pitch)
+             : desc_sw128(b_base + (uint32_t)(kk >> 6) * b_pitch + (uint32_t)(kk & 63) * 2u);
+    mma_bf16(d_tmem, da, db, idesc, (kk > 0) ? 1u : accumulate_first);
+  }
 }
 
 // Bytes of a K-major SW128 bf16 tile of `rows` rows and `cols` columns.

@@ -1,7 +1,8 @@
 // Test-only probe of the tensor-core building blocks in umma.cuh: one CTA loads
-// A [M x K] and B [N x K] (bf16, row-major) into K-major SW128 shared-memory
-// tiles, issues D = A B^T with tcgen05.mma, and dumps all 128 TMEM lanes x N
-// columns of the fp32 accumulator so the host can check the layout.
+// A [M x K] and B [N x K] (bf16, row-major) into SW128 shared-memory tiles
+// (K-major, or MN-major when a_mn / b_mn is set), issues D = A B^T with
+// tcgen05.mma, and dumps all 128 TMEM lanes x N columns of the fp32 accumulator
+// so the host can check the layout.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -9,24 +10,40 @@
 
 using namespace gdn::tc;
 
+// Bytes of one operand tile: K-major rows x ceil(K/64) blocks, or MN-major K rows
+// x ceil(rows/64) blocks.
+__host__ __device__ inline size_t tile_bytes(int rows, int K, bool mn) {
+  return mn ? (size_t)K * 128 * ((rows + 63) / 64) : (size_t)rows * 128 * ((K + 63) / 64);
+}
+
+// Stages X [rows x K] (row-major) as a K-major or an MN-major SW128 tile.
+__device__ void stage(uint8_t* t, const __nv_bfloat16* X, int rows, int K, bool mn) {
+  if (!mn) {
+    const int KB = (K + 63) / 64;
+    for (int i = threadIdx.x; i < rows * 64 * KB; i += blockDim.x) {
+      const int r = i / (64 * KB), k = i % (64 * KB);
+      *(__nv_bfloat16*)(t + sw128_offset(r, k, rows)) =
+          k < K ? X[r * K + k] : __float2bfloat16(0.f);
+    }
+  } else {
+    for (int i = threadIdx.x; i < rows * K; i += blockDim.x) {
+      const int r = i / K, k = i % K;
+      *(__nv_bfloat16*)(t + sw128_offset(k, r, K)) = X[r * K + k];
+    }
+  }
+}
+
 __global__ void k_umma_check(const __nv_bfloat16* A, const __nv_bfloat16* B, float* out, int M,
-                             int N, int K, int ncols, int* status) {
+                             int N, int K, int ncols, int a_mn, int b_mn, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const int KB = (K + 63) / 64;
   uint8_t* sA = sm;
-  uint8_t* sB = sA + (size_t)M * 128 * KB;
-  uint64_t* bar = (uint64_t*)(sB + (size_t)N * 128 * KB);
+  uint8_t* sB = sA + tile_bytes(M, K, a_mn);
+  uint64_t* bar = (uint64_t*)(sB + tile_bytes(N, K, b_mn));
   uint32_t* tslot = (uint32_t*)(bar + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < M * 64 * KB; i += blockDim.x) {
-    const int r = i / (64 * KB), k = i % (64 * KB);
-    *(__nv_bfloat16*)(sA + sw128_offset(r, k, M)) = k < K ? A[r * K + k] : __float2bfloat16(0.f);
-  }
-  for (int i = tid; i < N * 64 * KB; i += blockDim.x) {
-    const int r = i / (64 * KB), k = i % (64 * KB);
-    *(__nv_bfloat16*)(sB + sw128_offset(r, k, N)) = k < K ? B[r * K + k] : __float2bfloat16(0.f);
-  }
+  stage(sA, A, M, K, a_mn != 0);
+  stage(sB, B, N, K, b_mn != 0);
   fence_async_smem();
   if (tid == 0) {
     mbar_init(bar, 1);
@@ -41,7 +58,9 @@ __global__ void k_umma_check(const __nv_bfloat16* A, const __nv_bfloat16* B, flo
   fence_after_sync();
   const uint32_t tmem = *tslot;
   if (tid == 0) {
-    mma_tile(tmem, smem_u32(sA), M, smem_u32(sB), N, K, 0u);
+    const uint32_t ap = a_mn ? (uint32_t)K * 128u : (uint32_t)M * 128u;
+    const uint32_t bp = b_mn ? (uint32_t)K * 128u : (uint32_t)N * 128u;
+    mma_tile_x(tmem, smem_u32(sA), a_mn != 0, ap, M, smem_u32(sB), b_mn != 0, bp, N, K, 0u);
     mma_commit(bar);
   }
   const bool ok = mbar_wait(bar, 0, 1000000000ull);
@@ -61,15 +80,18 @@ __global__ void k_umma_check(const __nv_bfloat16* A, const __nv_bfloat16* B, flo
   if (warp == 0) tmem_dealloc(tmem, (uint32_t)ncols);
 }
 
+// MN-major operands need M (or N) a multiple of 64 and K a multiple of 16.
 extern "C" int umma_check(const void* A, const void* B, float* out, int M, int N, int K,
-                          int* status) {
+                          int a_mn, int b_mn, int* status) {
+  if ((a_mn && (M % 64 || K % 16)) || (b_mn && (N % 64 || K % 16))) return -3;
   int ncols = 32;
   while (ncols < N) ncols <<= 1;
-  const int KB = (K + 63) / 64;
-  const size_t smem = 1024 + (size_t)(M + N) * 128 * KB + 64;
+  // 16 KB of slack after the tiles: every address a descriptor can reach stays
+  // inside the allocation whatever the tile layout
+  const size_t smem = 1024 + tile_bytes(M, K, a_mn) + tile_bytes(N, K, b_mn) + 64 + 16384;
   cudaFuncSetAttribute(k_umma_check, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   k_umma_check<<<1, 128, smem>>>((const __nv_bfloat16*)A, (const __nv_bfloat16*)B, out, M, N, K,
-                                 ncols, status);
+                                 ncols, a_mn, b_mn, status);
   if (cudaGetLastError() != cudaSuccess) return -1;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -2;
 }

@@ -4,7 +4,8 @@ A probe kernel (tests/cuda/umma_check.cu, test-only) issues one tcgen05.mma of
 kind::f16 (bf16 x bf16 -> fp32) from K-major 128-byte-swizzled shared-memory
 tiles and dumps every TMEM lane.  Checks: the instruction and shared-memory
 descriptors give D = A B^T; for M = 128 row i sits in lane i; the lane layout of
-M = 64 is recorded (rows 16w..16w+15 in lanes 32w..32w+15)."""
+M = 64 is recorded (rows 16w..16w+15 in lanes 32w..32w+15); MN-major (transposed)
+storage of A and / or B gives the same product."""
 import ctypes
 import os
 import subprocess
@@ -29,12 +30,12 @@ def probe():
                            "-I", os.path.join(ROOT, "gated_deltanet_backward_gb300", "csrc"),
                            src, "-o", lib])
     L = ctypes.CDLL(lib)
-    L.umma_check.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    L.umma_check.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p]
     L.umma_check.restype = ctypes.c_int
     return torch, L
 
 
-def _run(probe, M, N, K, seed=0):
+def _run(probe, M, N, K, seed=0, a_mn=False, b_mn=False):
     torch, L = probe
     g = torch.Generator().manual_seed(seed)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
@@ -42,7 +43,8 @@ def _run(probe, M, N, K, seed=0):
     dA, dB = A.cuda(), B.cuda()
     out = torch.full((128, N), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = L.umma_check(dA.data_ptr(), dB.data_ptr(), out.data_ptr(), M, N, K, st.data_ptr())
+    rc = L.umma_check(dA.data_ptr(), dB.data_ptr(), out.data_ptr(), M, N, K, int(a_mn),
+                      int(b_mn), st.data_ptr())
     assert rc == 0 and int(st.item()) == 0
     ref = (A.double() @ B.double().T).numpy()
     return out.cpu().double().numpy(), ref
@@ -59,5 +61,20 @@ def test_m128_is_row_per_lane(probe, N, K):
 def test_m64_lane_layout(probe, N, K):
     got, ref = _run(probe, 64, N, K)
     lanes = np.array([32 * (i // 16) + (i % 16) for i in range(64)])
+    err = np.abs(got[lanes] - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("M,N,K,a_mn,b_mn", [
+    (128, 64, 64, True, False),    # dO^T P^T: A read from the natural dO tile
+    (128, 128, 128, False, True),  # [dO; dDelta] S^T: B read from the S^T tile
+    (128, 128, 64, True, True),
+    (64, 128, 128, True, False),
+    (64, 64, 64, False, True),
+])
+def test_mn_major_operands(probe, M, N, K, a_mn, b_mn):
+    got, ref = _run(probe, M, N, K, seed=3, a_mn=a_mn, b_mn=b_mn)
+    lanes = (np.arange(128) if M == 128 else
+             np.array([32 * (i // 16) + (i % 16) for i in range(64)]))
     err = np.abs(got[lanes] - ref).max() / np.abs(ref).max()
     assert err < 1e-5, err
