@@ -63,7 +63,8 @@ def alu_fp32_tflops(sm_mhz):
 
 # ----------------------------------------------------------------------------
 # Algorithmic work model.  Path level: what the method must move / compute per
-# token (bf16 q/k/v/o/dO and their grads, fp32 gates, fp32 chunk-start states).
+# token (bf16 q/k/v/o/dO and their grads, fp32 gates, chunk-start states in the
+# input type, written once by the forward and read once by the backward).
 # Kernel level: each kernel's compulsory reads and writes of its own inputs and
 # outputs (workspace intermediates of this decomposition included), and the
 # multiply-add work of its contractions (2 FLOP per MAC; triangular products
@@ -77,7 +78,7 @@ def path_model(wl: W.Workload):
     qk = 2 * Hk * Dk * es
     v = Hv * Dv * es
     gates = 2 * Hv * 4
-    states = NC * Hv * Dk * Dv * 4
+    states = NC * Hv * Dk * Dv * es          # chunk-start states, kept in the input type
     fwd = T * (qk + v + gates + v) + states
     bwd = T * (qk + v + gates + v) + states + T * (qk + v + gates)
     st = N * Hv * Dk * Dv * 4
@@ -124,7 +125,8 @@ def kernel_models(wl: W.Workload):
     sKC = (Dk + 63) // 64 * C * 128                  # [C][Dk] tile
     sVC = (Dv + 63) // 64 * C * 128                  # [C][Dv] tile
     sKt, sVt, sCC = Dk * 128, Dv * 128, C * C * 2    # [Dk][C], [Dv][C], [C][C] tiles
-    sDD = (Dv + 63) // 64 * Dk * 128                 # [Dk][Dv] tile
+    MV = max(Dv, 64)
+    sST = (Dk + 63) // 64 * MV * 128                 # S^T / dS^T state tile [MV][Dk]
     tok_in = T * (2 * Hk * Dk * es + Hv * Dv * es + 2 * Hv * 4)   # q, k, v, alpha, beta
     tc_prep_b = (tok_in + NC * Hk * (2 * sKC + sKt) +
                  NC * Hv * (2 * C * 4 + sVt + sKC + sCC))           # Q, K, K^T; G, b, U^T, W, P
@@ -136,13 +138,13 @@ def kernel_models(wl: W.Workload):
     fst_st = st * ((wl.S0_std > 0) + 1)                             # S0 read, S_T written
     bst_st = st * ((wl.dST_std > 0) + 1)                            # dS_T read, dS0 written
     fst_tc_b = (NC * Hk * (sKC + sKt) + NC * Hv * (sKC + sCC + sVt + C * 4) +
-                T * Hv * Dv * es + NC * Hv * Dk * Dv * 4 + fst_st)  # ... o, saved states
+                T * Hv * Dv * es + NC * Hv * sST + fst_st)          # ... o, saved S^T tiles
     fst_tc_f = NC * Hv * (6 * C * Dk * Dv + 2 * C * C * Dv)
     bst_tc_b = (NC * Hk * (sKC + sKt) + NC * Hv * (sCC + sKt + C * 4) + T * Hv * Dv * es +
-                NC * Hv * (sDD + sVC + sVt) + bst_st)               # ... dS, dDelta, dDelta^T
+                NC * Hv * (sST + sVC + MV * 128) + bst_st)          # ... dS^T, -dDelta(^T)
     bst_tc_f = NC * Hv * (2 * C * C * Dv + 6 * C * Dk * Dv)
     bgr_tc_b = (NC * Hk * (2 * sKt + C * C * 4 + 2 * C * 4) + T * Hk * 2 * Dk * es +
-                NC * Hv * (Dk * Dv * 4 + 2 * C * 4 + sKC + sVt + sVC + sCC + sDD + sVt +
+                NC * Hv * (sST + 2 * C * 4 + sKC + sVt + sVC + sCC + sST + MV * 128 +
                            3 * sCC + 8) +
                 T * Hv * (2 * Dv * es + 4) + T * Hv * (Dv * es + 8))
     bgr_tc_f = NC * Hv * (2 * C * Dk * Dv + 2 * 128 * Dk * Dv + 2 * C * Dk * Dv +

@@ -310,6 +310,8 @@ int gdn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t* chunk_offs
 
 size_t gdn_saved_state_bytes(const gdn_shape* s) {
   if (check_shape(s) != GDN_OK) return 0;
+  if (s->dtype == GDN_DTYPE_BF16)
+    return (size_t)s->total_chunks * s->Hv * gdn::state_tile_bytes(s->Dk, s->Dv);
   return (size_t)s->total_chunks * s->Hv * s->Dk * s->Dv * sizeof(float);
 }
 
@@ -322,7 +324,7 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
                 const void* v, int64_t v_ld, const float* alpha, int64_t alpha_ld,
                 const float* beta_raw, int64_t beta_ld, const float* a_log,
                 const float* dt_bias, const int32_t* cu_seqlens, const int32_t* chunk_offsets,
-                const float* S0, void* o, int64_t o_ld, float* S_T, float* saved_states,
+                const float* S0, void* o, int64_t o_ld, float* S_T, void* saved_states,
                 void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
   GDN_TRY(check_shape(s));
   if (flags & ~(uint32_t)GDN_FLAG_KEEP_FOR_BACKWARD) return GDN_ERR_INVALID_ARG;
@@ -345,7 +347,7 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
   p.o = o;
   p.o_ld = o_ld;
   p.S_T = S_T;
-  p.saved = saved_states;
+  p.saved = (float*)saved_states;
   (void)cudaGetLastError();  // report only errors of this call's own launches
   g_last_error[0] = 0;
   cudaError_t e = cudaMemsetAsync(workspace, 0, 256, st);
@@ -379,7 +381,7 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
                  const float* beta_raw, int64_t beta_ld, const float* a_log,
                  const float* dt_bias, const int32_t* cu_seqlens, const int32_t* chunk_offsets,
                  const float* S0, const void* dO, int64_t dO_ld, const float* dS_T,
-                 const float* saved_states, void* dq, int64_t dq_ld, void* dk, int64_t dk_ld,
+                 const void* saved_states, void* dq, int64_t dq_ld, void* dk, int64_t dk_ld,
                  void* dv, int64_t dv_ld, float* dalpha, int64_t dalpha_ld, float* dbeta_raw,
                  int64_t dbeta_ld, float* da_log, float* ddt_bias, float* dS0, void* workspace,
                  size_t workspace_bytes, uint32_t flags, void* stream) {
@@ -405,7 +407,7 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
   Params p;
   fill_common(p, s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
               dt_bias, cu_seqlens, chunk_offsets, S0, workspace, true);
-  p.saved_in = saved_states;
+  p.saved_in = (const float*)saved_states;
   p.dO = dO;
   p.dO_ld = dO_ld;
   p.dS_T = dS_T;

@@ -68,9 +68,9 @@ struct WsLayout {
   size_t Utb;     // [NC][Hv] [Dv][C]   U^T
   size_t KKf;     // [NC][Hk][C][C] fp32  K K^T (backward)
   size_t Tb;      // [NC][Hv] 3 x [C][C]: T, T^T, diag(b e^G) T^T (backward)
-  size_t dSb;     // [NC][Hv] [Dk][Dv]  state adjoint at each chunk end (backward)
-  size_t dDb;     // [NC][Hv] [C][Dv]   d Delta (backward)
-  size_t dDtb;    // [NC][Hv] [Dv][C]   d Delta^T (backward)
+  size_t dSb;     // [NC][Hv] [MV][Dk] dS^T: state adjoint at each chunk end (backward)
+  size_t dDb;     // [NC][Hv] [C][MV]  -d Delta (backward)
+  size_t dDtb;    // [NC][Hv] [MV][C]  -d Delta^T (backward); MV = max(Dv, 64)
   size_t total;
 };
 
@@ -78,6 +78,8 @@ struct WsLayout {
 inline size_t tile_CxD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
 inline size_t tile_DxC(int D) { return (size_t)D * 128; }
 inline size_t tile_DxD(int R, int D) { return (size_t)((D + 63) / 64) * R * 128; }
+// Bytes of one bf16 state tile: S^T (or dS^T) with max(Dv, 64) rows and Dk columns.
+inline size_t state_tile_bytes(int Dk, int Dv) { return tile_DxD(Dv < 64 ? 64 : Dv, Dk); }
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -125,9 +127,9 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
       L.Ptsw = take(NC * Hv * tile_CxD(64));
       L.KKf = take(NC * Hk * C * C * 4);
       L.Tb = take(NC * Hv * 3 * tile_CxD(64));
-      L.dSb = take(NC * Hv * tile_DxD(s.Dk, s.Dv));
+      L.dSb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
       L.dDb = take(NC * Hv * tile_CxD(s.Dv));
-      L.dDtb = take(NC * Hv * tile_DxC(s.Dv));
+      L.dDtb = take(NC * Hv * tile_DxC(s.Dv < 64 ? 64 : s.Dv));
     }
   }
   L.total = off;

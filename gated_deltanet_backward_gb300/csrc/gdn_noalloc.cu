@@ -53,7 +53,7 @@ extern "C" int gdn_forward_noalloc(const gdn_shape* s, const void* q, int64_t q_
                                    int64_t beta_ld, const float* a_log, const float* dt_bias,
                                    const int32_t* cu_seqlens, const int32_t* chunk_offsets,
                                    const float* S0, void* o, int64_t o_ld, float* S_T,
-                                   float* saved_states, void* stream) {
+                                   void* saved_states, void* stream) {
   const size_t need = gdn_workspace_bytes(s, 0);
   if (need == 0)  // invalid shape: let the regular entry point name the problem
     return gdn_forward(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,

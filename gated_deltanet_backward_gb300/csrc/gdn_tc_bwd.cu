@@ -43,16 +43,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   const uint32_t bK = (uint32_t)tileCD(DK), bKt = (uint32_t)tileDC(DK), bP = 8192, bG = C * 4;
   const int nbv = (Dv + 63) / 64;
   const uint32_t bO = (uint32_t)nbv * 8192;                  // natural dO tile [C][Dv]
-  uint8_t* tdSt = sm;                                        // [MV][DK]
-  uint8_t* tdOt = tdSt + tc::sw128_bytes(MV, DK);            // [MV][C] dO^T
-  uint8_t* tmDt = tdOt + MV * 128;                           // [MV][C] -dDelta^T
-  uint8_t* buf0 = tmDt + MV * 128;
+  const uint32_t bSt = tc::sw128_bytes(MV, DK);              // dS^T tile
+  const uint32_t bDt = (uint32_t)MV * 128, bD = tc::sw128_bytes(C, MV);
+  uint8_t* tdSt = sm;                                        // [MV][DK] dS^T
+  uint8_t* tmDt = tdSt + bSt;                                // [MV][C] -dDelta^T
+  uint8_t* tmD = tmDt + bDt;                                 // [C][MV] -dDelta
+  uint8_t* buf0 = tmD + bD;
   const uint32_t bufsz = bO + bK + bP + 2 * bKt + 1024;
   float* ev = (float*)(buf0 + 2 * bufsz);
   float* cv = ev + C;
   uint64_t* bars = (uint64_t*)(cv + C);
   uint32_t* tslot = (uint32_t*)(bars + 3);
-  // per stage buffer: natural dO tile (TMA; reused for (scale e^G dO)^T), K, P^T, Q^T, W^T, G
+  // per stage buffer: natural dO tile (TMA; the MN-major A operand of dO^T), K, P^T,
+  // Q^T (scaled in place to (scale e^G Q)^T), W^T, G
   auto sdO = [&](int b) { return buf0 + b * bufsz; };
   auto tK = [&](int b) { return buf0 + b * bufsz + bO; };
   auto tPt = [&](int b) { return buf0 + b * bufsz + bO + bK; };
@@ -60,7 +63,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   auto tWt = [&](int b) { return buf0 + b * bufsz + bO + bK + bP + bKt; };
   auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + bO + bK + bP + 2 * bKt); };
 
-  for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) + 2 * MV * 128) / 16; i += kThreads)
+  for (int i = tid; i < (int)(bSt + bDt + bD) / 16; i += kThreads)
     ((uint4*)tdSt)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     tc::mbar_init(&bars[0], 1);
@@ -93,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
 #pragma unroll
   for (int i = 0; i < NKC; ++i)
     if (half * 16 + 32 * i < DK && vok) tile_put16(tdSt, MV, vrow, half * 16 + 32 * i, dS[i]);
+  tc::fence_async_smem();
 
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
@@ -115,17 +119,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
     const int64_t t0 = s0 + (int64_t)(c - c0) * C;
     const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
     const size_t ch = (size_t)c * p.Hv + h;
-    // state adjoint at the end of this chunk, as a bf16 [DK][Dv] operand tile for the
-    // gradient kernel (a warp's lanes write consecutive columns of one tile row)
-    uint8_t* dst_dS = p.dSb + ch * (size_t)tc::sw128_bytes(DK, Dv);
-    if (vok)
-#pragma unroll
-      for (int ii = 0; ii < NKC; ++ii)
-        if (half * 16 + 32 * ii < DK)
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            *(__nv_bfloat16*)(dst_dS + tc::sw128_offset(half * 16 + 32 * ii + j, vrow, DK)) =
-                __float2bfloat16_rn(dS[ii][j]);
     const bool lok = tc::mbar_wait(&bars[1 + b], lph[b]);
     lph[b] ^= 1u;
     if (__syncthreads_or(lok ? 0 : 1)) {
@@ -133,9 +126,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
       ok = false;
       break;
     }
-    if (tid == 0 && c - 1 >= c0) {
-      tc::fence_async_smem();
-      issue_load(c - 1, b ^ 1);
+    if (tid == 0) {
+      // state adjoint at the end of this chunk: the dS^T tile, by one bulk store
+      tc::bulk_s2g(p.dSb + ch * bSt, tdSt, bSt);
+      tc::bulk_commit();
+      if (c - 1 >= c0) {
+        tc::fence_async_smem();
+        issue_load(c - 1, b ^ 1);
+      }
     }
     const float* G = sG(b);
     if (tid < C) {
@@ -143,41 +141,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
       cv[tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
     }
     __syncthreads();
-    // dO^T (rows v, columns r) from the natural dO tile; rows past the chunk are zero
-    for (int idx = tid; idx < Dv * (C / 8); idx += kThreads) {
-      const int vv = idx % Dv, r8 = (idx / Dv) * 8;
-      __align__(16) __nv_bfloat16 e[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        e[q] = r8 + q < len ? *(const __nv_bfloat16*)(sdO(b) + tc::sw128_offset(r8 + q, vv, C))
-                            : __float2bfloat16(0.f);
-      *(uint4*)(tdOt + tc::sw128_offset(vv, r8, MV)) = *(const uint4*)e;
-    }
-    __syncthreads();
-    // (scale e^G dO)^T over the natural tile's space (no longer read)
-    uint8_t* tdOet = sdO(b);
-    for (int idx = tid; idx < Dv * (C / 8); idx += kThreads) {
-      const int vv = idx % Dv, r8 = (idx / Dv) * 8;
-      const uint4 raw = *(const uint4*)(tdOt + tc::sw128_offset(vv, r8, MV));
+    // rows of the dO tile past the chunk (another sequence's tokens) read as zero
+    if (len < C)
+      for (int idx = tid; idx < nbv * (C - len) * 8; idx += kThreads) {
+        const int b2 = idx / ((C - len) * 8), rem = idx % ((C - len) * 8);
+        ((uint4*)(sdO(b) + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
+      }
+    // (scale e^G Q)^T in place: column r of the Q^T tile times scale e^{G_r}
+    for (int idx = tid; idx < DK * (C / 8); idx += kThreads) {
+      const int kk = idx % DK, r8 = (idx / DK) * 8;
+      uint4* at = (uint4*)(tQt(b) + tc::sw128_offset(kk, r8, DK));
+      const uint4 raw = *at;
       const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
       __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         pk[q] = __floats2bfloat162_rn(__bfloat162float(e[2 * q]) * p.scale * ev[r8 + 2 * q],
                                       __bfloat162float(e[2 * q + 1]) * p.scale * ev[r8 + 2 * q + 1]);
-      *(uint4*)(tdOet + tc::sw128_offset(vv, r8, MV)) = *(const uint4*)pk;
+      *at = *(const uint4*)pk;
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::mma_tile(tA1, tc::smem_u32(tdOt), MV, tc::smem_u32(tPt(b)), C, C, 0u);
+      tc::bulk_wait_read<1>();   // last chunk's dDelta stores have read their tiles
+      // dO^T as an MN-major operand straight from the natural tile (boxes 8 KB apart)
+      tc::mma_tile_x(tA1, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tPt(b)), false,
+                     (uint32_t)C * 128u, C, C, 0u);
       tc::mma_tile(tA2, tc::smem_u32(tdSt), MV, tc::smem_u32(tK(b)), C, DK, 0u);
-      tc::mma_tile(tA3, tc::smem_u32(tdOet), MV, tc::smem_u32(tQt(b)), DK, C, 0u);
+      tc::mma_tile_x(tA3, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tQt(b)), false,
+                     (uint32_t)DK * 128u, DK, C, 0u);
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // dDelta^T = scale (P^T dO)^T + c (K dS)^T
-    // dDelta as bf16 tiles for the gradient kernel: natural [C][Dv] and transposed [Dv][C]
-    uint8_t* dst_dD = p.dDb + ch * (size_t)tc::sw128_bytes(C, Dv);
-    uint8_t* dst_dDt = p.dDtb + ch * (size_t)Dv * 128;
+    // -dDelta^T (the A operand below) and -dDelta in shared memory; both go to the
+    // gradient kernel by bulk stores
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int col0 = half * 16 + 32 * q;
@@ -186,21 +182,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
       tc::tmem_ld16(tA2 + lane_quarter() + col0, a2);
       tc::tmem_ld_wait();
       if (vok) {
-        float d[16], md[16];
+        float md[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int s = col0 + j;
-          d[j] = s < len ? p.scale * a1[j] + cv[s] * a2[j] : 0.f;
-          md[j] = -d[j];
-          *(__nv_bfloat16*)(dst_dD + tc::sw128_offset(s, vrow, C)) = __float2bfloat16_rn(d[j]);
+          md[j] = s < len ? -(p.scale * a1[j] + cv[s] * a2[j]) : 0.f;
+          tile_put(tmD, C, s, vrow, md[j]);
         }
         tile_put16(tmDt, MV, vrow, col0, md);
-        tile_put16(dst_dDt, Dv, vrow, col0, d);
       }
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
+      tc::bulk_wait_read<0>();   // the dS^T store has read its tile: the update may rewrite it
       tc::mma_tile(tA3, tc::smem_u32(tmDt), MV, tc::smem_u32(tWt(b)), DK, C, 1u);
+      tc::bulk_s2g(p.dDtb + ch * bDt, tmDt, bDt);
+      tc::bulk_s2g(p.dDb + ch * bD, tmD, bD);
+      tc::bulk_commit();
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     const float eC = expf(G[len - 1]);
@@ -227,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           p.dS0[((size_t)n * p.Hv + h) * SZ + (size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = dS[ii][j];
+  if (tid == 0) tc::bulk_wait<0>();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -236,12 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
 // ---------------------------------------------------------------------------
 // Shared-memory plan of k_bwd_grads_tc (bytes for Dk = Dv = 128; phases A-E of one
 // value head reuse the regions):
-//   R1 64K  A: S^T [Dv][Dk], S [Dk][Dv] | B: Delta, c*Delta, dW [C][D], dW^T [Dk][C]
+//   R1 64K  A: S^T [Dv][Dk] (also read MN-major as S) | B: Delta, c*Delta, dW [C][D],
+//           dW^T [Dk][C]
 //           C-E: dPE, dPE^T, dT^T, Hs [C][C] (over Delta / c*Delta)
-//   R2 32K  A-B: [dO; dDelta] [128][Dv]   | B-E: fp32 [C][C] scratch
-//   R3 48K  A: W [C][Dk], scale e^G dO [C][Dv], U^T [Dv][C] | B: dS [Dk][Dv], P [C][C]
-//           C-E: dDelta^T [Dv][C], T^T, T, b e^G T^T, Y [C][C]
-//   R4 32K  B-C: V [C][Dv], e^G K [C][Dk]
+//   R2 32K  A-B: [dO; -dDelta] [128][Dv]  | B-E: fp32 [C][C] scratch
+//   R3 48K  A: W [C][Dk], scale e^G dO [C][Dv], U^T [Dv][C] | B: dS^T [Dv][Dk], P [C][C]
+//           C-E: -dDelta^T [Dv][C], T^T, T, b e^G T^T, Y [C][C]
+//   R4 32K  B-C: V [C][Dv], -e^G K [C][Dk]
 //   R5 32K  K^T, Q^T [Dk][C] of the key head (whole CTA)
 // TMEM (512 columns): dQ_hat @0, dK_hat @128 (M = 64 accumulators), scratch @256.
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
@@ -260,15 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   const int Dk = p.Dk, Dv = p.Dv;
   const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
   const uint32_t sCK = tc::sw128_bytes(C, Dk), sCV = tc::sw128_bytes(C, Dv);
-  const uint32_t sKC = (uint32_t)Dk * 128, sVC = (uint32_t)Dv * 128, sCC = 8192;
+  const uint32_t sKC = (uint32_t)Dk * 128, sCC = 8192;
+  // tiles handed over by the state kernels: S^T and dS^T [MV][Dk], -dDelta^T [MV][C],
+  // -dDelta [C][MV] (MV = Dv rounded up to 64); MMAs whose N is Dk read S / dS
+  // MN-major with N rounded up to 64 (the tiles' padding columns are zero)
+  const int MV = Dv < 64 ? 64 : Dv, NK = Dk < 64 ? 64 : Dk;
+  const uint32_t bSt = tc::sw128_bytes(MV, Dk), sVC = (uint32_t)MV * 128;
   uint8_t* R1 = sm;
   uint8_t* R2 = R1 + 65536;
   uint8_t* R3 = R2 + 32768;
   uint8_t* R4 = R3 + 49152;
   uint8_t* R5 = R4 + 32768;
   // R1
-  uint8_t* tSt = R1;                               // [Dv][Dk]
-  uint8_t* tS = R1 + tc::sw128_bytes(Dv, Dk);      // [Dk][Dv]
+  uint8_t* tSt = R1;                               // [MV][Dk] S^T (K-major), S (MN-major)
   uint8_t* tDl = R1;                               // [C][Dv]
   uint8_t* tDlc = R1 + 16384;                      // [C][Dv]
   uint8_t* tdW = R1 + 32768;                       // [C][Dk]
@@ -278,23 +282,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   uint8_t* tdTt = R1 + 16384;
   uint8_t* tHs = R1 + 24576;
   // R2
-  uint8_t* tA2 = R2;                               // [128][Dv]: rows 0-63 dO, 64-127 dDelta
+  uint8_t* tA2 = R2;                               // [128][Dv]: rows 0-63 dO, 64-127 -dDelta
   float* X = (float*)R2;                           // [C][C + 1] fp32 scratch (padded rows)
   constexpr int XL = C + 1;
   // R3
   uint8_t* tW = R3;                                // [C][Dk]
   uint8_t* tdOe = R3 + 16384;                      // [C][Dv]
   uint8_t* sU = R3 + 32768;                        // [Dv][C] SW128 tile of U^T
-  uint8_t* tdS = R3;                               // [Dk][Dv]
+  uint8_t* tdS = R3;                               // [MV][Dk] dS^T (read MN-major as dS)
   uint8_t* tP = R3 + 32768;                        // [C][C]
-  uint8_t* tdDt = R3;                              // [Dv][C]
+  uint8_t* tdDt = R3;                              // [MV][C] -dDelta^T
   uint8_t* tTt = R3 + 16384;
   uint8_t* tT = R3 + 24576;
   uint8_t* tTbe = R3 + 32768;
   uint8_t* tY = R3 + 40960;
   // R4
   uint8_t* tV = R4;                                // [C][Dv]
-  uint8_t* tKe = R4 + 16384;                       // [C][Dk]
+  uint8_t* tKe = R4 + 16384;                       // [C][Dk] -e^G K
   float* sKK = (float*)R4;                         // [C][C] fp32 K K^T (phase D)
   // R5
   uint8_t* tKt = R5;                               // [Dk][C]
@@ -329,7 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   const size_t ckk = (size_t)c * p.Hk + kh;
   const float* KK = p.KKf + ckk * C * C;
   const int row64 = acc_row(64);
-  const size_t SZ = (size_t)Dk * Dv;
   bool ok = true;
 
   // key-head tiles for the whole CTA
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     const int h = kh * p.r + hh;
     const size_t ch = (size_t)c * p.Hv + h;
     const uint32_t acc_first = hh > 0 ? 1u : 0u;
-    const float* S = p.saved_in + ch * SZ;
+    const uint8_t* Sg = (const uint8_t*)p.saved_in + ch * bSt;   // S^T tile
     if (tid < C) {
       const float g = p.G[ch * C + tid];
       gv[tid] = g;
@@ -363,7 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     // (TMA), overlapped with the staging below
     if (tid == 0) {
       const int nbv = (Dv + 63) / 64;
-      tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u);
+      tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u + bSt);
+      tc::bulk_g2s(tSt, Sg, bSt, &bars[1]);
       tc::bulk_g2s(tW, p.Wsw + ch * sCK, sCK, &bars[1]);
       tc::bulk_g2s(sU, p.Utb + ch * Dv * C, (uint32_t)Dv * C * 2, &bars[1]);
       for (int b = 0; b < nbv; ++b) {
@@ -378,8 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
       cv[tid] = tid < len ? expf(gv[len - 1] - gv[tid]) : 0.f;
     }
     __syncthreads();
-    // ---- phase A: S, S^T, [dO; dDelta], scale e^G dO
-    stage_f32(S, Dk, Dv, Dv, Dk, tS, tSt, Dv, One(), One());
+    // ---- phase A: S^T, [dO; -dDelta], scale e^G dO
     {
       const bool lok = tc::mbar_wait(&bars[1], lphase);
       lphase ^= 1u;
@@ -403,12 +406,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::mma_tile(tmp, tc::smem_u32(tW), 64, tc::smem_u32(tSt), Dv, Dk, 0u);           // W S
-      tc::mma_tile(tmp + 128, tc::smem_u32(tA2), 128, tc::smem_u32(tS), Dk, Dv, 0u);   // [dO;dD] S^T
-      tc::mma_tile(tdQ, tc::smem_u32(tdOe), 64, tc::smem_u32(tS), Dk, Dv, acc_first);  // dQ += s e^G dO S^T
+      tc::mma_tile_p(tmp, tc::smem_u32(tW), 64u * 128u, 64, tc::smem_u32(tSt), sVC, Dv, Dk,
+                     0u);                                                                // W S
+      tc::mma_tile_x(tmp + 128, tc::smem_u32(tA2), false, 128u * 128u, 128, tc::smem_u32(tSt),
+                     true, sVC, NK, Dv, 0u);                                             // [dO;-dD] S^T
+      tc::mma_tile_x(tdQ, tc::smem_u32(tdOe), false, 64u * 128u, 64, tc::smem_u32(tSt), true,
+                     sVC, NK, Dv, acc_first);                                            // dQ += s e^G dO S^T
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
-    // epilogue A: Delta = U - W S; dG += scale e^G (Q . dO S^T); dW = -dDelta S^T
+    // epilogue A: Delta = U - W S; dG += scale e^G (Q . dO S^T); dW = -dDelta S^T (the
+    // lower half of the stacked product)
     part[tid & 127] = 0.f;
     __syncthreads();
     for (int q = half; q * 16 < Dv; q += 2) {
@@ -438,10 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
           for (int j = 0; j < 16; ++j) rs = fmaf(tile_get(tQt, Dk, q * 16 + j, row), x[j], rs);
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            x[j] = -x[j];
-            tile_put(tdWt, Dk, q * 16 + j, row - C, x[j]);
-          }
+          for (int j = 0; j < 16; ++j) tile_put(tdWt, Dk, q * 16 + j, row - C, x[j]);
           tile_put16(tdW, C, row - C, q * 16, x);
         }
       }
@@ -451,17 +455,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     if (tid < C) dG[tid] += p.scale * ev[tid] * (part[tid] + part[C + tid]);
     // ---- phase B: dS tile, P tile (bulk), e^G K from K^T, <S, dS>
     if (tid == 0) {
-      tc::mbar_arrive_expect_tx(&bars[1], sCC + tc::sw128_bytes(Dk, Dv));
+      tc::mbar_arrive_expect_tx(&bars[1], sCC + bSt);
       tc::bulk_g2s(tP, p.Psw + ch * sCC, sCC, &bars[1]);
-      tc::bulk_g2s(tdS, p.dSb + ch * tc::sw128_bytes(Dk, Dv), tc::sw128_bytes(Dk, Dv), &bars[1]);
+      tc::bulk_g2s(tdS, p.dSb + ch * bSt, bSt, &bars[1]);
+    }
+    // S^T again, from global memory (L2), for <S, dS>: the shared copy is gone
+    uint4 sraw[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t i = tid + u * kThreads;
+      sraw[u] = i < bSt / 16 ? ((const uint4*)Sg)[i] : make_uint4(0, 0, 0, 0);
     }
     for (int idx = tid; idx < C * (Dk / 8); idx += kThreads) {
       const int s = idx % C, k8 = (idx / C) * 8;
       __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        pk[u] = __floats2bfloat162_rn(tile_get(tKt, Dk, k8 + 2 * u, s) * ev[s],
-                                      tile_get(tKt, Dk, k8 + 2 * u + 1, s) * ev[s]);
+        pk[u] = __floats2bfloat162_rn(-tile_get(tKt, Dk, k8 + 2 * u, s) * ev[s],
+                                      -tile_get(tKt, Dk, k8 + 2 * u + 1, s) * ev[s]);
       *(uint4*)(tKe + tc::sw128_offset(s, k8, C)) = *(const uint4*)pk;
     }
     {
@@ -474,35 +485,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
       }
     }
     {
-      // <S, dS> with S (fp32, L2-resident after phase A) and the dS tile
+      // <S, dS>: the S^T and dS^T tiles share one layout (zero padding included), so
+      // the dot product runs over them flat
       float sds = 0.f;
-      for (int idx = tid; idx < Dk * (Dv / 8); idx += kThreads) {
-        const int kk = idx % Dk, v8 = (idx / Dk) * 8;
-        const float4 a = *(const float4*)(S + (size_t)kk * Dv + v8);
-        const float4 b4 = *(const float4*)(S + (size_t)kk * Dv + v8 + 4);
-        const uint4 raw = *(const uint4*)(tdS + tc::sw128_offset(kk, v8, Dk));
-        const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
-        sds = fmaf(a.x, __bfloat162float(e[0]), sds);
-        sds = fmaf(a.y, __bfloat162float(e[1]), sds);
-        sds = fmaf(a.z, __bfloat162float(e[2]), sds);
-        sds = fmaf(a.w, __bfloat162float(e[3]), sds);
-        sds = fmaf(b4.x, __bfloat162float(e[4]), sds);
-        sds = fmaf(b4.y, __bfloat162float(e[5]), sds);
-        sds = fmaf(b4.z, __bfloat162float(e[6]), sds);
-        sds = fmaf(b4.w, __bfloat162float(e[7]), sds);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t i = tid + u * kThreads;
+        if (i < bSt / 16) {
+          const uint4 raw = ((const uint4*)tdS)[i];
+          const __nv_bfloat162* a = (const __nv_bfloat162*)&sraw[u];
+          const __nv_bfloat162* d = (const __nv_bfloat162*)&raw;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 fa = __bfloat1622float2(a[q]), fd = __bfloat1622float2(d[q]);
+            sds = fmaf(fa.x, fd.x, fmaf(fa.y, fd.y, sds));
+          }
+        }
       }
       sds = warp_sum(sds);
       if ((tid & 31) == 0) red[warp] = sds;
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::mma_tile(tmp, tc::smem_u32(tDlc), 64, tc::smem_u32(tdS), Dk, Dv, 0u);        // c Delta dS^T
-      tc::mma_tile(tdK, tc::smem_u32(tDlc), 64, tc::smem_u32(tdS), Dk, Dv, acc_first); // dK +=
+      tc::mma_tile_x(tmp, tc::smem_u32(tDlc), false, 64u * 128u, 64, tc::smem_u32(tdS), true,
+                     sVC, NK, Dv, 0u);                                                   // c Delta dS^T
+      tc::mma_tile_x(tdK, tc::smem_u32(tDlc), false, 64u * 128u, 64, tc::smem_u32(tdS), true,
+                     sVC, NK, Dv, acc_first);                                            // dK +=
       tc::mma_tile_p(tmp + 128, tc::smem_u32(tA2), 128u * 128u, 64, tc::smem_u32(tDl),
                      (uint32_t)C * 128u, C, Dv, 0u);                                     // dO Delta^T
       tc::mma_tile_p(tmp + 192, tc::smem_u32(tA2) + 64u * 128u, 128u * 128u, 64,
-                     tc::smem_u32(tV), (uint32_t)C * 128u, C, Dv, 0u);                  // dDelta V^T
-      tc::mma_tile(tmp + 192, tc::smem_u32(tdW), 64, tc::smem_u32(tKe), C, Dk, 1u);     // + dW (e^G K)^T
+                     tc::smem_u32(tV), (uint32_t)C * 128u, C, Dv, 0u);                  // -dDelta V^T
+      tc::mma_tile(tmp + 192, tc::smem_u32(tdW), 64, tc::smem_u32(tKe), C, Dk, 1u);     // - dW (e^G K)^T
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // epilogue B
@@ -535,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
           X[r * XL + s] = dP * pv[j];
           pe[j] = dP * E;
           tile_put(tdPEt, C, s, r, pe[j]);
-          tile_put(tdTt, C, s, r, bv[s] * y[j]);   // dT[r][s] = b_s (...)
+          tile_put(tdTt, C, s, r, -bv[s] * y[j]);  // dT[r][s] = b_s (dDelta V^T + dW (e^G K)^T)
         }
         tile_put16(tdPE, C, r, q * 16, pe);
       }
@@ -555,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
       for (int s = 0; s < C; ++s) sc += part[s] + part[C + s];
       dG[len - 1] += expf(gv[len - 1]) * tot + sc;
     }
-    // ---- phase C: dDelta^T, T^T, T, b e^G T^T
+    // ---- phase C: -dDelta^T, T^T, T, b e^G T^T
     if (tid == 0) {
       const uint8_t* tb = p.Tb + ch * 3 * sCC;
       tc::mbar_arrive_expect_tx(&bars[1], sVC + 3 * sCC);
@@ -577,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     ok = mma_run([&] {
       tc::mma_tile(tdQ, tc::smem_u32(tdPE), 64, tc::smem_u32(tKt), Dk, C, 1u);      // dQ += dPE K
       tc::mma_tile(tdK, tc::smem_u32(tdPEt), 64, tc::smem_u32(tQt), Dk, C, 1u);     // dK += dPE^T Q
-      tc::mma_tile(tmp, tc::smem_u32(tTt), 64, tc::smem_u32(tdDt), Dv, C, 0u);      // dBv = T^T dD
+      tc::mma_tile(tmp, tc::smem_u32(tTt), 64, tc::smem_u32(tdDt), Dv, C, 0u);      // -dBv = T^T (-dD)
       tc::mma_tile(tmp + 128, tc::smem_u32(tTt), 64, tc::smem_u32(tdTt), C, C, 0u); // Y = T^T dT
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
@@ -589,6 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         float x[16];
         tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = -x[j];
         if (row64 >= 0 && row64 < len) {
           const int s = row64;
           __align__(16) __nv_bfloat162 pk[8];

@@ -397,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
   const uint32_t bW = (uint32_t)tileCD(DK), bKt = (uint32_t)tileDC(DK), bP = 8192;
   const uint32_t bU = (uint32_t)Dv * C * 2, bG = C * 4;
+  const uint32_t bSt = tc::sw128_bytes(MV, DK);       // one saved S^T tile
   uint8_t* tSt = sm;                                  // [MV][DK]
   uint8_t* buf0 = tSt + tc::sw128_bytes(MV, DK);
   const uint32_t bufsz = bW * 2 + bKt + bP + ((bU + bG + 1023) & ~1023u);
@@ -448,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
 #pragma unroll
   for (int i = 0; i < NKC; ++i)
     if (half * 16 + 32 * i < DK && vok) tile_put16(tSt, MV, vrow, half * 16 + 32 * i, S[i]);
+  tc::fence_async_smem();
 
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
@@ -467,14 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     const int i = c - c0, b = i & 1;
     const int64_t t0 = s0 + (int64_t)i * C;
     const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
-    // chunk-start state: for each k, the warp's lanes write consecutive v (128-byte rows)
-    float* sv = p.saved + ((size_t)c * p.Hv + h) * SZ;
-    if (vok)
-#pragma unroll
-      for (int ii = 0; ii < NKC; ++ii)
-        if (half * 16 + 32 * ii < DK)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) sv[(size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = S[ii][j];
     // tiles of this chunk
     const bool lok = tc::mbar_wait(&bars[1 + b], b ? lphase1 : lphase0);
     if (b) lphase1 ^= 1u; else lphase0 ^= 1u;
@@ -483,9 +477,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
       ok = false;
       break;
     }
-    if (tid == 0 && c + 1 < c1) {
-      tc::fence_async_smem();
-      issue_load(c + 1, b ^ 1);
+    if (tid == 0) {
+      // chunk-start state: the S^T tile goes to the saved states as it is, by one
+      // bulk store that runs behind this chunk's work
+      tc::bulk_s2g((uint8_t*)p.saved + ((size_t)c * p.Hv + h) * bSt, tSt, bSt);
+      tc::bulk_commit();
+      if (c + 1 < c1) {
+        tc::fence_async_smem();
+        issue_load(c + 1, b ^ 1);
+      }
     }
     const float* G = sG(b);
     if (tid < C) {
@@ -522,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
+      tc::bulk_wait_read<0>();   // the saved-state store has read S^T: the update may rewrite it
       tc::mma_tile(tX, tc::smem_u32(tDt), MV, tc::smem_u32(tP(b)), C, C, 0u);
       tc::mma_tile(tS, tc::smem_u32(tDct), MV, tc::smem_u32(tKt(b)), DK, C, 0u);
     }, &bars[0], mphase, p.status, c);
@@ -574,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           p.S_T[((size_t)n * p.Hv + h) * SZ + (size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = S[ii][j];
+  if (tid == 0) tc::bulk_wait<0>();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();

@@ -28,14 +28,21 @@
  *  - `*_ld` arguments are row strides in ELEMENTS (one row per token).  Inside a
  *    row, head h occupies columns [h*D, (h+1)*D).
  *  - q, k, v, o, dO, dq, dk, dv have the element type `shape->dtype` (fp32 or
- *    bf16).  alpha, beta_raw, a_log, dt_bias, S_0, S_T, dS_T, dS_0, the saved
- *    states and d alpha, d beta_raw, d a_log, d dt_bias are fp32.  State and
- *    accumulation arithmetic is fp32.  bf16 outputs are rounded to nearest even.
+ *    bf16).  alpha, beta_raw, a_log, dt_bias, S_0, S_T, dS_T, dS_0 and d alpha,
+ *    d beta_raw, d a_log, d dt_bias are fp32.  State and accumulation
+ *    arithmetic is fp32.  bf16 outputs are rounded to nearest even.
  *  - State tensors (S_0, S_T, dS_T, dS_0) are [n_seqs, Hv, Dk, Dv] fp32,
- *    contiguous.  Saved states are [total_chunks, Hv, Dk, Dv] fp32: the state at
- *    the START of each 64-token chunk (chunks never span two sequences; the last
- *    chunk of a sequence may be short; the chunks of sequence n are numbered
- *    from chunk_offsets[n]).
+ *    contiguous.
+ *  - Saved states hold the state at the START of each 64-token chunk (chunks
+ *    never span two sequences; the last chunk of a sequence may be short; the
+ *    chunks of sequence n are numbered from chunk_offsets[n]), one block per
+ *    (chunk, value head), chunk-major.  fp32 inputs: [total_chunks, Hv, Dk, Dv]
+ *    fp32.  bf16 inputs: the state is kept in bf16, as the operand tile of the
+ *    backward's tensor-core products, S^T with MV = max(Dv, 64) rows (v) and
+ *    Dk columns (k), 128-byte-swizzled K-major: element (v, k) is the bf16 at
+ *    byte ((k / 64) * MV + v) * 128 + ((((k % 64) / 8) ^ (v % 8)) * 16) +
+ *    (k % 8) * 2 of its block (padding rows and columns hold zero); a block is
+ *    ceil(Dk / 64) * MV * 128 bytes.
  *  - Pointers marked "device" are CUDA device pointers; "host" ones are host
  *    pointers.  The caller owns every buffer.  The library allocates nothing
  *    and keeps no state between calls.  Outputs are overwritten, never
@@ -119,7 +126,8 @@ typedef struct {
 int gdn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t* chunk_offsets_host,
              int32_t* total_chunks);
 
-/* Bytes of the saved-state buffer: total_chunks * Hv * Dk * Dv * 4.
+/* Bytes of the saved-state buffer: total_chunks * Hv * Dk * Dv * 4 for fp32
+ * inputs, total_chunks * Hv * ceil(Dk / 64) * max(Dv, 64) * 128 for bf16.
  * Returns 0 for an invalid shape. */
 size_t gdn_saved_state_bytes(const gdn_shape* shape);
 
@@ -148,7 +156,7 @@ int gdn_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void*
                 int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
                 const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
                 const int32_t* chunk_offsets, const float* S0, void* o, int64_t o_ld,
-                float* S_T, float* saved_states, void* workspace, size_t workspace_bytes,
+                float* S_T, void* saved_states, void* workspace, size_t workspace_bytes,
                 uint32_t flags, void* stream);
 
 /* Backward (reverse chunk walk with a dS carry).  Inputs as gdn_forward, plus
@@ -172,7 +180,7 @@ int gdn_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void
                  int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
                  const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
                  const int32_t* chunk_offsets, const float* S0, const void* dO, int64_t dO_ld,
-                 const float* dS_T, const float* saved_states, void* dq, int64_t dq_ld,
+                 const float* dS_T, const void* saved_states, void* dq, int64_t dq_ld,
                  void* dk, int64_t dk_ld, void* dv, int64_t dv_ld, float* dalpha,
                  int64_t dalpha_ld, float* dbeta_raw, int64_t dbeta_ld, float* da_log,
                  float* ddt_bias, float* dS0, void* workspace, size_t workspace_bytes,
@@ -210,7 +218,7 @@ int gdn_forward_noalloc(const gdn_shape* shape, const void* q, int64_t q_ld, con
                         int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
                         const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
                         const int32_t* chunk_offsets, const float* S0, void* o, int64_t o_ld,
-                        float* S_T, float* saved_states, void* stream);
+                        float* S_T, void* saved_states, void* stream);
 
 /* Synchronises `stream` and returns the device-side status recorded in
  * `workspace` by the last gdn_forward / gdn_backward that used it (GDN_OK, or

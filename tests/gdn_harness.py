@@ -104,14 +104,32 @@ class DeviceRun:
         import torch
         torch.cuda.synchronize()
         out = dict(o=self.o.double().cpu().numpy(), S_T=self.S_T.double().cpu().numpy())
-        wl = self.inp.wl
-        nbytes = wl.total_chunks * wl.Hv * wl.Dk * wl.Dv
-        out["saved"] = self.layer.saved_states[:nbytes].double().cpu().numpy().reshape(
-            wl.total_chunks, wl.Hv, wl.Dk, wl.Dv)
+        out["saved"] = saved_states_dense(self.layer.saved_states, self.inp.wl)
         if self.grads is not None:
             for k, v in self.grads.items():
                 out[k] = v.double().cpu().numpy()
         return out
+
+
+def saved_states_dense(saved, wl: W.Workload) -> np.ndarray:
+    """The saved chunk-start states as [total_chunks, Hv, Dk, Dv] f64, decoded from the
+    buffer's documented format (include/gdn.h): fp32 blocks, or for bf16 inputs bf16
+    S^T tiles of max(Dv, 64) rows in the 128-byte-swizzled K-major layout."""
+    import torch
+    NC, Hv, Dk, Dv = wl.total_chunks, wl.Hv, wl.Dk, wl.Dv
+    raw = saved.detach().reshape(-1).view(torch.uint8).cpu().numpy()
+    if wl.dtype != "bf16":
+        return raw[:NC * Hv * Dk * Dv * 4].view(np.float32).astype(np.float64).reshape(
+            NC, Hv, Dk, Dv)
+    MV = max(Dv, 64)
+    tile = -(-Dk // 64) * MV * 128
+    u16 = raw[:NC * Hv * tile].view(np.uint16).reshape(NC * Hv, tile // 2)
+    v = np.arange(Dv)[:, None]
+    k = np.arange(Dk)[None, :]
+    off = ((k // 64) * MV + v) * 128 + (((k % 64) // 8) ^ (v % 8)) * 16 + (k % 8) * 2
+    bits = u16[:, off // 2].astype(np.uint32) << 16          # [NC*Hv, Dv, Dk]
+    st = bits.view(np.float32).astype(np.float64).reshape(NC, Hv, Dv, Dk)
+    return st.transpose(0, 1, 3, 2)
 
 
 def head_group_inputs(inp: W.Inputs, kh: int) -> W.Inputs:

@@ -56,7 +56,12 @@ def test_plan(gdn):
 
 def test_sizes(gdn):
     s = gdn.make_shape(16, 48, 128, 128, 1, 64, 4096, "bf16")
-    assert gdn.gdn_saved_state_bytes(s) == 64 * 48 * 128 * 128 * 4
+    # bf16: one bf16 S^T tile per (chunk, value head); fp32: the dense fp32 states
+    assert gdn.gdn_saved_state_bytes(s) == 64 * 48 * 128 * 128 * 2
+    assert gdn.gdn_saved_state_bytes(gdn.make_shape(2, 4, 16, 32, 1, 3, 150, "bf16")) == \
+        3 * 4 * 1 * 64 * 128                 # Dk 16 -> one 64-column block; Dv 32 -> 64 rows
+    assert gdn.gdn_saved_state_bytes(gdn.make_shape(2, 4, 16, 32, 1, 3, 150, "f32")) == \
+        3 * 4 * 16 * 32 * 4
     f, b = gdn.gdn_workspace_bytes(s, False), gdn.gdn_workspace_bytes(s, True)
     assert 256 < f < b and f % 256 == 0 and b % 256 == 0
     bad = gdn.make_shape(16, 48, 96, 128, 1, 64, 4096, "bf16")
