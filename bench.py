@@ -124,28 +124,28 @@ def kernel_models(wl: W.Workload):
     # distinct data (a key-head tile read by its r value-head CTAs counts once)
     sKC = (Dk + 63) // 64 * C * 128                  # [C][Dk] tile
     sVC = (Dv + 63) // 64 * C * 128                  # [C][Dv] tile
-    sKt, sVt, sCC = Dk * 128, Dv * 128, C * C * 2    # [Dk][C], [Dv][C], [C][C] tiles
+    sVt, sCC = Dv * 128, C * C * 2                   # [Dv][C], [C][C] tiles
     MV = max(Dv, 64)
     sST = (Dk + 63) // 64 * MV * 128                 # S^T / dS^T state tile [MV][Dk]
     tok_in = T * (2 * Hk * Dk * es + Hv * Dv * es + 2 * Hv * 4)   # q, k, v, alpha, beta
-    tc_prep_b = (tok_in + NC * Hk * (2 * sKC + sKt) +
-                 NC * Hv * (2 * C * 4 + sVt + sKC + sCC))           # Q, K, K^T; G, b, U^T, W, P
+    tc_prep_b = (tok_in + NC * Hk * 2 * sKC +                       # Q, K tiles
+                 NC * Hv * (2 * C * 4 + sVt + sKC + sCC))           # G, b, U^T, W, P
     tc_prep_f = (NC * Hk * 2 * 128 * C * Dk + NC * Hv * (2 * C * C * (Dk + Dv) + C ** 3 / 3 +
                                                           C * C * 8))
-    tc_prep_bwd_b = tc_prep_b + (NC * Hk * (2 * C * 4 + C * C * 4 + sKt) +   # norms, K K^T, Q^T
-                                 NC * Hv * (sKt + sCC + 3 * sCC))            # W^T, P^T, T tiles
+    tc_prep_bwd_b = tc_prep_b + (NC * Hk * (2 * C * 4 + C * C * 4) +   # norms, K K^T
+                                 NC * Hv * 2 * sCC)                   # T, T diag(b e^G)
     st = N * Hv * Dk * Dv * 4
     fst_st = st * ((wl.S0_std > 0) + 1)                             # S0 read, S_T written
     bst_st = st * ((wl.dST_std > 0) + 1)                            # dS_T read, dS0 written
-    fst_tc_b = (NC * Hk * (sKC + sKt) + NC * Hv * (sKC + sCC + sVt + C * 4) +
+    fst_tc_b = (NC * Hk * 2 * sKC + NC * Hv * (sKC + sCC + sVt + C * 4) +
                 T * Hv * Dv * es + NC * Hv * sST + fst_st)          # ... o, saved S^T tiles
     fst_tc_f = NC * Hv * (6 * C * Dk * Dv + 2 * C * C * Dv)
-    bst_tc_b = (NC * Hk * (sKC + sKt) + NC * Hv * (sCC + sKt + C * 4) + T * Hv * Dv * es +
+    bst_tc_b = (NC * Hk * 2 * sKC + NC * Hv * (sCC + sKC + C * 4) + T * Hv * Dv * es +
                 NC * Hv * (sST + sVC + MV * 128) + bst_st)          # ... dS^T, -dDelta(^T)
     bst_tc_f = NC * Hv * (2 * C * C * Dv + 6 * C * Dk * Dv)
-    bgr_tc_b = (NC * Hk * (2 * sKt + C * C * 4 + 2 * C * 4) + T * Hk * 2 * Dk * es +
+    bgr_tc_b = (NC * Hk * (2 * sKC + C * C * 4 + 2 * C * 4) + T * Hk * 2 * Dk * es +
                 NC * Hv * (sST + 2 * C * 4 + sKC + sVt + sVC + sCC + sST + MV * 128 +
-                           3 * sCC + 8) +
+                           2 * sCC + 8) +
                 T * Hv * (2 * Dv * es + 4) + T * Hv * (Dv * es + 8))
     bgr_tc_f = NC * Hv * (2 * C * Dk * Dv + 2 * 128 * Dk * Dv + 2 * C * Dk * Dv +
                           4 * C * Dk * Dv + 2 * C * C * Dv + 2 * C * C * (Dv + Dk) +

@@ -119,14 +119,10 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
   } else {
     p.Qsw = (uint8_t*)(base + L.Qsw);
     p.Ksw = (uint8_t*)(base + L.Ksw);
-    p.Ktsw = (uint8_t*)(base + L.Ktsw);
     p.Wsw = (uint8_t*)(base + L.Wsw);
     p.Psw = (uint8_t*)(base + L.Psw);
     p.Utb = (__nv_bfloat16*)(base + L.Utb);
     if (bwd) {
-      p.Qtsw = (uint8_t*)(base + L.Qtsw);
-      p.Wtsw = (uint8_t*)(base + L.Wtsw);
-      p.Ptsw = (uint8_t*)(base + L.Ptsw);
       p.KKf = (float*)(base + L.KKf);
       p.Tb = (uint8_t*)(base + L.Tb);
       p.dSb = (uint8_t*)(base + L.dSb);

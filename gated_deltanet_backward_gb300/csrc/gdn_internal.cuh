@@ -57,17 +57,14 @@ struct WsLayout {
   size_t dQh;     // [NC][Hv][C][Dk] per-value-head d q_hat partials (backward)
   size_t dKh;     // [NC][Hv][C][Dk] per-value-head d k_hat partials (backward)
   // bf16 path (tiles)
+  // (a product that wants one of these transposed reads it MN-major)
   size_t Qsw;     // [NC][Hk] [C][Dk]   normalised queries
   size_t Ksw;     // [NC][Hk] [C][Dk]   normalised keys
-  size_t Ktsw;    // [NC][Hk] [Dk][C]   K^T
-  size_t Qtsw;    // [NC][Hk] [Dk][C]   Q^T (backward)
   size_t Wsw;     // [NC][Hv] [C][Dk]   W
-  size_t Wtsw;    // [NC][Hv] [Dk][C]   W^T (backward)
   size_t Psw;     // [NC][Hv] [C][C]    P = E * (Q K^T), lower incl. diagonal
-  size_t Ptsw;    // [NC][Hv] [C][C]    P^T (backward)
   size_t Utb;     // [NC][Hv] [Dv][C]   U^T
   size_t KKf;     // [NC][Hk][C][C] fp32  K K^T (backward)
-  size_t Tb;      // [NC][Hv] 3 x [C][C]: T, T^T, diag(b e^G) T^T (backward)
+  size_t Tb;      // [NC][Hv] 2 x [C][C]: T, T diag(b e^G) (backward)
   size_t dSb;     // [NC][Hv] [MV][Dk] dS^T: state adjoint at each chunk end (backward)
   size_t dDb;     // [NC][Hv] [C][MV]  -d Delta (backward)
   size_t dDtb;    // [NC][Hv] [MV][C]  -d Delta^T (backward); MV = max(Dv, 64)
@@ -117,16 +114,12 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
   } else {
     L.Qsw = take(NC * Hk * tile_CxD(s.Dk));
     L.Ksw = take(NC * Hk * tile_CxD(s.Dk));
-    L.Ktsw = take(NC * Hk * tile_DxC(s.Dk));
     L.Wsw = take(NC * Hv * tile_CxD(s.Dk));
     L.Psw = take(NC * Hv * tile_CxD(64));
     L.Utb = take(NC * Hv * Dv * C * 2);
     if (bwd) {
-      L.Qtsw = take(NC * Hk * tile_DxC(s.Dk));
-      L.Wtsw = take(NC * Hv * tile_DxC(s.Dk));
-      L.Ptsw = take(NC * Hv * tile_CxD(64));
       L.KKf = take(NC * Hk * C * C * 4);
-      L.Tb = take(NC * Hv * 3 * tile_CxD(64));
+      L.Tb = take(NC * Hv * 2 * tile_CxD(64));
       L.dSb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
       L.dDb = take(NC * Hv * tile_CxD(s.Dv));
       L.dDtb = take(NC * Hv * tile_DxC(s.Dv < 64 ? 64 : s.Dv));
@@ -192,12 +185,8 @@ struct Params {
   float* pd;
   uint8_t* Qsw;
   uint8_t* Ksw;
-  uint8_t* Ktsw;
   uint8_t* Wsw;
-  uint8_t* Wtsw;
-  uint8_t* Qtsw;
   uint8_t* Psw;
-  uint8_t* Ptsw;
   __nv_bfloat16* Utb;
   float* KKf;
   uint8_t* Tb;

@@ -20,7 +20,6 @@ namespace gdn {
 namespace {
 constexpr int C = kChunk;
 __device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
-__device__ __forceinline__ size_t tileDC(int D) { return (size_t)D * 128; }
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -40,7 +39,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   constexpr int NKC = (DK + 31) / 32;
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
-  const uint32_t bK = (uint32_t)tileCD(DK), bKt = (uint32_t)tileDC(DK), bP = 8192, bG = C * 4;
+  constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read Q / W MN-major
+  const uint32_t bK = (uint32_t)tileCD(DK), bP = 8192, bG = C * 4;
   const int nbv = (Dv + 63) / 64;
   const uint32_t bO = (uint32_t)nbv * 8192;                  // natural dO tile [C][Dv]
   const uint32_t bSt = tc::sw128_bytes(MV, DK);              // dS^T tile
@@ -49,19 +49,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   uint8_t* tmDt = tdSt + bSt;                                // [MV][C] -dDelta^T
   uint8_t* tmD = tmDt + bDt;                                 // [C][MV] -dDelta
   uint8_t* buf0 = tmD + bD;
-  const uint32_t bufsz = bO + bK + bP + 2 * bKt + 1024;
+  const uint32_t bufsz = bO + 3 * bK + bP + 1024;
   float* ev = (float*)(buf0 + 2 * bufsz);
   float* cv = ev + C;
   uint64_t* bars = (uint64_t*)(cv + C);
   uint32_t* tslot = (uint32_t*)(bars + 3);
-  // per stage buffer: natural dO tile (TMA; the MN-major A operand of dO^T), K, P^T,
-  // Q^T (scaled in place to (scale e^G Q)^T), W^T, G
+  // per stage buffer: the natural tiles of dO (TMA), K, P, Q (scaled in place to
+  // scale e^G Q), W and the gates G; every transposed operand is read MN-major
   auto sdO = [&](int b) { return buf0 + b * bufsz; };
   auto tK = [&](int b) { return buf0 + b * bufsz + bO; };
-  auto tPt = [&](int b) { return buf0 + b * bufsz + bO + bK; };
-  auto tQt = [&](int b) { return buf0 + b * bufsz + bO + bK + bP; };
-  auto tWt = [&](int b) { return buf0 + b * bufsz + bO + bK + bP + bKt; };
-  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + bO + bK + bP + 2 * bKt); };
+  auto tP = [&](int b) { return buf0 + b * bufsz + bO + bK; };
+  auto tQ = [&](int b) { return buf0 + b * bufsz + bO + bK + bP; };
+  auto tW = [&](int b) { return buf0 + b * bufsz + bO + 2 * bK + bP; };
+  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + bO + 3 * bK + bP); };
 
   for (int i = tid; i < (int)(bSt + bDt + bD) / 16; i += kThreads)
     ((uint4*)tdSt)[i] = make_uint4(0, 0, 0, 0);
@@ -101,14 +101,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
     const size_t chh = (size_t)cc * p.Hv + h, ckk = (size_t)cc * p.Hk + kh;
-    tc::mbar_arrive_expect_tx(lb, bO + bK + bP + 2 * bKt + bG);
+    tc::mbar_arrive_expect_tx(lb, bO + 3 * bK + bP + bG);
     for (int b2 = 0; b2 < nbv; ++b2)
       tc::tma_load_2d(sdO(b) + b2 * 8192, &maps.dO, h * Dv + 64 * b2,
                       (int)(s0 + (int64_t)(cc - c0) * C), lb);
     tc::bulk_g2s(tK(b), p.Ksw + ckk * bK, bK, lb);
-    tc::bulk_g2s(tPt(b), p.Ptsw + chh * bP, bP, lb);
-    tc::bulk_g2s(tQt(b), p.Qtsw + ckk * bKt, bKt, lb);
-    tc::bulk_g2s(tWt(b), p.Wtsw + chh * bKt, bKt, lb);
+    tc::bulk_g2s(tP(b), p.Psw + chh * bP, bP, lb);
+    tc::bulk_g2s(tQ(b), p.Qsw + ckk * bK, bK, lb);
+    tc::bulk_g2s(tW(b), p.Wsw + chh * bK, bK, lb);
     tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
   };
   if (tid == 0 && c1 > c0) issue_load(c1 - 1, 0);
@@ -147,28 +147,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
         const int b2 = idx / ((C - len) * 8), rem = idx % ((C - len) * 8);
         ((uint4*)(sdO(b) + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
       }
-    // (scale e^G Q)^T in place: column r of the Q^T tile times scale e^{G_r}
-    for (int idx = tid; idx < DK * (C / 8); idx += kThreads) {
-      const int kk = idx % DK, r8 = (idx / DK) * 8;
-      uint4* at = (uint4*)(tQt(b) + tc::sw128_offset(kk, r8, DK));
+    // scale e^G Q in place: row r of the natural Q tile times scale e^{G_r}
+    for (int idx = tid; idx < C * (DK / 8); idx += kThreads) {
+      const int r = idx % C, k8 = (idx / C) * 8;
+      uint4* at = (uint4*)(tQ(b) + tc::sw128_offset(r, k8, C));
       const uint4 raw = *at;
-      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
+      const __nv_bfloat162* e = (const __nv_bfloat162*)&raw;
+      const float sc = p.scale * ev[r];
       __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        pk[q] = __floats2bfloat162_rn(__bfloat162float(e[2 * q]) * p.scale * ev[r8 + 2 * q],
-                                      __bfloat162float(e[2 * q + 1]) * p.scale * ev[r8 + 2 * q + 1]);
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(e[q]);
+        pk[q] = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+      }
       *at = *(const uint4*)pk;
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::bulk_wait_read<1>();   // last chunk's dDelta stores have read their tiles
       // dO^T as an MN-major operand straight from the natural tile (boxes 8 KB apart)
-      tc::mma_tile_x(tA1, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tPt(b)), false,
-                     (uint32_t)C * 128u, C, C, 0u);
+      // (P^T dO)^T = dO^T P: both operands MN-major (P^T from the natural P tile)
+      tc::mma_tile_x(tA1, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tP(b)), true,
+                     8192u, C, C, 0u);
       tc::mma_tile(tA2, tc::smem_u32(tdSt), MV, tc::smem_u32(tK(b)), C, DK, 0u);
-      tc::mma_tile_x(tA3, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tQt(b)), false,
-                     (uint32_t)DK * 128u, DK, C, 0u);
+      tc::mma_tile_x(tA3, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tQ(b)), true,
+                     8192u, NKF, C, 0u);
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // dDelta^T = scale (P^T dO)^T + c (K dS)^T
@@ -195,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::bulk_wait_read<0>();   // the dS^T store has read its tile: the update may rewrite it
-      tc::mma_tile(tA3, tc::smem_u32(tmDt), MV, tc::smem_u32(tWt(b)), DK, C, 1u);
+      tc::mma_tile_x(tA3, tc::smem_u32(tmDt), false, (uint32_t)MV * 128u, MV,
+                     tc::smem_u32(tW(b)), true, 8192u, NKF, C, 1u);
       tc::bulk_s2g(p.dDtb + ch * bDt, tmDt, bDt);
       tc::bulk_s2g(p.dDb + ch * bD, tmD, bD);
       tc::bulk_commit();
@@ -235,14 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
 // ---------------------------------------------------------------------------
 // Shared-memory plan of k_bwd_grads_tc (bytes for Dk = Dv = 128; phases A-E of one
 // value head reuse the regions):
-//   R1 64K  A: S^T [Dv][Dk] (also read MN-major as S) | B: Delta, c*Delta, dW [C][D],
-//           dW^T [Dk][C]
-//           C-E: dPE, dPE^T, dT^T, Hs [C][C] (over Delta / c*Delta)
+//   R1 65K  A: S^T [Dv][Dk] (also read MN-major as S) | B: Delta, c*Delta, dW [C][D]
+//           C-E: dPE, dT, H [C][C] (over Delta / c*Delta)
+//           A-E, from 48K: K K^T of the key head, fp32 [C][C + 4] (whole CTA)
 //   R2 32K  A-B: [dO; -dDelta] [128][Dv]  | B-E: fp32 [C][C] scratch
 //   R3 48K  A: W [C][Dk], scale e^G dO [C][Dv], U^T [Dv][C] | B: dS^T [Dv][Dk], P [C][C]
-//           C-E: -dDelta^T [Dv][C], T^T, T, b e^G T^T, Y [C][C]
+//           C-E: -dDelta^T [Dv][C], T, T diag(b e^G), Y [C][C]
 //   R4 32K  B-C: V [C][Dv], -e^G K [C][Dk]
-//   R5 32K  K^T, Q^T [Dk][C] of the key head (whole CTA)
+//   R5 32K  K, Q [C][Dk] of the key head (whole CTA)
+// Every transposed operand (T^T, dW^T, dPE^T, dT^T, K^T, Q^T, S, dS) is a natural
+// tile read MN-major.
 // TMEM (512 columns): dQ_hat @0, dK_hat @128 (M = 64 accumulators), scratch @256.
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
@@ -260,14 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   const int Dk = p.Dk, Dv = p.Dv;
   const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
   const uint32_t sCK = tc::sw128_bytes(C, Dk), sCV = tc::sw128_bytes(C, Dv);
-  const uint32_t sKC = (uint32_t)Dk * 128, sCC = 8192;
+  const uint32_t sCC = 8192;
   // tiles handed over by the state kernels: S^T and dS^T [MV][Dk], -dDelta^T [MV][C],
   // -dDelta [C][MV] (MV = Dv rounded up to 64); MMAs whose N is Dk read S / dS
   // MN-major with N rounded up to 64 (the tiles' padding columns are zero)
   const int MV = Dv < 64 ? 64 : Dv, NK = Dk < 64 ? 64 : Dk;
   const uint32_t bSt = tc::sw128_bytes(MV, Dk), sVC = (uint32_t)MV * 128;
   uint8_t* R1 = sm;
-  uint8_t* R2 = R1 + 65536;
+  uint8_t* R2 = R1 + 66560;
   uint8_t* R3 = R2 + 32768;
   uint8_t* R4 = R3 + 49152;
   uint8_t* R5 = R4 + 32768;
@@ -276,11 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   uint8_t* tDl = R1;                               // [C][Dv]
   uint8_t* tDlc = R1 + 16384;                      // [C][Dv]
   uint8_t* tdW = R1 + 32768;                       // [C][Dk]
-  uint8_t* tdWt = R1 + 49152;                      // [Dk][C]
   uint8_t* tdPE = R1;                              // [C][C]
-  uint8_t* tdPEt = R1 + 8192;
-  uint8_t* tdTt = R1 + 16384;
-  uint8_t* tHs = R1 + 24576;
+  uint8_t* tdT = R1 + 16384;                       // [C][C]
+  uint8_t* tH = R1 + 24576;                        // [C][C] H = dA b_r E (strictly lower)
+  float* sKK = (float*)(R1 + 49152);               // [C][KKL] fp32 K K^T (padded rows)
+  constexpr int KKL = C + 4;
   // R2
   uint8_t* tA2 = R2;                               // [128][Dv]: rows 0-63 dO, 64-127 -dDelta
   float* X = (float*)R2;                           // [C][C + 1] fp32 scratch (padded rows)
@@ -292,17 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   uint8_t* tdS = R3;                               // [MV][Dk] dS^T (read MN-major as dS)
   uint8_t* tP = R3 + 32768;                        // [C][C]
   uint8_t* tdDt = R3;                              // [MV][C] -dDelta^T
-  uint8_t* tTt = R3 + 16384;
-  uint8_t* tT = R3 + 24576;
-  uint8_t* tTbe = R3 + 32768;
+  uint8_t* tT = R3 + 16384;                        // [C][C] T
+  uint8_t* tTW = R3 + 24576;                       // [C][C] T diag(b e^G)
   uint8_t* tY = R3 + 40960;
   // R4
   uint8_t* tV = R4;                                // [C][Dv]
   uint8_t* tKe = R4 + 16384;                       // [C][Dk] -e^G K
-  float* sKK = (float*)R4;                         // [C][C] fp32 K K^T (phase D)
   // R5
-  uint8_t* tKt = R5;                               // [Dk][C]
-  uint8_t* tQt = R5 + 16384;                       // [Dk][C]
+  uint8_t* tK = R5;                                // [C][Dk]
+  uint8_t* tQ = R5 + 16384;                        // [C][Dk]
   float* vec = (float*)(R5 + 32768);
   float* gv = vec;            // G
   float* ev = gv + C;         // e^G
@@ -310,8 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   float* bv = cv + C;         // beta
   float* dG = bv + C;         // dL/dG
   float* db = dG + C;         // dL/d beta
-  float* part = db + C;       // [2][C] per-half partial row sums
-  float* red = part + 2 * C;  // [kThreads / 32]
+  float* xa = db + C;         // alpha + dt_bias of the chunk's tokens
+  float* part = xa + C;       // [2][C] per-half partial row sums
+  float* rowp = part + 2 * C; // [2][C] per-half partial row sums
+  float* colp = rowp + 2 * C; // [4][C] per-quarter partial column sums
+  float* red = colp + 4 * C;  // [kThreads / 32]
   uint64_t* bars = (uint64_t*)(red + 8);  // mma, load
   uint32_t* tslot = (uint32_t*)(bars + 2);
 
@@ -331,15 +338,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   const uint32_t tdQ = tmem, tdK = tmem + 128, tmp = tmem + 256;
   uint32_t mphase = 0, lphase = 0;
   const size_t ckk = (size_t)c * p.Hk + kh;
-  const float* KK = p.KKf + ckk * C * C;
   const int row64 = acc_row(64);
   bool ok = true;
 
   // key-head tiles for the whole CTA
   if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&bars[1], 2 * sKC);
-    tc::bulk_g2s(tKt, p.Ktsw + ckk * sKC, sKC, &bars[1]);
-    tc::bulk_g2s(tQt, p.Qtsw + ckk * sKC, sKC, &bars[1]);
+    tc::mbar_arrive_expect_tx(&bars[1], 2 * sCK);
+    tc::bulk_g2s(tK, p.Ksw + ckk * sCK, sCK, &bars[1]);
+    tc::bulk_g2s(tQ, p.Qsw + ckk * sCK, sCK, &bars[1]);
+  }
+  {
+    // K K^T of the key head into padded rows (conflict-free row reads in epilogue D)
+    const float4* KK = (const float4*)(p.KKf + ckk * C * C);
+    for (int i = tid; i < C * C / 4; i += kThreads)
+      *(float4*)(sKK + (i / (C / 4)) * KKL + (i % (C / 4)) * 4) = KK[i];
   }
   {
     const bool lok = tc::mbar_wait(&bars[1], lphase);
@@ -359,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
       const float g = p.G[ch * C + tid];
       gv[tid] = g;
       bv[tid] = p.b[ch * C + tid];
+      xa[tid] = tid < len ? p.alpha[(t0 + tid) * p.alpha_ld + h] + p.dt_bias[h] : 0.f;
       dG[tid] = 0.f;
       db[tid] = 0.f;
     }
@@ -441,11 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
         if (row < C) {
+          float qv[16];
+          tile_get16(tQ, C, row, q * 16, qv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(tile_get(tQt, Dk, q * 16 + j, row), x[j], rs);
+          for (int j = 0; j < 16; ++j) rs = fmaf(qv[j], x[j], rs);
         } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) tile_put(tdWt, Dk, q * 16 + j, row - C, x[j]);
           tile_put16(tdW, C, row - C, q * 16, x);
         }
       }
@@ -468,12 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     }
     for (int idx = tid; idx < C * (Dk / 8); idx += kThreads) {
       const int s = idx % C, k8 = (idx / C) * 8;
+      const uint32_t off = tc::sw128_offset(s, k8, C);
+      const uint4 raw = *(const uint4*)(tK + off);
+      const __nv_bfloat162* e = (const __nv_bfloat162*)&raw;
+      const float sc = -ev[s];
       __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        pk[u] = __floats2bfloat162_rn(-tile_get(tKt, Dk, k8 + 2 * u, s) * ev[s],
-                                      -tile_get(tKt, Dk, k8 + 2 * u + 1, s) * ev[s]);
-      *(uint4*)(tKe + tc::sw128_offset(s, k8, C)) = *(const uint4*)pk;
+      for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(e[u]);
+        pk[u] = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+      }
+      *(uint4*)(tKe + off) = *(const uint4*)pk;
     }
     {
       const bool lok = tc::mbar_wait(&bars[1], lphase);
@@ -518,6 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
       tc::mma_tile(tmp + 192, tc::smem_u32(tdW), 64, tc::smem_u32(tKe), C, Dk, 1u);     // - dW (e^G K)^T
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
+    // phase C's tiles land in the dS^T space (free now) while epilogue B runs
+    if (tid == 0) {
+      const uint8_t* tb = p.Tb + ch * 2 * sCC;
+      tc::mbar_arrive_expect_tx(&bars[1], sVC + 2 * sCC);
+      tc::bulk_g2s(tdDt, p.dDtb + ch * sVC, sVC, &bars[1]);
+      tc::bulk_g2s(tT, tb, sCC, &bars[1]);
+      tc::bulk_g2s(tTW, tb + sCC, sCC, &bars[1]);
+    }
     // epilogue B
     {
       float rs = 0.f;
@@ -525,41 +551,57 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         float x[16];
         tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
-        if (row64 >= 0)
+        if (row64 >= 0) {
+          float kv[16];
+          tile_get16(tK, C, row64, q * 16, kv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(tile_get(tKt, Dk, q * 16 + j, row64), x[j], rs);
+          for (int j = 0; j < 16; ++j) rs = fmaf(kv[j], x[j], rs);
+        }
       }
       if (row64 >= 0) part[half * C + row64] = rs;  // c_s * dc_s
     }
-    for (int q = half; q < 4; q += 2) {
-      float x[16], y[16];
-      tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
-      tc::tmem_ld16(tmp + 192 + lane_quarter() + q * 16, y);
-      tc::tmem_ld_wait();
-      if (row64 >= 0) {
-        const int r = row64;
-        float pv[16], pe[16];
-        tile_get16(tP, C, r, q * 16, pv);
+    {
+      float rsum = 0.f;
+      for (int q = half; q < 4; q += 2) {
+        float x[16], y[16];
+        tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
+        tc::tmem_ld16(tmp + 192 + lane_quarter() + q * 16, y);
+        tc::tmem_ld_wait();
+        if (row64 >= 0) {
+          const int r = row64;
+          float pv[16], pe[16], dt[16];
+          tile_get16(tP, C, r, q * 16, pv);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int s = q * 16 + j;
-          const float dP = (s <= r && r < len) ? p.scale * x[j] : 0.f;
-          const float E = s <= r ? expf(gv[r] - gv[s]) : 0.f;
-          X[r * XL + s] = dP * pv[j];
-          pe[j] = dP * E;
-          tile_put(tdPEt, C, s, r, pe[j]);
-          tile_put(tdTt, C, s, r, -bv[s] * y[j]);  // dT[r][s] = b_s (dDelta V^T + dW (e^G K)^T)
+          for (int j = 0; j < 16; ++j) {
+            const int s = q * 16 + j;
+            const float dP = (s <= r && r < len) ? p.scale * x[j] : 0.f;
+            const float E = s <= r ? expf(gv[r] - gv[s]) : 0.f;
+            const float xp = dP * pv[j];
+            X[r * XL + s] = xp;
+            rsum += xp;
+            pe[j] = dP * E;
+            dt[j] = -bv[s] * y[j];   // dT[r][s] = b_s (dDelta V^T + dW (e^G K)^T)[r][s]
+          }
+          tile_put16(tdPE, C, r, q * 16, pe);
+          tile_put16(tdT, C, r, q * 16, dt);
         }
-        tile_put16(tdPE, C, r, q * 16, pe);
       }
+      if (row64 >= 0) rowp[half * C + row64] = rsum;
+    }
+    __syncthreads();
+    {
+      // column sums of X in four quarters of rows
+      const int t = tid & (C - 1), qd = tid >> 6;
+      float cs = 0.f;
+#pragma unroll 4
+      for (int r = qd * 16; r < qd * 16 + 16; ++r) cs += X[r * XL + t];
+      colp[qd * C + t] = cs;
     }
     __syncthreads();
     if (tid < C) {
       const int t = tid;
-      float rsum = 0.f, csum = 0.f;
-      for (int s = 0; s < C; ++s) rsum += X[t * XL + s];
-      for (int r = 0; r < C; ++r) csum += X[r * XL + t];
-      dG[t] += rsum - csum - (part[t] + part[C + t]);
+      const float csum = (colp[t] + colp[C + t]) + (colp[2 * C + t] + colp[3 * C + t]);
+      dG[t] += (rowp[t] + rowp[C + t]) - csum - (part[t] + part[C + t]);
     }
     __syncthreads();
     if (tid == 0) {
@@ -568,15 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
       for (int s = 0; s < C; ++s) sc += part[s] + part[C + s];
       dG[len - 1] += expf(gv[len - 1]) * tot + sc;
     }
-    // ---- phase C: -dDelta^T, T^T, T, b e^G T^T
-    if (tid == 0) {
-      const uint8_t* tb = p.Tb + ch * 3 * sCC;
-      tc::mbar_arrive_expect_tx(&bars[1], sVC + 3 * sCC);
-      tc::bulk_g2s(tdDt, p.dDtb + ch * sVC, sVC, &bars[1]);
-      tc::bulk_g2s(tT, tb, sCC, &bars[1]);
-      tc::bulk_g2s(tTt, tb + sCC, sCC, &bars[1]);
-      tc::bulk_g2s(tTbe, tb + 2 * sCC, sCC, &bars[1]);
-    }
+    // ---- phase C: -dDelta^T, T, T diag(b e^G) (issued after the MMAs of phase B)
     {
       const bool lok = tc::mbar_wait(&bars[1], lphase);
       lphase ^= 1u;
@@ -588,10 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::mma_tile(tdQ, tc::smem_u32(tdPE), 64, tc::smem_u32(tKt), Dk, C, 1u);      // dQ += dPE K
-      tc::mma_tile(tdK, tc::smem_u32(tdPEt), 64, tc::smem_u32(tQt), Dk, C, 1u);     // dK += dPE^T Q
-      tc::mma_tile(tmp, tc::smem_u32(tTt), 64, tc::smem_u32(tdDt), Dv, C, 0u);      // -dBv = T^T (-dD)
-      tc::mma_tile(tmp + 128, tc::smem_u32(tTt), 64, tc::smem_u32(tdTt), C, C, 0u); // Y = T^T dT
+      const uint32_t T_ = tc::smem_u32(tT);
+      tc::mma_tile_x(tdQ, tc::smem_u32(tdPE), false, sCC, 64, tc::smem_u32(tK), true, 8192u, NK,
+                     C, 1u);                                                               // dQ += dPE K
+      tc::mma_tile_x(tdK, tc::smem_u32(tdPE), true, sCC, 64, tc::smem_u32(tQ), true, 8192u, NK,
+                     C, 1u);                                                               // dK += dPE^T Q
+      tc::mma_tile_x(tmp, T_, true, sCC, 64, tc::smem_u32(tdDt), false, sVC, Dv, C, 0u);  // -dBv = T^T (-dD)
+      tc::mma_tile_x(tmp + 128, T_, true, sCC, 64, tc::smem_u32(tdT), true, sCC, C, C, 0u); // Y = T^T dT
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // epilogue C: dv = b dBv, db += rowsum(dBv * V), Y tile
@@ -607,8 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
         if (row64 >= 0 && row64 < len) {
           const int s = row64;
           __align__(16) __nv_bfloat162 pk[8];
+          float vv[16];
+          tile_get16(tV, C, s, q * 16, vv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(x[j], tile_get(tV, C, s, q * 16 + j), rs);
+          for (int j = 0; j < 16; ++j) rs = fmaf(x[j], vv[j], rs);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             pk[j] = __floats2bfloat162_rn(bv[s] * x[2 * j], bv[s] * x[2 * j + 1]);
@@ -627,82 +666,101 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     }
     __syncthreads();
     if (tid < C) db[tid] += part[tid] + part[C + tid];
-    // K K^T into shared memory (R4 is free once epilogue C has read V)
-    for (int i = tid; i < C * C / 4; i += kThreads) ((float4*)sKK)[i] = ((const float4*)KK)[i];
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::mma_tile(tmp, tc::smem_u32(tTt), 64, tc::smem_u32(tdWt), Dk, C, 0u);    // dBk = T^T dW
-      tc::mma_tile(tdK, tc::smem_u32(tTbe), 64, tc::smem_u32(tdWt), Dk, C, 1u);   // dK += b e^G dBk
+      tc::mma_tile_x(tmp, tc::smem_u32(tT), true, sCC, 64, tc::smem_u32(tdW), true, 8192u, NK, C,
+                     0u);                                                         // dBk = T^T dW
+      tc::mma_tile_x(tdK, tc::smem_u32(tTW), true, sCC, 64, tc::smem_u32(tdW), true, 8192u, NK,
+                     C, 1u);                                                      // dK += b e^G dBk
       tc::mma_tile(tmp + 128, tc::smem_u32(tY), 64, tc::smem_u32(tT), C, C, 0u);  // Y T^T
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
-    // epilogue D: t_s = rowsum(dBk * K); dA = -(Y T^T) strictly lower
+    // epilogue D: t_s = rowsum(dBk * K); dA = -(Y T^T) strictly lower.  With
+    // A[r][s] = b_r E_rs KK_rs (s < r) and q = dA E KK: db_r += sum_s q[r][s],
+    // dG_r += b_r sum_s q[r][s], dG_s -= sum_r b_r q[r][s]; H = dA b_r E for the
+    // dK term (H + H^T) K
     {
       float rs = 0.f;
       for (int q = half; q * 16 < Dk; q += 2) {
         float x[16];
         tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
-        if (row64 >= 0)
+        if (row64 >= 0) {
+          float kv[16];
+          tile_get16(tK, C, row64, q * 16, kv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(tile_get(tKt, Dk, q * 16 + j, row64), x[j], rs);
+          for (int j = 0; j < 16; ++j) rs = fmaf(kv[j], x[j], rs);
+        }
       }
       if (row64 >= 0) part[half * C + row64] = rs;
+      float rq = 0.f;
       for (int q = half; q < 4; q += 2) {
         float x[16];
         tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
-        if (row64 >= 0)
+        if (row64 >= 0) {
+          const int r = row64;
+          const float* kkr = sKK + r * KKL + q * 16;
+          float hv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int s = q * 16 + j;
-            X[row64 * XL + s] = s < row64 ? -x[j] : 0.f;
+            const float E = s < r ? expf(gv[r] - gv[s]) : 0.f;
+            const float de = -x[j] * E;            // dA E (zero on and above the diagonal)
+            const float qq = de * kkr[j];
+            rq += qq;
+            X[r * XL + s] = qq * bv[r];
+            hv[j] = de * bv[r];
           }
+          tile_put16(tH, C, r, q * 16, hv);
+        }
       }
+      if (row64 >= 0) rowp[half * C + row64] = rq;
+    }
+    __syncthreads();
+    {
+      const int t = tid & (C - 1), qd = tid >> 6;
+      float cs = 0.f;
+#pragma unroll 4
+      for (int r = qd * 16; r < qd * 16 + 16; ++r) cs += X[r * XL + t];
+      colp[qd * C + t] = cs;
     }
     __syncthreads();
     if (tid < C) {
       const int t = tid;
-      const float ts = part[t] + part[C + t];
-      db[t] += ev[t] * ts;
-      dG[t] += bv[t] * ev[t] * ts;
-      // A[r][s] = b_r E_rs KK_rs (s < r): db_r += sum_s dA E KK, dG_r += sum_s dA*A, dG_s -= sum_r dA*A
-      float rdb = 0.f, ry = 0.f, cy = 0.f;
-      for (int s = 0; s < t; ++s) {
-        const float q = X[t * XL + s] * expf(gv[t] - gv[s]) * sKK[t * C + s];
-        rdb += q;
-        ry += q * bv[t];
-      }
-      for (int r = t + 1; r < C; ++r) cy += X[r * XL + t] * expf(gv[r] - gv[t]) * sKK[r * C + t] * bv[r];
-      db[t] += rdb;
-      dG[t] += ry - cy;
-    }
-    // H = dA * b_r E; Hs = H + H^T
-    for (int idx = tid; idx < C * C; idx += kThreads) {
-      const int s = idx / C, r = idx % C;
-      const float h1 = r < s ? X[s * XL + r] * bv[s] * expf(gv[s] - gv[r]) : 0.f;
-      const float h2 = s < r ? X[r * XL + s] * bv[r] * expf(gv[r] - gv[s]) : 0.f;
-      tile_put(tHs, C, s, r, h1 + h2);
+      const float ts = part[t] + part[C + t], rq = rowp[t] + rowp[C + t];
+      const float cy = (colp[t] + colp[C + t]) + (colp[2 * C + t] + colp[3 * C + t]);
+      db[t] += ev[t] * ts + rq;
+      dG[t] += bv[t] * (ev[t] * ts + rq) - cy;
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::mma_tile(tdK, tc::smem_u32(tHs), 64, tc::smem_u32(tKt), Dk, C, 1u);     // dK += Hs K
+      tc::mma_tile_x(tdK, tc::smem_u32(tH), false, sCC, 64, tc::smem_u32(tK), true, 8192u, NK,
+                     C, 1u);                                                      // dK += H K
+      tc::mma_tile_x(tdK, tc::smem_u32(tH), true, sCC, 64, tc::smem_u32(tK), true, 8192u, NK,
+                     C, 1u);                                                      // dK += H^T K
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
-    // gate and sigmoid epilogues: dl = reverse cumsum of dG
-    if (tid == 0) {
-      float run = 0.f;
-      for (int t = C - 1; t >= 0; --t) {
-        run += (t < len) ? dG[t] : 0.f;
-        part[t] = run;
+    // gate and sigmoid epilogues: dl = reverse cumsum of dG (one warp, two per lane)
+    __syncthreads();
+    if (warp == 0) {
+      const int l = tid;
+      const float a = 2 * l < len ? dG[2 * l] : 0.f, b2 = 2 * l + 1 < len ? dG[2 * l + 1] : 0.f;
+      float run = a + b2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, run, o);
+        if (l + o < 32) run += y;
       }
+      part[2 * l] = run;
+      part[2 * l + 1] = run - a;
     }
     __syncthreads();
     {
       float pa = 0.f, pd = 0.f;
       if (tid < len) {
         const int t = tid;
-        const float x = p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
+        const float x = xa[t];
         const float ea = expf(p.a_log[h]);
         const float l = -ea * softplus_f(x);
         const float dl = part[t];
@@ -731,15 +789,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   if (ok) {
     for (int which = 0; which < 2; ++which) {
       const uint32_t acc = which ? tdK : tdQ;
-      const uint8_t* xt = which ? tKt : tQt;   // x_hat^T tiles [Dk][C]
+      const uint8_t* xt = which ? tK : tQ;   // x_hat tiles [C][Dk]
       float dot = 0.f;
       for (int q = half; q * 16 < Dk; q += 2) {
         float x[16];
         tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
-        if (row64 >= 0)
+        if (row64 >= 0) {
+          float xv[16];
+          tile_get16(xt, C, row64, q * 16, xv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dot = fmaf(x[j], tile_get(xt, Dk, q * 16 + j, row64), dot);
+          for (int j = 0; j < 16; ++j) dot = fmaf(x[j], xv[j], dot);
+        }
       }
       if (row64 >= 0) part[half * C + row64] = dot;
       __syncthreads();
@@ -755,10 +816,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
           const int r = row64;
           const float d = part[r] + part[C + r], inv = 1.f / nrm[r];
           __align__(16) __nv_bfloat162 pk[8];
+          float xv[16];
+          tile_get16(xt, C, r, q * 16, xv);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float a = (x[2 * j] - tile_get(xt, Dk, q * 16 + 2 * j, r) * d) * inv;
-            const float b2 = (x[2 * j + 1] - tile_get(xt, Dk, q * 16 + 2 * j + 1, r) * d) * inv;
+            const float a = (x[2 * j] - xv[2 * j] * d) * inv;
+            const float b2 = (x[2 * j + 1] - xv[2 * j + 1] * d) * inv;
             pk[j] = __floats2bfloat162_rn(a, b2);
           }
           uint4* o = (uint4*)(dst + (int64_t)r * ld + q * 16);
@@ -792,9 +855,9 @@ __global__ void k_bwd_gates_tc(Params p) {
 template <int DK>
 static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, cudaStream_t st) {
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
-  const size_t bK = tc::sw128_bytes(64, DK), bKt = (size_t)DK * 128;
+  const size_t bK = tc::sw128_bytes(64, DK);
   const size_t bO = (size_t)((Dv + 63) / 64) * 8192;
-  const size_t bufsz = bO + bK + 8192 + 2 * bKt + 1024;
+  const size_t bufsz = bO + 3 * bK + 8192 + 1024;
   const size_t smem = tc::sw128_bytes(MV, DK) + 2 * (size_t)MV * 128 + 2 * bufsz + 2 * C * 4 + 64 + 1024;
   cudaFuncSetAttribute(k_bwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_BWD_STATE_TC);
@@ -814,7 +877,7 @@ cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st)
     }
     if (e != cudaSuccess) return e;
   }
-  const size_t smem = 65536 + 32768 + 49152 + 32768 + 32768 + (size_t)(10 * C + 8) * 4 + 64 + 1024;
+  const size_t smem = 66560 + 32768 + 49152 + 32768 + 32768 + (size_t)(16 * C + 8) * 4 + 64 + 1024;
   cudaFuncSetAttribute(k_bwd_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_BWD_GRADS_TC);
   k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, maps);

@@ -26,7 +26,6 @@ constexpr int C = kChunk;
 constexpr int RB = 3;  // value heads prepared together (triangular solves in parallel)
 
 __device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
-__device__ __forceinline__ size_t tileDC(int D) { return (size_t)D * 128; }
 
 // In-place inverse of (I + A) for nh strictly-lower 64x64 fp32 matrices A
 // (Tm[hh] holds A on entry, T = (I + A)^-1 on exit).  Diagonal 16x16 blocks by
@@ -102,20 +101,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
     return;
   }
   const int Dk = p.Dk, Dv = p.Dv;
-  const int MK = Dk < 64 ? 64 : Dk, MV = Dv < 64 ? 64 : Dv;
+  const int MV = Dv < 64 ? 64 : Dv, NK = Dk < 64 ? 64 : Dk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t aqk_pitch = 128u * 128u;
+  const int nbk = (Dk + 63) / 64, nbv = (Dv + 63) / 64;
+  const uint32_t aqk_pitch = 128u * 128u;               // 64-column blocks of the [K; Q] tile
+  const uint32_t bKC = tc::sw128_bytes(64, Dk);
   uint8_t* tAQK = sm;                                   // [128][Dk]: rows 0-63 K, 64-127 Q
-  uint8_t* tKt = tAQK + tc::sw128_bytes(128, Dk);       // [MK][C]  K^T
-  uint8_t* tVt = tKt + MK * 128;                        // [MV][C]  V^T of one head
-  uint8_t* tTW = tVt + MV * 128;                        // [C][C]   T diag(b e^G)
-  uint8_t* tTB = tTW + 8192;                            // [C][C]   T diag(b)
-  uint8_t* tOW = tTB + 8192;                            // [C][Dk]  W (staging)
-  uint8_t* tOWt = tOW + tc::sw128_bytes(64, Dk);        // [Dk][C]  W^T (staging)
-  uint8_t* tOP = tOWt + Dk * 128;                       // [C][C]   P (staging)
-  uint8_t* tOPt = tOP + 8192;                           // [C][C]   P^T (staging, backward)
-  uint8_t* tQt = tOW;  // [MK][C] Q^T (backward); shares tOW's space, used before the head loop
-  float* KK = (float*)(tOPt + 8192);                    // [C][C]
+  uint8_t* sV = tAQK + nbk * aqk_pitch;                 // [C][Dv] natural V of one head (TMA)
+  uint8_t* tTW = sV + nbv * 8192;                       // [C][C] T diag(b e^G)
+  uint8_t* tTB = tTW + 8192;                            // [C][C] T diag(b)
+  uint8_t* tP = tTB + 8192;                             // [C][C] P
+  uint8_t* tT = tP + 8192;                              // [C][C] T (backward)
+  uint8_t* tW = tT + 8192;                              // [C][Dk] W
+  float* KK = (float*)(tW + bKC);                       // [C][C]
   float* QK = KK + C * C;                               // [C][C]
   float* Tm = QK + C * C;                               // [RB][C][C]
   float* Mt = Tm + RB * C * C;                          // [RB][3][256]
@@ -124,12 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
   float* wv = bv + RB * C;                              // [RB][C]
   uint64_t* bar = (uint64_t*)(wv + RB * C);   // [0] MMA completion, [1] TMA loads
   uint32_t* tslot = (uint32_t*)(bar + 2);
-  uint8_t* sV = (uint8_t*)KK;  // [C][Dv] natural V tile of one head (KK is free by then)
 
-  // zero the transposed tiles (rows past Dk / Dv pad the M = 64 products)
-  for (int i = tid; i < MK * 128 / 16; i += kThreads) ((uint4*)tKt)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < MK * 128 / 16; i += kThreads) ((uint4*)tQt)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < MV * 128 / 16; i += kThreads) ((uint4*)tVt)[i] = make_uint4(0, 0, 0, 0);
+  // W's padding columns (Dk < 64) stay zero: the epilogue writes only columns < Dk
+  if (Dk < 64)
+    for (int i = tid; i < (int)bKC / 16; i += kThreads) ((uint4*)tW)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     tc::mbar_init(&bar[0], 1);
     tc::mbar_init(&bar[1], 1);
@@ -142,11 +138,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = *tslot;
+  // TMEM columns: [0, 64) the Gram products, [64, 64 + NK) W, [192, 256) U^T
+  const uint32_t tmem = *tslot, tAccW = tmem + 64, tAccU = tmem + 192;
   uint32_t phase = 0, lphase = 0;
   bool ok = true;
-  const int nbk = (Dk + 63) / 64, nbv = (Dv + 63) / 64;
-  const size_t ck = ((size_t)c * p.Hk + kh) * C;
+  const size_t ckk = (size_t)c * p.Hk + kh, ck = ckk * C;
   // raw k and q rows of the chunk: TMA boxes straight into the [K; Q] operand tile
   if (tid == 0) {
     tc::mbar_arrive_expect_tx(&bar[1], 2u * nbk * 8192u);
@@ -165,8 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
   }
   if (!ok) goto done;
 
-  // 1. L2-normalise q and k rows into the operand tiles.
-  // L2 normalisation in place: a row of Dk elements is Dk/8 consecutive threads
+  // 1. L2 normalisation in place: a row of Dk elements is Dk/8 consecutive threads;
+  // rows past the chunk become zero
   {
     const int lpr = Dk / 8;
     const int total = 2 * C * lpr;
@@ -196,19 +192,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
         if (bwd && c0 == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
       }
     }
-  }
-  __syncthreads();
-  // K^T (and Q^T) tiles from the natural rows: thread (k, chunk of 8 tokens)
-  for (int idx = tid; idx < (bwd ? 2 : 1) * Dk * (C / 8); idx += kThreads) {
-    const int which = idx / (Dk * (C / 8)), rem = idx % (Dk * (C / 8));
-    const int kk = rem % Dk, t8 = (rem / Dk) * 8;
-    __align__(16) __nv_bfloat16 v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      v[q] = *(const __nv_bfloat16*)(tAQK + tc::sw128_offset(which * C + t8 + q, kk, 128));
-    *(uint4*)((which ? tQt : tKt) + tc::sw128_offset(kk, t8, MK)) = *(const uint4*)v;
+    // Dk < 64: the box's columns past Dk (a neighbouring head) become zero padding
+    if (Dk < 64) {
+      const int padc = 8 - Dk / 8;
+      for (int idx = tid; idx < 2 * C * padc; idx += kThreads) {
+        const int row = idx / padc, c0 = (Dk / 8 + idx % padc) * 8;
+        *(uint4*)(tAQK + tc::sw128_offset(row, c0, 128)) = make_uint4(0, 0, 0, 0);
+      }
+    }
   }
   tc::fence_async_smem();
+  __syncthreads();
+  // the natural K and Q tiles of this key head go to the workspace as they are
+  if (tid == 0) {
+    for (int b = 0; b < nbk; ++b) {
+      tc::bulk_s2g(p.Ksw + ckk * bKC + b * 8192, tAQK + b * aqk_pitch, 8192);
+      tc::bulk_s2g(p.Qsw + ckk * bKC + b * 8192, tAQK + b * aqk_pitch + 8192, 8192);
+    }
+    tc::bulk_commit();
+  }
   // 2. [K; Q] K^T -> TMEM columns [0, 64): lanes 0-63 K K^T, lanes 64-127 Q K^T.
   ok = mma_run([&] { tc::mma_tile_p(tmem, tc::smem_u32(tAQK), aqk_pitch, 128, tc::smem_u32(tAQK),
                                      aqk_pitch, 64, Dk, 0u); },
@@ -216,25 +218,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
   if (!ok) goto done;
   acc_walk(tmem, 128, 64, 128, [&](int row, int col0, const float* v) {
     float* dst = row < C ? KK + row * C : QK + (row - C) * C;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) dst[col0 + j] = v[j];
-    if (bwd && row < C) {
-      float* g = p.KKf + (ck + row) * C + col0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) g[j] = v[j];
-    }
+    *(float4*)(dst + col0) = make_float4(v[0], v[1], v[2], v[3]);
+    *(float4*)(dst + col0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    *(float4*)(dst + col0 + 8) = make_float4(v[8], v[9], v[10], v[11]);
+    *(float4*)(dst + col0 + 12) = make_float4(v[12], v[13], v[14], v[15]);
   });
-  // operand tiles of this key head to the workspace
-  {
-    const size_t tcd = tileCD(Dk);
-    uint8_t* gq = p.Qsw + ((size_t)c * p.Hk + kh) * tcd;
-    uint8_t* gk = p.Ksw + ((size_t)c * p.Hk + kh) * tcd;
-    for (int b = 0; b * 64 < Dk; ++b) {
-      cta_copy16(gk + b * 8192, tAQK + b * aqk_pitch, 8192);
-      cta_copy16(gq + b * 8192, tAQK + b * aqk_pitch + 8192, 8192);
+  if (bwd) {
+    tc::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {   // K K^T (fp32, row-major) for the gradient kernel
+      tc::bulk_s2g(p.KKf + ck * C, KK, C * C * 4);
+      tc::bulk_commit();
     }
-    cta_copy16(p.Ktsw + ((size_t)c * p.Hk + kh) * tileDC(Dk), tKt, Dk * 128);
-    if (bwd) cta_copy16(p.Qtsw + ((size_t)c * p.Hk + kh) * tileDC(Dk), tQt, Dk * 128);
   }
   __syncthreads();
 
@@ -281,28 +276,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
     __syncthreads();
     // 4. T = (I + A)^-1 for the nh heads at once
     tri_inverse(Tm, nh, Mt);
-    // 5. per head: W^T = K^T (T diag(w))^T, U^T = V^T (T diag(b))^T, P
+    // 5. per head: W = T diag(w) K, U^T = V^T (T diag(b))^T, P
     for (int hh = 0; hh < nh; ++hh) {
       const int h = kh * p.r + g0 + hh;
       const size_t ch = (size_t)c * p.Hv + h;
       const float* T = Tm + hh * C * C;
-      if (tid == 0) {  // this head's V rows, landing while the T tiles are staged
+      if (tid == 0) {
+        // the previous head's tile stores have read their sources
+        tc::bulk_wait_read<0>();
+        // this head's V rows, landing while the T tiles are staged
         tc::mbar_arrive_expect_tx(&bar[1], (uint32_t)nbv * 8192u);
         for (int b = 0; b < nbv; ++b)
           tc::tma_load_2d(sV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bar[1]);
       }
+      __syncthreads();
       const float* w = wv + hh * C;
       const float* bb = bv + hh * C;
       const float* G = gv + hh * C;
-      stage_tile(tTW, C, C, [&](int r, int s) { return T[r * C + s] * w[s]; });
-      stage_tile(tTB, C, C, [&](int r, int s) { return T[r * C + s] * bb[s]; });
-      stage_tile(tOP, C, C, [&](int r, int s) {
-        return s <= r ? expf(G[r] - G[s]) * QK[r * C + s] : 0.f;
-      });
-      if (bwd)
-        stage_tile(tOPt, C, C, [&](int s, int r) {
-          return s <= r ? expf(G[r] - G[s]) * QK[r * C + s] : 0.f;
-        });
+      // T diag(w), T diag(b), P and (backward) T: one pass over 8-column pieces
+      for (int idx = tid; idx < C * (C / 8); idx += kThreads) {
+        const int r = idx % C, s8 = (idx / C) * 8;
+        const float4 ta = *(const float4*)(T + r * C + s8);
+        const float4 tb = *(const float4*)(T + r * C + s8 + 4);
+        const float4 qa = *(const float4*)(QK + r * C + s8);
+        const float4 qb = *(const float4*)(QK + r * C + s8 + 4);
+        const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
+        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        __align__(16) __nv_bfloat162 pw[4], pb[4], pp[4], pt[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int s = s8 + 2 * u;
+          pw[u] = __floats2bfloat162_rn(tv[2 * u] * w[s], tv[2 * u + 1] * w[s + 1]);
+          pb[u] = __floats2bfloat162_rn(tv[2 * u] * bb[s], tv[2 * u + 1] * bb[s + 1]);
+          pp[u] = __floats2bfloat162_rn(s <= r ? expf(G[r] - G[s]) * qv[2 * u] : 0.f,
+                                        s + 1 <= r ? expf(G[r] - G[s + 1]) * qv[2 * u + 1] : 0.f);
+          pt[u] = __floats2bfloat162_rn(tv[2 * u], tv[2 * u + 1]);
+        }
+        const uint32_t off = tc::sw128_offset(r, s8, C);
+        *(uint4*)(tTW + off) = *(const uint4*)pw;
+        *(uint4*)(tTB + off) = *(const uint4*)pb;
+        *(uint4*)(tP + off) = *(const uint4*)pp;
+        if (bwd) *(uint4*)(tT + off) = *(const uint4*)pt;
+      }
       {
         const bool lok = tc::mbar_wait(&bar[1], lphase);
         lphase ^= 1u;
@@ -312,68 +327,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
           goto done;
         }
       }
-      // V^T (rows v, columns s) from the natural V tile; rows past the chunk are zero
-      for (int idx = tid; idx < Dv * (C / 8); idx += kThreads) {
-        const int vv = idx % Dv, s8 = (idx / Dv) * 8;
-        __align__(16) __nv_bfloat16 e[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          e[q] = s8 + q < len ? *(const __nv_bfloat16*)(sV + tc::sw128_offset(s8 + q, vv, C))
-                              : __float2bfloat16(0.f);
-        *(uint4*)(tVt + tc::sw128_offset(vv, s8, MV)) = *(const uint4*)e;
-      }
+      // rows of the V tile past the chunk (another sequence's tokens) read as zero
+      if (len < C)
+        for (int idx = tid; idx < nbv * (C - len) * 8; idx += kThreads) {
+          const int b2 = idx / ((C - len) * 8), rem = idx % ((C - len) * 8);
+          ((uint4*)(sV + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
+        }
       tc::fence_async_smem();
       ok = mma_run([&] {
-        tc::mma_tile(tmem + 64, tc::smem_u32(tKt), MK, tc::smem_u32(tTW), C, C, 0u);
-        tc::mma_tile(tmem + 128, tc::smem_u32(tVt), MV, tc::smem_u32(tTB), C, C, 0u);
+        // W = (T diag(w)) K: B is K read MN-major from the rows of the [K; Q] tile
+        tc::mma_tile_x(tAccW, tc::smem_u32(tTW), false, 8192u, 64, tc::smem_u32(tAQK), true,
+                       aqk_pitch, NK, C, 0u);
+        // U^T = V^T (T diag(b))^T: A is V^T read MN-major from the natural V tile
+        tc::mma_tile_x(tAccU, tc::smem_u32(sV), true, 8192u, MV, tc::smem_u32(tTB), false,
+                       8192u, C, C, 0u);
       }, &bar[0], phase, p.status, c);
       if (!ok) goto done;
-      acc_walk(tmem + 64, MK, 64, Dk, [&](int k, int col0, const float* v) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) tile_put(tOW, C, col0 + j, k, v[j]);
-        if (bwd) tile_put16(tOWt, Dk, k, col0, v);
+      acc_walk(tAccW, 64, Dk, C, [&](int s, int col0, const float* v) {
+        tile_put16(tW, C, s, col0, v);
       });
-      acc_walk(tmem + 128, MV, 64, Dv, [&](int vv, int col0, const float* v) {
+      acc_walk(tAccU, MV, 64, Dv, [&](int vv, int col0, const float* v) {
         // U^T as a [Dv][C] SW128 tile, so that row reads by the state walks are conflict-free
         tile_put16((uint8_t*)(p.Utb + ch * Dv * C), Dv, vv, col0, v);
       });
-      if (bwd) {
-        // T, T^T and diag(b e^G) T^T as bf16 tiles, written straight to the workspace
-        uint8_t* tb = p.Tb + ch * 3 * 8192;
-        for (int idx = tid; idx < 3 * C * (C / 8); idx += kThreads) {
-          const int which = idx / (C * (C / 8)), rem = idx % (C * (C / 8));
-          const int row = rem % C, c8 = (rem / C) * 8;
-          __align__(16) __nv_bfloat162 pk[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float a, b2;
-            if (which == 0) {
-              a = T[row * C + c8 + 2 * u];
-              b2 = T[row * C + c8 + 2 * u + 1];
-            } else {
-              a = T[(c8 + 2 * u) * C + row];
-              b2 = T[(c8 + 2 * u + 1) * C + row];
-              if (which == 2) {
-                a *= w[row];
-                b2 *= w[row];
-              }
-            }
-            pk[u] = __floats2bfloat162_rn(a, b2);
-          }
-          *(uint4*)(tb + which * 8192 + tc::sw128_offset(row, c8, C)) = *(const uint4*)pk;
+      tc::fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc::bulk_s2g(p.Wsw + ch * bKC, tW, bKC);
+        tc::bulk_s2g(p.Psw + ch * 8192, tP, 8192);
+        if (bwd) {
+          tc::bulk_s2g(p.Tb + ch * 16384, tT, 8192);
+          tc::bulk_s2g(p.Tb + ch * 16384 + 8192, tTW, 8192);
         }
+        tc::bulk_commit();
       }
-      __syncthreads();
-      cta_copy16(p.Wsw + ch * tileCD(Dk), tOW, (uint32_t)tileCD(Dk));
-      cta_copy16(p.Psw + ch * tileCD(64), tOP, 8192);
-      if (bwd) {
-        cta_copy16(p.Wtsw + ch * tileDC(Dk), tOWt, Dk * 128);
-        cta_copy16(p.Ptsw + ch * 8192, tOPt, 8192);
-      }
-      __syncthreads();
     }
   }
 done:
+  if (tid == 0) tc::bulk_wait<0>();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -395,12 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   constexpr int NKC = (DK + 31) / 32;          // 16-column pieces of S^T per thread
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
-  const uint32_t bW = (uint32_t)tileCD(DK), bKt = (uint32_t)tileDC(DK), bP = 8192;
+  constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read K MN-major
+  const uint32_t bW = (uint32_t)tileCD(DK), bP = 8192;
   const uint32_t bU = (uint32_t)Dv * C * 2, bG = C * 4;
   const uint32_t bSt = tc::sw128_bytes(MV, DK);       // one saved S^T tile
   uint8_t* tSt = sm;                                  // [MV][DK]
   uint8_t* buf0 = tSt + tc::sw128_bytes(MV, DK);
-  const uint32_t bufsz = bW * 2 + bKt + bP + ((bU + bG + 1023) & ~1023u);
+  const uint32_t bufsz = bW * 3 + bP + ((bU + bG + 1023) & ~1023u);
   uint8_t* tDt = buf0 + 2 * bufsz;                    // [MV][C] Delta^T
   uint8_t* tDct = tDt + MV * 128;                     // [MV][C] Delta^T diag(c)
   float* ev = (float*)(tDct + MV * 128);              // [C]
@@ -409,10 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   uint32_t* tslot = (uint32_t*)(bars + 3);
   auto tW = [&](int b) { return buf0 + b * bufsz; };
   auto tQ = [&](int b) { return buf0 + b * bufsz + bW; };
-  auto tKt = [&](int b) { return buf0 + b * bufsz + 2 * bW; };
-  auto tP = [&](int b) { return buf0 + b * bufsz + 2 * bW + bKt; };
-  auto sU = [&](int b) { return (const __nv_bfloat16*)(buf0 + b * bufsz + 2 * bW + bKt + bP); };
-  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + 2 * bW + bKt + bP + bU); };
+  auto tK = [&](int b) { return buf0 + b * bufsz + 2 * bW; };
+  auto tP = [&](int b) { return buf0 + b * bufsz + 3 * bW; };
+  auto sU = [&](int b) { return (const __nv_bfloat16*)(buf0 + b * bufsz + 3 * bW + bP); };
+  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + 3 * bW + bP + bU); };
 
   for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) / 16); i += kThreads)
     ((uint4*)tSt)[i] = make_uint4(0, 0, 0, 0);
@@ -454,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
     const size_t chh = (size_t)cc * p.Hv + h, ckk = (size_t)cc * p.Hk + kh;
-    tc::mbar_arrive_expect_tx(lb, 2 * bW + bKt + bP + bU + bG);
+    tc::mbar_arrive_expect_tx(lb, 3 * bW + bP + bU + bG);
     tc::bulk_g2s(tW(b), p.Wsw + chh * bW, bW, lb);
     tc::bulk_g2s(tQ(b), p.Qsw + ckk * bW, bW, lb);
-    tc::bulk_g2s(tKt(b), p.Ktsw + ckk * bKt, bKt, lb);
+    tc::bulk_g2s(tK(b), p.Ksw + ckk * bW, bW, lb);
     tc::bulk_g2s(tP(b), p.Psw + chh * bP, bP, lb);
     tc::bulk_g2s((void*)sU(b), p.Utb + chh * Dv * C, bU, lb);
     tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
@@ -524,7 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     ok = mma_run([&] {
       tc::bulk_wait_read<0>();   // the saved-state store has read S^T: the update may rewrite it
       tc::mma_tile(tX, tc::smem_u32(tDt), MV, tc::smem_u32(tP(b)), C, C, 0u);
-      tc::mma_tile(tS, tc::smem_u32(tDct), MV, tc::smem_u32(tKt(b)), DK, C, 0u);
+      // K^T read MN-major from the natural K tile
+      tc::mma_tile_x(tS, tc::smem_u32(tDct), false, (uint32_t)MV * 128u, MV, tc::smem_u32(tK(b)),
+                     true, 8192u, NKF, C, 0u);
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // O = scale (e^G Q S + P Delta): column r of O^T is token t0 + r.  Staged as
@@ -584,9 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
 
 // ---------------------------------------------------------------------------
 static size_t prep_tc_smem(const Params& p) {
-  const int Dk = p.Dk, Dv = p.Dv, MK = Dk < 64 ? 64 : Dk, MV = Dv < 64 ? 64 : Dv;
-  size_t b = tc::sw128_bytes(128, Dk) + (size_t)MK * 128 + (size_t)MV * 128 + 8192 * 2 +
-             tc::sw128_bytes(64, Dk) + (size_t)Dk * 128 + 8192 * 2;
+  const int Dk = p.Dk, Dv = p.Dv;
+  size_t b = (size_t)((Dk + 63) / 64) * 128 * 128 + (size_t)((Dv + 63) / 64) * 8192 + 4 * 8192 +
+             tc::sw128_bytes(64, Dk);
   b += sizeof(float) * ((size_t)2 * C * C + (size_t)RB * C * C + RB * 3 * 256 + 3 * RB * C);
   return b + 64 + 1024;
 }
@@ -594,9 +588,9 @@ static size_t prep_tc_smem(const Params& p) {
 template <int DK>
 static size_t fwd_state_tc_smem(const Params& p) {
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
-  const size_t bW = tc::sw128_bytes(64, DK), bKt = (size_t)DK * 128, bP = 8192;
+  const size_t bW = tc::sw128_bytes(64, DK), bP = 8192;
   const size_t bU = (size_t)Dv * C * 2, bG = C * 4;
-  const size_t bufsz = bW * 2 + bKt + bP + ((bU + bG + 1023) & ~(size_t)1023);
+  const size_t bufsz = bW * 3 + bP + ((bU + bG + 1023) & ~(size_t)1023);
   return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 2 * C * 4 + 64 + 1024;
 }
 
