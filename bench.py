@@ -141,11 +141,10 @@ def kernel_models(wl: W.Workload):
                 T * Hv * Dv * es + NC * Hv * sST + fst_st)          # ... o, saved S^T tiles
     fst_tc_f = NC * Hv * (6 * C * Dk * Dv + 2 * C * C * Dv)
     bst_tc_b = (NC * Hk * 2 * sKC + NC * Hv * (sCC + sKC + C * 4) + T * Hv * Dv * es +
-                NC * Hv * (sST + sVC + MV * 128) + bst_st)          # ... dS^T, -dDelta(^T)
+                NC * Hv * (sST + sVC) + bst_st)                     # ... dS^T, -dDelta
     bst_tc_f = NC * Hv * (2 * C * C * Dv + 6 * C * Dk * Dv)
     bgr_tc_b = (NC * Hk * (2 * sKC + C * C * 4 + 2 * C * 4) + T * Hk * 2 * Dk * es +
-                NC * Hv * (sST + 2 * C * 4 + sKC + sVt + sVC + sCC + sST + MV * 128 +
-                           2 * sCC + 8) +
+                NC * Hv * (sST + 2 * C * 4 + sKC + sVt + 2 * sVC + sCC + sST + 2 * sCC + 8) +
                 T * Hv * (2 * Dv * es + 4) + T * Hv * (Dv * es + 8))
     bgr_tc_f = NC * Hv * (2 * C * Dk * Dv + 2 * 128 * Dk * Dv + 2 * C * Dk * Dv +
                           4 * C * Dk * Dv + 2 * C * C * Dv + 2 * C * C * (Dv + Dk) +

@@ -127,7 +127,6 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
       p.Tb = (uint8_t*)(base + L.Tb);
       p.dSb = (uint8_t*)(base + L.dSb);
       p.dDb = (uint8_t*)(base + L.dDb);
-      p.dDtb = (uint8_t*)(base + L.dDtb);
     }
   }
 }

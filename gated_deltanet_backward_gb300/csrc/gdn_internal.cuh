@@ -66,14 +66,12 @@ struct WsLayout {
   size_t KKf;     // [NC][Hk][C][C] fp32  K K^T (backward)
   size_t Tb;      // [NC][Hv] 2 x [C][C]: T, T diag(b e^G) (backward)
   size_t dSb;     // [NC][Hv] [MV][Dk] dS^T: state adjoint at each chunk end (backward)
-  size_t dDb;     // [NC][Hv] [C][MV]  -d Delta (backward)
-  size_t dDtb;    // [NC][Hv] [MV][C]  -d Delta^T (backward); MV = max(Dv, 64)
+  size_t dDb;     // [NC][Hv] [C][MV]  -d Delta (backward); MV = max(Dv, 64)
   size_t total;
 };
 
 // Bytes of the bf16 SW128 operand tiles (C = 64 rows or columns).
 inline size_t tile_CxD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
-inline size_t tile_DxC(int D) { return (size_t)D * 128; }
 inline size_t tile_DxD(int R, int D) { return (size_t)((D + 63) / 64) * R * 128; }
 // Bytes of one bf16 state tile: S^T (or dS^T) with max(Dv, 64) rows and Dk columns.
 inline size_t state_tile_bytes(int Dk, int Dv) { return tile_DxD(Dv < 64 ? 64 : Dv, Dk); }
@@ -122,7 +120,6 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
       L.Tb = take(NC * Hv * 2 * tile_CxD(64));
       L.dSb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
       L.dDb = take(NC * Hv * tile_CxD(s.Dv));
-      L.dDtb = take(NC * Hv * tile_DxC(s.Dv < 64 ? 64 : s.Dv));
     }
   }
   L.total = off;
@@ -192,7 +189,6 @@ struct Params {
   uint8_t* Tb;
   uint8_t* dSb;
   uint8_t* dDb;
-  uint8_t* dDtb;
 };
 
 // Kernel ids reported to the profiling hook (gdn_profile_begin).

@@ -210,4 +210,27 @@ __device__ __forceinline__ bool mma_run(F issue, uint64_t* bar, uint32_t& phase,
   return bad == 0;
 }
 
+// mma_run in two halves, for work that overlaps the tensor core: mma_issue
+// (all threads: barrier, then thread 0 issues and commits onto `bar`) and
+// mma_wait (all threads: bounded wait, then a barrier that agrees on the outcome).
+template <class F>
+__device__ __forceinline__ void mma_issue(F issue, uint64_t* bar) {
+  tc::fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tc::fence_after_sync();
+    issue();
+    tc::mma_commit(bar);
+  }
+}
+__device__ __forceinline__ bool mma_wait(uint64_t* bar, uint32_t& phase, DeviceStatus* status,
+                                         int detail) {
+  const bool ok = tc::mbar_wait(bar, phase);
+  phase ^= 1u;
+  tc::fence_after_sync();
+  const int bad = __syncthreads_or(ok ? 0 : 1);
+  if (bad && threadIdx.x == 0) set_status(status, GDN_ERR_TIMEOUT, detail);
+  return bad == 0;
+}
+
 }  // namespace gdn

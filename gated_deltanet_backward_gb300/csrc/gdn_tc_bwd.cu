@@ -44,10 +44,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   const int nbv = (Dv + 63) / 64;
   const uint32_t bO = (uint32_t)nbv * 8192;                  // natural dO tile [C][Dv]
   const uint32_t bSt = tc::sw128_bytes(MV, DK);              // dS^T tile
-  const uint32_t bDt = (uint32_t)MV * 128, bD = tc::sw128_bytes(C, MV);
+  const uint32_t bD = tc::sw128_bytes(C, MV);
   uint8_t* tdSt = sm;                                        // [MV][DK] dS^T
-  uint8_t* tmDt = tdSt + bSt;                                // [MV][C] -dDelta^T
-  uint8_t* tmD = tmDt + bDt;                                 // [C][MV] -dDelta
+  uint8_t* tmD = tdSt + bSt;                                 // [C][MV] -dDelta (token rows)
   uint8_t* buf0 = tmD + bD;
   const uint32_t bufsz = bO + 3 * bK + bP + 1024;
   float* ev = (float*)(buf0 + 2 * bufsz);
@@ -63,7 +62,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   auto tW = [&](int b) { return buf0 + b * bufsz + bO + 2 * bK + bP; };
   auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + bO + 3 * bK + bP); };
 
-  for (int i = tid; i < (int)(bSt + bDt + bD) / 16; i += kThreads)
+  for (int i = tid; i < (int)(bSt + bD) / 16; i += kThreads)
     ((uint4*)tdSt)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     tc::mbar_init(&bars[0], 1);
@@ -72,14 +71,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
     tc::fence_mbar_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(tslot, 256);
+    tc::tmem_alloc(tslot, 512);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const uint32_t tA1 = tmem, tA2 = tmem + 64, tA3 = tmem + 128;
+  // TMEM: dS^T update (rows v) @0; in token rows (M = 64): P^T dO @128, K dS @256
+  const uint32_t tA3 = tmem, tA1 = tmem + 128, tA2 = tmem + 256;
   uint32_t mphase = 0, lph[2] = {0, 0};
   const int vrow = acc_row(MV);
   const bool vok = vrow >= 0 && vrow < Dv;
@@ -164,43 +164,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::bulk_wait_read<1>();   // last chunk's dDelta stores have read their tiles
-      // dO^T as an MN-major operand straight from the natural tile (boxes 8 KB apart)
-      // (P^T dO)^T = dO^T P: both operands MN-major (P^T from the natural P tile)
-      tc::mma_tile_x(tA1, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tP(b)), true,
-                     8192u, C, C, 0u);
-      tc::mma_tile(tA2, tc::smem_u32(tdSt), MV, tc::smem_u32(tK(b)), C, DK, 0u);
+      tc::bulk_wait_read<1>();   // last chunk's dDelta store has read its tile
+      // token rows s: P^T dO (both operands MN-major: P^T from the natural P tile, dO
+      // from the natural dO boxes, 8 KB apart) and K dS (B = the dS^T tile)
+      tc::mma_tile_x(tA1, tc::smem_u32(tP(b)), true, 8192u, 64, tc::smem_u32(sdO(b)), true,
+                     8192u, MV, C, 0u);
+      tc::mma_tile_p(tA2, tc::smem_u32(tK(b)), 8192u, 64, tc::smem_u32(tdSt), (uint32_t)MV * 128u,
+                     Dv, DK, 0u);
+      // rows v: dO^T (scale e^G Q), dO^T read MN-major
       tc::mma_tile_x(tA3, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tQ(b)), true,
                      8192u, NKF, C, 0u);
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
-    // dDelta^T = scale (P^T dO)^T + c (K dS)^T
-    // -dDelta^T (the A operand below) and -dDelta in shared memory; both go to the
-    // gradient kernel by bulk stores
+    // dDelta = scale P^T dO + diag(c) K dS, stored negated in token rows (the A
+    // operand of the update below, read MN-major, and the gradient kernel's tile)
+    {
+      const int s = acc_row(64);
+      for (int q = half; q * 16 < Dv; q += 2) {
+        float a1[16], a2[16];
+        tc::tmem_ld16(tA1 + lane_quarter() + q * 16, a1);
+        tc::tmem_ld16(tA2 + lane_quarter() + q * 16, a2);
+        tc::tmem_ld_wait();
+        if (s >= 0) {
+          float md[16];
+          if (s < len) {
+            const float cs = cv[s];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int col0 = half * 16 + 32 * q;
-      float a1[16], a2[16];
-      tc::tmem_ld16(tA1 + lane_quarter() + col0, a1);
-      tc::tmem_ld16(tA2 + lane_quarter() + col0, a2);
-      tc::tmem_ld_wait();
-      if (vok) {
-        float md[16];
+            for (int j = 0; j < 16; ++j) md[j] = -fmaf(p.scale, a1[j], cs * a2[j]);
+          } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int s = col0 + j;
-          md[j] = s < len ? -(p.scale * a1[j] + cv[s] * a2[j]) : 0.f;
-          tile_put(tmD, C, s, vrow, md[j]);
+            for (int j = 0; j < 16; ++j) md[j] = 0.f;
+          }
+          tile_put16(tmD, C, s, q * 16, md);
         }
-        tile_put16(tmDt, MV, vrow, col0, md);
       }
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::bulk_wait_read<0>();   // the dS^T store has read its tile: the update may rewrite it
-      tc::mma_tile_x(tA3, tc::smem_u32(tmDt), false, (uint32_t)MV * 128u, MV,
-                     tc::smem_u32(tW(b)), true, 8192u, NKF, C, 1u);
-      tc::bulk_s2g(p.dDtb + ch * bDt, tmDt, bDt);
+      tc::mma_tile_x(tA3, tc::smem_u32(tmD), true, 8192u, MV, tc::smem_u32(tW(b)), true, 8192u,
+                     NKF, C, 1u);
       tc::bulk_s2g(p.dDb + ch * bD, tmD, bD);
       tc::bulk_commit();
     }, &bars[0], mphase, p.status, c);
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   uint8_t* sU = R3 + 32768;                        // [Dv][C] SW128 tile of U^T
   uint8_t* tdS = R3;                               // [MV][Dk] dS^T (read MN-major as dS)
   uint8_t* tP = R3 + 32768;                        // [C][C]
-  uint8_t* tdDt = R3;                              // [MV][C] -dDelta^T
+  uint8_t* tdDt = R3;                              // [C][MV] -dDelta (read MN-major)
   uint8_t* tT = R3 + 16384;                        // [C][C] T
   uint8_t* tTW = R3 + 24576;                       // [C][C] T diag(b e^G)
   uint8_t* tY = R3 + 40960;
@@ -539,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
     // phase C's tiles land in the dS^T space (free now) while epilogue B runs
     if (tid == 0) {
       const uint8_t* tb = p.Tb + ch * 2 * sCC;
-      tc::mbar_arrive_expect_tx(&bars[1], sVC + 2 * sCC);
-      tc::bulk_g2s(tdDt, p.dDtb + ch * sVC, sVC, &bars[1]);
+      tc::mbar_arrive_expect_tx(&bars[1], sCV + 2 * sCC);
+      tc::bulk_g2s(tdDt, p.dDb + ch * sCV, sCV, &bars[1]);
       tc::bulk_g2s(tT, tb, sCC, &bars[1]);
       tc::bulk_g2s(tTW, tb + sCC, sCC, &bars[1]);
     }
@@ -627,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
                      C, 1u);                                                               // dQ += dPE K
       tc::mma_tile_x(tdK, tc::smem_u32(tdPE), true, sCC, 64, tc::smem_u32(tQ), true, 8192u, NK,
                      C, 1u);                                                               // dK += dPE^T Q
-      tc::mma_tile_x(tmp, T_, true, sCC, 64, tc::smem_u32(tdDt), false, sVC, Dv, C, 0u);  // -dBv = T^T (-dD)
+      tc::mma_tile_x(tmp, T_, true, sCC, 64, tc::smem_u32(tdDt), true, 8192u, MV, C, 0u); // -dBv = T^T (-dD)
       tc::mma_tile_x(tmp + 128, T_, true, sCC, 64, tc::smem_u32(tdT), true, sCC, C, C, 0u); // Y = T^T dT
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
@@ -858,7 +861,8 @@ static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, c
   const size_t bK = tc::sw128_bytes(64, DK);
   const size_t bO = (size_t)((Dv + 63) / 64) * 8192;
   const size_t bufsz = bO + 3 * bK + 8192 + 1024;
-  const size_t smem = tc::sw128_bytes(MV, DK) + 2 * (size_t)MV * 128 + 2 * bufsz + 2 * C * 4 + 64 + 1024;
+  const size_t smem = tc::sw128_bytes(MV, DK) + tc::sw128_bytes(64, MV) + 2 * bufsz + 2 * C * 4 + 64 +
+                      1024;
   cudaFuncSetAttribute(k_bwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_BWD_STATE_TC);
   k_bwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kThreads, smem, st>>>(p, maps);

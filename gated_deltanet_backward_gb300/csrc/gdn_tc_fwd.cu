@@ -27,60 +27,109 @@ constexpr int RB = 3;  // value heads prepared together (triangular solves in pa
 
 __device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
 
-// In-place inverse of (I + A) for nh strictly-lower 64x64 fp32 matrices A
-// (Tm[hh] holds A on entry, T = (I + A)^-1 on exit).  Diagonal 16x16 blocks by
-// forward substitution, then block rows 1..3: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
-__device__ void tri_inverse(float* Tm, int nh, float* Mt) {
+constexpr int TS = C + 4;   // row stride (floats) of the fp32 [C][C] matrices of the inverse
+
+// In-place inverse T = (I + A)^-1 for nh strictly lower-triangular 64x64 fp32
+// matrices A (rows TS floats apart; everything on and above the diagonal zero on
+// entry), by 2x2 block inversion at two levels:
+//   16x16 diagonal blocks D_b = (I + A_bb)^-1   (forward substitution, a column per thread)
+//   32x32 diagonal blocks: lower-left 16x16 = -D_1 A_10 D_0
+//   64x64: lower-left 32x32 = -T_B A_BA T_A (T_A, T_B the 32x32 diagonal inverses)
+// Each product runs as 1 x 4 register tiles (one row, four columns per thread)
+// and skips the zero triangles.  Scratch M: nh * 1024 floats.
+__device__ void tri_inverse(float* Tm, int nh, float* M) {
   const int tid = threadIdx.x;
-  // diagonal blocks: one warp per (head, block); lane j < 16 keeps column j of the
-  // block inverse in registers (forward substitution, no block-wide barriers)
+  // 16x16 diagonal blocks: 16 threads per (head, block), thread j solves column j
   {
-    const int warp = tid >> 5, lane = tid & 31, j = lane & 15;
-    for (int unit = warp; unit < nh * 4; unit += blockDim.x / 32) {
-      const int hh = unit >> 2, blk = unit & 3;
-      float* T = Tm + hh * C * C + blk * 16 * C + blk * 16;   // block origin
-      float col[16];
+    const int unit = tid >> 4, j = tid & 15;
+    const bool act = unit < nh * 4;
+    float* B = Tm + (act ? (unit >> 2) * C * TS + (unit & 3) * (16 * TS + 16) : 0);
+    float x[16];
+    if (act) {
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        float acc = 0.f;
+      for (int i = 0; i < 16; ++i) {
+        float a0 = (i == j) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < rr; ++s2) acc = fmaf(T[rr * C + s2], col[s2], acc);
-        col[rr] = rr == j ? 1.f : (rr > j ? -acc : 0.f);
+        for (int k = 0; k + 1 < i; k += 2) {
+          a0 = fmaf(-B[i * TS + k], x[k], a0);
+          a1 = fmaf(-B[i * TS + k + 1], x[k + 1], a1);
+        }
+        if (i & 1) a0 = fmaf(-B[i * TS + i - 1], x[i - 1], a0);
+        x[i] = a0 + a1;
       }
-      __syncwarp();
-      if (lane < 16)
+    }
+    __syncthreads();
+    if (act)
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) T[rr * C + j] = col[rr];
-      __syncwarp();
-    }
+      for (int i = 0; i < 16; ++i) B[i * TS + j] = x[i];
     __syncthreads();
   }
-  // block rows
-  for (int bi = 1; bi < 4; ++bi) {
-    const int n_el = nh * bi * 256;
-    for (int idx = tid; idx < n_el; idx += blockDim.x) {
-      const int hh = idx / (bi * 256), rem = idx % (bi * 256), bj = rem / 256, e = rem % 256;
-      const int rr = e / 16, cc = e % 16;
-      const float* T = Tm + hh * C * C;
-      float acc = 0.f;
-      for (int kb = bj; kb < bi; ++kb)
-        for (int s = 0; s < 16; ++s)
-          acc = fmaf(T[(bi * 16 + rr) * C + kb * 16 + s], T[(kb * 16 + s) * C + bj * 16 + cc], acc);
-      Mt[(hh * 3 + bj) * 256 + e] = acc;
+  // 32x32 diagonal blocks (two per head): M = A_10 D_0, then L = -D_1 M
+  const int n1 = nh * 2 * 16 * 4;
+  for (int it = tid; it < n1; it += blockDim.x) {
+    const int pr = it >> 6, r = (it >> 2) & 15, c0 = (it & 3) * 4;
+    const float* T = Tm + (pr >> 1) * C * TS;
+    const int rb = ((pr & 1) * 2 + 1) * 16, cb = rb - 16;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = c0; k < 16; ++k) {   // D_0 is lower triangular
+      const float a = T[(rb + r) * TS + cb + k];
+      const float4 d = *(const float4*)(T + (cb + k) * TS + cb + c0);
+      acc.x = fmaf(a, d.x, acc.x);
+      acc.y = fmaf(a, d.y, acc.y);
+      acc.z = fmaf(a, d.z, acc.z);
+      acc.w = fmaf(a, d.w, acc.w);
     }
-    __syncthreads();
-    // T_ij = -T_ii M_ij, written over A_ij (no longer read: block row bi's M are done)
-    for (int idx = tid; idx < n_el; idx += blockDim.x) {
-      const int hh = idx / (bi * 256), rem = idx % (bi * 256), bj = rem / 256, e = rem % 256;
-      const int rr = e / 16, cc = e % 16;
-      float* T = Tm + hh * C * C;
-      float acc = 0.f;
-      for (int s = 0; s <= rr; ++s)
-        acc = fmaf(T[(bi * 16 + rr) * C + bi * 16 + s], Mt[(hh * 3 + bj) * 256 + s * 16 + cc], acc);
-      T[(bi * 16 + rr) * C + bj * 16 + cc] = -acc;
-    }
-    __syncthreads();
+    *(float4*)(M + pr * 256 + r * 16 + c0) = acc;
   }
+  __syncthreads();
+  for (int it = tid; it < n1; it += blockDim.x) {
+    const int pr = it >> 6, r = (it >> 2) & 15, c0 = (it & 3) * 4;
+    float* T = Tm + (pr >> 1) * C * TS;
+    const int rb = ((pr & 1) * 2 + 1) * 16, cb = rb - 16;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k <= r; ++k) {    // D_1 is lower triangular
+      const float d = T[(rb + r) * TS + rb + k];
+      const float4 m = *(const float4*)(M + pr * 256 + k * 16 + c0);
+      acc.x = fmaf(d, m.x, acc.x);
+      acc.y = fmaf(d, m.y, acc.y);
+      acc.z = fmaf(d, m.z, acc.z);
+      acc.w = fmaf(d, m.w, acc.w);
+    }
+    *(float4*)(T + (rb + r) * TS + cb + c0) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+  // 64x64: M = A_BA T_A, then lower-left = -T_B M
+  const int n2 = nh * 32 * 8;
+  for (int it = tid; it < n2; it += blockDim.x) {
+    const int hh = it >> 8, r = (it >> 3) & 31, c0 = (it & 7) * 4;
+    const float* T = Tm + hh * C * TS;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = c0; k < 32; ++k) {   // T_A is lower triangular
+      const float a = T[(32 + r) * TS + k];
+      const float4 t = *(const float4*)(T + k * TS + c0);
+      acc.x = fmaf(a, t.x, acc.x);
+      acc.y = fmaf(a, t.y, acc.y);
+      acc.z = fmaf(a, t.z, acc.z);
+      acc.w = fmaf(a, t.w, acc.w);
+    }
+    *(float4*)(M + hh * 1024 + r * 32 + c0) = acc;
+  }
+  __syncthreads();
+  for (int it = tid; it < n2; it += blockDim.x) {
+    const int hh = it >> 8, r = (it >> 3) & 31, c0 = (it & 7) * 4;
+    float* T = Tm + hh * C * TS;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k <= r; ++k) {    // T_B is lower triangular
+      const float t = T[(32 + r) * TS + 32 + k];
+      const float4 m = *(const float4*)(M + hh * 1024 + k * 32 + c0);
+      acc.x = fmaf(t, m.x, acc.x);
+      acc.y = fmaf(t, m.y, acc.y);
+      acc.z = fmaf(t, m.z, acc.z);
+      acc.w = fmaf(t, m.w, acc.w);
+    }
+    *(float4*)(T + (32 + r) * TS + c0) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
 }
 
 }  // namespace
@@ -115,9 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
   uint8_t* tW = tT + 8192;                              // [C][Dk] W
   float* KK = (float*)(tW + bKC);                       // [C][C]
   float* QK = KK + C * C;                               // [C][C]
-  float* Tm = QK + C * C;                               // [RB][C][C]
-  float* Mt = Tm + RB * C * C;                          // [RB][3][256]
-  float* gv = Mt + RB * 3 * 256;                        // [RB][C]
+  float* Tm = QK + C * C;                               // [RB][C][TS]
+  float* Mt = Tm + RB * C * TS;                         // [RB][1024] scratch of the inverse
+  float* gv = Mt + RB * 1024;                           // [RB][C]
   float* bv = gv + RB * C;                              // [RB][C]
   float* wv = bv + RB * C;                              // [RB][C]
   uint64_t* bar = (uint64_t*)(wv + RB * C);   // [0] MMA completion, [1] TMA loads
@@ -182,9 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
       if (idx < total) {
         const bool isq = row >= C;
         const int t = row & (C - 1);
-        const float nrm = sqrtf(ss + 1e-6f);
+        const float nrm = sqrtf(ss + 1e-6f), inv = t < len ? 1.f / nrm : 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = t < len ? x[q] / nrm : 0.f;
+        for (int q = 0; q < 8; ++q) x[q] *= inv;
         __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) pk[q] = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
@@ -271,7 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
     }
     for (int idx = tid; idx < nh * C * C; idx += kThreads) {
       const int hh = idx / (C * C), e = idx % (C * C), r = e / C, s = e % C;
-      Tm[idx] = s < r ? bv[hh * C + r] * expf(gv[hh * C + r] - gv[hh * C + s]) * KK[e] : 0.f;
+      float a = 0.f;
+      if (s < r) a = bv[hh * C + r] * expf(gv[hh * C + r] - gv[hh * C + s]) * KK[e];
+      Tm[hh * C * TS + r * TS + s] = a;
     }
     __syncthreads();
     // 4. T = (I + A)^-1 for the nh heads at once
@@ -280,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
     for (int hh = 0; hh < nh; ++hh) {
       const int h = kh * p.r + g0 + hh;
       const size_t ch = (size_t)c * p.Hv + h;
-      const float* T = Tm + hh * C * C;
+      const float* T = Tm + hh * C * TS;
       if (tid == 0) {
         // the previous head's tile stores have read their sources
         tc::bulk_wait_read<0>();
@@ -296,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
       // T diag(w), T diag(b), P and (backward) T: one pass over 8-column pieces
       for (int idx = tid; idx < C * (C / 8); idx += kThreads) {
         const int r = idx % C, s8 = (idx / C) * 8;
-        const float4 ta = *(const float4*)(T + r * C + s8);
-        const float4 tb = *(const float4*)(T + r * C + s8 + 4);
+        const float4 ta = *(const float4*)(T + r * TS + s8);
+        const float4 tb = *(const float4*)(T + r * TS + s8 + 4);
         const float4 qa = *(const float4*)(QK + r * C + s8);
         const float4 qb = *(const float4*)(QK + r * C + s8 + 4);
         const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
@@ -384,20 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     return;
   }
   constexpr int NKC = (DK + 31) / 32;          // 16-column pieces of S^T per thread
+  constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read K MN-major
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
-  constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read K MN-major
   const uint32_t bW = (uint32_t)tileCD(DK), bP = 8192;
   const uint32_t bU = (uint32_t)Dv * C * 2, bG = C * 4;
   const uint32_t bSt = tc::sw128_bytes(MV, DK);       // one saved S^T tile
   uint8_t* tSt = sm;                                  // [MV][DK]
   uint8_t* buf0 = tSt + tc::sw128_bytes(MV, DK);
   const uint32_t bufsz = bW * 3 + bP + ((bU + bG + 1023) & ~1023u);
-  uint8_t* tDt = buf0 + 2 * bufsz;                    // [MV][C] Delta^T
+  uint8_t* tDt = buf0 + 2 * bufsz;                    // [MV][C] Delta^T, then O rows
   uint8_t* tDct = tDt + MV * 128;                     // [MV][C] Delta^T diag(c)
-  float* ev = (float*)(tDct + MV * 128);              // [C]
-  float* cv = ev + C;                                 // [C]
-  uint64_t* bars = (uint64_t*)(cv + C);               // mma, load0, load1
+  float* evb = (float*)(tDct + MV * 128);             // [2][C] e^G, by chunk parity
+  float* cvb = evb + 2 * C;                           // [2][C] e^{G_last - G}
+  uint64_t* bars = (uint64_t*)(cvb + 2 * C);          // mma, load0, load1
   uint32_t* tslot = (uint32_t*)(bars + 3);
   auto tW = [&](int b) { return buf0 + b * bufsz; };
   auto tQ = [&](int b) { return buf0 + b * bufsz + bW; };
@@ -416,15 +467,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     tc::fence_mbar_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(tslot, 256);
+    tc::tmem_alloc(tslot, 512);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  // TMEM: X = S^T W^T @0, state update @64, and the output in token rows (M = 64):
+  // Q S @256, P Delta @384 (they survive into the next chunk's first product)
   const uint32_t tmem = *tslot;
-  const uint32_t tX = tmem, tO1 = tmem + 64, tS = tmem + 128;
-  uint32_t mphase = 0, lphase0 = 0, lphase1 = 0;
+  const uint32_t tX = tmem, tS = tmem + 64, tO1 = tmem + 256, tO2 = tmem + 384;
+  uint32_t mphase = 0, lph[2] = {0, 0};
   const int vrow = acc_row(MV);
   const bool vok = vrow >= 0 && vrow < Dv;
   const size_t SZ = (size_t)DK * Dv;
@@ -454,51 +507,58 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     tc::bulk_g2s((void*)sU(b), p.Utb + chh * Dv * C, bU, lb);
     tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
   };
-  if (tid == 0 && c1 > c0) issue_load(c0, 0);
-
-  bool ok = true;
-  for (int c = c0; c < c1 && ok; ++c) {
-    const int i = c - c0, b = i & 1;
-    const int64_t t0 = s0 + (int64_t)i * C;
-    const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
-    // tiles of this chunk
-    const bool lok = tc::mbar_wait(&bars[1 + b], b ? lphase1 : lphase0);
-    if (b) lphase1 ^= 1u; else lphase0 ^= 1u;
+  auto chunk_len = [&](int cc) {
+    const int64_t t = s0 + (int64_t)(cc - c0) * C;
+    return (int)((s1 - t) < C ? (s1 - t) : C);
+  };
+  // Brings chunk cc's tiles in (waits for them), fills its gate vectors, stores its
+  // chunk-start state and issues its first product X = S^T W^T.  Returns false on a
+  // timed-out wait.
+  auto start_chunk = [&](int cc) -> bool {
+    const int b = (cc - c0) & 1, len = chunk_len(cc);
+    const bool lok = tc::mbar_wait(&bars[1 + b], lph[b]);
+    lph[b] ^= 1u;
     if (__syncthreads_or(lok ? 0 : 1)) {
-      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
-      ok = false;
-      break;
-    }
-    if (tid == 0) {
-      // chunk-start state: the S^T tile goes to the saved states as it is, by one
-      // bulk store that runs behind this chunk's work
-      tc::bulk_s2g((uint8_t*)p.saved + ((size_t)c * p.Hv + h) * bSt, tSt, bSt);
-      tc::bulk_commit();
-      if (c + 1 < c1) {
-        tc::fence_async_smem();
-        issue_load(c + 1, b ^ 1);
-      }
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, cc);
+      return false;
     }
     const float* G = sG(b);
     if (tid < C) {
-      ev[tid] = expf(G[tid]);
-      cv[tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
+      evb[b * C + tid] = expf(G[tid]);
+      cvb[b * C + tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
     }
-    tc::fence_async_smem();
-    ok = mma_run([&] {
+    mma_issue([&] {
+      // the chunk-start state S^T goes to the saved states as it is, by one bulk store
+      tc::bulk_s2g((uint8_t*)p.saved + ((size_t)cc * p.Hv + h) * bSt, tSt, bSt);
+      tc::bulk_commit();
       tc::mma_tile(tX, tc::smem_u32(tSt), MV, tc::smem_u32(tW(b)), C, DK, 0u);
-      tc::mma_tile(tO1, tc::smem_u32(tSt), MV, tc::smem_u32(tQ(b)), C, DK, 0u);
-    }, &bars[0], mphase, p.status, c);
+    }, &bars[0]);
+    return true;
+  };
+
+  bool ok = true;
+  if (c1 > c0) {
+    if (tid == 0) {
+      issue_load(c0, 0);
+      if (c0 + 1 < c1) issue_load(c0 + 1, 1);
+    }
+    ok = start_chunk(c0);
+  }
+  for (int c = c0; c < c1 && ok; ++c) {
+    const int i = c - c0, b = i & 1;
+    const int64_t t0 = s0 + (int64_t)i * C;
+    const int len = chunk_len(c);
+    const float* ev = evb + b * C;
+    const float* cv = cvb + b * C;
+    ok = mma_wait(&bars[0], mphase, p.status, c);
     if (!ok) break;
-    // Delta^T = U^T - X^T; keep S^T Q^T for the output
-    float o1[2][16];
+    // Delta^T = U^T - X^T and Delta^T diag(c)
     const uint8_t* U = (const uint8_t*)sU(b);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int col0 = half * 16 + 32 * q;
       float x[16];
       tc::tmem_ld16(tX + lane_quarter() + col0, x);
-      tc::tmem_ld16(tO1 + lane_quarter() + col0, o1[q]);
       tc::tmem_ld_wait();
       if (vok) {
         float u[16], dc[16];
@@ -513,39 +573,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
       }
     }
     tc::fence_async_smem();
+    // state update first (the next chunk waits on it), then the output products
     ok = mma_run([&] {
       tc::bulk_wait_read<0>();   // the saved-state store has read S^T: the update may rewrite it
-      tc::mma_tile(tX, tc::smem_u32(tDt), MV, tc::smem_u32(tP(b)), C, C, 0u);
       // K^T read MN-major from the natural K tile
       tc::mma_tile_x(tS, tc::smem_u32(tDct), false, (uint32_t)MV * 128u, MV, tc::smem_u32(tK(b)),
                      true, 8192u, NKF, C, 0u);
+      // O in token rows: Q S (B = the S^T tile) and P Delta (B = the Delta^T tile)
+      tc::mma_tile_p(tO1, tc::smem_u32(tQ(b)), 8192u, 64, tc::smem_u32(tSt), (uint32_t)MV * 128u,
+                     Dv, DK, 0u);
+      tc::mma_tile(tO2, tc::smem_u32(tP(b)), 64, tc::smem_u32(tDt), Dv, C, 0u);
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
-    // O = scale (e^G Q S + P Delta): column r of O^T is token t0 + r.  Staged as
-    // [C][Dv] rows in the (now free) Delta^T tile, then stored row by row.
-    __nv_bfloat16* sO = (__nv_bfloat16*)tDt;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int col0 = half * 16 + 32 * q;
-      float x[16];
-      tc::tmem_ld16(tX + lane_quarter() + col0, x);
-      tc::tmem_ld_wait();
-      if (vok)
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          sO[(col0 + j) * Dv + vrow] = __float2bfloat16_rn(p.scale * (ev[col0 + j] * o1[q][j] + x[j]));
-    }
-    __syncthreads();
-    {
-      __nv_bfloat16* orow = (__nv_bfloat16*)p.o + t0 * p.o_ld + (int64_t)h * Dv;
-      const int cpr = Dv / 8;
-      for (int idx = tid; idx < len * cpr; idx += kThreads) {
-        const int r = idx / cpr, c8 = (idx % cpr) * 8;
-        *(uint4*)(orow + (int64_t)r * p.o_ld + c8) = *(const uint4*)(sO + r * Dv + c8);
-      }
-    }
+    // buffer b is free (no tile of chunk c is read from here on): chunk c + 2's tiles
+    if (tid == 0 && c + 2 < c1) issue_load(c + 2, b);
     // S^T <- e^{G_last} S^T + Delta^T diag(c) K
-    const float eC = expf(G[len - 1]);
+    const float eC = ev[len - 1];
 #pragma unroll
     for (int ii = 0; ii < NKC; ++ii) {
       const int col0 = half * 16 + 32 * ii;
@@ -561,6 +604,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
       }
     }
     tc::fence_async_smem();
+    // the next chunk's first product runs while this chunk's output is formed
+    if (c + 1 < c1 && !start_chunk(c + 1)) {
+      ok = false;
+      break;
+    }
+    // O = scale (e^G Q S + P Delta), token row r of the chunk per accumulator lane:
+    // each thread stores 16 consecutive values of its row
+    {
+      const int r = acc_row(64);
+      __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + (r < 0 ? 0 : r)) * p.o_ld + (int64_t)h * Dv;
+      for (int q = half; q * 16 < Dv; q += 2) {
+        float o1[16], o2[16];
+        tc::tmem_ld16(tO1 + lane_quarter() + q * 16, o1);
+        tc::tmem_ld16(tO2 + lane_quarter() + q * 16, o2);
+        tc::tmem_ld_wait();
+        if (r >= 0 && r < len) {
+          const float e = p.scale * ev[r];
+          __align__(16) __nv_bfloat162 pk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pk[j] = __floats2bfloat162_rn(fmaf(e, o1[2 * j], p.scale * o2[2 * j]),
+                                          fmaf(e, o1[2 * j + 1], p.scale * o2[2 * j + 1]));
+          uint4* dst = (uint4*)(orow + q * 16);
+          dst[0] = ((const uint4*)pk)[0];
+          dst[1] = ((const uint4*)pk)[1];
+        }
+      }
+    }
   }
   if (ok && p.S_T && vok)
 #pragma unroll
@@ -573,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -581,7 +652,7 @@ static size_t prep_tc_smem(const Params& p) {
   const int Dk = p.Dk, Dv = p.Dv;
   size_t b = (size_t)((Dk + 63) / 64) * 128 * 128 + (size_t)((Dv + 63) / 64) * 8192 + 4 * 8192 +
              tc::sw128_bytes(64, Dk);
-  b += sizeof(float) * ((size_t)2 * C * C + (size_t)RB * C * C + RB * 3 * 256 + 3 * RB * C);
+  b += sizeof(float) * ((size_t)2 * C * C + (size_t)RB * C * TS + RB * 1024 + 3 * RB * C);
   return b + 64 + 1024;
 }
 
@@ -591,7 +662,7 @@ static size_t fwd_state_tc_smem(const Params& p) {
   const size_t bW = tc::sw128_bytes(64, DK), bP = 8192;
   const size_t bU = (size_t)Dv * C * 2, bG = C * 4;
   const size_t bufsz = bW * 3 + bP + ((bU + bG + 1023) & ~(size_t)1023);
-  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 2 * C * 4 + 64 + 1024;
+  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 4 * C * 4 + 64 + 1024;
 }
 
 cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st) {
