@@ -165,6 +165,30 @@ def kernel_models(wl: W.Workload):
     }
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, one launch) of a kernel
+# from an ncu capture of this workload, with a hash of the sources it was built from;
+# a kernel whose sources changed since reports null (profiles/tc_kernels_l27b_bf16.md).
+NCU_TRAFFIC = {
+    ("gdn_bwd_grads_tc", "l27b_bf16"): (655.676416e6, "91b4d82f68e0ec3b"),
+}
+KERNEL_SOURCES = {
+    "gdn_bwd_grads_tc": ("gdn_tc_bwd.cu", "gdn_tc.cuh", "umma.cuh", "gdn_device.cuh",
+                         "gdn_internal.cuh"),
+}
+
+
+def measured_traffic(kernel, workload):
+    import hashlib
+    entry = NCU_TRAFFIC.get((kernel, workload))
+    if entry is None or kernel not in KERNEL_SOURCES:
+        return None
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "gated_deltanet_backward_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return entry[0] if h.hexdigest()[:16] == entry[1] else None
+
+
 def kernel_roofline(b, f, unit, avg_s, pk):
     """Roofline entry of one kernel: the roof (HBM bytes or FLOPs at the unit's peak)
     that bounds its algorithmic work, and the achieved rate against it."""
@@ -339,6 +363,7 @@ def run_ours(args):
     avg_s = sum(per[dom]) / len(per[dom]) * 1e-3
     roof = kernel_roofline(b, f, unit, avg_s, pk)
     roof["kernel"] = dom
+    roof["traffic"] = measured_traffic(dom, wl.name)
     for name in kernels:
         kb, kf, ku = models[name]
         r = kernel_roofline(kb, kf, ku, kernels[name]["avg_us"] * 1e-6, pk)
