@@ -96,6 +96,11 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
   const WsLayout L = gdn::ws_layout(*s, bwd);
   char* base = (char*)ws;
   p.status = (gdn::DeviceStatus*)(base + L.status);
+  // flag arrays are handed to the kernels only by the fused launchers
+  p.fwork = (uint32_t*)(base + L.fsync);
+  p.fready = nullptr;
+  p.bwork = (uint32_t*)(base + L.bsync);
+  p.bready = nullptr;
   p.nq = (float*)(base + L.nq);
   p.nk = (float*)(base + L.nk);
   p.G = (float*)(base + L.G);
@@ -226,6 +231,23 @@ bool encode_tma_2d(CUtensorMap* m, const void* base, int64_t cols, int64_t rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0, coop = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop)
+      cached[dev] = n;
+    else
+      cached[dev] = -1;
+  }
+  return cached[dev] > 0 ? cached[dev] : 0;
+}
+
 // Lets other translation units of the library explain a failure through
 // gdn_last_error().
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
@@ -281,6 +303,8 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_BWD_STATE_TC: return "gdn_bwd_state_tc";
     case gdn::KID_BWD_GRADS_TC: return "gdn_bwd_grads_tc";
     case gdn::KID_PREP_TC_FULL: return "gdn_prep_tc_full";
+    case gdn::KID_FWD_FUSED_TC: return "gdn_fwd_fused_tc";
+    case gdn::KID_BWD_FUSED_TC: return "gdn_bwd_fused_tc";
     default: return "?";
   }
 }
@@ -345,7 +369,9 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
   p.saved = (float*)saved_states;
   (void)cudaGetLastError();  // report only errors of this call's own launches
   g_last_error[0] = 0;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, st);
+  // status block and the fused forward's flags (they follow it)
+  const gdn::WsLayout L = gdn::ws_layout(*s, keep);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, L.bsync, st);
   if (e != cudaSuccess) return cuda_fail("gdn_forward: clearing the status word", e);
   if (s->n_seqs > 0 && s->total_chunks == 0) {
     // every sequence is empty: S_T = S_0
@@ -424,8 +450,13 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
   p.tag = shape_tag(s);
   (void)cudaGetLastError();  // report only errors of this call's own launches
   g_last_error[0] = 0;
-  // a reusing backward keeps the forward's tag (it sits after the status word)
-  cudaError_t e = cudaMemsetAsync(workspace, 0, p.reuse ? sizeof(int32_t) * 2 : 256, st);
+  // status block and the fused backward's flags; a reusing backward keeps the
+  // forward's tag (it sits after the status word) and clears the flags on their own
+  const gdn::WsLayout L = gdn::ws_layout(*s, true);
+  cudaError_t e = p.reuse ? cudaMemsetAsync(workspace, 0, sizeof(int32_t) * 2, st)
+                          : cudaMemsetAsync(workspace, 0, L.nq, st);
+  if (e == cudaSuccess && p.reuse)
+    e = cudaMemsetAsync((uint8_t*)workspace + L.bsync, 0, L.nq - L.bsync, st);
   if (e != cudaSuccess) return cuda_fail("gdn_backward: clearing the status word", e);
   if (s->total_chunks == 0 && s->n_seqs > 0 && dS0) {
     const size_t bytes = (size_t)s->n_seqs * s->Hv * s->Dk * s->Dv * sizeof(float);

@@ -224,7 +224,10 @@ cudaError_t launch_forward(const Params& p, const TmaMaps* maps, cudaStream_t st
   const bool bf16 = maps != nullptr;
   if (bf16) {
     // bf16 inputs: tensor-core chunk preparation and state walk
-    cudaError_t e = launch_prep_tc(p, *maps, p.keep != 0, st);
+    bool fused = false;
+    cudaError_t e = launch_fwd_fused_tc(p, *maps, st, &fused);
+    if (e != cudaSuccess || fused) return e;
+    e = launch_prep_tc(p, *maps, p.keep != 0, st);
     if (e != cudaSuccess) return e;
     return launch_fwd_state_tc(p, st);
   }

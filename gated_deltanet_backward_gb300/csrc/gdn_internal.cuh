@@ -40,6 +40,8 @@ struct DeviceStatus {
 // shared memory by the next.
 struct WsLayout {
   size_t status;  // DeviceStatus, 256 B
+  size_t fsync;   // forward fused launch: work counter + (chunk, key head) flags
+  size_t bsync;   // backward fused launch: work counter + (chunk, value head) flags
   size_t nq;      // [NC][Hk][C] query norms sqrt(|q|^2 + 1e-6)
   size_t nk;      // [NC][Hk][C] key norms
   size_t G;       // [NC][Hv][C] inclusive cumsum of log g
@@ -89,6 +91,11 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
     return at;
   };
   L.status = take(256);
+  // readiness flags of the fused launches, right after the status block so that one
+  // memset clears both: forward [256 B work counter | NC*Hk flags], backward
+  // [256 B work counter | NC*Hv flags]
+  L.fsync = take(256 + NC * Hk * 4);
+  L.bsync = take(256 + NC * Hv * 4);
   L.nq = take(NC * Hk * C * 4);
   L.nk = take(NC * Hk * C * 4);
   L.G = take(NC * Hv * C * 4);
@@ -162,6 +169,10 @@ struct Params {
   float* ddt_bias;
   float* dS0;
   DeviceStatus* status;
+  uint32_t* fwork;   // fused forward: next preparation unit
+  uint32_t* fready;  // fused forward: [NC][Hk] preparation unit done
+  uint32_t* bwork;   // fused backward: next gradient unit
+  uint32_t* bready;  // fused backward: [NC][Hv] state-walk chunk done
   uint32_t tag;  // shape tag (see shape_tag); written by a keeping forward, checked by a reusing backward
   int keep;      // forward: leave the backward's chunk operands in the workspace
   int reuse;     // backward: read them from the workspace instead of recomputing them
@@ -204,6 +215,8 @@ enum KernelId {
   KID_BWD_STATE_TC = 8,
   KID_BWD_GRADS_TC = 9,
   KID_PREP_TC_FULL = 10,
+  KID_FWD_FUSED_TC = 11,
+  KID_BWD_FUSED_TC = 12,
   KID_COUNT = 11
 };
 
@@ -225,6 +238,12 @@ bool encode_tma_2d(CUtensorMap* m, const void* base, int64_t cols, int64_t rows,
 
 // Tensor-core (bf16) launchers.
 cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st);
+// Fused launches need a producer CTA beside the walks on at least this many SMs.
+constexpr int kMinProducers = 8;
+// SMs of the current device (cached per device; 0 if the query fails).
+int sm_count();
+cudaError_t launch_fwd_fused_tc(const Params& p, const TmaMaps& maps, cudaStream_t st,
+                                bool* launched);
 cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st);
 cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st);
 

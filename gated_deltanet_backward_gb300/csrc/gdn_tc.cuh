@@ -13,6 +13,65 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
+// The first kCtlBytes of a tensor-core kernel's (1024-aligned) shared memory: its
+// mbarriers and the TMEM address, at the same place whatever role the CTA plays.
+constexpr uint32_t kCtlBytes = 1024;
+struct CtaCtl {
+  uint64_t bar[4];
+  uint32_t tmem;
+};
+// All threads: nbar mbarriers (arrival count 1) and ncols TMEM columns.
+__device__ __forceinline__ void cta_setup(CtaCtl* ctl, int nbar, uint32_t ncols) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nbar; ++i) tc::mbar_init(&ctl->bar[i], 1);
+    tc::fence_mbar_init();
+  }
+  if ((threadIdx.x >> 5) == 0) {
+    tc::tmem_alloc(&ctl->tmem, ncols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+}
+__device__ __forceinline__ void cta_teardown(CtaCtl* ctl, uint32_t ncols) {
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if ((threadIdx.x >> 5) == 0) tc::tmem_dealloc(ctl->tmem, ncols);
+}
+
+// Readiness flags between the CTAs of one cooperative launch (all co-resident).
+// The producer publishes after every write of the unit has completed (its bulk
+// stores waited for, a CTA barrier, then this call on one thread); the consumer
+// acquires before issuing bulk copies that read the unit's outputs.
+__device__ __forceinline__ void publish_flag(uint32_t* flag) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* flag) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v;
+}
+// One thread: true once *flag is set; false if it is still clear after 2 s.
+__device__ __forceinline__ bool flag_ready(const uint32_t* flag) {
+  return ld_acquire(flag) != 0u;
+}
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag) {
+  bool ok = flag_ready(flag);
+  if (!ok) {
+    const uint64_t t0 = tc::globaltimer_ns();
+    while (!(ok = flag_ready(flag))) {
+      __nanosleep(128);
+      if (tc::globaltimer_ns() - t0 > 2000000000ull) break;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return ok;
+}
+
 // Accumulator row held by this thread's TMEM lane for an M-row MMA, or -1.
 // M = 128: warp w (mod 4) owns rows 32w..32w+31 (row = lane).  M = 64: rows
 // 16w..16w+15 sit in lanes 32w..32w+15 (checked by tests/test_umma_layout.py).

@@ -135,19 +135,19 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
 }  // namespace
 
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
-                                                          const __grid_constant__ TmaMaps maps,
-                                                          int bwd) {
-  stamp_kept_operands(p);
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  const int c = blockIdx.x, kh = blockIdx.y;
+// One (chunk c, key head kh) unit of the preparation on a whole CTA.  `sm` is its
+// shared memory (1024-aligned, prep_tc_smem bytes), `tmem` 256 TMEM columns, bar[0] /
+// bar[1] the MMA and load mbarriers with their running phases.  Every write of the
+// unit has completed when it returns; false after a timed-out wait.
+__device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, int kh,
+                          uint8_t* sm, uint32_t tmem, uint64_t* bar, uint32_t& phase,
+                          uint32_t& lphase) {
   int n;
   int64_t t0;
   int len;
   if (!chunk_info(p, c, &n, &t0, &len)) {
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
-    return;
+    return true;
   }
   const int Dk = p.Dk, Dv = p.Dv;
   const int MV = Dv < 64 ? 64 : Dv, NK = Dk < 64 ? 64 : Dk;
@@ -169,27 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
   float* gv = Mt + RB * 1024;                           // [RB][C]
   float* bv = gv + RB * C;                              // [RB][C]
   float* wv = bv + RB * C;                              // [RB][C]
-  uint64_t* bar = (uint64_t*)(wv + RB * C);   // [0] MMA completion, [1] TMA loads
-  uint32_t* tslot = (uint32_t*)(bar + 2);
 
   // W's padding columns (Dk < 64) stay zero: the epilogue writes only columns < Dk
   if (Dk < 64)
     for (int i = tid; i < (int)bKC / 16; i += kThreads) ((uint4*)tW)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) {
-    tc::mbar_init(&bar[0], 1);
-    tc::mbar_init(&bar[1], 1);
-    tc::fence_mbar_init();
-  }
-  if (warp == 0) {
-    tc::tmem_alloc(tslot, 256);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
   __syncthreads();
-  tc::fence_after_sync();
   // TMEM columns: [0, 64) the Gram products, [64, 64 + NK) W, [192, 256) U^T
-  const uint32_t tmem = *tslot, tAccW = tmem + 64, tAccU = tmem + 192;
-  uint32_t phase = 0, lphase = 0;
+  const uint32_t tAccW = tmem + 64, tAccU = tmem + 192;
   bool ok = true;
   const size_t ckk = (size_t)c * p.Hk + kh, ck = ckk * C;
   // raw k and q rows of the chunk: TMA boxes straight into the [K; Q] operand tile
@@ -419,15 +405,32 @@ done:
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  return ok;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
+                                                          const __grid_constant__ TmaMaps maps,
+                                                          int bwd) {
+  stamp_kept_operands(p);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  CtaCtl* ctl = (CtaCtl*)base;
+  cta_setup(ctl, 2, 256);
+  uint32_t phase = 0, lphase = 0;
+  prep_unit(p, maps, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar, phase,
+            lphase);
+  cta_teardown(ctl, 256);
 }
 
 // ---------------------------------------------------------------------------
+// The chunk walk of sequence n, value head h on a whole CTA (`sm`: 1024-aligned,
+// fwd_state_tc_smem bytes; `tmem`: 512 columns; bars[0..2]: MMA and the two load
+// buffers).  In a fused launch (p.fready set) chunk c's tiles are read only after the
+// preparation unit (c, key head) has published them.
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  const int n = blockIdx.x, h = blockIdx.y, kh = h / p.r;
+__device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint32_t tmem,
+                               uint64_t* bars) {
+  const int kh = h / p.r;
   int64_t s0, s1;
   int c0, c1;
   if (!seq_info(p, n, &s0, &s1, &c0, &c1)) {
@@ -448,8 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   uint8_t* tDct = tDt + MV * 128;                     // [MV][C] Delta^T diag(c)
   float* evb = (float*)(tDct + MV * 128);             // [2][C] e^G, by chunk parity
   float* cvb = evb + 2 * C;                           // [2][C] e^{G_last - G}
-  uint64_t* bars = (uint64_t*)(cvb + 2 * C);          // mma, load0, load1
-  uint32_t* tslot = (uint32_t*)(bars + 3);
   auto tW = [&](int b) { return buf0 + b * bufsz; };
   auto tQ = [&](int b) { return buf0 + b * bufsz + bW; };
   auto tK = [&](int b) { return buf0 + b * bufsz + 2 * bW; };
@@ -460,22 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) / 16); i += kThreads)
     ((uint4*)tSt)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < MV * 128 * 2 / 16; i += kThreads) ((uint4*)tDt)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) {
-    tc::mbar_init(&bars[0], 1);
-    tc::mbar_init(&bars[1], 1);
-    tc::mbar_init(&bars[2], 1);
-    tc::fence_mbar_init();
-  }
-  if (warp == 0) {
-    tc::tmem_alloc(tslot, 512);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
   __syncthreads();
-  tc::fence_after_sync();
   // TMEM: X = S^T W^T @0, state update @64, and the output in token rows (M = 64):
   // Q S @256, P Delta @384 (they survive into the next chunk's first product)
-  const uint32_t tmem = *tslot;
   const uint32_t tX = tmem, tS = tmem + 64, tO1 = tmem + 256, tO2 = tmem + 384;
   uint32_t mphase = 0, lph[2] = {0, 0};
   const int vrow = acc_row(MV);
@@ -507,6 +495,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     tc::bulk_g2s((void*)sU(b), p.Utb + chh * Dv * C, bU, lb);
     tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
   };
+  // Thread 0 issues chunk loads in order; a fused launch first needs the preparation
+  // unit's flag (blocking only when the walk cannot go on without the chunk).
+  int issued = c0 - 1;
+  auto try_issue = [&](int cc, bool block) {
+    if (cc >= c1 || cc != issued + 1) return;
+    if (p.fready) {
+      const uint32_t* f = p.fready + (size_t)cc * p.Hk + kh;
+      if (block) {
+        if (!wait_flag(f)) set_status(p.status, GDN_ERR_TIMEOUT, cc);
+      } else if (!flag_ready(f)) {
+        return;
+      } else {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+    }
+    issue_load(cc, (cc - c0) & 1);
+    issued = cc;
+  };
   auto chunk_len = [&](int cc) {
     const int64_t t = s0 + (int64_t)(cc - c0) * C;
     return (int)((s1 - t) < C ? (s1 - t) : C);
@@ -516,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   // timed-out wait.
   auto start_chunk = [&](int cc) -> bool {
     const int b = (cc - c0) & 1, len = chunk_len(cc);
+    if (tid == 0) try_issue(cc, true);
     const bool lok = tc::mbar_wait(&bars[1 + b], lph[b]);
     lph[b] ^= 1u;
     if (__syncthreads_or(lok ? 0 : 1)) {
@@ -539,8 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
   bool ok = true;
   if (c1 > c0) {
     if (tid == 0) {
-      issue_load(c0, 0);
-      if (c0 + 1 < c1) issue_load(c0 + 1, 1);
+      try_issue(c0, true);
+      try_issue(c0 + 1, false);
     }
     ok = start_chunk(c0);
   }
@@ -586,7 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // buffer b is free (no tile of chunk c is read from here on): chunk c + 2's tiles
-    if (tid == 0 && c + 2 < c1) issue_load(c + 2, b);
+    if (tid == 0) {
+      try_issue(c + 1, false);
+      try_issue(c + 2, false);
+    }
     // S^T <- e^{G_last} S^T + Delta^T diag(c) K
     const float eC = ev[len - 1];
 #pragma unroll
@@ -641,10 +651,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
         for (int j = 0; j < 16; ++j)
           p.S_T[((size_t)n * p.Hv + h) * SZ + (size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = S[ii][j];
   if (tid == 0) tc::bulk_wait<0>();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  CtaCtl* ctl = (CtaCtl*)base;
+  cta_setup(ctl, 3, 512);
+  fwd_state_unit<DK>(p, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
+  cta_teardown(ctl, 512);
+}
+
+// The forward as one cooperative launch of one CTA per SM, for batches with fewer
+// (sequence, value head) walks than SMs: CTAs [0, n_seqs * Hv) walk the chunks while
+// the others prepare (chunk, key head) units in chunk order, taken from a work
+// counter, and publish each one's flag; a walk waits for the flag of the chunk it
+// needs next.  Walks never block the preparation, so the launch always finishes.
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1) k_fwd_fused_tc(Params p,
+                                                               const __grid_constant__ TmaMaps maps) {
+  stamp_kept_operands(p);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  CtaCtl* ctl = (CtaCtl*)base;
+  __shared__ int s_unit;
+  cta_setup(ctl, 3, 512);
+  const int walks = p.n_seqs * p.Hv;
+  if ((int)blockIdx.x < walks) {
+    fwd_state_unit<DK>(p, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes, ctl->tmem,
+                       ctl->bar);
+  } else {
+    uint32_t phase = 0, lphase = 0;
+    const int units = p.NC * p.Hk;
+    for (;;) {
+      if (threadIdx.x == 0) s_unit = (int)atomicAdd(p.fwork, 1u);
+      __syncthreads();
+      const int u = s_unit;
+      __syncthreads();
+      if (u >= units) break;
+      const bool ok = prep_unit(p, maps, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
+                                ctl->bar, phase, lphase);
+      if (threadIdx.x == 0) publish_flag(p.fready + u);
+      if (!ok) break;
+    }
+  }
+  cta_teardown(ctl, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -653,7 +705,7 @@ static size_t prep_tc_smem(const Params& p) {
   size_t b = (size_t)((Dk + 63) / 64) * 128 * 128 + (size_t)((Dv + 63) / 64) * 8192 + 4 * 8192 +
              tc::sw128_bytes(64, Dk);
   b += sizeof(float) * ((size_t)2 * C * C + (size_t)RB * C * TS + RB * 1024 + 3 * RB * C);
-  return b + 64 + 1024;
+  return b + kCtlBytes + 1024;
 }
 
 template <int DK>
@@ -662,7 +714,8 @@ static size_t fwd_state_tc_smem(const Params& p) {
   const size_t bW = tc::sw128_bytes(64, DK), bP = 8192;
   const size_t bU = (size_t)Dv * C * 2, bG = C * 4;
   const size_t bufsz = bW * 3 + bP + ((bU + bG + 1023) & ~(size_t)1023);
-  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 4 * C * 4 + 64 + 1024;
+  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 4 * C * 4 + kCtlBytes +
+         1024;
 }
 
 cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st) {
@@ -692,6 +745,46 @@ cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st) {
     case 32: return launch_fwd_state_tc_t<32>(p, st);
     case 64: return launch_fwd_state_tc_t<64>(p, st);
     default: return launch_fwd_state_tc_t<128>(p, st);
+  }
+}
+
+// The fused forward (k_fwd_fused_tc) when the walks leave at least kMinProducers SMs
+// to the preparation and one CTA fits per SM; *launched = false otherwise (the caller
+// then runs the preparation and the walk as two launches).
+template <int DK>
+static cudaError_t launch_fwd_fused_t(const Params& p, const TmaMaps& maps, cudaStream_t st,
+                                      bool* launched) {
+  *launched = false;
+  const int sms = sm_count();
+  const int walks = p.n_seqs * p.Hv;
+  if (sms <= 0 || walks + kMinProducers > sms || p.NC == 0) return cudaSuccess;
+  const size_t a = prep_tc_smem(p), b = fwd_state_tc_smem<DK>(p);
+  const size_t smem = (a > b ? a : b) + 64;
+  cudaError_t e = cudaFuncSetAttribute(k_fwd_fused_tc<DK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_fused_tc<DK>, kThreads, smem);
+  if (e != cudaSuccess || per_sm < 1) return cudaSuccess;
+  Params pp = p;
+  pp.fready = p.fwork + 64;   // the work counter's 256-byte slot, then the flags
+  TmaMaps mm = maps;
+  void* args[] = {&pp, &mm};
+  profile_pre(st, KID_FWD_FUSED_TC);
+  e = cudaLaunchCooperativeKernel((const void*)k_fwd_fused_tc<DK>, dim3(sms), dim3(kThreads), args,
+                                  smem, st);
+  profile_post(st);
+  if (e == cudaSuccess) *launched = true;
+  return e;
+}
+
+cudaError_t launch_fwd_fused_tc(const Params& p, const TmaMaps& maps, cudaStream_t st,
+                                bool* launched) {
+  switch (p.Dk) {
+    case 16: return launch_fwd_fused_t<16>(p, maps, st, launched);
+    case 32: return launch_fwd_fused_t<32>(p, maps, st, launched);
+    case 64: return launch_fwd_fused_t<64>(p, maps, st, launched);
+    default: return launch_fwd_fused_t<128>(p, maps, st, launched);
   }
 }
 
