@@ -152,6 +152,7 @@ def kernel_models(wl: W.Workload):
                           2 * C * C * Dk)
     return {
         "gdn_fwd_fused_tc": (tc_prep_bwd_b + fst_tc_b, tc_prep_f + fst_tc_f, "tensor"),
+        "gdn_bwd_fused_tc": (bst_tc_b + bgr_tc_b, bst_tc_f + bgr_tc_f, "tensor"),
         "gdn_prep_tc": (tc_prep_b, tc_prep_f, "tensor"),
         "gdn_prep_tc_full": (tc_prep_bwd_b, tc_prep_f, "tensor"),
         "gdn_fwd_state_tc": (fst_tc_b, fst_tc_f, "tensor"),

@@ -23,13 +23,14 @@ __device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64)
 }  // namespace
 
 // ---------------------------------------------------------------------------
+// The reverse chunk walk of sequence n, value head h on a whole CTA (`sm`: 1024-aligned,
+// bwd_state_tc_smem bytes; `tmem`: 512 columns; bars[0..2]: MMA and the two load
+// buffers).  In a fused launch (p.bready set) chunk c's flag is published once its dS^T
+// and -dDelta tiles have reached global memory.
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
-                                                               const __grid_constant__ TmaMaps maps) {
-  if (kept_operands_missing(p)) return;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  const int n = blockIdx.x, h = blockIdx.y, kh = h / p.r;
+__device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int h, uint8_t* sm,
+                               uint32_t tmem, uint64_t* bars) {
+  const int kh = h / p.r;
   int64_t s0, s1;
   int c0, c1;
   if (!seq_info(p, n, &s0, &s1, &c0, &c1)) {
@@ -51,8 +52,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
   const uint32_t bufsz = bO + 3 * bK + bP + 1024;
   float* ev = (float*)(buf0 + 2 * bufsz);
   float* cv = ev + C;
-  uint64_t* bars = (uint64_t*)(cv + C);
-  uint32_t* tslot = (uint32_t*)(bars + 3);
   // per stage buffer: the natural tiles of dO (TMA), K, P, Q (scaled in place to
   // scale e^G Q), W and the gates G; every transposed operand is read MN-major
   auto sdO = [&](int b) { return buf0 + b * bufsz; };
@@ -64,20 +63,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
 
   for (int i = tid; i < (int)(bSt + bD) / 16; i += kThreads)
     ((uint4*)tdSt)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) {
-    tc::mbar_init(&bars[0], 1);
-    tc::mbar_init(&bars[1], 1);
-    tc::mbar_init(&bars[2], 1);
-    tc::fence_mbar_init();
-  }
-  if (warp == 0) {
-    tc::tmem_alloc(tslot, 512);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
   __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tslot;
+  // fused launch: chunks whose tiles are in global memory are published (thread 0;
+  // the walk goes down, so every chunk >= published is)
+  int published = c1;
+  auto publish_down_to = [&](int cc) {
+    for (; published > cc; --published)
+      publish_flag(p.bready + ((size_t)(published - 1) * p.Hv + h));
+  };
   // TMEM: dS^T update (rows v) @0; in token rows (M = 64): P^T dO @128, K dS @256
   const uint32_t tA3 = tmem, tA1 = tmem + 128, tA2 = tmem + 256;
   uint32_t mphase = 0, lph[2] = {0, 0};
@@ -201,6 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
+      if (p.bready && c + 1 < c1) {
+        // everything but this chunk's dS^T store has landed: chunk c + 1 is published
+        tc::bulk_wait<1>();
+        publish_down_to(c + 1);
+      }
       tc::bulk_wait_read<0>();   // the dS^T store has read its tile: the update may rewrite it
       tc::mma_tile_x(tA3, tc::smem_u32(tmD), true, 8192u, MV, tc::smem_u32(tW(b)), true, 8192u,
                      NKF, C, 1u);
@@ -232,11 +230,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           p.dS0[((size_t)n * p.Hv + h) * SZ + (size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = dS[ii][j];
-  if (tid == 0) tc::bulk_wait<0>();
-  tc::fence_before_sync();
+  if (tid == 0) {
+    tc::bulk_wait<0>();
+    // the rest (also after an error: consumers then read what there is, the status
+    // word already holds the error)
+    if (p.bready) publish_down_to(c0);
+  }
   __syncthreads();
-  tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
+                                                               const __grid_constant__ TmaMaps maps) {
+  if (kept_operands_missing(p)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  CtaCtl* ctl = (CtaCtl*)base;
+  cta_setup(ctl, 3, 512);
+  bwd_state_unit<DK>(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
+  cta_teardown(ctl, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -253,12 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
 // Every transposed operand (T^T, dW^T, dPE^T, dT^T, K^T, Q^T, S, dS) is a natural
 // tile read MN-major.
 // TMEM (512 columns): dQ_hat @0, dK_hat @128 (M = 64 accumulators), scratch @256.
-__global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
-                                                               const __grid_constant__ TmaMaps maps) {
-  if (kept_operands_missing(p)) return;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  const int c = blockIdx.x, kh = blockIdx.y;
+// One (chunk c, key head kh) gradient unit on a whole CTA (`sm`: 1024-aligned,
+// grads_tc_smem bytes; `tmem`: 512 columns; bars[0] / bars[1]: MMA and loads with
+// their running phases).  In a fused launch (p.bready set) it first waits until the
+// reverse walks of the key head's value heads have published chunk c.
+__device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, uint8_t* sm,
+                           uint32_t tmem, uint64_t* bars, uint32_t& mphase, uint32_t& lphase) {
   int n;
   int64_t t0;
   int len;
@@ -322,28 +334,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   float* rowp = part + 2 * C; // [2][C] per-half partial row sums
   float* colp = rowp + 2 * C; // [4][C] per-quarter partial column sums
   float* red = colp + 4 * C;  // [kThreads / 32]
-  uint64_t* bars = (uint64_t*)(red + 8);  // mma, load
-  uint32_t* tslot = (uint32_t*)(bars + 2);
 
-  if (tid == 0) {
-    tc::mbar_init(&bars[0], 1);
-    tc::mbar_init(&bars[1], 1);
-    tc::fence_mbar_init();
-  }
-  if (warp == 0) {
-    tc::tmem_alloc(tslot, 512);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tslot;
   const uint32_t tdQ = tmem, tdK = tmem + 128, tmp = tmem + 256;
-  uint32_t mphase = 0, lphase = 0;
   const size_t ckk = (size_t)c * p.Hk + kh;
   const int row64 = acc_row(64);
   bool ok = true;
 
+  // fused launch: this chunk's dS^T / -dDelta tiles of every value head of the group
+  if (tid == 0 && p.bready)
+    for (int hh = 0; hh < p.r; ++hh)
+      if (!wait_flag(p.bready + (size_t)c * p.Hv + kh * p.r + hh))
+        set_status(p.status, GDN_ERR_TIMEOUT, c);
   // key-head tiles for the whole CTA
   if (tid == 0) {
     tc::mbar_arrive_expect_tx(&bars[1], 2 * sCK);
@@ -838,7 +839,62 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
+                                                               const __grid_constant__ TmaMaps maps) {
+  if (kept_operands_missing(p)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  CtaCtl* ctl = (CtaCtl*)base;
+  cta_setup(ctl, 2, 512);
+  uint32_t mphase = 0, lphase = 0;
+  grads_unit(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar, mphase,
+             lphase);
+  cta_teardown(ctl, 512);
+}
+
+// The backward as one cooperative launch of one CTA per SM, for batches with fewer
+// (sequence, value head) walks than SMs: CTAs [0, n_seqs * Hv) walk the chunks in
+// reverse and publish each chunk's tiles; the others take (chunk, key head) gradient
+// units in descending chunk order from a work counter, each waiting for its chunk's
+// flags, and every walk joins them when it is done.  Walks never wait on gradient
+// units, so the launch always finishes.
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_fused_tc(Params p,
+                                                               const __grid_constant__ TmaMaps maps) {
+  if (kept_operands_missing(p)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  CtaCtl* ctl = (CtaCtl*)base;
+  __shared__ int s_unit;
+  cta_setup(ctl, 3, 512);
+  const int walks = p.n_seqs * p.Hv;
+  if ((int)blockIdx.x < walks) {
+    bwd_state_unit<DK>(p, maps, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes,
+                       ctl->tmem, ctl->bar);
+    // fresh mbarriers for the gradient role
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < 3; ++i) {
+        tc::mbar_inval(&ctl->bar[i]);
+        tc::mbar_init(&ctl->bar[i], 1);
+      }
+      tc::fence_mbar_init();
+    }
+    __syncthreads();
+  }
+  uint32_t mphase = 0, lphase = 0;
+  const int units = p.NC * p.Hk;
+  for (;;) {
+    if (threadIdx.x == 0) s_unit = (int)atomicAdd(p.bwork, 1u);
+    __syncthreads();
+    const int u = s_unit;
+    __syncthreads();
+    if (u >= units) break;
+    grads_unit(p, maps, p.NC - 1 - u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem, ctl->bar,
+               mphase, lphase);
+  }
+  cta_teardown(ctl, 512);
 }
 
 __global__ void k_bwd_gates_tc(Params p) {
@@ -856,13 +912,21 @@ __global__ void k_bwd_gates_tc(Params p) {
 
 // ---------------------------------------------------------------------------
 template <int DK>
-static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, cudaStream_t st) {
+static size_t bwd_state_tc_smem(const Params& p) {
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const size_t bK = tc::sw128_bytes(64, DK);
   const size_t bO = (size_t)((Dv + 63) / 64) * 8192;
   const size_t bufsz = bO + 3 * bK + 8192 + 1024;
-  const size_t smem = tc::sw128_bytes(MV, DK) + tc::sw128_bytes(64, MV) + 2 * bufsz + 2 * C * 4 + 64 +
-                      1024;
+  return tc::sw128_bytes(MV, DK) + tc::sw128_bytes(64, MV) + 2 * bufsz + 2 * C * 4 + kCtlBytes +
+         1024;
+}
+static size_t grads_tc_smem() {
+  return 66560 + 32768 + 49152 + 32768 + 32768 + (size_t)(16 * C + 8) * 4 + kCtlBytes + 1024;
+}
+
+template <int DK>
+static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, cudaStream_t st) {
+  const size_t smem = bwd_state_tc_smem<DK>(p);
   cudaFuncSetAttribute(k_bwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_BWD_STATE_TC);
   k_bwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kThreads, smem, st>>>(p, maps);
@@ -870,23 +934,62 @@ static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, c
   return cudaGetLastError();
 }
 
+// The fused backward (k_bwd_fused_tc) under the same conditions as the fused forward;
+// *launched = false otherwise.
+template <int DK>
+static cudaError_t launch_bwd_fused_t(const Params& p, const TmaMaps& maps, cudaStream_t st,
+                                      bool* launched) {
+  *launched = false;
+  const int sms = sm_count();
+  const int walks = p.n_seqs * p.Hv;
+  if (sms <= 0 || walks + kMinProducers > sms || p.NC == 0) return cudaSuccess;
+  const size_t a = bwd_state_tc_smem<DK>(p), b = grads_tc_smem();
+  const size_t smem = (a > b ? a : b) + 64;
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_fused_tc<DK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bwd_fused_tc<DK>, kThreads, smem);
+  if (e != cudaSuccess || per_sm < 1) return cudaSuccess;
+  Params pp = p;
+  pp.bready = p.bwork + 64;   // the work counter's 256-byte slot, then the flags
+  TmaMaps mm = maps;
+  void* args[] = {&pp, &mm};
+  profile_pre(st, KID_BWD_FUSED_TC);
+  e = cudaLaunchCooperativeKernel((const void*)k_bwd_fused_tc<DK>, dim3(sms), dim3(kThreads), args,
+                                  smem, st);
+  profile_post(st);
+  if (e == cudaSuccess) *launched = true;
+  return e;
+}
+
 cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
-  if (p.n_seqs > 0) {
-    switch (p.Dk) {
-      case 16: e = launch_bwd_state_tc_t<16>(p, maps, st); break;
-      case 32: e = launch_bwd_state_tc_t<32>(p, maps, st); break;
-      case 64: e = launch_bwd_state_tc_t<64>(p, maps, st); break;
-      default: e = launch_bwd_state_tc_t<128>(p, maps, st); break;
-    }
-    if (e != cudaSuccess) return e;
+  bool fused = false;
+  switch (p.Dk) {
+    case 16: e = launch_bwd_fused_t<16>(p, maps, st, &fused); break;
+    case 32: e = launch_bwd_fused_t<32>(p, maps, st, &fused); break;
+    case 64: e = launch_bwd_fused_t<64>(p, maps, st, &fused); break;
+    default: e = launch_bwd_fused_t<128>(p, maps, st, &fused); break;
   }
-  const size_t smem = 66560 + 32768 + 49152 + 32768 + 32768 + (size_t)(16 * C + 8) * 4 + 64 + 1024;
-  cudaFuncSetAttribute(k_bwd_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  profile_pre(st, KID_BWD_GRADS_TC);
-  k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, maps);
-  profile_post(st);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
+  if (!fused) {
+    if (p.n_seqs > 0) {
+      switch (p.Dk) {
+        case 16: e = launch_bwd_state_tc_t<16>(p, maps, st); break;
+        case 32: e = launch_bwd_state_tc_t<32>(p, maps, st); break;
+        case 64: e = launch_bwd_state_tc_t<64>(p, maps, st); break;
+        default: e = launch_bwd_state_tc_t<128>(p, maps, st); break;
+      }
+      if (e != cudaSuccess) return e;
+    }
+    const size_t smem = grads_tc_smem();
+    cudaFuncSetAttribute(k_bwd_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    profile_pre(st, KID_BWD_GRADS_TC);
+    k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, maps);
+    profile_post(st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   profile_pre(st, KID_BWD_GATES);
   k_bwd_gates_tc<<<1, kThreads, 0, st>>>(p);
   profile_post(st);
