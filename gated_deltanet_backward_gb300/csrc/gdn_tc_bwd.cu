@@ -897,16 +897,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_fused_tc(Params p,
   cta_teardown(ctl, 512);
 }
 
+// d a_log, d dt_bias: one warp per value head; lane l sums chunks l, l + 32, ... in
+// order, then a fixed shuffle tree (the same order on every run)
 __global__ void k_bwd_gates_tc(Params p) {
   if (kept_operands_missing(p)) return;
-  for (int h = threadIdx.x; h < p.Hv; h += blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  for (int h = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); h < p.Hv;
+       h += gridDim.x * (blockDim.x / 32)) {
     float a = 0.f, d = 0.f;
-    for (int c = 0; c < p.NC; ++c) {
+    for (int c = lane; c < p.NC; c += 32) {
       a += p.pa[(size_t)c * p.Hv + h];
       d += p.pd[(size_t)c * p.Hv + h];
     }
-    p.da_log[h] = a;
-    p.ddt_bias[h] = d;
+    a = warp_sum(a);
+    d = warp_sum(d);
+    if (lane == 0) {
+      p.da_log[h] = a;
+      p.ddt_bias[h] = d;
+    }
   }
 }
 
@@ -991,7 +999,7 @@ cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st)
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   profile_pre(st, KID_BWD_GATES);
-  k_bwd_gates_tc<<<1, kThreads, 0, st>>>(p);
+  k_bwd_gates_tc<<<(p.Hv + kThreads / 32 - 1) / (kThreads / 32), kThreads, 0, st>>>(p);
   profile_post(st);
   return cudaGetLastError();
 }

@@ -177,6 +177,16 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   // TMEM columns: [0, 64) the Gram products, [64, 64 + NK) W, [192, 256) U^T
   const uint32_t tAccW = tmem + 64, tAccU = tmem + 192;
   bool ok = true;
+  // the first head group's raw gate inputs, loaded while the q/k tiles are in flight
+  float pre_beta = 0.f, pre_x = 0.f;
+  {
+    const int nh0 = p.r < RB ? p.r : RB;
+    if (tid < nh0 * C && tid % C < len) {
+      const int t = tid % C, h = kh * p.r + tid / C;
+      pre_beta = p.beta_raw[(t0 + t) * p.beta_ld + h];
+      pre_x = p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
+    }
+  }
   const size_t ckk = (size_t)c * p.Hk + kh, ck = ckk * C;
   // raw k and q rows of the chunk: TMA boxes straight into the [K; Q] operand tile
   if (tid == 0) {
@@ -275,8 +285,9 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       const int hh = tid / C, t = tid % C, h = kh * p.r + g0 + hh;
       float l = 0.f, b = 0.f;
       if (t < len) {
-        b = sigmoid_f(p.beta_raw[(t0 + t) * p.beta_ld + h]);
-        const float x = p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
+        const float braw = g0 == 0 ? pre_beta : p.beta_raw[(t0 + t) * p.beta_ld + h];
+        const float x = g0 == 0 ? pre_x : p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
+        b = sigmoid_f(braw);
         l = -expf(p.a_log[h]) * softplus_f(x);
       }
       gv[hh * C + t] = l;
@@ -304,11 +315,20 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       p.G[ch * C + t] = gv[hh * C + t];
       p.b[ch * C + t] = bv[hh * C + t];
     }
-    for (int idx = tid; idx < nh * C * C; idx += kThreads) {
-      const int hh = idx / (C * C), e = idx % (C * C), r = e / C, s = e % C;
-      float a = 0.f;
-      if (s < r) a = bv[hh * C + r] * expf(gv[hh * C + r] - gv[hh * C + s]) * KK[e];
-      Tm[hh * C * TS + r * TS + s] = a;
+    // A = diag(b) (E * K K^T), strictly lower, four columns per step
+    for (int idx = tid; idx < nh * C * (C / 4); idx += kThreads) {
+      const int hh = idx / (C * C / 4), e4 = idx % (C * C / 4), r = e4 / (C / 4), s0 = (e4 % (C / 4)) * 4;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 < r) {
+        const float* g = gv + hh * C;
+        const float br = bv[hh * C + r], gr = g[r];
+        const float4 kk = *(const float4*)(KK + r * C + s0);
+        a.x = br * expf(gr - g[s0]) * kk.x;
+        if (s0 + 1 < r) a.y = br * expf(gr - g[s0 + 1]) * kk.y;
+        if (s0 + 2 < r) a.z = br * expf(gr - g[s0 + 2]) * kk.z;
+        if (s0 + 3 < r) a.w = br * expf(gr - g[s0 + 3]) * kk.w;
+      }
+      *(float4*)(Tm + hh * C * TS + r * TS + s0) = a;
     }
     __syncthreads();
     // 4. T = (I + A)^-1 for the nh heads at once
