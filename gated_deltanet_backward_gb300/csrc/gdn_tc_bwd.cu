@@ -333,7 +333,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   float* part = xa + C;       // [2][C] per-half partial row sums
   float* rowp = part + 2 * C; // [2][C] per-half partial row sums
   float* colp = rowp + 2 * C; // [4][C] per-quarter partial column sums
-  float* red = colp + 4 * C;  // [kThreads / 32]
+  float* invn = colp + 4 * C; // [2][C] 1 / |q|, 1 / |k| of the chunk's tokens
+  float* red = invn + 2 * C;  // [kThreads / 32]
 
   const uint32_t tdQ = tmem, tdK = tmem + 128, tmp = tmem + 256;
   const size_t ckk = (size_t)c * p.Hk + kh;
@@ -345,6 +346,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     for (int hh = 0; hh < p.r; ++hh)
       if (!wait_flag(p.bready + (size_t)c * p.Hv + kh * p.r + hh))
         set_status(p.status, GDN_ERR_TIMEOUT, c);
+  // the norms for the L2 backward at the end
+  if (tid < 2 * C) invn[tid] = 1.f / (tid < C ? p.nq : p.nk)[ckk * C + (tid & (C - 1))];
   // key-head tiles for the whole CTA
   if (tid == 0) {
     tc::mbar_arrive_expect_tx(&bars[1], 2 * sCK);
@@ -789,26 +792,38 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       __syncthreads();
     }
   }
-  // dq, dk of the key head: L2-norm backward of the accumulated dQ_hat, dK_hat
+  // dq, dk of the key head: L2-norm backward of the accumulated dQ_hat, dK_hat,
+  // dx = (dx_hat - x_hat (x_hat . dx_hat)) / |x|; the two row dots first, one barrier
   if (ok) {
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t acc = which ? tdK : tdQ;
-      const uint8_t* xt = which ? tK : tQ;   // x_hat tiles [C][Dk]
-      float dot = 0.f;
-      for (int q = half; q * 16 < Dk; q += 2) {
-        float x[16];
-        tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
-        tc::tmem_ld_wait();
-        if (row64 >= 0) {
-          float xv[16];
-          tile_get16(xt, C, row64, q * 16, xv);
+    {
+      float dot[2] = {0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dot = fmaf(x[j], xv[j], dot);
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t acc = which ? tdK : tdQ;
+        const uint8_t* xt = which ? tK : tQ;   // x_hat tiles [C][Dk]
+        for (int q = half; q * 16 < Dk; q += 2) {
+          float x[16];
+          tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
+          tc::tmem_ld_wait();
+          if (row64 >= 0) {
+            float xv[16];
+            tile_get16(xt, C, row64, q * 16, xv);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dot[which] = fmaf(x[j], xv[j], dot[which]);
+          }
         }
       }
-      if (row64 >= 0) part[half * C + row64] = dot;
-      __syncthreads();
-      const float* nrm = (which ? p.nk : p.nq) + ckk * C;
+      if (row64 >= 0) {
+        part[half * C + row64] = dot[0];
+        rowp[half * C + row64] = dot[1];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t acc = which ? tdK : tdQ;
+      const uint8_t* xt = which ? tK : tQ;
+      const float* pr = which ? rowp : part;
       __nv_bfloat16* dst = (__nv_bfloat16*)(which ? p.dk : p.dq) +
                            t0 * (which ? p.dk_ld : p.dq_ld) + (int64_t)kh * Dk;
       const int64_t ld = which ? p.dk_ld : p.dq_ld;
@@ -818,7 +833,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
         tc::tmem_ld_wait();
         if (row64 >= 0 && row64 < len) {
           const int r = row64;
-          const float d = part[r] + part[C + r], inv = 1.f / nrm[r];
+          const float d = pr[r] + pr[C + r], inv = invn[which * C + r];
           __align__(16) __nv_bfloat162 pk[8];
           float xv[16];
           tile_get16(xt, C, r, q * 16, xv);
@@ -833,7 +848,6 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
           o[1] = ((const uint4*)pk)[1];
         }
       }
-      __syncthreads();
     }
   }
   tc::fence_before_sync();
@@ -885,12 +899,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_fused_tc(Params p,
   }
   uint32_t mphase = 0, lphase = 0;
   const int units = p.NC * p.Hk;
+  // the next unit is taken while the current one runs
+  int next = threadIdx.x == 0 ? (int)atomicAdd(p.bwork, 1u) : 0;
   for (;;) {
-    if (threadIdx.x == 0) s_unit = (int)atomicAdd(p.bwork, 1u);
+    if (threadIdx.x == 0) s_unit = next;
     __syncthreads();
     const int u = s_unit;
     __syncthreads();
     if (u >= units) break;
+    if (threadIdx.x == 0) next = (int)atomicAdd(p.bwork, 1u);
     grads_unit(p, maps, p.NC - 1 - u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem, ctl->bar,
                mphase, lphase);
   }
@@ -929,7 +946,7 @@ static size_t bwd_state_tc_smem(const Params& p) {
          1024;
 }
 static size_t grads_tc_smem() {
-  return 66560 + 32768 + 49152 + 32768 + 32768 + (size_t)(16 * C + 8) * 4 + kCtlBytes + 1024;
+  return 66560 + 32768 + 49152 + 32768 + 32768 + (size_t)(18 * C + 8) * 4 + kCtlBytes + 1024;
 }
 
 template <int DK>

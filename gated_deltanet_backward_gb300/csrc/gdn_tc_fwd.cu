@@ -704,12 +704,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_fused_tc(Params p,
   } else {
     uint32_t phase = 0, lphase = 0;
     const int units = p.NC * p.Hk;
+    // the next unit is taken while the current one runs
+    int next = threadIdx.x == 0 ? (int)atomicAdd(p.fwork, 1u) : 0;
     for (;;) {
-      if (threadIdx.x == 0) s_unit = (int)atomicAdd(p.fwork, 1u);
+      if (threadIdx.x == 0) s_unit = next;
       __syncthreads();
       const int u = s_unit;
       __syncthreads();
       if (u >= units) break;
+      if (threadIdx.x == 0) next = (int)atomicAdd(p.fwork, 1u);
       const bool ok = prep_unit(p, maps, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
                                 ctl->bar, phase, lphase);
       if (threadIdx.x == 0) publish_flag(p.fready + u);
