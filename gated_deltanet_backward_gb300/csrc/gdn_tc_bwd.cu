@@ -369,6 +369,21 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
   }
 
+  // S^T, W, U^T (bulk copies), dO rows into the [dO; -dDelta] tile and V rows (TMA),
+  // -dDelta rows (bulk) of value head h
+  auto issue_phase_a = [&](int h) {
+    const size_t ch = (size_t)c * p.Hv + h;
+    const int nbv = (Dv + 63) / 64;
+    tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u + bSt);
+    tc::bulk_g2s(tSt, (const uint8_t*)p.saved_in + ch * bSt, bSt, &bars[1]);
+    tc::bulk_g2s(tW, p.Wsw + ch * sCK, sCK, &bars[1]);
+    tc::bulk_g2s(sU, p.Utb + ch * Dv * C, (uint32_t)Dv * C * 2, &bars[1]);
+    for (int b = 0; b < nbv; ++b) {
+      tc::tma_load_2d(tA2 + b * 16384, &maps.dO, h * Dv + 64 * b, (int)t0, &bars[1]);
+      tc::tma_load_2d(tV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bars[1]);
+      tc::bulk_g2s(tA2 + b * 16384 + 8192, p.dDb + ch * sCV + b * 8192, 8192, &bars[1]);
+    }
+  };
   for (int hh = 0; hh < p.r && ok; ++hh) {
     const int h = kh * p.r + hh;
     const size_t ch = (size_t)c * p.Hv + h;
@@ -382,20 +397,9 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       dG[tid] = 0.f;
       db[tid] = 0.f;
     }
-    // W and U^T tiles (bulk copies), dO rows into the [dO; dDelta] tile and V rows
-    // (TMA), overlapped with the staging below
-    if (tid == 0) {
-      const int nbv = (Dv + 63) / 64;
-      tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u + bSt);
-      tc::bulk_g2s(tSt, Sg, bSt, &bars[1]);
-      tc::bulk_g2s(tW, p.Wsw + ch * sCK, sCK, &bars[1]);
-      tc::bulk_g2s(sU, p.Utb + ch * Dv * C, (uint32_t)Dv * C * 2, &bars[1]);
-      for (int b = 0; b < nbv; ++b) {
-        tc::tma_load_2d(tA2 + b * 16384, &maps.dO, h * Dv + 64 * b, (int)t0, &bars[1]);
-        tc::tma_load_2d(tV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bars[1]);
-        tc::bulk_g2s(tA2 + b * 16384 + 8192, p.dDb + ch * sCV + b * 8192, 8192, &bars[1]);
-      }
-    }
+    // phase A's tiles: the first head issues its own; every later head's were issued
+    // when the previous head's last product finished
+    if (tid == 0 && hh == 0) issue_phase_a(h);
     __syncthreads();
     if (tid < C) {
       ev[tid] = expf(gv[tid]);
@@ -434,6 +438,12 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
                      sVC, NK, Dv, acc_first);                                            // dQ += s e^G dO S^T
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
+    // the dS^T tile lands over W and scale e^G dO (read by the products above) while
+    // epilogue A runs; P follows once epilogue A has read U^T
+    if (tid == 0) {
+      tc::mbar_expect_tx(&bars[1], bSt);
+      tc::bulk_g2s(tdS, p.dSb + ch * bSt, bSt, &bars[1]);
+    }
     // epilogue A: Delta = U - W S; dG += scale e^G (Q . dO S^T); dW = -dDelta S^T (the
     // lower half of the stacked product)
     part[tid & 127] = 0.f;
@@ -475,9 +485,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     if (tid < C) dG[tid] += p.scale * ev[tid] * (part[tid] + part[C + tid]);
     // ---- phase B: dS tile, P tile (bulk), e^G K from K^T, <S, dS>
     if (tid == 0) {
-      tc::mbar_arrive_expect_tx(&bars[1], sCC + bSt);
+      tc::mbar_arrive_expect_tx(&bars[1], sCC);
       tc::bulk_g2s(tP, p.Psw + ch * sCC, sCC, &bars[1]);
-      tc::bulk_g2s(tdS, p.dSb + ch * bSt, bSt, &bars[1]);
     }
     // S^T again, from global memory (L2), for <S, dS>: the shared copy is gone
     uint4 sraw[8];
@@ -748,6 +757,9 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
                      C, 1u);                                                      // dK += H^T K
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
+    // every tile region but K, Q and K K^T is free: the next head's phase A loads run
+    // under the gate epilogue
+    if (tid == 0 && hh + 1 < p.r) issue_phase_a(h + 1);
     // gate and sigmoid epilogues: dl = reverse cumsum of dG (one warp, two per lane)
     __syncthreads();
     if (warp == 0) {
