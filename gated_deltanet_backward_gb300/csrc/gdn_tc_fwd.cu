@@ -64,72 +64,133 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
       for (int i = 0; i < 16; ++i) B[i * TS + j] = x[i];
     __syncthreads();
   }
-  // 32x32 diagonal blocks (two per head): M = A_10 D_0, then L = -D_1 M
-  const int n1 = nh * 2 * 16 * 4;
-  for (int it = tid; it < n1; it += blockDim.x) {
-    const int pr = it >> 6, r = (it >> 2) & 15, c0 = (it & 3) * 4;
-    const float* T = Tm + (pr >> 1) * C * TS;
-    const int rb = ((pr & 1) * 2 + 1) * 16, cb = rb - 16;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = c0; k < 16; ++k) {   // D_0 is lower triangular
-      const float a = T[(rb + r) * TS + cb + k];
-      const float4 d = *(const float4*)(T + (cb + k) * TS + cb + c0);
-      acc.x = fmaf(a, d.x, acc.x);
-      acc.y = fmaf(a, d.y, acc.y);
-      acc.z = fmaf(a, d.z, acc.z);
-      acc.w = fmaf(a, d.w, acc.w);
+  // 32x32 diagonal blocks (two per head): M = A_10 D_0, then L = -D_1 M.  A thread
+  // runs all its 1 x 4 tiles together over the whole k range (the zero triangles
+  // add exact zeros), so its accumulators form independent chains.
+  {
+    constexpr int kMax = (RB * 2 * 16 * 4 + kThreads - 1) / kThreads;   // tiles per thread
+    const int n1 = nh * 2 * 16 * 4;
+    float4 acc[kMax];
+    int off_a[kMax], off_b[kMax];
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int it = tid + j * kThreads;
+      const int pr = it < n1 ? it >> 6 : 0, r = (it >> 2) & 15, c0 = (it & 3) * 4;
+      const int rb = ((pr & 1) * 2 + 1) * 16, cb = rb - 16;
+      off_a[j] = (pr >> 1) * C * TS + (rb + r) * TS + cb;          // row r of A_10
+      off_b[j] = (pr >> 1) * C * TS + cb * TS + cb + c0;           // column piece of D_0
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *(float4*)(M + pr * 256 + r * 16 + c0) = acc;
-  }
-  __syncthreads();
-  for (int it = tid; it < n1; it += blockDim.x) {
-    const int pr = it >> 6, r = (it >> 2) & 15, c0 = (it & 3) * 4;
-    float* T = Tm + (pr >> 1) * C * TS;
-    const int rb = ((pr & 1) * 2 + 1) * 16, cb = rb - 16;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k <= r; ++k) {    // D_1 is lower triangular
-      const float d = T[(rb + r) * TS + rb + k];
-      const float4 m = *(const float4*)(M + pr * 256 + k * 16 + c0);
-      acc.x = fmaf(d, m.x, acc.x);
-      acc.y = fmaf(d, m.y, acc.y);
-      acc.z = fmaf(d, m.z, acc.z);
-      acc.w = fmaf(d, m.w, acc.w);
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k)
+#pragma unroll
+      for (int j = 0; j < kMax; ++j) {
+        const float a = Tm[off_a[j] + k];
+        const float4 d = *(const float4*)(Tm + off_b[j] + k * TS);
+        acc[j].x = fmaf(a, d.x, acc[j].x);
+        acc[j].y = fmaf(a, d.y, acc[j].y);
+        acc[j].z = fmaf(a, d.z, acc[j].z);
+        acc[j].w = fmaf(a, d.w, acc[j].w);
+      }
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int it = tid + j * kThreads;
+      if (it < n1) *(float4*)(M + (it >> 6) * 256 + ((it >> 2) & 15) * 16 + (it & 3) * 4) = acc[j];
     }
-    *(float4*)(T + (rb + r) * TS + cb + c0) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-  }
-  __syncthreads();
-  // 64x64: M = A_BA T_A, then lower-left = -T_B M
-  const int n2 = nh * 32 * 8;
-  for (int it = tid; it < n2; it += blockDim.x) {
-    const int hh = it >> 8, r = (it >> 3) & 31, c0 = (it & 7) * 4;
-    const float* T = Tm + hh * C * TS;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = c0; k < 32; ++k) {   // T_A is lower triangular
-      const float a = T[(32 + r) * TS + k];
-      const float4 t = *(const float4*)(T + k * TS + c0);
-      acc.x = fmaf(a, t.x, acc.x);
-      acc.y = fmaf(a, t.y, acc.y);
-      acc.z = fmaf(a, t.z, acc.z);
-      acc.w = fmaf(a, t.w, acc.w);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int it = tid + j * kThreads;
+      const int pr = it < n1 ? it >> 6 : 0, r = (it >> 2) & 15;
+      const int rb = ((pr & 1) * 2 + 1) * 16;
+      off_a[j] = (pr >> 1) * C * TS + (rb + r) * TS + rb;          // row r of D_1
+      off_b[j] = pr * 256 + (it & 3) * 4;                          // column piece of M
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *(float4*)(M + hh * 1024 + r * 32 + c0) = acc;
-  }
-  __syncthreads();
-  for (int it = tid; it < n2; it += blockDim.x) {
-    const int hh = it >> 8, r = (it >> 3) & 31, c0 = (it & 7) * 4;
-    float* T = Tm + hh * C * TS;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k <= r; ++k) {    // T_B is lower triangular
-      const float t = T[(32 + r) * TS + 32 + k];
-      const float4 m = *(const float4*)(M + hh * 1024 + k * 32 + c0);
-      acc.x = fmaf(t, m.x, acc.x);
-      acc.y = fmaf(t, m.y, acc.y);
-      acc.z = fmaf(t, m.z, acc.z);
-      acc.w = fmaf(t, m.w, acc.w);
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k)
+#pragma unroll
+      for (int j = 0; j < kMax; ++j) {
+        const float d = Tm[off_a[j] + k];
+        const float4 m = *(const float4*)(M + off_b[j] + k * 16);
+        acc[j].x = fmaf(d, m.x, acc[j].x);
+        acc[j].y = fmaf(d, m.y, acc[j].y);
+        acc[j].z = fmaf(d, m.z, acc[j].z);
+        acc[j].w = fmaf(d, m.w, acc[j].w);
+      }
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int it = tid + j * kThreads;
+      if (it < n1) {
+        const int pr = it >> 6, r = (it >> 2) & 15, c0 = (it & 3) * 4;
+        const int rb = ((pr & 1) * 2 + 1) * 16, cb = rb - 16;
+        *(float4*)(Tm + (pr >> 1) * C * TS + (rb + r) * TS + cb + c0) =
+            make_float4(-acc[j].x, -acc[j].y, -acc[j].z, -acc[j].w);
+      }
     }
-    *(float4*)(T + (32 + r) * TS + c0) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    __syncthreads();
   }
-  __syncthreads();
+  // 64x64: M = A_BA T_A, then lower-left = -T_B M (same scheme, k over 32)
+  {
+    constexpr int kMax = (RB * 32 * 8 + kThreads - 1) / kThreads;
+    const int n2 = nh * 32 * 8;
+    float4 acc[kMax];
+    int off_a[kMax], off_b[kMax];
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int it = tid + j * kThreads;
+      const int hh = it < n2 ? it >> 8 : 0, r = (it >> 3) & 31, c0 = (it & 7) * 4;
+      off_a[j] = hh * C * TS + (32 + r) * TS;                      // row r of A_BA
+      off_b[j] = hh * C * TS + c0;                                 // column piece of T_A
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k)
+#pragma unroll
+      for (int j = 0; j < kMax; ++j) {
+        const float a = Tm[off_a[j] + k];
+        const float4 t = *(const float4*)(Tm + off_b[j] + k * TS);
+        acc[j].x = fmaf(a, t.x, acc[j].x);
+        acc[j].y = fmaf(a, t.y, acc[j].y);
+        acc[j].z = fmaf(a, t.z, acc[j].z);
+        acc[j].w = fmaf(a, t.w, acc[j].w);
+      }
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int it = tid + j * kThreads;
+      if (it < n2) *(float4*)(M + (it >> 8) * 1024 + ((it >> 3) & 31) * 32 + (it & 7) * 4) = acc[j];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int it = tid + j * kThreads;
+      const int hh = it < n2 ? it >> 8 : 0, r = (it >> 3) & 31;
+      off_a[j] = hh * C * TS + (32 + r) * TS + 32;                 // row r of T_B
+      off_b[j] = hh * 1024 + (it & 7) * 4;                         // column piece of M
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k)
+#pragma unroll
+      for (int j = 0; j < kMax; ++j) {
+        const float t = Tm[off_a[j] + k];
+        const float4 m = *(const float4*)(M + off_b[j] + k * 32);
+        acc[j].x = fmaf(t, m.x, acc[j].x);
+        acc[j].y = fmaf(t, m.y, acc[j].y);
+        acc[j].z = fmaf(t, m.z, acc[j].z);
+        acc[j].w = fmaf(t, m.w, acc[j].w);
+      }
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int it = tid + j * kThreads;
+      if (it < n2) {
+        const int hh = it >> 8, r = (it >> 3) & 31, c0 = (it & 7) * 4;
+        *(float4*)(Tm + hh * C * TS + (32 + r) * TS + c0) =
+            make_float4(-acc[j].x, -acc[j].y, -acc[j].z, -acc[j].w);
+      }
+    }
+    __syncthreads();
+  }
 }
 
 }  // namespace
@@ -206,37 +267,41 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   }
   if (!ok) goto done;
 
-  // 1. L2 normalisation in place: a row of Dk elements is Dk/8 consecutive threads;
-  // rows past the chunk become zero
+  // 1. L2 normalisation in place, two threads per row (K rows 0-63, Q rows 64-127),
+  // each with its half of the row's 16-byte pieces in registers; rows past the chunk
+  // become zero
   {
-    const int lpr = Dk / 8;
-    const int total = 2 * C * lpr;
-    for (int idx0 = 0; idx0 < total; idx0 += kThreads) {
-      const int idx = idx0 + tid;
-      const int row = idx / lpr, c0 = (idx % lpr) * 8;
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (idx < total) raw = *(const uint4*)(tAQK + tc::sw128_offset(row, c0, 128));
-      const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
-      float x[8], ss = 0.f;
+    const int row = tid >> 1, part = tid & 1, cpt = Dk / 16;
+    const bool isq = row >= C;
+    const int t = row & (C - 1);
+    uint4 raw[8];
+    float ss = 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        x[q] = __bfloat162float(e[q]);
-        ss = fmaf(x[q], x[q], ss);
+    for (int j = 0; j < 8; ++j)
+      if (j < cpt) {
+        raw[j] = *(const uint4*)(tAQK + tc::sw128_offset(row, (part * cpt + j) * 8, 128));
+        const __nv_bfloat162* e = (const __nv_bfloat162*)&raw[j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(e[q]);
+          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+        }
       }
-      for (int o = lpr >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (idx < total) {
-        const bool isq = row >= C;
-        const int t = row & (C - 1);
-        const float nrm = sqrtf(ss + 1e-6f), inv = t < len ? 1.f / nrm : 0.f;
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    const float nrm = sqrtf(ss + 1e-6f), inv = t < len ? 1.f / nrm : 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] *= inv;
+    for (int j = 0; j < 8; ++j)
+      if (j < cpt) {
+        const __nv_bfloat162* e = (const __nv_bfloat162*)&raw[j];
         __align__(16) __nv_bfloat162 pk[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) pk[q] = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
-        *(uint4*)(tAQK + tc::sw128_offset(row, c0, 128)) = *(const uint4*)pk;
-        if (bwd && c0 == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(e[q]);
+          pk[q] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+        }
+        *(uint4*)(tAQK + tc::sw128_offset(row, (part * cpt + j) * 8, 128)) = *(const uint4*)pk;
       }
-    }
+    if (bwd && part == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
     // Dk < 64: the box's columns past Dk (a neighbouring head) become zero padding
     if (Dk < 64) {
       const int padc = 8 - Dk / 8;
