@@ -194,14 +194,15 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
+      tc::mma_tile_x(tA3, tc::smem_u32(tmD), true, 8192u, MV, tc::smem_u32(tW(b)), true, 8192u,
+                     NKF, C, 1u);
+      // while the tensor core works: everything but this chunk's dS^T store has landed,
+      // so chunk c + 1 is published
       if (p.bready && c + 1 < c1) {
-        // everything but this chunk's dS^T store has landed: chunk c + 1 is published
         tc::bulk_wait<1>();
         publish_down_to(c + 1);
       }
       tc::bulk_wait_read<0>();   // the dS^T store has read its tile: the update may rewrite it
-      tc::mma_tile_x(tA3, tc::smem_u32(tmD), true, 8192u, MV, tc::smem_u32(tW(b)), true, 8192u,
-                     NKF, C, 1u);
       tc::bulk_s2g(p.dDb + ch * bD, tmD, bD);
       tc::bulk_commit();
     }, &bars[0], mphase, p.status, c);

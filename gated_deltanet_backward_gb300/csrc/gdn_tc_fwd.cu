@@ -582,10 +582,12 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   };
   // Thread 0 issues chunk loads in order; a fused launch first needs the preparation
   // unit's flag (blocking only when the walk cannot go on without the chunk).
-  int issued = c0 - 1;
+  int issued = c0 - 1, acquired = c0 - 1;   // acquired: the flag was already read set
   auto try_issue = [&](int cc, bool block) {
     if (cc >= c1 || cc != issued + 1) return;
-    if (p.fready) {
+    if (p.fready && cc == acquired) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    } else if (p.fready) {
       const uint32_t* f = p.fready + (size_t)cc * p.Hk + kh;
       if (block) {
         if (!wait_flag(f)) set_status(p.status, GDN_ERR_TIMEOUT, cc);
@@ -675,6 +677,10 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       tc::mma_tile_p(tO1, tc::smem_u32(tQ(b)), 8192u, 64, tc::smem_u32(tSt), (uint32_t)MV * 128u,
                      Dv, DK, 0u);
       tc::mma_tile(tO2, tc::smem_u32(tP(b)), 64, tc::smem_u32(tDt), Dv, C, 0u);
+      // while the tensor core works: is chunk c + 2 prepared (flag read ahead)?
+      if (p.fready && c + 2 < c1 && issued == c + 1 &&
+          flag_ready(p.fready + (size_t)(c + 2) * p.Hk + kh))
+        acquired = c + 2;
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // buffer b is free (no tile of chunk c is read from here on): chunk c + 2's tiles
