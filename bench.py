@@ -172,9 +172,12 @@ def kernel_models(wl: W.Workload):
 # a kernel whose sources changed since reports null (profiles/tc_kernels_l27b_bf16.md).
 NCU_TRAFFIC = {
     ("gdn_bwd_grads_tc", "l27b_bf16"): (655.676416e6, "91b4d82f68e0ec3b"),
+    ("gdn_bwd_fused_tc", "l27b_bf16"): (948.073984e6, "b147bfe7dbe60c9a"),
 }
 KERNEL_SOURCES = {
     "gdn_bwd_grads_tc": ("gdn_tc_bwd.cu", "gdn_tc.cuh", "umma.cuh", "gdn_device.cuh",
+                         "gdn_internal.cuh"),
+    "gdn_bwd_fused_tc": ("gdn_tc_bwd.cu", "gdn_tc.cuh", "umma.cuh", "gdn_device.cuh",
                          "gdn_internal.cuh"),
 }
 
