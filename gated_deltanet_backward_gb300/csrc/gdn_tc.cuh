@@ -13,6 +13,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
+// Threads per CTA of the tensor-core kernels: 16 warps, so that each TMEM lane
+// quarter (warps w, w + 4, w + 8, w + 12) is read by kGroups warps that split an
+// accumulator's columns between them.
+constexpr int kTcThreads = 512;
+constexpr int kGroups = kTcThreads / 128;
+__device__ __forceinline__ int col_group() { return (int)(threadIdx.x >> 7); }
+
 // The first kCtlBytes of a tensor-core kernel's (1024-aligned) shared memory: its
 // mbarriers and the TMEM address, at the same place whatever role the CTA plays.
 constexpr uint32_t kCtlBytes = 1024;
@@ -84,14 +91,13 @@ __device__ __forceinline__ uint32_t lane_quarter() {
   return (uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16;
 }
 
-// Walks the accumulator columns [0, N) in 16-column pieces; the two warps that
-// share a lane quarter (w and w + 4 of an 8-warp CTA) take alternate pieces.
-// f(row, col0, v[16]) runs for rows < valid.  Whole warps must call this.
+// Walks the accumulator columns [0, N) in 16-column pieces; the kGroups warps that
+// share a lane quarter take every kGroups-th piece.  f(row, col0, v[16]) runs for
+// rows < valid.  Whole warps must call this.
 template <class F>
 __device__ __forceinline__ void acc_walk(uint32_t tmem, int M, int N, int valid, F f) {
-  const int half = (int)(threadIdx.x >> 7);  // 0 for warps 0-3, 1 for warps 4-7
   const int row = acc_row(M);
-  for (int c = half * 16; c < N; c += 32) {
+  for (int c = col_group() * 16; c < N; c += 16 * kGroups) {
     float v[16];
     tc::tmem_ld16(tmem + lane_quarter() + (uint32_t)c, v);
     tc::tmem_ld_wait();

@@ -19,6 +19,7 @@ namespace gdn {
 
 namespace {
 constexpr int C = kChunk;
+constexpr int kColParts = kTcThreads / 64;   // row blocks of the column sums of a C x C scratch
 __device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
 }  // namespace
 
@@ -37,9 +38,9 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, n);
     return;
   }
-  constexpr int NKC = (DK + 31) / 32;
+  constexpr int NKC = (DK + 16 * kGroups - 1) / (16 * kGroups);   // dS^T pieces per thread
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
-  const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
+  const int tid = threadIdx.x, grp = col_group();
   constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read Q / W MN-major
   const uint32_t bK = (uint32_t)tileCD(DK), bP = 8192, bG = C * 4;
   const int nbv = (Dv + 63) / 64;
@@ -61,7 +62,7 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
   auto tW = [&](int b) { return buf0 + b * bufsz + bO + 2 * bK + bP; };
   auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + bO + 3 * bK + bP); };
 
-  for (int i = tid; i < (int)(bSt + bD) / 16; i += kThreads)
+  for (int i = tid; i < (int)(bSt + bD) / 16; i += kTcThreads)
     ((uint4*)tdSt)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   // fused launch: chunks whose tiles are in global memory are published (thread 0;
@@ -83,12 +84,13 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
   for (int i = 0; i < NKC; ++i)
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const int k = half * 16 + 32 * i + j;
+      const int k = grp * 16 + 16 * kGroups * i + j;
       dS[i][j] = (vok && k < DK && p.dS_T) ? p.dS_T[((size_t)n * p.Hv + h) * SZ + (size_t)k * Dv + vrow] : 0.f;
     }
 #pragma unroll
   for (int i = 0; i < NKC; ++i)
-    if (half * 16 + 32 * i < DK && vok) tile_put16(tdSt, MV, vrow, half * 16 + 32 * i, dS[i]);
+    if (grp * 16 + 16 * kGroups * i < DK && vok)
+      tile_put16(tdSt, MV, vrow, grp * 16 + 16 * kGroups * i, dS[i]);
   tc::fence_async_smem();
 
   auto issue_load = [&](int cc, int b) {
@@ -136,12 +138,12 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
     __syncthreads();
     // rows of the dO tile past the chunk (another sequence's tokens) read as zero
     if (len < C)
-      for (int idx = tid; idx < nbv * (C - len) * 8; idx += kThreads) {
+      for (int idx = tid; idx < nbv * (C - len) * 8; idx += kTcThreads) {
         const int b2 = idx / ((C - len) * 8), rem = idx % ((C - len) * 8);
         ((uint4*)(sdO(b) + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
       }
     // scale e^G Q in place: row r of the natural Q tile times scale e^{G_r}
-    for (int idx = tid; idx < C * (DK / 8); idx += kThreads) {
+    for (int idx = tid; idx < C * (DK / 8); idx += kTcThreads) {
       const int r = idx % C, k8 = (idx / C) * 8;
       uint4* at = (uint4*)(tQ(b) + tc::sw128_offset(r, k8, C));
       const uint4 raw = *at;
@@ -173,7 +175,7 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
     // operand of the update below, read MN-major, and the gradient kernel's tile)
     {
       const int s = acc_row(64);
-      for (int q = half; q * 16 < Dv; q += 2) {
+      for (int q = grp; q * 16 < Dv; q += kGroups) {
         float a1[16], a2[16];
         tc::tmem_ld16(tA1 + lane_quarter() + q * 16, a1);
         tc::tmem_ld16(tA2 + lane_quarter() + q * 16, a2);
@@ -210,7 +212,7 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
     const float eC = expf(G[len - 1]);
 #pragma unroll
     for (int ii = 0; ii < NKC; ++ii) {
-      const int col0 = half * 16 + 32 * ii;
+      const int col0 = grp * 16 + 16 * kGroups * ii;
       if (col0 < DK) {
         float x[16];
         tc::tmem_ld16(tA3 + lane_quarter() + col0, x);
@@ -227,10 +229,11 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
   if (ok && p.dS0 && vok)
 #pragma unroll
     for (int ii = 0; ii < NKC; ++ii)
-      if (half * 16 + 32 * ii < DK)
+      if (grp * 16 + 16 * kGroups * ii < DK)
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          p.dS0[((size_t)n * p.Hv + h) * SZ + (size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = dS[ii][j];
+          p.dS0[((size_t)n * p.Hv + h) * SZ + (size_t)(grp * 16 + 16 * kGroups * ii + j) * Dv +
+                vrow] = dS[ii][j];
   if (tid == 0) {
     tc::bulk_wait<0>();
     // the rest (also after an error: consumers then read what there is, the status
@@ -241,7 +244,7 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
 }
 
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 1) k_bwd_state_tc(Params p,
+__global__ void __launch_bounds__(kTcThreads, 1) k_bwd_state_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   if (kept_operands_missing(p)) return;
   extern __shared__ uint8_t smem_raw[];
@@ -280,7 +283,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     return;
   }
   const int Dk = p.Dk, Dv = p.Dv;
-  const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
+  const int tid = threadIdx.x, warp = tid >> 5, grp = col_group();
   const uint32_t sCK = tc::sw128_bytes(C, Dk), sCV = tc::sw128_bytes(C, Dv);
   const uint32_t sCC = 8192;
   // tiles handed over by the state kernels: S^T and dS^T [MV][Dk], -dDelta^T [MV][C],
@@ -303,6 +306,13 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   uint8_t* tH = R1 + 24576;                        // [C][C] H = dA b_r E (strictly lower)
   float* sKK = (float*)(R1 + 49152);               // [C][KKL] fp32 K K^T (padded rows)
   constexpr int KKL = C + 4;
+  // per-row partial sums of the kGroups column groups, added in a fixed order
+  auto rsum_g = [&](const float* a, int t) {
+    float v = a[t];
+#pragma unroll
+    for (int g = 1; g < kGroups; ++g) v += a[g * C + t];
+    return v;
+  };
   // R2
   uint8_t* tA2 = R2;                               // [128][Dv]: rows 0-63 dO, 64-127 -dDelta
   float* X = (float*)R2;                           // [C][C + 1] fp32 scratch (padded rows)
@@ -331,11 +341,11 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   float* dG = bv + C;         // dL/dG
   float* db = dG + C;         // dL/d beta
   float* xa = db + C;         // alpha + dt_bias of the chunk's tokens
-  float* part = xa + C;       // [2][C] per-half partial row sums
-  float* rowp = part + 2 * C; // [2][C] per-half partial row sums
-  float* colp = rowp + 2 * C; // [4][C] per-quarter partial column sums
-  float* invn = colp + 4 * C; // [2][C] 1 / |q|, 1 / |k| of the chunk's tokens
-  float* red = invn + 2 * C;  // [kThreads / 32]
+  float* part = xa + C;       // [kGroups][C] per-group partial row sums
+  float* rowp = part + kGroups * C;  // [kGroups][C] per-group partial row sums
+  float* colp = rowp + kGroups * C;  // [kColParts][C] partial column sums
+  float* invn = colp + kColParts * C;  // [2][C] 1 / |q|, 1 / |k| of the chunk's tokens
+  float* red = invn + 2 * C;  // [kTcThreads / 32]
 
   const uint32_t tdQ = tmem, tdK = tmem + 128, tmp = tmem + 256;
   const size_t ckk = (size_t)c * p.Hk + kh;
@@ -358,7 +368,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   {
     // K K^T of the key head into padded rows (conflict-free row reads in epilogue D)
     const float4* KK = (const float4*)(p.KKf + ckk * C * C);
-    for (int i = tid; i < C * C / 4; i += kThreads)
+    for (int i = tid; i < C * C / 4; i += kTcThreads)
       *(float4*)(sKK + (i / (C / 4)) * KKL + (i % (C / 4)) * 4) = KK[i];
   }
   {
@@ -418,7 +428,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       }
     }
     // scale e^G dO (rows past the chunk zero) from the dO rows of the [dO; dDelta] tile
-    for (int idx = tid; idx < C * (Dv / 8); idx += kThreads) {
+    for (int idx = tid; idx < C * (Dv / 8); idx += kTcThreads) {
       const int r = idx % C, c8 = (idx / C) * 8;
       const uint4 raw = *(const uint4*)(tA2 + tc::sw128_offset(r, c8, 128));
       const __nv_bfloat16* e = (const __nv_bfloat16*)&raw;
@@ -447,9 +457,9 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
     // epilogue A: Delta = U - W S; dG += scale e^G (Q . dO S^T); dW = -dDelta S^T (the
     // lower half of the stacked product)
-    part[tid & 127] = 0.f;
+    if (tid < kGroups * C) part[tid] = 0.f;
     __syncthreads();
-    for (int q = half; q * 16 < Dv; q += 2) {
+    for (int q = grp; q * 16 < Dv; q += kGroups) {
       float x[16];
       tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
       tc::tmem_ld_wait();
@@ -467,7 +477,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     {
       const int row = acc_row(128);
       float rs = 0.f;
-      for (int q = half; q * 16 < Dk; q += 2) {
+      for (int q = grp; q * 16 < Dk; q += kGroups) {
         float x[16];
         tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
@@ -480,23 +490,24 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
           tile_put16(tdW, C, row - C, q * 16, x);
         }
       }
-      if (row < C) part[half * C + row] = rs;
+      if (row < C) part[grp * C + row] = rs;
     }
     __syncthreads();
-    if (tid < C) dG[tid] += p.scale * ev[tid] * (part[tid] + part[C + tid]);
+    if (tid < C) dG[tid] += p.scale * ev[tid] * rsum_g(part, tid);
     // ---- phase B: dS tile, P tile (bulk), e^G K from K^T, <S, dS>
     if (tid == 0) {
       tc::mbar_arrive_expect_tx(&bars[1], sCC);
       tc::bulk_g2s(tP, p.Psw + ch * sCC, sCC, &bars[1]);
     }
     // S^T again, from global memory (L2), for <S, dS>: the shared copy is gone
-    uint4 sraw[8];
+    constexpr int kSraw = 32768 / 16 / kTcThreads;   // 16-byte pieces per thread (32 KB tile max)
+    uint4 sraw[kSraw];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t i = tid + u * kThreads;
+    for (int u = 0; u < kSraw; ++u) {
+      const uint32_t i = tid + u * kTcThreads;
       sraw[u] = i < bSt / 16 ? ((const uint4*)Sg)[i] : make_uint4(0, 0, 0, 0);
     }
-    for (int idx = tid; idx < C * (Dk / 8); idx += kThreads) {
+    for (int idx = tid; idx < C * (Dk / 8); idx += kTcThreads) {
       const int s = idx % C, k8 = (idx / C) * 8;
       const uint32_t off = tc::sw128_offset(s, k8, C);
       const uint4 raw = *(const uint4*)(tK + off);
@@ -524,8 +535,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       // the dot product runs over them flat
       float sds = 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint32_t i = tid + u * kThreads;
+      for (int u = 0; u < kSraw; ++u) {
+        const uint32_t i = tid + u * kTcThreads;
         if (i < bSt / 16) {
           const uint4 raw = ((const uint4*)tdS)[i];
           const __nv_bfloat162* a = (const __nv_bfloat162*)&sraw[u];
@@ -564,7 +575,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     // epilogue B
     {
       float rs = 0.f;
-      for (int q = half; q * 16 < Dk; q += 2) {
+      for (int q = grp; q * 16 < Dk; q += kGroups) {
         float x[16];
         tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
@@ -575,11 +586,11 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
           for (int j = 0; j < 16; ++j) rs = fmaf(kv[j], x[j], rs);
         }
       }
-      if (row64 >= 0) part[half * C + row64] = rs;  // c_s * dc_s
+      if (row64 >= 0) part[grp * C + row64] = rs;  // c_s * dc_s
     }
     {
       float rsum = 0.f;
-      for (int q = half; q < 4; q += 2) {
+      for (int q = grp; q < 4; q += kGroups) {
         float x[16], y[16];
         tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
         tc::tmem_ld16(tmp + 192 + lane_quarter() + q * 16, y);
@@ -603,28 +614,31 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
           tile_put16(tdT, C, r, q * 16, dt);
         }
       }
-      if (row64 >= 0) rowp[half * C + row64] = rsum;
+      if (row64 >= 0) rowp[grp * C + row64] = rsum;
     }
     __syncthreads();
     {
       // column sums of X in four quarters of rows
-      const int t = tid & (C - 1), qd = tid >> 6;
+      const int t = tid & (C - 1), qd = tid / C;
+      constexpr int rows = C / kColParts;
       float cs = 0.f;
 #pragma unroll 4
-      for (int r = qd * 16; r < qd * 16 + 16; ++r) cs += X[r * XL + t];
+      for (int r = qd * rows; r < qd * rows + rows; ++r) cs += X[r * XL + t];
       colp[qd * C + t] = cs;
     }
     __syncthreads();
     if (tid < C) {
       const int t = tid;
-      const float csum = (colp[t] + colp[C + t]) + (colp[2 * C + t] + colp[3 * C + t]);
-      dG[t] += (rowp[t] + rowp[C + t]) - csum - (part[t] + part[C + t]);
+      float csum = 0.f;
+#pragma unroll
+      for (int g = 0; g < kColParts; ++g) csum += colp[g * C + t];
+      dG[t] += rsum_g(rowp, t) - csum - rsum_g(part, t);
     }
     __syncthreads();
     if (tid == 0) {
       float tot = 0.f, sc = 0.f;
-      for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
-      for (int s = 0; s < C; ++s) sc += part[s] + part[C + s];
+      for (int w = 0; w < kTcThreads / 32; ++w) tot += red[w];
+      for (int s = 0; s < C; ++s) sc += rsum_g(part, s);
       dG[len - 1] += expf(gv[len - 1]) * tot + sc;
     }
     // ---- phase C: -dDelta^T, T, T diag(b e^G) (issued after the MMAs of phase B)
@@ -652,7 +666,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     {
       __nv_bfloat16* dvc = (__nv_bfloat16*)p.dv + t0 * p.dv_ld + (int64_t)h * Dv;
       float rs = 0.f;
-      for (int q = half; q * 16 < Dv; q += 2) {
+      for (int q = grp; q * 16 < Dv; q += kGroups) {
         float x[16];
         tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
@@ -673,8 +687,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
           dst[1] = ((const uint4*)pk)[1];
         }
       }
-      if (row64 >= 0) part[half * C + row64] = rs;
-      for (int q = half; q < 4; q += 2) {
+      if (row64 >= 0) part[grp * C + row64] = rs;
+      for (int q = grp; q < 4; q += kGroups) {
         float x[16];
         tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
@@ -682,7 +696,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       }
     }
     __syncthreads();
-    if (tid < C) db[tid] += part[tid] + part[C + tid];
+    if (tid < C) db[tid] += rsum_g(part, tid);
     tc::fence_async_smem();
     ok = mma_run([&] {
       tc::mma_tile_x(tmp, tc::smem_u32(tT), true, sCC, 64, tc::smem_u32(tdW), true, 8192u, NK, C,
@@ -698,7 +712,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     // dK term (H + H^T) K
     {
       float rs = 0.f;
-      for (int q = half; q * 16 < Dk; q += 2) {
+      for (int q = grp; q * 16 < Dk; q += kGroups) {
         float x[16];
         tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
@@ -709,9 +723,9 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
           for (int j = 0; j < 16; ++j) rs = fmaf(kv[j], x[j], rs);
         }
       }
-      if (row64 >= 0) part[half * C + row64] = rs;
+      if (row64 >= 0) part[grp * C + row64] = rs;
       float rq = 0.f;
-      for (int q = half; q < 4; q += 2) {
+      for (int q = grp; q < 4; q += kGroups) {
         float x[16];
         tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
@@ -732,21 +746,24 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
           tile_put16(tH, C, r, q * 16, hv);
         }
       }
-      if (row64 >= 0) rowp[half * C + row64] = rq;
+      if (row64 >= 0) rowp[grp * C + row64] = rq;
     }
     __syncthreads();
     {
-      const int t = tid & (C - 1), qd = tid >> 6;
+      const int t = tid & (C - 1), qd = tid / C;
+      constexpr int rows = C / kColParts;
       float cs = 0.f;
 #pragma unroll 4
-      for (int r = qd * 16; r < qd * 16 + 16; ++r) cs += X[r * XL + t];
+      for (int r = qd * rows; r < qd * rows + rows; ++r) cs += X[r * XL + t];
       colp[qd * C + t] = cs;
     }
     __syncthreads();
     if (tid < C) {
       const int t = tid;
-      const float ts = part[t] + part[C + t], rq = rowp[t] + rowp[C + t];
-      const float cy = (colp[t] + colp[C + t]) + (colp[2 * C + t] + colp[3 * C + t]);
+      const float ts = rsum_g(part, t), rq = rsum_g(rowp, t);
+      float cy = 0.f;
+#pragma unroll
+      for (int g = 0; g < kColParts; ++g) cy += colp[g * C + t];
       db[t] += ev[t] * ts + rq;
       dG[t] += bv[t] * (ev[t] * ts + rq) - cy;
     }
@@ -814,7 +831,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       for (int which = 0; which < 2; ++which) {
         const uint32_t acc = which ? tdK : tdQ;
         const uint8_t* xt = which ? tK : tQ;   // x_hat tiles [C][Dk]
-        for (int q = half; q * 16 < Dk; q += 2) {
+        for (int q = grp; q * 16 < Dk; q += kGroups) {
           float x[16];
           tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
           tc::tmem_ld_wait();
@@ -827,8 +844,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
         }
       }
       if (row64 >= 0) {
-        part[half * C + row64] = dot[0];
-        rowp[half * C + row64] = dot[1];
+        part[grp * C + row64] = dot[0];
+        rowp[grp * C + row64] = dot[1];
       }
     }
     __syncthreads();
@@ -840,13 +857,13 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       __nv_bfloat16* dst = (__nv_bfloat16*)(which ? p.dk : p.dq) +
                            t0 * (which ? p.dk_ld : p.dq_ld) + (int64_t)kh * Dk;
       const int64_t ld = which ? p.dk_ld : p.dq_ld;
-      for (int q = half; q * 16 < Dk; q += 2) {
+      for (int q = grp; q * 16 < Dk; q += kGroups) {
         float x[16];
         tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
         tc::tmem_ld_wait();
         if (row64 >= 0 && row64 < len) {
           const int r = row64;
-          const float d = pr[r] + pr[C + r], inv = invn[which * C + r];
+          const float d = rsum_g(pr, r), inv = invn[which * C + r];
           __align__(16) __nv_bfloat162 pk[8];
           float xv[16];
           tile_get16(xt, C, r, q * 16, xv);
@@ -868,7 +885,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   tc::fence_after_sync();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
+__global__ void __launch_bounds__(kTcThreads, 1) k_bwd_grads_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   if (kept_operands_missing(p)) return;
   extern __shared__ uint8_t smem_raw[];
@@ -888,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_grads_tc(Params p,
 // flags, and every walk joins them when it is done.  Walks never wait on gradient
 // units, so the launch always finishes.
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 1) k_bwd_fused_tc(Params p,
+__global__ void __launch_bounds__(kTcThreads, 1) k_bwd_fused_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   if (kept_operands_missing(p)) return;
   extern __shared__ uint8_t smem_raw[];
@@ -959,7 +976,8 @@ static size_t bwd_state_tc_smem(const Params& p) {
          1024;
 }
 static size_t grads_tc_smem() {
-  return 66560 + 32768 + 49152 + 32768 + 32768 + (size_t)(18 * C + 8) * 4 + kCtlBytes + 1024;
+  return 66560 + 32768 + 49152 + 32768 + 32768 +
+         (size_t)((9 + 2 * kGroups + kColParts) * C + kTcThreads / 32) * 4 + kCtlBytes + 1024;
 }
 
 template <int DK>
@@ -967,7 +985,7 @@ static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, c
   const size_t smem = bwd_state_tc_smem<DK>(p);
   cudaFuncSetAttribute(k_bwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_BWD_STATE_TC);
-  k_bwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kThreads, smem, st>>>(p, maps);
+  k_bwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kTcThreads, smem, st>>>(p, maps);
   profile_post(st);
   return cudaGetLastError();
 }
@@ -987,14 +1005,14 @@ static cudaError_t launch_bwd_fused_t(const Params& p, const TmaMaps& maps, cuda
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bwd_fused_tc<DK>, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bwd_fused_tc<DK>, kTcThreads, smem);
   if (e != cudaSuccess || per_sm < 1) return cudaSuccess;
   Params pp = p;
   pp.bready = p.bwork + 64;   // the work counter's 256-byte slot, then the flags
   TmaMaps mm = maps;
   void* args[] = {&pp, &mm};
   profile_pre(st, KID_BWD_FUSED_TC);
-  e = cudaLaunchCooperativeKernel((const void*)k_bwd_fused_tc<DK>, dim3(sms), dim3(kThreads), args,
+  e = cudaLaunchCooperativeKernel((const void*)k_bwd_fused_tc<DK>, dim3(sms), dim3(kTcThreads), args,
                                   smem, st);
   profile_post(st);
   if (e == cudaSuccess) *launched = true;
@@ -1024,7 +1042,7 @@ cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st)
     const size_t smem = grads_tc_smem();
     cudaFuncSetAttribute(k_bwd_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     profile_pre(st, KID_BWD_GRADS_TC);
-    k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, maps);
+    k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kTcThreads, smem, st>>>(p, maps);
     profile_post(st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

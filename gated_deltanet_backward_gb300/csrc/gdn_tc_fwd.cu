@@ -68,13 +68,13 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
   // runs all its 1 x 4 tiles together over the whole k range (the zero triangles
   // add exact zeros), so its accumulators form independent chains.
   {
-    constexpr int kMax = (RB * 2 * 16 * 4 + kThreads - 1) / kThreads;   // tiles per thread
+    constexpr int kMax = (RB * 2 * 16 * 4 + kTcThreads - 1) / kTcThreads;   // tiles per thread
     const int n1 = nh * 2 * 16 * 4;
     float4 acc[kMax];
     int off_a[kMax], off_b[kMax];
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kThreads;
+      const int it = tid + j * kTcThreads;
       const int pr = it < n1 ? it >> 6 : 0, r = (it >> 2) & 15, c0 = (it & 3) * 4;
       const int rb = ((pr & 1) * 2 + 1) * 16, cb = rb - 16;
       off_a[j] = (pr >> 1) * C * TS + (rb + r) * TS + cb;          // row r of A_10
@@ -94,13 +94,13 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
       }
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kThreads;
+      const int it = tid + j * kTcThreads;
       if (it < n1) *(float4*)(M + (it >> 6) * 256 + ((it >> 2) & 15) * 16 + (it & 3) * 4) = acc[j];
     }
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kThreads;
+      const int it = tid + j * kTcThreads;
       const int pr = it < n1 ? it >> 6 : 0, r = (it >> 2) & 15;
       const int rb = ((pr & 1) * 2 + 1) * 16;
       off_a[j] = (pr >> 1) * C * TS + (rb + r) * TS + rb;          // row r of D_1
@@ -120,7 +120,7 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
       }
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kThreads;
+      const int it = tid + j * kTcThreads;
       if (it < n1) {
         const int pr = it >> 6, r = (it >> 2) & 15, c0 = (it & 3) * 4;
         const int rb = ((pr & 1) * 2 + 1) * 16, cb = rb - 16;
@@ -132,13 +132,13 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
   }
   // 64x64: M = A_BA T_A, then lower-left = -T_B M (same scheme, k over 32)
   {
-    constexpr int kMax = (RB * 32 * 8 + kThreads - 1) / kThreads;
+    constexpr int kMax = (RB * 32 * 8 + kTcThreads - 1) / kTcThreads;
     const int n2 = nh * 32 * 8;
     float4 acc[kMax];
     int off_a[kMax], off_b[kMax];
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kThreads;
+      const int it = tid + j * kTcThreads;
       const int hh = it < n2 ? it >> 8 : 0, r = (it >> 3) & 31, c0 = (it & 7) * 4;
       off_a[j] = hh * C * TS + (32 + r) * TS;                      // row r of A_BA
       off_b[j] = hh * C * TS + c0;                                 // column piece of T_A
@@ -157,13 +157,13 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
       }
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kThreads;
+      const int it = tid + j * kTcThreads;
       if (it < n2) *(float4*)(M + (it >> 8) * 1024 + ((it >> 3) & 31) * 32 + (it & 7) * 4) = acc[j];
     }
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kThreads;
+      const int it = tid + j * kTcThreads;
       const int hh = it < n2 ? it >> 8 : 0, r = (it >> 3) & 31;
       off_a[j] = hh * C * TS + (32 + r) * TS + 32;                 // row r of T_B
       off_b[j] = hh * 1024 + (it & 7) * 4;                         // column piece of M
@@ -182,7 +182,7 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
       }
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kThreads;
+      const int it = tid + j * kTcThreads;
       if (it < n2) {
         const int hh = it >> 8, r = (it >> 3) & 31, c0 = (it & 7) * 4;
         *(float4*)(Tm + hh * C * TS + (32 + r) * TS + c0) =
@@ -233,7 +233,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
 
   // W's padding columns (Dk < 64) stay zero: the epilogue writes only columns < Dk
   if (Dk < 64)
-    for (int i = tid; i < (int)bKC / 16; i += kThreads) ((uint4*)tW)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < (int)bKC / 16; i += kTcThreads) ((uint4*)tW)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   // TMEM columns: [0, 64) the Gram products, [64, 64 + NK) W, [192, 256) U^T
   const uint32_t tAccW = tmem + 64, tAccU = tmem + 192;
@@ -267,17 +267,18 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   }
   if (!ok) goto done;
 
-  // 1. L2 normalisation in place, two threads per row (K rows 0-63, Q rows 64-127),
-  // each with its half of the row's 16-byte pieces in registers; rows past the chunk
-  // become zero
+  // 1. L2 normalisation in place, four threads per row (K rows 0-63, Q rows 64-127),
+  // each with its share of the row's 16-byte pieces in registers; rows past the
+  // chunk become zero
   {
-    const int row = tid >> 1, part = tid & 1, cpt = Dk / 16;
+    const int row = tid >> 2, part = tid & 3;
+    const int nch = Dk / 8, tpr = nch < 4 ? nch : 4, cpt = part < tpr ? nch / tpr : 0;
     const bool isq = row >= C;
     const int t = row & (C - 1);
-    uint4 raw[8];
+    uint4 raw[4];
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < 4; ++j)
       if (j < cpt) {
         raw[j] = *(const uint4*)(tAQK + tc::sw128_offset(row, (part * cpt + j) * 8, 128));
         const __nv_bfloat162* e = (const __nv_bfloat162*)&raw[j];
@@ -288,9 +289,10 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
         }
       }
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
     const float nrm = sqrtf(ss + 1e-6f), inv = t < len ? 1.f / nrm : 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < 4; ++j)
       if (j < cpt) {
         const __nv_bfloat162* e = (const __nv_bfloat162*)&raw[j];
         __align__(16) __nv_bfloat162 pk[4];
@@ -305,7 +307,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
     // Dk < 64: the box's columns past Dk (a neighbouring head) become zero padding
     if (Dk < 64) {
       const int padc = 8 - Dk / 8;
-      for (int idx = tid; idx < 2 * C * padc; idx += kThreads) {
+      for (int idx = tid; idx < 2 * C * padc; idx += kTcThreads) {
         const int row = idx / padc, c0 = (Dk / 8 + idx % padc) * 8;
         *(uint4*)(tAQK + tc::sw128_offset(row, c0, 128)) = make_uint4(0, 0, 0, 0);
       }
@@ -381,7 +383,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       p.b[ch * C + t] = bv[hh * C + t];
     }
     // A = diag(b) (E * K K^T), strictly lower, four columns per step
-    for (int idx = tid; idx < nh * C * (C / 4); idx += kThreads) {
+    for (int idx = tid; idx < nh * C * (C / 4); idx += kTcThreads) {
       const int hh = idx / (C * C / 4), e4 = idx % (C * C / 4), r = e4 / (C / 4), s0 = (e4 % (C / 4)) * 4;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
       if (s0 < r) {
@@ -416,7 +418,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       const float* bb = bv + hh * C;
       const float* G = gv + hh * C;
       // T diag(w), T diag(b), P and (backward) T: one pass over 8-column pieces
-      for (int idx = tid; idx < C * (C / 8); idx += kThreads) {
+      for (int idx = tid; idx < C * (C / 8); idx += kTcThreads) {
         const int r = idx % C, s8 = (idx / C) * 8;
         const float4 ta = *(const float4*)(T + r * TS + s8);
         const float4 tb = *(const float4*)(T + r * TS + s8 + 4);
@@ -451,7 +453,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       }
       // rows of the V tile past the chunk (another sequence's tokens) read as zero
       if (len < C)
-        for (int idx = tid; idx < nbv * (C - len) * 8; idx += kThreads) {
+        for (int idx = tid; idx < nbv * (C - len) * 8; idx += kTcThreads) {
           const int b2 = idx / ((C - len) * 8), rem = idx % ((C - len) * 8);
           ((uint4*)(sV + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
         }
@@ -493,7 +495,7 @@ done:
   return ok;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_prep_tc(Params p,
+__global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
                                                           const __grid_constant__ TmaMaps maps,
                                                           int bwd) {
   stamp_kept_operands(p);
@@ -522,10 +524,10 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, n);
     return;
   }
-  constexpr int NKC = (DK + 31) / 32;          // 16-column pieces of S^T per thread
+  constexpr int NKC = (DK + 16 * kGroups - 1) / (16 * kGroups);   // S^T pieces per thread
   constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read K MN-major
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
-  const int tid = threadIdx.x, warp = tid >> 5, half = tid >> 7;
+  const int tid = threadIdx.x, grp = col_group();
   const uint32_t bW = (uint32_t)tileCD(DK), bP = 8192;
   const uint32_t bU = (uint32_t)Dv * C * 2, bG = C * 4;
   const uint32_t bSt = tc::sw128_bytes(MV, DK);       // one saved S^T tile
@@ -543,9 +545,9 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   auto sU = [&](int b) { return (const __nv_bfloat16*)(buf0 + b * bufsz + 3 * bW + bP); };
   auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + 3 * bW + bP + bU); };
 
-  for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) / 16); i += kThreads)
+  for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) / 16); i += kTcThreads)
     ((uint4*)tSt)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < MV * 128 * 2 / 16; i += kThreads) ((uint4*)tDt)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < MV * 128 * 2 / 16; i += kTcThreads) ((uint4*)tDt)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   // TMEM: X = S^T W^T @0, state update @64, and the output in token rows (M = 64):
   // Q S @256, P Delta @384 (they survive into the next chunk's first product)
@@ -561,12 +563,13 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   for (int i = 0; i < NKC; ++i)
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const int k = half * 16 + 32 * i + j;
+      const int k = grp * 16 + 16 * kGroups * i + j;
       S[i][j] = (vok && k < DK && p.S0) ? p.S0[((size_t)n * p.Hv + h) * SZ + (size_t)k * Dv + vrow] : 0.f;
     }
 #pragma unroll
   for (int i = 0; i < NKC; ++i)
-    if (half * 16 + 32 * i < DK && vok) tile_put16(tSt, MV, vrow, half * 16 + 32 * i, S[i]);
+    if (grp * 16 + 16 * kGroups * i < DK && vok)
+      tile_put16(tSt, MV, vrow, grp * 16 + 16 * kGroups * i, S[i]);
   tc::fence_async_smem();
 
   auto issue_load = [&](int cc, int b) {
@@ -649,8 +652,8 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
     // Delta^T = U^T - X^T and Delta^T diag(c)
     const uint8_t* U = (const uint8_t*)sU(b);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int col0 = half * 16 + 32 * q;
+    for (int q = 0; q < C / (16 * kGroups); ++q) {
+      const int col0 = grp * 16 + 16 * kGroups * q;
       float x[16];
       tc::tmem_ld16(tX + lane_quarter() + col0, x);
       tc::tmem_ld_wait();
@@ -692,7 +695,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
     const float eC = ev[len - 1];
 #pragma unroll
     for (int ii = 0; ii < NKC; ++ii) {
-      const int col0 = half * 16 + 32 * ii;
+      const int col0 = grp * 16 + 16 * kGroups * ii;
       if (col0 < DK) {
         float x[16];
         tc::tmem_ld16(tS + lane_quarter() + col0, x);
@@ -715,7 +718,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
     {
       const int r = acc_row(64);
       __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + (r < 0 ? 0 : r)) * p.o_ld + (int64_t)h * Dv;
-      for (int q = half; q * 16 < Dv; q += 2) {
+      for (int q = grp; q * 16 < Dv; q += kGroups) {
         float o1[16], o2[16];
         tc::tmem_ld16(tO1 + lane_quarter() + q * 16, o1);
         tc::tmem_ld16(tO2 + lane_quarter() + q * 16, o2);
@@ -737,15 +740,16 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   if (ok && p.S_T && vok)
 #pragma unroll
     for (int ii = 0; ii < NKC; ++ii)
-      if (half * 16 + 32 * ii < DK)
+      if (grp * 16 + 16 * kGroups * ii < DK)
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          p.S_T[((size_t)n * p.Hv + h) * SZ + (size_t)(half * 16 + 32 * ii + j) * Dv + vrow] = S[ii][j];
+          p.S_T[((size_t)n * p.Hv + h) * SZ + (size_t)(grp * 16 + 16 * kGroups * ii + j) * Dv +
+                vrow] = S[ii][j];
   if (tid == 0) tc::bulk_wait<0>();
 }
 
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
+__global__ void __launch_bounds__(kTcThreads, 1) k_fwd_state_tc(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
@@ -760,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_state_tc(Params p) {
 // counter, and publish each one's flag; a walk waits for the flag of the chunk it
 // needs next.  Walks never block the preparation, so the launch always finishes.
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 1) k_fwd_fused_tc(Params p,
+__global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   stamp_kept_operands(p);
   extern __shared__ uint8_t smem_raw[];
@@ -817,7 +821,7 @@ cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaS
   const size_t smem = prep_tc_smem(p);
   cudaFuncSetAttribute(k_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, bwd ? KID_PREP_TC_FULL : KID_PREP_TC);
-  k_prep_tc<<<dim3(p.NC, p.Hk), kThreads, smem, st>>>(p, maps, bwd ? 1 : 0);
+  k_prep_tc<<<dim3(p.NC, p.Hk), kTcThreads, smem, st>>>(p, maps, bwd ? 1 : 0);
   profile_post(st);
   return cudaGetLastError();
 }
@@ -827,7 +831,7 @@ static cudaError_t launch_fwd_state_tc_t(const Params& p, cudaStream_t st) {
   const size_t smem = fwd_state_tc_smem<DK>(p);
   cudaFuncSetAttribute(k_fwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_FWD_STATE_TC);
-  k_fwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kThreads, smem, st>>>(p);
+  k_fwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kTcThreads, smem, st>>>(p);
   profile_post(st);
   return cudaGetLastError();
 }
@@ -858,14 +862,14 @@ static cudaError_t launch_fwd_fused_t(const Params& p, const TmaMaps& maps, cuda
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_fused_tc<DK>, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_fused_tc<DK>, kTcThreads, smem);
   if (e != cudaSuccess || per_sm < 1) return cudaSuccess;
   Params pp = p;
   pp.fready = p.fwork + 64;   // the work counter's 256-byte slot, then the flags
   TmaMaps mm = maps;
   void* args[] = {&pp, &mm};
   profile_pre(st, KID_FWD_FUSED_TC);
-  e = cudaLaunchCooperativeKernel((const void*)k_fwd_fused_tc<DK>, dim3(sms), dim3(kThreads), args,
+  e = cudaLaunchCooperativeKernel((const void*)k_fwd_fused_tc<DK>, dim3(sms), dim3(kTcThreads), args,
                                   smem, st);
   profile_post(st);
   if (e == cudaSuccess) *launched = true;
