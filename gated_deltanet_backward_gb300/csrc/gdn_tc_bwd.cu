@@ -344,73 +344,97 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   float* part = xa + C;       // [kGroups][C] per-group partial row sums
   float* rowp = part + kGroups * C;  // [kGroups][C] per-group partial row sums
   float* colp = rowp + kGroups * C;  // [kColParts][C] partial column sums
-  float* invn = colp + kColParts * C;  // [2][C] 1 / |q|, 1 / |k| of the chunk's tokens
-  float* red = invn + 2 * C;  // [kTcThreads / 32]
+  float* invn = colp + kColParts * C;  // [2][C] |q|, |k| of the chunk's tokens
+  float* al = invn + 2 * C;   // a_log of the value head, one copy per token slot
+  float* stg = al + C;        // [2][5][C] next value head's G, beta, alpha, dt_bias, a_log
+  float* red = stg + 10 * C;  // [kTcThreads / 32]
 
   const uint32_t tdQ = tmem, tdK = tmem + 128, tmp = tmem + 256;
   const size_t ckk = (size_t)c * p.Hk + kh;
   const int row64 = acc_row(64);
   bool ok = true;
 
-  // fused launch: this chunk's dS^T / -dDelta tiles of every value head of the group
-  if (tid == 0 && p.bready)
-    for (int hh = 0; hh < p.r; ++hh)
-      if (!wait_flag(p.bready + (size_t)c * p.Hv + kh * p.r + hh))
-        set_status(p.status, GDN_ERR_TIMEOUT, c);
-  // the norms for the L2 backward at the end
-  if (tid < 2 * C) invn[tid] = 1.f / (tid < C ? p.nq : p.nk)[ckk * C + (tid & (C - 1))];
-  // key-head tiles for the whole CTA
-  if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&bars[1], 2 * sCK);
-    tc::bulk_g2s(tK, p.Ksw + ckk * sCK, sCK, &bars[1]);
-    tc::bulk_g2s(tQ, p.Qsw + ckk * sCK, sCK, &bars[1]);
-  }
-  {
-    // K K^T of the key head into padded rows (conflict-free row reads in epilogue D)
-    const float4* KK = (const float4*)(p.KKf + ckk * C * C);
-    for (int i = tid; i < C * C / 4; i += kTcThreads)
-      *(float4*)(sKK + (i / (C / 4)) * KKL + (i % (C / 4)) * 4) = KK[i];
-  }
-  {
-    const bool lok = tc::mbar_wait(&bars[1], lphase);
-    lphase ^= 1u;
-    if (__syncthreads_or(lok ? 0 : 1)) {
-      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
-      ok = false;
-    }
-  }
-
-  // S^T, W, U^T (bulk copies), dO rows into the [dO; -dDelta] tile and V rows (TMA),
-  // -dDelta rows (bulk) of value head h
-  auto issue_phase_a = [&](int h) {
+  // Phase A's tiles of value head h: S^T, W, U^T (bulk copies), dO rows into the
+  // [dO; -dDelta] tile and V rows (TMA) need nothing from the reverse walks; the
+  // -dDelta rows (bulk) are the walk's and wait for its flag.  All land in one phase
+  // of bars[1] of phase_a_bytes.
+  const int nbv = (Dv + 63) / 64;
+  const uint32_t phase_a_bytes = sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u + bSt;
+  auto issue_phase_a_inputs = [&](int h) {
     const size_t ch = (size_t)c * p.Hv + h;
-    const int nbv = (Dv + 63) / 64;
-    tc::mbar_arrive_expect_tx(&bars[1], sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u + bSt);
     tc::bulk_g2s(tSt, (const uint8_t*)p.saved_in + ch * bSt, bSt, &bars[1]);
     tc::bulk_g2s(tW, p.Wsw + ch * sCK, sCK, &bars[1]);
     tc::bulk_g2s(sU, p.Utb + ch * Dv * C, (uint32_t)Dv * C * 2, &bars[1]);
     for (int b = 0; b < nbv; ++b) {
       tc::tma_load_2d(tA2 + b * 16384, &maps.dO, h * Dv + 64 * b, (int)t0, &bars[1]);
       tc::tma_load_2d(tV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bars[1]);
-      tc::bulk_g2s(tA2 + b * 16384 + 8192, p.dDb + ch * sCV + b * 8192, 8192, &bars[1]);
     }
   };
+  auto issue_phase_a_walk = [&](int h) {
+    const size_t ch = (size_t)c * p.Hv + h;
+    for (int b = 0; b < nbv; ++b)
+      tc::bulk_g2s(tA2 + b * 16384 + 8192, p.dDb + ch * sCV + b * 8192, 8192, &bars[1]);
+  };
+  // G, beta, alpha, dt_bias and a_log of value head h into staging buffer h & 1 (token
+  // slot tid; the alpha rows past the chunk are not read)
+  auto prefetch_vectors = [&](int hh) {
+    if (tid < C) {
+      const int h = kh * p.r + hh;
+      const size_t ch = (size_t)c * p.Hv + h;
+      float* sg = stg + (hh & 1) * 5 * C;
+      tc::cp_async4(sg + tid, p.G + ch * C + tid);
+      tc::cp_async4(sg + C + tid, p.b + ch * C + tid);
+      if (tid < len) tc::cp_async4(sg + 2 * C + tid, p.alpha + (t0 + tid) * p.alpha_ld + h);
+      tc::cp_async4(sg + 3 * C + tid, p.dt_bias + h);
+      tc::cp_async4(sg + 4 * C + tid, p.a_log + h);
+    }
+  };
+
+  // K, Q of the key head and the first value head's phase-A tiles in one phase of
+  // bars[1]; the copies that need no walk start before the flags are read
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bars[1], 2 * sCK + phase_a_bytes);
+    tc::bulk_g2s(tK, p.Ksw + ckk * sCK, sCK, &bars[1]);
+    tc::bulk_g2s(tQ, p.Qsw + ckk * sCK, sCK, &bars[1]);
+    issue_phase_a_inputs(kh * p.r);
+  }
+  // K K^T of the key head into padded rows (conflict-free row reads in epilogue D),
+  // the norms for the L2 backward at the end and the first head's vectors
+  for (int i = tid; i < C * C / 4; i += kTcThreads)
+    tc::cp_async16(sKK + (i / (C / 4)) * KKL + (i % (C / 4)) * 4, p.KKf + ckk * C * C + i * 4);
+  if (tid < 2 * C) tc::cp_async4(invn + tid, (tid < C ? p.nq : p.nk) + ckk * C + (tid & (C - 1)));
+  prefetch_vectors(0);
+  // fused launch: this chunk's dS^T / -dDelta tiles of every value head of the group
+  // (one thread per value head)
+  if (p.bready) {
+    for (int hh = tid; hh < p.r; hh += kTcThreads)
+      if (!wait_flag(p.bready + (size_t)c * p.Hv + kh * p.r + hh))
+        set_status(p.status, GDN_ERR_TIMEOUT, c);
+    __syncthreads();
+  }
+  if (tid == 0) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    issue_phase_a_walk(kh * p.r);
+  }
   for (int hh = 0; hh < p.r && ok; ++hh) {
     const int h = kh * p.r + hh;
     const size_t ch = (size_t)c * p.Hv + h;
     const uint32_t acc_first = hh > 0 ? 1u : 0u;
     const uint8_t* Sg = (const uint8_t*)p.saved_in + ch * bSt;   // S^T tile
+    // this head's vectors (prefetched), then the next head's prefetch
+    tc::cp_async_wait_all();
     if (tid < C) {
-      const float g = p.G[ch * C + tid];
-      gv[tid] = g;
-      bv[tid] = p.b[ch * C + tid];
-      xa[tid] = tid < len ? p.alpha[(t0 + tid) * p.alpha_ld + h] + p.dt_bias[h] : 0.f;
+      const float* sg = stg + (hh & 1) * 5 * C;
+      gv[tid] = sg[tid];
+      bv[tid] = sg[C + tid];
+      xa[tid] = tid < len ? sg[2 * C + tid] + sg[3 * C + tid] : 0.f;
+      al[tid] = sg[4 * C + tid];
       dG[tid] = 0.f;
       db[tid] = 0.f;
     }
-    // phase A's tiles: the first head issues its own; every later head's were issued
-    // when the previous head's last product finished
-    if (tid == 0 && hh == 0) issue_phase_a(h);
+    if (hh + 1 < p.r) prefetch_vectors(hh + 1);
+    // phase A's tiles were issued at the start of the unit (first head) or when the
+    // previous head's last product finished
     __syncthreads();
     if (tid < C) {
       ev[tid] = expf(gv[tid]);
@@ -777,7 +801,11 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     if (!ok) break;
     // every tile region but K, Q and K K^T is free: the next head's phase A loads run
     // under the gate epilogue
-    if (tid == 0 && hh + 1 < p.r) issue_phase_a(h + 1);
+    if (tid == 0 && hh + 1 < p.r) {
+      tc::mbar_arrive_expect_tx(&bars[1], phase_a_bytes);
+      issue_phase_a_inputs(h + 1);
+      issue_phase_a_walk(h + 1);
+    }
     // gate and sigmoid epilogues: dl = reverse cumsum of dG (one warp, two per lane)
     __syncthreads();
     if (warp == 0) {
@@ -798,7 +826,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       if (tid < len) {
         const int t = tid;
         const float x = xa[t];
-        const float ea = expf(p.a_log[h]);
+        const float ea = expf(al[t]);
         const float l = -ea * softplus_f(x);
         const float dl = part[t];
         const float da = dl * (-ea) * sigmoid_f(x);
@@ -809,6 +837,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       }
       pa = warp_sum(pa);
       pd = warp_sum(pd);
+      // every read of the scan's sums in part is done past this barrier
       __syncthreads();
       if (tid < C && (tid & 31) == 0) {
         red[tid >> 5] = pa;
@@ -819,7 +848,6 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
         p.pa[ch] = red[0] + red[1];
         p.pd[ch] = red[2] + red[3];
       }
-      __syncthreads();
     }
   }
   // dq, dk of the key head: L2-norm backward of the accumulated dQ_hat, dK_hat,
@@ -863,7 +891,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
         tc::tmem_ld_wait();
         if (row64 >= 0 && row64 < len) {
           const int r = row64;
-          const float d = rsum_g(pr, r), inv = invn[which * C + r];
+          const float d = rsum_g(pr, r), inv = 1.f / invn[which * C + r];
           __align__(16) __nv_bfloat162 pk[8];
           float xv[16];
           tile_get16(xt, C, r, q * 16, xv);
@@ -880,6 +908,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       }
     }
   }
+  tc::cp_async_wait_all();   // a unit that stopped early leaves no copy in flight
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -977,7 +1006,7 @@ static size_t bwd_state_tc_smem(const Params& p) {
 }
 static size_t grads_tc_smem() {
   return 66560 + 32768 + 49152 + 32768 + 32768 +
-         (size_t)((9 + 2 * kGroups + kColParts) * C + kTcThreads / 32) * 4 + kCtlBytes + 1024;
+         (size_t)((20 + 2 * kGroups + kColParts) * C + kTcThreads / 32) * 4 + kCtlBytes + 1024;
 }
 
 template <int DK>

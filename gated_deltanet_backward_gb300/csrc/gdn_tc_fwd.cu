@@ -35,8 +35,8 @@ constexpr int TS = C + 4;   // row stride (floats) of the fp32 [C][C] matrices o
 //   16x16 diagonal blocks D_b = (I + A_bb)^-1   (forward substitution, a column per thread)
 //   32x32 diagonal blocks: lower-left 16x16 = -D_1 A_10 D_0
 //   64x64: lower-left 32x32 = -T_B A_BA T_A (T_A, T_B the 32x32 diagonal inverses)
-// Each product runs as 1 x 4 register tiles (one row, four columns per thread)
-// and skips the zero triangles.  Scratch M: nh * 1024 floats.
+// The 32x32 level runs 1 x 4 register tiles (one row, four columns per thread), the
+// 64x64 level 4 x 4 tiles on 2 nh warps.  Scratch M: nh * 1024 floats.
 __device__ void tri_inverse(float* Tm, int nh, float* M) {
   const int tid = threadIdx.x;
   // 16x16 diagonal blocks: 16 threads per (head, block), thread j solves column j
@@ -130,64 +130,56 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
     }
     __syncthreads();
   }
-  // 64x64: M = A_BA T_A, then lower-left = -T_B M (same scheme, k over 32)
+  // 64x64: M = A_BA T_A, then lower-left = -T_B M.  Warp w < 2 nh owns a 32 x 16
+  // piece of head w / 2 (columns 16 (w % 2) ...); a thread holds the 4 x 4 tile of rows
+  // rg + 8i (i < 4) and columns 4 cg ... 4 cg + 3, so a k step costs four broadcast
+  // row loads (distinct banks) and one 16-byte column load for 16 FMAs.  T_A is lower
+  // triangular: the right half's product starts at k = 16.
   {
-    constexpr int kMax = (RB * 32 * 8 + kTcThreads - 1) / kTcThreads;
-    const int n2 = nh * 32 * 8;
-    float4 acc[kMax];
-    int off_a[kMax], off_b[kMax];
+    const int w = tid >> 5, l = tid & 31, rg = l >> 2, cg = l & 3;
+    const bool act = w < 2 * nh;
+    const int hh = act ? w >> 1 : 0, cb = (w & 1) * 16 + cg * 4;
+    const float* Th = Tm + hh * C * TS;
+    float* Mh = M + hh * 1024;
+    float4 acc[4];
+    if (act) {
 #pragma unroll
-    for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kTcThreads;
-      const int hh = it < n2 ? it >> 8 : 0, r = (it >> 3) & 31, c0 = (it & 7) * 4;
-      off_a[j] = hh * C * TS + (32 + r) * TS;                      // row r of A_BA
-      off_b[j] = hh * C * TS + c0;                                 // column piece of T_A
-      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+      for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (int k = 0; k < 32; ++k)
+      for (int k = (w & 1) * 16; k < 32; ++k) {
+        const float4 t = *(const float4*)(Th + k * TS + cb);
 #pragma unroll
-      for (int j = 0; j < kMax; ++j) {
-        const float a = Tm[off_a[j] + k];
-        const float4 t = *(const float4*)(Tm + off_b[j] + k * TS);
-        acc[j].x = fmaf(a, t.x, acc[j].x);
-        acc[j].y = fmaf(a, t.y, acc[j].y);
-        acc[j].z = fmaf(a, t.z, acc[j].z);
-        acc[j].w = fmaf(a, t.w, acc[j].w);
+        for (int i = 0; i < 4; ++i) {
+          const float a = Th[(32 + rg + 8 * i) * TS + k];
+          acc[i].x = fmaf(a, t.x, acc[i].x);
+          acc[i].y = fmaf(a, t.y, acc[i].y);
+          acc[i].z = fmaf(a, t.z, acc[i].z);
+          acc[i].w = fmaf(a, t.w, acc[i].w);
+        }
       }
 #pragma unroll
-    for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kTcThreads;
-      if (it < n2) *(float4*)(M + (it >> 8) * 1024 + ((it >> 3) & 31) * 32 + (it & 7) * 4) = acc[j];
+      for (int i = 0; i < 4; ++i) *(float4*)(Mh + (rg + 8 * i) * 32 + cb) = acc[i];
     }
     __syncthreads();
+    if (act) {
 #pragma unroll
-    for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kTcThreads;
-      const int hh = it < n2 ? it >> 8 : 0, r = (it >> 3) & 31;
-      off_a[j] = hh * C * TS + (32 + r) * TS + 32;                 // row r of T_B
-      off_b[j] = hh * 1024 + (it & 7) * 4;                         // column piece of M
-      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+      for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (int k = 0; k < 32; ++k)
+      for (int k = 0; k < 32; ++k) {
+        const float4 m = *(const float4*)(Mh + k * 32 + cb);
 #pragma unroll
-      for (int j = 0; j < kMax; ++j) {
-        const float t = Tm[off_a[j] + k];
-        const float4 m = *(const float4*)(M + off_b[j] + k * 32);
-        acc[j].x = fmaf(t, m.x, acc[j].x);
-        acc[j].y = fmaf(t, m.y, acc[j].y);
-        acc[j].z = fmaf(t, m.z, acc[j].z);
-        acc[j].w = fmaf(t, m.w, acc[j].w);
+        for (int i = 0; i < 4; ++i) {
+          const float t = Th[(32 + rg + 8 * i) * TS + 32 + k];
+          acc[i].x = fmaf(t, m.x, acc[i].x);
+          acc[i].y = fmaf(t, m.y, acc[i].y);
+          acc[i].z = fmaf(t, m.z, acc[i].z);
+          acc[i].w = fmaf(t, m.w, acc[i].w);
+        }
       }
 #pragma unroll
-    for (int j = 0; j < kMax; ++j) {
-      const int it = tid + j * kTcThreads;
-      if (it < n2) {
-        const int hh = it >> 8, r = (it >> 3) & 31, c0 = (it & 7) * 4;
-        *(float4*)(Tm + hh * C * TS + (32 + r) * TS + c0) =
-            make_float4(-acc[j].x, -acc[j].y, -acc[j].z, -acc[j].w);
-      }
+      for (int i = 0; i < 4; ++i)
+        *(float4*)(Tm + hh * C * TS + (32 + rg + 8 * i) * TS + cb) =
+            make_float4(-acc[i].x, -acc[i].y, -acc[i].z, -acc[i].w);
     }
     __syncthreads();
   }
