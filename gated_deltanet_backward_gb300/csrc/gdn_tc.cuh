@@ -105,6 +105,48 @@ __device__ __forceinline__ void acc_walk(uint32_t tmem, int M, int N, int valid,
   }
 }
 
+// M = 64 accumulators read with the 16x32bx2 loads, which hand both halves of a warp
+// the quarter's 16 live lanes: thread t of warp w holds row 16 (w % 4) + (t % 16), and
+// threads 16-31 take the second column piece of each load.
+__device__ __forceinline__ int x2_row() {
+  return 16 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 15);
+}
+__device__ __forceinline__ int x2_half() { return (threadIdx.x >> 4) & 1; }
+
+// Walks the columns [0, N) of an M = 64 accumulator in 16-column pieces, two per load:
+// the kGroups warps of a lane quarter take pieces grp + 2 kGroups i (threads 0-15) and
+// grp + kGroups (2i + 1) (threads 16-31).  f(row, col0, v[16]) runs for rows < valid.
+// The loads may read up to 16 kGroups + 15 columns past N (allocated TMEM, ignored).
+// Whole warps must call this.
+template <class F>
+__device__ __forceinline__ void acc_walk64(uint32_t tmem, int N, int valid, F f) {
+  const int row = x2_row(), half = x2_half();
+  for (int c = col_group() * 16; c < N; c += 32 * kGroups) {
+    float v[16];
+    tc::tmem_ld16_x2<16 * kGroups>(tmem + lane_quarter() + (uint32_t)c, v);
+    tc::tmem_ld_wait();
+    const int col = c + half * 16 * kGroups;
+    if (row < valid && col < N) f(row, col, v);
+  }
+}
+// As acc_walk64 in 8-column halves of each warp's 16-column piece (for N <= 16 kGroups):
+// threads 0-15 take columns [c, c + 8), threads 16-31 [c + 8, c + 16); f(row, col0, v[8]).
+template <class F>
+__device__ __forceinline__ void acc_walk64_8(uint32_t tmem, int N, int valid, F f) {
+  const int row = x2_row(), half = x2_half();
+  for (int c = col_group() * 16; c < N; c += 16 * kGroups) {
+    float v[8];
+    tc::tmem_ld8_x2<8>(tmem + lane_quarter() + (uint32_t)c, v);
+    tc::tmem_ld_wait();
+    const int col = c + half * 8;
+    if (row < valid && col < N) f(row, col, v);
+  }
+}
+// Sum of a per-thread value over the two threads that hold the same x2 row.
+__device__ __forceinline__ float x2_pair_sum(float v) {
+  return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
+
 // Stages a bf16 K-major SW128 tile of rows x cols (cols a multiple of 8) from
 // f(r, c) -> float, 8 elements (one 16-byte store) per step.
 template <class F>
@@ -234,6 +276,20 @@ __device__ __forceinline__ void tile_get16(const uint8_t* tile, int rows, int r,
     v[j] = __bfloat162float(ea[j]);
     v[8 + j] = __bfloat162float(eb[j]);
   }
+}
+
+// 8 consecutive elements (c0 a multiple of 8): one 16-byte chunk of a SW128 bf16 tile.
+__device__ __forceinline__ void tile_put8(uint8_t* tile, int rows, int r, int c0, const float* v) {
+  __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) pk[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+  *(uint4*)(tile + tc::sw128_offset(r, c0, rows)) = *(const uint4*)pk;
+}
+__device__ __forceinline__ void tile_get8(const uint8_t* tile, int rows, int r, int c0, float* v) {
+  const uint4 a = *(const uint4*)(tile + tc::sw128_offset(r, c0, rows));
+  const __nv_bfloat16* ea = (const __nv_bfloat16*)&a;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __bfloat162float(ea[j]);
 }
 
 // Reads one bf16 element of a K-major SW128 tile as float.

@@ -174,13 +174,15 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
     // dDelta = scale P^T dO + diag(c) K dS, stored negated in token rows (the A
     // operand of the update below, read MN-major, and the gradient kernel's tile)
     {
-      const int s = acc_row(64);
-      for (int q = grp; q * 16 < Dv; q += kGroups) {
+      // M = 64 accumulators, two 16-column pieces per load (x2_row / x2_half)
+      const int s = x2_row();
+      for (int c0 = grp * 16; c0 < Dv; c0 += 32 * kGroups) {
         float a1[16], a2[16];
-        tc::tmem_ld16(tA1 + lane_quarter() + q * 16, a1);
-        tc::tmem_ld16(tA2 + lane_quarter() + q * 16, a2);
+        tc::tmem_ld16_x2<16 * kGroups>(tA1 + lane_quarter() + c0, a1);
+        tc::tmem_ld16_x2<16 * kGroups>(tA2 + lane_quarter() + c0, a2);
         tc::tmem_ld_wait();
-        if (s >= 0) {
+        const int col = c0 + x2_half() * 16 * kGroups;
+        if (col < Dv) {
           float md[16];
           if (s < len) {
             const float cs = cv[s];
@@ -190,7 +192,7 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
 #pragma unroll
             for (int j = 0; j < 16; ++j) md[j] = 0.f;
           }
-          tile_put16(tmD, C, s, q * 16, md);
+          tile_put16(tmD, C, s, col, md);
         }
       }
     }
@@ -351,7 +353,6 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
 
   const uint32_t tdQ = tmem, tdK = tmem + 128, tmp = tmem + 256;
   const size_t ckk = (size_t)c * p.Hk + kh;
-  const int row64 = acc_row(64);
   bool ok = true;
 
   // Phase A's tiles of value head h: S^T, W, U^T (bulk copies), dO rows into the
@@ -483,21 +484,16 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     // lower half of the stacked product)
     if (tid < kGroups * C) part[tid] = 0.f;
     __syncthreads();
-    for (int q = grp; q * 16 < Dv; q += kGroups) {
-      float x[16];
-      tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
-      tc::tmem_ld_wait();
-      if (row64 >= 0) {
-        float dc[16];
+    acc_walk64(tmp, Dv, C, [&](int r, int col0, float* x) {
+      float dc[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          x[j] = tile_get(sU, Dv, q * 16 + j, row64) - x[j];
-          dc[j] = x[j] * cv[row64];
-        }
-        tile_put16(tDl, C, row64, q * 16, x);
-        tile_put16(tDlc, C, row64, q * 16, dc);
+      for (int j = 0; j < 16; ++j) {
+        x[j] = tile_get(sU, Dv, col0 + j, r) - x[j];
+        dc[j] = x[j] * cv[r];
       }
-    }
+      tile_put16(tDl, C, r, col0, x);
+      tile_put16(tDlc, C, r, col0, dc);
+    });
     {
       const int row = acc_row(128);
       float rs = 0.f;
@@ -599,33 +595,30 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     // epilogue B
     {
       float rs = 0.f;
-      for (int q = grp; q * 16 < Dk; q += kGroups) {
-        float x[16];
-        tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
-        tc::tmem_ld_wait();
-        if (row64 >= 0) {
-          float kv[16];
-          tile_get16(tK, C, row64, q * 16, kv);
+      acc_walk64(tmp, Dk, C, [&](int r, int col0, const float* x) {
+        float kv[16];
+        tile_get16(tK, C, r, col0, kv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(kv[j], x[j], rs);
-        }
-      }
-      if (row64 >= 0) part[grp * C + row64] = rs;  // c_s * dc_s
+        for (int j = 0; j < 16; ++j) rs = fmaf(kv[j], x[j], rs);
+      });
+      rs = x2_pair_sum(rs);
+      if (x2_half() == 0) part[grp * C + x2_row()] = rs;  // c_s * dc_s
     }
     {
+      // dO Delta^T @128 and the dT terms @192, 8 columns per thread
       float rsum = 0.f;
-      for (int q = grp; q < 4; q += kGroups) {
-        float x[16], y[16];
-        tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
-        tc::tmem_ld16(tmp + 192 + lane_quarter() + q * 16, y);
+      {
+        const int r = x2_row(), s0 = grp * 16 + 8 * x2_half();
+        float x[8], y[8];
+        tc::tmem_ld8_x2<8>(tmp + 128 + lane_quarter() + grp * 16, x);
+        tc::tmem_ld8_x2<8>(tmp + 192 + lane_quarter() + grp * 16, y);
         tc::tmem_ld_wait();
-        if (row64 >= 0) {
-          const int r = row64;
-          float pv[16], pe[16], dt[16];
-          tile_get16(tP, C, r, q * 16, pv);
+        if (s0 < C) {
+          float pv[8], pe[8], dt[8];
+          tile_get8(tP, C, r, s0, pv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int s = q * 16 + j;
+          for (int j = 0; j < 8; ++j) {
+            const int s = s0 + j;
             const float dP = (s <= r && r < len) ? p.scale * x[j] : 0.f;
             const float E = s <= r ? expf(gv[r] - gv[s]) : 0.f;
             const float xp = dP * pv[j];
@@ -634,11 +627,12 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
             pe[j] = dP * E;
             dt[j] = -bv[s] * y[j];   // dT[r][s] = b_s (dDelta V^T + dW (e^G K)^T)[r][s]
           }
-          tile_put16(tdPE, C, r, q * 16, pe);
-          tile_put16(tdT, C, r, q * 16, dt);
+          tile_put8(tdPE, C, r, s0, pe);
+          tile_put8(tdT, C, r, s0, dt);
         }
       }
-      if (row64 >= 0) rowp[grp * C + row64] = rsum;
+      rsum = x2_pair_sum(rsum);
+      if (x2_half() == 0) rowp[grp * C + x2_row()] = rsum;
     }
     __syncthreads();
     {
@@ -690,34 +684,26 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     {
       __nv_bfloat16* dvc = (__nv_bfloat16*)p.dv + t0 * p.dv_ld + (int64_t)h * Dv;
       float rs = 0.f;
-      for (int q = grp; q * 16 < Dv; q += kGroups) {
-        float x[16];
-        tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
-        tc::tmem_ld_wait();
+      acc_walk64(tmp, Dv, len, [&](int s, int col0, float* x) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = -x[j];
-        if (row64 >= 0 && row64 < len) {
-          const int s = row64;
-          __align__(16) __nv_bfloat162 pk[8];
-          float vv[16];
-          tile_get16(tV, C, s, q * 16, vv);
+        __align__(16) __nv_bfloat162 pk[8];
+        float vv[16];
+        tile_get16(tV, C, s, col0, vv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(x[j], vv[j], rs);
+        for (int j = 0; j < 16; ++j) rs = fmaf(x[j], vv[j], rs);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            pk[j] = __floats2bfloat162_rn(bv[s] * x[2 * j], bv[s] * x[2 * j + 1]);
-          uint4* dst = (uint4*)(dvc + (int64_t)s * p.dv_ld + q * 16);
-          dst[0] = ((const uint4*)pk)[0];
-          dst[1] = ((const uint4*)pk)[1];
-        }
-      }
-      if (row64 >= 0) part[grp * C + row64] = rs;
-      for (int q = grp; q < 4; q += kGroups) {
-        float x[16];
-        tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
-        tc::tmem_ld_wait();
-        if (row64 >= 0) tile_put16(tY, C, row64, q * 16, x);
-      }
+        for (int j = 0; j < 8; ++j)
+          pk[j] = __floats2bfloat162_rn(bv[s] * x[2 * j], bv[s] * x[2 * j + 1]);
+        uint4* dst = (uint4*)(dvc + (int64_t)s * p.dv_ld + col0);
+        dst[0] = ((const uint4*)pk)[0];
+        dst[1] = ((const uint4*)pk)[1];
+      });
+      rs = x2_pair_sum(rs);
+      if (x2_half() == 0) part[grp * C + x2_row()] = rs;
+      acc_walk64_8(tmp + 128, C, C, [&](int r, int col0, const float* x) {
+        tile_put8(tY, C, r, col0, x);
+      });
     }
     __syncthreads();
     if (tid < C) db[tid] += rsum_g(part, tid);
@@ -736,41 +722,32 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     // dK term (H + H^T) K
     {
       float rs = 0.f;
-      for (int q = grp; q * 16 < Dk; q += kGroups) {
-        float x[16];
-        tc::tmem_ld16(tmp + lane_quarter() + q * 16, x);
-        tc::tmem_ld_wait();
-        if (row64 >= 0) {
-          float kv[16];
-          tile_get16(tK, C, row64, q * 16, kv);
+      acc_walk64(tmp, Dk, C, [&](int r, int col0, const float* x) {
+        float kv[16];
+        tile_get16(tK, C, r, col0, kv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rs = fmaf(kv[j], x[j], rs);
-        }
-      }
-      if (row64 >= 0) part[grp * C + row64] = rs;
+        for (int j = 0; j < 16; ++j) rs = fmaf(kv[j], x[j], rs);
+      });
+      rs = x2_pair_sum(rs);
+      if (x2_half() == 0) part[grp * C + x2_row()] = rs;
       float rq = 0.f;
-      for (int q = grp; q < 4; q += kGroups) {
-        float x[16];
-        tc::tmem_ld16(tmp + 128 + lane_quarter() + q * 16, x);
-        tc::tmem_ld_wait();
-        if (row64 >= 0) {
-          const int r = row64;
-          const float* kkr = sKK + r * KKL + q * 16;
-          float hv[16];
+      acc_walk64_8(tmp + 128, C, C, [&](int r, int s0, const float* x) {
+        const float* kkr = sKK + r * KKL + s0;
+        float hv[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int s = q * 16 + j;
-            const float E = s < r ? expf(gv[r] - gv[s]) : 0.f;
-            const float de = -x[j] * E;            // dA E (zero on and above the diagonal)
-            const float qq = de * kkr[j];
-            rq += qq;
-            X[r * XL + s] = qq * bv[r];
-            hv[j] = de * bv[r];
-          }
-          tile_put16(tH, C, r, q * 16, hv);
+        for (int j = 0; j < 8; ++j) {
+          const int s = s0 + j;
+          const float E = s < r ? expf(gv[r] - gv[s]) : 0.f;
+          const float de = -x[j] * E;            // dA E (zero on and above the diagonal)
+          const float qq = de * kkr[j];
+          rq += qq;
+          X[r * XL + s] = qq * bv[r];
+          hv[j] = de * bv[r];
         }
-      }
-      if (row64 >= 0) rowp[grp * C + row64] = rq;
+        tile_put8(tH, C, r, s0, hv);
+      });
+      rq = x2_pair_sum(rq);
+      if (x2_half() == 0) rowp[grp * C + x2_row()] = rq;
     }
     __syncthreads();
     {
@@ -857,55 +834,44 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       float dot[2] = {0.f, 0.f};
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t acc = which ? tdK : tdQ;
         const uint8_t* xt = which ? tK : tQ;   // x_hat tiles [C][Dk]
-        for (int q = grp; q * 16 < Dk; q += kGroups) {
-          float x[16];
-          tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
-          tc::tmem_ld_wait();
-          if (row64 >= 0) {
-            float xv[16];
-            tile_get16(xt, C, row64, q * 16, xv);
+        acc_walk64(which ? tdK : tdQ, Dk, C, [&](int r, int col0, const float* x) {
+          float xv[16];
+          tile_get16(xt, C, r, col0, xv);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) dot[which] = fmaf(x[j], xv[j], dot[which]);
-          }
-        }
+          for (int j = 0; j < 16; ++j) dot[which] = fmaf(x[j], xv[j], dot[which]);
+        });
       }
-      if (row64 >= 0) {
-        part[grp * C + row64] = dot[0];
-        rowp[grp * C + row64] = dot[1];
+      dot[0] = x2_pair_sum(dot[0]);
+      dot[1] = x2_pair_sum(dot[1]);
+      if (x2_half() == 0) {
+        part[grp * C + x2_row()] = dot[0];
+        rowp[grp * C + x2_row()] = dot[1];
       }
     }
     __syncthreads();
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
-      const uint32_t acc = which ? tdK : tdQ;
       const uint8_t* xt = which ? tK : tQ;
       const float* pr = which ? rowp : part;
       __nv_bfloat16* dst = (__nv_bfloat16*)(which ? p.dk : p.dq) +
                            t0 * (which ? p.dk_ld : p.dq_ld) + (int64_t)kh * Dk;
       const int64_t ld = which ? p.dk_ld : p.dq_ld;
-      for (int q = grp; q * 16 < Dk; q += kGroups) {
-        float x[16];
-        tc::tmem_ld16(acc + lane_quarter() + q * 16, x);
-        tc::tmem_ld_wait();
-        if (row64 >= 0 && row64 < len) {
-          const int r = row64;
-          const float d = rsum_g(pr, r), inv = 1.f / invn[which * C + r];
-          __align__(16) __nv_bfloat162 pk[8];
-          float xv[16];
-          tile_get16(xt, C, r, q * 16, xv);
+      acc_walk64(which ? tdK : tdQ, Dk, len, [&](int r, int col0, const float* x) {
+        const float d = rsum_g(pr, r), inv = 1.f / invn[which * C + r];
+        __align__(16) __nv_bfloat162 pk[8];
+        float xv[16];
+        tile_get16(xt, C, r, col0, xv);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float a = (x[2 * j] - xv[2 * j] * d) * inv;
-            const float b2 = (x[2 * j + 1] - xv[2 * j + 1] * d) * inv;
-            pk[j] = __floats2bfloat162_rn(a, b2);
-          }
-          uint4* o = (uint4*)(dst + (int64_t)r * ld + q * 16);
-          o[0] = ((const uint4*)pk)[0];
-          o[1] = ((const uint4*)pk)[1];
+        for (int j = 0; j < 8; ++j) {
+          const float a = (x[2 * j] - xv[2 * j] * d) * inv;
+          const float b2 = (x[2 * j + 1] - xv[2 * j + 1] * d) * inv;
+          pk[j] = __floats2bfloat162_rn(a, b2);
         }
-      }
+        uint4* o = (uint4*)(dst + (int64_t)r * ld + col0);
+        o[0] = ((const uint4*)pk)[0];
+        o[1] = ((const uint4*)pk)[1];
+      });
     }
   }
   tc::cp_async_wait_all();   // a unit that stopped early leaves no copy in flight

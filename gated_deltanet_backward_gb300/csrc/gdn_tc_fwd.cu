@@ -459,7 +459,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
                        8192u, C, C, 0u);
       }, &bar[0], phase, p.status, c);
       if (!ok) goto done;
-      acc_walk(tAccW, 64, Dk, C, [&](int s, int col0, const float* v) {
+      acc_walk64(tAccW, Dk, C, [&](int s, int col0, const float* v) {
         tile_put16(tW, C, s, col0, v);
       });
       acc_walk(tAccU, MV, 64, Dv, [&](int vv, int col0, const float* v) {
@@ -708,21 +708,23 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
     // O = scale (e^G Q S + P Delta), token row r of the chunk per accumulator lane:
     // each thread stores 16 consecutive values of its row
     {
-      const int r = acc_row(64);
-      __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + (r < 0 ? 0 : r)) * p.o_ld + (int64_t)h * Dv;
-      for (int q = grp; q * 16 < Dv; q += kGroups) {
+      // M = 64 accumulators, two 16-column pieces per load (x2_row / x2_half)
+      const int r = x2_row();
+      __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + r) * p.o_ld + (int64_t)h * Dv;
+      for (int c0 = grp * 16; c0 < Dv; c0 += 32 * kGroups) {
         float o1[16], o2[16];
-        tc::tmem_ld16(tO1 + lane_quarter() + q * 16, o1);
-        tc::tmem_ld16(tO2 + lane_quarter() + q * 16, o2);
+        tc::tmem_ld16_x2<16 * kGroups>(tO1 + lane_quarter() + c0, o1);
+        tc::tmem_ld16_x2<16 * kGroups>(tO2 + lane_quarter() + c0, o2);
         tc::tmem_ld_wait();
-        if (r >= 0 && r < len) {
+        const int col = c0 + x2_half() * 16 * kGroups;
+        if (r < len && col < Dv) {
           const float e = p.scale * ev[r];
           __align__(16) __nv_bfloat162 pk[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             pk[j] = __floats2bfloat162_rn(fmaf(e, o1[2 * j], p.scale * o2[2 * j]),
                                           fmaf(e, o1[2 * j + 1], p.scale * o2[2 * j + 1]));
-          uint4* dst = (uint4*)(orow + q * 16);
+          uint4* dst = (uint4*)(orow + col);
           dst[0] = ((const uint4*)pk)[0];
           dst[1] = ((const uint4*)pk)[1];
         }

@@ -80,6 +80,53 @@ __global__ void k_umma_check(const __nv_bfloat16* A, const __nv_bfloat16* B, flo
   if (warp == 0) tmem_dealloc(tmem, (uint32_t)ncols);
 }
 
+// Lane layout of the 16x32bx2 TMEM load (tmem_ld16_x2): 4 warps store lane * 1000 +
+// column into 128 lanes x 128 columns with 32x32b stores, then read them back with
+// tmem_ld16_x2<64> at columns 0, 16, 32, 48.  out[((warp * 32 + t) * 4 + piece) * 16 + j].
+__global__ void k_tmem_x2_check(float* out, int* status) {
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // all 512 columns, so that every column the loads can name is allocated
+  if (warp == 0) {
+    tmem_alloc(&tslot, 512u);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tslot;
+  const uint32_t lbase = (uint32_t)(32 * warp) << 16;
+  for (int c = 0; c < 128; c += 16) {
+    uint32_t r[16];
+    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint((float)((32 * warp + lane) * 1000 + c + j));
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(tmem + lbase + c),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  for (int piece = 0; piece < 4; ++piece) {
+    float v[16];
+    tmem_ld16_x2<64>(tmem + lbase + 16 * piece, v);
+    tmem_ld_wait();
+    for (int j = 0; j < 16; ++j) out[((warp * 32 + lane) * 4 + piece) * 16 + j] = v[j];
+  }
+  if (tid == 0) *status = 0;
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512u);
+}
+
+extern "C" int tmem_x2_check(float* out, int* status) {
+  k_tmem_x2_check<<<1, 128>>>(out, status);
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -2;
+}
+
 // MN-major operands need M (or N) a multiple of 64 and K a multiple of 16.
 extern "C" int umma_check(const void* A, const void* B, float* out, int M, int N, int K,
                           int a_mn, int b_mn, int* status) {

@@ -5,7 +5,8 @@ kind::f16 (bf16 x bf16 -> fp32) from K-major 128-byte-swizzled shared-memory
 tiles and dumps every TMEM lane.  Checks: the instruction and shared-memory
 descriptors give D = A B^T; for M = 128 row i sits in lane i; the lane layout of
 M = 64 is recorded (rows 16w..16w+15 in lanes 32w..32w+15); MN-major (transposed)
-storage of A and / or B gives the same product."""
+storage of A and / or B gives the same product; the 16x32bx2 TMEM load hands the
+upper half of a warp the first 16 lanes at a second column offset."""
 import ctypes
 import os
 import subprocess
@@ -32,6 +33,8 @@ def probe():
     L = ctypes.CDLL(lib)
     L.umma_check.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p]
     L.umma_check.restype = ctypes.c_int
+    L.tmem_x2_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    L.tmem_x2_check.restype = ctypes.c_int
     return torch, L
 
 
@@ -78,3 +81,16 @@ def test_mn_major_operands(probe, M, N, K, a_mn, b_mn):
              np.array([32 * (i // 16) + (i % 16) for i in range(64)]))
     err = np.abs(got[lanes] - ref).max() / np.abs(ref).max()
     assert err < 1e-5, err
+
+
+def test_tmem_ld16_x2_lane_layout(probe):
+    torch, L = probe
+    out = torch.full((4, 32, 4, 16), float("nan"), device="cuda")
+    st = torch.ones(1, dtype=torch.int32, device="cuda")
+    assert L.tmem_x2_check(out.data_ptr(), st.data_ptr()) == 0 and int(st.item()) == 0
+    got = out.cpu().numpy()
+    w, t, piece, j = np.meshgrid(np.arange(4), np.arange(32), np.arange(4), np.arange(16),
+                                 indexing="ij")
+    lane = 32 * w + (t % 16)
+    col = 16 * piece + j + 64 * (t // 16)
+    assert np.array_equal(got, (lane * 1000 + col).astype(np.float32))
