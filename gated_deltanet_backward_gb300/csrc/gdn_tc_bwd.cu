@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_state_tc(Params p,
 // ---------------------------------------------------------------------------
 // Shared-memory plan of k_bwd_grads_tc (bytes for Dk = Dv = 128; phases A-E of one
 // value head reuse the regions):
-//   R1 65K  A: S^T [Dv][Dk] (also read MN-major as S) | B: Delta, c*Delta, dW [C][D]
+//   R1 65K  A: S^T [Dv][Dk] (also read MN-major as S) | B: Delta^T, c Delta^T [Dv][C],
+//           dW [C][Dk]
 //           C-E: dPE, dT, H [C][C] (over Delta / c*Delta)
 //           A-E, from 48K: K K^T of the key head, fp32 [C][C + 4] (whole CTA)
 //   R2 32K  A-B: [dO; -dDelta] [128][Dv]  | B-E: fp32 [C][C] scratch
@@ -300,8 +301,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   uint8_t* R5 = R4 + 32768;
   // R1
   uint8_t* tSt = R1;                               // [MV][Dk] S^T (K-major), S (MN-major)
-  uint8_t* tDl = R1;                               // [C][Dv]
-  uint8_t* tDlc = R1 + 16384;                      // [C][Dv]
+  uint8_t* tDl = R1;                               // [Dv][C] Delta^T (read MN-major as Delta)
+  uint8_t* tDlc = R1 + 16384;                      // [Dv][C] Delta^T diag(c)
   uint8_t* tdW = R1 + 32768;                       // [C][Dk]
   uint8_t* tdPE = R1;                              // [C][C]
   uint8_t* tdT = R1 + 16384;                       // [C][C]
@@ -466,8 +467,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::mma_tile_p(tmp, tc::smem_u32(tW), 64u * 128u, 64, tc::smem_u32(tSt), sVC, Dv, Dk,
-                     0u);                                                                // W S
+      tc::mma_tile_p(tmp, tc::smem_u32(tSt), sVC, MV, tc::smem_u32(tW), 64u * 128u, C, Dk,
+                     0u);                                                                // S^T W^T
       tc::mma_tile_x(tmp + 128, tc::smem_u32(tA2), false, 128u * 128u, 128, tc::smem_u32(tSt),
                      true, sVC, NK, Dv, 0u);                                             // [dO;-dD] S^T
       tc::mma_tile_x(tdQ, tc::smem_u32(tdOe), false, 64u * 128u, 64, tc::smem_u32(tSt), true,
@@ -480,19 +481,20 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       tc::mbar_expect_tx(&bars[1], bSt);
       tc::bulk_g2s(tdS, p.dSb + ch * bSt, bSt, &bars[1]);
     }
-    // epilogue A: Delta = U - W S; dG += scale e^G (Q . dO S^T); dW = -dDelta S^T (the
-    // lower half of the stacked product)
+    // epilogue A: Delta^T = U^T - S^T W^T; dG += scale e^G (Q . dO S^T); dW = -dDelta S^T
+    // (the lower half of the stacked product)
     if (tid < kGroups * C) part[tid] = 0.f;
     __syncthreads();
-    acc_walk64(tmp, Dv, C, [&](int r, int col0, float* x) {
-      float dc[16];
+    acc_walk(tmp, MV, C, Dv, [&](int v, int col0, const float* x) {
+      float d[16], dc[16];
+      tile_get16(sU, Dv, v, col0, d);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        x[j] = tile_get(sU, Dv, col0 + j, r) - x[j];
-        dc[j] = x[j] * cv[r];
+        d[j] -= x[j];
+        dc[j] = d[j] * cv[col0 + j];
       }
-      tile_put16(tDl, C, r, col0, x);
-      tile_put16(tDlc, C, r, col0, dc);
+      tile_put16(tDl, Dv, v, col0, d);
+      tile_put16(tDlc, Dv, v, col0, dc);
     });
     {
       const int row = acc_row(128);
@@ -573,12 +575,13 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      tc::mma_tile_x(tmp, tc::smem_u32(tDlc), false, 64u * 128u, 64, tc::smem_u32(tdS), true,
-                     sVC, NK, Dv, 0u);                                                   // c Delta dS^T
-      tc::mma_tile_x(tdK, tc::smem_u32(tDlc), false, 64u * 128u, 64, tc::smem_u32(tdS), true,
-                     sVC, NK, Dv, acc_first);                                            // dK +=
-      tc::mma_tile_p(tmp + 128, tc::smem_u32(tA2), 128u * 128u, 64, tc::smem_u32(tDl),
-                     (uint32_t)C * 128u, C, Dv, 0u);                                     // dO Delta^T
+      const uint32_t dvp = (uint32_t)Dv * 128u;   // Delta^T tiles read MN-major
+      tc::mma_tile_x(tmp, tc::smem_u32(tDlc), true, dvp, 64, tc::smem_u32(tdS), true, sVC, NK, Dv,
+                     0u);                                                                // c Delta dS^T
+      tc::mma_tile_x(tdK, tc::smem_u32(tDlc), true, dvp, 64, tc::smem_u32(tdS), true, sVC, NK, Dv,
+                     acc_first);                                                         // dK +=
+      tc::mma_tile_x(tmp + 128, tc::smem_u32(tA2), false, 128u * 128u, 64, tc::smem_u32(tDl), true,
+                     dvp, C, Dv, 0u);                                                    // dO Delta^T
       tc::mma_tile_p(tmp + 192, tc::smem_u32(tA2) + 64u * 128u, 128u * 128u, 64,
                      tc::smem_u32(tV), (uint32_t)C * 128u, C, Dv, 0u);                  // -dDelta V^T
       tc::mma_tile(tmp + 192, tc::smem_u32(tdW), 64, tc::smem_u32(tKe), C, Dk, 1u);     // - dW (e^G K)^T
