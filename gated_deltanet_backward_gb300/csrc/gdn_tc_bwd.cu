@@ -649,18 +649,19 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
     __syncthreads();
     if (tid < C) {
-      const int t = tid;
+      const int t = tid, l = tid & 31;
       float csum = 0.f;
 #pragma unroll
       for (int g = 0; g < kColParts; ++g) csum += colp[g * C + t];
-      dG[t] += rsum_g(rowp, t) - csum - rsum_g(part, t);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float tot = 0.f, sc = 0.f;
-      for (int w = 0; w < kTcThreads / 32; ++w) tot += red[w];
-      for (int s = 0; s < C; ++s) sc += rsum_g(part, s);
-      dG[len - 1] += expf(gv[len - 1]) * tot + sc;
+      float upd = rsum_g(rowp, t) - csum - rsum_g(part, t);
+      // the last token takes e^{G_last} <S, dS> + sum_s c_s dc_s: both warps reduce all
+      // rows and all warp partials in the same order
+      float sc = rsum_g(part, l) + rsum_g(part, l + 32);
+      float tot = l < kTcThreads / 32 ? red[l] : 0.f;
+      sc = warp_sum(sc);
+      tot = warp_sum(tot);
+      if (t == len - 1) upd += expf(gv[len - 1]) * tot + sc;
+      dG[t] += upd;
     }
     // ---- phase C: -dDelta^T, T, T diag(b e^G) (issued after the MMAs of phase B)
     {
