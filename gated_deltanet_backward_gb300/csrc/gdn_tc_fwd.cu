@@ -188,16 +188,47 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
 }  // namespace
 
 // ---------------------------------------------------------------------------
+// Hand-over between the preparation units one CTA of the fused forward runs in a row,
+// as thread 0 sees it.
+struct PrepLink {
+  int pending;     // the previous unit, whose tile stores may still be in flight and whose
+                   // flag is unpublished; -1 if none
+  int next;        // the unit this CTA takes next, or -1
+  bool kq_issued;  // this unit's raw k / q tiles were issued by the previous unit
+};
+
+// Thread 0: the raw k and q rows of unit (c, kh) as TMA boxes into the [K; Q] tile,
+// on one phase of `bar`.  False (nothing issued) for a chunk outside the batch.
+__device__ bool issue_kq(const Params& p, const TmaMaps& maps, int c, int kh, uint8_t* tAQK,
+                         uint64_t* bar) {
+  int n, len;
+  int64_t t0;
+  if (!chunk_info(p, c, &n, &t0, &len)) return false;
+  const int nbk = (p.Dk + 63) / 64;
+  tc::mbar_arrive_expect_tx(bar, 2u * nbk * 8192u);
+  for (int b = 0; b < nbk; ++b) {
+    tc::tma_load_2d(tAQK + b * 128 * 128, &maps.k, kh * p.Dk + 64 * b, (int)t0, bar);
+    tc::tma_load_2d(tAQK + b * 128 * 128 + 8192, &maps.q, kh * p.Dk + 64 * b, (int)t0, bar);
+  }
+  return true;
+}
+
 // One (chunk c, key head kh) unit of the preparation on a whole CTA.  `sm` is its
 // shared memory (1024-aligned, prep_tc_smem bytes), `tmem` 256 TMEM columns, bar[0] /
-// bar[1] the MMA and load mbarriers with their running phases.  Every write of the
-// unit has completed when it returns; false after a timed-out wait.
+// bar[1] the MMA and load mbarriers with their running phases.  Without `link` every
+// write of the unit has completed when it returns.  With it (fused forward) the unit
+// publishes link->pending's flag once that unit's stores are done, before issuing its
+// own, returns with its own stores possibly in flight, and issues link->next's k / q
+// tiles once its last product has read its own (setting link->kq_issued).  False
+// after a timed-out wait.
 __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, int kh,
                           uint8_t* sm, uint32_t tmem, uint64_t* bar, uint32_t& phase,
-                          uint32_t& lphase) {
+                          uint32_t& lphase, PrepLink* link) {
   int n;
   int64_t t0;
   int len;
+  const bool kq_issued = link != nullptr && link->kq_issued;
+  if (link != nullptr && threadIdx.x == 0) link->kq_issued = false;
   if (!chunk_info(p, c, &n, &t0, &len)) {
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
     return true;
@@ -223,9 +254,13 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   float* bv = gv + RB * C;                              // [RB][C]
   float* wv = bv + RB * C;                              // [RB][C]
 
-  // W's padding columns (Dk < 64) stay zero: the epilogue writes only columns < Dk
-  if (Dk < 64)
+  // W's padding columns (Dk < 64) stay zero: the epilogue writes only columns < Dk (once
+  // the previous unit's W store has read the tile)
+  if (Dk < 64) {
+    if (tid == 0) tc::bulk_wait_read<0>();
+    __syncthreads();
     for (int i = tid; i < (int)bKC / 16; i += kTcThreads) ((uint4*)tW)[i] = make_uint4(0, 0, 0, 0);
+  }
   __syncthreads();
   // TMEM columns: [0, 64) the Gram products, [64, 64 + NK) W, [192, 256) U^T
   const uint32_t tAccW = tmem + 64, tAccU = tmem + 192;
@@ -242,13 +277,8 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   }
   const size_t ckk = (size_t)c * p.Hk + kh, ck = ckk * C;
   // raw k and q rows of the chunk: TMA boxes straight into the [K; Q] operand tile
-  if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&bar[1], 2u * nbk * 8192u);
-    for (int b = 0; b < nbk; ++b) {
-      tc::tma_load_2d(tAQK + b * aqk_pitch, &maps.k, kh * Dk + 64 * b, (int)t0, &bar[1]);
-      tc::tma_load_2d(tAQK + b * aqk_pitch + 8192, &maps.q, kh * Dk + 64 * b, (int)t0, &bar[1]);
-    }
-  }
+  // (issued by the previous unit when it could)
+  if (tid == 0 && !kq_issued) issue_kq(p, maps, c, kh, tAQK, &bar[1]);
   {
     const bool lok = tc::mbar_wait(&bar[1], lphase);
     lphase ^= 1u;
@@ -307,8 +337,14 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   }
   tc::fence_async_smem();
   __syncthreads();
-  // the natural K and Q tiles of this key head go to the workspace as they are
+  // the natural K and Q tiles of this key head go to the workspace as they are; first
+  // the previous unit's stores are waited for and its flag published
   if (tid == 0) {
+    if (link != nullptr && link->pending >= 0) {
+      tc::bulk_wait<0>();
+      publish_flag(p.fready + link->pending);
+      link->pending = -1;
+    }
     for (int b = 0; b < nbk; ++b) {
       tc::bulk_s2g(p.Ksw + ckk * bKC + b * 8192, tAQK + b * aqk_pitch, 8192);
       tc::bulk_s2g(p.Qsw + ckk * bKC + b * 8192, tAQK + b * aqk_pitch + 8192, 8192);
@@ -459,6 +495,10 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
                        8192u, C, C, 0u);
       }, &bar[0], phase, p.status, c);
       if (!ok) goto done;
+      // the unit's last product has read the [K; Q] tile: the next unit's rows may land
+      if (tid == 0 && link != nullptr && link->next >= 0 && g0 + nh == p.r && hh + 1 == nh)
+        link->kq_issued =
+            issue_kq(p, maps, link->next / p.Hk, link->next % p.Hk, tAQK, &bar[1]);
       acc_walk64(tAccW, Dk, C, [&](int s, int col0, const float* v) {
         tile_put16(tW, C, s, col0, v);
       });
@@ -480,7 +520,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
     }
   }
 done:
-  if (tid == 0) tc::bulk_wait<0>();
+  if (tid == 0 && link == nullptr) tc::bulk_wait<0>();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -497,7 +537,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
   cta_setup(ctl, 2, 256);
   uint32_t phase = 0, lphase = 0;
   prep_unit(p, maps, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar, phase,
-            lphase);
+            lphase, nullptr);
   cta_teardown(ctl, 256);
 }
 
@@ -617,10 +657,11 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       cvb[b * C + tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
     }
     mma_issue([&] {
+      tc::mma_tile(tX, tc::smem_u32(tSt), MV, tc::smem_u32(tW(b)), C, DK, 0u);
       // the chunk-start state S^T goes to the saved states as it is, by one bulk store
+      // issued behind the product (the two would contend for the tile's reads)
       tc::bulk_s2g((uint8_t*)p.saved + ((size_t)cc * p.Hv + h) * bSt, tSt, bSt);
       tc::bulk_commit();
-      tc::mma_tile(tX, tc::smem_u32(tSt), MV, tc::smem_u32(tW(b)), C, DK, 0u);
     }, &bars[0]);
     return true;
   };
@@ -747,7 +788,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_state_tc(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
-  cta_setup(ctl, 3, 512);
+  cta_setup(ctl, 4, 512);
   fwd_state_unit<DK>(p, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
   cta_teardown(ctl, 512);
 }
@@ -765,7 +806,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
   __shared__ int s_unit;
-  cta_setup(ctl, 3, 512);
+  cta_setup(ctl, 4, 512);
   const int walks = p.n_seqs * p.Hv;
   if ((int)blockIdx.x < walks) {
     fwd_state_unit<DK>(p, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes, ctl->tmem,
@@ -773,7 +814,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
   } else {
     uint32_t phase = 0, lphase = 0;
     const int units = p.NC * p.Hk;
-    // the next unit is taken while the current one runs
+    // the next unit is taken while the current one runs (thread 0's view)
+    PrepLink link{-1, -1, false};
     int next = threadIdx.x == 0 ? (int)atomicAdd(p.fwork, 1u) : 0;
     for (;;) {
       if (threadIdx.x == 0) s_unit = next;
@@ -781,11 +823,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
       const int u = s_unit;
       __syncthreads();
       if (u >= units) break;
-      if (threadIdx.x == 0) next = (int)atomicAdd(p.fwork, 1u);
+      if (threadIdx.x == 0) {
+        next = (int)atomicAdd(p.fwork, 1u);
+        link.next = next < units ? next : -1;
+      }
       const bool ok = prep_unit(p, maps, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
-                                ctl->bar, phase, lphase);
-      if (threadIdx.x == 0) publish_flag(p.fready + u);
+                                ctl->bar, phase, lphase, &link);
+      if (threadIdx.x == 0) {
+        if (link.pending >= 0) {   // a unit that stopped before its stores
+          tc::bulk_wait<0>();
+          publish_flag(p.fready + link.pending);
+        }
+        link.pending = u;
+      }
       if (!ok) break;
+    }
+    if (threadIdx.x == 0) {
+      // the last unit's stores, and k / q rows issued for a unit that will not run
+      if (link.kq_issued) tc::mbar_wait(&ctl->bar[1], lphase);
+      tc::bulk_wait<0>();
+      if (link.pending >= 0) publish_flag(p.fready + link.pending);
     }
   }
   cta_teardown(ctl, 512);
