@@ -122,13 +122,17 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
       break;
     }
     if (tid == 0) {
+      // every fourth chunk, before this chunk's first store: all but the last two
+      // store groups (the previous chunk's) have landed, so the chunks down to c + 2
+      // are published (the gradient units trail the walk; waiting only for old stores
+      // keeps the wait short)
+      if (p.bready && i > 1 && (i & 3) == 0) {
+        tc::bulk_wait<2>();
+        publish_down_to(c + 2);
+      }
       // state adjoint at the end of this chunk: the dS^T tile, by one bulk store
       tc::bulk_s2g(p.dSb + ch * bSt, tdSt, bSt);
       tc::bulk_commit();
-      if (c - 1 >= c0) {
-        tc::fence_async_smem();
-        issue_load(c - 1, b ^ 1);
-      }
     }
     const float* G = sG(b);
     if (tid < C) {
@@ -169,6 +173,9 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
       // rows v: dO^T (scale e^G Q), dO^T read MN-major
       tc::mma_tile_x(tA3, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tQ(b)), true,
                      8192u, NKF, C, 0u);
+      // the next chunk's tiles into the other buffer (its last chunk's products are
+      // done), issued while these products finish
+      if (c - 1 >= c0) issue_load(c - 1, b ^ 1);
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // dDelta = scale P^T dO + diag(c) K dS, stored negated in token rows (the A
@@ -200,12 +207,6 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
     ok = mma_run([&] {
       tc::mma_tile_x(tA3, tc::smem_u32(tmD), true, 8192u, MV, tc::smem_u32(tW(b)), true, 8192u,
                      NKF, C, 1u);
-      // while the tensor core works: everything but this chunk's dS^T store has landed,
-      // so chunk c + 1 is published
-      if (p.bready && c + 1 < c1) {
-        tc::bulk_wait<1>();
-        publish_down_to(c + 1);
-      }
       tc::bulk_wait_read<0>();   // the dS^T store has read its tile: the update may rewrite it
       tc::bulk_s2g(p.dDb + ch * bD, tmD, bD);
       tc::bulk_commit();
