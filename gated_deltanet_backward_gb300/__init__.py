@@ -73,6 +73,9 @@ _lib.gdn_backward.restype = ctypes.c_int
 _lib.gdn_forward_noalloc.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] +
                                      [_vp, _vp, _vp])
 _lib.gdn_forward_noalloc.restype = ctypes.c_int
+# shape; q,k,v,alpha,beta_raw (+ld); a_log, dt_bias, S_in, S_out; o (+ld); stream
+_lib.gdn_decode_step.argtypes = [_SP] + [_vp, _i64] * 5 + [_vp] * 4 + [_vp, _i64, _vp]
+_lib.gdn_decode_step.restype = ctypes.c_int
 _lib.gdn_read_device_status.argtypes = [_vp, _vp]
 _lib.gdn_read_device_status.restype = ctypes.c_int
 _lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -88,7 +91,8 @@ _lib.gdn_kernel_name.restype = ctypes.c_char_p
 
 EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_forward",
             "gdn_backward", "gdn_read_device_status", "gdn_status_string", "gdn_profile_begin",
-            "gdn_profile_end", "gdn_kernel_name", "gdn_last_error", "gdn_forward_noalloc")
+            "gdn_profile_end", "gdn_kernel_name", "gdn_last_error", "gdn_forward_noalloc",
+            "gdn_decode_step")
 
 
 class GdnError(RuntimeError):
@@ -211,6 +215,19 @@ def gdn_forward_noalloc(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seql
     _check(_lib.gdn_forward_noalloc(*args), "gdn_forward_noalloc")
 
 
+def gdn_decode_step(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, S_in, S_out, o,
+                    stream=None) -> None:
+    """Calls gdn_decode_step: one new token per sequence (row n of q, k, v, alpha,
+    beta_raw, o); the state goes from S_in (None = zero) to S_out (may be S_in)."""
+    args = [ctypes.byref(shape)]
+    for t in (q, k, v, alpha, beta_raw):
+        args += list(_mat(t))
+    args += [_ptr(a_log), _ptr(dt_bias), _ptr(S_in), _ptr(S_out)]
+    args += list(_mat(o))
+    args += [_stream(stream)]
+    _check(_lib.gdn_decode_step(*args), "gdn_decode_step")
+
+
 def gdn_read_device_status(workspace, stream=None) -> int:
     return int(_lib.gdn_read_device_status(_ptr(workspace), _stream(stream)))
 
@@ -285,9 +302,12 @@ class Layer:
                    saved, ws_f, ws_b)
 
     def forward(self, q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream=None,
-                train=False):
+                train=False, keep_states=True):
+        """keep_states=False (only without train) stores no chunk-start states: a
+        forward that no backward reads (prefill, inference)."""
         gdn_forward(self.shape, q, k, v, alpha, beta_raw, a_log, dt_bias, self.cu_seqlens,
-                    self.chunk_offsets, S0, o, S_T, self.saved_states,
+                    self.chunk_offsets, S0, o, S_T,
+                    self.saved_states if (keep_states or train) else None,
                     self.ws_bwd if train else self.ws_fwd, stream,
                     GDN_FLAG_KEEP_FOR_BACKWARD if train else 0)
 

@@ -305,6 +305,7 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_PREP_TC_FULL: return "gdn_prep_tc_full";
     case gdn::KID_FWD_FUSED_TC: return "gdn_fwd_fused_tc";
     case gdn::KID_BWD_FUSED_TC: return "gdn_bwd_fused_tc";
+    case gdn::KID_DECODE: return "gdn_decode";
     default: return "?";
   }
 }
@@ -353,7 +354,8 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
   const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
   GDN_TRY(check_matrix(o, o_ld, (int64_t)s->Hv * s->Dv, es, s->total_tokens));
   GDN_TRY(check_vec(S_T, false));
-  GDN_TRY(check_vec(saved_states, s->total_chunks > 0));
+  // a forward that no backward reads (prefill, inference) may skip the saved states
+  GDN_TRY(check_vec(saved_states, keep && s->total_chunks > 0));
   GDN_TRY(check_workspace(s, workspace, workspace_bytes, keep));
   cudaStream_t st = (cudaStream_t)stream;
   Params p;
@@ -478,6 +480,39 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
   }
   e = gdn::launch_backward(p, bf16 ? &maps : nullptr, st);
   if (e != cudaSuccess) return cuda_fail("gdn_backward: kernel launch", e);
+  return GDN_OK;
+}
+
+int gdn_decode_step(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                    int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                    int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                    const float* a_log, const float* dt_bias, const float* S_in, float* S_out,
+                    void* o, int64_t o_ld, void* stream) {
+  if (!s) return GDN_ERR_INVALID_ARG;
+  // one token per sequence: the token and chunk counts are the sequence count
+  gdn_shape one = *s;
+  one.total_tokens = s->n_seqs;
+  one.total_chunks = s->n_seqs;
+  GDN_TRY(check_shape(&one));
+  const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
+  const int64_t N = s->n_seqs;
+  GDN_TRY(check_matrix(q, q_ld, (int64_t)s->Hk * s->Dk, es, N));
+  GDN_TRY(check_matrix(k, k_ld, (int64_t)s->Hk * s->Dk, es, N));
+  GDN_TRY(check_matrix(v, v_ld, (int64_t)s->Hv * s->Dv, es, N));
+  GDN_TRY(check_matrix(o, o_ld, (int64_t)s->Hv * s->Dv, es, N));
+  GDN_TRY(check_gate_matrix(alpha, alpha_ld, s->Hv, N));
+  GDN_TRY(check_gate_matrix(beta_raw, beta_ld, s->Hv, N));
+  GDN_TRY(check_vec(a_log, true));
+  GDN_TRY(check_vec(dt_bias, true));
+  GDN_TRY(check_vec(S_in, false));
+  GDN_TRY(check_vec(S_out, N > 0));
+  if (N == 0) return GDN_OK;
+  (void)cudaGetLastError();  // report only errors of this call's own launch
+  g_last_error[0] = 0;
+  const cudaError_t e = gdn::launch_decode(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld,
+                                           beta_raw, beta_ld, a_log, dt_bias, S_in, S_out, o,
+                                           o_ld, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("gdn_decode_step: kernel launch", e);
   return GDN_OK;
 }
 

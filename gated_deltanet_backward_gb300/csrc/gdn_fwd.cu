@@ -146,10 +146,12 @@ __global__ void __launch_bounds__(kThreads) k_fwd_state(Params p, int DVS) {
     const int64_t t0 = s0 + (int64_t)(c - c0) * C;
     const int len = (int)((s1 - t0) < C ? (s1 - t0) : C);
     const size_t ch = (size_t)c * p.Hv + h;
-    float* sv = p.saved + ch * SZ;
-    for (int idx = threadIdx.x; idx < Dk * DVS; idx += kThreads) {
-      const int kk = idx / DVS, j = idx % DVS;
-      sv[(size_t)kk * Dv + v0 + j] = S[idx];
+    if (p.saved) {
+      float* sv = p.saved + ch * SZ;
+      for (int idx = threadIdx.x; idx < Dk * DVS; idx += kThreads) {
+        const int kk = idx / DVS, j = idx % DVS;
+        sv[(size_t)kk * Dv + v0 + j] = S[idx];
+      }
     }
     if (threadIdx.x < C) gv[threadIdx.x] = p.G[ch * C + threadIdx.x];
     __syncthreads();

@@ -217,7 +217,8 @@ enum KernelId {
   KID_PREP_TC_FULL = 10,
   KID_FWD_FUSED_TC = 11,
   KID_BWD_FUSED_TC = 12,
-  KID_COUNT = 11
+  KID_DECODE = 13,
+  KID_COUNT = 14
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
@@ -246,6 +247,13 @@ cudaError_t launch_fwd_fused_tc(const Params& p, const TmaMaps& maps, cudaStream
                                 bool* launched);
 cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st);
 cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st);
+
+// One decode step (gdn_decode_step): arguments validated by the caller.
+cudaError_t launch_decode(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                          int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                          int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                          const float* a_log, const float* dt_bias, const float* S_in,
+                          float* S_out, void* o, int64_t o_ld, cudaStream_t st);
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t st);

@@ -659,9 +659,12 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
     mma_issue([&] {
       tc::mma_tile(tX, tc::smem_u32(tSt), MV, tc::smem_u32(tW(b)), C, DK, 0u);
       // the chunk-start state S^T goes to the saved states as it is, by one bulk store
-      // issued behind the product (the two would contend for the tile's reads)
-      tc::bulk_s2g((uint8_t*)p.saved + ((size_t)cc * p.Hv + h) * bSt, tSt, bSt);
-      tc::bulk_commit();
+      // issued behind the product (the two would contend for the tile's reads); a
+      // forward that keeps no states skips it
+      if (p.saved) {
+        tc::bulk_s2g((uint8_t*)p.saved + ((size_t)cc * p.Hv + h) * bSt, tSt, bSt);
+        tc::bulk_commit();
+      }
     }, &bars[0]);
     return true;
   };

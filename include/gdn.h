@@ -146,7 +146,9 @@ size_t gdn_workspace_bytes(const gdn_shape* shape, int is_backward);
  *   o         device, [total_tokens, o_ld] dtype (written)
  *   S_T       device, [n_seqs, Hv, Dk, Dv] fp32 final states, or NULL
  *   saved_states device, gdn_saved_state_bytes() bytes (written; the backward
- *             reads it)
+ *             reads it), or NULL for a forward no backward will read (prefill,
+ *             inference: the chunk-start states are then not stored); required
+ *             with GDN_FLAG_KEEP_FOR_BACKWARD
  *   workspace device scratch, gdn_workspace_bytes(shape, 0) bytes
  *             (gdn_workspace_bytes(shape, 1) with GDN_FLAG_KEEP_FOR_BACKWARD)
  *   flags     0 or GDN_FLAG_KEEP_FOR_BACKWARD
@@ -219,6 +221,32 @@ int gdn_forward_noalloc(const gdn_shape* shape, const void* q, int64_t q_ld, con
                         const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
                         const int32_t* chunk_offsets, const float* S0, void* o, int64_t o_ld,
                         float* S_T, void* saved_states, void* stream);
+
+/* One decode step: every sequence takes one new token (the recurrence above applied
+ * once, in its token form; Gated Delta Networks, the gated delta rule update).  For
+ * every sequence n and value head h, with kh = h / (Hv / Hk):
+ *   q_hat, k_hat = q / sqrt(|q|^2 + 1e-6), k / sqrt(|k|^2 + 1e-6)   (key head kh)
+ *   g = exp(-e^{a_log[h]} softplus(alpha + dt_bias[h])),  beta = sigmoid(beta_raw)
+ *   delta = beta (v - g S^T k_hat);  S <- g S + k_hat delta^T;  o = scale S^T q_hat
+ * shape: Hk, Hv, Dk, Dv, dtype and scale as for gdn_forward; n_seqs sequences of one
+ *   token each (total_tokens and total_chunks are not read).
+ *   q, k      device, [n_seqs, *_ld] dtype: the new token's query / key rows
+ *   v         device, [n_seqs, v_ld] dtype
+ *   alpha, beta_raw  device, [n_seqs, *_ld] fp32
+ *   a_log, dt_bias   device, [Hv] fp32
+ *   S_in      device, [n_seqs, Hv, Dk, Dv] fp32 state before the token, or NULL
+ *             for a zero state
+ *   S_out     device, [n_seqs, Hv, Dk, Dv] fp32 state after the token (written);
+ *             S_out == S_in updates the state in place; partly overlapping
+ *             buffers are not supported
+ *   o         device, [n_seqs, o_ld] dtype (written)
+ * Needs no workspace and keeps nothing for a backward.  Validation, alignment rules
+ * and return values as for gdn_forward (nothing is launched on an error). */
+int gdn_decode_step(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
+                    int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                    int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                    const float* a_log, const float* dt_bias, const float* S_in, float* S_out,
+                    void* o, int64_t o_ld, void* stream);
 
 /* Synchronises `stream` and returns the device-side status recorded in
  * `workspace` by the last gdn_forward / gdn_backward that used it (GDN_OK, or

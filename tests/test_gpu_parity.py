@@ -181,3 +181,26 @@ def test_reuse_without_a_kept_forward_is_refused_on_the_device():
     run = DeviceRun(inp, train=True)
     assert run.status() == 0 and run.status(backward=True) == 0
     compare(run.host(), oracle_outputs(inp), TOL["bf16"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_forward_without_saved_states_gives_the_same_bits(dtype):
+    """A forward that keeps no chunk-start states (prefill / inference: saved_states =
+    NULL) writes the same o and S_T, bit for bit, as one that keeps them, and leaves the
+    saved-state buffer untouched."""
+    import torch
+    import gated_deltanet_backward_gb300 as gdn
+    wl = W.custom(dtype=dtype, seed=11, Hk=2, Hv=4, Dk=64, Dv=64, seqlens=(130, 0, 70),
+                  S0_std=0.3, dt_bias_std=0.2)
+    run = DeviceRun(W.generate(wl), run_backward=False, train=False)
+    o2 = torch.full_like(run.o, float("nan"))
+    S_T2 = torch.full_like(run.S_T, float("nan"))
+    run.layer.saved_states.fill_(7.0)
+    run.layer.forward(run.q, run.k, run.v, run.alpha, run.beta_raw, run.a_log, run.dt_bias,
+                      run.S0, o2, S_T2, keep_states=False)
+    torch.cuda.synchronize()
+    assert gdn.gdn_read_device_status(run.layer.ws_fwd) == 0
+    assert torch.equal(o2.view(torch.int16 if dtype == "bf16" else torch.int32),
+                       run.o.view(torch.int16 if dtype == "bf16" else torch.int32))
+    assert torch.equal(S_T2.view(torch.int32), run.S_T.view(torch.int32))
+    assert bool((run.layer.saved_states == 7.0).all())
