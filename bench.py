@@ -401,12 +401,54 @@ def run_ours(args):
         "roofline": roof, "path_roofline": path_roof, "kernels": kernels,
         "gpu_launches": launches, "clocks": clocks, "e2e": e2e,
     }
+    if rank == 0 and world == 1 and not args.no_decode:
+        result["decode"] = run_decode(wl, device, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_decode(wl, device, pk, n_seqs=64, steps=50, warmup=5):
+    """gdn_decode_step on a batch of n_seqs sequences with the workload's head shape:
+    one new token per sequence per step, the fp32 state updated in place (its
+    n_seqs * Hv * Dk * Dv * 4 bytes, read and written once a step, exceed the L2, so
+    no flush is needed).  Synthetic inputs, resident on the device."""
+    import torch
+    import gated_deltanet_backward_gb300 as gdn
+    Hk, Hv, Dk, Dv = wl.Hk, wl.Hv, wl.Dk, wl.Dv
+    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    g = torch.Generator(device=device).manual_seed(1234)
+    rn = lambda *sh, dt=torch.float32: torch.randn(*sh, generator=g, device=device).to(dt)
+    q, k = rn(n_seqs, Hk * Dk, dt=td), rn(n_seqs, Hk * Dk, dt=td)
+    v, o = rn(n_seqs, Hv * Dv, dt=td), torch.empty(n_seqs, Hv * Dv, device=device, dtype=td)
+    alpha, beta_raw = rn(n_seqs, Hv), rn(n_seqs, Hv)
+    a_log = torch.rand(Hv, generator=g, device=device) * 2 - 1
+    dt_bias = rn(Hv) * 0.1
+    S = rn(n_seqs, Hv, Dk, Dv) * 0.1
+    shape = gdn.make_shape(Hk, Hv, Dk, Dv, n_seqs, n_seqs, n_seqs, wl.dtype, 0.0)
+    step = lambda: gdn.gdn_decode_step(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, S, S, o)
+    for _ in range(warmup):
+        step()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / steps
+    state_bytes = 2 * n_seqs * Hv * Dk * Dv * 4
+    io_bytes = n_seqs * ((2 * Hk * Dk + 2 * Hv * Dv) * (2 if wl.dtype == "bf16" else 4) + 8 * Hv)
+    gbs = (state_bytes + io_bytes) / (us * 1e-6) / 1e9
+    return {"n_seqs": n_seqs, "us_per_step": us, "tokens_per_s": n_seqs / (us * 1e-6),
+            "bytes_per_step": state_bytes + io_bytes, "achieved_gbs": gbs,
+            "frac": gbs / pk["hbm_gbs"], "bound": "hbm",
+            "note": "gdn_decode_step, one token per sequence, state in place; "
+                    "value head shape of the workload"}
 
 
 def run_e2e(args, inp, layer, device, tdt, world):
@@ -540,6 +582,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=512)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -35,6 +35,8 @@ GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 GDN_FLAG_KEEP_FOR_BACKWARD = 1
 GDN_FLAG_REUSE_FORWARD = 2
+GDN_HEAD_MAP_CONSECUTIVE = 0
+GDN_HEAD_MAP_MODULO = 1
 GDN_ERR_NOT_KEPT = -8
 CHUNK = 64
 
@@ -43,7 +45,8 @@ class gdn_shape(ctypes.Structure):
     _fields_ = [("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32),
                 ("Dv", ctypes.c_int32), ("n_seqs", ctypes.c_int32),
                 ("total_chunks", ctypes.c_int32), ("total_tokens", ctypes.c_int64),
-                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("head_map", ctypes.c_int32)]
 
 
 _vp = ctypes.c_void_p
@@ -127,11 +130,14 @@ def gdn_plan(cu_seqlens_host) -> tuple:
     return off, int(tot.value)
 
 
-def make_shape(Hk, Hv, Dk, Dv, n_seqs, total_chunks, total_tokens, dtype, scale=0.0) -> gdn_shape:
+def make_shape(Hk, Hv, Dk, Dv, n_seqs, total_chunks, total_tokens, dtype, scale=0.0,
+               head_map=0) -> gdn_shape:
+    """head_map: GDN_HEAD_MAP_CONSECUTIVE (0, key head h // (Hv // Hk)) or
+    GDN_HEAD_MAP_MODULO (1, key head h % Hk)."""
     if not isinstance(dtype, int):
         dtype = GDN_DTYPE_BF16 if str(dtype) in ("bf16", "torch.bfloat16") else GDN_DTYPE_F32
     return gdn_shape(int(Hk), int(Hv), int(Dk), int(Dv), int(n_seqs), int(total_chunks),
-                     int(total_tokens), int(dtype), float(scale or 0.0))
+                     int(total_tokens), int(dtype), float(scale or 0.0), int(head_map))
 
 
 def gdn_saved_state_bytes(shape: gdn_shape) -> int:
@@ -287,11 +293,13 @@ class Layer:
     ws_bwd: object
 
     @classmethod
-    def create(cls, Hk, Hv, Dk, Dv, cu_seqlens_host, dtype, scale=0.0, device="cuda"):
+    def create(cls, Hk, Hv, Dk, Dv, cu_seqlens_host, dtype, scale=0.0, device="cuda",
+               head_map=0):
         import torch
         off, nc = gdn_plan(cu_seqlens_host)
         cu = np.asarray(cu_seqlens_host, dtype=np.int32)
-        shape = make_shape(Hk, Hv, Dk, Dv, len(cu) - 1, nc, int(cu[-1]), dtype, scale)
+        shape = make_shape(Hk, Hv, Dk, Dv, len(cu) - 1, nc, int(cu[-1]), dtype, scale,
+                           head_map)
         saved = torch.empty(max(4, gdn_saved_state_bytes(shape) // 4), dtype=torch.float32,
                             device=device)
         ws_f = torch.empty(max(256, gdn_workspace_bytes(shape, False)), dtype=torch.uint8,
@@ -321,4 +329,5 @@ class Layer:
 
 __all__ = list(EXPORTED) + ["gdn_profile", "gdn_shape", "make_shape", "Layer", "GdnError", "LIB_PATH", "CHUNK",
                             "GDN_DTYPE_F32", "GDN_DTYPE_BF16", "GDN_FLAG_KEEP_FOR_BACKWARD",
-                            "GDN_FLAG_REUSE_FORWARD", "GDN_ERR_NOT_KEPT"]
+                            "GDN_FLAG_REUSE_FORWARD", "GDN_ERR_NOT_KEPT",
+                            "GDN_HEAD_MAP_CONSECUTIVE", "GDN_HEAD_MAP_MODULO"]

@@ -23,6 +23,8 @@ int check_shape(const gdn_shape* s) {
   if (s->Hv % s->Hk != 0) return GDN_ERR_INVALID_ARG;
   if (!head_size_ok(s->Dk) || !head_size_ok(s->Dv)) return GDN_ERR_UNSUPPORTED;
   if (s->dtype != GDN_DTYPE_F32 && s->dtype != GDN_DTYPE_BF16) return GDN_ERR_UNSUPPORTED;
+  if (s->head_map != GDN_HEAD_MAP_CONSECUTIVE && s->head_map != GDN_HEAD_MAP_MODULO)
+    return GDN_ERR_INVALID_ARG;
   if (!(s->scale >= 0.f) || std::isinf(s->scale)) return GDN_ERR_INVALID_ARG;
   // a chunk holds at least one token, and every token lies in some chunk
   if ((int64_t)s->total_chunks > s->total_tokens) return GDN_ERR_INVALID_ARG;
@@ -74,6 +76,7 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
   p.Dk = s->Dk;
   p.Dv = s->Dv;
   p.r = s->Hv / s->Hk;
+  p.head_map = s->head_map;
   p.n_seqs = s->n_seqs;
   p.NC = s->total_chunks;
   p.T = s->total_tokens;
@@ -166,13 +169,13 @@ int check_workspace(const gdn_shape* s, void* ws, size_t bytes, bool bwd) {
 // into the workspace's status block and a reusing backward compares it.
 uint32_t shape_tag(const gdn_shape* s) {
   const int64_t f[9] = {s->Hk, s->Hv, s->Dk, s->Dv, s->n_seqs, s->total_chunks, s->total_tokens,
-                        s->dtype, 0};
+                        s->dtype, s->head_map};
   uint32_t h = 2166136261u;
   auto mix = [&](const void* data, size_t n) {
     const unsigned char* b = (const unsigned char*)data;
     for (size_t i = 0; i < n; ++i) h = (h ^ b[i]) * 16777619u;
   };
-  mix(f, sizeof(int64_t) * 8);
+  mix(f, sizeof(int64_t) * 9);
   mix(&s->scale, sizeof(float));
   return h | 1u;
 }

@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_state(Params p, int DVS) {
   if (kept_operands_missing(p)) return;
   extern __shared__ __align__(16) float sm[];
   const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * DVS;
-  const int kh = h / p.r, Dk = p.Dk, Dv = p.Dv, C = kChunk;
+  const int kh = key_head(p, h), Dk = p.Dk, Dv = p.Dv, C = kChunk;
   int64_t s0, s1;
   int c0, c1;
   if (!seq_info(p, n, &s0, &s1, &c0, &c1)) {
@@ -106,7 +106,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) k_bwd_grads(Params p) {
   if (kept_operands_missing(p)) return;
   extern __shared__ __align__(16) float sm[];
-  const int c = blockIdx.x, h = blockIdx.y, kh = h / p.r;
+  const int c = blockIdx.x, h = blockIdx.y, kh = key_head(p, h);
   int n;
   int64_t t0;
   int len;
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads) k_bwd_qk(Params p) {
       g[u] = 0.f;
       if (i < Dk) {
         for (int hh = 0; hh < p.r; ++hh)
-          g[u] += part[(((size_t)c * p.Hv + kh * p.r + hh) * C + r) * Dk + i];
+          g[u] += part[(((size_t)c * p.Hv + value_head(p, kh, hh)) * C + r) * Dk + i];
         dot = fmaf(g[u], xh[i], dot);
       }
     }

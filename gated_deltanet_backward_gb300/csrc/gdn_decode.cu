@@ -19,7 +19,7 @@ namespace {
 constexpr int kDecodeThreads = 128;   // >= Dv: one thread per value column
 
 struct DecodeParams {
-  int Hv, Dk, Dv, r;
+  int Hk, Hv, Dk, Dv, r, head_map;
   float scale;
   const void* q;
   int64_t q_ld;
@@ -49,7 +49,8 @@ __device__ __forceinline__ void store_io(__nv_bfloat16* p, int64_t i, float x) {
 }
 
 // One CTA per (sequence n, value head h): the state tile [Dk][Dv] in shared memory
-// (16-byte coalesced loads and stores), q_hat and k_hat of key head h / r, then
+// (16-byte coalesced loads and stores), q_hat and k_hat of the value head's key head
+// (h / r, or h % Hk with the modulo head map), then
 // thread v forms column v: kv_v = sum_k S[k][v] k_hat[k], delta_v, the new column
 // and o_v.  S_in may equal S_out (the tile is read before anything is written).
 template <typename T>
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(kDecodeThreads) k_decode(DecodeParams p) {
   float* qs = S + p.Dk * p.Dv;                  // [Dk] q, then q_hat
   float* ks = qs + p.Dk;                        // [Dk] k, then k_hat
   float* red = ks + p.Dk;                       // [2][kDecodeThreads / 32]
-  const int n = blockIdx.x, h = blockIdx.y, kh = h / p.r;
+  const int n = blockIdx.x, h = blockIdx.y, kh = p.head_map ? h % p.Hk : h / p.r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Dk = p.Dk, Dv = p.Dv;
   const size_t SZ = (size_t)Dk * Dv;
@@ -125,7 +126,9 @@ cudaError_t launch_decode(const gdn_shape* s, const void* q, int64_t q_ld, const
                           const float* a_log, const float* dt_bias, const float* S_in,
                           float* S_out, void* o, int64_t o_ld, cudaStream_t st) {
   DecodeParams p;
+  p.Hk = s->Hk;
   p.Hv = s->Hv;
+  p.head_map = s->head_map;
   p.Dk = s->Dk;
   p.Dv = s->Dv;
   p.r = s->Hv / s->Hk;

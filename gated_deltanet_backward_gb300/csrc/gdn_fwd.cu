@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kThreads) k_prep(Params p, int write_T) {
            [&](int i, int j, float acc) { KK[i * C + j] = acc; });
   __syncthreads();
   for (int hh = 0; hh < p.r; ++hh) {
-    const int h = kh * p.r + hh;
+    const int h = value_head(p, kh, hh);
     const size_t ch = (size_t)c * p.Hv + h;
     if (threadIdx.x < C) {
       const int t = threadIdx.x;
@@ -123,7 +123,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) k_fwd_state(Params p, int DVS) {
   extern __shared__ __align__(16) float sm[];
   const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * DVS;
-  const int kh = h / p.r, Dk = p.Dk, Dv = p.Dv, C = kChunk;
+  const int kh = key_head(p, h), Dk = p.Dk, Dv = p.Dv, C = kChunk;
   int64_t s0, s1;
   int c0, c1;
   if (!seq_info(p, n, &s0, &s1, &c0, &c1)) {

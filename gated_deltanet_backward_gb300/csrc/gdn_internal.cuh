@@ -136,6 +136,7 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
 // Everything a kernel needs, passed by value.
 struct Params {
   int Hk, Hv, Dk, Dv, r, n_seqs, NC;
+  int head_map;  // 0: key head h / r; 1: key head h % Hk
   int64_t T;
   float scale;
   const void* q;
@@ -201,6 +202,16 @@ struct Params {
   uint8_t* dSb;
   uint8_t* dDb;
 };
+
+// Key head of value head h, and the j-th (j < r) value head of key head kh: value
+// heads h and h' share a key head when h / r == h' / r (head_map 0, consecutive) or
+// h % Hk == h' % Hk (head_map 1, modulo).
+__host__ __device__ __forceinline__ int key_head(const Params& p, int h) {
+  return p.head_map ? h % p.Hk : h / p.r;
+}
+__host__ __device__ __forceinline__ int value_head(const Params& p, int kh, int j) {
+  return p.head_map ? kh + j * p.Hk : kh * p.r + j;
+}
 
 // Kernel ids reported to the profiling hook (gdn_profile_begin).
 enum KernelId {

@@ -31,7 +31,7 @@ __device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64)
 template <int DK>
 __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int h, uint8_t* sm,
                                uint32_t tmem, uint64_t* bars) {
-  const int kh = h / p.r;
+  const int kh = key_head(p, h);
   int64_t s0, s1;
   int c0, c1;
   if (!seq_info(p, n, &s0, &s1, &c0, &c1)) {
@@ -382,7 +382,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   // slot tid; the alpha rows past the chunk are not read)
   auto prefetch_vectors = [&](int hh) {
     if (tid < C) {
-      const int h = kh * p.r + hh;
+      const int h = value_head(p, kh, hh);
       const size_t ch = (size_t)c * p.Hv + h;
       float* sg = stg + (hh & 1) * 5 * C;
       tc::cp_async4(sg + tid, p.G + ch * C + tid);
@@ -399,7 +399,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     tc::mbar_arrive_expect_tx(&bars[1], 2 * sCK + phase_a_bytes);
     tc::bulk_g2s(tK, p.Ksw + ckk * sCK, sCK, &bars[1]);
     tc::bulk_g2s(tQ, p.Qsw + ckk * sCK, sCK, &bars[1]);
-    issue_phase_a_inputs(kh * p.r);
+    issue_phase_a_inputs(value_head(p, kh, 0));
   }
   // K K^T of the key head into padded rows (conflict-free row reads in epilogue D),
   // the norms for the L2 backward at the end and the first head's vectors
@@ -411,16 +411,16 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   // (one thread per value head)
   if (p.bready) {
     for (int hh = tid; hh < p.r; hh += kTcThreads)
-      if (!wait_flag(p.bready + (size_t)c * p.Hv + kh * p.r + hh))
+      if (!wait_flag(p.bready + (size_t)c * p.Hv + value_head(p, kh, hh)))
         set_status(p.status, GDN_ERR_TIMEOUT, c);
     __syncthreads();
   }
   if (tid == 0) {
     asm volatile("fence.proxy.async.global;" ::: "memory");
-    issue_phase_a_walk(kh * p.r);
+    issue_phase_a_walk(value_head(p, kh, 0));
   }
   for (int hh = 0; hh < p.r && ok; ++hh) {
-    const int h = kh * p.r + hh;
+    const int h = value_head(p, kh, hh);
     const size_t ch = (size_t)c * p.Hv + h;
     const uint32_t acc_first = hh > 0 ? 1u : 0u;
     const uint8_t* Sg = (const uint8_t*)p.saved_in + ch * bSt;   // S^T tile
@@ -785,8 +785,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     // under the gate epilogue
     if (tid == 0 && hh + 1 < p.r) {
       tc::mbar_arrive_expect_tx(&bars[1], phase_a_bytes);
-      issue_phase_a_inputs(h + 1);
-      issue_phase_a_walk(h + 1);
+      issue_phase_a_inputs(value_head(p, kh, hh + 1));
+      issue_phase_a_walk(value_head(p, kh, hh + 1));
     }
     // gate and sigmoid epilogues: dl = reverse cumsum of dG (one warp, two per lane)
     __syncthreads();

@@ -270,7 +270,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   {
     const int nh0 = p.r < RB ? p.r : RB;
     if (tid < nh0 * C && tid % C < len) {
-      const int t = tid % C, h = kh * p.r + tid / C;
+      const int t = tid % C, h = value_head(p, kh, tid / C);
       pre_beta = p.beta_raw[(t0 + t) * p.beta_ld + h];
       pre_x = p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
     }
@@ -377,7 +377,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
     const int nh = (p.r - g0) < RB ? (p.r - g0) : RB;
     // 3. gates of the nh value heads
     if (tid < nh * C) {
-      const int hh = tid / C, t = tid % C, h = kh * p.r + g0 + hh;
+      const int hh = tid / C, t = tid % C, h = value_head(p, kh, g0 + hh);
       float l = 0.f, b = 0.f;
       if (t < len) {
         const float braw = g0 == 0 ? pre_beta : p.beta_raw[(t0 + t) * p.beta_ld + h];
@@ -404,7 +404,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
     }
     __syncthreads();
     if (tid < nh * C) {
-      const int hh = tid / C, t = tid % C, h = kh * p.r + g0 + hh;
+      const int hh = tid / C, t = tid % C, h = value_head(p, kh, g0 + hh);
       const size_t ch = (size_t)c * p.Hv + h;
       wv[hh * C + t] = bv[hh * C + t] * expf(gv[hh * C + t]);
       p.G[ch * C + t] = gv[hh * C + t];
@@ -430,7 +430,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
     tri_inverse(Tm, nh, Mt);
     // 5. per head: W = T diag(w) K, U^T = V^T (T diag(b))^T, P
     for (int hh = 0; hh < nh; ++hh) {
-      const int h = kh * p.r + g0 + hh;
+      const int h = value_head(p, kh, g0 + hh);
       const size_t ch = (size_t)c * p.Hv + h;
       const float* T = Tm + hh * C * TS;
       if (tid == 0) {
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
 template <int DK>
 __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint32_t tmem,
                                uint64_t* bars) {
-  const int kh = h / p.r;
+  const int kh = key_head(p, h);
   int64_t s0, s1;
   int c0, c1;
   if (!seq_info(p, n, &s0, &s1, &c0, &c1)) {

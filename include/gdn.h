@@ -106,6 +106,15 @@ typedef enum {
   GDN_FLAG_REUSE_FORWARD = 2      /* gdn_backward only */
 } gdn_flag;
 
+/* Key head of value head h (v_repeat = Hv / Hk value heads share each key head).
+ * GDN_HEAD_MAP_CONSECUTIVE: kh = h / v_repeat (value heads kh*v_repeat ..
+ * kh*v_repeat + v_repeat - 1 share key head kh; the default, and the head map of the
+ * Rust forward/backward page).  GDN_HEAD_MAP_MODULO: kh = h % Hk (value heads kh,
+ * kh + Hk, kh + 2 Hk, ... share key head kh; the broadcast the ggml page's op uses).
+ * Every other argument keeps its meaning; dq / dk still sum over the value heads that
+ * read the key head. */
+typedef enum { GDN_HEAD_MAP_CONSECUTIVE = 0, GDN_HEAD_MAP_MODULO = 1 } gdn_head_map;
+
 typedef struct {
   int32_t Hk;           /* key heads (q and k heads) */
   int32_t Hv;           /* value heads; Hv % Hk == 0, v_repeat = Hv / Hk */
@@ -116,6 +125,7 @@ typedef struct {
   int64_t total_tokens; /* cu_seqlens[n_seqs] */
   int32_t dtype;        /* gdn_dtype of q, k, v, o, dO, dq, dk, dv */
   float scale;          /* output scale; 0 selects 1/sqrt(Dk) */
+  int32_t head_map;     /* gdn_head_map: which key head value head h reads */
 } gdn_shape;
 
 /* Chunk planning (host only).  From host cu_seqlens[n_seqs+1] (non-decreasing,

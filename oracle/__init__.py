@@ -49,7 +49,8 @@ class _Shape(ctypes.Structure):
     _fields_ = [("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32),
                 ("Dv", ctypes.c_int32), ("n_seqs", ctypes.c_int32),
                 ("total_tokens", ctypes.c_int64), ("scale", ctypes.c_double),
-                ("n_threads", ctypes.c_int32), ("segment", ctypes.c_int32)]
+                ("n_threads", ctypes.c_int32), ("segment", ctypes.c_int32),
+                ("head_map", ctypes.c_int32)]
 
 
 _P = ctypes.POINTER(ctypes.c_double)
@@ -103,7 +104,7 @@ class _Args:
     """Holds f64 copies of one set of inputs alive while the C code runs."""
 
     def __init__(self, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, S0, Hk, Hv, Dk, Dv,
-                 scale, n_threads, segment):
+                 scale, n_threads, segment, head_map=0):
         self.q, self.k, self.v = _f64(q), _f64(k), _f64(v)
         self.alpha, self.beta_raw = _f64(alpha), _f64(beta_raw)
         self.a_log = np.ascontiguousarray(a_log, dtype=np.float64)
@@ -114,7 +115,7 @@ class _Args:
         self.N = int(len(self.cu) - 1)
         self.Hk, self.Hv, self.Dk, self.Dv = Hk, Hv, Dk, Dv
         self.shape = _Shape(Hk, Hv, Dk, Dv, self.N, self.T, float(scale or 0.0), int(n_threads),
-                            int(segment))
+                            int(segment), int(head_map))
         self.inputs = _Inputs(_ptr(self.q), _ld(self.q), _ptr(self.k), _ld(self.k), _ptr(self.v),
                               _ld(self.v), _ptr(self.alpha), _ld(self.alpha), _ptr(self.beta_raw),
                               _ld(self.beta_raw), _ptr(self.a_log), _ptr(self.dt_bias),
@@ -132,11 +133,12 @@ def chunk_offsets(cu_seqlens, chunk: int) -> np.ndarray:
 
 
 def forward(q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, S0=None, *, Hk, Hv, Dk, Dv,
-            scale=None, n_threads=0, chunk=0):
+            scale=None, n_threads=0, chunk=0, head_map=0):
     """Token-by-token f64 forward.  Returns (o [T, Hv*Dv], S_T [N, Hv, Dk, Dv]), and when
-    ``chunk`` > 0 also the state at the start of every chunk [NC, Hv, Dk, Dv]."""
+    ``chunk`` > 0 also the state at the start of every chunk [NC, Hv, Dk, Dv].
+    head_map 0: value head h reads key head h // (Hv // Hk); 1: key head h % Hk."""
     a = _Args(q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, S0, Hk, Hv, Dk, Dv, scale,
-              n_threads, 0)
+              n_threads, 0, head_map)
     o = np.zeros((a.T, Hv * Dv), np.float64)
     S_T = np.zeros((a.N, Hv, Dk, Dv), np.float64)
     if chunk > 0:
@@ -155,12 +157,13 @@ def forward(q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, S0=None, *, Hk
 
 
 def backward(q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, dO, S0=None, dS_T=None, *,
-             Hk, Hv, Dk, Dv, scale=None, n_threads=0, segment=64):
+             Hk, Hv, Dk, Dv, scale=None, n_threads=0, segment=64, head_map=0):
     """Token-by-token f64 backward.  Returns a dict of gradients:
     dq, dk [T, Hk*Dk] (summed over the value heads sharing a key head), dv [T, Hv*Dv],
-    dalpha, dbeta_raw [T, Hv], da_log, ddt_bias [Hv], dS0 [N, Hv, Dk, Dv]."""
+    dalpha, dbeta_raw [T, Hv], da_log, ddt_bias [Hv], dS0 [N, Hv, Dk, Dv].
+    head_map as for forward()."""
     a = _Args(q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, S0, Hk, Hv, Dk, Dv, scale,
-              n_threads, segment)
+              n_threads, segment, head_map)
     dO = _f64(dO)
     dS_T = None if dS_T is None else np.ascontiguousarray(dS_T, dtype=np.float64)
     out = dict(dq=np.zeros((a.T, Hk * Dk)), dk=np.zeros((a.T, Hk * Dk)),
@@ -181,7 +184,8 @@ def backward(q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, dO, S0=None, 
 def run_inputs(inp, which="both", n_threads=0, segment=64):
     """Run the oracle on a ``workloads.Inputs`` draw.  Returns (fwd, bwd) dicts."""
     wl = inp.wl
-    kw = dict(Hk=wl.Hk, Hv=wl.Hv, Dk=wl.Dk, Dv=wl.Dv, scale=wl.scale_value(), n_threads=n_threads)
+    kw = dict(Hk=wl.Hk, Hv=wl.Hv, Dk=wl.Dk, Dv=wl.Dv, scale=wl.scale_value(), n_threads=n_threads,
+              head_map=getattr(wl, "head_map", 0))
     fwd = bwd = None
     if which in ("both", "fwd"):
         o, S_T = forward(inp.q, inp.k, inp.v, inp.alpha, inp.beta_raw, inp.a_log, inp.dt_bias,

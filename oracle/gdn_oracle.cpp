@@ -7,7 +7,9 @@
 //
 // What it follows (lattice-inference 0.6.0, src/attention/gdn_backward.rs, as
 // shown on docs.rs):
-//   * module header "Forward recap": per value head h the key head is h / ratio;
+//   * module header "Forward recap": per value head h the key head is h / ratio
+//     (head_map 0); with head_map 1 it is h % Hk, the broadcast of the ggml page's
+//     op ("modulo convention");
 //     g = exp(-exp(a_log[h]) * softplus(alpha + dt_bias[h])); retrieval from the
 //     pre-decayed state kv_mem = S_{t-1}^T k_hat; delta = (v - g kv_mem) beta;
 //     S_t = g S_{t-1} + k_hat delta^T; o_t = scale S_t^T q_hat, scale = 1/sqrt(Dk).
@@ -48,6 +50,7 @@ typedef struct {
   double scale;       // <= 0 selects 1/sqrt(Dk)
   int32_t n_threads;  // <= 0 selects std::thread::hardware_concurrency()
   int32_t segment;    // backward checkpoint interval in tokens; <= 0 selects 64
+  int32_t head_map;   // 0: key head of value head h is h / (Hv/Hk); 1: h % Hk
 } gdn_oracle_shape;
 
 typedef struct {
@@ -87,9 +90,11 @@ double softplus(double x) { return std::max(x, 0.0) + std::log1p(std::exp(-std::
 double sigmoid(double x) { return 1.0 / (1.0 + std::exp(-x)); }
 
 struct Dims {
-  int Hk, Hv, Dk, Dv, r;
+  int Hk, Hv, Dk, Dv, r, head_map;
   double scale;
   int64_t DkDv() const { return (int64_t)Dk * Dv; }
+  // value head number hh (0 <= hh < r) of key head kh
+  int vh(int kh, int hh) const { return head_map ? kh + hh * Hk : kh * r + hh; }
 };
 
 // Gate quantities of value head h at token t.
@@ -165,6 +170,8 @@ int check_shape(const gdn_oracle_shape* s, const gdn_oracle_inputs* in, Dims* d)
   d->Dk = s->Dk;
   d->Dv = s->Dv;
   d->r = s->Hv / s->Hk;
+  if (s->head_map != 0 && s->head_map != 1) return -1;
+  d->head_map = s->head_map;
   d->scale = s->scale > 0.0 ? s->scale : 1.0 / std::sqrt((double)s->Dk);
   return 0;
 }
@@ -195,20 +202,20 @@ extern "C" int gdn_oracle_forward_states(const gdn_oracle_shape* shape,
     std::vector<double> S((size_t)d.r * d.DkDv(), 0.0);
     if (in.S0)
       for (int hh = 0; hh < d.r; ++hh)
-        std::memcpy(&S[(size_t)hh * d.DkDv()], in.S0 + ((int64_t)n * d.Hv + kh * d.r + hh) * d.DkDv(),
+        std::memcpy(&S[(size_t)hh * d.DkDv()], in.S0 + ((int64_t)n * d.Hv + d.vh(kh, hh)) * d.DkDv(),
                     sizeof(double) * d.DkDv());
     std::vector<double> qh(d.Dk), kh_(d.Dk), kv(d.Dv), delta(d.Dv);
     for (int64_t t = t0; t < t1; ++t) {
       if (chunk_states && (t - t0) % chunk == 0) {
         const int64_t c = chunk_offsets[n] + (t - t0) / chunk;
         for (int hh = 0; hh < d.r; ++hh)
-          std::memcpy(chunk_states + (c * d.Hv + kh * d.r + hh) * d.DkDv(), &S[(size_t)hh * d.DkDv()],
+          std::memcpy(chunk_states + (c * d.Hv + d.vh(kh, hh)) * d.DkDv(), &S[(size_t)hh * d.DkDv()],
                       sizeof(double) * d.DkDv());
       }
       l2_normalise(in.q + t * in.q_ld + (int64_t)kh * d.Dk, d.Dk, qh.data());
       l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, kh_.data());
       for (int hh = 0; hh < d.r; ++hh) {
-        const int h = kh * d.r + hh;
+        const int h = d.vh(kh, hh);
         double* Sh = &S[(size_t)hh * d.DkDv()];
         const Gate G = gate_at(in, t, h);
         token_step(d, Sh, kh_.data(), in.v + t * in.v_ld + (int64_t)h * d.Dv, G, kv.data(),
@@ -222,7 +229,7 @@ extern "C" int gdn_oracle_forward_states(const gdn_oracle_shape* shape,
     }
     if (S_T)
       for (int hh = 0; hh < d.r; ++hh)
-        std::memcpy(S_T + ((int64_t)n * d.Hv + kh * d.r + hh) * d.DkDv(), &S[(size_t)hh * d.DkDv()],
+        std::memcpy(S_T + ((int64_t)n * d.Hv + d.vh(kh, hh)) * d.DkDv(), &S[(size_t)hh * d.DkDv()],
                     sizeof(double) * d.DkDv());
   });
   return 0;
@@ -254,14 +261,14 @@ extern "C" int gdn_oracle_backward(const gdn_oracle_shape* shape, const gdn_orac
     std::vector<double> S((size_t)d.r * SZ, 0.0);
     if (in.S0)
       for (int hh = 0; hh < d.r; ++hh)
-        std::memcpy(&S[hh * SZ], in.S0 + ((int64_t)n * d.Hv + kh * d.r + hh) * SZ, sizeof(double) * SZ);
+        std::memcpy(&S[hh * SZ], in.S0 + ((int64_t)n * d.Hv + d.vh(kh, hh)) * SZ, sizeof(double) * SZ);
     std::vector<double> qh(d.Dk), khat(d.Dk), kv(d.Dv), delta(d.Dv);
     for (int64_t t = t0; t < t1; ++t) {
       if ((t - t0) % seg == 0)
         std::memcpy(&ck[(size_t)((t - t0) / seg) * d.r * SZ], S.data(), sizeof(double) * d.r * SZ);
       l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, khat.data());
       for (int hh = 0; hh < d.r; ++hh) {
-        const int h = kh * d.r + hh;
+        const int h = d.vh(kh, hh);
         token_step(d, &S[hh * SZ], khat.data(), in.v + t * in.v_ld + (int64_t)h * d.Dv,
                    gate_at(in, t, h), kv.data(), delta.data());
       }
@@ -270,7 +277,7 @@ extern "C" int gdn_oracle_backward(const gdn_oracle_shape* shape, const gdn_orac
     std::vector<double> dS((size_t)d.r * SZ, 0.0);
     if (dS_T)
       for (int hh = 0; hh < d.r; ++hh)
-        std::memcpy(&dS[hh * SZ], dS_T + ((int64_t)n * d.Hv + kh * d.r + hh) * SZ, sizeof(double) * SZ);
+        std::memcpy(&dS[hh * SZ], dS_T + ((int64_t)n * d.Hv + d.vh(kh, hh)) * SZ, sizeof(double) * SZ);
     // States before each token of the current segment (plus the one after its end).
     std::vector<double> Sbuf((size_t)(seg + 1) * d.r * SZ);
     std::vector<double> S_t(SZ), dqh(d.Dk), dkh(d.Dk), ddelta(d.Dv), dkv(d.Dv);
@@ -283,7 +290,7 @@ extern "C" int gdn_oracle_backward(const gdn_oracle_shape* shape, const gdn_orac
         double* nxt = &Sbuf[(size_t)(t - ta + 1) * d.r * SZ];
         std::memcpy(nxt, &Sbuf[(size_t)(t - ta) * d.r * SZ], sizeof(double) * d.r * SZ);
         for (int hh = 0; hh < d.r; ++hh) {
-          const int h = kh * d.r + hh;
+          const int h = d.vh(kh, hh);
           token_step(d, nxt + hh * SZ, khat.data(), in.v + t * in.v_ld + (int64_t)h * d.Dv,
                      gate_at(in, t, h), kv.data(), delta.data());
         }
@@ -294,7 +301,7 @@ extern "C" int gdn_oracle_backward(const gdn_oracle_shape* shape, const gdn_orac
         std::fill(dq_acc.begin(), dq_acc.end(), 0.0);
         std::fill(dk_acc.begin(), dk_acc.end(), 0.0);
         for (int hh = 0; hh < d.r; ++hh) {
-          const int h = kh * d.r + hh;
+          const int h = d.vh(kh, hh);
           const double* S_prev = &Sbuf[(size_t)(t - ta) * d.r * SZ + hh * SZ];
           const double* vrow = in.v + t * in.v_ld + (int64_t)h * d.Dv;
           const double* dOrow = dO + t * dO_ld + (int64_t)h * d.Dv;
@@ -365,7 +372,7 @@ extern "C" int gdn_oracle_backward(const gdn_oracle_shape* shape, const gdn_orac
     }
     if (dS0)
       for (int hh = 0; hh < d.r; ++hh)
-        std::memcpy(dS0 + ((int64_t)n * d.Hv + kh * d.r + hh) * SZ, &dS[hh * SZ], sizeof(double) * SZ);
+        std::memcpy(dS0 + ((int64_t)n * d.Hv + d.vh(kh, hh)) * SZ, &dS[hh * SZ], sizeof(double) * SZ);
   });
   for (int h = 0; h < d.Hv; ++h) {
     double a = 0.0, b = 0.0;

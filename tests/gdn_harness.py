@@ -58,7 +58,7 @@ class DeviceRun:
         self.dO = dev(inp.dO, self.tdtype)
         self.dS_T = None if inp.dS_T is None else dev(inp.dS_T)
         self.layer = gdn.Layer.create(Hk, Hv, Dk, Dv, inp.cu_seqlens, wl.dtype,
-                                      wl.scale_value(), device=device)
+                                      wl.scale_value(), device=device, head_map=wl.head_map)
         N = wl.n_seqs
         self.o = torch.full((T, Hv * Dv), float("nan"), device=device, dtype=self.tdtype)
         self.S_T = torch.full((N, Hv, Dk, Dv), float("nan"), device=device)
@@ -163,7 +163,7 @@ def head_group_outputs(out: dict, wl: W.Workload, kh: int) -> dict:
 def oracle_outputs(inp: W.Inputs, backward=True, n_threads=0) -> dict:
     wl = inp.wl
     kw = dict(Hk=wl.Hk, Hv=wl.Hv, Dk=wl.Dk, Dv=wl.Dv, scale=wl.scale_value(),
-              n_threads=n_threads)
+              n_threads=n_threads, head_map=wl.head_map)
     o, S_T, states = oracle.forward(inp.q, inp.k, inp.v, inp.alpha, inp.beta_raw, inp.a_log,
                                     inp.dt_bias, inp.cu_seqlens, inp.S0, chunk=W.CHUNK, **kw)
     out = dict(o=o, S_T=S_T, saved=states)

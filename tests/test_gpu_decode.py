@@ -94,3 +94,27 @@ def test_rejects_bad_arguments_before_launching():
     bad = gdn.make_shape(Hk, Hv, 24, D, N, N, N, "f32", 0.0)             # unsupported Dk
     with pytest.raises(gdn.GdnError):
         gdn.gdn_decode_step(bad, q, k, v, g, g, a, a, None, z(N, Hv, 24, D), o)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_one_step_with_the_modulo_head_map(dtype):
+    torch = pytest.importorskip("torch")
+    import gated_deltanet_backward_gb300 as gdn
+    N, Hk, Hv, Dk, Dv = 3, 2, 6, 64, 32
+    wl = W.custom(dtype=dtype, seed=23, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, seqlens=(1,) * N,
+                  S0_std=0.3, dt_bias_std=0.2, packed=False, head_map=1)
+    inp = W.generate(wl)
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.alpha, inp.beta_raw, inp.a_log,
+                                  inp.dt_bias, inp.cu_seqlens, inp.S0, Hk=Hk, Hv=Hv, Dk=Dk,
+                                  Dv=Dv, scale=wl.scale_value(), head_map=1)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    q, k, v = (_dev(torch, x, td) for x in (inp.q, inp.k, inp.v))
+    S = _dev(torch, inp.S0)
+    o = torch.full((N, Hv * Dv), float("nan"), device="cuda", dtype=td)
+    shape = gdn.make_shape(Hk, Hv, Dk, Dv, N, N, N, dtype, wl.scale_value(),
+                           gdn.GDN_HEAD_MAP_MODULO)
+    gdn.gdn_decode_step(shape, q, k, v, _dev(torch, inp.alpha), _dev(torch, inp.beta_raw),
+                        _dev(torch, inp.a_log), _dev(torch, inp.dt_bias), S, S, o)
+    torch.cuda.synchronize()
+    assert rel_err(o.float().cpu().numpy(), o_ref) <= TOL[dtype]
+    assert rel_err(S.cpu().numpy(), S_ref) <= TOL["f32"]

@@ -204,3 +204,20 @@ def test_forward_without_saved_states_gives_the_same_bits(dtype):
                        run.o.view(torch.int16 if dtype == "bf16" else torch.int32))
     assert torch.equal(S_T2.view(torch.int32), run.S_T.view(torch.int32))
     assert bool((run.layer.saved_states == 7.0).all())
+
+
+@pytest.mark.parametrize("dtype,kw", [
+    ("bf16", dict(Hk=2, Hv=6, Dk=64, Dv=64, seqlens=(130, 70))),
+    ("f32", dict(Hk=2, Hv=6, Dk=32, Dv=64, seqlens=(100, 1))),
+    ("bf16", dict(Hk=4, Hv=8, Dk=128, Dv=128, seqlens=(200,))),
+], ids=["bf16_r3", "f32_r3", "bf16_r2_d128"])
+def test_modulo_head_map_against_the_oracle(dtype, kw):
+    """head_map = GDN_HEAD_MAP_MODULO (value head h reads key head h % Hk), forward and
+    backward (training step and recomputing backward), against the oracle's modulo map."""
+    wl = W.custom(dtype=dtype, seed=17, S0_std=0.3, dST_std=0.2, dt_bias_std=0.2, head_map=1,
+                  **kw)
+    inp = W.generate(wl)
+    _, run = _check_full(inp)
+    run.run_backward(train=False)
+    compare(run.host(), oracle_outputs(inp), TOL[dtype],
+            keys=["dq", "dk", "dv", "dalpha", "dbeta_raw", "da_log", "ddt_bias", "dS0"])

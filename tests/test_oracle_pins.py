@@ -265,6 +265,38 @@ def test_shared_key_head_equals_explicit_repeat():
         assert _rel(summed, g[key]) < 1e-13, key
 
 
+def test_modulo_head_map_equals_consecutive_map_on_permuted_heads():
+    """head_map 1 (value head h reads key head h % Hk) on some inputs == head_map 0 (key
+    head h // r) on the same inputs with the value heads renumbered: consecutive head
+    j = kh * r + i is modulo head kh + i * Hk.  Every per-head output is the renumbered
+    one and dq/dk (each key head's sum over its value heads, in the same order) agree."""
+    Hk, Hv, Dk, Dv, r = 2, 6, 4, 5, 3
+    wl, inp, a = _draw(Hk, Hv, Dk, Dv, (7, 4), 97)
+    perm = np.array([(j % r) * Hk + j // r for j in range(Hv)])   # modulo head of head j
+    cols = lambda x, D: np.concatenate([x[:, h * D:(h + 1) * D] for h in perm], 1)
+    b = dict(a, v=cols(a["v"], Dv), alpha=a["alpha"][:, perm], beta_raw=a["beta_raw"][:, perm],
+             a_log=a["a_log"][perm], dt_bias=a["dt_bias"][perm], S0=a["S0"][:, perm])
+    o, s = _fwd(wl, inp.cu_seqlens, a, head_map=1)
+    o1, s1 = _fwd(wl, inp.cu_seqlens, b, head_map=0)
+    assert np.array_equal(o1, cols(o, Dv)) and np.array_equal(s1, s[:, perm])
+    rng = np.random.default_rng(7)
+    dO = rng.standard_normal(o.shape)
+    dS = rng.standard_normal(s.shape)
+    g = _bwd(wl, inp.cu_seqlens, a, dO, dS, head_map=1)
+    g1 = _bwd(wl, inp.cu_seqlens, b, cols(dO, Dv), dS[:, perm], head_map=0)
+    assert np.array_equal(g1["dv"], cols(g["dv"], Dv))
+    for key in ("dalpha", "dbeta_raw"):
+        assert np.array_equal(g1[key], g[key][:, perm]), key
+    for key in ("da_log", "ddt_bias"):
+        assert np.array_equal(g1[key], g[key][perm]), key
+    assert np.array_equal(g1["dS0"], g["dS0"][:, perm])
+    for key in ("dq", "dk"):
+        assert np.array_equal(g1[key], g[key]), key
+    # and the two maps do differ on these inputs
+    o0, _ = _fwd(wl, inp.cu_seqlens, a, head_map=0)
+    assert not np.allclose(o0, o)
+
+
 def test_heads_and_sequences_are_independent():
     wl, inp, a = _draw(2, 2, 4, 3, (6, 9), 101)
     o, s = _fwd(wl, inp.cu_seqlens, a)

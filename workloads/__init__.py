@@ -46,6 +46,7 @@ class Workload:
     S0_std: float = 0.0         # 0 -> no initial state (S_0 = 0)
     dST_std: float = 0.0        # 0 -> no final-state adjoint (dS_T = 0)
     scale: Optional[float] = None  # None -> 1/sqrt(Dk)
+    head_map: int = 0           # key head of value head h: 0 -> h // (Hv // Hk), 1 -> h % Hk
 
     @property
     def n_seqs(self) -> int:
