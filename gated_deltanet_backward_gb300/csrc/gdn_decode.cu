@@ -12,11 +12,12 @@
 
 #include "gdn_device.cuh"
 #include "gdn_internal.cuh"
+#include "umma.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kDecodeThreads = 128;   // >= Dv: one thread per value column
+constexpr int kDecodeThreads = 128;
 
 struct DecodeParams {
   int Hk, Hv, Dk, Dv, r, head_map;
@@ -48,28 +49,39 @@ __device__ __forceinline__ void store_io(__nv_bfloat16* p, int64_t i, float x) {
   p[i] = __float2bfloat16_rn(x);
 }
 
-// One CTA per (sequence n, value head h): the state tile [Dk][Dv] in shared memory
-// (16-byte coalesced loads and stores), q_hat and k_hat of the value head's key head
-// (h / r, or h % Hk with the modulo head map), then
-// thread v forms column v: kv_v = sum_k S[k][v] k_hat[k], delta_v, the new column
-// and o_v.  S_in may equal S_out (the tile is read before anything is written).
-template <typename T>
+// One CTA per (sequence n, value head h, slice of VS value columns): the state columns
+// of the slice ([Dk][VS], 16-byte asynchronous copies, all in flight at once) in shared
+// memory, q_hat and k_hat of the value head's key head (h / r, or h % Hk with the
+// modulo head map), then thread (part, v) of the slice's VS columns and 128 / VS
+// row parts forms its share of kv_v = sum_k S[k][v] k_hat[k]; the parts are summed in
+// a fixed order, every part updates its rows of column v and adds its share of
+// o_v = sum_k S'[k][v] q_hat[k].  Columns are independent, so the slices are too.
+// S_in may equal S_out (a CTA reads its slice before it writes it, and no other CTA
+// touches it).
+template <typename T, int VS>
 __global__ void __launch_bounds__(kDecodeThreads) k_decode(DecodeParams p) {
+  constexpr int KP = kDecodeThreads / VS;       // row parts
   extern __shared__ float4 dsm4[];
-  float* S = (float*)dsm4;                      // [Dk][Dv]
-  float* qs = S + p.Dk * p.Dv;                  // [Dk] q, then q_hat
+  float* S = (float*)dsm4;                      // [Dk][VS]
+  float* qs = S + p.Dk * VS;                    // [Dk] q, then q_hat
   float* ks = qs + p.Dk;                        // [Dk] k, then k_hat
-  float* red = ks + p.Dk;                       // [2][kDecodeThreads / 32]
-  const int n = blockIdx.x, h = blockIdx.y, kh = p.head_map ? h % p.Hk : h / p.r;
+  float* red = ks + p.Dk;                       // [2][kDecodeThreads / 32] norms
+  float* part = red + 2 * (kDecodeThreads / 32);  // [KP][VS] partial sums
+  const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VS;
+  const int kh = p.head_map ? h % p.Hk : h / p.r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Dk = p.Dk, Dv = p.Dv;
-  const size_t SZ = (size_t)Dk * Dv;
-  const size_t so = ((size_t)n * p.Hv + h) * SZ;
+  const size_t so = ((size_t)n * p.Hv + h) * (size_t)Dk * Dv + v0;   // column v0 of row 0
   const T* q = (const T*)p.q + (int64_t)n * p.q_ld + (int64_t)kh * Dk;
   const T* k = (const T*)p.k + (int64_t)n * p.k_ld + (int64_t)kh * Dk;
 
-  for (int i = tid; i < (int)(SZ / 4); i += kDecodeThreads)
-    dsm4[i] = p.S_in ? ((const float4*)(p.S_in + so))[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int C4 = VS / 4;                    // 16-byte pieces of a slice row
+  if (p.S_in) {
+    for (int i = tid; i < Dk * C4; i += kDecodeThreads)
+      tc::cp_async16(dsm4 + i, (const float4*)(p.S_in + so + (size_t)(i / C4) * Dv) + i % C4);
+  } else {
+    for (int i = tid; i < Dk * C4; i += kDecodeThreads) dsm4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float sq = 0.f, sk = 0.f;
   for (int i = tid; i < Dk; i += kDecodeThreads) {
     const float qf = load_io(q, i), kf = load_io(k, i);
@@ -96,26 +108,38 @@ __global__ void __launch_bounds__(kDecodeThreads) k_decode(DecodeParams p) {
     qs[i] *= iq;
     ks[i] *= ik;
   }
+  tc::cp_async_wait_all();   // this thread's share of the slice has landed
   __syncthreads();
-  if (tid < Dv) {
-    const int v = tid;
-    const float x = p.alpha[(int64_t)n * p.alpha_ld + h] + p.dt_bias[h];
-    const float g = expf(-expf(p.a_log[h]) * softplus_f(x));
-    const float b = sigmoid_f(p.beta_raw[(int64_t)n * p.beta_ld + h]);
-    float kv = 0.f;
-    for (int kk = 0; kk < Dk; ++kk) kv = fmaf(S[kk * Dv + v], ks[kk], kv);
-    const float d = b * (load_io((const T*)p.v + (int64_t)n * p.v_ld + (int64_t)h * Dv, v) - g * kv);
-    float o = 0.f;
-    for (int kk = 0; kk < Dk; ++kk) {
-      const float s = fmaf(g, S[kk * Dv + v], ks[kk] * d);
-      S[kk * Dv + v] = s;
-      o = fmaf(s, qs[kk], o);
-    }
+  const int vl = tid % VS, kp = tid / VS, v = v0 + vl;
+  const int rows = Dk / KP, r0 = kp * rows;
+  float kv = 0.f;
+  for (int kk = r0; kk < r0 + rows; ++kk) kv = fmaf(S[kk * VS + vl], ks[kk], kv);
+  part[kp * VS + vl] = kv;
+  __syncthreads();
+  kv = 0.f;
+#pragma unroll
+  for (int j = 0; j < KP; ++j) kv += part[j * VS + vl];
+  const float x = p.alpha[(int64_t)n * p.alpha_ld + h] + p.dt_bias[h];
+  const float g = expf(-expf(p.a_log[h]) * softplus_f(x));
+  const float b = sigmoid_f(p.beta_raw[(int64_t)n * p.beta_ld + h]);
+  const float d = b * (load_io((const T*)p.v + (int64_t)n * p.v_ld + (int64_t)h * Dv, v) - g * kv);
+  float o = 0.f;
+  for (int kk = r0; kk < r0 + rows; ++kk) {
+    const float sv = fmaf(g, S[kk * VS + vl], ks[kk] * d);
+    S[kk * VS + vl] = sv;
+    o = fmaf(sv, qs[kk], o);
+  }
+  __syncthreads();   // every part has read the kv partials
+  part[kp * VS + vl] = o;
+  __syncthreads();
+  if (kp == 0) {
+    o = 0.f;
+#pragma unroll
+    for (int j = 0; j < KP; ++j) o += part[j * VS + vl];
     store_io((T*)p.o + (int64_t)n * p.o_ld + (int64_t)h * Dv, v, p.scale * o);
   }
-  __syncthreads();
-  for (int i = tid; i < (int)(SZ / 4); i += kDecodeThreads)
-    ((float4*)(p.S_out + so))[i] = dsm4[i];
+  for (int i = tid; i < Dk * C4; i += kDecodeThreads)
+    ((float4*)(p.S_out + so + (size_t)(i / C4) * Dv))[i % C4] = dsm4[i];
 }
 
 }  // namespace
@@ -149,16 +173,22 @@ cudaError_t launch_decode(const gdn_shape* s, const void* q, int64_t q_ld, const
   p.S_out = S_out;
   p.o = o;
   p.o_ld = o_ld;
-  const size_t smem = sizeof(float) * ((size_t)s->Dk * s->Dv + 2 * s->Dk + 2 * kDecodeThreads / 32);
-  const dim3 grid((unsigned)s->n_seqs, (unsigned)s->Hv);
+  // slices of 32 value columns (16 for Dv = 16), 128 / VS row parts each
+  const int VS = s->Dv >= 32 ? 32 : 16;
+  const size_t smem = sizeof(float) * ((size_t)s->Dk * VS + 2 * s->Dk + 2 * kDecodeThreads / 32 +
+                                       kDecodeThreads);
+  const dim3 grid((unsigned)s->n_seqs, (unsigned)s->Hv, (unsigned)(s->Dv / VS));
   profile_pre(st, KID_DECODE);
   if (s->dtype == GDN_DTYPE_BF16) {
-    cudaFuncSetAttribute(k_decode<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    k_decode<__nv_bfloat16><<<grid, kDecodeThreads, smem, st>>>(p);
+    if (VS == 32)
+      k_decode<__nv_bfloat16, 32><<<grid, kDecodeThreads, smem, st>>>(p);
+    else
+      k_decode<__nv_bfloat16, 16><<<grid, kDecodeThreads, smem, st>>>(p);
   } else {
-    cudaFuncSetAttribute(k_decode<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_decode<float><<<grid, kDecodeThreads, smem, st>>>(p);
+    if (VS == 32)
+      k_decode<float, 32><<<grid, kDecodeThreads, smem, st>>>(p);
+    else
+      k_decode<float, 16><<<grid, kDecodeThreads, smem, st>>>(p);
   }
   profile_post(st);
   return cudaGetLastError();
