@@ -195,3 +195,74 @@ def run_inputs(inp, which="both", n_threads=0, segment=64):
         bwd = backward(inp.q, inp.k, inp.v, inp.alpha, inp.beta_raw, inp.a_log, inp.dt_bias,
                        inp.cu_seqlens, inp.dO, inp.S0, inp.dS_T, segment=segment, **kw)
     return fwd, bwd
+
+
+# ---------------------------------------------------------------------------
+# The layer steps on either side of the recurrence (causal depthwise conv1d + SiLU
+# before q/k/v, gated RMSNorm after o), f64.
+def _i32p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def conv1d_silu_forward(x, w, cu_seqlens):
+    """y[t, ch] = SiLU(sum_j w[ch, j] x[t - (K-1) + j, ch]), inputs before a sequence's start
+    read as zero.  x [T, C], w [C, K]."""
+    x = _f64(x)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    T, C = x.shape
+    y = np.zeros((T, C))
+    rc = _load().gdn_oracle_conv1d_silu_forward(
+        ctypes.c_int64(T), ctypes.c_int32(C), ctypes.c_int32(w.shape[1]),
+        ctypes.c_int32(len(cu) - 1), _i32p(cu), _ptr(x), ctypes.c_int64(_ld(x)), _ptr(w),
+        _ptr(y), ctypes.c_int64(C))
+    if rc != 0:
+        raise ValueError("gdn_oracle_conv1d_silu_forward rejected its arguments")
+    return y
+
+
+def conv1d_silu_backward(x, w, cu_seqlens, dy):
+    """Returns (dx [T, C], dw [C, K])."""
+    x, dy = _f64(x), _f64(dy)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    T, C = x.shape
+    dx = np.zeros((T, C))
+    dw = np.zeros_like(w)
+    rc = _load().gdn_oracle_conv1d_silu_backward(
+        ctypes.c_int64(T), ctypes.c_int32(C), ctypes.c_int32(w.shape[1]),
+        ctypes.c_int32(len(cu) - 1), _i32p(cu), _ptr(x), ctypes.c_int64(_ld(x)), _ptr(w),
+        _ptr(dy), ctypes.c_int64(_ld(dy)), _ptr(dx), ctypes.c_int64(C), _ptr(dw))
+    if rc != 0:
+        raise ValueError("gdn_oracle_conv1d_silu_backward rejected its arguments")
+    return dx, dw
+
+
+def gated_rmsnorm_forward(o, z, gamma, H, D, eps):
+    """y = (o / rms(o)) gamma SiLU(z) per (token, head); o, z [T, H*D], gamma [D]."""
+    o, z = _f64(o), _f64(z)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float64)
+    y = np.zeros((o.shape[0], H * D))
+    rc = _load().gdn_oracle_gated_rmsnorm_forward(
+        ctypes.c_int64(o.shape[0]), ctypes.c_int32(H), ctypes.c_int32(D), ctypes.c_double(eps),
+        _ptr(o), ctypes.c_int64(_ld(o)), _ptr(z), ctypes.c_int64(_ld(z)), _ptr(gamma), _ptr(y),
+        ctypes.c_int64(H * D))
+    if rc != 0:
+        raise ValueError("gdn_oracle_gated_rmsnorm_forward rejected its arguments")
+    return y
+
+
+def gated_rmsnorm_backward(o, z, gamma, dy, H, D, eps):
+    """Returns (do, dz [T, H*D], dgamma [D])."""
+    o, z, dy = _f64(o), _f64(z), _f64(dy)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float64)
+    T = o.shape[0]
+    d_o, dz, dg = np.zeros((T, H * D)), np.zeros((T, H * D)), np.zeros(D)
+    rc = _load().gdn_oracle_gated_rmsnorm_backward(
+        ctypes.c_int64(T), ctypes.c_int32(H), ctypes.c_int32(D), ctypes.c_double(eps), _ptr(o),
+        ctypes.c_int64(_ld(o)), _ptr(z), ctypes.c_int64(_ld(z)), _ptr(gamma), _ptr(dy),
+        ctypes.c_int64(_ld(dy)), _ptr(d_o), ctypes.c_int64(H * D), _ptr(dz),
+        ctypes.c_int64(H * D), _ptr(dg))
+    if rc != 0:
+        raise ValueError("gdn_oracle_gated_rmsnorm_backward rejected its arguments")
+    return d_o, dz, dg

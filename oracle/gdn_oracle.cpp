@@ -21,7 +21,7 @@
 //     gate backward, L2-norm backward, accumulation over the value heads that
 //     share a key head, sigmoid backward).  d_beta is formed without dividing by
 //     beta, as step 4c there does.
-// Readings where the page is silent (each is listed in the design doc):
+// Readings where the page is silent:
 //   * S_0 and dS_T are inputs (zero when absent); dS_0 is returned.
 //   * d a_log[h] = sum over every token of every sequence of dl * l (dl/d a_log
 //     = l because l = -exp(a_log) softplus(x)); d dt_bias[h] = sum of d alpha.
@@ -383,5 +383,131 @@ extern "C" int gdn_oracle_backward(const gdn_oracle_shape* shape, const gdn_orac
     da_log[h] = a;
     ddt_bias[h] = b;
   }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// The layer steps on either side of the recurrence, from the forward of lattice-inference
+// 0.6.0, src/attention/gdn_backward.rs (its "Causal conv1d + SiLU" and "Gated RMSNorm +
+// output projection" steps) and its backward (sections 2 and 5), in f64 with plain loops.  Readings where the page is silent:
+//   * the conv's rolling buffer starts at zero at every sequence start (varlen);
+//   * the weight gradients dw (conv) and dgamma (norm), which the page does not form
+//     (its base weights are frozen), are the sums over every token of the products
+//     the forward multiplies the weights into;
+//   * rms_eps is an argument.
+
+namespace {
+double silu(double x) { return x / (1.0 + std::exp(-x)); }
+double silu_grad(double x) {  // d/dx x sigmoid(x) = sigmoid(x) (1 + x (1 - sigmoid(x)))
+  const double s = 1.0 / (1.0 + std::exp(-x));
+  return s * (1.0 + x * (1.0 - s));
+}
+// Pre-activation of channel ch at token t (sequence start t_start): the page's
+// sum_pre = sum_tb buf[ch,tb] w[ch*K + tb] + x[t][ch] w[ch*K + K-1], buf[ch,tb] the
+// input K-1-tb tokens back (zero before the sequence start).
+double conv_pre(const double* x, int64_t x_ld, const double* w, int K, int ch, int64_t t,
+                int64_t t_start) {
+  double s = 0.0;
+  for (int j = 0; j < K; ++j) {
+    const int64_t src = t - (K - 1 - j);
+    if (src >= t_start) s += x[src * x_ld + ch] * w[(int64_t)ch * K + j];
+  }
+  return s;
+}
+bool check_cu(int32_t n_seqs, const int32_t* cu, int64_t T) {
+  if (!cu || n_seqs < 0 || cu[0] != 0 || cu[n_seqs] != T) return false;
+  for (int n = 0; n < n_seqs; ++n)
+    if (cu[n + 1] < cu[n]) return false;
+  return true;
+}
+}  // namespace
+
+extern "C" int gdn_oracle_conv1d_silu_forward(int64_t T, int32_t C, int32_t K, int32_t n_seqs,
+                                               const int32_t* cu, const double* x, int64_t x_ld,
+                                               const double* w, double* y, int64_t y_ld) {
+  if (C <= 0 || K <= 0 || !x || !w || !y || !check_cu(n_seqs, cu, T)) return -1;
+  for (int n = 0; n < n_seqs; ++n)
+    for (int64_t t = cu[n]; t < cu[n + 1]; ++t)
+      for (int ch = 0; ch < C; ++ch)
+        y[t * y_ld + ch] = silu(conv_pre(x, x_ld, w, K, ch, t, cu[n]));
+  return 0;
+}
+
+// Backward (the page's section 5): d_sum = dy * SiLU'(sum_pre); the input K-1-j tokens
+// before an output gets d_sum * w[ch*K + j]; dw[ch*K + j] sums d_sum times that input.
+extern "C" int gdn_oracle_conv1d_silu_backward(int64_t T, int32_t C, int32_t K, int32_t n_seqs,
+                                                const int32_t* cu, const double* x, int64_t x_ld,
+                                                const double* w, const double* dy, int64_t dy_ld,
+                                                double* dx, int64_t dx_ld, double* dw) {
+  if (C <= 0 || K <= 0 || !x || !w || !dy || !dx || !check_cu(n_seqs, cu, T)) return -1;
+  for (int64_t t = 0; t < T; ++t)
+    for (int ch = 0; ch < C; ++ch) dx[t * dx_ld + ch] = 0.0;
+  if (dw)
+    for (int64_t i = 0; i < (int64_t)C * K; ++i) dw[i] = 0.0;
+  for (int n = 0; n < n_seqs; ++n)
+    for (int64_t t = cu[n]; t < cu[n + 1]; ++t)
+      for (int ch = 0; ch < C; ++ch) {
+        const double d_sum = dy[t * dy_ld + ch] * silu_grad(conv_pre(x, x_ld, w, K, ch, t, cu[n]));
+        for (int j = 0; j < K; ++j) {
+          const int64_t src = t - (K - 1 - j);
+          if (src < cu[n]) continue;
+          dx[src * dx_ld + ch] += d_sum * w[(int64_t)ch * K + j];
+          if (dw) dw[(int64_t)ch * K + j] += d_sum * x[src * x_ld + ch];
+        }
+      }
+  return 0;
+}
+
+// Gated RMSNorm of every (token, value head): rms = sqrt(mean_j o_j^2 + eps),
+// y_j = (o_j / rms) gamma_j SiLU(z_j), gamma shared by the heads.
+extern "C" int gdn_oracle_gated_rmsnorm_forward(int64_t T, int32_t H, int32_t D, double eps,
+                                                 const double* o, int64_t o_ld, const double* z,
+                                                 int64_t z_ld, const double* gamma, double* y,
+                                                 int64_t y_ld) {
+  if (T < 0 || H <= 0 || D <= 0 || !o || !z || !gamma || !y) return -1;
+  for (int64_t t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h) {
+      const double* oh = o + t * o_ld + (int64_t)h * D;
+      const double* zh = z + t * z_ld + (int64_t)h * D;
+      double ss = 0.0;
+      for (int j = 0; j < D; ++j) ss += oh[j] * oh[j];
+      const double rms = std::sqrt(ss / D + eps);
+      for (int j = 0; j < D; ++j) y[t * y_ld + (int64_t)h * D + j] = oh[j] / rms * gamma[j] * silu(zh[j]);
+    }
+  return 0;
+}
+
+// Backward (the page's section 2): d_xnorm = dy gamma SiLU(z); dz = dy gamma x_norm
+// SiLU'(z); do = d_xnorm / rms - o (sum_k d_xnorm_k o_k) / (rms^3 D); dgamma sums
+// dy x_norm SiLU(z) over every token and head.
+extern "C" int gdn_oracle_gated_rmsnorm_backward(int64_t T, int32_t H, int32_t D, double eps,
+                                                  const double* o, int64_t o_ld, const double* z,
+                                                  int64_t z_ld, const double* gamma,
+                                                  const double* dy, int64_t dy_ld, double* d_o,
+                                                  int64_t do_ld, double* dz, int64_t dz_ld,
+                                                  double* dgamma) {
+  if (T < 0 || H <= 0 || D <= 0 || !o || !z || !gamma || !dy || !d_o || !dz) return -1;
+  if (dgamma)
+    for (int j = 0; j < D; ++j) dgamma[j] = 0.0;
+  std::vector<double> dxn(D);
+  for (int64_t t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h) {
+      const double* oh = o + t * o_ld + (int64_t)h * D;
+      const double* zh = z + t * z_ld + (int64_t)h * D;
+      const double* dg = dy + t * dy_ld + (int64_t)h * D;
+      double ss = 0.0;
+      for (int j = 0; j < D; ++j) ss += oh[j] * oh[j];
+      const double rms = std::sqrt(ss / D + eps);
+      double dot = 0.0;
+      for (int j = 0; j < D; ++j) {
+        const double xn = oh[j] / rms;
+        dxn[j] = dg[j] * gamma[j] * silu(zh[j]);
+        dz[t * dz_ld + (int64_t)h * D + j] = dg[j] * gamma[j] * xn * silu_grad(zh[j]);
+        if (dgamma) dgamma[j] += dg[j] * xn * silu(zh[j]);
+        dot += dxn[j] * oh[j];
+      }
+      for (int j = 0; j < D; ++j)
+        d_o[t * do_ld + (int64_t)h * D + j] = dxn[j] / rms - oh[j] * dot / (rms * rms * rms * D);
+    }
   return 0;
 }
