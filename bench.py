@@ -403,6 +403,8 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_decode:
         result["decode"] = run_decode(wl, device, pk)
+    if rank == 0 and world == 1 and not args.no_layer_steps:
+        result["layer_steps"] = run_layer_steps(wl, device, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
     if rank == 0:
@@ -449,6 +451,73 @@ def run_decode(wl, device, pk, n_seqs=64, steps=50, warmup=5):
             "frac": gbs / pk["hbm_gbs"], "bound": "hbm",
             "note": "gdn_decode_step, one token per sequence, state in place; "
                     "value head shape of the workload"}
+
+
+def run_layer_steps(wl, device, pk, K=4, eps=1e-6, steps=10, warmup=3):
+    """The layer steps either side of the recurrence at the workload's layer shape: the
+    causal conv1d + SiLU over the packed q|k|v rows (C = 2 Hk Dk + Hv Dv channels, kernel
+    K) and the gated RMSNorm over the Hv heads of o, forward and backward (weight
+    gradients included).  Each kernel is timed alone with CUDA events around its own
+    launch, after a 256 MB write that flushes the L2; bytes are the algorithmic ones
+    (every operand read once, every result written once).  Synthetic inputs (N(0, 1)
+    activations, conv weights U(-0.05, 0.05), norm weights U(0.9, 1.1)), resident."""
+    import torch
+    import gated_deltanet_backward_gb300 as gdn
+    T, Hk, Hv, Dk, Dv = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv
+    C, Wd = 2 * Hk * Dk + Hv * Dv, Hv * Dv
+    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    es = 2 if wl.dtype == "bf16" else 4
+    g = torch.Generator(device=device).manual_seed(4321)
+    rn = lambda *sh: torch.randn(*sh, generator=g, device=device).to(td)
+    x, dyc = rn(T, C), rn(T, C)
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    w = (torch.rand(C, K, generator=g, device=device) * 2 - 1) * 0.05
+    dw = torch.empty_like(w)
+    o, z, dyn = rn(T, Wd), rn(T, Wd), rn(T, Wd)
+    yn, d_o, dz = torch.empty_like(o), torch.empty_like(o), torch.empty_like(o)
+    gamma = 0.9 + 0.2 * torch.rand(Dv, generator=g, device=device)
+    dg = torch.empty_like(gamma)
+    cu_h = np.asarray([0] + list(np.cumsum(wl.seqlens)), dtype=np.int32)
+    cu = torch.from_numpy(cu_h).to(device)
+    ws_c = torch.empty(max(256, gdn.gdn_conv1d_silu_workspace_bytes(T, C, K)), dtype=torch.uint8,
+                       device=device)
+    ws_n = torch.empty(gdn.gdn_gated_rmsnorm_workspace_bytes(Dv), dtype=torch.uint8,
+                       device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=device)
+    calls = {
+        "conv1d_silu_fwd": (lambda: gdn.gdn_conv1d_silu_forward(x, w, cu, y),
+                            2 * T * C * es + C * K * 4),
+        "conv1d_silu_bwd": (lambda: gdn.gdn_conv1d_silu_backward(x, w, cu, dyc, dx, dw, ws_c),
+                            3 * T * C * es + 2 * C * K * 4),
+        "gated_rmsnorm_fwd": (lambda: gdn.gdn_gated_rmsnorm_forward(o, z, gamma, yn, eps),
+                              3 * T * Wd * es + Dv * 4),
+        "gated_rmsnorm_bwd": (lambda: gdn.gdn_gated_rmsnorm_backward(o, z, gamma, dyn, d_o, dz,
+                                                                     eps, dg, ws_n),
+                              5 * T * Wd * es + 2 * Dv * 4),
+    }
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(warmup):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"us": us, "bytes": nbytes, "achieved_gbs": gbs,
+                     "frac": gbs / pk["hbm_gbs"], "bound": "hbm"}
+    out["shape"] = {"tokens": T, "channels": C, "kernel_size": K, "heads": Hv, "head_dim": Dv,
+                    "dtype": wl.dtype}
+    out["note"] = ("each call timed alone (the weight-gradient partial sums inside the "
+                   "backward calls), L2 flushed before every launch")
+    return out
 
 
 def run_e2e(args, inp, layer, device, tdt, world):
@@ -583,6 +652,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-layer-steps", action="store_true",
+                    help="skip the conv1d + SiLU / gated RMSNorm measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -79,6 +79,25 @@ _lib.gdn_forward_noalloc.restype = ctypes.c_int
 # shape; q,k,v,alpha,beta_raw (+ld); a_log, dt_bias, S_in, S_out; o (+ld); stream
 _lib.gdn_decode_step.argtypes = [_SP] + [_vp, _i64] * 5 + [_vp] * 4 + [_vp, _i64, _vp]
 _lib.gdn_decode_step.restype = ctypes.c_int
+_lib.gdn_conv1d_silu_forward.argtypes = ([ctypes.c_int32, _i64, ctypes.c_int32, ctypes.c_int32,
+                                          _vp, ctypes.c_int32, _vp, _i64, _vp, _vp, _i64, _vp])
+_lib.gdn_conv1d_silu_forward.restype = ctypes.c_int
+_lib.gdn_conv1d_silu_workspace_bytes.argtypes = [_i64, ctypes.c_int32, ctypes.c_int32]
+_lib.gdn_conv1d_silu_workspace_bytes.restype = _sz
+_lib.gdn_conv1d_silu_backward.argtypes = ([ctypes.c_int32, _i64, ctypes.c_int32, ctypes.c_int32,
+                                           _vp, ctypes.c_int32, _vp, _i64, _vp, _vp, _i64, _vp,
+                                           _i64, _vp, _vp, _sz, _vp])
+_lib.gdn_conv1d_silu_backward.restype = ctypes.c_int
+_lib.gdn_gated_rmsnorm_forward.argtypes = ([ctypes.c_int32, _i64, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_float] + [_vp, _i64] * 2 + [_vp, _vp, _i64,
+                                                                                 _vp])
+_lib.gdn_gated_rmsnorm_forward.restype = ctypes.c_int
+_lib.gdn_gated_rmsnorm_workspace_bytes.argtypes = [ctypes.c_int32]
+_lib.gdn_gated_rmsnorm_workspace_bytes.restype = _sz
+_lib.gdn_gated_rmsnorm_backward.argtypes = ([ctypes.c_int32, _i64, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_float] + [_vp, _i64] * 2 + [_vp] +
+                                            [_vp, _i64] * 3 + [_vp, _vp, _sz, _vp])
+_lib.gdn_gated_rmsnorm_backward.restype = ctypes.c_int
 _lib.gdn_read_device_status.argtypes = [_vp, _vp]
 _lib.gdn_read_device_status.restype = ctypes.c_int
 _lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -95,7 +114,9 @@ _lib.gdn_kernel_name.restype = ctypes.c_char_p
 EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_forward",
             "gdn_backward", "gdn_read_device_status", "gdn_status_string", "gdn_profile_begin",
             "gdn_profile_end", "gdn_kernel_name", "gdn_last_error", "gdn_forward_noalloc",
-            "gdn_decode_step")
+            "gdn_decode_step", "gdn_conv1d_silu_forward", "gdn_conv1d_silu_workspace_bytes",
+            "gdn_conv1d_silu_backward", "gdn_gated_rmsnorm_forward",
+            "gdn_gated_rmsnorm_workspace_bytes", "gdn_gated_rmsnorm_backward")
 
 
 class GdnError(RuntimeError):
@@ -232,6 +253,80 @@ def gdn_decode_step(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, S_in, S_out
     args += list(_mat(o))
     args += [_stream(stream)]
     _check(_lib.gdn_decode_step(*args), "gdn_decode_step")
+
+
+def _dtype_code(t) -> int:
+    """gdn_dtype of a tensor: 1 for bfloat16, 0 for float32 (others are passed as -1, which
+    the library rejects)."""
+    name = str(t.dtype)
+    return 1 if name == "torch.bfloat16" else 0 if name == "torch.float32" else -1
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else int(t.numel() * t.element_size())
+
+
+def gdn_conv1d_silu_workspace_bytes(total_tokens: int, channels: int, kernel_size: int) -> int:
+    return int(_lib.gdn_conv1d_silu_workspace_bytes(int(total_tokens), int(channels),
+                                                    int(kernel_size)))
+
+
+def gdn_conv1d_silu_forward(x, w, cu_seqlens, y, stream=None) -> None:
+    """Calls gdn_conv1d_silu_forward: x, y [T, C] (row strides taken from the tensors),
+    w [C, K] fp32, cu_seqlens int32 [n_seqs + 1] on the device."""
+    C, K = int(w.shape[0]), int(w.shape[1])
+    xp, xld = _mat(x)
+    yp, yld = _mat(y)
+    _check(_lib.gdn_conv1d_silu_forward(_dtype_code(x), int(x.shape[0]), C, K, _ptr(cu_seqlens),
+                                        int(cu_seqlens.numel()) - 1, xp, xld, _ptr(w), yp, yld,
+                                        _stream(stream)), "gdn_conv1d_silu_forward")
+
+
+def gdn_conv1d_silu_backward(x, w, cu_seqlens, dy, dx, dw=None, workspace=None,
+                             stream=None) -> None:
+    """Calls gdn_conv1d_silu_backward; dw (fp32 [C, K]) needs a workspace of
+    gdn_conv1d_silu_workspace_bytes(T, C, K) bytes."""
+    C, K = int(w.shape[0]), int(w.shape[1])
+    xp, xld = _mat(x)
+    gp, gld = _mat(dy)
+    dp, dld = _mat(dx)
+    _check(_lib.gdn_conv1d_silu_backward(_dtype_code(x), int(x.shape[0]), C, K,
+                                         _ptr(cu_seqlens), int(cu_seqlens.numel()) - 1, xp, xld,
+                                         _ptr(w), gp, gld, dp, dld, _ptr(dw), _ptr(workspace),
+                                         _nbytes(workspace), _stream(stream)),
+           "gdn_conv1d_silu_backward")
+
+
+def gdn_gated_rmsnorm_workspace_bytes(head_dim: int) -> int:
+    return int(_lib.gdn_gated_rmsnorm_workspace_bytes(int(head_dim)))
+
+
+def gdn_gated_rmsnorm_forward(o, z, gamma, y, eps, stream=None) -> None:
+    """Calls gdn_gated_rmsnorm_forward: o, z, y [T, H*D] with D = gamma.numel()."""
+    D = int(gamma.numel())
+    H = int(o.shape[1]) // D
+    op, old = _mat(o)
+    zp, zld = _mat(z)
+    yp, yld = _mat(y)
+    _check(_lib.gdn_gated_rmsnorm_forward(_dtype_code(o), int(o.shape[0]), H, D, float(eps), op,
+                                          old, zp, zld, _ptr(gamma), yp, yld, _stream(stream)),
+           "gdn_gated_rmsnorm_forward")
+
+
+def gdn_gated_rmsnorm_backward(o, z, gamma, dy, d_o, dz, eps, dgamma=None, workspace=None,
+                               stream=None) -> None:
+    """Calls gdn_gated_rmsnorm_backward; dgamma (fp32 [D]) needs a workspace of
+    gdn_gated_rmsnorm_workspace_bytes(D) bytes."""
+    D = int(gamma.numel())
+    H = int(o.shape[1]) // D
+    args = [_dtype_code(o), int(o.shape[0]), H, D, float(eps)]
+    for t in (o, z):
+        args += list(_mat(t))
+    args += [_ptr(gamma)]
+    for t in (dy, d_o, dz):
+        args += list(_mat(t))
+    args += [_ptr(dgamma), _ptr(workspace), _nbytes(workspace), _stream(stream)]
+    _check(_lib.gdn_gated_rmsnorm_backward(*args), "gdn_gated_rmsnorm_backward")
 
 
 def gdn_read_device_status(workspace, stream=None) -> int:

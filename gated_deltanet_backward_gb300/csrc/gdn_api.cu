@@ -60,11 +60,52 @@ int check_vec(const void* p, bool required) {
   return GDN_OK;
 }
 
+// Byte ranges of two [rows, ld] matrices (width used columns) intersect.
+bool overlaps(const void* a, int64_t a_ld, const void* b, int64_t b_ld, int64_t rows,
+              int64_t width, size_t esize) {
+  if (!a || !b || rows == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  const uintptr_t a1 = a0 + ((size_t)(rows - 1) * a_ld + width) * esize;
+  const uintptr_t b1 = b0 + ((size_t)(rows - 1) * b_ld + width) * esize;
+  return a0 < b1 && b0 < a1;
+}
+
+int check_dtype(int32_t dtype, size_t* esize) {
+  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_UNSUPPORTED;
+  *esize = dtype == GDN_DTYPE_BF16 ? 2 : 4;
+  return GDN_OK;
+}
+
+int check_scratch(const void* ws, size_t bytes, size_t need) {
+  if (need == 0) return GDN_OK;
+  if (!ws || bytes < need) return GDN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return GDN_ERR_WORKSPACE;
+  return GDN_OK;
+}
+
 #define GDN_TRY(x)                 \
   do {                             \
     const int _rc = (x);           \
     if (_rc != GDN_OK) return _rc; \
   } while (0)
+
+int check_conv(int32_t dtype, int64_t T, int32_t C, int32_t K, const int32_t* cu, int32_t n_seqs,
+               const float* w, size_t* es) {
+  GDN_TRY(check_dtype(dtype, es));
+  if (T < 0 || C <= 0 || n_seqs < 0 || (T > 0 && n_seqs == 0)) return GDN_ERR_INVALID_ARG;
+  if (K < 1 || K > 4 || C % 8 != 0) return GDN_ERR_UNSUPPORTED;
+  if (T > 0 && !cu) return GDN_ERR_INVALID_ARG;
+  if (cu && ((uintptr_t)cu & 3u) != 0) return GDN_ERR_MISALIGNED;
+  return check_vec(w, true);
+}
+
+int check_norm(int32_t dtype, int64_t T, int32_t H, int32_t D, float eps, const float* gamma,
+               size_t* es) {
+  GDN_TRY(check_dtype(dtype, es));
+  if (T < 0 || H <= 0 || !(eps >= 0.f) || eps > 3.0e38f) return GDN_ERR_INVALID_ARG;
+  if (!head_size_ok(D)) return GDN_ERR_UNSUPPORTED;
+  return check_vec(gamma, true);
+}
 
 void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
                  int64_t k_ld, const void* v, int64_t v_ld, const float* alpha, int64_t alpha_ld,
@@ -309,6 +350,11 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_FWD_FUSED_TC: return "gdn_fwd_fused_tc";
     case gdn::KID_BWD_FUSED_TC: return "gdn_bwd_fused_tc";
     case gdn::KID_DECODE: return "gdn_decode";
+    case gdn::KID_CONV_FWD: return "gdn_conv1d_silu_fwd";
+    case gdn::KID_CONV_BWD: return "gdn_conv1d_silu_bwd";
+    case gdn::KID_NORM_FWD: return "gdn_gated_rmsnorm_fwd";
+    case gdn::KID_NORM_BWD: return "gdn_gated_rmsnorm_bwd";
+    case gdn::KID_SUM_PARTS: return "gdn_sum_partials";
     default: return "?";
   }
 }
@@ -516,6 +562,130 @@ int gdn_decode_step(const gdn_shape* s, const void* q, int64_t q_ld, const void*
                                            beta_raw, beta_ld, a_log, dt_bias, S_in, S_out, o,
                                            o_ld, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail("gdn_decode_step: kernel launch", e);
+  return GDN_OK;
+}
+
+size_t gdn_conv1d_silu_workspace_bytes(int64_t total_tokens, int32_t channels,
+                                       int32_t kernel_size) {
+  if (total_tokens <= 0 || channels <= 0 || kernel_size <= 0) return 0;
+  return gdn::align256(gdn::conv_partial_floats(total_tokens, channels, kernel_size) * 4);
+}
+
+size_t gdn_gated_rmsnorm_workspace_bytes(int32_t head_dim) {
+  if (head_dim <= 0) return 0;
+  return gdn::align256(gdn::norm_partial_floats(head_dim) * 4);
+}
+
+int gdn_conv1d_silu_forward(int32_t dtype, int64_t total_tokens, int32_t channels,
+                            int32_t kernel_size, const int32_t* cu_seqlens, int32_t n_seqs,
+                            const void* x, int64_t x_ld, const float* w, void* y, int64_t y_ld,
+                            void* stream) {
+  size_t es = 0;
+  const int64_t T = total_tokens;
+  GDN_TRY(check_conv(dtype, T, channels, kernel_size, cu_seqlens, n_seqs, w, &es));
+  GDN_TRY(check_matrix(x, x_ld, channels, es, T));
+  GDN_TRY(check_matrix(y, y_ld, channels, es, T));
+  if (overlaps(x, x_ld, y, y_ld, T, channels, es)) return GDN_ERR_INVALID_ARG;
+  if (T == 0) return GDN_OK;
+  (void)cudaGetLastError();
+  g_last_error[0] = 0;
+  const cudaError_t e = gdn::launch_conv1d_silu(
+      false, dtype, T, channels, kernel_size, cu_seqlens, n_seqs, x, x_ld, w, nullptr, 0, y, y_ld,
+      nullptr, nullptr, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("gdn_conv1d_silu_forward: kernel launch", e);
+  return GDN_OK;
+}
+
+int gdn_conv1d_silu_backward(int32_t dtype, int64_t total_tokens, int32_t channels,
+                             int32_t kernel_size, const int32_t* cu_seqlens, int32_t n_seqs,
+                             const void* x, int64_t x_ld, const float* w, const void* dy,
+                             int64_t dy_ld, void* dx, int64_t dx_ld, float* dw, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  size_t es = 0;
+  const int64_t T = total_tokens;
+  GDN_TRY(check_conv(dtype, T, channels, kernel_size, cu_seqlens, n_seqs, w, &es));
+  GDN_TRY(check_matrix(x, x_ld, channels, es, T));
+  GDN_TRY(check_matrix(dy, dy_ld, channels, es, T));
+  GDN_TRY(check_matrix(dx, dx_ld, channels, es, T));
+  GDN_TRY(check_vec(dw, false));
+  if (overlaps(x, x_ld, dx, dx_ld, T, channels, es) ||
+      overlaps(dy, dy_ld, dx, dx_ld, T, channels, es))
+    return GDN_ERR_INVALID_ARG;
+  if (dw)
+    GDN_TRY(check_scratch(workspace, workspace_bytes,
+                          gdn_conv1d_silu_workspace_bytes(T, channels, kernel_size)));
+  (void)cudaGetLastError();
+  g_last_error[0] = 0;
+  cudaError_t e = cudaSuccess;
+  if (T == 0) {
+    if (dw) e = cudaMemsetAsync(dw, 0, sizeof(float) * channels * kernel_size, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail("gdn_conv1d_silu_backward: cudaMemsetAsync", e);
+    return GDN_OK;
+  }
+  e = gdn::launch_conv1d_silu(true, dtype, T, channels, kernel_size, cu_seqlens, n_seqs, x, x_ld,
+                              w, dy, dy_ld, dx, dx_ld, dw, (float*)workspace,
+                              (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("gdn_conv1d_silu_backward: kernel launch", e);
+  return GDN_OK;
+}
+
+int gdn_gated_rmsnorm_forward(int32_t dtype, int64_t total_tokens, int32_t n_heads,
+                              int32_t head_dim, float eps, const void* o, int64_t o_ld,
+                              const void* z, int64_t z_ld, const float* gamma, void* y,
+                              int64_t y_ld, void* stream) {
+  size_t es = 0;
+  const int64_t T = total_tokens, W = (int64_t)n_heads * head_dim;
+  GDN_TRY(check_norm(dtype, T, n_heads, head_dim, eps, gamma, &es));
+  GDN_TRY(check_matrix(o, o_ld, W, es, T));
+  GDN_TRY(check_matrix(z, z_ld, W, es, T));
+  GDN_TRY(check_matrix(y, y_ld, W, es, T));
+  if (overlaps(o, o_ld, y, y_ld, T, W, es) || overlaps(z, z_ld, y, y_ld, T, W, es))
+    return GDN_ERR_INVALID_ARG;
+  if (T == 0) return GDN_OK;
+  (void)cudaGetLastError();
+  g_last_error[0] = 0;
+  const cudaError_t e = gdn::launch_gated_rmsnorm(
+      false, dtype, T, n_heads, head_dim, eps, o, o_ld, z, z_ld, gamma, nullptr, 0, y, y_ld,
+      nullptr, 0, nullptr, nullptr, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("gdn_gated_rmsnorm_forward: kernel launch", e);
+  return GDN_OK;
+}
+
+int gdn_gated_rmsnorm_backward(int32_t dtype, int64_t total_tokens, int32_t n_heads,
+                               int32_t head_dim, float eps, const void* o, int64_t o_ld,
+                               const void* z, int64_t z_ld, const float* gamma, const void* dy,
+                               int64_t dy_ld, void* d_o, int64_t do_ld, void* dz, int64_t dz_ld,
+                               float* dgamma, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  size_t es = 0;
+  const int64_t T = total_tokens, W = (int64_t)n_heads * head_dim;
+  GDN_TRY(check_norm(dtype, T, n_heads, head_dim, eps, gamma, &es));
+  GDN_TRY(check_matrix(o, o_ld, W, es, T));
+  GDN_TRY(check_matrix(z, z_ld, W, es, T));
+  GDN_TRY(check_matrix(dy, dy_ld, W, es, T));
+  GDN_TRY(check_matrix(d_o, do_ld, W, es, T));
+  GDN_TRY(check_matrix(dz, dz_ld, W, es, T));
+  GDN_TRY(check_vec(dgamma, false));
+  const void* ins[3] = {o, z, dy};
+  const int64_t lds[3] = {o_ld, z_ld, dy_ld};
+  for (int i = 0; i < 3; ++i)
+    if (overlaps(ins[i], lds[i], d_o, do_ld, T, W, es) || overlaps(ins[i], lds[i], dz, dz_ld, T, W, es))
+      return GDN_ERR_INVALID_ARG;
+  if (overlaps(d_o, do_ld, dz, dz_ld, T, W, es)) return GDN_ERR_INVALID_ARG;
+  if (dgamma)
+    GDN_TRY(check_scratch(workspace, workspace_bytes, gdn_gated_rmsnorm_workspace_bytes(head_dim)));
+  (void)cudaGetLastError();
+  g_last_error[0] = 0;
+  cudaError_t e = cudaSuccess;
+  if (T == 0) {
+    if (dgamma) e = cudaMemsetAsync(dgamma, 0, sizeof(float) * head_dim, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail("gdn_gated_rmsnorm_backward: cudaMemsetAsync", e);
+    return GDN_OK;
+  }
+  e = gdn::launch_gated_rmsnorm(true, dtype, T, n_heads, head_dim, eps, o, o_ld, z, z_ld, gamma,
+                                dy, dy_ld, d_o, do_ld, dz, dz_ld, dgamma, (float*)workspace,
+                                (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("gdn_gated_rmsnorm_backward: kernel launch", e);
   return GDN_OK;
 }
 

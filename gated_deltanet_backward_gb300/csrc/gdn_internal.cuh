@@ -229,7 +229,12 @@ enum KernelId {
   KID_FWD_FUSED_TC = 11,
   KID_BWD_FUSED_TC = 12,
   KID_DECODE = 13,
-  KID_COUNT = 14
+  KID_CONV_FWD = 14,
+  KID_CONV_BWD = 15,
+  KID_NORM_FWD = 16,
+  KID_NORM_BWD = 17,
+  KID_SUM_PARTS = 18,
+  KID_COUNT = 19
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
@@ -260,6 +265,20 @@ cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st);
 cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st);
 
 // One decode step (gdn_decode_step): arguments validated by the caller.
+// Causal depthwise conv1d + SiLU and gated RMSNorm (gdn_neighbours.cu).  `part` is the
+// caller's scratch for the weight gradient's per-block partial sums (conv_partial_floats /
+// norm_partial_floats floats); dw / dgamma null skips them.
+size_t conv_partial_floats(int64_t T, int C, int K);
+size_t norm_partial_floats(int D);
+cudaError_t launch_conv1d_silu(bool bwd, int dtype, int64_t T, int C, int K, const int32_t* cu,
+                               int n_seqs, const void* x, int64_t x_ld, const float* w,
+                               const void* dy, int64_t dy_ld, void* y, int64_t y_ld, float* dw,
+                               float* part, cudaStream_t st);
+cudaError_t launch_gated_rmsnorm(bool bwd, int dtype, int64_t T, int H, int D, float eps,
+                                 const void* o, int64_t o_ld, const void* z, int64_t z_ld,
+                                 const float* gamma, const void* dy, int64_t dy_ld, void* y,
+                                 int64_t y_ld, void* dz, int64_t dz_ld, float* dgamma,
+                                 float* part, cudaStream_t st);
 cudaError_t launch_decode(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
                           int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
                           int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,

@@ -258,6 +258,77 @@ int gdn_decode_step(const gdn_shape* shape, const void* q, int64_t q_ld, const v
                     const float* a_log, const float* dt_bias, const float* S_in, float* S_out,
                     void* o, int64_t o_ld, void* stream);
 
+/* ---- The layer steps on either side of the recurrence --------------------------------
+ * lattice-inference 0.6.0, src/attention/gdn_backward.rs: the forward's "Causal conv1d +
+ * SiLU" step (which makes the recurrence's q|k|v from the packed projection) and "Gated
+ * RMSNorm + output projection" step (which normalises o), and their backward (the
+ * backward's sections 5 and 2).  They take plain sizes instead of a gdn_shape.  dtype is
+ * a gdn_dtype; x, y, dy, dx, o, z and the norm's outputs have that element type, the
+ * weights and their gradients are fp32, arithmetic is fp32.  Matrices are [rows, ld] with
+ * ld in elements, 16-byte aligned, ld * element size a multiple of 16.  An output may not
+ * overlap an input or another output (GDN_ERR_INVALID_ARG).  The weight gradients (dw,
+ * d gamma) are optional (NULL skips them); when asked for they are formed in a fixed order
+ * from per-block partial sums kept in `workspace` (16-byte aligned, at least the size the
+ * matching *_workspace_bytes returns), so they are bit-reproducible run to run.
+ *
+ * Causal depthwise conv1d + SiLU, channel c of token t of sequence n:
+ *   y[t, c] = SiLU(sum_{j<K} w[c*K + j] * x[t - (K-1) + j, c])
+ * where inputs before cu_seqlens[n] (the sequence's first token) read as zero: each
+ * sequence starts with an empty rolling buffer.  The last tap (j = K-1) is the current
+ * token.  Backward, with pre[t, c] the argument of SiLU and d_sum = dy * SiLU'(pre):
+ *   dx[s, c] = sum_{j<K} d_sum[s + K-1-j, c] * w[c*K + j]   (terms inside s's sequence)
+ *   dw[c*K + j] = sum_t d_sum[t, c] * x[t - (K-1) + j, c]
+ *   channels     C, a multiple of 8 (the packed q|k|v width 2 Hk Dk + Hv Dv is one)
+ *   kernel_size  K in 1..4
+ *   cu_seqlens   device, int32 [n_seqs + 1]: 0 = cu[0] <= ... <= cu[n_seqs] = total_tokens
+ *                (not checked on the host; a malformed one gives wrong values but every
+ *                access stays inside the buffers)
+ *   x            device, [total_tokens, x_ld]: the projection rows (q|k|v packed)
+ *   w            device, fp32 [C, K]
+ *   y            device, [total_tokens, y_ld] (written): q, k and v of gdn_forward are
+ *                strided views of it (q = y, k = y + Hk Dk, v = y + 2 Hk Dk, ld = y_ld)
+ *   dy           device, [total_tokens, dy_ld]: the gradient of y (dq|dk|dv packed)
+ *   dx           device, [total_tokens, dx_ld] (written);  dw  device, fp32 [C, K] or NULL
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_MISALIGNED,
+ * GDN_ERR_WORKSPACE or GDN_ERR_CUDA; nothing is launched on an error. */
+int gdn_conv1d_silu_forward(int32_t dtype, int64_t total_tokens, int32_t channels,
+                            int32_t kernel_size, const int32_t* cu_seqlens, int32_t n_seqs,
+                            const void* x, int64_t x_ld, const float* w, void* y, int64_t y_ld,
+                            void* stream);
+size_t gdn_conv1d_silu_workspace_bytes(int64_t total_tokens, int32_t channels,
+                                       int32_t kernel_size);
+int gdn_conv1d_silu_backward(int32_t dtype, int64_t total_tokens, int32_t channels,
+                             int32_t kernel_size, const int32_t* cu_seqlens, int32_t n_seqs,
+                             const void* x, int64_t x_ld, const float* w, const void* dy,
+                             int64_t dy_ld, void* dx, int64_t dx_ld, float* dw, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Gated RMSNorm of every (token t, head h) row of head_dim values (o, z of that head):
+ *   rms = sqrt(mean_j o_j^2 + eps),   y_j = (o_j / rms) * gamma[j] * SiLU(z_j)
+ * with gamma shared by the heads.  Backward, with x_n = o / rms:
+ *   d_xn = dy gamma SiLU(z),  dz = dy gamma x_n SiLU'(z),
+ *   do = d_xn / rms - o (sum_j d_xn_j o_j) / (rms^3 head_dim),
+ *   d gamma[j] = sum over tokens and heads of dy_j x_n,j SiLU(z_j)
+ *   n_heads      H >= 1;  head_dim D in {16, 32, 64, 128};  eps >= 0 (finite)
+ *   o, z         device, [total_tokens, *_ld] holding H*D used columns
+ *   gamma        device, fp32 [D]
+ *   y            device, [total_tokens, y_ld] (written)
+ *   dy           device, [total_tokens, dy_ld]: the gradient of y
+ *   d_o, dz      device, [total_tokens, *_ld] (written): d_o is the recurrence's dO
+ *   dgamma       device, fp32 [D] or NULL
+ * Returns as the conv entry points do. */
+int gdn_gated_rmsnorm_forward(int32_t dtype, int64_t total_tokens, int32_t n_heads,
+                              int32_t head_dim, float eps, const void* o, int64_t o_ld,
+                              const void* z, int64_t z_ld, const float* gamma, void* y,
+                              int64_t y_ld, void* stream);
+size_t gdn_gated_rmsnorm_workspace_bytes(int32_t head_dim);
+int gdn_gated_rmsnorm_backward(int32_t dtype, int64_t total_tokens, int32_t n_heads,
+                               int32_t head_dim, float eps, const void* o, int64_t o_ld,
+                               const void* z, int64_t z_ld, const float* gamma, const void* dy,
+                               int64_t dy_ld, void* d_o, int64_t do_ld, void* dz, int64_t dz_ld,
+                               float* dgamma, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 /* Synchronises `stream` and returns the device-side status recorded in
  * `workspace` by the last gdn_forward / gdn_backward that used it (GDN_OK, or
  * the first device error), or GDN_ERR_CUDA if the stream itself failed. */

@@ -174,3 +174,49 @@ def generate(wl: Workload, token_limit: Optional[int] = None) -> Inputs:
 
 __all__ = ["Workload", "Inputs", "WORKLOADS", "get", "custom", "generate", "round_bf16",
            "CHUNK", "replace"]
+
+
+@dataclass
+class LayerStepInputs:
+    """One seeded draw for the layer steps either side of the recurrence.  Float arrays
+    are float32 holding values exact in the workload's dtype (weights are fp32)."""
+    cu_seqlens: np.ndarray           # [N+1] int32
+    x: np.ndarray                    # [T, C] projection rows before the conv (q|k|v packed)
+    w: np.ndarray                    # [C, K] conv weights, fp32
+    dy_conv: np.ndarray              # [T, C] gradient of the conv output
+    o: np.ndarray                    # [T, Hv*Dv] recurrence output
+    z: np.ndarray                    # [T, Hv*Dv] gate projection
+    gamma: np.ndarray                # [Dv] norm weight, fp32
+    dy_norm: np.ndarray              # [T, Hv*Dv] gradient of the norm output
+
+
+def generate_layer_steps(wl: Workload, K: int = 4, w_range: float = 0.05,
+                         token_limit: Optional[int] = None) -> LayerStepInputs:
+    """Inputs of the conv1d + SiLU and gated RMSNorm steps for ``wl``'s layer shape
+    (C = 2 Hk Dk + Hv Dv channels, Hv heads of Dv).  Distributions follow the
+    lattice-inference test model's initialisation: conv weights U(-w_range, w_range)
+    (0.05 there), norm weights U(0.9, 1.1); the activations x, o, z and both incoming
+    gradients are N(0, 1).  Seeded with seed + 7919 so it does not repeat the
+    recurrence's draw.  Draw order: x, w, dy_conv, o, z, gamma, dy_norm."""
+    rng = np.random.Generator(np.random.PCG64(wl.seed + 7919))
+    T = wl.total_tokens if token_limit is None else min(wl.total_tokens, token_limit)
+    lens, acc = [], 0
+    for n in wl.seqlens:
+        take = min(n, T - acc)
+        if take <= 0 and acc >= T:
+            break
+        lens.append(take)
+        acc += take
+    cu = np.zeros(len(lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    C = 2 * wl.Hk * wl.Dk + wl.Hv * wl.Dv
+    W = wl.Hv * wl.Dv
+    rnd = round_bf16 if wl.dtype == "bf16" else (lambda a: np.ascontiguousarray(a, np.float32))
+    x = rnd(_normal(rng, (T, C)))
+    w = rng.uniform(-w_range, w_range, size=(C, K)).astype(np.float32)
+    dy_conv = rnd(_normal(rng, (T, C)))
+    o = rnd(_normal(rng, (T, W)))
+    z = rnd(_normal(rng, (T, W)))
+    gamma = rng.uniform(0.9, 1.1, size=(wl.Dv,)).astype(np.float32)
+    dy_norm = rnd(_normal(rng, (T, W)))
+    return LayerStepInputs(cu, x, w, dy_conv, o, z, gamma, dy_norm)
