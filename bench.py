@@ -8,8 +8,9 @@ resident in HBM.  Prints one JSON line (rank 0).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
-events on the launch stream, with a 256 MB write between steps (flushes the
-129 MB L2) outside the events; barrier + synchronize around the timed loop;
+events on the launch stream, with an L2 flush between steps outside the events
+(a 256 MB write, then a 256 MB read of another buffer: the 129 MB L2 then holds
+none of the step's data and no dirty lines whose write-back the step would pay); barrier + synchronize around the timed loop;
 max over ranks.  The library's profiling hook times every kernel launch of the
 timed steps with CUDA events on the same stream, which gives the dominant
 kernel's average duration for the roofline entry.
@@ -41,6 +42,21 @@ import workloads as W  # noqa: E402
 
 METRIC = "GDN fwd+bwd tokens/s (Hk16/Hv48, d128, bf16) and % of roofline on 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Evicts the L2 between timed launches: writes one buffer larger than the L2, then
+    reads another, so the writes' dirty lines are written back before the next timed
+    launch instead of during it."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, device=device)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 def _peaks():
@@ -308,7 +324,7 @@ def run_ours(args):
     da_log = torch.empty(Hv, device=device)
     ddt = torch.empty(Hv, device=device)
     dS0 = torch.empty(N, Hv, Dk, Dv, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, device=device)
+    flush = L2Flush(device)
     stream = torch.cuda.current_stream(device)
 
     def fwd():
@@ -321,7 +337,7 @@ def run_ours(args):
     for _ in range(args.warmup):
         fwd()
         bwd()
-        flush.zero_()
+        flush()
     torch.cuda.synchronize()
     assert gdn.gdn_read_device_status(layer.ws_bwd) == 0
 
@@ -339,7 +355,7 @@ def run_ours(args):
             ev[i][1].record(stream)
             bwd()
             ev[i][2].record(stream)
-            flush.zero_()
+            flush()
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -393,7 +409,7 @@ def run_ours(args):
                    "tokens_per_gpu": T, "io_dtype": wl.dtype,
                    "compute": ("tcgen05 bf16 MMA, fp32 accumulate and state" if wl.dtype == "bf16"
                                else "fp32 CUDA-core FMA"),
-                   "l2": "flushed: 256 MB write between timed steps",
+                   "l2": "flushed between timed steps: 256 MB write, then 256 MB read",
                    "step": "training step: the forward keeps its chunk operands for the "
                            "backward (GDN_FLAG_KEEP_FOR_BACKWARD / GDN_FLAG_REUSE_FORWARD)",
                    "parallelism": "independent batch per GPU" if world > 1 else "single GPU"},
@@ -458,7 +474,7 @@ def run_layer_steps(wl, device, pk, K=4, eps=1e-6, steps=10, warmup=3):
     causal conv1d + SiLU over the packed q|k|v rows (C = 2 Hk Dk + Hv Dv channels, kernel
     K) and the gated RMSNorm over the Hv heads of o, forward and backward (weight
     gradients included).  Each kernel is timed alone with CUDA events around its own
-    launch, after a 256 MB write that flushes the L2; bytes are the algorithmic ones
+    launch, after an L2 flush (L2Flush); bytes are the algorithmic ones
     (every operand read once, every result written once).  Synthetic inputs (N(0, 1)
     activations, conv weights U(-0.05, 0.05), norm weights U(0.9, 1.1)), resident."""
     import torch
@@ -483,7 +499,7 @@ def run_layer_steps(wl, device, pk, K=4, eps=1e-6, steps=10, warmup=3):
                        device=device)
     ws_n = torch.empty(gdn.gdn_gated_rmsnorm_workspace_bytes(Dv), dtype=torch.uint8,
                        device=device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, device=device)
+    flush = L2Flush(device)
     calls = {
         "conv1d_silu_fwd": (lambda: gdn.gdn_conv1d_silu_forward(x, w, cu, y),
                             2 * T * C * es + C * K * 4),
@@ -504,7 +520,7 @@ def run_layer_steps(wl, device, pk, K=4, eps=1e-6, steps=10, warmup=3):
               for _ in range(steps)]
         torch.cuda.synchronize()
         for e0, e1 in ev:
-            flush.zero_()
+            flush()
             e0.record(stream)
             fn()
             e1.record(stream)

@@ -94,6 +94,7 @@ int check_conv(int32_t dtype, int64_t T, int32_t C, int32_t K, const int32_t* cu
   GDN_TRY(check_dtype(dtype, es));
   if (T < 0 || C <= 0 || n_seqs < 0 || (T > 0 && n_seqs == 0)) return GDN_ERR_INVALID_ARG;
   if (K < 1 || K > 4 || C % 8 != 0) return GDN_ERR_UNSUPPORTED;
+  if (T > (int64_t)1 << 30 || C > 1 << 24) return GDN_ERR_UNSUPPORTED;  // 32-bit tile indices
   if (T > 0 && !cu) return GDN_ERR_INVALID_ARG;
   if (cu && ((uintptr_t)cu & 3u) != 0) return GDN_ERR_MISALIGNED;
   return check_vec(w, true);
@@ -104,6 +105,7 @@ int check_norm(int32_t dtype, int64_t T, int32_t H, int32_t D, float eps, const 
   GDN_TRY(check_dtype(dtype, es));
   if (T < 0 || H <= 0 || !(eps >= 0.f) || eps > 3.0e38f) return GDN_ERR_INVALID_ARG;
   if (!head_size_ok(D)) return GDN_ERR_UNSUPPORTED;
+  if (T * H * (int64_t)D > (int64_t)1 << 31) return GDN_ERR_UNSUPPORTED;  // 32-bit vector indices
   return check_vec(gamma, true);
 }
 

@@ -5,36 +5,30 @@
 // forward's "Causal conv1d + SiLU" and "Gated RMSNorm + output projection" steps, the
 // backward's sections 5 and 2).
 //
-// Both are elementwise or row-local and stream their operands once: HBM-bound work on
-// CUDA cores.  Every thread moves vectors of 4 or 8 channels (8 or 16 bytes), so a warp
-// covers 256 or 512 contiguous bytes of a row, and the weight gradients (dw of the conv,
-// d gamma of the norm) are reduced in a fixed order -- per thread over its tokens, per
-// block over its warps or row slots through shared memory, then over blocks by a
-// second small kernel -- so they are bit-reproducible run to run.
+// Both stream their operands once: HBM-bound work on CUDA cores, with enough arithmetic
+// per byte (a sigmoid per element, up to a dozen FMAs) that the instruction count
+// matters too.  So every thread moves 16-byte vectors (8 bf16 or 4 fp32 channels), the
+// sigmoid is ex2.approx + rcp.approx (__expf, __fdividef), and index arithmetic is
+// 32-bit.  The conv stages token tiles of a channel slab in shared memory through a
+// multistage cp.async pipeline (a persistent block walks the tiles of its slab, two or
+// three tiles in flight while it computes one); the norm keeps 2-4 rows of loads in
+// flight per thread.  The weight gradients (dw of the conv, d gamma of the norm) are
+// reduced in a fixed order -- per thread over its tokens, per block through shared
+// memory, then over blocks by a second small kernel -- so they are bit-reproducible run
+// to run.
 #include <cuda_bf16.h>
 
 #include "gdn_device.cuh"
 #include "gdn_internal.cuh"
+#include "umma.cuh"
 
 namespace gdn {
 namespace {
 
-// ---- vectors of V channels (8 or 16 bytes), converted to and from fp32 ------------------
-template <typename T, int V>
-struct Vec;
-template <>
-struct Vec<float, 4> {
-  __device__ __forceinline__ static void load(const float* p, float* f) {
-    const float4 a = *(const float4*)p;
-    f[0] = a.x;
-    f[1] = a.y;
-    f[2] = a.z;
-    f[3] = a.w;
-  }
-  __device__ __forceinline__ static void store(float* p, const float* f) {
-    *(float4*)p = make_float4(f[0], f[1], f[2], f[3]);
-  }
-};
+// ---- 16-byte vectors <-> fp32 ------------------------------------------------------------
+template <typename T>
+constexpr int kVec = 16 / (int)sizeof(T);  // channels of a 16-byte vector
+
 __device__ __forceinline__ void unpack_bf2(uint32_t w, float* f) {
   __nv_bfloat162 b;
   memcpy(&b, &w, 4);
@@ -48,52 +42,102 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
   memcpy(&w, &h, 4);
   return w;
 }
-template <>
-struct Vec<__nv_bfloat16, 8> {
-  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* f) {
-    const uint4 u = *(const uint4*)p;
-    unpack_bf2(u.x, f);
-    unpack_bf2(u.y, f + 2);
-    unpack_bf2(u.z, f + 4);
-    unpack_bf2(u.w, f + 6);
-  }
-  __device__ __forceinline__ static void store(__nv_bfloat16* p, const float* f) {
-    *(uint4*)p = make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]),
-                            pack_bf2(f[6], f[7]));
-  }
-};
-template <>
-struct Vec<__nv_bfloat16, 4> {
-  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* f) {
-    const uint2 u = *(const uint2*)p;
-    unpack_bf2(u.x, f);
-    unpack_bf2(u.y, f + 2);
-  }
-  __device__ __forceinline__ static void store(__nv_bfloat16* p, const float* f) {
-    *(uint2*)p = make_uint2(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]));
-  }
-};
+__device__ __forceinline__ void unpack(const uint4& u, float* f, float) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack(const uint4& u, float* f, __nv_bfloat16) {
+  unpack_bf2(u.x, f);
+  unpack_bf2(u.y, f + 2);
+  unpack_bf2(u.z, f + 4);
+  unpack_bf2(u.w, f + 6);
+}
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4& u, float* f) {
+  unpack(u, f, T());
+}
+__device__ __forceinline__ uint4 pack(const float* f, float) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+__device__ __forceinline__ uint4 pack(const float* f, __nv_bfloat16) {
+  return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]),
+                    pack_bf2(f[6], f[7]));
+}
+template <typename T>
+__device__ __forceinline__ uint4 pack(const float* f) {
+  return pack(f, T());
+}
+template <typename T>
+__device__ __forceinline__ uint4 ld16(const T* p) {
+  return *(const uint4*)p;
+}
+template <typename T>
+__device__ __forceinline__ void st16(T* p, const uint4& u) {
+  *(uint4*)p = u;
+}
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.f + expf(-x)); }
-// d/dx x sigmoid(x) = sigmoid(x) (1 + x (1 - sigmoid(x)))
-__device__ __forceinline__ float silu_grad_f(float x) {
-  const float s = 1.f / (1.f + expf(-x));
-  return s * (1.f + x * (1.f - s));
+// sigmoid(x) = 1 / (1 + e^-x), with e^-x = 2^(-x log2 e) from the hardware's base-2
+// exponential and the reciprocal from its reciprocal approximation (each within a couple
+// of ulp).  For x -> -inf the exponential overflows to +inf and the reciprocal gives 0;
+// for x -> +inf it underflows to 0 and the result is 1.
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-x * kLog2e));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return r;
+}
+
+// ---- sequences of a varlen batch ------------------------------------------------------------
+// Sequence n holding token t: the largest n < n_seqs with cu[n] <= t (empty sequences
+// are skipped).  Clamped to [0, n_seqs - 1], so a malformed cu_seqlens only changes
+// which inputs count as "before the start", never where a load goes.
+__device__ __forceinline__ int seq_of(const int32_t* cu, int n_seqs, int t) {
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
 }
 
 // ---- causal depthwise conv1d + SiLU --------------------------------------------------------
+// Window entry j of row t holds input t - (K-1) + j; entries before the row's sequence
+// start (j < K-1-dist, dist = t - start) are zeroed, which drops their taps from every
+// product that follows.  As the window slides within a sequence those entries stay
+// before its start, and a row that starts a new sequence zeroes all K-1 again.
+template <int K, int V>
+__device__ __forceinline__ void mask_window(float (&win)[K][V], int dist) {
+  if (dist < K - 1) {
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j)
+      if (j < K - 1 - dist)
+#pragma unroll
+        for (int c = 0; c < V; ++c) win[j][c] = 0.f;
+  }
+}
+
 // y[t, c] = SiLU(sum_j w[c, j] x[t - (K-1) + j, c]), inputs before the start of t's
-// sequence read as zero.  A block is 8 warps: lane l takes the channel vector (V channels)
-// 32 * blockIdx.x + l, warp i the kConvTT tokens starting at 256 * blockIdx.y + kConvTT i.
-// A thread walks its tokens in order, holding the K-1 previous inputs in registers and
-// issuing the loads of U tokens ahead.
-constexpr int kConvWarps = 8;
-constexpr int kConvTT = 32;                     // tokens of one warp
-constexpr int kConvRows = kConvWarps * kConvTT; // tokens of one block
+// sequence read as zero.  The channels are cut into slabs of kSlabVec 16-byte vectors,
+// the tokens into tiles of kConvTR; tile i is token tile i % n_tt of slab i / n_tt, and
+// block b walks tiles b q .. b q + q - 1 (consecutive token tiles of a slab, so the K-1
+// rows before a tile are the L2-resident end of the previous one).  A tile's rows (with
+// the K-1 before it) land in a ring of kConvNS shared-memory stages through cp.async,
+// issued kConvNS-1 tiles ahead.  Thread (v, g) then computes vector v of the tile's rows
+// g*RPT .. g*RPT+RPT-1, sliding a K-row window down them.
+constexpr int kConvThreads = 256;
+constexpr int kConvTR = 32;   // tokens of a tile
+constexpr int kConvNS = 3;    // pipeline stages
+constexpr int kSlabVec = 64;  // 16-byte vectors of a slab row (1 KB)
 
 struct ConvArgs {
-  int64_t T;
-  int C, n_seqs;
+  int T, C, K, n_seqs, n_slabs, q;  // q: tiles of a block (a contiguous run, slab-major)
   const int32_t* cu;
   const void* x;
   int64_t x_ld;
@@ -102,245 +146,333 @@ struct ConvArgs {
   int64_t dy_ld;
   void* y;  // forward: y; backward: dx
   int64_t y_ld;
-  float* dw_part;  // backward: [ceil(T / kConvRows), C, K] partial dw, or null
+  float* dw_part;  // backward: [gridDim.x, 2, slab channels, K] partial dw, or null
 };
 
-// Sequence n holding token t: the largest n < n_seqs with cu[n] <= t (empty sequences
-// are skipped).  Clamped to [0, n_seqs - 1], so a malformed cu_seqlens only changes
-// which inputs count as "before the start", never where a load goes.
-__device__ __forceinline__ int seq_of(const int32_t* cu, int n_seqs, int64_t t) {
-  int lo = 0, hi = n_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((int64_t)__ldg(cu + mid) <= t)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  return lo;
+// Stages rows r0 .. r0 + ROWS - 1 (those inside [0, T)), vectors 0 .. nvec-1 of each, as
+// dst[row][vector].  Thread i copies vector i % NV of rows i / NV, + 256 / NV, ...: one
+// cp.async and a pointer step per 16 bytes.
+template <int ROWS, int NV>
+__device__ __forceinline__ void stage_rows(uint4* dst, const char* base, int64_t ld_bytes, int r0,
+                                           int T, int nvec) {
+  constexpr int RS = kConvThreads / NV;  // rows between a thread's copies
+  const int v = threadIdx.x % NV, row0 = threadIdx.x / NV;
+  if (v >= nvec) return;
+  int src = r0 + row0;
+  const char* p = base + (int64_t)src * ld_bytes + v * 16;
+  uint4* d = dst + row0 * NV + v;
+  const int64_t step = RS * ld_bytes;
+#pragma unroll 4
+  for (int row = row0; row < ROWS; row += RS, src += RS, p += step, d += RS * NV)
+    if ((unsigned)src < (unsigned)T) tc::cp_async16(d, p);
 }
 
-// Steps the sequence cursor (n, end = cu[n + 1]) forward until it holds token t; true
-// when it moved (t is then the first token of its sequence).
-__device__ __forceinline__ bool seq_advance(const int32_t* cu, int n_seqs, int64_t t, int& n,
-                                            int64_t& end) {
-  bool moved = false;
-  while (t >= end && n + 1 < n_seqs) {
-    ++n;
-    end = __ldg(cu + n + 1);
-    moved = true;
-  }
-  return moved;
-}
-
-template <typename T, int V, int K, int U>
-__global__ void __launch_bounds__(kConvWarps * 32, 2) k_conv_fwd(ConvArgs a) {
-  using VT = Vec<T, V>;
-  constexpr int KR = K > 1 ? K - 1 : 1;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c0 = (blockIdx.x * 32 + lane) * V;
-  const int64_t t0 = (int64_t)blockIdx.y * kConvRows + warp * kConvTT;
-  if (c0 >= a.C || t0 >= a.T) return;
-  const int64_t t1 = t0 + kConvTT < a.T ? t0 + kConvTT : a.T;
-  const T* x = (const T*)a.x + c0;
-  T* y = (T*)a.y + c0;
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads, 2) k_conv_fwd(ConvArgs a) {
+  constexpr int V = kVec<T>, NV = kSlabVec, SW = NV * V, RG = kConvThreads / NV;
+  constexpr int RPT = kConvTR / RG;
+  constexpr int ROWS = kConvTR + K - 1;  // staged rows: the tile and the K-1 before it
+  extern __shared__ uint4 cstage[];      // [kConvNS][ROWS][NV]
+  const int n_tt = (a.T + kConvTR - 1) / kConvTR, total = a.n_slabs * n_tt;
+  const int i0 = blockIdx.x * a.q, i1 = min(i0 + a.q, total);
+  const int v = threadIdx.x % NV, g = threadIdx.x / NV;
+  const int64_t xld = a.x_ld * (int64_t)sizeof(T);
+  auto issue = [&](int i) {
+    if (i < i1) {
+      const int slab = i / n_tt, tt = i % n_tt, c0 = slab * SW;
+      stage_rows<ROWS, NV>(cstage + ((i - i0) % kConvNS) * ROWS * NV,
+                           (const char*)((const T*)a.x + c0), xld, tt * kConvTR - (K - 1), a.T,
+                           min(NV, (a.C - c0) / V));
+    }
+    tc::cp_async_commit();  // possibly empty: keeps the group count uniform
+  };
+#pragma unroll
+  for (int s = 0; s < kConvNS - 1; ++s) issue(i0 + s);
   float wt[K][V];
+  int cur_slab = -1;
+  for (int i = i0; i < i1; ++i) {  // uniform
+    const int slab = i / n_tt, tt = i % n_tt, c0 = slab * SW;
+    const bool vok = v < min(NV, (a.C - c0) / V);
+    if (slab != cur_slab) {
+      cur_slab = slab;
+      if (vok) {
 #pragma unroll
-  for (int i = 0; i < V; ++i)
+        for (int c = 0; c < V; ++c)
 #pragma unroll
-    for (int j = 0; j < K; ++j) wt[j][i] = __ldg(a.w + (int64_t)(c0 + i) * K + j);
-  int n = seq_of(a.cu, a.n_seqs, t0);
-  int64_t start = __ldg(a.cu + n), end = __ldg(a.cu + n + 1);
-  float ring[KR][V];  // inputs t-K+1 .. t-1 (zero before the sequence start)
+          for (int j = 0; j < K; ++j) wt[j][c] = __ldg(a.w + (int64_t)(c0 + v * V + c) * K + j);
+      }
+    }
+    issue(i + kConvNS - 1);
+    tc::cp_async_wait<kConvNS - 1>();
+    __syncthreads();
+    const uint4* st = cstage + ((i - i0) % kConvNS) * ROWS * NV + v;
+    const int tr = tt * kConvTR + g * RPT;  // first row of this thread
+    if (vok && tr < a.T) {
+      int n = seq_of(a.cu, a.n_seqs, tr);
+      int start = __ldg(a.cu + n), end = __ldg(a.cu + n + 1);
+      float win[K][V];  // rows t-K+1 .. t (stage rows g*RPT + r .. g*RPT + r + K-1)
 #pragma unroll
-  for (int j = 0; j < K - 1; ++j) {
-    const int64_t src = t0 - (K - 1) + j;
-    if (src >= start && src >= 0)
-      VT::load(x + src * a.x_ld, ring[j]);
-    else
+      for (int j = 0; j < K - 1; ++j) unpack<T>(st[(g * RPT + j) * NV], win[j]);
+      T* yb = (T*)a.y + c0 + v * V;
 #pragma unroll
-      for (int i = 0; i < V; ++i) ring[j][i] = 0.f;
-  }
-  for (int64_t tb = t0; tb < t1; tb += U) {
-    float xv[U][V];
+      for (int r = 0; r < RPT; ++r) {
+        const int t = tr + r;
+        if (t >= a.T) break;
+        while (t >= end && n + 1 < a.n_seqs) {  // next sequence
+          ++n;
+          start = end;
+          end = __ldg(a.cu + n + 1);
+        }
+        unpack<T>(st[(g * RPT + r + K - 1) * NV], win[K - 1]);
+        mask_window<K, V>(win, t - start);
+        float out[V];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (tb + u < t1) VT::load(x + (tb + u) * a.x_ld, xv[u]);
+        for (int c = 0; c < V; ++c) {
+          float s = wt[K - 1][c] * win[K - 1][c];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t t = tb + u;
-      if (t >= t1) break;
-      if (seq_advance(a.cu, a.n_seqs, t, n, end)) {
+          for (int j = 0; j < K - 1; ++j) s = fmaf(wt[j][c], win[j][c], s);
+          out[c] = s * sigmoid_fast(s);
+        }
+        st16(yb + (int64_t)t * a.y_ld, pack<T>(out));
 #pragma unroll
         for (int j = 0; j < K - 1; ++j)
 #pragma unroll
-          for (int i = 0; i < V; ++i) ring[j][i] = 0.f;
+          for (int c = 0; c < V; ++c) win[j][c] = win[j + 1][c];
       }
-      float out[V];
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        float s = wt[K - 1][i] * xv[u][i];
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j) s = fmaf(wt[j][i], ring[j][i], s);
-        out[i] = silu_f(s);
-      }
-      VT::store(y + t * a.y_ld, out);
-#pragma unroll
-      for (int j = 0; j + 1 < K - 1; ++j)
-#pragma unroll
-        for (int i = 0; i < V; ++i) ring[j][i] = ring[j + 1][i];
-      if (K > 1)
-#pragma unroll
-        for (int i = 0; i < V; ++i) ring[KR - 1][i] = xv[u][i];
     }
+    __syncthreads();  // the stage is refilled by a later issue
   }
+  tc::cp_async_wait<0>();
 }
 
 // Backward (section 5 of the backward): d_sum[t] = dy[t] SiLU'(pre[t]) with pre[t] the
-// forward's pre-activation (recomputed); dx[s] = sum_m d_sum[s + m] w[K-1-m] over the
-// s + m inside s's sequence; dw[c, j] = sum_t d_sum[t] x[t - (K-1) + j].  A warp's
-// tokens s are [t0, t1); it walks t from t0 to t1 + K - 2 (the K-1 tokens after t1 are
-// recomputed, not counted into dw), holding the K-1 previous inputs and d_sums.
-template <typename T, int V, int K, int U>
-__global__ void __launch_bounds__(kConvWarps * 32, 2) k_conv_bwd(ConvArgs a) {
-  using VT = Vec<T, V>;
-  constexpr int KR = K > 1 ? K - 1 : 1;
-  __shared__ float red[kConvWarps][K * V][32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c0 = (blockIdx.x * 32 + lane) * V;
-  const int64_t t0 = (int64_t)blockIdx.y * kConvRows + warp * kConvTT;
+// forward's pre-activation (recomputed from x); dx[s] = sum_m d_sum[s + m] w[K-1-m] over
+// the s + m inside s's sequence; dw[c, j] = sum_t d_sum[t] x[t - (K-1) + j].
+// Tiles are kConvTRB tokens of a slab of kSlabVecB vectors; a stage holds the tile's x
+// rows with K-1 before and K-1 after it, and its dy rows with K-1 after it.  Phase A forms
+// d_sum of the tile's rows and the K-1 after them (those once more in the next tile) into
+// an fp32 shared buffer, accumulating dw over the tile's own rows; phase B reads it back
+// for dx.  Block b takes tiles [b q, (b+1) q) of the slab-major tile order, so it spans
+// at most two slabs: its dw is kept per slab it touches (slot 0 the first, slot 1 the
+// second) and summed over blocks by k_conv_dw_sum in block order.
+constexpr int kConvTRB = 64;   // tokens of a backward tile
+constexpr int kConvNSB = 4;    // backward pipeline stages
+constexpr int kSlabVecB = 16;  // 16-byte vectors of a backward slab row (256 B)
+
+template <typename T, int K>
+struct ConvBwdGeom {
+  static constexpr int V = kVec<T>, NV = kSlabVecB, SW = NV * V;  // slab channels
+  static constexpr int RG = kConvThreads / NV, RPT = kConvTRB / RG;
+  static constexpr int XR = kConvTRB + 2 * (K - 1), GR = kConvTRB + (K - 1);
+  static constexpr int STAGE = (XR + GR) * NV;  // 16-byte vectors of a stage
+  static constexpr size_t smem = sizeof(uint4) * (size_t)STAGE * kConvNSB +
+                                 sizeof(float) * (size_t)GR * SW;
+};
+
+template <typename T, int K>
+__device__ __forceinline__ void conv_dw_flush(float (&dwa)[K][kVec<T>], float* red, float* part,
+                                              int v, int g) {
+  using G = ConvBwdGeom<T, K>;
+  constexpr int V = G::V, NV = G::NV, KV = K * V;
+  __syncthreads();  // red aliases the d_sum buffer
+#pragma unroll
+  for (int j = 0; j < K; ++j)
+#pragma unroll
+    for (int c = 0; c < V; ++c) red[(g * NV + v) * KV + c * K + j] = dwa[j][c];
+  __syncthreads();
+  for (int e = threadIdx.x; e < NV * KV; e += kConvThreads) {  // e = (vector, c, j)
+    float s = 0.f;
+    for (int gg = 0; gg < G::RG; ++gg) s += red[gg * NV * KV + e];
+    part[e] = s;  // [slab channel][tap]
+  }
+#pragma unroll
+  for (int j = 0; j < K; ++j)
+#pragma unroll
+    for (int c = 0; c < V; ++c) dwa[j][c] = 0.f;
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
+  using G = ConvBwdGeom<T, K>;
+  constexpr int V = G::V, NV = G::NV, RPT = G::RPT, XR = G::XR, GR = G::GR, SW = G::SW;
+  extern __shared__ uint4 cstage[];  // [kConvNSB][XR + GR][NV], then d_sum [GR][SW] fp32
+  float* dsb = (float*)(cstage + (size_t)G::STAGE * kConvNSB);
+  const int n_tt = (a.T + kConvTRB - 1) / kConvTRB, total = a.n_slabs * n_tt;
+  const int i0 = blockIdx.x * a.q, i1 = min(i0 + a.q, total);
+  const int v = threadIdx.x % NV, g = threadIdx.x / NV;
+  const int64_t xld = a.x_ld * (int64_t)sizeof(T), gld = a.dy_ld * (int64_t)sizeof(T);
+  auto issue = [&](int i) {
+    if (i < i1) {
+      const int slab = i / n_tt, tt = i % n_tt, c0 = slab * SW, t0 = tt * kConvTRB;
+      const int nvec = min(NV, (a.C - c0) / V);
+      uint4* st = cstage + (size_t)((i - i0) % kConvNSB) * G::STAGE;
+      stage_rows<XR, NV>(st, (const char*)((const T*)a.x + c0), xld, t0 - (K - 1), a.T, nvec);
+      stage_rows<GR, NV>(st + XR * NV, (const char*)((const T*)a.dy + c0), gld, t0, a.T, nvec);
+    }
+    tc::cp_async_commit();
+  };
+#pragma unroll
+  for (int s = 0; s < kConvNSB - 1; ++s) issue(i0 + s);
   float dwa[K][V];
 #pragma unroll
   for (int j = 0; j < K; ++j)
 #pragma unroll
-    for (int i = 0; i < V; ++i) dwa[j][i] = 0.f;
-  if (c0 < a.C && t0 < a.T) {
-    const int64_t t1 = t0 + kConvTT < a.T ? t0 + kConvTT : a.T;
-    const int64_t te = t1 + (K - 1);  // walk end (exclusive)
-    const T* x = (const T*)a.x + c0;
-    const T* dy = (const T*)a.dy + c0;
-    T* dx = (T*)a.y + c0;
-    float wt[K][V];
+    for (int c = 0; c < V; ++c) dwa[j][c] = 0.f;
+  float wt[K][V];
+  int cur_slab = -1;
+  for (int i = i0; i < i1; ++i) {  // uniform
+    const int slab = i / n_tt, tt = i % n_tt, c0 = slab * SW, t0 = tt * kConvTRB;
+    const int nvec = min(NV, (a.C - c0) / V);
+    if (slab != cur_slab) {
+      if (cur_slab >= 0 && a.dw_part)  // the block's first slab ends: slot 0
+        conv_dw_flush<T, K>(dwa, dsb, a.dw_part + (size_t)blockIdx.x * 2 * SW * K, v, g);
+      cur_slab = slab;
+      if (v < nvec) {
 #pragma unroll
-    for (int i = 0; i < V; ++i)
+        for (int c = 0; c < V; ++c)
 #pragma unroll
-      for (int j = 0; j < K; ++j) wt[j][i] = __ldg(a.w + (int64_t)(c0 + i) * K + j);
-    int nt = seq_of(a.cu, a.n_seqs, t0);
-    int64_t end_t = __ldg(a.cu + nt + 1);
-    const int64_t start0 = __ldg(a.cu + nt);
-    int ns = nt;  // sequence of the token s whose dx is emitted next
-    int64_t end_s = end_t;
-    float xr[KR][V], dr[KR][V];  // inputs t-K+1 .. t-1; d_sum of t-K+1 .. t-1
-#pragma unroll
-    for (int j = 0; j < K - 1; ++j) {
-      const int64_t src = t0 - (K - 1) + j;
-      if (src >= start0 && src >= 0)
-        VT::load(x + src * a.x_ld, xr[j]);
-      else
-#pragma unroll
-        for (int i = 0; i < V; ++i) xr[j][i] = 0.f;
-#pragma unroll
-      for (int i = 0; i < V; ++i) dr[j][i] = 0.f;
-    }
-    for (int64_t tb = t0; tb < te; tb += U) {
-      float xv[U][V], gv[U][V];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (tb + u < te && tb + u < a.T) {
-          VT::load(x + (tb + u) * a.x_ld, xv[u]);
-          VT::load(dy + (tb + u) * a.dy_ld, gv[u]);
-        }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t t = tb + u;
-        if (t >= te) break;
-        float ds[V];
-        if (t < a.T) {
-          if (seq_advance(a.cu, a.n_seqs, t, nt, end_t)) {
-#pragma unroll
-            for (int j = 0; j < K - 1; ++j)
-#pragma unroll
-              for (int i = 0; i < V; ++i) xr[j][i] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < V; ++i) {
-            float s = wt[K - 1][i] * xv[u][i];
-#pragma unroll
-            for (int j = 0; j < K - 1; ++j) s = fmaf(wt[j][i], xr[j][i], s);
-            ds[i] = gv[u][i] * silu_grad_f(s);
-          }
-          if (t < t1) {
-#pragma unroll
-            for (int i = 0; i < V; ++i) {
-#pragma unroll
-              for (int j = 0; j < K - 1; ++j) dwa[j][i] = fmaf(ds[i], xr[j][i], dwa[j][i]);
-              dwa[K - 1][i] = fmaf(ds[i], xv[u][i], dwa[K - 1][i]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < V; ++i) ds[i] = 0.f;
-        }
-        const int64_t s = t - (K - 1);
-        if (s >= t0) {
-          seq_advance(a.cu, a.n_seqs, s, ns, end_s);
-          float out[V];
-#pragma unroll
-          for (int i = 0; i < V; ++i) out[i] = s + (K - 1) < end_s ? ds[i] * wt[0][i] : 0.f;
-#pragma unroll
-          for (int m = 0; m < K - 1; ++m)
-            if (s + m < end_s)
-#pragma unroll
-              for (int i = 0; i < V; ++i) out[i] = fmaf(dr[m][i], wt[K - 1 - m][i], out[i]);
-          VT::store(dx + s * a.y_ld, out);
-        }
-#pragma unroll
-        for (int j = 0; j + 1 < K - 1; ++j)
-#pragma unroll
-          for (int i = 0; i < V; ++i) {
-            xr[j][i] = xr[j + 1][i];
-            dr[j][i] = dr[j + 1][i];
-          }
-        if (K > 1)
-#pragma unroll
-          for (int i = 0; i < V; ++i) {
-            xr[KR - 1][i] = t < a.T ? xv[u][i] : 0.f;
-            dr[KR - 1][i] = ds[i];
-          }
+          for (int j = 0; j < K; ++j) wt[j][c] = __ldg(a.w + (int64_t)(c0 + v * V + c) * K + j);
       }
     }
+    issue(i + kConvNSB - 1);
+    tc::cp_async_wait<kConvNSB - 1>();
+    __syncthreads();
+    const uint4* xs = cstage + (size_t)((i - i0) % kConvNSB) * G::STAGE + v;
+    const uint4* gs = xs + XR * NV;
+    const bool vok = v < nvec;
+    // ---- phase A: d_sum of rows u = g*RPT .. g*RPT+RPT-1 (and u = kConvTRB + g, g < K-1)
+    // dist: tokens of t's sequence before t
+    auto dsum_row = [&](int u, int dist, float (&win)[K][V], bool own) {
+      const int t = t0 + u;
+      float ds[V];
+      if (t < a.T) {
+        float gy[V];
+        unpack<T>(gs[u * NV], gy);
+        mask_window<K, V>(win, dist);
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          float s = wt[K - 1][c] * win[K - 1][c];
+#pragma unroll
+          for (int j = 0; j < K - 1; ++j) s = fmaf(wt[j][c], win[j][c], s);
+          const float sg = sigmoid_fast(s);
+          ds[c] = gy[c] * fmaf(s * sg, 1.f - sg, sg);  // dy * SiLU'(s)
+        }
+        if (own) {
+#pragma unroll
+          for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int c = 0; c < V; ++c) dwa[j][c] = fmaf(ds[c], win[j][c], dwa[j][c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < V; ++c) ds[c] = 0.f;
+      }
+      float4* d = (float4*)(dsb + u * SW + v * V);
+#pragma unroll
+      for (int c = 0; c < V; c += 4) d[c / 4] = make_float4(ds[c], ds[c + 1], ds[c + 2], ds[c + 3]);
+    };
+    if (vok) {
+      float win[K][V];
+      const int tr = min(t0 + g * RPT, a.T - 1);
+      int n = seq_of(a.cu, a.n_seqs, tr);
+      int start = __ldg(a.cu + n), end = __ldg(a.cu + n + 1);
+#pragma unroll
+      for (int j = 0; j < K - 1; ++j) unpack<T>(xs[(g * RPT + j) * NV], win[j]);
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        const int u = g * RPT + r, t = t0 + u;
+        while (t >= end && n + 1 < a.n_seqs) {
+          ++n;
+          start = end;
+          end = __ldg(a.cu + n + 1);
+        }
+        unpack<T>(xs[(u + K - 1) * NV], win[K - 1]);
+        dsum_row(u, t - start, win, true);
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+          for (int c = 0; c < V; ++c) win[j][c] = win[j + 1][c];
+      }
+      if (g < K - 1) {  // one of the K-1 rows after the tile
+        const int u = kConvTRB + g, t = min(t0 + u, a.T - 1);
+#pragma unroll
+        for (int j = 0; j < K; ++j) unpack<T>(xs[(u + j) * NV], win[j]);
+        dsum_row(u, t - __ldg(a.cu + seq_of(a.cu, a.n_seqs, t)), win, false);
+      }
+    }
+    __syncthreads();
+    // ---- phase B: dx of rows s = t0 + g*RPT + r
+    if (vok) {
+      const int s0 = t0 + g * RPT;
+      int n = seq_of(a.cu, a.n_seqs, s0 < a.T ? s0 : a.T - 1);
+      int end = __ldg(a.cu + n + 1);
+      T* dxb = (T*)a.y + c0 + v * V;
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        const int s = s0 + r;
+        if (s >= a.T) break;
+        while (s >= end && n + 1 < a.n_seqs) end = __ldg(a.cu + (++n) + 1);
+        const int room = end - s;  // d_sum[s + m] counts iff m < room
+        float out[V];
+#pragma unroll
+        for (int c = 0; c < V; ++c) out[c] = 0.f;
+#pragma unroll
+        for (int m = 0; m < K; ++m) {
+          if (m < room) {
+            const float4* d = (const float4*)(dsb + (g * RPT + r + m) * SW + v * V);
+#pragma unroll
+            for (int c = 0; c < V; c += 4) {
+              const float4 f = d[c / 4];
+              out[c] = fmaf(f.x, wt[K - 1 - m][c], out[c]);
+              out[c + 1] = fmaf(f.y, wt[K - 1 - m][c + 1], out[c + 1]);
+              out[c + 2] = fmaf(f.z, wt[K - 1 - m][c + 2], out[c + 2]);
+              out[c + 3] = fmaf(f.w, wt[K - 1 - m][c + 3], out[c + 3]);
+            }
+          }
+        }
+        st16(dxb + (int64_t)s * a.y_ld, pack<T>(out));
+      }
+    }
+    __syncthreads();  // d_sum buffer and stage reused
   }
-  if (!a.dw_part) return;  // uniform: the same for every thread of the launch
-  // dw of the block's tokens: warps summed in order through shared memory
-#pragma unroll
-  for (int j = 0; j < K; ++j)
-#pragma unroll
-    for (int i = 0; i < V; ++i) red[warp][i * K + j][lane] = dwa[j][i];
-  __syncthreads();
-  float* part = a.dw_part + (int64_t)blockIdx.y * a.C * K;
-  const int64_t cb = (int64_t)blockIdx.x * 32 * V;  // first channel of the block
-  for (int e = threadIdx.x; e < 32 * K * V; e += kConvWarps * 32) {
-    const int l = e / (K * V), ij = e % (K * V);   // lane l, channel c0(l) + i, tap j
-    const int64_t c = cb + (int64_t)l * V + ij / K;
-    if (c >= a.C) continue;
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConvWarps; ++w) s += red[w][ij][l];
-    part[c * K + ij % K] = s;
+  tc::cp_async_wait<0>();
+  if (a.dw_part && cur_slab >= 0) {  // uniform
+    const bool second = cur_slab != (i0 / n_tt);
+    conv_dw_flush<T, K>(dwa, dsb, a.dw_part + ((size_t)blockIdx.x * 2 + (second ? 1 : 0)) * SW * K,
+                        v, g);
   }
+}
+
+// dw[c, j] = sum over the blocks b whose tiles touch c's slab, in order, of their partial
+// for that slab (slot 0 when the slab is the block's first, else slot 1).
+__global__ void __launch_bounds__(256) k_conv_dw_sum(const float* part, int C, int K, int SW,
+                                                     int n_tt, int q, float* dw) {
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  if (e >= C * K) return;
+  const int c = e / K, j = e % K, s = c / SW, cc = c % SW;
+  const int b0 = (s * n_tt) / q, b1 = ((s + 1) * n_tt - 1) / q;
+  float acc = 0.f;
+  for (int b = b0; b <= b1; ++b) {
+    const int slot = (b * q) / n_tt == s ? 0 : 1;
+    acc += part[(((size_t)b * 2 + slot) * SW + cc) * K + j];
+  }
+  dw[e] = acc;
 }
 
 // ---- gated RMSNorm --------------------------------------------------------------------------
 // Per (token t, head h) row of D values: rms = sqrt(mean o^2 + eps),
-// y = (o / rms) gamma SiLU(z), gamma [D] shared by the heads.  LPR = D / V lanes own a
-// row (V channels each, 16 bytes); a warp holds 32 / LPR rows; the row sums are
-// butterfly shuffles inside the LPR lanes.
+// y = (o / rms) gamma SiLU(z), gamma [D] shared by the heads.  A token's H*D values are
+// H*LPR 16-byte vectors (LPR = D / V a row), numbered j; vector g of the launch is vector
+// g % (H LPR) of token g / (H LPR), its column j V.  The LPR vectors of a row are
+// consecutive lanes of one warp, so the row sums are butterflies over LPR lanes; a thread
+// always holds the same column of gamma (vector index mod LPR = lane mod LPR).
 constexpr int kNormThreads = 256;
-constexpr int kNormBwdBlocks = 608;  // grid cap of the backward (fixed: d gamma's order)
+constexpr int kNormFwdNI = 4;          // vectors of a forward thread (loads in flight)
+constexpr int kNormBwdNI = 2;          // vectors of a backward thread per step
+constexpr int kNormBwdMaxBlocks = 1024;
 
 struct NormArgs {
-  int64_t rows;  // T * H
-  int H, D;
+  int T, H, D;
   float eps;
   const void* o;
   int64_t o_ld;
@@ -363,159 +495,198 @@ __device__ __forceinline__ float row_sum(float x) {
   return x;
 }
 
-template <typename T, int V, int LPR>
+template <typename T, int LPR>
 __global__ void __launch_bounds__(kNormThreads) k_norm_fwd(NormArgs a) {
-  using VT = Vec<T, V>;
-  const int64_t g = (int64_t)blockIdx.x * kNormThreads + threadIdx.x;
-  const int64_t r = g / LPR;
-  const int li = (int)(g % LPR);
-  const bool ok = r < a.rows;  // every lane joins the shuffles
-  const int64_t t = ok ? r / a.H : 0;
-  const int h = ok ? (int)(r % a.H) : 0;
-  const int64_t col = (int64_t)h * a.D + li * V;
-  float o[V], z[V];
-  if (ok) {
-    VT::load((const T*)a.o + t * a.o_ld + col, o);
-    VT::load((const T*)a.z + t * a.z_ld + col, z);
-  } else {
+  constexpr int V = kVec<T>, NI = kNormFwdNI;
+  const uint32_t HV = (uint32_t)a.H * LPR, nv = (uint32_t)a.T * HV;
+  const int li = threadIdx.x % LPR;
+  uint4 ov[NI], zv[NI];
+  uint32_t tk[NI], jv[NI];
 #pragma unroll
-    for (int i = 0; i < V; ++i) o[i] = z[i] = 0.f;
+  for (int k = 0; k < NI; ++k) {
+    const uint32_t g = ((uint32_t)blockIdx.x * NI + k) * kNormThreads + threadIdx.x;
+    tk[k] = g / HV;
+    jv[k] = g - tk[k] * HV;
+    if (g < nv) {
+      ov[k] = ld16((const T*)a.o + tk[k] * a.o_ld + jv[k] * V);
+      zv[k] = ld16((const T*)a.z + tk[k] * a.z_ld + jv[k] * V);
+    } else {
+      ov[k] = zv[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
-  float ss = 0.f;
+  float gm[V];
 #pragma unroll
-  for (int i = 0; i < V; ++i) ss = fmaf(o[i], o[i], ss);
-  ss = row_sum<LPR>(ss);
-  const float inv = 1.f / sqrtf(ss / (float)a.D + a.eps);
-  if (!ok) return;
-  float y[V];
+  for (int c = 0; c < V; ++c) gm[c] = __ldg(a.gamma + li * V + c);
+  const float invD = 1.f / (float)a.D;
 #pragma unroll
-  for (int i = 0; i < V; ++i) y[i] = o[i] * inv * __ldg(a.gamma + li * V + i) * silu_f(z[i]);
-  VT::store((T*)a.y + t * a.y_ld + col, y);
+  for (int k = 0; k < NI; ++k) {
+    float o[V], z[V];
+    unpack<T>(ov[k], o);
+    unpack<T>(zv[k], z);
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) ss = fmaf(o[c], o[c], ss);
+    ss = row_sum<LPR>(ss);  // every lane: the shuffles need the whole warp
+    const float inv = rsqrtf(fmaf(ss, invD, a.eps));
+    float y[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) y[c] = o[c] * inv * gm[c] * (z[c] * sigmoid_fast(z[c]));
+    if (tk[k] < (uint32_t)a.T) st16((T*)a.y + tk[k] * a.y_ld + jv[k] * V, pack<T>(y));
+  }
 }
 
 // Backward (section 2 of the backward): d_xn = dy gamma SiLU(z),
 // dz = dy gamma x_n SiLU'(z), do = d_xn / rms - o (sum_j d_xn_j o_j) / (rms^3 D),
-// d gamma = sum over rows of dy x_n SiLU(z).  Rows are taken grid-stride (a fixed grid),
-// so each thread's d gamma share, and the block sum over its row slots, have a fixed order.
-template <typename T, int V, int LPR>
+// d gamma = sum over rows of dy x_n SiLU(z).  Blocks take groups of NI * 256 vectors
+// grid-stride (a fixed grid), so each thread's d gamma share, and the block sum over its
+// row slots, have a fixed order.
+template <typename T, int LPR>
 __global__ void __launch_bounds__(kNormThreads) k_norm_bwd(NormArgs a) {
-  using VT = Vec<T, V>;
-  constexpr int RPB = kNormThreads / LPR;  // row slots of a block
+  constexpr int V = kVec<T>, NI = kNormBwdNI, RPB = kNormThreads / LPR;
   __shared__ float red[RPB][LPR * V];
+  const uint32_t HV = (uint32_t)a.H * LPR, nv = (uint32_t)a.T * HV;
   const int li = threadIdx.x % LPR, slot = threadIdx.x / LPR;
-  float dga[V];
+  float gm[V], dga[V];
 #pragma unroll
-  for (int i = 0; i < V; ++i) dga[i] = 0.f;
-  float gm[V];
+  for (int c = 0; c < V; ++c) {
+    gm[c] = __ldg(a.gamma + li * V + c);
+    dga[c] = 0.f;
+  }
+  const float invD = 1.f / (float)a.D;
+  const uint32_t n_groups = (nv + NI * kNormThreads - 1) / (NI * kNormThreads);
+  for (uint32_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {  // uniform per block
+    uint4 ov[NI], zv[NI], gv[NI];
+    uint32_t tk[NI], jv[NI];
 #pragma unroll
-  for (int i = 0; i < V; ++i) gm[i] = __ldg(a.gamma + li * V + i);
-  const int64_t n_groups = (a.rows + RPB - 1) / RPB;
-  for (int64_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {  // uniform per block
-    const int64_t r = grp * RPB + slot;
-    const bool ok = r < a.rows;
-    const int64_t t = ok ? r / a.H : 0;
-    const int h = ok ? (int)(r % a.H) : 0;
-    const int64_t col = (int64_t)h * a.D + li * V;
-    float o[V], z[V], dy[V];
-    if (ok) {
-      VT::load((const T*)a.o + t * a.o_ld + col, o);
-      VT::load((const T*)a.z + t * a.z_ld + col, z);
-      VT::load((const T*)a.dy + t * a.dy_ld + col, dy);
-    } else {
-#pragma unroll
-      for (int i = 0; i < V; ++i) o[i] = z[i] = dy[i] = 0.f;
+    for (int k = 0; k < NI; ++k) {
+      const uint32_t g = (grp * NI + k) * kNormThreads + threadIdx.x;
+      tk[k] = g / HV;
+      jv[k] = g - tk[k] * HV;
+      if (g < nv) {
+        ov[k] = ld16((const T*)a.o + tk[k] * a.o_ld + jv[k] * V);
+        zv[k] = ld16((const T*)a.z + tk[k] * a.z_ld + jv[k] * V);
+        gv[k] = ld16((const T*)a.dy + tk[k] * a.dy_ld + jv[k] * V);
+      } else {
+        ov[k] = zv[k] = gv[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
-    float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < V; ++i) ss = fmaf(o[i], o[i], ss);
-    ss = row_sum<LPR>(ss);
-    const float rms = sqrtf(ss / (float)a.D + a.eps), inv = 1.f / rms;
-    float dxn[V], dz[V], dot = 0.f;
+    for (int k = 0; k < NI; ++k) {
+      float o[V], z[V], dy[V];
+      unpack<T>(ov[k], o);
+      unpack<T>(zv[k], z);
+      unpack<T>(gv[k], dy);
+      float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const float xn = o[i] * inv, sz = silu_f(z[i]);
-      dxn[i] = dy[i] * gm[i] * sz;
-      dz[i] = dy[i] * gm[i] * xn * silu_grad_f(z[i]);
-      dga[i] = fmaf(dy[i] * xn, sz, dga[i]);
-      dot = fmaf(dxn[i], o[i], dot);
-    }
-    dot = row_sum<LPR>(dot);
-    const float c = dot * inv * inv * inv / (float)a.D;
-    if (ok) {
-      float d_o[V];
+      for (int c = 0; c < V; ++c) ss = fmaf(o[c], o[c], ss);
+      ss = row_sum<LPR>(ss);
+      const float inv = rsqrtf(fmaf(ss, invD, a.eps));
+      float dxn[V], dz[V], dot = 0.f;
 #pragma unroll
-      for (int i = 0; i < V; ++i) d_o[i] = fmaf(dxn[i], inv, -o[i] * c);
-      VT::store((T*)a.y + t * a.y_ld + col, d_o);
-      VT::store((T*)a.dz + t * a.dz_ld + col, dz);
+      for (int c = 0; c < V; ++c) {
+        const float sg = sigmoid_fast(z[c]), sz = z[c] * sg;
+        const float xn = o[c] * inv, dyg = dy[c] * gm[c];
+        dxn[c] = dyg * sz;
+        dz[c] = dyg * xn * fmaf(sz, 1.f - sg, sg);  // SiLU'(z) = sg + z sg (1 - sg)
+        dga[c] = fmaf(dy[c] * xn, sz, dga[c]);
+        dot = fmaf(dxn[c], o[c], dot);
+      }
+      dot = row_sum<LPR>(dot);
+      const float cc = dot * inv * inv * inv * invD;
+      if (tk[k] < (uint32_t)a.T) {
+        float d_o[V];
+#pragma unroll
+        for (int c = 0; c < V; ++c) d_o[c] = fmaf(dxn[c], inv, -o[c] * cc);
+        st16((T*)a.y + tk[k] * a.y_ld + jv[k] * V, pack<T>(d_o));
+        st16((T*)a.dz + tk[k] * a.dz_ld + jv[k] * V, pack<T>(dz));
+      }
     }
   }
   if (!a.dg_part) return;  // uniform
 #pragma unroll
-  for (int i = 0; i < V; ++i) red[slot][li * V + i] = dga[i];
+  for (int c = 0; c < V; ++c) red[slot][li * V + c] = dga[c];
   __syncthreads();
   for (int j = threadIdx.x; j < a.D; j += kNormThreads) {
     float s = 0.f;
     for (int sl = 0; sl < RPB; ++sl) s += red[sl][j];
-    a.dg_part[(int64_t)blockIdx.x * a.D + j] = s;
+    a.dg_part[(size_t)blockIdx.x * a.D + j] = s;
   }
 }
 
-// ---- fixed-order sums of per-block partials: out[i] = sum_b part[b * n + i] -------------
-// Few blocks (the conv's token tiles): one thread per output, b in order.
-__global__ void __launch_bounds__(256) k_sum_parts_thread(const float* part, int nb, int64_t n,
-                                                          float* out) {
-  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  if (i >= n) return;
-  float s = 0.f;
-  for (int b = 0; b < nb; ++b) s += part[(int64_t)b * n + i];
-  out[i] = s;
-}
-// Many blocks (the norm's grid): one warp per output, lane l summing b = l, l + 32, ...
-// in order, then a butterfly over the lanes (a fixed order too).
-__global__ void __launch_bounds__(256) k_sum_parts_warp(const float* part, int nb, int64_t n,
+// d gamma[i] = sum over blocks b in order of part[b, i]: one warp per output, lane l
+// summing b = l, l + 32, ... in order, then a butterfly over the lanes (a fixed order).
+__global__ void __launch_bounds__(256) k_sum_parts_warp(const float* part, int nb, int n,
                                                         float* out) {
-  const int64_t i = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (i >= n) return;  // whole warps
   float s = 0.f;
-  for (int b = lane; b < nb; b += 32) s += part[(int64_t)b * n + i];
+  for (int b = lane; b < nb; b += 32) s += part[(size_t)b * n + i];
   out[i] = warp_sum(s);
 }
 
-template <bool BWD, typename T, int V, int U>
-cudaError_t conv_dispatch(int K, const ConvArgs& a, dim3 grid, cudaStream_t st) {
-  const dim3 block(kConvWarps * 32);
-#define GDN_CONV_CASE(KK)                                \
-  case KK:                                               \
-    if constexpr (BWD)                                   \
-      k_conv_bwd<T, V, KK, U><<<grid, block, 0, st>>>(a); \
-    else                                                 \
-      k_conv_fwd<T, V, KK, U><<<grid, block, 0, st>>>(a); \
-    break;
-  switch (K) {
-    GDN_CONV_CASE(1)
-    GDN_CONV_CASE(2)
-    GDN_CONV_CASE(3)
-    GDN_CONV_CASE(4)
-    default: return cudaErrorInvalidValue;
+// ---- launch geometry ------------------------------------------------------------------------
+struct ConvGeom {
+  int n_slabs, n_tt, total, q, grid;
+};
+// Forward: 2 blocks an SM; backward: 1 block an SM and at most 2 slabs a block (q <= n_tt).
+// `blocks` is the number of resident blocks to fill (capped at 1024).
+inline ConvGeom conv_geom(bool bwd, int T, int C, int es, int blocks) {
+  ConvGeom g;
+  const int sw = (bwd ? kSlabVecB : kSlabVec) * (16 / es);
+  const int tr = bwd ? kConvTRB : kConvTR;
+  g.n_slabs = (C + sw - 1) / sw;
+  g.n_tt = (T + tr - 1) / tr;
+  g.total = g.n_slabs * g.n_tt;
+  blocks = blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks);
+  g.q = (g.total + blocks - 1) / blocks;
+  if (bwd && g.q > g.n_tt) g.q = g.n_tt;
+  if (g.q < 1) g.q = 1;
+  g.grid = (g.total + g.q - 1) / g.q;
+  return g;
+}
+
+template <bool BWD, typename T, int K>
+cudaError_t conv_launch(const ConvArgs& a, int grid, cudaStream_t st) {
+  const size_t smem = BWD ? ConvBwdGeom<T, K>::smem
+                          : sizeof(uint4) * (size_t)kConvNS * (kConvTR + K - 1) * kSlabVec;
+  static bool attr_set = false;  // one instantiation, one attribute
+  if (!attr_set) {
+    const cudaError_t e =
+        BWD ? cudaFuncSetAttribute(k_conv_bwd<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem)
+            : cudaFuncSetAttribute(k_conv_fwd<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
   }
-#undef GDN_CONV_CASE
+  if constexpr (BWD)
+    k_conv_bwd<T, K><<<grid, kConvThreads, smem, st>>>(a);
+  else
+    k_conv_fwd<T, K><<<grid, kConvThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
-template <typename T, int V>
-cudaError_t norm_dispatch(bool bwd, const NormArgs& a, cudaStream_t st) {
-  const int LPR = a.D / V;
-  const int64_t threads = a.rows * LPR;
-  const int64_t n_groups = (a.rows + kNormThreads / LPR - 1) / (kNormThreads / LPR);
-  const unsigned grid = bwd ? (unsigned)(n_groups < kNormBwdBlocks ? n_groups : kNormBwdBlocks)
-                            : (unsigned)((threads + kNormThreads - 1) / kNormThreads);
-#define GDN_NORM_CASE(L)                                                  \
-  case L:                                                                 \
-    if (bwd)                                                              \
-      k_norm_bwd<T, V, L><<<grid, kNormThreads, 0, st>>>(a);              \
-    else                                                                  \
-      k_norm_fwd<T, V, L><<<grid, kNormThreads, 0, st>>>(a);              \
+template <bool BWD, typename T>
+cudaError_t conv_dispatch(int K, const ConvArgs& a, int grid, cudaStream_t st) {
+  switch (K) {
+    case 1: return conv_launch<BWD, T, 1>(a, grid, st);
+    case 2: return conv_launch<BWD, T, 2>(a, grid, st);
+    case 3: return conv_launch<BWD, T, 3>(a, grid, st);
+    case 4: return conv_launch<BWD, T, 4>(a, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool BWD, typename T>
+cudaError_t norm_dispatch(const NormArgs& a, int grid, cudaStream_t st) {
+  const int LPR = a.D / kVec<T>;
+#define GDN_NORM_CASE(L)                                      \
+  case L:                                                     \
+    if constexpr (BWD)                                        \
+      k_norm_bwd<T, L><<<grid, kNormThreads, 0, st>>>(a);     \
+    else                                                      \
+      k_norm_fwd<T, L><<<grid, kNormThreads, 0, st>>>(a);     \
     break;
   switch (LPR) {
     GDN_NORM_CASE(2)
@@ -529,21 +700,51 @@ cudaError_t norm_dispatch(bool bwd, const NormArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <typename T>
+int norm_bwd_resident_blocks(int D) {
+  int per_sm = 0;
+  const int LPR = D / kVec<T>;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (LPR) {
+    case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_norm_bwd<T, 2>, kNormThreads, 0); break;
+    case 4: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_norm_bwd<T, 4>, kNormThreads, 0); break;
+    case 8: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_norm_bwd<T, 8>, kNormThreads, 0); break;
+    case 16: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_norm_bwd<T, 16>, kNormThreads, 0); break;
+    case 32: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_norm_bwd<T, 32>, kNormThreads, 0); break;
+    default: break;
+  }
+  if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+  return per_sm * sm_count();
+}
+
 }  // namespace
 
 size_t conv_partial_floats(int64_t T, int C, int K) {
-  return (size_t)((T + kConvRows - 1) / kConvRows) * (size_t)C * (size_t)K;
+  // the largest backward grid any device could get (1024 resident blocks), either dtype
+  size_t most = 0;
+  for (int es : {2, 4}) {
+    const ConvGeom g = conv_geom(true, (int)T, C, es, 1024);
+    const size_t f = (size_t)g.grid * 2 * kSlabVecB * (16 / es) * K;
+    most = f > most ? f : most;
+  }
+  return most;
 }
-size_t norm_partial_floats(int D) { return (size_t)kNormBwdBlocks * (size_t)D; }
+size_t norm_partial_floats(int D) { return (size_t)kNormBwdMaxBlocks * (size_t)D; }
 
 cudaError_t launch_conv1d_silu(bool bwd, int dtype, int64_t T, int C, int K, const int32_t* cu,
                                int n_seqs, const void* x, int64_t x_ld, const float* w,
                                const void* dy, int64_t dy_ld, void* y, int64_t y_ld, float* dw,
                                float* part, cudaStream_t st) {
+  const bool bf = dtype == GDN_DTYPE_BF16;
+  const int es = bf ? 2 : 4;
+  const ConvGeom g = conv_geom(bwd, (int)T, C, es, (bwd ? 1 : 2) * sm_count());
   ConvArgs a;
-  a.T = T;
+  a.T = (int)T;
   a.C = C;
+  a.K = K;
   a.n_seqs = n_seqs;
+  a.n_slabs = g.n_slabs;
+  a.q = g.q;
   a.cu = cu;
   a.x = x;
   a.x_ld = x_ld;
@@ -552,26 +753,20 @@ cudaError_t launch_conv1d_silu(bool bwd, int dtype, int64_t T, int C, int K, con
   a.dy_ld = dy_ld;
   a.y = y;
   a.y_ld = y_ld;
-  a.dw_part = dw ? part : nullptr;
-  // forward: 16-byte vectors, 32 bytes of loads ahead (bf16) or 64 (fp32); backward: 4
-  // channels a thread and 2 tokens ahead (the walk holds twice the forward's registers)
-  const bool bf = dtype == GDN_DTYPE_BF16;
-  const int V = bwd ? 4 : (bf ? 8 : 4);
-  const int n_tiles = (int)((T + kConvRows - 1) / kConvRows);
-  const dim3 grid((unsigned)((C / V + 31) / 32), (unsigned)n_tiles);
+  a.dw_part = bwd && dw ? part : nullptr;
   profile_pre(st, bwd ? KID_CONV_BWD : KID_CONV_FWD);
   cudaError_t e;
   if (bwd)
-    e = bf ? conv_dispatch<true, __nv_bfloat16, 4, 2>(K, a, grid, st)
-           : conv_dispatch<true, float, 4, 2>(K, a, grid, st);
+    e = bf ? conv_dispatch<true, __nv_bfloat16>(K, a, g.grid, st)
+           : conv_dispatch<true, float>(K, a, g.grid, st);
   else
-    e = bf ? conv_dispatch<false, __nv_bfloat16, 8, 2>(K, a, grid, st)
-           : conv_dispatch<false, float, 4, 4>(K, a, grid, st);
+    e = bf ? conv_dispatch<false, __nv_bfloat16>(K, a, g.grid, st)
+           : conv_dispatch<false, float>(K, a, g.grid, st);
   profile_post(st);
   if (e != cudaSuccess || !a.dw_part) return e;
-  const int64_t n = (int64_t)C * K;
   profile_pre(st, KID_SUM_PARTS);
-  k_sum_parts_thread<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(part, n_tiles, n, dw);
+  k_conv_dw_sum<<<(C * K + 255) / 256, 256, 0, st>>>(part, C, K, kSlabVecB * (16 / es), g.n_tt,
+                                                     g.q, dw);
   profile_post(st);
   return cudaGetLastError();
 }
@@ -582,7 +777,7 @@ cudaError_t launch_gated_rmsnorm(bool bwd, int dtype, int64_t T, int H, int D, f
                                  int64_t y_ld, void* dz, int64_t dz_ld, float* dgamma,
                                  float* part, cudaStream_t st) {
   NormArgs a;
-  a.rows = T * H;
+  a.T = (int)T;
   a.H = H;
   a.D = D;
   a.eps = eps;
@@ -599,16 +794,26 @@ cudaError_t launch_gated_rmsnorm(bool bwd, int dtype, int64_t T, int H, int D, f
   a.dz_ld = dz_ld;
   a.dg_part = bwd && dgamma ? part : nullptr;
   const bool bf = dtype == GDN_DTYPE_BF16;
+  const int64_t nv = T * H * (D / (bf ? 8 : 4));  // 16-byte vectors
+  const int NI = bwd ? kNormBwdNI : kNormFwdNI;
+  const int64_t groups = (nv + NI * kNormThreads - 1) / (NI * kNormThreads);
+  int grid = (int)groups;
+  if (bwd) {
+    int res = bf ? norm_bwd_resident_blocks<__nv_bfloat16>(D) : norm_bwd_resident_blocks<float>(D);
+    res = res > kNormBwdMaxBlocks ? kNormBwdMaxBlocks : res;
+    grid = groups < res ? (int)groups : res;
+  }
   profile_pre(st, bwd ? KID_NORM_BWD : KID_NORM_FWD);
-  const cudaError_t e = bf ? norm_dispatch<__nv_bfloat16, 8>(bwd, a, st)
-                           : norm_dispatch<float, 4>(bwd, a, st);
+  cudaError_t e;
+  if (bwd)
+    e = bf ? norm_dispatch<true, __nv_bfloat16>(a, grid, st) : norm_dispatch<true, float>(a, grid, st);
+  else
+    e = bf ? norm_dispatch<false, __nv_bfloat16>(a, grid, st)
+           : norm_dispatch<false, float>(a, grid, st);
   profile_post(st);
   if (e != cudaSuccess || !a.dg_part) return e;
-  const int V = bf ? 8 : 4, LPR = D / V;
-  const int64_t n_groups = (a.rows + kNormThreads / LPR - 1) / (kNormThreads / LPR);
-  const int nb = (int)(n_groups < kNormBwdBlocks ? n_groups : kNormBwdBlocks);
   profile_pre(st, KID_SUM_PARTS);
-  k_sum_parts_warp<<<(unsigned)((D + 7) / 8), 256, 0, st>>>(part, nb, D, dgamma);
+  k_sum_parts_warp<<<(D + 7) / 8, 256, 0, st>>>(part, grid, D, dgamma);
   profile_post(st);
   return cudaGetLastError();
 }

@@ -278,7 +278,8 @@ int gdn_decode_step(const gdn_shape* shape, const void* q, int64_t q_ld, const v
  * token.  Backward, with pre[t, c] the argument of SiLU and d_sum = dy * SiLU'(pre):
  *   dx[s, c] = sum_{j<K} d_sum[s + K-1-j, c] * w[c*K + j]   (terms inside s's sequence)
  *   dw[c*K + j] = sum_t d_sum[t, c] * x[t - (K-1) + j, c]
- *   channels     C, a multiple of 8 (the packed q|k|v width 2 Hk Dk + Hv Dv is one)
+ *   channels     C, a multiple of 8 (the packed q|k|v width 2 Hk Dk + Hv Dv is one),
+ *                at most 2^24;  total_tokens at most 2^30
  *   kernel_size  K in 1..4
  *   cu_seqlens   device, int32 [n_seqs + 1]: 0 = cu[0] <= ... <= cu[n_seqs] = total_tokens
  *                (not checked on the host; a malformed one gives wrong values but every
@@ -309,7 +310,8 @@ int gdn_conv1d_silu_backward(int32_t dtype, int64_t total_tokens, int32_t channe
  *   d_xn = dy gamma SiLU(z),  dz = dy gamma x_n SiLU'(z),
  *   do = d_xn / rms - o (sum_j d_xn_j o_j) / (rms^3 head_dim),
  *   d gamma[j] = sum over tokens and heads of dy_j x_n,j SiLU(z_j)
- *   n_heads      H >= 1;  head_dim D in {16, 32, 64, 128};  eps >= 0 (finite)
+ *   n_heads      H >= 1;  head_dim D in {16, 32, 64, 128};  eps >= 0 (finite);
+ *                total_tokens * H * D at most 2^31
  *   o, z         device, [total_tokens, *_ld] holding H*D used columns
  *   gamma        device, fp32 [D]
  *   y            device, [total_tokens, y_ld] (written)
