@@ -98,6 +98,9 @@ _lib.gdn_gated_rmsnorm_backward.argtypes = ([ctypes.c_int32, _i64, ctypes.c_int3
                                              ctypes.c_float] + [_vp, _i64] * 2 + [_vp] +
                                             [_vp, _i64] * 3 + [_vp, _vp, _sz, _vp])
 _lib.gdn_gated_rmsnorm_backward.restype = ctypes.c_int
+_lib.gdn_state_compose.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp,
+                                   _vp, ctypes.c_int32, _vp]
+_lib.gdn_state_compose.restype = ctypes.c_int
 _lib.gdn_read_device_status.argtypes = [_vp, _vp]
 _lib.gdn_read_device_status.restype = ctypes.c_int
 _lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -116,7 +119,8 @@ EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_for
             "gdn_profile_end", "gdn_kernel_name", "gdn_last_error", "gdn_forward_noalloc",
             "gdn_decode_step", "gdn_conv1d_silu_forward", "gdn_conv1d_silu_workspace_bytes",
             "gdn_conv1d_silu_backward", "gdn_gated_rmsnorm_forward",
-            "gdn_gated_rmsnorm_workspace_bytes", "gdn_gated_rmsnorm_backward")
+            "gdn_gated_rmsnorm_workspace_bytes", "gdn_gated_rmsnorm_backward",
+            "gdn_state_compose")
 
 
 class GdnError(RuntimeError):
@@ -327,6 +331,18 @@ def gdn_gated_rmsnorm_backward(o, z, gamma, dy, d_o, dz, eps, dgamma=None, works
         args += list(_mat(t))
     args += [_ptr(dgamma), _ptr(workspace), _nbytes(workspace), _stream(stream)]
     _check(_lib.gdn_gated_rmsnorm_backward(*args), "gdn_gated_rmsnorm_backward")
+
+
+def gdn_state_compose(Phi, S, R, out, transpose=False, stream=None) -> None:
+    """Calls gdn_state_compose: out[b] = op(Phi[b]) S[b] + R[b] over the leading blocks
+    (Phi [..., Dk, Dk], S / R / out [..., Dk, Dv], fp32, contiguous; R may be None)."""
+    Dk, Dv = int(S.shape[-2]), int(S.shape[-1])
+    n = int(S.numel()) // (Dk * Dv) if S.numel() else 0
+    for t in (Phi, S, R, out):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("gdn_state_compose needs contiguous tensors")
+    _check(_lib.gdn_state_compose(n, Dk, Dv, _ptr(Phi), _ptr(S), _ptr(R), _ptr(out),
+                                  1 if transpose else 0, _stream(stream)), "gdn_state_compose")
 
 
 def gdn_read_device_status(workspace, stream=None) -> int:

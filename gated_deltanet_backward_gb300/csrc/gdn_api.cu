@@ -357,6 +357,7 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_NORM_FWD: return "gdn_gated_rmsnorm_fwd";
     case gdn::KID_NORM_BWD: return "gdn_gated_rmsnorm_bwd";
     case gdn::KID_SUM_PARTS: return "gdn_sum_partials";
+    case gdn::KID_COMPOSE: return "gdn_state_compose";
     default: return "?";
   }
 }
@@ -688,6 +689,28 @@ int gdn_gated_rmsnorm_backward(int32_t dtype, int64_t total_tokens, int32_t n_he
                                 dy, dy_ld, d_o, do_ld, dz, dz_ld, dgamma, (float*)workspace,
                                 (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail("gdn_gated_rmsnorm_backward: kernel launch", e);
+  return GDN_OK;
+}
+
+int gdn_state_compose(int32_t n, int32_t Dk, int32_t Dv, const float* Phi, const float* S,
+                      const float* R, float* out, int32_t transpose, void* stream) {
+  if (n < 0 || Dk <= 0 || Dv <= 0 || Dk > 4096 || Dv > 4096 || (transpose != 0 && transpose != 1))
+    return GDN_ERR_INVALID_ARG;
+  if (n > 65535) return GDN_ERR_UNSUPPORTED;
+  GDN_TRY(check_vec(Phi, n > 0));
+  GDN_TRY(check_vec(S, n > 0));
+  GDN_TRY(check_vec(R, false));
+  GDN_TRY(check_vec(out, n > 0));
+  const int64_t sz = (int64_t)n * Dk * Dv;
+  if (overlaps(Phi, 0, out, 0, 1, (int64_t)n * Dk * Dk, 4) || overlaps(S, 0, out, 0, 1, sz, 4))
+    return GDN_ERR_INVALID_ARG;
+  if (R && R != out && overlaps(R, 0, out, 0, 1, sz, 4)) return GDN_ERR_INVALID_ARG;
+  if (n == 0) return GDN_OK;
+  (void)cudaGetLastError();
+  g_last_error[0] = 0;
+  const cudaError_t e = gdn::launch_state_compose(n, Dk, Dv, Phi, S, R, out, transpose != 0,
+                                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("gdn_state_compose: kernel launch", e);
   return GDN_OK;
 }
 

@@ -234,7 +234,8 @@ enum KernelId {
   KID_NORM_FWD = 16,
   KID_NORM_BWD = 17,
   KID_SUM_PARTS = 18,
-  KID_COUNT = 19
+  KID_COMPOSE = 19,
+  KID_COUNT = 20
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
@@ -279,6 +280,9 @@ cudaError_t launch_gated_rmsnorm(bool bwd, int dtype, int64_t T, int H, int D, f
                                  const float* gamma, const void* dy, int64_t dy_ld, void* y,
                                  int64_t y_ld, void* dz, int64_t dz_ld, float* dgamma,
                                  float* part, cudaStream_t st);
+// out = op(Phi) S + R for n blocks (gdn_context.cu); R may be null (zero).
+cudaError_t launch_state_compose(int n, int Dk, int Dv, const float* Phi, const float* S,
+                                 const float* R, float* out, bool transpose, cudaStream_t st);
 cudaError_t launch_decode(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
                           int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
                           int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,

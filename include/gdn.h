@@ -331,6 +331,25 @@ int gdn_gated_rmsnorm_backward(int32_t dtype, int64_t total_tokens, int32_t n_he
                                float* dgamma, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* ---- Context parallelism: composing segment state maps ---------------------------------
+ * A sequence cut into consecutive segments maps each segment's start state affinely to its
+ * end state (the forward recap's update rewritten as S_t = g_t (I - beta_t k_t k_t^T)
+ * S_{t-1} + beta_t k_t v_t^T):  S_out = Phi S_in + R, Phi = prod_t g_t (I - beta_t k_t
+ * k_t^T) (Dk x Dk, latest token leftmost), R the end state from a zero start; the
+ * start-state gradient is dS_in = Phi^T dS_out + G.  Phi is gdn_forward's S_T for the
+ * segment run with v = 0 from S_0 = I (a shape with Dv = Dk); R is its S_T from S_0 = 0;
+ * G is gdn_backward's dS_0 with dS_T = 0.  This call does the composition:
+ *   out[b] = op(Phi[b]) S[b] + R[b]   for b < n,  op = identity or transpose
+ *   Phi   device, fp32 [n, Dk, Dk] contiguous
+ *   S     device, fp32 [n, Dk, Dv] contiguous
+ *   R     device, fp32 [n, Dk, Dv] contiguous, or NULL (zero)
+ *   out   device, fp32 [n, Dk, Dv] (written); may be R itself, must not overlap Phi or S
+ *   transpose  0: Phi S + R;  1: Phi^T S + R
+ * n at most 65535, Dk and Dv at most 4096; buffers 16-byte aligned.  Returns GDN_OK,
+ * GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_MISALIGNED or GDN_ERR_CUDA. */
+int gdn_state_compose(int32_t n, int32_t Dk, int32_t Dv, const float* Phi, const float* S,
+                      const float* R, float* out, int32_t transpose, void* stream);
+
 /* Synchronises `stream` and returns the device-side status recorded in
  * `workspace` by the last gdn_forward / gdn_backward that used it (GDN_OK, or
  * the first device error), or GDN_ERR_CUDA if the stream itself failed. */

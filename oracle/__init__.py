@@ -72,6 +72,7 @@ def _load():
             lib.gdn_oracle_backward.restype = ctypes.c_int
             lib.gdn_oracle_forward_states.restype = ctypes.c_int
             lib.gdn_oracle_hardware_threads.restype = ctypes.c_int
+            lib.gdn_oracle_state_map.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -266,3 +267,21 @@ def gated_rmsnorm_backward(o, z, gamma, dy, H, D, eps):
     if rc != 0:
         raise ValueError("gdn_oracle_gated_rmsnorm_backward rejected its arguments")
     return d_o, dz, dg
+
+
+# ---------------------------------------------------------------------------
+# Context parallelism: the state map of a sequence, S_T = Phi S_0 + R.
+def state_map(q, k, alpha, beta_raw, a_log, dt_bias, cu_seqlens, *, Hk, Hv, Dk, n_threads=0,
+              head_map=0):
+    """Phi [N, Hv, Dk, Dk] (f64): the product over a sequence's tokens of
+    g_t (I - beta_t k_hat_t k_hat_t^T), latest token leftmost, so that the forward's final
+    state is Phi S_0 + (the final state from S_0 = 0).  q is not read (any [T, Hk*Dk])."""
+    T = int(np.asarray(cu_seqlens)[-1])
+    v = np.zeros((T, Hv * Dk))
+    a = _Args(q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, None, Hk, Hv, Dk, Dk, None,
+              n_threads, 0, head_map)
+    Phi = np.zeros((a.N, Hv, Dk, Dk))
+    rc = _load().gdn_oracle_state_map(ctypes.byref(a.shape), ctypes.byref(a.inputs), _ptr(Phi))
+    if rc != 0:
+        raise ValueError("gdn_oracle_state_map rejected its arguments")
+    return Phi

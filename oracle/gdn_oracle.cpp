@@ -511,3 +511,39 @@ extern "C" int gdn_oracle_gated_rmsnorm_backward(int64_t T, int32_t H, int32_t D
     }
   return 0;
 }
+
+// ---------------------------------------------------------------------------
+// The linear part of a sequence's state map, for splitting one sequence over several
+// workers (context parallelism).  The token update of the forward recap above rewrites as
+//   S_t = g_t (I - beta_t k_hat_t k_hat_t^T) S_{t-1} + beta_t k_hat_t v_t^T,
+// so a sequence maps its start state affinely, S_T = Phi S_0 + R, with
+//   Phi = A_L ... A_2 A_1,  A_t = g_t (I - beta_t k_hat_t k_hat_t^T)   (Dk x Dk),
+// and R the final state from S_0 = 0.  Phi is formed here by applying each A_t in turn to
+// the identity; Phi[n, h] is [Dk, Dk] row-major, value head h of sequence n.
+extern "C" int gdn_oracle_state_map(const gdn_oracle_shape* shape, const gdn_oracle_inputs* inp,
+                                    double* Phi) {
+  Dims d;
+  if (check_shape(shape, inp, &d) != 0 || !Phi) return -1;
+  const gdn_oracle_inputs& in = *inp;
+  const int64_t DD = (int64_t)d.Dk * d.Dk;
+  run_units(shape->n_seqs * d.Hv, shape->n_threads, [&](int u) {
+    const int n = u / d.Hv, h = u % d.Hv;
+    const int kh = d.head_map ? h % d.Hk : h / d.r;
+    double* P = Phi + ((int64_t)n * d.Hv + h) * DD;
+    for (int64_t i = 0; i < DD; ++i) P[i] = 0.0;
+    for (int i = 0; i < d.Dk; ++i) P[(int64_t)i * d.Dk + i] = 1.0;
+    std::vector<double> kh_(d.Dk), w(d.Dk);
+    for (int64_t t = in.cu_seqlens[n]; t < in.cu_seqlens[n + 1]; ++t) {
+      l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, kh_.data());
+      const Gate G = gate_at(in, t, h);
+      // P <- g (P - beta k_hat (k_hat^T P))
+      for (int j = 0; j < d.Dk; ++j) w[j] = 0.0;
+      for (int i = 0; i < d.Dk; ++i)
+        for (int j = 0; j < d.Dk; ++j) w[j] += kh_[i] * P[(int64_t)i * d.Dk + j];
+      for (int i = 0; i < d.Dk; ++i)
+        for (int j = 0; j < d.Dk; ++j)
+          P[(int64_t)i * d.Dk + j] = G.g * (P[(int64_t)i * d.Dk + j] - G.b * kh_[i] * w[j]);
+    }
+  });
+  return 0;
+}
