@@ -421,6 +421,8 @@ def run_ours(args):
         result["decode"] = run_decode(wl, device, pk)
     if rank == 0 and world == 1 and not args.no_layer_steps:
         result["layer_steps"] = run_layer_steps(wl, device, pk)
+    if rank == 0 and world == 1 and not args.no_context_parallel:
+        result["context_parallel"] = run_context_parallel(wl, device, step_ms)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
     if rank == 0:
@@ -534,6 +536,62 @@ def run_layer_steps(wl, device, pk, K=4, eps=1e-6, steps=10, warmup=3):
     out["note"] = ("each call timed alone (the weight-gradient partial sums inside the "
                    "backward calls), L2 flushed before every launch")
     return out
+
+
+def run_context_parallel(wl, device, plain_step_ms, segments=4, steps=3, warmup=1):
+    """One sequence of the workload's length cut into `segments` equal segments, all on this
+    GPU (context parallelism run serially): the whole segmented training step (segment
+    maps, scans, final passes) and each pass alone, with CUDA events.  per_rank_ms adds up
+    the passes one rank of a `segments`-GPU group would run (exchange not included).
+    Synthetic inputs, resident."""
+    import torch
+    from gated_deltanet_backward_gb300 import context_parallel as cp
+    T, Hk, Hv, Dk, Dv = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv
+    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    g = torch.Generator(device=device).manual_seed(99)
+    rn = lambda *sh, dt=torch.float32: torch.randn(*sh, generator=g, device=device).to(dt)
+    L = T // segments
+    a_log = torch.rand(Hv, generator=g, device=device) * 2 - 1
+    dt_bias = rn(Hv) * 0.1
+    segs = [cp.Segment(rn(L, Hk * Dk, dt=td), rn(L, Hk * Dk, dt=td), rn(L, Hv * Dv, dt=td),
+                       rn(L, Hv), rn(L, Hv), a_log, dt_bias) for _ in range(segments)]
+    dOs = [rn(L, Hv * Dv, dt=td) for _ in range(segments)]
+    S0, dS_T = rn(1, Hv, Dk, Dv) * 0.1, rn(1, Hv, Dk, Dv) * 0.1
+    ops = cp.GpuSegmentOps(Hk, Hv, Dk, Dv, wl.dtype)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            out = fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n, out
+
+    def step():
+        outs, S_T, S_ins = cp.forward(ops, segs, S0)
+        return cp.backward(ops, segs, S_ins, dOs, dS_T)
+
+    step_ms, _ = timed(step, steps)
+    s0 = segs[0]
+    map_ms, Phi = timed(lambda: ops.state_map(s0), steps)
+    fz_ms, _ = timed(lambda: ops.forward(s0, None, keep=False), steps)
+    fwd_ms, _ = timed(lambda: ops.forward(s0, S0, keep=True), steps)
+    bwd_ms, _ = timed(lambda: ops.backward(s0, S0, dOs[0], dS_T), steps)
+    comp_ms, _ = timed(lambda: ops.compose(Phi, S0, S0, False), steps)
+    per_rank = map_ms + fz_ms + fwd_ms + 2 * bwd_ms + 2 * (segments - 1) * comp_ms
+    return {"segments": segments, "tokens_per_segment": L, "one_gpu_step_ms": step_ms,
+            "plain_step_ms": plain_step_ms,
+            "segment_pass_ms": {"state_map": map_ms, "forward_from_zero": fz_ms,
+                                "forward": fwd_ms, "backward": bwd_ms, "compose": comp_ms},
+            "per_rank_ms": per_rank,
+            "note": "per_rank_ms: the passes one rank of a %d-GPU group runs (state map, "
+                    "forward from zero, forward, 2 backwards, 2 scans), measured here one "
+                    "by one; the all-gathers are not included" % segments}
 
 
 def run_e2e(args, inp, layer, device, tdt, world):
@@ -668,6 +726,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-context-parallel", action="store_true",
+                    help="skip the context-parallel (segmented sequence) measurement")
     ap.add_argument("--no-layer-steps", action="store_true",
                     help="skip the conv1d + SiLU / gated RMSNorm measurement")
     args = ap.parse_args()
