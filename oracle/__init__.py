@@ -73,6 +73,8 @@ def _load():
             lib.gdn_oracle_forward_states.restype = ctypes.c_int
             lib.gdn_oracle_hardware_threads.restype = ctypes.c_int
             lib.gdn_oracle_state_map.restype = ctypes.c_int
+            lib.gdn_oracle_kda_forward.restype = ctypes.c_int
+            lib.gdn_oracle_kda_backward.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -285,3 +287,43 @@ def state_map(q, k, alpha, beta_raw, a_log, dt_bias, cu_seqlens, *, Hk, Hv, Dk, 
     if rc != 0:
         raise ValueError("gdn_oracle_state_map rejected its arguments")
     return Phi
+
+
+# ---------------------------------------------------------------------------
+# KDA variant: a decay gate per key channel.  alpha [T, Hv*Dk], b_alpha [Hv*Dk]; channel c
+# of value head h decays by exp(-exp(a_log[h]) softplus(alpha[t, h*Dk+c] + b_alpha[h*Dk+c])).
+def kda_forward(q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens, S0=None, *, Hk, Hv, Dk,
+                Dv, scale=None, n_threads=0, head_map=0):
+    """Token-by-token f64 KDA forward.  Returns (o [T, Hv*Dv], S_T [N, Hv, Dk, Dv])."""
+    a = _Args(q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens, S0, Hk, Hv, Dk, Dv, scale,
+              n_threads, 0, head_map)
+    o = np.zeros((a.T, Hv * Dv))
+    S_T = np.zeros((a.N, Hv, Dk, Dv))
+    rc = _load().gdn_oracle_kda_forward(ctypes.byref(a.shape), ctypes.byref(a.inputs), _ptr(o),
+                                        ctypes.c_int64(Hv * Dv), _ptr(S_T))
+    if rc != 0:
+        raise ValueError("gdn_oracle_kda_forward rejected its arguments")
+    return o, S_T
+
+
+def kda_backward(q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens, dO, S0=None, dS_T=None,
+                 *, Hk, Hv, Dk, Dv, scale=None, n_threads=0, head_map=0):
+    """Token-by-token f64 KDA backward (keeps every state: small shapes).  Returns dq, dk,
+    dv, dalpha [T, Hv*Dk], dbeta_raw [T, Hv], da_log [Hv], db_alpha [Hv*Dk], dS0."""
+    a = _Args(q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens, S0, Hk, Hv, Dk, Dv, scale,
+              n_threads, 0, head_map)
+    dO = _f64(dO)
+    dS_T = None if dS_T is None else np.ascontiguousarray(dS_T, dtype=np.float64)
+    out = dict(dq=np.zeros((a.T, Hk * Dk)), dk=np.zeros((a.T, Hk * Dk)),
+               dv=np.zeros((a.T, Hv * Dv)), dalpha=np.zeros((a.T, Hv * Dk)),
+               dbeta_raw=np.zeros((a.T, Hv)), da_log=np.zeros(Hv), db_alpha=np.zeros(Hv * Dk),
+               dS0=np.zeros((a.N, Hv, Dk, Dv)))
+    rc = _load().gdn_oracle_kda_backward(
+        ctypes.byref(a.shape), ctypes.byref(a.inputs), _ptr(dO), ctypes.c_int64(_ld(dO)),
+        _ptr(dS_T), _ptr(out["dq"]), ctypes.c_int64(Hk * Dk), _ptr(out["dk"]),
+        ctypes.c_int64(Hk * Dk), _ptr(out["dv"]), ctypes.c_int64(Hv * Dv), _ptr(out["dalpha"]),
+        ctypes.c_int64(Hv * Dk), _ptr(out["dbeta_raw"]), ctypes.c_int64(Hv), _ptr(out["da_log"]),
+        _ptr(out["db_alpha"]), _ptr(out["dS0"]))
+    if rc != 0:
+        raise ValueError("gdn_oracle_kda_backward rejected its arguments")
+    return out

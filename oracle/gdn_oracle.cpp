@@ -547,3 +547,216 @@ extern "C" int gdn_oracle_state_map(const gdn_oracle_shape* shape, const gdn_ora
   });
   return 0;
 }
+
+// ---------------------------------------------------------------------------
+// KDA variant: the recurrence with a decay gate per key channel instead of one per head
+// (the dormouse "KDA attention arm" page names the module's decay parameters a_log and
+// b_alpha; the recurrence itself is not printed there).  Reading: channel c of value head
+// h decays by g[c] = exp(l[c]), l[c] = -exp(a_log[h]) softplus(alpha[t, h*Dk + c] +
+// b_alpha[h*Dk + c]), and the forward recap's update becomes
+//   S_d = diag(g) S_{t-1},  kv = S_d^T k_hat,  delta = beta (v - kv),
+//   S_t = S_d + k_hat delta^T,  o_t = scale S_t^T q_hat.
+// With every channel's alpha and b_alpha equal it is the scalar-gate recurrence above.
+// In the input struct, alpha is [T, alpha_ld >= Hv*Dk] and dt_bias holds b_alpha [Hv*Dk].
+// Plain loops per (sequence, value head); the backward keeps every state of a unit
+// (small shapes only).
+namespace {
+void kda_gates(const gdn_oracle_inputs& in, const Dims& d, int64_t t, int h, double* g,
+               double* l, double* x) {
+  for (int c = 0; c < d.Dk; ++c) {
+    x[c] = in.alpha[t * in.alpha_ld + (int64_t)h * d.Dk + c] + in.dt_bias[(int64_t)h * d.Dk + c];
+    l[c] = -std::exp(in.a_log[h]) * softplus(x[c]);
+    g[c] = std::exp(l[c]);
+  }
+}
+// One KDA token step of one value head: S (Dk x Dv) updated in place; kv and delta out.
+void kda_step(const Dims& d, double* S, const double* khat, const double* v, const double* g,
+              double b, double* kv, double* delta) {
+  for (int i = 0; i < d.Dk; ++i)
+    for (int j = 0; j < d.Dv; ++j) S[(int64_t)i * d.Dv + j] *= g[i];
+  for (int j = 0; j < d.Dv; ++j) kv[j] = 0.0;
+  for (int i = 0; i < d.Dk; ++i)
+    for (int j = 0; j < d.Dv; ++j) kv[j] += S[(int64_t)i * d.Dv + j] * khat[i];
+  for (int j = 0; j < d.Dv; ++j) delta[j] = b * (v[j] - kv[j]);
+  for (int i = 0; i < d.Dk; ++i)
+    for (int j = 0; j < d.Dv; ++j) S[(int64_t)i * d.Dv + j] += khat[i] * delta[j];
+}
+}  // namespace
+
+extern "C" int gdn_oracle_kda_forward(const gdn_oracle_shape* shape, const gdn_oracle_inputs* inp,
+                                      double* o, int64_t o_ld, double* S_T) {
+  Dims d;
+  if (check_shape(shape, inp, &d) != 0 || !o) return -1;
+  const gdn_oracle_inputs& in = *inp;
+  const int64_t SZ = d.DkDv();
+  run_units(shape->n_seqs * d.Hv, shape->n_threads, [&](int u) {
+    const int n = u / d.Hv, h = u % d.Hv;
+    const int kh = d.head_map ? h % d.Hk : h / d.r;
+    std::vector<double> S(SZ, 0.0), qh(d.Dk), khat(d.Dk), kv(d.Dv), delta(d.Dv), g(d.Dk),
+        l(d.Dk), x(d.Dk);
+    if (in.S0) std::memcpy(S.data(), in.S0 + ((int64_t)n * d.Hv + h) * SZ, sizeof(double) * SZ);
+    for (int64_t t = in.cu_seqlens[n]; t < in.cu_seqlens[n + 1]; ++t) {
+      l2_normalise(in.q + t * in.q_ld + (int64_t)kh * d.Dk, d.Dk, qh.data());
+      l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, khat.data());
+      kda_gates(in, d, t, h, g.data(), l.data(), x.data());
+      const double b = sigmoid(in.beta_raw[t * in.beta_ld + h]);
+      kda_step(d, S.data(), khat.data(), in.v + t * in.v_ld + (int64_t)h * d.Dv, g.data(), b,
+               kv.data(), delta.data());
+      double* orow = o + t * o_ld + (int64_t)h * d.Dv;
+      for (int j = 0; j < d.Dv; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < d.Dk; ++i) acc += S[(int64_t)i * d.Dv + j] * qh[i];
+        orow[j] = d.scale * acc;
+      }
+    }
+    if (S_T) std::memcpy(S_T + ((int64_t)n * d.Hv + h) * SZ, S.data(), sizeof(double) * SZ);
+  });
+  return 0;
+}
+
+// Reverse mode of gdn_oracle_kda_forward: the adjoint steps of the scalar-gate backward
+// with dg per channel, dg[c] = sum_j S_prev[c][j] dS_d[c][j].  dalpha is [T, Hv*Dk];
+// ddt_bias receives d b_alpha [Hv*Dk]; both gate-parameter sums run over every token of
+// every sequence, reduced in sequence order.
+extern "C" int gdn_oracle_kda_backward(const gdn_oracle_shape* shape,
+                                       const gdn_oracle_inputs* inp, const double* dO,
+                                       int64_t dO_ld, const double* dS_T, double* dq,
+                                       int64_t dq_ld, double* dk, int64_t dk_ld, double* dv,
+                                       int64_t dv_ld, double* dalpha, int64_t dalpha_ld,
+                                       double* dbeta_raw, int64_t dbeta_ld, double* da_log,
+                                       double* db_alpha, double* dS0) {
+  Dims d;
+  if (check_shape(shape, inp, &d) != 0) return -1;
+  if (!dO || !dq || !dk || !dv || !dalpha || !dbeta_raw || !da_log || !db_alpha) return -1;
+  const gdn_oracle_inputs& in = *inp;
+  const int N = shape->n_seqs;
+  const int64_t SZ = d.DkDv();
+  std::vector<double> pa((size_t)std::max(N, 1) * d.Hv, 0.0);
+  std::vector<double> pb((size_t)std::max(N, 1) * d.Hv * d.Dk, 0.0);
+  run_units(N * d.Hk, shape->n_threads, [&](int u) {
+    const int n = u / d.Hk, kh = u % d.Hk;
+    const int64_t t0 = in.cu_seqlens[n], t1 = in.cu_seqlens[n + 1], L = t1 - t0;
+    // states before every token, per value head of the group: [L + 1][r][SZ]
+    std::vector<double> Sh((size_t)(L + 1) * d.r * SZ, 0.0);
+    if (in.S0)
+      for (int hh = 0; hh < d.r; ++hh)
+        std::memcpy(&Sh[hh * SZ], in.S0 + ((int64_t)n * d.Hv + d.vh(kh, hh)) * SZ,
+                    sizeof(double) * SZ);
+    std::vector<double> qh(d.Dk), khat(d.Dk), kv(d.Dv), delta(d.Dv), g(d.Dk), l(d.Dk), x(d.Dk);
+    for (int64_t t = t0; t < t1; ++t) {
+      l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, khat.data());
+      double* nxt = &Sh[(size_t)(t - t0 + 1) * d.r * SZ];
+      std::memcpy(nxt, &Sh[(size_t)(t - t0) * d.r * SZ], sizeof(double) * d.r * SZ);
+      for (int hh = 0; hh < d.r; ++hh) {
+        const int h = d.vh(kh, hh);
+        kda_gates(in, d, t, h, g.data(), l.data(), x.data());
+        kda_step(d, nxt + hh * SZ, khat.data(), in.v + t * in.v_ld + (int64_t)h * d.Dv, g.data(),
+                 sigmoid(in.beta_raw[t * in.beta_ld + h]), kv.data(), delta.data());
+      }
+    }
+    std::vector<double> dS((size_t)d.r * SZ, 0.0);
+    if (dS_T)
+      for (int hh = 0; hh < d.r; ++hh)
+        std::memcpy(&dS[hh * SZ], dS_T + ((int64_t)n * d.Hv + d.vh(kh, hh)) * SZ,
+                    sizeof(double) * SZ);
+    std::vector<double> Sd(SZ), S_t(SZ), dqh(d.Dk), dkh(d.Dk), ddelta(d.Dv), dkv(d.Dv), dg(d.Dk);
+    std::vector<double> dq_acc(d.Dk), dk_acc(d.Dk);
+    for (int64_t t = t1 - 1; t >= t0; --t) {
+      const double nq = l2_normalise(in.q + t * in.q_ld + (int64_t)kh * d.Dk, d.Dk, qh.data());
+      const double nk = l2_normalise(in.k + t * in.k_ld + (int64_t)kh * d.Dk, d.Dk, khat.data());
+      std::fill(dq_acc.begin(), dq_acc.end(), 0.0);
+      std::fill(dk_acc.begin(), dk_acc.end(), 0.0);
+      for (int hh = 0; hh < d.r; ++hh) {
+        const int h = d.vh(kh, hh);
+        const double* S_prev = &Sh[(size_t)(t - t0) * d.r * SZ + hh * SZ];
+        const double* vrow = in.v + t * in.v_ld + (int64_t)h * d.Dv;
+        const double* dOrow = dO + t * dO_ld + (int64_t)h * d.Dv;
+        double* dSh = &dS[hh * SZ];
+        kda_gates(in, d, t, h, g.data(), l.data(), x.data());
+        const double b = sigmoid(in.beta_raw[t * in.beta_ld + h]);
+        // recompute S_d, kv, delta, S_t
+        for (int i = 0; i < d.Dk; ++i)
+          for (int j = 0; j < d.Dv; ++j) Sd[(int64_t)i * d.Dv + j] = g[i] * S_prev[(int64_t)i * d.Dv + j];
+        std::memcpy(S_t.data(), S_prev, sizeof(double) * SZ);
+        kda_step(d, S_t.data(), khat.data(), vrow, g.data(), b, kv.data(), delta.data());
+        // o = scale S_t^T q_hat
+        for (int i = 0; i < d.Dk; ++i) {
+          double acc = 0.0;
+          for (int j = 0; j < d.Dv; ++j) {
+            dSh[(int64_t)i * d.Dv + j] += d.scale * qh[i] * dOrow[j];
+            acc += S_t[(int64_t)i * d.Dv + j] * dOrow[j];
+          }
+          dqh[i] = d.scale * acc;
+        }
+        // S_t = S_d + k_hat delta^T  (dS_d = dS)
+        std::fill(dkh.begin(), dkh.end(), 0.0);
+        std::fill(ddelta.begin(), ddelta.end(), 0.0);
+        for (int i = 0; i < d.Dk; ++i)
+          for (int j = 0; j < d.Dv; ++j) {
+            const double ds = dSh[(int64_t)i * d.Dv + j];
+            dkh[i] += ds * delta[j];
+            ddelta[j] += ds * khat[i];
+          }
+        // delta = beta (v - kv)
+        double db = 0.0;
+        for (int j = 0; j < d.Dv; ++j) {
+          dv[t * dv_ld + (int64_t)h * d.Dv + j] = b * ddelta[j];
+          dkv[j] = -b * ddelta[j];
+          db += (vrow[j] - kv[j]) * ddelta[j];
+        }
+        // kv = S_d^T k_hat
+        for (int i = 0; i < d.Dk; ++i)
+          for (int j = 0; j < d.Dv; ++j) {
+            dSh[(int64_t)i * d.Dv + j] += khat[i] * dkv[j];
+            dkh[i] += Sd[(int64_t)i * d.Dv + j] * dkv[j];
+          }
+        // S_d = diag(g) S_prev
+        for (int i = 0; i < d.Dk; ++i) {
+          double acc = 0.0;
+          for (int j = 0; j < d.Dv; ++j) {
+            acc += S_prev[(int64_t)i * d.Dv + j] * dSh[(int64_t)i * d.Dv + j];
+            dSh[(int64_t)i * d.Dv + j] *= g[i];
+          }
+          dg[i] = acc;
+        }
+        // g = exp(l), l = -exp(a_log) softplus(x)
+        for (int c = 0; c < d.Dk; ++c) {
+          const double dl = dg[c] * g[c];
+          const double dx = dl * (-std::exp(in.a_log[h])) * sigmoid(x[c]);
+          dalpha[t * dalpha_ld + (int64_t)h * d.Dk + c] = dx;
+          pb[((size_t)n * d.Hv + h) * d.Dk + c] += dx;
+          pa[(size_t)n * d.Hv + h] += dl * l[c];
+        }
+        dbeta_raw[t * dbeta_ld + h] = db * b * (1.0 - b);
+        double dot_q = 0.0, dot_k = 0.0;
+        for (int i = 0; i < d.Dk; ++i) {
+          dot_q += dqh[i] * qh[i];
+          dot_k += dkh[i] * khat[i];
+        }
+        for (int i = 0; i < d.Dk; ++i) {
+          dq_acc[i] += (dqh[i] - qh[i] * dot_q) / nq;
+          dk_acc[i] += (dkh[i] - khat[i] * dot_k) / nk;
+        }
+      }
+      for (int i = 0; i < d.Dk; ++i) {
+        dq[t * dq_ld + (int64_t)kh * d.Dk + i] = dq_acc[i];
+        dk[t * dk_ld + (int64_t)kh * d.Dk + i] = dk_acc[i];
+      }
+    }
+    if (dS0)
+      for (int hh = 0; hh < d.r; ++hh)
+        std::memcpy(dS0 + ((int64_t)n * d.Hv + d.vh(kh, hh)) * SZ, &dS[hh * SZ],
+                    sizeof(double) * SZ);
+  });
+  for (int h = 0; h < d.Hv; ++h) {
+    double a = 0.0;
+    for (int n = 0; n < N; ++n) a += pa[(size_t)n * d.Hv + h];
+    da_log[h] = a;
+    for (int c = 0; c < d.Dk; ++c) {
+      double s = 0.0;
+      for (int n = 0; n < N; ++n) s += pb[((size_t)n * d.Hv + h) * d.Dk + c];
+      db_alpha[(int64_t)h * d.Dk + c] = s;
+    }
+  }
+  return 0;
+}
