@@ -421,6 +421,8 @@ def run_ours(args):
         result["decode"] = run_decode(wl, device, pk)
     if rank == 0 and world == 1 and not args.no_layer_steps:
         result["layer_steps"] = run_layer_steps(wl, device, pk)
+    if rank == 0 and world == 1 and not args.no_decode:
+        result["kda"] = run_kda(wl, device, pk)
     if rank == 0 and world == 1 and not args.no_context_parallel:
         result["context_parallel"] = run_context_parallel(wl, device, step_ms)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -535,6 +537,56 @@ def run_layer_steps(wl, device, pk, K=4, eps=1e-6, steps=10, warmup=3):
                     "dtype": wl.dtype}
     out["note"] = ("each call timed alone (the weight-gradient partial sums inside the "
                    "backward calls), L2 flushed before every launch")
+    return out
+
+
+def run_kda(wl, device, pk, n_seqs=64, prefill_tokens=1024, steps=20, warmup=3):
+    """The KDA variant (a decay gate per key channel) with the workload's head shape:
+    gdn_kda_forward as a decode step on n_seqs one-token sequences (state in place; bytes
+    as for the decode step plus the per-channel gate rows) against HBM, and as a prefill
+    of one prefill_tokens-token sequence in token form (tokens/s).  Synthetic inputs."""
+    import torch
+    import gated_deltanet_backward_gb300 as gdn
+    Hk, Hv, Dk, Dv = wl.Hk, wl.Hv, wl.Dk, wl.Dv
+    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    es = 2 if wl.dtype == "bf16" else 4
+    g = torch.Generator(device=device).manual_seed(77)
+    rn = lambda *sh, dt=torch.float32: torch.randn(*sh, generator=g, device=device).to(dt)
+    a_log = torch.rand(Hv, generator=g, device=device) * 2 - 1
+    b_alpha = rn(Hv * Dk) * 0.1
+    out = {}
+    for name, N, T in (("decode", n_seqs, n_seqs), ("prefill", 1, prefill_tokens)):
+        q, k, v = rn(T, Hk * Dk, dt=td), rn(T, Hk * Dk, dt=td), rn(T, Hv * Dv, dt=td)
+        alpha, beta = rn(T, Hv * Dk), rn(T, Hv)
+        o = torch.empty(T, Hv * Dv, device=device, dtype=td)
+        S = rn(N, Hv, Dk, Dv) * 0.1
+        cu = (torch.arange(N + 1, device=device, dtype=torch.int32) if name == "decode"
+              else torch.tensor([0, T], device=device, dtype=torch.int32))
+        shape = gdn.make_shape(Hk, Hv, Dk, Dv, N, 0, T, wl.dtype, 0.0)
+        step = lambda: gdn.gdn_kda_forward(shape, q, k, v, alpha, beta, a_log, b_alpha, cu, S, S,
+                                           o)
+        n_steps = steps if name == "decode" else 2
+        for _ in range(warmup if name == "decode" else 1):
+            step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / n_steps
+        entry = {"sequences": N, "tokens": T, "us_per_call": us,
+                 "tokens_per_s": T / (us * 1e-6)}
+        if name == "decode":
+            nbytes = (2 * N * Hv * Dk * Dv * 4 + N * (2 * Hk * Dk + 2 * Hv * Dv) * es
+                      + N * Hv * (Dk + 1) * 4)
+            gbs = nbytes / (us * 1e-6) / 1e9
+            entry.update({"bytes_per_call": nbytes, "achieved_gbs": gbs,
+                          "frac": gbs / pk["hbm_gbs"], "bound": "hbm"})
+        else:
+            entry["note"] = "token form: one token after another per (value head, column slice)"
+        out[name] = entry
     return out
 
 

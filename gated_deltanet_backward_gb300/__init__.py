@@ -101,6 +101,8 @@ _lib.gdn_gated_rmsnorm_backward.restype = ctypes.c_int
 _lib.gdn_state_compose.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp,
                                    _vp, ctypes.c_int32, _vp]
 _lib.gdn_state_compose.restype = ctypes.c_int
+_lib.gdn_kda_forward.argtypes = [_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64, _vp]
+_lib.gdn_kda_forward.restype = ctypes.c_int
 _lib.gdn_read_device_status.argtypes = [_vp, _vp]
 _lib.gdn_read_device_status.restype = ctypes.c_int
 _lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -120,7 +122,7 @@ EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_for
             "gdn_decode_step", "gdn_conv1d_silu_forward", "gdn_conv1d_silu_workspace_bytes",
             "gdn_conv1d_silu_backward", "gdn_gated_rmsnorm_forward",
             "gdn_gated_rmsnorm_workspace_bytes", "gdn_gated_rmsnorm_backward",
-            "gdn_state_compose")
+            "gdn_state_compose", "gdn_kda_forward")
 
 
 class GdnError(RuntimeError):
@@ -343,6 +345,19 @@ def gdn_state_compose(Phi, S, R, out, transpose=False, stream=None) -> None:
             raise ValueError("gdn_state_compose needs contiguous tensors")
     _check(_lib.gdn_state_compose(n, Dk, Dv, _ptr(Phi), _ptr(S), _ptr(R), _ptr(out),
                                   1 if transpose else 0, _stream(stream)), "gdn_state_compose")
+
+
+def gdn_kda_forward(shape, q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens, S_in, S_out, o,
+                    stream=None) -> None:
+    """Calls gdn_kda_forward: the per-channel-gate variant in token form (alpha
+    [T, Hv*Dk], b_alpha [Hv*Dk]); S_in None = zero, S_out may be S_in."""
+    args = [ctypes.byref(shape)]
+    for t in (q, k, v, alpha, beta_raw):
+        args += list(_mat(t))
+    args += [_ptr(a_log), _ptr(b_alpha), _ptr(cu_seqlens), _ptr(S_in), _ptr(S_out)]
+    args += list(_mat(o))
+    args += [_stream(stream)]
+    _check(_lib.gdn_kda_forward(*args), "gdn_kda_forward")
 
 
 def gdn_read_device_status(workspace, stream=None) -> int:

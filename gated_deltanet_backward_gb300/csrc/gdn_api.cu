@@ -358,6 +358,7 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_NORM_BWD: return "gdn_gated_rmsnorm_bwd";
     case gdn::KID_SUM_PARTS: return "gdn_sum_partials";
     case gdn::KID_COMPOSE: return "gdn_state_compose";
+    case gdn::KID_KDA_FWD: return "gdn_kda_fwd";
     default: return "?";
   }
 }
@@ -711,6 +712,41 @@ int gdn_state_compose(int32_t n, int32_t Dk, int32_t Dv, const float* Phi, const
   const cudaError_t e = gdn::launch_state_compose(n, Dk, Dv, Phi, S, R, out, transpose != 0,
                                                   (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail("gdn_state_compose: kernel launch", e);
+  return GDN_OK;
+}
+
+int gdn_kda_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                    int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                    int64_t alpha_ld, const float* beta_raw, int64_t beta_ld, const float* a_log,
+                    const float* b_alpha, const int32_t* cu_seqlens, const float* S_in,
+                    float* S_out, void* o, int64_t o_ld, void* stream) {
+  if (!s) return GDN_ERR_INVALID_ARG;
+  gdn_shape sh = *s;
+  // chunks are not used (no saved states); a count consistent with total_tokens
+  sh.total_chunks = (int32_t)((s->total_tokens + gdn::kChunk - 1) / gdn::kChunk);
+  GDN_TRY(check_shape(&sh));
+  const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
+  const int64_t T = s->total_tokens;
+  if (T > ((int64_t)1 << 31) - 1) return GDN_ERR_UNSUPPORTED;
+  GDN_TRY(check_matrix(q, q_ld, (int64_t)s->Hk * s->Dk, es, T));
+  GDN_TRY(check_matrix(k, k_ld, (int64_t)s->Hk * s->Dk, es, T));
+  GDN_TRY(check_matrix(v, v_ld, (int64_t)s->Hv * s->Dv, es, T));
+  GDN_TRY(check_matrix(o, o_ld, (int64_t)s->Hv * s->Dv, es, T));
+  GDN_TRY(check_gate_matrix(alpha, alpha_ld, (int64_t)s->Hv * s->Dk, T));
+  GDN_TRY(check_gate_matrix(beta_raw, beta_ld, s->Hv, T));
+  GDN_TRY(check_vec(a_log, true));
+  GDN_TRY(check_vec(b_alpha, true));
+  GDN_TRY(check_vec(S_in, false));
+  GDN_TRY(check_vec(S_out, s->n_seqs > 0));
+  if (s->n_seqs > 0 && (!cu_seqlens || ((uintptr_t)cu_seqlens & 3u) != 0))
+    return cu_seqlens ? GDN_ERR_MISALIGNED : GDN_ERR_INVALID_ARG;
+  if (s->n_seqs == 0) return GDN_OK;
+  (void)cudaGetLastError();
+  g_last_error[0] = 0;
+  const cudaError_t e = gdn::launch_kda_forward(&sh, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld,
+                                                beta_raw, beta_ld, a_log, b_alpha, cu_seqlens,
+                                                S_in, S_out, o, o_ld, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("gdn_kda_forward: kernel launch", e);
   return GDN_OK;
 }
 

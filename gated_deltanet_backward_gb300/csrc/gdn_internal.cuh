@@ -235,7 +235,8 @@ enum KernelId {
   KID_NORM_BWD = 17,
   KID_SUM_PARTS = 18,
   KID_COMPOSE = 19,
-  KID_COUNT = 20
+  KID_KDA_FWD = 20,
+  KID_COUNT = 21
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
@@ -283,6 +284,13 @@ cudaError_t launch_gated_rmsnorm(bool bwd, int dtype, int64_t T, int H, int D, f
 // out = op(Phi) S + R for n blocks (gdn_context.cu); R may be null (zero).
 cudaError_t launch_state_compose(int n, int Dk, int Dv, const float* Phi, const float* S,
                                  const float* R, float* out, bool transpose, cudaStream_t st);
+// The KDA variant's token-form forward (gdn_kda.cu).
+cudaError_t launch_kda_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                               int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                               int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                               const float* a_log, const float* b_alpha, const int32_t* cu,
+                               const float* S_in, float* S_out, void* o, int64_t o_ld,
+                               cudaStream_t st);
 cudaError_t launch_decode(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
                           int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
                           int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,

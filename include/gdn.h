@@ -350,6 +350,34 @@ int gdn_gated_rmsnorm_backward(int32_t dtype, int64_t total_tokens, int32_t n_he
 int gdn_state_compose(int32_t n, int32_t Dk, int32_t Dv, const float* Phi, const float* S,
                       const float* R, float* out, int32_t transpose, void* stream);
 
+/* ---- KDA variant: a decay gate per key channel ------------------------------------------
+ * The recurrence with the scalar gate g of a value head replaced by one gate per key
+ * channel (the KDA module's decay, whose parameters a_log and b_alpha the dormouse "KDA
+ * attention arm" page names):
+ *   g[c] = exp(-exp(a_log[h]) * softplus(alpha[t, h*Dk + c] + b_alpha[h*Dk + c]))
+ *   S_d = diag(g) S_{t-1};  kv = S_d^T k_hat;  delta = beta (v - kv)
+ *   S_t = S_d + k_hat delta^T;  o_t = scale S_t^T q_hat
+ * (q_hat, k_hat, beta and the key-head map as for gdn_forward).  Equal gates on every
+ * channel give gdn_forward's recurrence.  This is its forward in token form, one token
+ * after another per (sequence, value head): a decode step is a batch of one-token
+ * sequences.
+ * shape: as for gdn_forward (total_chunks and saved states are not used).
+ *   q, k, v, o    device, as for gdn_forward (o written)
+ *   alpha         device, fp32 [total_tokens, alpha_ld >= Hv*Dk]: channel c of value head
+ *                 h at column h*Dk + c
+ *   beta_raw      device, fp32 [total_tokens, beta_ld >= Hv]
+ *   a_log         device, fp32 [Hv];  b_alpha  device, fp32 [Hv*Dk]
+ *   cu_seqlens    device, int32 [n_seqs + 1] (token ranges are clamped to [0,
+ *                 total_tokens))
+ *   S_in          device, fp32 [n_seqs, Hv, Dk, Dv] or NULL (zero)
+ *   S_out         device, fp32 [n_seqs, Hv, Dk, Dv] (written; may be S_in)
+ * Needs no workspace.  Returns as gdn_decode_step does. */
+int gdn_kda_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
+                    int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                    int64_t alpha_ld, const float* beta_raw, int64_t beta_ld, const float* a_log,
+                    const float* b_alpha, const int32_t* cu_seqlens, const float* S_in,
+                    float* S_out, void* o, int64_t o_ld, void* stream);
+
 /* Synchronises `stream` and returns the device-side status recorded in
  * `workspace` by the last gdn_forward / gdn_backward that used it (GDN_OK, or
  * the first device error), or GDN_ERR_CUDA if the stream itself failed. */

@@ -220,3 +220,15 @@ def generate_layer_steps(wl: Workload, K: int = 4, w_range: float = 0.05,
     gamma = rng.uniform(0.9, 1.1, size=(wl.Dv,)).astype(np.float32)
     dy_norm = rnd(_normal(rng, (T, W)))
     return LayerStepInputs(cu, x, w, dy_conv, o, z, gamma, dy_norm)
+
+
+def generate_kda_gates(wl: Workload, T: Optional[int] = None):
+    """Per-channel decay-gate inputs of the KDA variant for ``wl``'s head shape: alpha
+    [T, Hv*Dk] ~ N(0, 1) and b_alpha [Hv*Dk] ~ N(0, dt_bias_std) (zero when that is 0),
+    fp32.  Seeded with seed + 104729; draw order alpha, b_alpha."""
+    rng = np.random.Generator(np.random.PCG64(wl.seed + 104729))
+    T = wl.total_tokens if T is None else T
+    alpha = _normal(rng, (T, wl.Hv * wl.Dk))
+    b_alpha = (_normal(rng, (wl.Hv * wl.Dk,), wl.dt_bias_std) if wl.dt_bias_std
+               else np.zeros(wl.Hv * wl.Dk, np.float32))
+    return alpha, b_alpha
