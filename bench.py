@@ -647,8 +647,14 @@ def run_context_parallel(wl, device, plain_step_ms, segments=4, steps=3, warmup=
 
 
 def run_e2e(args, inp, layer, device, tdt, world):
-    """Same metric through the public API with host buffers: every step copies its inputs
-    from pinned host memory to the device and reads the results back."""
+    """Same metric through the public API with host buffers: every step copies all its
+    inputs from pinned host memory to the device and reads all its results (o, S_T and
+    every gradient) back into pinned host memory.  The steps are pipelined over three
+    streams, as a training loop feeding a GPU from the host would run them: step i's
+    uploads (one copy stream) overlap step i-1's compute, its downloads (another copy
+    stream) overlap step i+1's compute; device inputs and outputs are double-buffered and
+    ordered by events.  value = K steps' tokens / the time from the first upload to the
+    last download; serial_ms_per_step is the same steps on one stream, nothing overlapped."""
     import torch
     wl = inp.wl
     T, Hk, Hv, Dk, Dv, N = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv, wl.n_seqs
@@ -659,54 +665,102 @@ def run_e2e(args, inp, layer, device, tdt, world):
     h_in = dict(qkv=pin(inp.qkv, tdt), alpha=pin(inp.alpha), beta_raw=pin(inp.beta_raw),
                 a_log=pin(inp.a_log), dt_bias=pin(inp.dt_bias), dO=pin(inp.dO, tdt),
                 S0=pin(inp.S0), dS_T=pin(inp.dS_T))
-    d_in = {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, device=device))
-            for k, v in h_in.items()}
     outs = dict(o=(T, Hv * Dv, tdt), dq=(T, Hk * Dk, tdt), dk=(T, Hk * Dk, tdt),
                 dv=(T, Hv * Dv, tdt), dalpha=(T, Hv, torch.float32),
                 dbeta=(T, Hv, torch.float32), da_log=(Hv, None, torch.float32),
                 ddt=(Hv, None, torch.float32), S_T=(N, Hv * Dk * Dv, torch.float32),
                 dS0=(N, Hv * Dk * Dv, torch.float32))
-    d_out = {k: torch.empty(s[:2] if s[1] else (s[0],), dtype=s[2], device=device)
-             for k, s in outs.items()}
-    h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in d_out.items()}
-    stream = torch.cuda.current_stream(device)
-    bytes_in = sum(v.numel() * v.element_size() for v in h_in.values() if v is not None)
-    bytes_out = sum(v.numel() * v.element_size() for v in h_out.values())
 
-    def step():
+    def dev_in():
+        return {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, device=device))
+                for k, v in h_in.items()}
+
+    def dev_out():
+        return {k: torch.empty(s[:2] if s[1] else (s[0],), dtype=s[2], device=device)
+                for k, s in outs.items()}
+
+    d_in, d_out = [dev_in(), dev_in()], [dev_out(), dev_out()]
+    h_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in d_out[0].items()}
+             for _ in range(2)]
+    bytes_in = sum(v.numel() * v.element_size() for v in h_in.values() if v is not None)
+    bytes_out = sum(v.numel() * v.element_size() for v in h_out[0].values())
+
+    def compute(di, do, st):
+        qkv = di["qkv"]
+        q, k, v = qkv[:, :Hk * Dk], qkv[:, Hk * Dk:2 * Hk * Dk], qkv[:, 2 * Hk * Dk:]
+        layer.forward(q, k, v, di["alpha"], di["beta_raw"], di["a_log"], di["dt_bias"], di["S0"],
+                      do["o"], do["S_T"].view(N, Hv, Dk, Dv), st, train=True)
+        layer.backward(q, k, v, di["alpha"], di["beta_raw"], di["a_log"], di["dt_bias"],
+                       di["S0"], di["dO"], di["dS_T"], do["dq"], do["dk"], do["dv"], do["dalpha"],
+                       do["dbeta"], do["da_log"], do["ddt"], do["dS0"].view(N, Hv, Dk, Dv), st,
+                       train=True)
+
+    def upload(di):
         for key, h in h_in.items():
             if h is not None:
-                d_in[key].copy_(h, non_blocking=True)
-        qkv = d_in["qkv"]
-        q, k, v = qkv[:, :Hk * Dk], qkv[:, Hk * Dk:2 * Hk * Dk], qkv[:, 2 * Hk * Dk:]
-        S0 = None if d_in["S0"] is None else d_in["S0"]
-        dS_T = None if d_in["dS_T"] is None else d_in["dS_T"]
-        layer.forward(q, k, v, d_in["alpha"], d_in["beta_raw"], d_in["a_log"], d_in["dt_bias"],
-                      S0, d_out["o"], d_out["S_T"].view(N, Hv, Dk, Dv), stream, train=True)
-        layer.backward(q, k, v, d_in["alpha"], d_in["beta_raw"], d_in["a_log"],
-                       d_in["dt_bias"], S0, d_in["dO"], dS_T, d_out["dq"], d_out["dk"],
-                       d_out["dv"], d_out["dalpha"], d_out["dbeta"], d_out["da_log"],
-                       d_out["ddt"], d_out["dS0"].view(N, Hv, Dk, Dv), stream, train=True)
-        for key, h in h_out.items():
-            h.copy_(d_out[key], non_blocking=True)
+                di[key].copy_(h, non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
-        step()
-    torch.cuda.synchronize()
+    def download(do, ho):
+        for key, h in ho.items():
+            h.copy_(do[key], non_blocking=True)
+
+    s_up, s_cmp, s_down = (torch.cuda.Stream(device) for _ in range(3))
+
+    def pipelined(K):
+        ev_up = [torch.cuda.Event() for _ in range(K)]
+        ev_cmp = [torch.cuda.Event() for _ in range(K)]
+        ev_down = [torch.cuda.Event() for _ in range(K)]
+        for i in range(K):
+            b = i % 2
+            if i >= 2:
+                s_up.wait_event(ev_cmp[i - 2])    # step i-2's compute has read d_in[b]
+            with torch.cuda.stream(s_up):
+                upload(d_in[b])
+            ev_up[i].record(s_up)
+            s_cmp.wait_event(ev_up[i])
+            if i >= 2:
+                s_cmp.wait_event(ev_down[i - 2])  # step i-2's downloads have read d_out[b]
+            compute(d_in[b], d_out[b], s_cmp)
+            ev_cmp[i].record(s_cmp)
+            s_down.wait_event(ev_cmp[i])
+            with torch.cuda.stream(s_down):
+                download(d_out[b], h_out[b])
+            ev_down[i].record(s_down)
+
+    def serial(K):
+        st = torch.cuda.current_stream(device)
+        for _ in range(K):
+            upload(d_in[0])
+            compute(d_in[0], d_out[0], st)
+            download(d_out[0], h_out[0])
+
     K = args.steps
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / K
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    res = {}
+    for name, fn, first in (("serial", serial, None), ("pipelined", pipelined, s_up)):
+        fn(max(2, args.warmup))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(first or torch.cuda.current_stream(device))
+        fn(K)
+        e1.record(s_down if first else torch.cuda.current_stream(device))
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / K
+        if world > 1:
+            t = torch.tensor([ms], device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        res[name] = ms
+    assert gdn_status_ok(layer)
+    ms = res["pipelined"]
     return {"value": world * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": int(bytes_in), "d2h_bytes_per_step": int(bytes_out)}
+            "serial_ms_per_step": res["serial"], "h2d_bytes_per_step": int(bytes_in),
+            "d2h_bytes_per_step": int(bytes_out),
+            "pipeline": "3 streams (upload, compute, download), double-buffered device I/O"}
+
+
+def gdn_status_ok(layer):
+    import gated_deltanet_backward_gb300 as gdn
+    return gdn.gdn_read_device_status(layer.ws_bwd) == 0
 
 
 def _oracle_step(inp, tokens):
