@@ -522,21 +522,27 @@ def run_layer_steps(wl, device, pk, K=4, eps=1e-6, steps=10, warmup=3):
             fn()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
+        prof = gdn.gdn_profile(max_launches=4 * steps)
         torch.cuda.synchronize()
-        for e0, e1 in ev:
-            flush()
-            e0.record(stream)
-            fn()
-            e1.record(stream)
+        with prof:
+            for e0, e1 in ev:
+                flush()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
         torch.cuda.synchronize()
-        us = 1e3 * sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+        call_us = 1e3 * sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+        # the library's events around each of its launches (the kernels alone)
+        us = 1e3 * sum(ms for _, ms in prof.launches()) / steps
         gbs = nbytes / (us * 1e-6) / 1e9
-        out[name] = {"us": us, "bytes": nbytes, "achieved_gbs": gbs,
-                     "frac": gbs / pk["hbm_gbs"], "bound": "hbm"}
+        out[name] = {"us": us, "call_us": call_us, "bytes": nbytes, "achieved_gbs": gbs,
+                     "frac": gbs / pk["hbm_gbs"], "bound": "hbm",
+                     "kernels": sorted({k for k, _ in prof.launches()})}
     out["shape"] = {"tokens": T, "channels": C, "kernel_size": K, "heads": Hv, "head_dim": Dv,
                     "dtype": wl.dtype}
-    out["note"] = ("each call timed alone (the weight-gradient partial sums inside the "
-                   "backward calls), L2 flushed before every launch")
+    out["note"] = ("each call timed alone after an L2 flush: us = the library's CUDA events "
+                   "around its launches (the weight-gradient partial sums of the backward "
+                   "calls included), call_us = events around the whole Python call")
     return out
 
 

@@ -123,18 +123,43 @@ __device__ __forceinline__ void mask_window(float (&win)[K][V], int dist) {
   }
 }
 
+// A thread's channel vector: 4 channels (8 bytes of bf16, 16 of fp32), read from a staged
+// row in shared memory and written to global memory.
+__device__ __forceinline__ void ld4(const char* p, float* f, float) {
+  const float4 a = *(const float4*)p;
+  f[0] = a.x;
+  f[1] = a.y;
+  f[2] = a.z;
+  f[3] = a.w;
+}
+__device__ __forceinline__ void ld4(const char* p, float* f, __nv_bfloat16) {
+  const uint2 u = *(const uint2*)p;
+  unpack_bf2(u.x, f);
+  unpack_bf2(u.y, f + 2);
+}
+template <typename T>
+__device__ __forceinline__ void ld4(const char* p, float* f) {
+  ld4(p, f, T());
+}
+__device__ __forceinline__ void st4(float* p, const float* f) {
+  *(float4*)p = make_float4(f[0], f[1], f[2], f[3]);
+}
+__device__ __forceinline__ void st4(__nv_bfloat16* p, const float* f) {
+  *(uint2*)p = make_uint2(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]));
+}
+
 // y[t, c] = SiLU(sum_j w[c, j] x[t - (K-1) + j, c]), inputs before the start of t's
-// sequence read as zero.  The channels are cut into slabs of kSlabVec 16-byte vectors,
-// the tokens into tiles of kConvTR; tile i is token tile i % n_tt of slab i / n_tt, and
-// block b walks tiles b q .. b q + q - 1 (consecutive token tiles of a slab, so the K-1
-// rows before a tile are the L2-resident end of the previous one).  A tile's rows (with
-// the K-1 before it) land in a ring of kConvNS shared-memory stages through cp.async,
-// issued kConvNS-1 tiles ahead.  Thread (v, g) then computes vector v of the tile's rows
-// g*RPT .. g*RPT+RPT-1, sliding a K-row window down them.
-constexpr int kConvThreads = 256;
-constexpr int kConvTR = 32;   // tokens of a tile
-constexpr int kConvNS = 3;    // pipeline stages
-constexpr int kSlabVec = 64;  // 16-byte vectors of a slab row (1 KB)
+// sequence read as zero.  The channels are cut into slabs of 1 KB rows, the tokens into
+// tiles of kConvTR; tile i is token tile i % n_tt of slab i / n_tt, and block b walks
+// tiles b q .. b q + q - 1 (consecutive token tiles of a slab, so the K-1 rows before a
+// tile are the L2-resident end of the previous one).  A tile's rows (with the K-1 before
+// it) land in a ring of kConvNS shared-memory stages through 16-byte cp.async copies,
+// issued kConvNS-1 tiles ahead.  Thread (v, g) then computes the 4 channels v of the
+// tile's rows g*RPT .. g*RPT+RPT-1, sliding a K-row window down them.
+constexpr int kConvTR = 32;    // tokens of a forward tile
+constexpr int kConvNS = 3;     // forward pipeline stages
+constexpr int kConvRB = 1024;  // bytes of a forward slab row
+constexpr int kConvFThreads = 512;
 
 struct ConvArgs {
   int T, C, K, n_seqs, n_slabs, q;  // q: tiles of a block (a contiguous run, slab-major)
@@ -149,40 +174,49 @@ struct ConvArgs {
   float* dw_part;  // backward: [gridDim.x, 2, slab channels, K] partial dw, or null
 };
 
-// Stages rows r0 .. r0 + ROWS - 1 (those inside [0, T)), vectors 0 .. nvec-1 of each, as
-// dst[row][vector].  Thread i copies vector i % NV of rows i / NV, + 256 / NV, ...: one
-// cp.async and a pointer step per 16 bytes.
-template <int ROWS, int NV>
-__device__ __forceinline__ void stage_rows(uint4* dst, const char* base, int64_t ld_bytes, int r0,
-                                           int T, int nvec) {
-  constexpr int RS = kConvThreads / NV;  // rows between a thread's copies
+// Stages rows r0 .. r0 + ROWS - 1 (those inside [0, T)) of a slab, row bytes RB, the
+// first nbytes of each (a multiple of 16), as dst[row][RB]: thread i copies the 16-byte
+// vector i % (RB/16) of rows i / (RB/16), + THREADS / (RB/16), ...
+template <int ROWS, int RB, int THREADS>
+__device__ __forceinline__ void stage_rows(char* dst, const char* base, int64_t ld_bytes, int r0,
+                                           int T, int nbytes) {
+  constexpr int NV = RB / 16, RS = THREADS / NV;
   const int v = threadIdx.x % NV, row0 = threadIdx.x / NV;
-  if (v >= nvec) return;
+  if (v * 16 >= nbytes) return;
   int src = r0 + row0;
   const char* p = base + (int64_t)src * ld_bytes + v * 16;
-  uint4* d = dst + row0 * NV + v;
+  char* d = dst + row0 * RB + v * 16;
   const int64_t step = RS * ld_bytes;
 #pragma unroll 4
-  for (int row = row0; row < ROWS; row += RS, src += RS, p += step, d += RS * NV)
+  for (int row = row0; row < ROWS; row += RS, src += RS, p += step, d += RS * RB)
     if ((unsigned)src < (unsigned)T) tc::cp_async16(d, p);
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, 2) k_conv_fwd(ConvArgs a) {
-  constexpr int V = kVec<T>, NV = kSlabVec, SW = NV * V, RG = kConvThreads / NV;
-  constexpr int RPT = kConvTR / RG;
-  constexpr int ROWS = kConvTR + K - 1;  // staged rows: the tile and the K-1 before it
-  extern __shared__ uint4 cstage[];      // [kConvNS][ROWS][NV]
+struct ConvFwdGeom {
+  static constexpr int V = 4, SW = kConvRB / (int)sizeof(T);  // slab channels
+  static constexpr int NTV = SW / V, RG = kConvFThreads / NTV, RPT = kConvTR / RG;
+  static constexpr int ROWS = kConvTR + K - 1;  // the tile and the K-1 rows before it
+  static constexpr size_t smem = (size_t)kConvNS * ROWS * kConvRB;
+};
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvFThreads, 2) k_conv_fwd(ConvArgs a) {
+  using G = ConvFwdGeom<T, K>;
+  constexpr int V = G::V, SW = G::SW, NTV = G::NTV, RPT = G::RPT, ROWS = G::ROWS;
+  constexpr int TVB = V * (int)sizeof(T);  // bytes of a thread's vector
+  extern __shared__ uint4 cstage[];        // [kConvNS][ROWS][kConvRB bytes]
+  char* stg = (char*)cstage;
   const int n_tt = (a.T + kConvTR - 1) / kConvTR, total = a.n_slabs * n_tt;
   const int i0 = blockIdx.x * a.q, i1 = min(i0 + a.q, total);
-  const int v = threadIdx.x % NV, g = threadIdx.x / NV;
+  const int v = threadIdx.x % NTV, g = threadIdx.x / NTV;
   const int64_t xld = a.x_ld * (int64_t)sizeof(T);
   auto issue = [&](int i) {
     if (i < i1) {
       const int slab = i / n_tt, tt = i % n_tt, c0 = slab * SW;
-      stage_rows<ROWS, NV>(cstage + ((i - i0) % kConvNS) * ROWS * NV,
-                           (const char*)((const T*)a.x + c0), xld, tt * kConvTR - (K - 1), a.T,
-                           min(NV, (a.C - c0) / V));
+      stage_rows<ROWS, kConvRB, kConvFThreads>(
+          stg + ((i - i0) % kConvNS) * ROWS * kConvRB, (const char*)((const T*)a.x + c0), xld,
+          tt * kConvTR - (K - 1), a.T, min(SW, a.C - c0) * (int)sizeof(T));
     }
     tc::cp_async_commit();  // possibly empty: keeps the group count uniform
   };
@@ -192,7 +226,7 @@ __global__ void __launch_bounds__(kConvThreads, 2) k_conv_fwd(ConvArgs a) {
   int cur_slab = -1;
   for (int i = i0; i < i1; ++i) {  // uniform
     const int slab = i / n_tt, tt = i % n_tt, c0 = slab * SW;
-    const bool vok = v < min(NV, (a.C - c0) / V);
+    const bool vok = v * V < a.C - c0;
     if (slab != cur_slab) {
       cur_slab = slab;
       if (vok) {
@@ -205,14 +239,14 @@ __global__ void __launch_bounds__(kConvThreads, 2) k_conv_fwd(ConvArgs a) {
     issue(i + kConvNS - 1);
     tc::cp_async_wait<kConvNS - 1>();
     __syncthreads();
-    const uint4* st = cstage + ((i - i0) % kConvNS) * ROWS * NV + v;
+    const char* st = stg + ((i - i0) % kConvNS) * ROWS * kConvRB + v * TVB;
     const int tr = tt * kConvTR + g * RPT;  // first row of this thread
     if (vok && tr < a.T) {
       int n = seq_of(a.cu, a.n_seqs, tr);
       int start = __ldg(a.cu + n), end = __ldg(a.cu + n + 1);
       float win[K][V];  // rows t-K+1 .. t (stage rows g*RPT + r .. g*RPT + r + K-1)
 #pragma unroll
-      for (int j = 0; j < K - 1; ++j) unpack<T>(st[(g * RPT + j) * NV], win[j]);
+      for (int j = 0; j < K - 1; ++j) ld4<T>(st + (g * RPT + j) * kConvRB, win[j]);
       T* yb = (T*)a.y + c0 + v * V;
 #pragma unroll
       for (int r = 0; r < RPT; ++r) {
@@ -223,7 +257,7 @@ __global__ void __launch_bounds__(kConvThreads, 2) k_conv_fwd(ConvArgs a) {
           start = end;
           end = __ldg(a.cu + n + 1);
         }
-        unpack<T>(st[(g * RPT + r + K - 1) * NV], win[K - 1]);
+        ld4<T>(st + (g * RPT + r + K - 1) * kConvRB, win[K - 1]);
         mask_window<K, V>(win, t - start);
         float out[V];
 #pragma unroll
@@ -233,7 +267,7 @@ __global__ void __launch_bounds__(kConvThreads, 2) k_conv_fwd(ConvArgs a) {
           for (int j = 0; j < K - 1; ++j) s = fmaf(wt[j][c], win[j][c], s);
           out[c] = s * sigmoid_fast(s);
         }
-        st16(yb + (int64_t)t * a.y_ld, pack<T>(out));
+        st4(yb + (int64_t)t * a.y_ld, out);
 #pragma unroll
         for (int j = 0; j < K - 1; ++j)
 #pragma unroll
@@ -248,8 +282,8 @@ __global__ void __launch_bounds__(kConvThreads, 2) k_conv_fwd(ConvArgs a) {
 // Backward (section 5 of the backward): d_sum[t] = dy[t] SiLU'(pre[t]) with pre[t] the
 // forward's pre-activation (recomputed from x); dx[s] = sum_m d_sum[s + m] w[K-1-m] over
 // the s + m inside s's sequence; dw[c, j] = sum_t d_sum[t] x[t - (K-1) + j].
-// Tiles are kConvTRB tokens of a slab of kSlabVecB vectors; a stage holds the tile's x
-// rows with K-1 before and K-1 after it, and its dy rows with K-1 after it.  Phase A forms
+// Tiles are kConvTRB tokens of a slab of 256-byte rows; a stage holds the tile's x rows
+// with K-1 before and K-1 after it, and its dy rows with K-1 after it.  Phase A forms
 // d_sum of the tile's rows and the K-1 after them (those once more in the next tile) into
 // an fp32 shared buffer, accumulating dw over the tile's own rows; phase B reads it back
 // for dx.  Block b takes tiles [b q, (b+1) q) of the slab-major tile order, so it spans
@@ -257,32 +291,31 @@ __global__ void __launch_bounds__(kConvThreads, 2) k_conv_fwd(ConvArgs a) {
 // second) and summed over blocks by k_conv_dw_sum in block order.
 constexpr int kConvTRB = 64;   // tokens of a backward tile
 constexpr int kConvNSB = 4;    // backward pipeline stages
-constexpr int kSlabVecB = 16;  // 16-byte vectors of a backward slab row (256 B)
+constexpr int kConvRBB = 256;  // bytes of a backward slab row
 
 template <typename T, int K>
 struct ConvBwdGeom {
-  static constexpr int V = kVec<T>, NV = kSlabVecB, SW = NV * V;  // slab channels
-  static constexpr int RG = kConvThreads / NV, RPT = kConvTRB / RG;
+  static constexpr int V = 4, SW = kConvRBB / (int)sizeof(T);  // slab channels
+  static constexpr int NTV = SW / V, RG = 16, THREADS = NTV * RG, RPT = kConvTRB / RG;
   static constexpr int XR = kConvTRB + 2 * (K - 1), GR = kConvTRB + (K - 1);
-  static constexpr int STAGE = (XR + GR) * NV;  // 16-byte vectors of a stage
-  static constexpr size_t smem = sizeof(uint4) * (size_t)STAGE * kConvNSB +
-                                 sizeof(float) * (size_t)GR * SW;
+  static constexpr int STAGE = (XR + GR) * kConvRBB;  // bytes of a stage
+  static constexpr size_t smem = (size_t)STAGE * kConvNSB + sizeof(float) * (size_t)GR * SW;
 };
 
 template <typename T, int K>
-__device__ __forceinline__ void conv_dw_flush(float (&dwa)[K][kVec<T>], float* red, float* part,
-                                              int v, int g) {
+__device__ __forceinline__ void conv_dw_flush(float (&dwa)[K][4], float* red, float* part, int v,
+                                              int g) {
   using G = ConvBwdGeom<T, K>;
-  constexpr int V = G::V, NV = G::NV, KV = K * V;
+  constexpr int V = G::V, NTV = G::NTV, KV = K * V;
   __syncthreads();  // red aliases the d_sum buffer
 #pragma unroll
   for (int j = 0; j < K; ++j)
 #pragma unroll
-    for (int c = 0; c < V; ++c) red[(g * NV + v) * KV + c * K + j] = dwa[j][c];
+    for (int c = 0; c < V; ++c) red[(g * NTV + v) * KV + c * K + j] = dwa[j][c];
   __syncthreads();
-  for (int e = threadIdx.x; e < NV * KV; e += kConvThreads) {  // e = (vector, c, j)
+  for (int e = threadIdx.x; e < NTV * KV; e += G::THREADS) {  // e = (vector, c, j)
     float s = 0.f;
-    for (int gg = 0; gg < G::RG; ++gg) s += red[gg * NV * KV + e];
+    for (int gg = 0; gg < G::RG; ++gg) s += red[gg * NTV * KV + e];
     part[e] = s;  // [slab channel][tap]
   }
 #pragma unroll
@@ -292,22 +325,26 @@ __device__ __forceinline__ void conv_dw_flush(float (&dwa)[K][kVec<T>], float* r
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
+__global__ void __launch_bounds__(ConvBwdGeom<T, K>::THREADS, 1) k_conv_bwd(ConvArgs a) {
   using G = ConvBwdGeom<T, K>;
-  constexpr int V = G::V, NV = G::NV, RPT = G::RPT, XR = G::XR, GR = G::GR, SW = G::SW;
-  extern __shared__ uint4 cstage[];  // [kConvNSB][XR + GR][NV], then d_sum [GR][SW] fp32
-  float* dsb = (float*)(cstage + (size_t)G::STAGE * kConvNSB);
+  constexpr int V = G::V, NTV = G::NTV, RPT = G::RPT, XR = G::XR, GR = G::GR, SW = G::SW;
+  constexpr int TVB = V * (int)sizeof(T), RB = kConvRBB;
+  extern __shared__ uint4 cstage[];  // [kConvNSB][XR + GR][RB bytes], then d_sum [GR][SW]
+  char* stg = (char*)cstage;
+  float* dsb = (float*)(stg + (size_t)G::STAGE * kConvNSB);
   const int n_tt = (a.T + kConvTRB - 1) / kConvTRB, total = a.n_slabs * n_tt;
   const int i0 = blockIdx.x * a.q, i1 = min(i0 + a.q, total);
-  const int v = threadIdx.x % NV, g = threadIdx.x / NV;
+  const int v = threadIdx.x % NTV, g = threadIdx.x / NTV;
   const int64_t xld = a.x_ld * (int64_t)sizeof(T), gld = a.dy_ld * (int64_t)sizeof(T);
   auto issue = [&](int i) {
     if (i < i1) {
       const int slab = i / n_tt, tt = i % n_tt, c0 = slab * SW, t0 = tt * kConvTRB;
-      const int nvec = min(NV, (a.C - c0) / V);
-      uint4* st = cstage + (size_t)((i - i0) % kConvNSB) * G::STAGE;
-      stage_rows<XR, NV>(st, (const char*)((const T*)a.x + c0), xld, t0 - (K - 1), a.T, nvec);
-      stage_rows<GR, NV>(st + XR * NV, (const char*)((const T*)a.dy + c0), gld, t0, a.T, nvec);
+      const int nb = min(SW, a.C - c0) * (int)sizeof(T);
+      char* st = stg + (size_t)((i - i0) % kConvNSB) * G::STAGE;
+      stage_rows<XR, RB, G::THREADS>(st, (const char*)((const T*)a.x + c0), xld, t0 - (K - 1),
+                                     a.T, nb);
+      stage_rows<GR, RB, G::THREADS>(st + XR * RB, (const char*)((const T*)a.dy + c0), gld, t0,
+                                     a.T, nb);
     }
     tc::cp_async_commit();
   };
@@ -322,12 +359,11 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
   int cur_slab = -1;
   for (int i = i0; i < i1; ++i) {  // uniform
     const int slab = i / n_tt, tt = i % n_tt, c0 = slab * SW, t0 = tt * kConvTRB;
-    const int nvec = min(NV, (a.C - c0) / V);
     if (slab != cur_slab) {
       if (cur_slab >= 0 && a.dw_part)  // the block's first slab ends: slot 0
         conv_dw_flush<T, K>(dwa, dsb, a.dw_part + (size_t)blockIdx.x * 2 * SW * K, v, g);
       cur_slab = slab;
-      if (v < nvec) {
+      if (v * V < a.C - c0) {
 #pragma unroll
         for (int c = 0; c < V; ++c)
 #pragma unroll
@@ -337,9 +373,9 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
     issue(i + kConvNSB - 1);
     tc::cp_async_wait<kConvNSB - 1>();
     __syncthreads();
-    const uint4* xs = cstage + (size_t)((i - i0) % kConvNSB) * G::STAGE + v;
-    const uint4* gs = xs + XR * NV;
-    const bool vok = v < nvec;
+    const char* xs = stg + (size_t)((i - i0) % kConvNSB) * G::STAGE + v * TVB;
+    const char* gs = xs + XR * RB;
+    const bool vok = v * V < a.C - c0;
     // ---- phase A: d_sum of rows u = g*RPT .. g*RPT+RPT-1 (and u = kConvTRB + g, g < K-1)
     // dist: tokens of t's sequence before t
     auto dsum_row = [&](int u, int dist, float (&win)[K][V], bool own) {
@@ -347,7 +383,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
       float ds[V];
       if (t < a.T) {
         float gy[V];
-        unpack<T>(gs[u * NV], gy);
+        ld4<T>(gs + u * RB, gy);
         mask_window<K, V>(win, dist);
 #pragma unroll
         for (int c = 0; c < V; ++c) {
@@ -367,9 +403,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
 #pragma unroll
         for (int c = 0; c < V; ++c) ds[c] = 0.f;
       }
-      float4* d = (float4*)(dsb + u * SW + v * V);
-#pragma unroll
-      for (int c = 0; c < V; c += 4) d[c / 4] = make_float4(ds[c], ds[c + 1], ds[c + 2], ds[c + 3]);
+      *(float4*)(dsb + u * SW + v * V) = make_float4(ds[0], ds[1], ds[2], ds[3]);
     };
     if (vok) {
       float win[K][V];
@@ -377,7 +411,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
       int n = seq_of(a.cu, a.n_seqs, tr);
       int start = __ldg(a.cu + n), end = __ldg(a.cu + n + 1);
 #pragma unroll
-      for (int j = 0; j < K - 1; ++j) unpack<T>(xs[(g * RPT + j) * NV], win[j]);
+      for (int j = 0; j < K - 1; ++j) ld4<T>(xs + (g * RPT + j) * RB, win[j]);
 #pragma unroll
       for (int r = 0; r < RPT; ++r) {
         const int u = g * RPT + r, t = t0 + u;
@@ -386,7 +420,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
           start = end;
           end = __ldg(a.cu + n + 1);
         }
-        unpack<T>(xs[(u + K - 1) * NV], win[K - 1]);
+        ld4<T>(xs + (u + K - 1) * RB, win[K - 1]);
         dsum_row(u, t - start, win, true);
 #pragma unroll
         for (int j = 0; j < K - 1; ++j)
@@ -396,7 +430,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
       if (g < K - 1) {  // one of the K-1 rows after the tile
         const int u = kConvTRB + g, t = min(t0 + u, a.T - 1);
 #pragma unroll
-        for (int j = 0; j < K; ++j) unpack<T>(xs[(u + j) * NV], win[j]);
+        for (int j = 0; j < K; ++j) ld4<T>(xs + (u + j) * RB, win[j]);
         dsum_row(u, t - __ldg(a.cu + seq_of(a.cu, a.n_seqs, t)), win, false);
       }
     }
@@ -419,18 +453,14 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bwd(ConvArgs a) {
 #pragma unroll
         for (int m = 0; m < K; ++m) {
           if (m < room) {
-            const float4* d = (const float4*)(dsb + (g * RPT + r + m) * SW + v * V);
-#pragma unroll
-            for (int c = 0; c < V; c += 4) {
-              const float4 f = d[c / 4];
-              out[c] = fmaf(f.x, wt[K - 1 - m][c], out[c]);
-              out[c + 1] = fmaf(f.y, wt[K - 1 - m][c + 1], out[c + 1]);
-              out[c + 2] = fmaf(f.z, wt[K - 1 - m][c + 2], out[c + 2]);
-              out[c + 3] = fmaf(f.w, wt[K - 1 - m][c + 3], out[c + 3]);
-            }
+            const float4 f = *(const float4*)(dsb + (g * RPT + r + m) * SW + v * V);
+            out[0] = fmaf(f.x, wt[K - 1 - m][0], out[0]);
+            out[1] = fmaf(f.y, wt[K - 1 - m][1], out[1]);
+            out[2] = fmaf(f.z, wt[K - 1 - m][2], out[2]);
+            out[3] = fmaf(f.w, wt[K - 1 - m][3], out[3]);
           }
         }
-        st16(dxb + (int64_t)s * a.y_ld, pack<T>(out));
+        st4(dxb + (int64_t)s * a.y_ld, out);
       }
     }
     __syncthreads();  // d_sum buffer and stage reused
@@ -633,7 +663,7 @@ struct ConvGeom {
 // `blocks` is the number of resident blocks to fill (capped at 1024).
 inline ConvGeom conv_geom(bool bwd, int T, int C, int es, int blocks) {
   ConvGeom g;
-  const int sw = (bwd ? kSlabVecB : kSlabVec) * (16 / es);
+  const int sw = (bwd ? kConvRBB : kConvRB) / es;  // slab channels
   const int tr = bwd ? kConvTRB : kConvTR;
   g.n_slabs = (C + sw - 1) / sw;
   g.n_tt = (T + tr - 1) / tr;
@@ -648,8 +678,8 @@ inline ConvGeom conv_geom(bool bwd, int T, int C, int es, int blocks) {
 
 template <bool BWD, typename T, int K>
 cudaError_t conv_launch(const ConvArgs& a, int grid, cudaStream_t st) {
-  const size_t smem = BWD ? ConvBwdGeom<T, K>::smem
-                          : sizeof(uint4) * (size_t)kConvNS * (kConvTR + K - 1) * kSlabVec;
+  const size_t smem = BWD ? ConvBwdGeom<T, K>::smem : ConvFwdGeom<T, K>::smem;
+  const int threads = BWD ? ConvBwdGeom<T, K>::THREADS : kConvFThreads;
   static bool attr_set = false;  // one instantiation, one attribute
   if (!attr_set) {
     const cudaError_t e =
@@ -661,9 +691,9 @@ cudaError_t conv_launch(const ConvArgs& a, int grid, cudaStream_t st) {
     attr_set = true;
   }
   if constexpr (BWD)
-    k_conv_bwd<T, K><<<grid, kConvThreads, smem, st>>>(a);
+    k_conv_bwd<T, K><<<grid, threads, smem, st>>>(a);
   else
-    k_conv_fwd<T, K><<<grid, kConvThreads, smem, st>>>(a);
+    k_conv_fwd<T, K><<<grid, threads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -724,7 +754,7 @@ size_t conv_partial_floats(int64_t T, int C, int K) {
   size_t most = 0;
   for (int es : {2, 4}) {
     const ConvGeom g = conv_geom(true, (int)T, C, es, 1024);
-    const size_t f = (size_t)g.grid * 2 * kSlabVecB * (16 / es) * K;
+    const size_t f = (size_t)g.grid * 2 * (kConvRBB / es) * K;
     most = f > most ? f : most;
   }
   return most;
@@ -765,7 +795,7 @@ cudaError_t launch_conv1d_silu(bool bwd, int dtype, int64_t T, int C, int K, con
   profile_post(st);
   if (e != cudaSuccess || !a.dw_part) return e;
   profile_pre(st, KID_SUM_PARTS);
-  k_conv_dw_sum<<<(C * K + 255) / 256, 256, 0, st>>>(part, C, K, kSlabVecB * (16 / es), g.n_tt,
+  k_conv_dw_sum<<<(C * K + 255) / 256, 256, 0, st>>>(part, C, K, kConvRBB / es, g.n_tt,
                                                      g.q, dw);
   profile_post(st);
   return cudaGetLastError();
