@@ -185,13 +185,13 @@ def kernel_models(wl: W.Workload):
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, one launch) of a kernel
 # from an ncu capture of this workload, with a hash of the sources it was built from;
-# a kernel whose sources changed since reports null (profiles/tc_kernels_l27b_bf16.md).
+# a kernel whose sources changed since reports null (profiles/fused_kernels_l27b_bf16.md).
 NCU_TRAFFIC = {
-    ("gdn_bwd_grads_tc", "l27b_bf16"): (655.676416e6, "91b4d82f68e0ec3b"),
-    ("gdn_bwd_fused_tc", "l27b_bf16"): (935.549952e6, "1f338a226f8254f2"),
+    ("gdn_fwd_fused_tc", "l27b_bf16"): (441.436672e6, "5267567a4d147c9a"),
+    ("gdn_bwd_fused_tc", "l27b_bf16"): (941.737728e6, "fd01625b7bbe0c71"),
 }
 KERNEL_SOURCES = {
-    "gdn_bwd_grads_tc": ("gdn_tc_bwd.cu", "gdn_tc.cuh", "umma.cuh", "gdn_device.cuh",
+    "gdn_fwd_fused_tc": ("gdn_tc_fwd.cu", "gdn_tc.cuh", "umma.cuh", "gdn_device.cuh",
                          "gdn_internal.cuh"),
     "gdn_bwd_fused_tc": ("gdn_tc_bwd.cu", "gdn_tc.cuh", "umma.cuh", "gdn_device.cuh",
                          "gdn_internal.cuh"),
