@@ -18,6 +18,8 @@
 // to run.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "gdn_device.cuh"
 #include "gdn_internal.cuh"
 #include "umma.cuh"
@@ -247,18 +249,9 @@ __global__ void __launch_bounds__(kConvFThreads, 2) k_conv_fwd(ConvArgs a) {
       float win[K][V];  // rows t-K+1 .. t (stage rows g*RPT + r .. g*RPT + r + K-1)
 #pragma unroll
       for (int j = 0; j < K - 1; ++j) ld4<T>(st + (g * RPT + j) * kConvRB, win[j]);
-      T* yb = (T*)a.y + c0 + v * V;
-#pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        const int t = tr + r;
-        if (t >= a.T) break;
-        while (t >= end && n + 1 < a.n_seqs) {  // next sequence
-          ++n;
-          start = end;
-          end = __ldg(a.cu + n + 1);
-        }
+      T* yb = (T*)a.y + c0 + v * V + (int64_t)tr * a.y_ld;
+      auto row = [&](int r) {
         ld4<T>(st + (g * RPT + r + K - 1) * kConvRB, win[K - 1]);
-        mask_window<K, V>(win, t - start);
         float out[V];
 #pragma unroll
         for (int c = 0; c < V; ++c) {
@@ -267,11 +260,29 @@ __global__ void __launch_bounds__(kConvFThreads, 2) k_conv_fwd(ConvArgs a) {
           for (int j = 0; j < K - 1; ++j) s = fmaf(wt[j][c], win[j][c], s);
           out[c] = s * sigmoid_fast(s);
         }
-        st4(yb + (int64_t)t * a.y_ld, out);
+        st4(yb + (int64_t)r * a.y_ld, out);
 #pragma unroll
         for (int j = 0; j < K - 1; ++j)
 #pragma unroll
           for (int c = 0; c < V; ++c) win[j][c] = win[j + 1][c];
+      };
+      if (tr - (K - 1) >= start && tr + RPT <= end && tr + RPT <= a.T) {
+        // the rows and their windows lie inside one sequence: no checks per row
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) row(r);
+      } else {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+          const int t = tr + r;
+          if (t >= a.T) break;
+          while (t >= end && n + 1 < a.n_seqs) {  // next sequence
+            ++n;
+            start = end;
+            end = __ldg(a.cu + n + 1);
+          }
+          mask_window<K, V>(win, t - start);  // the rows before t's start (window[0..K-2])
+          row(r);
+        }
       }
     }
     __syncthreads();  // the stage is refilled by a later issue
@@ -378,13 +389,15 @@ __global__ void __launch_bounds__(ConvBwdGeom<T, K>::THREADS, 1) k_conv_bwd(Conv
     const bool vok = v * V < a.C - c0;
     // ---- phase A: d_sum of rows u = g*RPT .. g*RPT+RPT-1 (and u = kConvTRB + g, g < K-1)
     // dist: tokens of t's sequence before t
-    auto dsum_row = [&](int u, int dist, float (&win)[K][V], bool own) {
+    // CHECK false: the caller knows t < T and the whole window lies in t's sequence
+    auto dsum_row = [&](int u, int dist, float (&win)[K][V], bool own, auto check) {
+      constexpr bool CHECK = decltype(check)::value;
       const int t = t0 + u;
       float ds[V];
-      if (t < a.T) {
+      if (!CHECK || t < a.T) {
         float gy[V];
         ld4<T>(gs + u * RB, gy);
-        mask_window<K, V>(win, dist);
+        if (CHECK) mask_window<K, V>(win, dist);
 #pragma unroll
         for (int c = 0; c < V; ++c) {
           float s = wt[K - 1][c] * win[K - 1][c];
@@ -412,26 +425,41 @@ __global__ void __launch_bounds__(ConvBwdGeom<T, K>::THREADS, 1) k_conv_bwd(Conv
       int start = __ldg(a.cu + n), end = __ldg(a.cu + n + 1);
 #pragma unroll
       for (int j = 0; j < K - 1; ++j) ld4<T>(xs + (g * RPT + j) * RB, win[j]);
+      const int ta = t0 + g * RPT;
+      if (ta - (K - 1) >= start && ta + RPT <= end && ta + RPT <= a.T) {
+        // the rows and their windows lie inside one sequence: no checks per row
 #pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        const int u = g * RPT + r, t = t0 + u;
-        while (t >= end && n + 1 < a.n_seqs) {
-          ++n;
-          start = end;
-          end = __ldg(a.cu + n + 1);
+        for (int r = 0; r < RPT; ++r) {
+          const int u = g * RPT + r;
+          ld4<T>(xs + (u + K - 1) * RB, win[K - 1]);
+          dsum_row(u, K - 1, win, true, std::false_type());
+#pragma unroll
+          for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+            for (int c = 0; c < V; ++c) win[j][c] = win[j + 1][c];
         }
-        ld4<T>(xs + (u + K - 1) * RB, win[K - 1]);
-        dsum_row(u, t - start, win, true);
+      } else {
 #pragma unroll
-        for (int j = 0; j < K - 1; ++j)
+        for (int r = 0; r < RPT; ++r) {
+          const int u = g * RPT + r, t = t0 + u;
+          while (t >= end && n + 1 < a.n_seqs) {
+            ++n;
+            start = end;
+            end = __ldg(a.cu + n + 1);
+          }
+          ld4<T>(xs + (u + K - 1) * RB, win[K - 1]);
+          dsum_row(u, t - start, win, true, std::true_type());
 #pragma unroll
-          for (int c = 0; c < V; ++c) win[j][c] = win[j + 1][c];
+          for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+            for (int c = 0; c < V; ++c) win[j][c] = win[j + 1][c];
+        }
       }
       if (g < K - 1) {  // one of the K-1 rows after the tile
         const int u = kConvTRB + g, t = min(t0 + u, a.T - 1);
 #pragma unroll
         for (int j = 0; j < K; ++j) ld4<T>(xs + (u + j) * RB, win[j]);
-        dsum_row(u, t - __ldg(a.cu + seq_of(a.cu, a.n_seqs, t)), win, false);
+        dsum_row(u, t - __ldg(a.cu + seq_of(a.cu, a.n_seqs, t)), win, false, std::true_type());
       }
     }
     __syncthreads();
@@ -441,12 +469,8 @@ __global__ void __launch_bounds__(ConvBwdGeom<T, K>::THREADS, 1) k_conv_bwd(Conv
       int n = seq_of(a.cu, a.n_seqs, s0 < a.T ? s0 : a.T - 1);
       int end = __ldg(a.cu + n + 1);
       T* dxb = (T*)a.y + c0 + v * V;
-#pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        const int s = s0 + r;
-        if (s >= a.T) break;
-        while (s >= end && n + 1 < a.n_seqs) end = __ldg(a.cu + (++n) + 1);
-        const int room = end - s;  // d_sum[s + m] counts iff m < room
+      // dx of row s0 + r from d_sum rows r .. r+K-1 (room: how many of them count)
+      auto dx_row = [&](int r, int room) {
         float out[V];
 #pragma unroll
         for (int c = 0; c < V; ++c) out[c] = 0.f;
@@ -460,7 +484,20 @@ __global__ void __launch_bounds__(ConvBwdGeom<T, K>::THREADS, 1) k_conv_bwd(Conv
             out[3] = fmaf(f.w, wt[K - 1 - m][3], out[3]);
           }
         }
-        st4(dxb + (int64_t)s * a.y_ld, out);
+        st4(dxb + (int64_t)(s0 + r) * a.y_ld, out);
+      };
+      if (s0 + RPT - 1 + (K - 1) < end && s0 + RPT <= a.T) {
+        // every row's K taps lie inside its sequence
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) dx_row(r, K);
+      } else {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+          const int s = s0 + r;
+          if (s >= a.T) break;
+          while (s >= end && n + 1 < a.n_seqs) end = __ldg(a.cu + (++n) + 1);
+          dx_row(r, end - s);
+        }
       }
     }
     __syncthreads();  // d_sum buffer and stage reused
