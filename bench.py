@@ -425,6 +425,8 @@ def run_ours(args):
         result["kda"] = run_kda(wl, device, pk)
     if rank == 0 and world == 1 and not args.no_context_parallel:
         result["context_parallel"] = run_context_parallel(wl, device, step_ms)
+        result["context_parallel_long"] = run_context_parallel(wl, device, None, segments=8,
+                                                               tokens=16 * wl.total_tokens)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
     if rank == 0:
@@ -596,15 +598,16 @@ def run_kda(wl, device, pk, n_seqs=64, prefill_tokens=1024, steps=20, warmup=3):
     return out
 
 
-def run_context_parallel(wl, device, plain_step_ms, segments=4, steps=3, warmup=1):
-    """One sequence of the workload's length cut into `segments` equal segments, all on this
-    GPU (context parallelism run serially): the whole segmented training step (segment
-    maps, scans, final passes) and each pass alone, with CUDA events.  per_rank_ms adds up
-    the passes one rank of a `segments`-GPU group would run (exchange not included).
-    Synthetic inputs, resident."""
+def run_context_parallel(wl, device, plain_step_ms, segments=4, steps=3, warmup=1, tokens=None):
+    """One sequence of the workload's length (or `tokens`) cut into `segments` equal
+    segments, all on this GPU (context parallelism run serially): the whole segmented
+    training step (segment maps, scans, final passes) and each pass alone, with CUDA
+    events.  per_rank_ms adds up the passes one rank of a `segments`-GPU group would run
+    (exchange not included).  With `tokens` the unsegmented step on the whole sequence is
+    timed too (plain_step_ms).  Synthetic inputs, resident."""
     import torch
     from gated_deltanet_backward_gb300 import context_parallel as cp
-    T, Hk, Hv, Dk, Dv = wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv
+    T, Hk, Hv, Dk, Dv = tokens or wl.total_tokens, wl.Hk, wl.Hv, wl.Dk, wl.Dv
     td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     g = torch.Generator(device=device).manual_seed(99)
     rn = lambda *sh, dt=torch.float32: torch.randn(*sh, generator=g, device=device).to(dt)
@@ -635,6 +638,18 @@ def run_context_parallel(wl, device, plain_step_ms, segments=4, steps=3, warmup=
         return cp.backward(ops, segs, S_ins, dOs, dS_T)
 
     step_ms, _ = timed(step, steps)
+    if tokens:
+        whole = cp.Segment(torch.cat([sg.q for sg in segs]), torch.cat([sg.k for sg in segs]),
+                           torch.cat([sg.v for sg in segs]), torch.cat([sg.alpha for sg in segs]),
+                           torch.cat([sg.beta_raw for sg in segs]), a_log, dt_bias)
+        dO_all = torch.cat(dOs)
+
+        def plain():
+            ops.forward(whole, S0, keep=True)
+            return ops.backward(whole, S0, dO_all, dS_T)
+
+        plain_step_ms, _ = timed(plain, steps)
+        del whole
     s0 = segs[0]
     map_ms, Phi = timed(lambda: ops.state_map(s0), steps)
     fz_ms, _ = timed(lambda: ops.forward(s0, None, keep=False), steps)
