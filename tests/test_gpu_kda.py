@@ -109,3 +109,20 @@ def test_rejects_bad_arguments():
     with pytest.raises(gdn.GdnError):     # no cu_seqlens
         gdn.gdn_kda_forward(shape, q, q, v, z(N, Hv * D), z(N, Hv), z(Hv), z(Hv * D), None, None,
                             z(N, Hv, D, D), v.clone())
+
+
+@pytest.mark.slow
+def test_full_layer_prefill_against_the_oracle_on_every_element():
+    """The 27B-shaped layer (4096 tokens, 16 key / 48 value heads of 128, bf16) as one KDA
+    prefill in token form."""
+    torch = pytest.importorskip("torch")
+    import gated_deltanet_backward_gb300 as gdn
+    base = W.get("l27b_bf16")
+    wl = W.custom(dtype="bf16", seed=base.seed, Hk=base.Hk, Hv=base.Hv, Dk=base.Dk, Dv=base.Dv,
+                  seqlens=base.seqlens, S0_std=0.1, dt_bias_std=0.3, packed=True)
+    inp = W.generate(wl)
+    alpha, b_alpha = W.generate_kda_gates(wl)
+    o, S_T = _run(torch, gdn, wl, inp, alpha, b_alpha)
+    o_ref, S_ref = _ref(wl, inp, alpha, b_alpha)
+    assert rel_err(o, o_ref) <= TOL["bf16"]
+    assert rel_err(S_T, S_ref) <= TOL["bf16"]
