@@ -188,7 +188,6 @@ class GpuSegmentOps:
 
     def backward(self, seg, S_in, dO, dS_out):
         torch = self._torch()
-        L = int(seg.q.shape[0])
         layer = seg.state["layer"]
         g = dict(dq=torch.empty_like(seg.q), dk=torch.empty_like(seg.k),
                  dv=torch.empty_like(seg.v), dalpha=torch.empty_like(seg.alpha),
@@ -198,7 +197,6 @@ class GpuSegmentOps:
         layer.backward(seg.q, seg.k, seg.v, seg.alpha, seg.beta_raw, seg.a_log, seg.dt_bias, S_in,
                        dO, dS_out, g["dq"], g["dk"], g["dv"], g["dalpha"], g["dbeta_raw"],
                        g["da_log"], g["ddt_bias"], g["dS0"], train=True)
-        assert L == g["dq"].shape[0]
         return g
 
     def compose(self, Phi, S, R, transpose):
