@@ -103,6 +103,11 @@ _lib.gdn_state_compose.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int3
 _lib.gdn_state_compose.restype = ctypes.c_int
 _lib.gdn_kda_forward.argtypes = [_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64, _vp]
 _lib.gdn_kda_forward.restype = ctypes.c_int
+_lib.gdn_kda_backward_workspace_bytes.argtypes = [_SP]
+_lib.gdn_kda_backward_workspace_bytes.restype = _sz
+_lib.gdn_kda_backward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 4 + [_vp, _i64] + [_vp] +
+                                  [_vp, _i64] * 5 + [_vp] * 3 + [_vp, _sz, _vp])
+_lib.gdn_kda_backward.restype = ctypes.c_int
 _lib.gdn_read_device_status.argtypes = [_vp, _vp]
 _lib.gdn_read_device_status.restype = ctypes.c_int
 _lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -122,7 +127,8 @@ EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_for
             "gdn_decode_step", "gdn_conv1d_silu_forward", "gdn_conv1d_silu_workspace_bytes",
             "gdn_conv1d_silu_backward", "gdn_gated_rmsnorm_forward",
             "gdn_gated_rmsnorm_workspace_bytes", "gdn_gated_rmsnorm_backward",
-            "gdn_state_compose", "gdn_kda_forward")
+            "gdn_state_compose", "gdn_kda_forward", "gdn_kda_backward_workspace_bytes",
+            "gdn_kda_backward")
 
 
 class GdnError(RuntimeError):
@@ -358,6 +364,27 @@ def gdn_kda_forward(shape, q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens,
     args += list(_mat(o))
     args += [_stream(stream)]
     _check(_lib.gdn_kda_forward(*args), "gdn_kda_forward")
+
+
+def gdn_kda_backward_workspace_bytes(shape) -> int:
+    return int(_lib.gdn_kda_backward_workspace_bytes(ctypes.byref(shape)))
+
+
+def gdn_kda_backward(shape, q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens, S0, dO, dS_T,
+                     dq, dk, dv, dalpha, dbeta_raw, da_log, db_alpha, dS0, workspace,
+                     stream=None) -> None:
+    """Calls gdn_kda_backward (S0, dS_T, dS0 may be None); workspace of
+    gdn_kda_backward_workspace_bytes(shape) bytes."""
+    args = [ctypes.byref(shape)]
+    for t in (q, k, v, alpha, beta_raw):
+        args += list(_mat(t))
+    args += [_ptr(a_log), _ptr(b_alpha), _ptr(cu_seqlens), _ptr(S0)]
+    args += list(_mat(dO)) + [_ptr(dS_T)]
+    for t in (dq, dk, dv, dalpha, dbeta_raw):
+        args += list(_mat(t))
+    args += [_ptr(da_log), _ptr(db_alpha), _ptr(dS0), _ptr(workspace), _nbytes(workspace),
+             _stream(stream)]
+    _check(_lib.gdn_kda_backward(*args), "gdn_kda_backward")
 
 
 def gdn_read_device_status(workspace, stream=None) -> int:

@@ -359,6 +359,7 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_SUM_PARTS: return "gdn_sum_partials";
     case gdn::KID_COMPOSE: return "gdn_state_compose";
     case gdn::KID_KDA_FWD: return "gdn_kda_fwd";
+    case gdn::KID_KDA_BWD: return "gdn_kda_bwd";
     default: return "?";
   }
 }
@@ -747,6 +748,69 @@ int gdn_kda_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void*
                                                 beta_raw, beta_ld, a_log, b_alpha, cu_seqlens,
                                                 S_in, S_out, o, o_ld, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail("gdn_kda_forward: kernel launch", e);
+  return GDN_OK;
+}
+
+size_t gdn_kda_backward_workspace_bytes(const gdn_shape* s) {
+  if (!s || s->total_tokens < 0 || s->n_seqs < 0 || s->Hv <= 0 || s->Dk <= 0 || s->Dv <= 0)
+    return 0;
+  return gdn::align256(gdn::kda_bwd_workspace_floats(s) * sizeof(float));
+}
+
+int gdn_kda_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                     int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                     int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                     const float* a_log, const float* b_alpha, const int32_t* cu_seqlens,
+                     const float* S0, const void* dO, int64_t dO_ld, const float* dS_T,
+                     void* dq, int64_t dq_ld, void* dk, int64_t dk_ld, void* dv, int64_t dv_ld,
+                     float* dalpha, int64_t dalpha_ld, float* dbeta_raw, int64_t dbeta_ld,
+                     float* da_log, float* db_alpha, float* dS0, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (!s) return GDN_ERR_INVALID_ARG;
+  gdn_shape sh = *s;
+  sh.total_chunks = (int32_t)((s->total_tokens + gdn::kChunk - 1) / gdn::kChunk);
+  GDN_TRY(check_shape(&sh));
+  if (s->Dv < 32) return GDN_ERR_UNSUPPORTED;  // 32-column slices
+  const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
+  const int64_t T = s->total_tokens;
+  if (T > ((int64_t)1 << 31) - 1 || s->n_seqs > 65535) return GDN_ERR_UNSUPPORTED;
+  const int64_t wk = (int64_t)s->Hk * s->Dk, wv = (int64_t)s->Hv * s->Dv;
+  GDN_TRY(check_matrix(q, q_ld, wk, es, T));
+  GDN_TRY(check_matrix(k, k_ld, wk, es, T));
+  GDN_TRY(check_matrix(v, v_ld, wv, es, T));
+  GDN_TRY(check_matrix(dO, dO_ld, wv, es, T));
+  GDN_TRY(check_matrix(dq, dq_ld, wk, es, T));
+  GDN_TRY(check_matrix(dk, dk_ld, wk, es, T));
+  GDN_TRY(check_matrix(dv, dv_ld, wv, es, T));
+  GDN_TRY(check_gate_matrix(alpha, alpha_ld, (int64_t)s->Hv * s->Dk, T));
+  GDN_TRY(check_gate_matrix(dalpha, dalpha_ld, (int64_t)s->Hv * s->Dk, T));
+  GDN_TRY(check_gate_matrix(beta_raw, beta_ld, s->Hv, T));
+  GDN_TRY(check_gate_matrix(dbeta_raw, dbeta_ld, s->Hv, T));
+  GDN_TRY(check_vec(a_log, true));
+  GDN_TRY(check_vec(b_alpha, true));
+  GDN_TRY(check_vec(da_log, true));
+  GDN_TRY(check_vec(db_alpha, true));
+  GDN_TRY(check_vec(S0, false));
+  GDN_TRY(check_vec(dS_T, false));
+  GDN_TRY(check_vec(dS0, false));
+  if (s->n_seqs > 0 && (!cu_seqlens || ((uintptr_t)cu_seqlens & 3u) != 0))
+    return cu_seqlens ? GDN_ERR_MISALIGNED : GDN_ERR_INVALID_ARG;
+  GDN_TRY(check_scratch(workspace, workspace_bytes, gdn_kda_backward_workspace_bytes(s)));
+  (void)cudaGetLastError();
+  g_last_error[0] = 0;
+  cudaError_t e = cudaSuccess;
+  if (s->n_seqs == 0) {  // nothing to walk: the parameter gradients are zero
+    e = cudaMemsetAsync(da_log, 0, sizeof(float) * s->Hv, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(db_alpha, 0, sizeof(float) * s->Hv * s->Dk, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail("gdn_kda_backward: cudaMemsetAsync", e);
+    return GDN_OK;
+  }
+  e = gdn::launch_kda_backward(&sh, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld,
+                               a_log, b_alpha, cu_seqlens, S0, dO, dO_ld, dS_T, dq, dq_ld, dk,
+                               dk_ld, dv, dv_ld, dalpha, dalpha_ld, dbeta_raw, dbeta_ld, da_log,
+                               db_alpha, dS0, (float*)workspace, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("gdn_kda_backward: kernel launch", e);
   return GDN_OK;
 }
 

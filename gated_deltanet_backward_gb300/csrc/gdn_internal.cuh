@@ -236,7 +236,8 @@ enum KernelId {
   KID_SUM_PARTS = 18,
   KID_COMPOSE = 19,
   KID_KDA_FWD = 20,
-  KID_COUNT = 21
+  KID_KDA_BWD = 21,
+  KID_COUNT = 22
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
@@ -291,6 +292,18 @@ cudaError_t launch_kda_forward(const gdn_shape* s, const void* q, int64_t q_ld, 
                                const float* a_log, const float* b_alpha, const int32_t* cu,
                                const float* S_in, float* S_out, void* o, int64_t o_ld,
                                cudaStream_t st);
+// Its backward (gdn_kda.cu): saved states, per-slice shares and sums in `ws`
+// (kda_bwd_workspace_floats floats).
+size_t kda_bwd_workspace_floats(const gdn_shape* s);
+cudaError_t launch_kda_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                                int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                                int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                                const float* a_log, const float* b_alpha, const int32_t* cu,
+                                const float* S0, const void* dO, int64_t dO_ld,
+                                const float* dS_T, void* dq, int64_t dq_ld, void* dk,
+                                int64_t dk_ld, void* dv, int64_t dv_ld, float* dalpha,
+                                int64_t dalpha_ld, float* dbeta, int64_t dbeta_ld, float* da_log,
+                                float* db_alpha, float* dS0, float* ws, cudaStream_t st);
 cudaError_t launch_decode(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
                           int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
                           int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,

@@ -378,6 +378,32 @@ int gdn_kda_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const v
                     const float* b_alpha, const int32_t* cu_seqlens, const float* S_in,
                     float* S_out, void* o, int64_t o_ld, void* stream);
 
+/* Reverse mode of gdn_kda_forward, in token form: given dO and dS_T (NULL = zero) it
+ * returns dq, dk (summed over the value heads that share a key head), dv, d alpha
+ * [total_tokens, Hv*Dk], d beta_raw, d a_log [Hv], d b_alpha [Hv*Dk] (sums over every
+ * token of every sequence) and dS_0 (NULL skips it).  All sums over value columns, value
+ * heads and tokens are formed in a fixed order: results are bit-reproducible.
+ * Each (sequence, value head, 32-column slice of the state) first walks its tokens
+ * forward saving the state every 8 tokens, then walks them in reverse, recomputing each
+ * 8-token segment from its saved state.  The workspace (16-byte aligned, at least
+ * gdn_kda_backward_workspace_bytes(shape) bytes) holds those states and the per-slice
+ * shares of dq_hat, dk_hat, dg, d beta: about (T/8 + n_seqs) * Hv * Dk * Dv * 4 +
+ * T * Hv * (Dv/32) * (3 Dk + 1) * 4 bytes.
+ * shape: as for gdn_kda_forward, with Dv >= 32.  Buffers and strides as there; dq, dk,
+ * dv, dO have the dtype; dalpha and dbeta_raw are fp32 with strides >= Hv*Dk and >= Hv.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_MISALIGNED,
+ * GDN_ERR_WORKSPACE or GDN_ERR_CUDA; nothing is launched on an error. */
+size_t gdn_kda_backward_workspace_bytes(const gdn_shape* shape);
+int gdn_kda_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
+                     int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                     int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                     const float* a_log, const float* b_alpha, const int32_t* cu_seqlens,
+                     const float* S0, const void* dO, int64_t dO_ld, const float* dS_T,
+                     void* dq, int64_t dq_ld, void* dk, int64_t dk_ld, void* dv, int64_t dv_ld,
+                     float* dalpha, int64_t dalpha_ld, float* dbeta_raw, int64_t dbeta_ld,
+                     float* da_log, float* db_alpha, float* dS0, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream` and returns the device-side status recorded in
  * `workspace` by the last gdn_forward / gdn_backward that used it (GDN_OK, or
  * the first device error), or GDN_ERR_CUDA if the stream itself failed. */

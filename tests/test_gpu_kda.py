@@ -126,3 +126,53 @@ def test_full_layer_prefill_against_the_oracle_on_every_element():
     o_ref, S_ref = _ref(wl, inp, alpha, b_alpha)
     assert rel_err(o, o_ref) <= TOL["bf16"]
     assert rel_err(S_T, S_ref) <= TOL["bf16"]
+
+
+def _run_bwd(torch, gdn, wl, inp, alpha, b_alpha, dS_T):
+    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    T, N = wl.total_tokens, len(inp.cu_seqlens) - 1
+    Hk, Hv, Dk, Dv = wl.Hk, wl.Hv, wl.Dk, wl.Dv
+    q, k, v, dO = (_dev(torch, x, td) for x in (inp.q, inp.k, inp.v, inp.dO))
+    nan = lambda *s, dt=torch.float32: torch.full(s, float("nan"), device="cuda", dtype=dt)
+    g = dict(dq=nan(T, Hk * Dk, dt=td), dk=nan(T, Hk * Dk, dt=td), dv=nan(T, Hv * Dv, dt=td),
+             dalpha=nan(T, Hv * Dk), dbeta_raw=nan(T, Hv), da_log=nan(Hv), db_alpha=nan(Hv * Dk),
+             dS0=nan(N, Hv, Dk, Dv))
+    shape = gdn.make_shape(Hk, Hv, Dk, Dv, N, 0, T, wl.dtype, wl.scale_value(), wl.head_map)
+    ws = torch.empty(gdn.gdn_kda_backward_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    gdn.gdn_kda_backward(shape, q, k, v, _dev(torch, alpha), _dev(torch, inp.beta_raw),
+                         _dev(torch, inp.a_log), _dev(torch, b_alpha),
+                         _dev(torch, inp.cu_seqlens, torch.int32),
+                         None if inp.S0 is None else _dev(torch, inp.S0), dO,
+                         None if dS_T is None else _dev(torch, dS_T), g["dq"], g["dk"], g["dv"],
+                         g["dalpha"], g["dbeta_raw"], g["da_log"], g["db_alpha"], g["dS0"], ws)
+    torch.cuda.synchronize()
+    return {key: val.float().cpu().numpy() for key, val in g.items()}
+
+
+@pytest.mark.parametrize("dtype,Hk,Hv,Dk,Dv,seqlens,head_map", [
+    ("f32", 1, 2, 16, 32, (1, 9, 0, 20), 0),      # segments of 8: ragged, empty, one-token
+    ("f32", 2, 4, 64, 64, (37, 70), 0),
+    ("bf16", 2, 6, 128, 128, (45, 18), 0),
+    ("bf16", 2, 4, 32, 64, (33,), 1),              # modulo head map
+])
+def test_backward_matches_the_oracle(dtype, Hk, Hv, Dk, Dv, seqlens, head_map):
+    torch = pytest.importorskip("torch")
+    import gated_deltanet_backward_gb300 as gdn
+    wl, inp, alpha, b_alpha = _case(dtype, Hk, Hv, Dk, Dv, seqlens, head_map=head_map, seed=17)
+    dS_T = (0.3 * np.random.default_rng(4).standard_normal(inp.S0.shape)).astype(np.float32)
+    got = _run_bwd(torch, gdn, wl, inp, alpha, b_alpha, dS_T)
+    ref = oracle.kda_backward(inp.q, inp.k, inp.v, alpha, inp.beta_raw, inp.a_log, b_alpha,
+                              inp.cu_seqlens, inp.dO, inp.S0, dS_T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv,
+                              scale=wl.scale_value(), head_map=head_map)
+    for key in ("dq", "dk", "dv", "dalpha", "dbeta_raw", "da_log", "db_alpha", "dS0"):
+        assert rel_err(got[key], ref[key]) <= TOL[dtype], key
+
+
+def test_backward_is_bit_reproducible():
+    torch = pytest.importorskip("torch")
+    import gated_deltanet_backward_gb300 as gdn
+    wl, inp, alpha, b_alpha = _case("bf16", 2, 4, 64, 64, (50, 31), seed=19)
+    a = _run_bwd(torch, gdn, wl, inp, alpha, b_alpha, None)
+    b = _run_bwd(torch, gdn, wl, inp, alpha, b_alpha, None)
+    for key in a:
+        assert np.array_equal(a[key], b[key]), key
