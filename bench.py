@@ -552,7 +552,8 @@ def run_kda(wl, device, pk, n_seqs=64, prefill_tokens=1024, steps=20, warmup=3):
     """The KDA variant (a decay gate per key channel) with the workload's head shape:
     gdn_kda_forward as a decode step on n_seqs one-token sequences (state in place; bytes
     as for the decode step plus the per-channel gate rows) against HBM, and as a prefill
-    of one prefill_tokens-token sequence in token form (tokens/s).  Synthetic inputs."""
+    of one prefill_tokens-token sequence in token form (tokens/s), and that prefill's
+    training step (gdn_kda_forward + gdn_kda_backward).  Synthetic inputs."""
     import torch
     import gated_deltanet_backward_gb300 as gdn
     Hk, Hv, Dk, Dv = wl.Hk, wl.Hv, wl.Dk, wl.Dv
@@ -594,6 +595,34 @@ def run_kda(wl, device, pk, n_seqs=64, prefill_tokens=1024, steps=20, warmup=3):
                           "frac": gbs / pk["hbm_gbs"], "bound": "hbm"})
         else:
             entry["note"] = "token form: one token after another per (value head, column slice)"
+            # the training step of the same prefill: forward, then gdn_kda_backward
+            dO = rn(T, Hv * Dv, dt=td)
+            dS_T = rn(N, Hv, Dk, Dv) * 0.1
+            S0 = rn(N, Hv, Dk, Dv) * 0.1
+            dq, dk = torch.empty_like(q), torch.empty_like(k)
+            dv = torch.empty_like(v)
+            dalpha, dbeta = torch.empty_like(alpha), torch.empty_like(beta)
+            da_log, db_al = torch.empty_like(a_log), torch.empty_like(b_alpha)
+            dS0 = torch.empty_like(S0)
+            ws = torch.empty(gdn.gdn_kda_backward_workspace_bytes(shape), dtype=torch.uint8,
+                             device=device)
+            S_T = torch.empty_like(S0)
+
+            def train():
+                gdn.gdn_kda_forward(shape, q, k, v, alpha, beta, a_log, b_alpha, cu, S0, S_T, o)
+                gdn.gdn_kda_backward(shape, q, k, v, alpha, beta, a_log, b_alpha, cu, S0, dO,
+                                     dS_T, dq, dk, dv, dalpha, dbeta, da_log, db_al, dS0, ws)
+
+            train()
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(2):
+                train()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / 2
+            entry["training_step_ms"] = ms
+            entry["training_tokens_per_s"] = T / (ms * 1e-3)
         out[name] = entry
     return out
 

@@ -176,3 +176,19 @@ def test_backward_is_bit_reproducible():
     b = _run_bwd(torch, gdn, wl, inp, alpha, b_alpha, None)
     for key in a:
         assert np.array_equal(a[key], b[key]), key
+
+
+@pytest.mark.slow
+def test_backward_at_the_full_head_shape():
+    """16 key heads shared by 48 value heads of 128, bf16, two sequences (256 tokens: the
+    oracle's KDA backward keeps every state)."""
+    torch = pytest.importorskip("torch")
+    import gated_deltanet_backward_gb300 as gdn
+    wl, inp, alpha, b_alpha = _case("bf16", 16, 48, 128, 128, (100, 156), seed=23)
+    dS_T = (0.1 * np.random.default_rng(6).standard_normal(inp.S0.shape)).astype(np.float32)
+    got = _run_bwd(torch, gdn, wl, inp, alpha, b_alpha, dS_T)
+    ref = oracle.kda_backward(inp.q, inp.k, inp.v, alpha, inp.beta_raw, inp.a_log, b_alpha,
+                              inp.cu_seqlens, inp.dO, inp.S0, dS_T, Hk=16, Hv=48, Dk=128, Dv=128,
+                              scale=wl.scale_value())
+    for key in ("dq", "dk", "dv", "dalpha", "dbeta_raw", "da_log", "db_alpha", "dS0"):
+        assert rel_err(got[key], ref[key]) <= TOL["bf16"], key
