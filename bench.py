@@ -187,8 +187,8 @@ def kernel_models(wl: W.Workload):
 # from an ncu capture of this workload, with a hash of the sources it was built from;
 # a kernel whose sources changed since reports null (profiles/fused_kernels_l27b_bf16.md).
 NCU_TRAFFIC = {
-    ("gdn_fwd_fused_tc", "l27b_bf16"): (441.436672e6, "5267567a4d147c9a"),
-    ("gdn_bwd_fused_tc", "l27b_bf16"): (941.737728e6, "fd01625b7bbe0c71"),
+    ("gdn_fwd_fused_tc", "l27b_bf16"): (440.291072e6, "52e851de94be002f"),
+    ("gdn_bwd_fused_tc", "l27b_bf16"): (941.44896e6, "f42d443a5bb37b89"),
 }
 KERNEL_SOURCES = {
     "gdn_fwd_fused_tc": ("gdn_tc_fwd.cu", "gdn_tc.cuh", "umma.cuh", "gdn_device.cuh",
