@@ -127,3 +127,14 @@ def test_python_layer_holds_no_cpu_path():
     src = open(os.path.join(ROOT, "gated_deltanet_backward_gb300", "__init__.py")).read()
     assert "oracle" not in src.replace("no fallback", "")
     assert "torch.matmul" not in src and "einsum" not in src
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/gdn.h is a C header: a C99 translation unit that includes it and calls every
+    declared entry point through a function pointer compiles cleanly, pedantic."""
+    names = sorted(_declared())
+    src = tmp_path / "use_gdn.c"
+    body = "\n".join("  (void)&%s;" % n for n in names)
+    src.write_text('#include "gdn.h"\nint main(void) {\n%s\n  return 0;\n}\n' % body)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-fsyntax-only", "-I", os.path.join(ROOT, "include"), str(src)], check=True)
