@@ -281,6 +281,17 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (every rank calls it): the whole job is as slow as its
+    slowest rank."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -362,11 +373,7 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     f_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     b_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    step_ms = sum(f_ms[i] + b_ms[i] for i in range(K)) / K
-    if world > 1:
-        t = torch.tensor([step_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(sum(f_ms[i] + b_ms[i] for i in range(K)) / K, world, device)
     value = world * T / (step_ms * 1e-3)
 
     # per-kernel durations from the profiling hook
@@ -794,12 +801,7 @@ def run_e2e(args, inp, layer, device, tdt, world):
         fn(K)
         e1.record(s_down if first else torch.cuda.current_stream(device))
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / K
-        if world > 1:
-            t = torch.tensor([ms], device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        res[name] = ms
+        res[name] = max_over_ranks(e0.elapsed_time(e1) / K, world, device)
     assert gdn_status_ok(layer)
     ms = res["pipelined"]
     return {"value": world * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
