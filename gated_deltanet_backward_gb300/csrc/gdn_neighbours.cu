@@ -608,7 +608,7 @@ __global__ void __launch_bounds__(kNormThreads) k_norm_fwd(NormArgs a) {
 // grid-stride (a fixed grid), so each thread's d gamma share, and the block sum over its
 // row slots, have a fixed order.
 template <typename T, int LPR>
-__global__ void __launch_bounds__(kNormThreads) k_norm_bwd(NormArgs a) {
+__global__ void __launch_bounds__(kNormThreads, 4) k_norm_bwd(NormArgs a) {
   constexpr int V = kVec<T>, NI = kNormBwdNI, RPB = kNormThreads / LPR;
   __shared__ float red[RPB][LPR * V];
   const uint32_t HV = (uint32_t)a.H * LPR, nv = (uint32_t)a.T * HV;
