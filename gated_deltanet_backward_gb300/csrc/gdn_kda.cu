@@ -1,5 +1,5 @@
-// gdn_kda.cu -- the KDA variant's forward in token form: the recurrence with a decay gate
-// per key channel instead of one per head.  Channel c of value head h decays by
+// gdn_kda.cu -- the KDA variant in token form, forward and backward: the recurrence with a
+// decay gate per key channel instead of one per head.  Channel c of value head h decays by
 // g[c] = exp(-exp(a_log[h]) softplus(alpha[t, h*Dk + c] + b_alpha[h*Dk + c])) (the module
 // parameters a_log and b_alpha named on the dormouse "KDA attention arm" page), and the
 // forward recap's update (lattice-inference 0.6.0, src/attention/gdn_backward.rs) becomes
@@ -8,7 +8,8 @@
 // The state's value columns evolve independently, so one CTA owns (sequence, value head,
 // slice of VS columns) and walks the sequence's tokens in order with its [Dk][VS] slice in
 // shared memory.  A sequence of one token is a decode step; longer ones are a prefill in
-// token form (one token after another: latency-bound, not the chunked form).
+// token form (one token after another: latency-bound, not the chunked form).  The
+// backward (below) walks the same slices in reverse from states saved every few tokens.
 #include <cuda_bf16.h>
 
 #include "gdn_device.cuh"
