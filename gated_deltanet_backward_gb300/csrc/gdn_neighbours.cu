@@ -7,12 +7,13 @@
 //
 // Both stream their operands once: HBM-bound work on CUDA cores, with enough arithmetic
 // per byte (a sigmoid per element, up to a dozen FMAs) that the instruction count
-// matters too.  So every thread moves 16-byte vectors (8 bf16 or 4 fp32 channels), the
-// sigmoid is ex2.approx + rcp.approx (__expf, __fdividef), and index arithmetic is
-// 32-bit.  The conv stages token tiles of a channel slab in shared memory through a
-// multistage cp.async pipeline (a persistent block walks the tiles of its slab, two or
-// three tiles in flight while it computes one); the norm keeps 2-4 rows of loads in
-// flight per thread.  The weight gradients (dw of the conv, d gamma of the norm) are
+// matters too.  So the sigmoid is ex2.approx + rcp.approx, index arithmetic is 32-bit,
+// and rows whose windows lie inside one sequence take a branch-free path.  The conv
+// stages token tiles of channel slabs in shared memory through 16-byte cp.async copies
+// in a multistage ring (a persistent block walks a contiguous run of tiles, two or three
+// in flight while it computes one) and works on 4 channels a thread; the norm moves
+// 16-byte vectors (8 bf16 or 4 fp32 values) and keeps 2-4 rows of loads in flight per
+// thread.  The weight gradients (dw of the conv, d gamma of the norm) are
 // reduced in a fixed order -- per thread over its tokens, per block through shared
 // memory, then over blocks by a second small kernel -- so they are bit-reproducible run
 // to run.
