@@ -281,6 +281,17 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+def workload_config(wl, world):
+    """The `config` object both arms print for the workload (the reference arm adds its
+    per-step sample)."""
+    T, N = wl.total_tokens, wl.n_seqs
+    return {"workload": "%s: %d x %d tokens, Hk=%d, Hv=%d, Dk=%d, Dv=%d, %s q/k/v/o/dO, "
+                        "fp32 gates/state" % (wl.name, N, T // max(N, 1), wl.Hk, wl.Hv, wl.Dk,
+                                               wl.Dv, wl.dtype),
+            "tokens_per_gpu": T, "io_dtype": wl.dtype,
+            "parallelism": "independent batch per GPU" if world > 1 else "single GPU"}
+
+
 def max_over_ranks(x, world, device):
     """The largest of every rank's x (every rank calls it): the whole job is as slow as its
     slowest rank."""
@@ -410,16 +421,13 @@ def run_ours(args):
         "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": "%s: %d x %d tokens, Hk=%d, Hv=%d, Dk=%d, Dv=%d, %s q/k/v/o/dO, "
-                               "fp32 gates/state" % (wl.name, N, T // max(N, 1), Hk, Hv, Dk, Dv,
-                                                      wl.dtype),
-                   "tokens_per_gpu": T, "io_dtype": wl.dtype,
+        "config": {**workload_config(wl, world),
                    "compute": ("tcgen05 bf16 MMA, fp32 accumulate and state" if wl.dtype == "bf16"
                                else "fp32 CUDA-core FMA"),
                    "l2": "flushed between timed steps: 256 MB write, then 256 MB read",
                    "step": "training step: the forward keeps its chunk operands for the "
                            "backward (GDN_FLAG_KEEP_FOR_BACKWARD / GDN_FLAG_REUSE_FORWARD)",
-                   "parallelism": "independent batch per GPU" if world > 1 else "single GPU"},
+                   },
         "fwd_ms": sum(f_ms) / K, "bwd_ms": sum(b_ms) / K,
         "roofline": roof, "path_roofline": path_roof, "kernels": kernels,
         "gpu_launches": launches, "clocks": clocks, "e2e": e2e,
@@ -864,7 +872,9 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": wl.name, "tokens_per_step": tokens},
+        "config": {**workload_config(wl, world),
+                   "sample_tokens_per_step": tokens,
+                   "compute": "f64 token-by-token CPU oracle on the host cores"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.hardware_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
