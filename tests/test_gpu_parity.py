@@ -221,3 +221,21 @@ def test_modulo_head_map_against_the_oracle(dtype, kw):
     run.run_backward(train=False)
     compare(run.host(), oracle_outputs(inp), TOL[dtype],
             keys=["dq", "dk", "dv", "dalpha", "dbeta_raw", "da_log", "ddt_bias", "dS0"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_no_write_and_no_decay_leave_the_state_unchanged(dtype):
+    """beta = 0 (beta_raw = -1000) and g = 1 (alpha = -1000: softplus = 0): nothing is
+    written and nothing decays, so S_T is S_0 bit for bit and dv, d beta_raw are exactly
+    zero; o and the rest of the gradients still match the oracle (o = scale S_0^T q_hat)."""
+    wl = W.custom(dtype=dtype, Hk=2, Hv=4, Dk=64, Dv=64, seqlens=(100, 37), seed=29,
+                  S0_std=0.5, dST_std=0.3, dt_bias_std=0.0)
+    inp = W.generate(wl)
+    inp.beta_raw[:] = -1000.0
+    inp.alpha[:] = -1000.0
+    gpu = DeviceRun(inp).host()
+    assert np.array_equal(gpu["S_T"], inp.S0.astype(np.float64))
+    assert np.abs(gpu["dv"]).max() == 0.0 and np.abs(gpu["dbeta_raw"]).max() == 0.0
+    ref = oracle_outputs(inp)
+    for key in ("o", "dq", "dS0"):
+        assert rel_err(gpu[key], ref[key]) <= TOL[dtype], key
