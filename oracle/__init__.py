@@ -38,8 +38,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle shared library with the host C++ compiler."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp%d" % os.getpid()
-        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
-               "-ffp-contract=off", _SRC, "-o", tmp]
+        cmd = ["g++"] + compile_flags() + [_SRC, "-o", tmp]
         subprocess.check_call(cmd)
         os.replace(tmp, _LIB)
     return _LIB
@@ -63,19 +62,33 @@ class _Inputs(ctypes.Structure):
                 ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)), ("S0", _P)]
 
 
+def open_library(path: str):
+    """Load a build of ``gdn_oracle.cpp`` at ``path`` with the result types set.  The
+    planted-mistake tests load edited builds this way and put them in place of the
+    module's own library (``oracle._lib``) for the length of one test."""
+    lib = ctypes.CDLL(path)
+    lib.gdn_oracle_forward.restype = ctypes.c_int
+    lib.gdn_oracle_backward.restype = ctypes.c_int
+    lib.gdn_oracle_forward_states.restype = ctypes.c_int
+    lib.gdn_oracle_hardware_threads.restype = ctypes.c_int
+    lib.gdn_oracle_state_map.restype = ctypes.c_int
+    lib.gdn_oracle_kda_forward.restype = ctypes.c_int
+    lib.gdn_oracle_kda_backward.restype = ctypes.c_int
+    return lib
+
+
+def compile_flags() -> list:
+    """The host compiler flags every build of the oracle uses (strict IEEE f64: no fast
+    math, no contraction into fused multiply-adds)."""
+    return ["-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+            "-ffp-contract=off"]
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            lib.gdn_oracle_forward.restype = ctypes.c_int
-            lib.gdn_oracle_backward.restype = ctypes.c_int
-            lib.gdn_oracle_forward_states.restype = ctypes.c_int
-            lib.gdn_oracle_hardware_threads.restype = ctypes.c_int
-            lib.gdn_oracle_state_map.restype = ctypes.c_int
-            lib.gdn_oracle_kda_forward.restype = ctypes.c_int
-            lib.gdn_oracle_kda_backward.restype = ctypes.c_int
-            _lib = lib
+            _lib = open_library(build())
     return _lib
 
 
