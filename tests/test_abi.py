@@ -85,6 +85,12 @@ def _fwd_args(gdn, shape, **over):
             a["flags"], a["stream"]]
 
 
+def _device_visible():
+    import torch
+    return torch.cuda.is_available()
+
+
+@pytest.mark.skipif(_device_visible(), reason="fake device addresses: host-only machines")
 def test_forward_rejects_bad_arguments_before_launching(gdn):
     lib = gdn._lib
     s = gdn.make_shape(2, 6, 64, 64, 1, 2, 100, "f32")
