@@ -12,6 +12,9 @@ Contents
 * ``chunked.py``     -- an f64 numpy restatement of the 64-token chunked (WY/UT)
   algebra that the GPU path uses, derived from the same recurrence.  It is
   pinned against the token-by-token oracle, never the other way round.
+* ``chunked_kda.py`` -- the same chunked algebra for the KDA variant (a decay gate per
+  key channel), with the Gram products formed by blocks of rows so that no factor
+  overflows; pinned against the token-by-token KDA oracle.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test
 (finite differences, closed forms, invariants, brute force); see

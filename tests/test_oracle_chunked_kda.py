@@ -1,0 +1,113 @@
+"""The chunked restatement of the KDA variant (oracle/chunked_kda.py) against the
+token-by-token KDA oracle, in f64:
+
+* forward and backward agree with the token oracle for chunks of 1, 16 and 64 tokens,
+  ragged and empty sequences, both head maps, and Gram products formed whole or by
+  blocks of 4 and 16 rows;
+* with gates that differ strongly between channels (some channels lose 12 nats a token,
+  others 0.01), a 64-token chunk decays by more than the f64 range: the single-factor
+  product (K e^G)(K e^-G)^T overflows, while the blocked Gram product stays finite and
+  agrees with the pairwise definition and with the token oracle;
+* with the same gate on every channel of a head it equals the scalar-gate chunked
+  restatement (oracle/chunked.py), which is pinned on its own.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import chunked, chunked_kda
+
+
+def _inputs(seed, seqlens=(37, 0, 70), Hk=2, Hv=4, Dk=8, Dv=6, strong=False):
+    rng = np.random.default_rng(seed)
+    T = sum(seqlens)
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    d = dict(q=rng.standard_normal((T, Hk * Dk)), k=rng.standard_normal((T, Hk * Dk)),
+             v=rng.standard_normal((T, Hv * Dv)), alpha=rng.standard_normal((T, Hv * Dk)),
+             beta_raw=rng.standard_normal((T, Hv)), a_log=0.5 * rng.standard_normal(Hv),
+             b_alpha=0.3 * rng.standard_normal(Hv * Dk),
+             S0=0.5 * rng.standard_normal((len(seqlens), Hv, Dk, Dv)),
+             dO=rng.standard_normal((T, Hv * Dv)),
+             dS_T=rng.standard_normal((len(seqlens), Hv, Dk, Dv)))
+    if strong:
+        # even channels: softplus(12) ~ 12 nats a token; odd channels: ~0.01
+        d["a_log"][:] = 0.0
+        d["b_alpha"][:] = 0.0
+        x = d["alpha"].reshape(T, Hv, Dk)
+        x[:, :, 0::2] = 12.0 + 0.1 * x[:, :, 0::2]
+        x[:, :, 1::2] = np.log(np.expm1(0.01)) + 0.1 * x[:, :, 1::2]
+    return d, cu, dict(Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv)
+
+
+def _rel(a, b):
+    den = np.abs(b).max()
+    return np.abs(a - b).max() / (den if den > 0 else 1.0)
+
+
+def _token_fwd(d, cu, kw, head_map=0):
+    return oracle.kda_forward(d["q"], d["k"], d["v"], d["alpha"], d["beta_raw"], d["a_log"],
+                              d["b_alpha"], cu, d["S0"], head_map=head_map, **kw)
+
+
+def _token_bwd(d, cu, kw, head_map=0):
+    return oracle.kda_backward(d["q"], d["k"], d["v"], d["alpha"], d["beta_raw"], d["a_log"],
+                               d["b_alpha"], cu, d["dO"], d["S0"], d["dS_T"], head_map=head_map,
+                               **kw)
+
+
+@pytest.mark.parametrize("chunk,sub", [(1, None), (16, None), (16, 4), (64, None), (64, 16)])
+@pytest.mark.parametrize("head_map", [0, 1])
+def test_chunked_forward_equals_token_oracle(chunk, sub, head_map):
+    d, cu, kw = _inputs(1)
+    o, S_T = _token_fwd(d, cu, kw, head_map)
+    oc, Sc = chunked_kda.forward(d["q"], d["k"], d["v"], d["alpha"], d["beta_raw"], d["a_log"],
+                                 d["b_alpha"], cu, d["S0"], chunk=chunk, sub=sub,
+                                 head_map=head_map, **kw)
+    assert _rel(oc, o) < 1e-12 and _rel(Sc, S_T) < 1e-12
+
+
+@pytest.mark.parametrize("chunk,head_map", [(16, 0), (64, 0), (64, 1)])
+def test_chunked_backward_equals_token_oracle(chunk, head_map):
+    d, cu, kw = _inputs(2, seqlens=(21, 0, 40))
+    g = _token_bwd(d, cu, kw, head_map)
+    gc = chunked_kda.backward(d["q"], d["k"], d["v"], d["alpha"], d["beta_raw"], d["a_log"],
+                              d["b_alpha"], cu, d["dO"], d["S0"], d["dS_T"], chunk=chunk,
+                              head_map=head_map, **kw)
+    for key in g:
+        assert gc[key].shape == g[key].shape, key
+        assert _rel(gc[key], g[key]) < 1e-11, (key, _rel(gc[key], g[key]))
+
+
+def test_blocked_gram_stays_finite_where_one_factor_overflows():
+    d, cu, kw = _inputs(3, seqlens=(64,), Hk=1, Hv=1, strong=True)
+    Dk = kw["Dk"]
+    K, _ = chunked._l2(d["k"][:, :Dk])
+    b, _, l = chunked_kda._gates(d["alpha"][:, :Dk], d["beta_raw"][:, 0], d["a_log"][0],
+                                 d["b_alpha"][:Dk])
+    G = np.cumsum(l, 0)
+    assert -G.min() > 709.0                         # e^-G leaves the f64 range
+    with np.errstate(over="ignore", invalid="ignore"):
+        naive = np.tril((K * np.exp(G)) @ (K * np.exp(-G)).T, -1)
+    assert not np.isfinite(naive).all()
+    pair = chunked_kda.gram(K, K, G, strict=True)
+    blocked = chunked_kda.gram(K, K, G, strict=True, sub=16)
+    assert np.isfinite(blocked).all()
+    assert _rel(blocked, pair) < 1e-14
+    o, S_T = _token_fwd(d, cu, kw)
+    oc, Sc = chunked_kda.forward(d["q"], d["k"], d["v"], d["alpha"], d["beta_raw"], d["a_log"],
+                                 d["b_alpha"], cu, d["S0"], chunk=64, sub=16, **kw)
+    assert _rel(oc, o) < 1e-12 and _rel(Sc, S_T) < 1e-12
+
+
+def test_equal_channel_gates_equal_the_scalar_chunked_form():
+    d, cu, kw = _inputs(4, seqlens=(50, 13))
+    Hv, Dk = kw["Hv"], kw["Dk"]
+    rng = np.random.default_rng(9)
+    a_s = rng.standard_normal((int(cu[-1]), Hv))
+    dt = 0.3 * rng.standard_normal(Hv)
+    d["alpha"], d["b_alpha"] = np.repeat(a_s, Dk, axis=1), np.repeat(dt, Dk)
+    oc, Sc = chunked_kda.forward(d["q"], d["k"], d["v"], d["alpha"], d["beta_raw"], d["a_log"],
+                                 d["b_alpha"], cu, d["S0"], chunk=16, sub=4, **kw)
+    o, S = chunked.forward(d["q"], d["k"], d["v"], a_s, d["beta_raw"], d["a_log"], dt, cu,
+                           d["S0"], chunk=16, **kw)
+    assert _rel(oc, o) < 1e-12 and _rel(Sc, S) < 1e-12
