@@ -206,3 +206,44 @@ def backward(q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, dO, S0=None, 
                 out["dk"][t0:t1, sl_k] += (dK - K * (dK * K).sum(1, keepdims=True)) / nk
             out["dS0"][n, h] = dS
     return out
+
+
+# ---------------------------------------------------------------------------
+# Chunk maps.  A chunk maps its start state affinely to its end state,
+#   S_next = Phi S + R,  Phi = e^{G[c-1]} I - (diag(cdec) K)^T W  (Dk x Dk),
+#   R = (diag(cdec) K)^T U  (Dk x Dv),
+# both from the chunk's own inputs (the last line of the forward above with
+# Delta = U - W S expanded).  The reverse carry is affine with the transposed map:
+#   dS_prev = Phi^T dS + Gc,  Gc = scale Q^T diag(e^G) dO - W^T (scale P^T dO).
+# So the chunk-start states of a sequence are a prefix scan of the maps, which a
+# log-depth scan forms in ceil(log2 n) rounds instead of n dependent chunk steps.
+
+def chunk_map(Q, K, V, b, G, scale):
+    """(Phi, R) of one chunk."""
+    _, _, cache = chunk_forward(Q, K, V, b, G, np.zeros((K.shape[1], V.shape[1])), scale)
+    Kd = cache["cdec"][:, None] * K
+    Phi = np.exp(G[-1]) * np.eye(K.shape[1]) - Kd.T @ cache["W"]
+    return Phi, Kd.T @ cache["U"]
+
+
+def chunk_carry_term(Q, K, V, b, G, scale, dO):
+    """Gc of one chunk: the start-state gradient when the end-state gradient is zero."""
+    _, _, cache = chunk_forward(Q, K, V, b, G, np.zeros((K.shape[1], V.shape[1])), scale)
+    return scale * (Q.T @ (cache["eG"][:, None] * dO)) - cache["W"].T @ (scale * (cache["P"].T @ dO))
+
+
+def compose(later, earlier):
+    """The map of `earlier` followed by `later`: (P2, R2) o (P1, R1) = (P2 P1, P2 R1 + R2)."""
+    (P2, R2), (P1, R1) = later, earlier
+    return P2 @ P1, P2 @ R1 + R2
+
+
+def scan_start_states(maps, S0):
+    """State at the start of every chunk from the chunk maps, by a log-depth inclusive
+    scan (Hillis-Steele: in round j every prefix takes in the one 2^j chunks before it)."""
+    pre = list(maps)
+    step = 1
+    while step < len(pre):
+        pre = [pre[i] if i < step else compose(pre[i], pre[i - step]) for i in range(len(pre))]
+        step *= 2
+    return [S0] + [P @ S0 + R for P, R in pre[:-1]]

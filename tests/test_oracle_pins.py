@@ -381,3 +381,45 @@ def test_chunked_restatement_on_tiny_workload_with_chunk16():
     gc = chunked.backward(*args, inp.dO, inp.S0, inp.dS_T, chunk=16, **kw)
     for key in b:
         assert _rel(gc[key], b[key]) < 1e-11, key
+
+
+def test_chunk_maps_scan_to_the_token_oracles_chunk_states():
+    """Chunk maps (Phi, R) reproduce a chunk's end state from any start state; their
+    log-depth scan gives the token oracle's state at every chunk start; the transposed
+    maps carry dS back to the token oracle's dS_0."""
+    C = 16
+    wl, inp, a = _draw(1, 2, 8, 6, (75,), 101)
+    cu = inp.cu_seqlens
+    o, S_T, states = _fwd(wl, cu, a, chunk=C)
+    rng = np.random.default_rng(8)
+    dO = rng.standard_normal(o.shape)
+    dS_T = rng.standard_normal(S_T.shape)
+    g = _bwd(wl, cu, a, dO, dS_T)
+    scale = 1.0 / np.sqrt(8)
+    for h in range(2):
+        maps, carries = [], []
+        for t0 in range(0, 75, C):
+            t1 = min(t0 + C, 75)
+            Q, _ = chunked._l2(a["q"][t0:t1, :8])
+            K, _ = chunked._l2(a["k"][t0:t1, :8])
+            V = a["v"][t0:t1, h * 6:(h + 1) * 6]
+            b, _, l = chunked._gates(a["alpha"][t0:t1, h], a["beta_raw"][t0:t1, h],
+                                     a["a_log"][h], a["dt_bias"][h])
+            G = np.cumsum(l)
+            maps.append(chunked.chunk_map(Q, K, V, b, G, scale))
+            carries.append(chunked.chunk_carry_term(Q, K, V, b, G, scale,
+                                                    dO[t0:t1, h * 6:(h + 1) * 6]))
+            S = rng.standard_normal((8, 6))
+            _, S_next, _ = chunked.chunk_forward(Q, K, V, b, G, S, scale)
+            Phi, R = maps[-1]
+            assert _rel(Phi @ S + R, S_next) < 1e-13
+        starts = chunked.scan_start_states(maps, a["S0"][0, h])
+        assert len(starts) == len(maps) == states.shape[0]
+        for c, S in enumerate(starts):
+            assert _rel(S, states[c, h]) < 1e-12, c
+        Phi, R = maps[-1]
+        assert _rel(Phi @ starts[-1] + R, S_T[0, h]) < 1e-12
+        d = dS_T[0, h]
+        for (Phi, _), Gc in zip(reversed(maps), reversed(carries)):
+            d = Phi.T @ d + Gc
+        assert _rel(d, g["dS0"][0, h]) < 1e-12
