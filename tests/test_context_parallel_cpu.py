@@ -1,7 +1,8 @@
 """Context parallelism's host logic on the CPU: the orchestration of
 gated_deltanet_backward_gb300.context_parallel (segment maps, exchange, scans, final
 passes, the all-reduce of the shared-parameter gradients) driven by an oracle backend,
-in one process and as two gloo ranks, against the oracle run over the whole sequence.
+in one process and as two or four gloo ranks, against the oracle run over the whole
+sequence.
 The CUDA backend is checked on the GPU (tests/test_gpu_context.py)."""
 import os
 import socket
@@ -148,6 +149,8 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def test_two_gloo_ranks_with_two_segments_each_equal_the_whole_sequence():
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_ranks_holding_consecutive_segments_equal_the_whole_sequence(world):
+    """Two ranks with two segments each, and four ranks with one segment each."""
     import torch.multiprocessing as mp
-    mp.spawn(_rank_main, args=(2, _free_port()), nprocs=2, join=True)
+    mp.spawn(_rank_main, args=(world, _free_port()), nprocs=world, join=True)
