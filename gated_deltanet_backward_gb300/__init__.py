@@ -132,9 +132,10 @@ EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_for
 
 
 class GdnError(RuntimeError):
-    def __init__(self, code: int, where: str):
+    def __init__(self, code: int, where: str, detail: str = ""):
         self.code = code
-        detail = gdn_last_error() if code == -4 else ""
+        if not detail and code == -4:
+            detail = gdn_last_error()
         super().__init__("%s failed: %s (%d)%s" % (where, gdn_status_string(code), code,
                                                    (" -- " + detail) if detail else ""))
 
@@ -209,17 +210,148 @@ def _stream(stream) -> Optional[int]:
     return int(stream.cuda_stream)
 
 
+def _nbytes(t) -> int:
+    return 0 if t is None else int(t.numel() * t.element_size())
+
+
+F32, BF16, I32 = "torch.float32", "torch.bfloat16", "torch.int32"
+_TOKEN_DTYPE = {GDN_DTYPE_F32: F32, GDN_DTYPE_BF16: BF16}
+_TORCH = {}     # dtype name -> torch dtype, and whether CUDA is present (filled on first use)
+
+
+def _torch_state():
+    if not _TORCH:
+        import torch
+        _TORCH.update({F32: torch.float32, BF16: torch.bfloat16, I32: torch.int32,
+                       "cuda": torch.cuda.is_available(), "torch": torch})
+    return _TORCH
+
+
+class _Call:
+    """The tensors of one call, checked before any pointer reaches the library against
+    what the call will read and write: the dtype, at least the rows and columns (or the
+    elements, or the bytes) it touches, and then, after every size, that each tensor
+    lives on the current CUDA device.  The library sees only pointers and strides, so a
+    tensor that is too small, of another dtype or in host memory would otherwise be read
+    or written out of its bounds.  A failed check raises GdnError with
+    GDN_ERR_INVALID_ARG (GDN_ERR_UNSUPPORTED for an input dtype the library lacks) and
+    calls nothing; a None is left to the library's own checks."""
+
+    __slots__ = ("where", "tensors", "dt")
+
+    def __init__(self, where: str):
+        self.where = where
+        self.tensors = []
+        self.dt = _torch_state()
+
+    def fail(self, detail: str, code: int = -1):
+        raise GdnError(code, self.where, detail)
+
+    def _dtype(self, t, name, dtype):
+        if t.dtype is not self.dt[dtype]:
+            self.fail("%s is %s, expected %s" % (name, t.dtype, dtype[len("torch."):]))
+
+    def token_dtype(self, shape) -> str:
+        if int(shape.dtype) not in _TOKEN_DTYPE:
+            self.fail("shape.dtype %d is neither f32 nor bf16" % shape.dtype, -2)
+        return _TOKEN_DTYPE[int(shape.dtype)]
+
+    def io_dtype(self, t, name) -> str:
+        if t is None or (t.dtype is not self.dt[F32] and t.dtype is not self.dt[BF16]):
+            self.fail("%s must be a float32 or bfloat16 tensor" % name, -2)
+        return F32 if t.dtype is self.dt[F32] else BF16
+
+    def mat(self, t, name, rows, cols, dtype):
+        """(pointer, row stride in elements) of a 2-D tensor of at least [rows, cols]
+        with unit column stride; (None, 0) for None."""
+        if t is None:
+            return None, 0
+        self.tensors.append((name, t))
+        if t.dim() != 2:
+            self.fail("%s must be 2-D, got shape %s" % (name, tuple(t.shape)))
+        self._dtype(t, name, dtype)
+        r, w = t.shape
+        if r < rows or w < cols:
+            self.fail("%s is %s, needs at least [%d, %d]" % (name, tuple(t.shape), rows, cols))
+        s0, s1 = t.stride()
+        if r == 0 or w == 0:
+            return t.data_ptr(), max(s0, w)
+        if w > 1 and s1 != 1:
+            self.fail("%s needs contiguous columns (stride(1) == 1)" % name)
+        return t.data_ptr(), s0
+
+    def vec(self, t, name, numel, dtype):
+        """Pointer of a contiguous tensor of at least `numel` elements, or None."""
+        if t is None:
+            return None
+        self.tensors.append((name, t))
+        self._dtype(t, name, dtype)
+        if t.numel() < numel:
+            self.fail("%s has %d elements, needs at least %d" % (name, t.numel(), numel))
+        if not t.is_contiguous():
+            self.fail("%s must be contiguous" % name)
+        return t.data_ptr()
+
+    def buf(self, t, name, nbytes=0):
+        """Pointer of a contiguous buffer of at least `nbytes` bytes, or None."""
+        if t is None:
+            return None
+        self.tensors.append((name, t))
+        if _nbytes(t) < nbytes:
+            self.fail("%s has %d bytes, needs at least %d" % (name, _nbytes(t), nbytes))
+        if not t.is_contiguous():
+            self.fail("%s must be contiguous" % name)
+        return t.data_ptr()
+
+    def ready(self):
+        """Every tensor of the call on the current CUDA device (checked after the sizes)."""
+        if not self.tensors:
+            return
+        dev = self.dt["torch"].cuda.current_device() if self.dt["cuda"] else -2
+        for name, t in self.tensors:
+            if not t.is_cuda or t.get_device() != dev:
+                self.fail("%s is on %s, not on the current CUDA device" % (name, t.device))
+
+
+def _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, dt_bias, rows, gate_cols,
+                       tok):
+    """Arguments q, k, v, alpha, beta_raw (each with its row stride), a_log, dt_bias of
+    the recurrence's entry points (gate_cols: Hv, or Hv * Dk for the per-channel gate)."""
+    Hk, Hv, Dk, Dv = int(shape.Hk), int(shape.Hv), int(shape.Dk), int(shape.Dv)
+    args = []
+    args += c.mat(q, "q", rows, Hk * Dk, tok)
+    args += c.mat(k, "k", rows, Hk * Dk, tok)
+    args += c.mat(v, "v", rows, Hv * Dv, tok)
+    args += c.mat(alpha, "alpha", rows, gate_cols, F32)
+    args += c.mat(beta_raw, "beta_raw", rows, Hv, F32)
+    args += [c.vec(a_log, "a_log", Hv, F32),
+             c.vec(dt_bias, "dt_bias" if gate_cols == Hv else "b_alpha", gate_cols, F32)]
+    return args
+
+
+def _state_elems(shape) -> int:
+    return max(0, int(shape.n_seqs)) * max(0, int(shape.Hv)) * max(0, int(shape.Dk)) * \
+        max(0, int(shape.Dv))
+
+
 def gdn_forward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, chunk_offsets, S0,
                 o, S_T, saved_states, workspace, stream=None, flags=0) -> None:
     """Calls gdn_forward.  All tensors are CUDA tensors (S0 / S_T may be None).
     flags: 0 or GDN_FLAG_KEEP_FOR_BACKWARD (workspace then of the backward's size)."""
+    c = _Call("gdn_forward")
+    tok = c.token_dtype(shape)
+    T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
     args = [ctypes.byref(shape)]
-    for t in (q, k, v, alpha, beta_raw):
-        args += list(_mat(t))
-    args += [_ptr(a_log), _ptr(dt_bias), _ptr(cu_seqlens), _ptr(chunk_offsets), _ptr(S0)]
-    args += list(_mat(o))
-    args += [_ptr(S_T), _ptr(saved_states), _ptr(workspace),
-             int(workspace.numel() * workspace.element_size()), int(flags), _stream(stream)]
+    args += _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, dt_bias, T,
+                               int(shape.Hv), tok)
+    args += [c.vec(cu_seqlens, "cu_seqlens", N + 1, I32),
+             c.vec(chunk_offsets, "chunk_offsets", N + 1, I32), c.vec(S0, "S0", ns, F32)]
+    args += c.mat(o, "o", T, int(shape.Hv) * int(shape.Dv), tok)
+    args += [c.vec(S_T, "S_T", ns, F32),
+             c.buf(saved_states, "saved_states", gdn_saved_state_bytes(shape)),
+             c.buf(workspace, "workspace"), _nbytes(workspace), int(flags)]
+    c.ready()
+    args.append(_stream(stream))
     _check(_lib.gdn_forward(*args), "gdn_forward")
 
 
@@ -228,16 +360,27 @@ def gdn_backward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, ch
                  workspace, stream=None, flags=0) -> None:
     """Calls gdn_backward.  All tensors are CUDA tensors (S0, dS_T, dS0 may be None).
     flags: 0 or GDN_FLAG_REUSE_FORWARD (workspace then the one a keeping forward used)."""
+    c = _Call("gdn_backward")
+    tok = c.token_dtype(shape)
+    T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
+    Hv, wk, wv = int(shape.Hv), int(shape.Hk) * int(shape.Dk), int(shape.Hv) * int(shape.Dv)
     args = [ctypes.byref(shape)]
-    for t in (q, k, v, alpha, beta_raw):
-        args += list(_mat(t))
-    args += [_ptr(a_log), _ptr(dt_bias), _ptr(cu_seqlens), _ptr(chunk_offsets), _ptr(S0)]
-    args += list(_mat(dO))
-    args += [_ptr(dS_T), _ptr(saved_states)]
-    for t in (dq, dk, dv, dalpha, dbeta_raw):
-        args += list(_mat(t))
-    args += [_ptr(da_log), _ptr(ddt_bias), _ptr(dS0), _ptr(workspace),
-             int(workspace.numel() * workspace.element_size()), int(flags), _stream(stream)]
+    args += _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, dt_bias, T, Hv, tok)
+    args += [c.vec(cu_seqlens, "cu_seqlens", N + 1, I32),
+             c.vec(chunk_offsets, "chunk_offsets", N + 1, I32), c.vec(S0, "S0", ns, F32)]
+    args += c.mat(dO, "dO", T, wv, tok)
+    args += [c.vec(dS_T, "dS_T", ns, F32),
+             c.buf(saved_states, "saved_states", gdn_saved_state_bytes(shape))]
+    args += c.mat(dq, "dq", T, wk, tok)
+    args += c.mat(dk, "dk", T, wk, tok)
+    args += c.mat(dv, "dv", T, wv, tok)
+    args += c.mat(dalpha, "dalpha", T, Hv, F32)
+    args += c.mat(dbeta_raw, "dbeta_raw", T, Hv, F32)
+    args += [c.vec(da_log, "da_log", Hv, F32), c.vec(ddt_bias, "ddt_bias", Hv, F32),
+             c.vec(dS0, "dS0", ns, F32), c.buf(workspace, "workspace"), _nbytes(workspace),
+             int(flags)]
+    c.ready()
+    args.append(_stream(stream))
     _check(_lib.gdn_backward(*args), "gdn_backward")
 
 
@@ -245,12 +388,19 @@ def gdn_forward_noalloc(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seql
                         chunk_offsets, S0, o, S_T, saved_states, stream=None) -> None:
     """Calls gdn_forward_noalloc: the forward using the library's built-in scratch array
     instead of a caller workspace, for callers that cannot allocate device memory."""
+    c = _Call("gdn_forward_noalloc")
+    tok = c.token_dtype(shape)
+    T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
     args = [ctypes.byref(shape)]
-    for t in (q, k, v, alpha, beta_raw):
-        args += list(_mat(t))
-    args += [_ptr(a_log), _ptr(dt_bias), _ptr(cu_seqlens), _ptr(chunk_offsets), _ptr(S0)]
-    args += list(_mat(o))
-    args += [_ptr(S_T), _ptr(saved_states), _stream(stream)]
+    args += _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, dt_bias, T,
+                               int(shape.Hv), tok)
+    args += [c.vec(cu_seqlens, "cu_seqlens", N + 1, I32),
+             c.vec(chunk_offsets, "chunk_offsets", N + 1, I32), c.vec(S0, "S0", ns, F32)]
+    args += c.mat(o, "o", T, int(shape.Hv) * int(shape.Dv), tok)
+    args += [c.vec(S_T, "S_T", ns, F32),
+             c.buf(saved_states, "saved_states", gdn_saved_state_bytes(shape))]
+    c.ready()
+    args.append(_stream(stream))
     _check(_lib.gdn_forward_noalloc(*args), "gdn_forward_noalloc")
 
 
@@ -258,12 +408,16 @@ def gdn_decode_step(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, S_in, S_out
                     stream=None) -> None:
     """Calls gdn_decode_step: one new token per sequence (row n of q, k, v, alpha,
     beta_raw, o); the state goes from S_in (None = zero) to S_out (may be S_in)."""
+    c = _Call("gdn_decode_step")
+    tok = c.token_dtype(shape)
+    N, ns = int(shape.n_seqs), _state_elems(shape)
     args = [ctypes.byref(shape)]
-    for t in (q, k, v, alpha, beta_raw):
-        args += list(_mat(t))
-    args += [_ptr(a_log), _ptr(dt_bias), _ptr(S_in), _ptr(S_out)]
-    args += list(_mat(o))
-    args += [_stream(stream)]
+    args += _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, dt_bias, N,
+                               int(shape.Hv), tok)
+    args += [c.vec(S_in, "S_in", ns, F32), c.vec(S_out, "S_out", ns, F32)]
+    args += c.mat(o, "o", N, int(shape.Hv) * int(shape.Dv), tok)
+    c.ready()
+    args.append(_stream(stream))
     _check(_lib.gdn_decode_step(*args), "gdn_decode_step")
 
 
@@ -274,23 +428,31 @@ def _dtype_code(t) -> int:
     return 1 if name == "torch.bfloat16" else 0 if name == "torch.float32" else -1
 
 
-def _nbytes(t) -> int:
-    return 0 if t is None else int(t.numel() * t.element_size())
-
-
 def gdn_conv1d_silu_workspace_bytes(total_tokens: int, channels: int, kernel_size: int) -> int:
     return int(_lib.gdn_conv1d_silu_workspace_bytes(int(total_tokens), int(channels),
                                                     int(kernel_size)))
 
 
+def _conv_weights(c, w):
+    if w is None or w.dim() != 2:
+        c.fail("w must be a 2-D [channels, kernel_size] tensor")
+    return int(w.shape[0]), int(w.shape[1])
+
+
 def gdn_conv1d_silu_forward(x, w, cu_seqlens, y, stream=None) -> None:
     """Calls gdn_conv1d_silu_forward: x, y [T, C] (row strides taken from the tensors),
     w [C, K] fp32, cu_seqlens int32 [n_seqs + 1] on the device."""
-    C, K = int(w.shape[0]), int(w.shape[1])
-    xp, xld = _mat(x)
-    yp, yld = _mat(y)
-    _check(_lib.gdn_conv1d_silu_forward(_dtype_code(x), int(x.shape[0]), C, K, _ptr(cu_seqlens),
-                                        int(cu_seqlens.numel()) - 1, xp, xld, _ptr(w), yp, yld,
+    c = _Call("gdn_conv1d_silu_forward")
+    dt = c.io_dtype(x, "x")
+    C, K = _conv_weights(c, w)
+    T = int(x.shape[0]) if x.dim() else 0
+    xp, xld = c.mat(x, "x", T, C, dt)
+    wp = c.vec(w, "w", C * K, F32)
+    cp = c.vec(cu_seqlens, "cu_seqlens", 1, I32)
+    yp, yld = c.mat(y, "y", T, C, dt)
+    c.ready()
+    n = int(cu_seqlens.numel()) - 1 if cu_seqlens is not None else 0
+    _check(_lib.gdn_conv1d_silu_forward(_dtype_code(x), T, C, K, cp, n, xp, xld, wp, yp, yld,
                                         _stream(stream)), "gdn_conv1d_silu_forward")
 
 
@@ -298,14 +460,21 @@ def gdn_conv1d_silu_backward(x, w, cu_seqlens, dy, dx, dw=None, workspace=None,
                              stream=None) -> None:
     """Calls gdn_conv1d_silu_backward; dw (fp32 [C, K]) needs a workspace of
     gdn_conv1d_silu_workspace_bytes(T, C, K) bytes."""
-    C, K = int(w.shape[0]), int(w.shape[1])
-    xp, xld = _mat(x)
-    gp, gld = _mat(dy)
-    dp, dld = _mat(dx)
-    _check(_lib.gdn_conv1d_silu_backward(_dtype_code(x), int(x.shape[0]), C, K,
-                                         _ptr(cu_seqlens), int(cu_seqlens.numel()) - 1, xp, xld,
-                                         _ptr(w), gp, gld, dp, dld, _ptr(dw), _ptr(workspace),
-                                         _nbytes(workspace), _stream(stream)),
+    c = _Call("gdn_conv1d_silu_backward")
+    dt = c.io_dtype(x, "x")
+    C, K = _conv_weights(c, w)
+    T = int(x.shape[0]) if x.dim() else 0
+    xp, xld = c.mat(x, "x", T, C, dt)
+    wp = c.vec(w, "w", C * K, F32)
+    cp = c.vec(cu_seqlens, "cu_seqlens", 1, I32)
+    gp, gld = c.mat(dy, "dy", T, C, dt)
+    dp, dld = c.mat(dx, "dx", T, C, dt)
+    dwp = c.vec(dw, "dw", C * K, F32)
+    wsp = c.buf(workspace, "workspace")
+    c.ready()
+    n = int(cu_seqlens.numel()) - 1 if cu_seqlens is not None else 0
+    _check(_lib.gdn_conv1d_silu_backward(_dtype_code(x), T, C, K, cp, n, xp, xld, wp, gp, gld,
+                                         dp, dld, dwp, wsp, _nbytes(workspace), _stream(stream)),
            "gdn_conv1d_silu_backward")
 
 
@@ -313,15 +482,27 @@ def gdn_gated_rmsnorm_workspace_bytes(head_dim: int) -> int:
     return int(_lib.gdn_gated_rmsnorm_workspace_bytes(int(head_dim)))
 
 
+def _norm_dims(c, o, gamma):
+    if gamma is None or gamma.numel() == 0:
+        c.fail("gamma must hold head_dim > 0 elements")
+    if o.dim() != 2:
+        c.fail("o must be 2-D, got shape %s" % (tuple(o.shape),))
+    D = int(gamma.numel())
+    return int(o.shape[0]), int(o.shape[1]) // D, D
+
+
 def gdn_gated_rmsnorm_forward(o, z, gamma, y, eps, stream=None) -> None:
     """Calls gdn_gated_rmsnorm_forward: o, z, y [T, H*D] with D = gamma.numel()."""
-    D = int(gamma.numel())
-    H = int(o.shape[1]) // D
-    op, old = _mat(o)
-    zp, zld = _mat(z)
-    yp, yld = _mat(y)
-    _check(_lib.gdn_gated_rmsnorm_forward(_dtype_code(o), int(o.shape[0]), H, D, float(eps), op,
-                                          old, zp, zld, _ptr(gamma), yp, yld, _stream(stream)),
+    c = _Call("gdn_gated_rmsnorm_forward")
+    dt = c.io_dtype(o, "o")
+    T, H, D = _norm_dims(c, o, gamma)
+    op, old = c.mat(o, "o", T, H * D, dt)
+    zp, zld = c.mat(z, "z", T, H * D, dt)
+    gp = c.vec(gamma, "gamma", D, F32)
+    yp, yld = c.mat(y, "y", T, H * D, dt)
+    c.ready()
+    _check(_lib.gdn_gated_rmsnorm_forward(_dtype_code(o), T, H, D, float(eps), op, old, zp, zld,
+                                          gp, yp, yld, _stream(stream)),
            "gdn_gated_rmsnorm_forward")
 
 
@@ -329,40 +510,54 @@ def gdn_gated_rmsnorm_backward(o, z, gamma, dy, d_o, dz, eps, dgamma=None, works
                                stream=None) -> None:
     """Calls gdn_gated_rmsnorm_backward; dgamma (fp32 [D]) needs a workspace of
     gdn_gated_rmsnorm_workspace_bytes(D) bytes."""
-    D = int(gamma.numel())
-    H = int(o.shape[1]) // D
-    args = [_dtype_code(o), int(o.shape[0]), H, D, float(eps)]
-    for t in (o, z):
-        args += list(_mat(t))
-    args += [_ptr(gamma)]
-    for t in (dy, d_o, dz):
-        args += list(_mat(t))
-    args += [_ptr(dgamma), _ptr(workspace), _nbytes(workspace), _stream(stream)]
+    c = _Call("gdn_gated_rmsnorm_backward")
+    dt = c.io_dtype(o, "o")
+    T, H, D = _norm_dims(c, o, gamma)
+    args = [_dtype_code(o), T, H, D, float(eps)]
+    args += c.mat(o, "o", T, H * D, dt)
+    args += c.mat(z, "z", T, H * D, dt)
+    args += [c.vec(gamma, "gamma", D, F32)]
+    args += c.mat(dy, "dy", T, H * D, dt)
+    args += c.mat(d_o, "d_o", T, H * D, dt)
+    args += c.mat(dz, "dz", T, H * D, dt)
+    args += [c.vec(dgamma, "dgamma", D, F32), c.buf(workspace, "workspace"),
+             _nbytes(workspace)]
+    c.ready()
+    args.append(_stream(stream))
     _check(_lib.gdn_gated_rmsnorm_backward(*args), "gdn_gated_rmsnorm_backward")
 
 
 def gdn_state_compose(Phi, S, R, out, transpose=False, stream=None) -> None:
     """Calls gdn_state_compose: out[b] = op(Phi[b]) S[b] + R[b] over the leading blocks
     (Phi [..., Dk, Dk], S / R / out [..., Dk, Dv], fp32, contiguous; R may be None)."""
+    c = _Call("gdn_state_compose")
+    if S is None or S.dim() < 2:
+        c.fail("S must be a [..., Dk, Dv] tensor")
     Dk, Dv = int(S.shape[-2]), int(S.shape[-1])
     n = int(S.numel()) // (Dk * Dv) if S.numel() else 0
-    for t in (Phi, S, R, out):
-        if t is not None and not t.is_contiguous():
-            raise ValueError("gdn_state_compose needs contiguous tensors")
-    _check(_lib.gdn_state_compose(n, Dk, Dv, _ptr(Phi), _ptr(S), _ptr(R), _ptr(out),
-                                  1 if transpose else 0, _stream(stream)), "gdn_state_compose")
+    args = [n, Dk, Dv, c.vec(Phi, "Phi", n * Dk * Dk, F32), c.vec(S, "S", n * Dk * Dv, F32),
+            c.vec(R, "R", n * Dk * Dv, F32), c.vec(out, "out", n * Dk * Dv, F32),
+            1 if transpose else 0]
+    c.ready()
+    args.append(_stream(stream))
+    _check(_lib.gdn_state_compose(*args), "gdn_state_compose")
 
 
 def gdn_kda_forward(shape, q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens, S_in, S_out, o,
                     stream=None) -> None:
     """Calls gdn_kda_forward: the per-channel-gate variant in token form (alpha
     [T, Hv*Dk], b_alpha [Hv*Dk]); S_in None = zero, S_out may be S_in."""
+    c = _Call("gdn_kda_forward")
+    tok = c.token_dtype(shape)
+    T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
     args = [ctypes.byref(shape)]
-    for t in (q, k, v, alpha, beta_raw):
-        args += list(_mat(t))
-    args += [_ptr(a_log), _ptr(b_alpha), _ptr(cu_seqlens), _ptr(S_in), _ptr(S_out)]
-    args += list(_mat(o))
-    args += [_stream(stream)]
+    args += _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, b_alpha, T,
+                               int(shape.Hv) * int(shape.Dk), tok)
+    args += [c.vec(cu_seqlens, "cu_seqlens", N + 1, I32), c.vec(S_in, "S_in", ns, F32),
+             c.vec(S_out, "S_out", ns, F32)]
+    args += c.mat(o, "o", T, int(shape.Hv) * int(shape.Dv), tok)
+    c.ready()
+    args.append(_stream(stream))
     _check(_lib.gdn_kda_forward(*args), "gdn_kda_forward")
 
 
@@ -375,20 +570,35 @@ def gdn_kda_backward(shape, q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens
                      stream=None) -> None:
     """Calls gdn_kda_backward (S0, dS_T, dS0 may be None); workspace of
     gdn_kda_backward_workspace_bytes(shape) bytes."""
+    c = _Call("gdn_kda_backward")
+    tok = c.token_dtype(shape)
+    T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
+    Hv, Dk = int(shape.Hv), int(shape.Dk)
+    wk, wv = int(shape.Hk) * Dk, Hv * int(shape.Dv)
     args = [ctypes.byref(shape)]
-    for t in (q, k, v, alpha, beta_raw):
-        args += list(_mat(t))
-    args += [_ptr(a_log), _ptr(b_alpha), _ptr(cu_seqlens), _ptr(S0)]
-    args += list(_mat(dO)) + [_ptr(dS_T)]
-    for t in (dq, dk, dv, dalpha, dbeta_raw):
-        args += list(_mat(t))
-    args += [_ptr(da_log), _ptr(db_alpha), _ptr(dS0), _ptr(workspace), _nbytes(workspace),
-             _stream(stream)]
+    args += _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, b_alpha, T, Hv * Dk,
+                               tok)
+    args += [c.vec(cu_seqlens, "cu_seqlens", N + 1, I32), c.vec(S0, "S0", ns, F32)]
+    args += c.mat(dO, "dO", T, wv, tok)
+    args += [c.vec(dS_T, "dS_T", ns, F32)]
+    args += c.mat(dq, "dq", T, wk, tok)
+    args += c.mat(dk, "dk", T, wk, tok)
+    args += c.mat(dv, "dv", T, wv, tok)
+    args += c.mat(dalpha, "dalpha", T, Hv * Dk, F32)
+    args += c.mat(dbeta_raw, "dbeta_raw", T, Hv, F32)
+    args += [c.vec(da_log, "da_log", Hv, F32), c.vec(db_alpha, "db_alpha", Hv * Dk, F32),
+             c.vec(dS0, "dS0", ns, F32), c.buf(workspace, "workspace"), _nbytes(workspace)]
+    c.ready()
+    args.append(_stream(stream))
     _check(_lib.gdn_kda_backward(*args), "gdn_kda_backward")
 
 
 def gdn_read_device_status(workspace, stream=None) -> int:
-    return int(_lib.gdn_read_device_status(_ptr(workspace), _stream(stream)))
+    """Synchronises the stream and returns the status word of a workspace."""
+    c = _Call("gdn_read_device_status")
+    wp = c.buf(workspace, "workspace", 4)
+    c.ready()
+    return int(_lib.gdn_read_device_status(wp, _stream(stream)))
 
 
 def gdn_kernel_name(kernel_id: int) -> str:
