@@ -1,6 +1,6 @@
 """The C-ABI library on the host (no GPU needed): it builds, loads, exports every
-entry point declared in include/gdn.h, and rejects bad arguments before any
-launch.  No call here reaches a kernel."""
+entry point declared in include/gdn.h, links into a plain C program, and rejects bad
+arguments before any launch.  No call here reaches a kernel."""
 import ctypes
 import os
 import re
@@ -144,3 +144,38 @@ def test_header_is_plain_c(tmp_path):
     src.write_text('#include "gdn.h"\nint main(void) {\n%s\n  return 0;\n}\n' % body)
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
                     "-fsyntax-only", "-I", os.path.join(ROOT, "include"), str(src)], check=True)
+
+
+def test_a_c_program_plans_sizes_and_gets_refusals(gdn, tmp_path):
+    """A plain C99 program links libgdn.so and uses its host-only entry points: the chunk
+    plan of a varlen batch, the buffer sizes of the 27B-shaped layer, and a forward that
+    is refused before any launch (null q), with its status string."""
+    src = tmp_path / "plan.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "gdn.h"
+int main(void) {
+  const int32_t cu[5] = {0, 64, 64, 200, 201};
+  int32_t off[5], nc = -1;
+  if (gdn_plan(cu, 4, off, &nc) != GDN_OK) return 1;
+  printf("plan %d %d %d %d %d total %d\n", off[0], off[1], off[2], off[3], off[4], nc);
+  gdn_shape s = {16, 48, 128, 128, 1, 64, 4096, GDN_DTYPE_BF16, 0.0f,
+                 GDN_HEAD_MAP_CONSECUTIVE};
+  printf("saved %zu\n", gdn_saved_state_bytes(&s));
+  printf("ws %d\n", gdn_workspace_bytes(&s, 1) > gdn_workspace_bytes(&s, 0));
+  int rc = gdn_forward(&s, NULL, 10240, NULL, 10240, NULL, 10240, NULL, 48, NULL, 48, NULL,
+                       NULL, NULL, NULL, NULL, NULL, 6144, NULL, NULL, NULL, 0, 0u, NULL);
+  printf("forward %d %s\n", rc, gdn_status_string(rc));
+  return 0;
+}
+''')
+    exe = tmp_path / "plan"
+    libdir = os.path.dirname(gdn.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lgdn",
+                    "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert out[0] == "plan 0 1 1 4 5 total 5"
+    assert out[1] == "saved %d" % (64 * 48 * 128 * 128 * 2)
+    assert out[2] == "ws 1"
+    assert out[3] == "forward -1 GDN_ERR_INVALID_ARG"
