@@ -9,7 +9,10 @@ token-by-token KDA oracle, in f64:
   product (K e^G)(K e^-G)^T overflows, while the blocked Gram product stays finite and
   agrees with the pairwise definition and with the token oracle;
 * with the same gate on every channel of a head it equals the scalar-gate chunked
-  restatement (oracle/chunked.py), which is pinned on its own.
+  restatement (oracle/chunked.py), which is pinned on its own;
+* a design check for a tensor-core kernel: computed in fp32 with bf16 operands in every
+  product, the blocked form stays within 1e-2 (about 5e-3 measured) of the token oracle,
+  inside the 2e-2 bar of bf16 outputs.
 """
 import numpy as np
 import pytest
@@ -111,3 +114,73 @@ def test_equal_channel_gates_equal_the_scalar_chunked_form():
     o, S = chunked.forward(d["q"], d["k"], d["v"], a_s, d["beta_raw"], d["a_log"], dt, cu,
                            d["S0"], chunk=16, **kw)
     assert _rel(oc, o) < 1e-12 and _rel(Sc, S) < 1e-12
+
+
+def _bf16(x):
+    """Round to bfloat16 (nearest even), returned as float32."""
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32)
+
+
+def _blocked_forward_bf16_operands(d, cu, kw, chunk=64, sub=16):
+    """The blocked chunked forward with the arithmetic a tensor-core kernel would use: fp32
+    throughout, and every product (the off-diagonal Gram blocks, U, W, W S, Qg S, P Delta
+    and the state update) fed bf16-rounded operands with fp32 accumulation.  The
+    diagonal Gram blocks and the triangular solve stay fp32."""
+    f = lambda a: np.asarray(a, np.float32)
+
+    def gram(X, K, G, strict):
+        c = X.shape[0]
+        out = np.zeros((c, c), np.float32)
+        for a0 in range(0, c, sub):
+            a1 = min(a0 + sub, c)
+            for r in range(a0, a1):
+                for s in range(a0, r + (0 if strict else 1)):
+                    out[r, s] = (X[r] * K[s] * np.exp(G[r] - G[s])).sum(dtype=np.float32)
+            if a0 > 0:
+                out[a0:a1, :a0] = _bf16(X[a0:a1] * np.exp(G[a0:a1] - G[a0])) @ \
+                    _bf16(K[:a0] * np.exp(G[a0] - G[:a0])).T
+        return out
+
+    Hk, Hv, Dk, Dv = kw["Hk"], kw["Hv"], kw["Dk"], kw["Dv"]
+    scale = np.float32(1.0 / np.sqrt(Dk))
+    r = Hv // Hk
+    o = np.zeros((int(cu[-1]), Hv * Dv), np.float32)
+    S_T = np.zeros((len(cu) - 1, Hv, Dk, Dv), np.float32)
+    for n in range(len(cu) - 1):
+        for h in range(Hv):
+            sk = slice((h // r) * Dk, (h // r + 1) * Dk)
+            sv, sa = slice(h * Dv, (h + 1) * Dv), slice(h * Dk, (h + 1) * Dk)
+            S = f(d["S0"][n, h])
+            for t0 in range(int(cu[n]), int(cu[n + 1]), chunk):
+                t1 = min(t0 + chunk, int(cu[n + 1]))
+                Q, K = (f(chunked._l2(d[x][t0:t1, sk])[0]) for x in ("q", "k"))
+                b, _, l = chunked_kda._gates(d["alpha"][t0:t1, sa], d["beta_raw"][t0:t1, h],
+                                             d["a_log"][h], d["b_alpha"][sa])
+                b, G, V = f(b), f(np.cumsum(l, 0)), f(d["v"][t0:t1, sv])
+                c = t1 - t0
+                A = b[:, None] * gram(K, K, G, True)
+                T = f(np.linalg.solve(np.eye(c) + A, np.eye(c)))
+                eG = np.exp(G)
+                U = _bf16(T) @ _bf16(b[:, None] * V)
+                W = _bf16(T) @ _bf16(b[:, None] * K * eG)
+                Delta = U - _bf16(W) @ _bf16(S)
+                P = gram(Q, K, G, False)
+                o[t0:t1, sv] = scale * (_bf16(Q * eG) @ _bf16(S) + _bf16(P) @ _bf16(Delta))
+                S = np.exp(G[-1])[:, None] * S + _bf16(K * np.exp(G[-1] - G)).T @ _bf16(Delta)
+            S_T[n, h] = S
+    return o, S_T
+
+
+@pytest.mark.parametrize("strong", [False, True])
+def test_blocked_form_with_bf16_operands_stays_inside_the_bf16_bar(strong):
+    """Design check for a tensor-core chunked KDA: the blocked form, computed in fp32 with
+    bf16 operands in every product, stays well inside the bf16 bar (2e-2 of max|ref|) of
+    the f64 token oracle, for typical gates and for gates that decay 12 nats a token on
+    half the channels."""
+    d, cu, kw = _inputs(11, seqlens=(150, 41), Hk=1, Hv=2, Dk=32, Dv=32, strong=strong)
+    o, S_T = _token_fwd(d, cu, kw)
+    oc, Sc = _blocked_forward_bf16_operands(d, cu, kw)
+    assert np.isfinite(oc).all() and np.isfinite(Sc).all()
+    assert _rel(oc, o) < 1e-2 and _rel(Sc, S_T) < 1e-2
