@@ -14,8 +14,9 @@ is dS_in = Phi^T dS_out + G, G being dS_in when dS_out = 0.
 Forward:  every segment forms (Phi, R) on its own; the pairs are all-gathered; each worker
           scans them, S_in(s) = Phi(s-1) S_in(s-1) + R(s-1) from S_in(0) = S_0, and runs
           its segment's forward from S_in(s).
-Backward: every segment's backward with dS_out = 0 gives G(s); the G are all-gathered;
-          each worker scans in reverse, dS_out(s) = Phi(s+1)^T dS_out(s+1) + G(s+1) from
+Backward: every segment's backward with dS_out = 0 gives G(s); the G are all-gathered
+          (the maps are kept from the forward's exchange, not sent again); each worker
+          scans in reverse, dS_out(s) = Phi(s+1)^T dS_out(s+1) + G(s+1) from
           dS_out(last) = dS_T, and runs its segment's backward with dS_out(s).  d a_log and
           d dt_bias are sums over segments (an all-reduce); dS_0 is the first segment's.
 
@@ -99,7 +100,7 @@ def forward(ops, segments: Sequence[Segment], S0, group=None):
     outs, S_ins = [], []
     for j, seg in enumerate(segments):
         S_in = S_in_all[first + j]
-        seg.state["Phi"] = Phi_loc[j]
+        seg.state["Phis"] = Phis          # every segment's map, for the backward's scan
         o, _ = ops.forward(seg, S_in, keep=True)
         outs.append(o)
         S_ins.append(S_in)
@@ -115,7 +116,7 @@ def backward(ops, segments: Sequence[Segment], S_ins, dOs, dS_T, group=None):
     G_loc = [ops.backward(seg, S_in, dO, None)["dS0"]
              for seg, S_in, dO in zip(segments, S_ins, dOs)]
     Gs = group.all_gather(G_loc)
-    Phis = group.all_gather([seg.state["Phi"] for seg in segments])
+    Phis = segments[0].state["Phis"] if segments else []   # gathered by the forward
     first = _first_index(group, len(segments))
     n = len(Gs)
     dS_out = [None] * n
