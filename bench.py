@@ -78,13 +78,15 @@ def alu_fp32_tflops(sm_mhz):
 
 
 # ----------------------------------------------------------------------------
-# Algorithmic work model.  Path level: what the method must move / compute per
-# token (bf16 q/k/v/o/dO and their grads, fp32 gates, chunk-start states in the
-# input type, written once by the forward and read once by the backward).
-# Kernel level: each kernel's compulsory reads and writes of its own inputs and
-# outputs (workspace intermediates of this decomposition included), and the
-# multiply-add work of its contractions (2 FLOP per MAC; triangular products
-# counted at half).
+# Algorithmic work model of the method (the headline roofline).  Per token it counts
+# what the chunked method must move: the forward reads q, k, v, alpha, beta_raw and
+# writes o and the fp32 chunk-start states (Hv Dk Dv 4 bytes per chunk); the backward
+# reads q, k, v, alpha, beta_raw, dO and the states and writes dq, dk, dv, dalpha,
+# dbeta_raw.  S_0 / S_T / dS_T / dS_0 add N Hv Dk Dv 4 bytes each where present.
+# FLOPs are those of the chunked WY form (2 per multiply-add; triangular products at
+# half), the Gram products shared by the v_repeat value heads of a key head, and the
+# backward recomputing T, W, U and Delta.  The states count in fp32 whatever the
+# library keeps, so the fraction does not depend on that choice.
 # ----------------------------------------------------------------------------
 def path_model(wl: W.Workload):
     es = 2 if wl.dtype == "bf16" else 4
@@ -94,27 +96,42 @@ def path_model(wl: W.Workload):
     qk = 2 * Hk * Dk * es
     v = Hv * Dv * es
     gates = 2 * Hv * 4
-    states = NC * Hv * Dk * Dv * es          # chunk-start states, kept in the input type
+    states = NC * Hv * Dk * Dv * 4           # fp32 chunk-start states
     fwd = T * (qk + v + gates + v) + states
     bwd = T * (qk + v + gates + v) + states + T * (qk + v + gates)
     st = N * Hv * Dk * Dv * 4
     fwd += st * ((wl.S0_std > 0) + 1)
     bwd += st * ((wl.S0_std > 0) + (wl.dST_std > 0) + 1)
-    # chunked-method FLOPs per chunk and value head (Grams shared by the r heads)
+    # chunked-method FLOPs per chunk and value head; the Gram products K K^T and Q K^T
+    # are formed once per key head and shared by its r value heads
     gram = 2 * C * C * Dk / r
-    f_fwd = (gram + 2 * C * C * Dk + 2 * C * C * Dv + C ** 3 / 3 + 2 * C * Dk * Dv + gram +
-             2 * C * Dk * Dv + C * C * Dv + 2 * C * Dk * Dv)
-    f_bwd = (f_fwd - 2 * C * Dk * Dv - C * C * Dv  # recompute everything but O
-             + C * C * Dv + 2 * C * Dk * Dv + 4 * C * Dk * Dv  # dDelta, dS carry
-             + 2 * C * C * Dv + 4 * C * Dk * Dv + 4 * C * C * Dk  # dP, dQ, dK
-             + 4 * C * Dk * Dv + 2 * C * Dk * Dv  # (QS).dO, (K dS).Delta, dW
-             + 2 * C * C * (Dv + Dk) + 2 * C * C * (Dv + Dk) + 4 * C ** 3 + 4 * C * C * Dk)
-    flops = NC * Hv * (f_fwd + f_bwd)
-    return dict(bytes_fwd=fwd, bytes_bwd=bwd, bytes=fwd + bwd, flops=flops)
+    f_fwd = (2 * gram + C ** 3 / 3                    # K K^T, Q K^T; T = (I + A)^-1
+             + 2 * C * C * Dk + 2 * C * C * Dv        # W, U
+             + 2 * C * C * Dv + 6 * C * Dk * Dv)      # P Delta; W S, Q S, K^T Delta
+    f_bwd = (2 * gram + C ** 3 / 3 + 2 * C * C * (Dk + Dv) + 2 * C * Dk * Dv   # recompute
+             + 2 * C * C * Dv + 6 * C * Dk * Dv       # dDelta and the dS carry
+             + 6 * C * C * Dv + 12 * C * C * Dk + 6 * C * Dk * Dv + 4 * C ** 3)  # chunk VJP
+    return dict(bytes_fwd=fwd, bytes_bwd=bwd, bytes=fwd + bwd, flops_fwd=NC * Hv * f_fwd,
+                flops_bwd=NC * Hv * f_bwd, flops=NC * Hv * (f_fwd + f_bwd),
+                bytes_per_token=(fwd + bwd) / max(T, 1), flops_per_token=NC * Hv *
+                (f_fwd + f_bwd) / max(T, 1))
+
+
+# The kernels of each pass: a pass's algorithmic work (path_model) is what its kernels
+# do between them; a fused pass is one launch.
+FWD_KERNELS = ("gdn_fwd_fused_tc", "gdn_prep_tc", "gdn_prep_tc_full", "gdn_fwd_state_tc",
+               "gdn_prep", "gdn_fwd_state")
+BWD_KERNELS = ("gdn_bwd_fused_tc", "gdn_bwd_state_tc", "gdn_bwd_grads_tc", "gdn_bwd_state",
+               "gdn_bwd_grads", "gdn_bwd_qk", "gdn_bwd_gates")
 
 
 def kernel_models(wl: W.Workload):
-    """kernel name -> (algorithmic bytes per launch, FLOPs per launch, compute unit)."""
+    """kernel name -> (implementation bytes per launch, FLOPs per launch, compute unit).
+
+    Implementation bytes: each kernel's compulsory reads and writes of its own inputs
+    and outputs in this library's decomposition, workspace intermediates (the operand
+    tiles one kernel hands the next) included.  A diagnostic beside the measured DRAM
+    traffic, not the method's algorithmic work (path_model)."""
     es = 2 if wl.dtype == "bf16" else 4
     NC, N = wl.total_chunks, wl.n_seqs
     Hk, Hv, Dk, Dv, C = wl.Hk, wl.Hv, wl.Dk, wl.Dv, W.CHUNK
@@ -185,7 +202,7 @@ def kernel_models(wl: W.Workload):
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, one launch) of a kernel
 # from an ncu capture of this workload, with a hash of the sources it was built from;
-# a kernel whose sources changed since reports null (profiles/fused_kernels_l27b_bf16.md).
+# a kernel whose sources changed since the capture reports null.
 NCU_TRAFFIC = {
     ("gdn_fwd_fused_tc", "l27b_bf16"): (440.291072e6, "52e851de94be002f"),
     ("gdn_bwd_fused_tc", "l27b_bf16"): (941.44896e6, "f42d443a5bb37b89"),
@@ -211,8 +228,8 @@ def measured_traffic(kernel, workload):
 
 
 def kernel_roofline(b, f, unit, avg_s, pk):
-    """Roofline entry of one kernel: the roof (HBM bytes or FLOPs at the unit's peak)
-    that bounds its algorithmic work, and the achieved rate against it."""
+    """Per-kernel diagnostic: the roof (HBM bytes or FLOPs at the unit's peak) that bounds
+    the kernel's implementation bytes (kernel_models) and FLOPs, and the achieved rate."""
     peak_alu = alu_fp32_tflops(pk["sm_max_mhz"])
     t_mem = b / (pk["hbm_gbs"] * 1e9)
     peak_c = peak_alu if unit == "alu" else pk["bf16_tflops"]
@@ -225,9 +242,45 @@ def kernel_roofline(b, f, unit, avg_s, pk):
         roof = {"bound": "hbm", "achieved": b / avg_s / 1e9, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "peak_source": pk["source"] + " HBM"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
-    roof["algorithmic_bytes"] = b
-    roof["algorithmic_flops"] = f
+    roof["implementation_bytes"] = b
+    roof["flops"] = f
+    return roof
+
+
+def pass_roofline(per, steps, pm, pk, workload):
+    """Roofline entry of the dominant pass (forward or backward) of the step: its
+    algorithmic bytes and FLOPs (path_model, fp32 chunk-start states) over the average
+    per-step time of its kernels (the library's CUDA events on the launch stream).  A
+    fused pass is one launch, so this is that kernel's roofline; `traffic` is the ncu
+    DRAM bytes of the same launch when the capture matches the current sources."""
+    t_pass = {}
+    for which, names in (("forward", FWD_KERNELS), ("backward", BWD_KERNELS)):
+        t_pass[which] = sum(sum(per.get(n, [])) for n in names) * 1e-3 / steps
+    which = max(t_pass, key=t_pass.get)
+    names = FWD_KERNELS if which == "forward" else BWD_KERNELS
+    launched = [n for n in names if n in per]
+    dom = max(launched, key=lambda n: sum(per[n]))
+    b = pm["bytes_fwd" if which == "forward" else "bytes_bwd"]
+    f = pm["flops_fwd" if which == "forward" else "flops_bwd"]
+    t_mem, t_cmp = b / (pk["hbm_gbs"] * 1e9), f / (pk["bf16_tflops"] * 1e12)
+    t = t_pass[which]
+    if t_cmp > t_mem:
+        roof = {"bound": "tensor", "achieved": f / t / 1e12, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "peak_source": pk["source"] + " bf16 burst"}
+    else:
+        roof = {"bound": "hbm", "achieved": b / t / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "peak_source": pk["source"] + " HBM"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    fused = len(launched) == 1 or dom.endswith("_fused_tc")
+    traffic = measured_traffic(dom, workload) if fused else None
+    roof.update({
+        "traffic": traffic, "traffic_over_algorithmic": (traffic / b) if traffic else None,
+        "kernel": dom, "pass": which, "pass_kernels": launched,
+        "pass_us": t * 1e6, "algorithmic_bytes": b, "algorithmic_flops": f,
+        "tensor_frac": (f / t / 1e12) / pk["bf16_tflops"],
+        "model": "method bytes per token: q, k, v, alpha, beta_raw, o (forward), dO, dq, dk, "
+                 "dv, dalpha, dbeta_raw (backward) and fp32 chunk-start states written once "
+                 "and read once, plus the N Hv Dk Dv fp32 boundary states"})
     return roof
 
 
@@ -397,23 +450,22 @@ def run_ours(args):
                    "share": sum(v) / tot if tot else 0.0} for n, v in per.items()}
     pk = _peaks()
     models = kernel_models(wl)
-    dom = max(per, key=lambda n: sum(per[n]))
-    b, f, unit = models[dom]
-    avg_s = sum(per[dom]) / len(per[dom]) * 1e-3
-    roof = kernel_roofline(b, f, unit, avg_s, pk)
-    roof["kernel"] = dom
-    roof["traffic"] = measured_traffic(dom, wl.name)
+    pm = path_model(wl)
+    roof = pass_roofline(per, K, pm, pk, wl.name)
     for name in kernels:
         kb, kf, ku = models[name]
         r = kernel_roofline(kb, kf, ku, kernels[name]["avg_us"] * 1e-6, pk)
-        kernels[name].update(bound=r["bound"], frac=r["frac"])
-    pm = path_model(wl)
+        kernels[name].update(implementation_bytes=kb, implementation_frac=r["frac"],
+                             implementation_bound=r["bound"])
     t_roof = max(pm["bytes"] / (pk["hbm_gbs"] * 1e9), pm["flops"] / (pk["bf16_tflops"] * 1e12))
     path_roof = {"bytes_per_step": pm["bytes"], "flops_per_step": pm["flops"],
+                 "bytes_per_token": pm["bytes_per_token"],
+                 "flops_per_token": pm["flops_per_token"],
                  "roofline_us": t_roof * 1e6, "roofline_tokens_per_s": T / t_roof,
                  "frac": (T / (step_ms * 1e-3)) / (T / t_roof),
                  "bound": "hbm" if pm["bytes"] / (pk["hbm_gbs"] * 1e9) >= pm["flops"] / (
-                     pk["bf16_tflops"] * 1e12) else "tensor"}
+                     pk["bf16_tflops"] * 1e12) else "tensor",
+                 "peak_source": pk["source"]}
 
     e2e = run_e2e(args, inp, layer, device, tdt, world) if not args.no_e2e else None
     result = {
@@ -678,8 +730,8 @@ def run_context_parallel(wl, device, plain_step_ms, segments=4, steps=3, warmup=
         return e0.elapsed_time(e1) / n, out
 
     def step():
-        outs, S_T, S_ins = cp.forward(ops, segs, S0)
-        return cp.backward(ops, segs, S_ins, dOs, dS_T)
+        outs, S_T, ctx = cp.forward(ops, segs, S0)
+        return cp.backward(ops, segs, ctx, dOs, dS_T)
 
     step_ms, _ = timed(step, steps)
     if tokens:
@@ -823,30 +875,41 @@ def gdn_status_ok(layer):
     return gdn.gdn_read_device_status(layer.ws_bwd) == 0
 
 
-def _oracle_step(inp, tokens):
+def _oracle_step(inp, tokens, n_threads=0):
     import oracle
     wl = inp.wl
     cu = np.array([0, tokens], np.int32) if tokens < wl.total_tokens else inp.cu_seqlens
     sl = slice(0, tokens)
     S0 = inp.S0 if tokens >= wl.total_tokens else (None if inp.S0 is None else inp.S0[:1])
     dS_T = inp.dS_T if tokens >= wl.total_tokens else (None if inp.dS_T is None else inp.dS_T[:1])
-    kw = dict(Hk=wl.Hk, Hv=wl.Hv, Dk=wl.Dk, Dv=wl.Dv, scale=wl.scale_value())
+    kw = dict(Hk=wl.Hk, Hv=wl.Hv, Dk=wl.Dk, Dv=wl.Dv, scale=wl.scale_value(),
+              n_threads=n_threads)
     oracle.forward(inp.q[sl], inp.k[sl], inp.v[sl], inp.alpha[sl], inp.beta_raw[sl], inp.a_log,
                    inp.dt_bias, cu, S0, **kw)
     oracle.backward(inp.q[sl], inp.k[sl], inp.v[sl], inp.alpha[sl], inp.beta_raw[sl], inp.a_log,
                     inp.dt_bias, cu, inp.dO[sl], S0, dS_T, **kw)
 
 
-def cpu_baseline(wl, inp, tokens):
+def cpu_baseline(wl, inp, tokens, one_thread_tokens=256):
+    """The oracle (f64, token by token) on the host cores: the whole workload (up to
+    `tokens` tokens) on every hardware thread, and a shorter sample on one thread."""
     import oracle
     tokens = min(tokens, wl.total_tokens)
     t0 = time.perf_counter()
     _oracle_step(inp, tokens)
     dt = time.perf_counter() - t0
-    return {"value": tokens / dt, "unit": "tokens/s", "cores": oracle.hardware_threads(),
-            "kind": "oracle",
-            "sample": "f64 token-by-token forward + backward of the first %d tokens of %s "
-                      "(all %d value heads), one pass, %.1f s" % (tokens, wl.name, wl.Hv, dt)}
+    out = {"value": tokens / dt, "unit": "tokens/s", "cores": oracle.hardware_threads(),
+           "kind": "oracle",
+           "sample": "f64 token-by-token forward + backward of the first %d tokens of %s "
+                     "(all %d value heads), one pass, %.1f s" % (tokens, wl.name, wl.Hv, dt)}
+    n1 = min(one_thread_tokens, wl.total_tokens)
+    if n1 > 0:
+        t0 = time.perf_counter()
+        _oracle_step(inp, n1, n_threads=1)
+        dt1 = time.perf_counter() - t0
+        out["one_thread"] = {"value": n1 / dt1, "unit": "tokens/s", "cores": 1,
+                             "sample": "the first %d tokens, one pass, %.1f s" % (n1, dt1)}
+    return out
 
 
 def run_reference(args):
@@ -865,8 +928,9 @@ def run_reference(args):
         _oracle_step(inp, tokens)
     dt = (time.perf_counter() - t0) / args.steps
     value = tokens / dt
-    sample = ("f64 token-by-token CPU oracle, forward + backward of the first %d tokens of %s "
-              "(all %d value heads) per step" % (tokens, wl.name, wl.Hv))
+    sample = ("f64 token-by-token CPU oracle, forward + backward of %s of %s (all %d value "
+              "heads) per step" % ("all %d tokens" % tokens if tokens == wl.total_tokens else
+                                   "the first %d tokens" % tokens, wl.name, wl.Hv))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
@@ -890,7 +954,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="l27b_bf16", choices=sorted(W.WORKLOADS))
     ap.add_argument("--cpu-tokens", type=int, default=4096)
-    ap.add_argument("--ref-tokens", type=int, default=512)
+    ap.add_argument("--ref-tokens", type=int, default=4096)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")

@@ -76,5 +76,33 @@ def build(verbose: bool = False, extra_flags=(), force: bool = False) -> str:
     return OUT
 
 
+def build_variant(out_path: str, defines, sources=("gdn_tc_fwd.cu", "gdn_tc_bwd.cu"),
+                  verbose: bool = False) -> str:
+    """A second copy of the library at out_path whose `sources` are compiled with extra
+    preprocessor definitions (e.g. {"GDN_FLAG_WAIT_LIMIT_NS": 0}); the other translation
+    units are the regular build's objects.  Builds the regular library first."""
+    build(verbose=verbose)
+    nvcc = _nvcc()
+    work = os.path.dirname(os.path.abspath(out_path))
+    os.makedirs(work, exist_ok=True)
+    dflags = ["-D%s=%s" % (k, v) for k, v in sorted(dict(defines).items())]
+    objs = []
+    for src in SOURCES:
+        if src in sources:
+            o = os.path.join(work, src.replace(".cu", ".variant.o"))
+            cmd = [nvcc] + _flags(dflags) + ["-c", os.path.join(CSRC, src), "-o", o]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError("nvcc failed:\n%s\n%s%s" % (" ".join(cmd), r.stdout, r.stderr))
+            objs.append(o)
+        else:
+            objs.append(os.path.join(OBJ, src.replace(".cu", ".o")))
+    cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", out_path] + objs
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s\n%s%s" % (" ".join(cmd), r.stdout, r.stderr))
+    return out_path
+
+
 if __name__ == "__main__":
     print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))

@@ -76,6 +76,15 @@ class TorchGroup:
         return x
 
 
+@dataclass
+class ForwardContext:
+    """What forward() hands the backward() of the same segments: each local segment's
+    start state and every segment's map, gathered once by the forward."""
+    S_ins: List[Any]
+    Phis: List[Any]
+    n_local: int
+
+
 def _first_index(group, n_local: int) -> int:
     if isinstance(group, TorchGroup):
         return group.dist.get_rank(group.group) * n_local
@@ -83,8 +92,8 @@ def _first_index(group, n_local: int) -> int:
 
 
 def forward(ops, segments: Sequence[Segment], S0, group=None):
-    """Returns ([o of each local segment], S_T of the whole sequence, [S_in of each local
-    segment]).  S0: [1, Hv, Dk, Dv] start state or None (zero)."""
+    """Returns ([o of each local segment], S_T of the whole sequence, a ForwardContext for
+    the backward of the same segments).  S0: [1, Hv, Dk, Dv] start state or None (zero)."""
     group = group or LocalGroup()
     Phi_loc, R_loc = [], []
     for seg in segments:
@@ -100,23 +109,27 @@ def forward(ops, segments: Sequence[Segment], S0, group=None):
     outs, S_ins = [], []
     for j, seg in enumerate(segments):
         S_in = S_in_all[first + j]
-        seg.state["Phis"] = Phis          # every segment's map, for the backward's scan
         o, _ = ops.forward(seg, S_in, keep=True)
         outs.append(o)
         S_ins.append(S_in)
-    return outs, S, S_ins
+    return outs, S, ForwardContext(S_ins, list(Phis), len(segments))
 
 
-def backward(ops, segments: Sequence[Segment], S_ins, dOs, dS_T, group=None):
+def backward(ops, segments: Sequence[Segment], ctx: ForwardContext, dOs, dS_T, group=None):
     """Gradients of every local segment (dict per segment: dq, dk, dv, dalpha, dbeta_raw)
     and of the shared parameters summed over all segments (da_log, ddt_bias), plus dS_0
-    (of the first segment; None on ranks that do not hold it).  Needs the forward() of the
-    same segments just before (its kept state)."""
+    (of the first segment; None on ranks that do not hold it).  `ctx` is what forward()
+    returned for the same segments, run just before (the backend keeps its state)."""
     group = group or LocalGroup()
+    if ctx.n_local != len(segments) or len(dOs) != len(segments):
+        raise ValueError("backward: %d segments and %d dO for a forward of %d segments"
+                         % (len(segments), len(dOs), ctx.n_local))
+    S_ins, Phis = ctx.S_ins, ctx.Phis
     G_loc = [ops.backward(seg, S_in, dO, None)["dS0"]
              for seg, S_in, dO in zip(segments, S_ins, dOs)]
     Gs = group.all_gather(G_loc)
-    Phis = segments[0].state["Phis"] if segments else []   # gathered by the forward
+    if len(Phis) != len(Gs):
+        raise ValueError("backward: %d gathered maps for %d segments" % (len(Phis), len(Gs)))
     first = _first_index(group, len(segments))
     n = len(Gs)
     dS_out = [None] * n

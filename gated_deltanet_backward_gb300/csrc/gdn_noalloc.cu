@@ -23,19 +23,29 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
-int scratch_address(void** out) {
+// Device address of the scratch on the current device.  Outside stream capture it is
+// looked up again on every call (cudaGetSymbolAddress, with that device current): a
+// device reset reloads the module and another context of the same device maps the
+// array elsewhere, so an address kept from an earlier call can be stale.  While
+// `stream` is capturing, the address of this device's last call outside capture is
+// used (a symbol lookup can load the module, which capture does not allow); a first
+// call on a device inside capture is refused.
+int scratch_address(cudaStream_t stream, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return GDN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess || p == nullptr) return GDN_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+  } else if (!g_scratch_ptr[dev]) {
+    return GDN_ERR_UNSUPPORTED;
   }
   *out = g_scratch_ptr[dev];
   return GDN_OK;
@@ -66,9 +76,12 @@ extern "C" int gdn_forward_noalloc(const gdn_shape* s, const void* q, int64_t q_
     return GDN_ERR_WORKSPACE;
   }
   void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
+  const int rc = scratch_address((cudaStream_t)stream, &scratch);
   if (rc != GDN_OK) {
-    gdn::set_last_error("gdn_forward_noalloc: cudaGetSymbolAddress of the scratch failed");
+    gdn::set_last_error(rc == GDN_ERR_UNSUPPORTED
+                            ? "gdn_forward_noalloc: first call on this device inside a stream "
+                              "capture (call it once outside capture first)"
+                            : "gdn_forward_noalloc: cudaGetSymbolAddress of the scratch failed");
     return rc;
   }
   // The scratch's status word is cleared by gdn_forward itself; every other

@@ -62,7 +62,14 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* flag) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
   return v;
 }
-// One thread: true once *flag is set; false if it is still clear after 2 s.
+// How long a wait on another CTA's readiness flag may take before it gives up and
+// records GDN_ERR_TIMEOUT (wall time, ns).  A build with 0 makes every wait that is not
+// satisfied at once run out, which is how the failure path is tested.
+#ifndef GDN_FLAG_WAIT_LIMIT_NS
+#define GDN_FLAG_WAIT_LIMIT_NS 2000000000ull
+#endif
+// One thread: true once *flag is set; false if it is still clear after
+// GDN_FLAG_WAIT_LIMIT_NS (2 s).
 __device__ __forceinline__ bool flag_ready(const uint32_t* flag) {
   return ld_acquire(flag) != 0u;
 }
@@ -72,7 +79,7 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag) {
     const uint64_t t0 = tc::globaltimer_ns();
     while (!(ok = flag_ready(flag))) {
       __nanosleep(128);
-      if (tc::globaltimer_ns() - t0 > 2000000000ull) break;
+      if (tc::globaltimer_ns() - t0 > (uint64_t)(GDN_FLAG_WAIT_LIMIT_NS)) break;
     }
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");

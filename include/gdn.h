@@ -215,9 +215,13 @@ int gdn_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void
  *  - Shapes whose gdn_workspace_bytes(shape, 0) exceeds GDN_NOALLOC_SCRATCH_BYTES
  *    are rejected with GDN_ERR_WORKSPACE before anything is launched
  *    (gdn_last_error() says why); use gdn_forward with a caller workspace.
- *  - The first call on a device looks up the scratch's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make that
- *    first call before any stream capture.
+ *  - The scratch's device address is looked up (cudaGetSymbolAddress, with the
+ *    calling device current) on every call made outside stream capture, so a
+ *    device reset or another context of the device does not leave a stale
+ *    address behind.  A call on a capturing stream reuses the address of that
+ *    device's last call outside capture: make the first call on each device
+ *    before any stream capture (a first call inside capture returns
+ *    GDN_ERR_UNSUPPORTED), and repeat one outside capture after a device reset.
  *  - All calls on a device share the one scratch array, which keeps the last
  *    call's contents (each call clears what must start at zero).  Calls whose
  *    work overlaps on the GPU (concurrent streams, or host threads) race on it:

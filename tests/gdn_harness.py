@@ -63,13 +63,25 @@ class DeviceRun:
         self.o = torch.full((T, Hv * Dv), float("nan"), device=device, dtype=self.tdtype)
         self.S_T = torch.full((N, Hv, Dk, Dv), float("nan"), device=device)
         self.train = train
-        self.layer.forward(self.q, self.k, self.v, self.alpha, self.beta_raw, self.a_log,
-                           self.dt_bias, self.S0, self.o, self.S_T, train=train)
-        # a training step's backward shares the forward's workspace (and status word)
-        self.fwd_status = gdn.gdn_read_device_status(self.layer.ws_bwd) if train else None
         self.grads = None
+        self.run_forward()
         if run_backward:
             self.run_backward()
+
+    def run_forward(self):
+        """The forward again on the same inputs, into the same o, S_T and saved states."""
+        import gated_deltanet_backward_gb300 as gdn
+        self.layer.forward(self.q, self.k, self.v, self.alpha, self.beta_raw, self.a_log,
+                           self.dt_bias, self.S0, self.o, self.S_T, train=self.train)
+        # a training step's backward shares the forward's workspace (and status word)
+        self.fwd_status = gdn.gdn_read_device_status(self.layer.ws_bwd) if self.train else None
+
+    def device_outputs(self) -> dict:
+        """Every output of the last forward (and backward) as device tensors."""
+        out = dict(o=self.o, S_T=self.S_T, saved=self.layer.saved_states)
+        if self.grads is not None:
+            out.update(self.grads)
+        return out
 
     def run_backward(self, train=None):
         import torch
@@ -132,26 +144,28 @@ def saved_states_dense(saved, wl: W.Workload) -> np.ndarray:
     return st.transpose(0, 1, 3, 2)
 
 
-def head_group_inputs(inp: W.Inputs, kh: int) -> W.Inputs:
-    """The inputs of key head kh and its v_repeat value heads, as a stand-alone draw
-    (heads are independent, so the oracle can check one group of a large batch)."""
+def head_group_inputs(inp: W.Inputs, kh: int, count: int = 1) -> W.Inputs:
+    """The inputs of key heads kh .. kh + count - 1 and their v_repeat value heads each, as
+    a stand-alone draw (heads are independent, so the oracle can check some groups of a
+    large batch)."""
     wl = inp.wl
     r, Dk, Dv = wl.v_repeat, wl.Dk, wl.Dv
-    hs = slice(kh * r, (kh + 1) * r)
-    sub = W.replace(wl, Hk=1, Hv=r, name=wl.name + "_kh%d" % kh)
+    hs = slice(kh * r, (kh + count) * r)
+    sub = W.replace(wl, Hk=count, Hv=r * count, name=wl.name + "_kh%d+%d" % (kh, count))
     return W.Inputs(sub, inp.cu_seqlens, None,
-                    inp.q[:, kh * Dk:(kh + 1) * Dk], inp.k[:, kh * Dk:(kh + 1) * Dk],
-                    inp.v[:, kh * r * Dv:(kh + 1) * r * Dv], inp.alpha[:, hs], inp.beta_raw[:, hs],
-                    inp.a_log[hs], inp.dt_bias[hs], None if inp.S0 is None else inp.S0[:, hs],
-                    inp.dO[:, kh * r * Dv:(kh + 1) * r * Dv],
+                    inp.q[:, kh * Dk:(kh + count) * Dk], inp.k[:, kh * Dk:(kh + count) * Dk],
+                    inp.v[:, kh * r * Dv:(kh + count) * r * Dv], inp.alpha[:, hs],
+                    inp.beta_raw[:, hs], inp.a_log[hs], inp.dt_bias[hs],
+                    None if inp.S0 is None else inp.S0[:, hs],
+                    inp.dO[:, kh * r * Dv:(kh + count) * r * Dv],
                     None if inp.dS_T is None else inp.dS_T[:, hs])
 
 
-def head_group_outputs(out: dict, wl: W.Workload, kh: int) -> dict:
+def head_group_outputs(out: dict, wl: W.Workload, kh: int, count: int = 1) -> dict:
     r, Dk, Dv = wl.v_repeat, wl.Dk, wl.Dv
-    hs = slice(kh * r, (kh + 1) * r)
-    vs = slice(kh * r * Dv, (kh + 1) * r * Dv)
-    ks = slice(kh * Dk, (kh + 1) * Dk)
+    hs = slice(kh * r, (kh + count) * r)
+    vs = slice(kh * r * Dv, (kh + count) * r * Dv)
+    ks = slice(kh * Dk, (kh + count) * Dk)
     sel = dict(o=out["o"][:, vs], S_T=out["S_T"][:, hs], saved=out["saved"][:, hs])
     if "dq" in out:
         sel.update(dq=out["dq"][:, ks], dk=out["dk"][:, ks], dv=out["dv"][:, vs],

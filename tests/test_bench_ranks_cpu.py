@@ -41,7 +41,8 @@ def test_step_time_is_the_slowest_ranks():
 def test_reference_arm_prints_on_rank_zero_only():
     env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1")
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--steps", "1", "--warmup", "0"], cwd=ROOT, env=env,
+                          "--steps", "1", "--warmup", "0", "--ref-tokens", "512"], cwd=ROOT,
+                         env=env,
                          capture_output=True, text=True, timeout=300)
     assert out.returncode == 0, out.stderr[-500:]
     assert out.stdout.strip() == ""
@@ -53,7 +54,7 @@ def test_reference_arm_line_keeps_the_contract():
     import json
     env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--steps", "1", "--warmup", "3"], cwd=ROOT, env=env,
+                          "--steps", "1", "--warmup", "3", "--ref-tokens", "512"], cwd=ROOT, env=env,
                          capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-500:]
     lines = [l for l in out.stdout.splitlines() if l.strip()]

@@ -105,9 +105,9 @@ def _run_and_check(cp, group, which, wl, inp, dS_T, L):
     ops = OracleSegmentOps(wl.Hk, wl.Hv, wl.Dk, wl.Dv, wl.scale_value())
     segs, bounds = _segments(cp, inp, L, which)
     f = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
-    outs, S_T, S_ins = cp.forward(ops, segs, f(inp.S0), group)
+    outs, S_T, ctx = cp.forward(ops, segs, f(inp.S0), group)
     dOs = [f(inp.dO[bounds[s]:bounds[s + 1]]) for s in which]
-    grads, da_log, ddt, dS0 = cp.backward(ops, segs, S_ins, dOs, f(dS_T), group)
+    grads, da_log, ddt, dS0 = cp.backward(ops, segs, ctx, dOs, f(dS_T), group)
     o_ref, S_ref, g_ref = _whole(wl, inp, dS_T)
     tol = dict(rtol=0, atol=1e-10)
     assert np.allclose(S_T.numpy(), S_ref, **tol)

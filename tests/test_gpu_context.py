@@ -75,8 +75,8 @@ def test_segments_equal_the_whole_sequence(dtype, L):
                                _dev(torch, inp.beta_raw[r]), a_log, dt_bias))
         dOs.append(_dev(torch, inp.dO[r], td))
     ops = cp.GpuSegmentOps(Hk, Hv, D, D, dtype, wl.scale_value())
-    outs, S_T, S_ins = cp.forward(ops, segs, _dev(torch, inp.S0))
-    grads, da_log, ddt, dS0 = cp.backward(ops, segs, S_ins, dOs, _dev(torch, dS_T))
+    outs, S_T, ctx = cp.forward(ops, segs, _dev(torch, inp.S0))
+    grads, da_log, ddt, dS0 = cp.backward(ops, segs, ctx, dOs, _dev(torch, dS_T))
     torch.cuda.synchronize()
     cat = lambda key: np.concatenate([g[key].float().cpu().numpy() for g in grads])
     tol = TOL[dtype]

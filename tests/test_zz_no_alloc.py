@@ -5,7 +5,8 @@ a plugin host that passes only inputs and outputs, a path that cannot take the
 implicit synchronisation of cudaMalloc / cudaFree) use this entry point; it runs
 the forward with the library's built-in 64 MiB scratch array instead of a caller
 workspace.  These tests call it through the C ABI twice in a row and compare
-every output with the regular gdn_forward (same tolerance as the parity tests),
+every output with the regular gdn_forward (same tolerance as the parity tests, and
+bit for bit, since both run the same kernels),
 and check that a shape needing more scratch is refused before any launch.
 
 This file sorts last so that a run stopping at its first failure has already run
@@ -38,7 +39,8 @@ def test_noalloc_forward_matches_the_workspace_forward(torch_cuda, wl):
     torch = torch_cuda
     import gated_deltanet_backward_gb300 as gdn
     inp = W.generate(wl)
-    run = DeviceRun(inp, run_backward=False)          # gdn_forward with a workspace
+    # gdn_forward with a caller workspace and no flags: the same kernels as the no-alloc call
+    run = DeviceRun(inp, run_backward=False, train=False)
     ref = run.host()
     nsaved = wl.total_chunks * wl.Hv * wl.Dk * wl.Dv
     for call in range(2):
@@ -59,6 +61,8 @@ def test_noalloc_forward_matches_the_workspace_forward(torch_cuda, wl):
         for key in got:
             assert np.all(np.isfinite(got[key])), (call, key)
             assert rel_err(got[key], ref[key]) <= TOL[wl.dtype], (call, key)
+            # both calls run the same kernels on the same inputs: the same bits
+            assert np.array_equal(got[key], ref[key]), (call, key)
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(torch_cuda):
