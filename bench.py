@@ -467,6 +467,41 @@ def run_ours(args):
                      pk["bf16_tflops"] * 1e12) else "tensor",
                  "peak_source": pk["source"]}
 
+    bf16_states = None
+    if wl.dtype == "bf16" and min(Dk, Dv) >= 64 and not args.no_variants:
+        # the same step with the chunk-start states kept as bf16 tiles
+        # (GDN_FLAG_BF16_SAVED_STATES): same gradients, half the largest byte stream
+        layer_b = gdn.Layer.create(Hk, Hv, Dk, Dv, inp.cu_seqlens, wl.dtype, wl.scale_value(),
+                                   device=device, bf16_states=True)
+
+        def step_b():
+            layer_b.forward(q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream,
+                            train=True)
+            layer_b.backward(q, k, v, alpha, beta_raw, a_log, dt_bias, S0, dO, dS_T, dq, dk, dv,
+                             dalpha, dbeta, da_log, ddt, dS0, stream, train=True)
+
+        for _ in range(args.warmup):
+            step_b()
+            flush()
+        evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        torch.cuda.synchronize()
+        for e0, e1 in evb:
+            e0.record(stream)
+            step_b()
+            e1.record(stream)
+            flush()
+        torch.cuda.synchronize()
+        assert gdn.gdn_read_device_status(layer_b.ws_bwd) == 0
+        ms_b = max_over_ranks(sum(a.elapsed_time(b) for a, b in evb) / K, world, device)
+        bf16_states = {"ms_per_step": ms_b, "value": world * T / (ms_b * 1e-3),
+                       "unit": "tokens/s",
+                       "path_frac": (T / (ms_b * 1e-3)) / (T / t_roof),
+                       "note": "GDN_FLAG_BF16_SAVED_STATES: chunk-start states kept as bf16 "
+                               "tiles; the same gradients bit for bit; path_frac against the "
+                               "same method bytes (fp32 states)"}
+        del layer_b
+
     e2e = run_e2e(args, inp, layer, device, tdt, world) if not args.no_e2e else None
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -483,6 +518,7 @@ def run_ours(args):
         "fwd_ms": sum(f_ms) / K, "bwd_ms": sum(b_ms) / K,
         "roofline": roof, "path_roofline": path_roof, "kernels": kernels,
         "gpu_launches": launches, "clocks": clocks, "e2e": e2e,
+        "bf16_saved_states": bf16_states,
     }
     if rank == 0 and world == 1 and not args.no_decode:
         result["decode"] = run_decode(wl, device, pk)
@@ -962,6 +998,8 @@ def main():
                     help="skip the context-parallel (segmented sequence) measurement")
     ap.add_argument("--no-layer-steps", action="store_true",
                     help="skip the conv1d + SiLU / gated RMSNorm measurement")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the step with bf16 chunk-start states")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -35,6 +35,7 @@ GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 GDN_FLAG_KEEP_FOR_BACKWARD = 1
 GDN_FLAG_REUSE_FORWARD = 2
+GDN_FLAG_BF16_SAVED_STATES = 4
 GDN_HEAD_MAP_CONSECUTIVE = 0
 GDN_HEAD_MAP_MODULO = 1
 GDN_ERR_NOT_KEPT = -8
@@ -337,7 +338,8 @@ def _state_elems(shape) -> int:
 def gdn_forward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, chunk_offsets, S0,
                 o, S_T, saved_states, workspace, stream=None, flags=0) -> None:
     """Calls gdn_forward.  All tensors are CUDA tensors (S0 / S_T may be None).
-    flags: 0 or GDN_FLAG_KEEP_FOR_BACKWARD (workspace then of the backward's size)."""
+    flags: GDN_FLAG_KEEP_FOR_BACKWARD (workspace then of the backward's size) and / or
+    GDN_FLAG_BF16_SAVED_STATES (saved states as bf16 tiles instead of fp32)."""
     c = _Call("gdn_forward")
     tok = c.token_dtype(shape)
     T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
@@ -359,7 +361,8 @@ def gdn_backward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, ch
                  dO, dS_T, saved_states, dq, dk, dv, dalpha, dbeta_raw, da_log, ddt_bias, dS0,
                  workspace, stream=None, flags=0) -> None:
     """Calls gdn_backward.  All tensors are CUDA tensors (S0, dS_T, dS0 may be None).
-    flags: 0 or GDN_FLAG_REUSE_FORWARD (workspace then the one a keeping forward used)."""
+    flags: GDN_FLAG_REUSE_FORWARD (workspace then the one a keeping forward used) and /
+    or GDN_FLAG_BF16_SAVED_STATES (as given to the forward that wrote saved_states)."""
     c = _Call("gdn_backward")
     tok = c.token_dtype(shape)
     T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
@@ -654,10 +657,11 @@ class Layer:
     saved_states: object
     ws_fwd: object
     ws_bwd: object
+    bf16_states: bool = False   # GDN_FLAG_BF16_SAVED_STATES on both calls
 
     @classmethod
     def create(cls, Hk, Hv, Dk, Dv, cu_seqlens_host, dtype, scale=0.0, device="cuda",
-               head_map=0):
+               head_map=0, bf16_states=False):
         import torch
         off, nc = gdn_plan(cu_seqlens_host)
         cu = np.asarray(cu_seqlens_host, dtype=np.int32)
@@ -670,7 +674,7 @@ class Layer:
         ws_b = torch.empty(max(256, gdn_workspace_bytes(shape, True)), dtype=torch.uint8,
                            device=device)
         return cls(shape, torch.from_numpy(cu).to(device), torch.from_numpy(off).to(device),
-                   saved, ws_f, ws_b)
+                   saved, ws_f, ws_b, bool(bf16_states))
 
     def forward(self, q, k, v, alpha, beta_raw, a_log, dt_bias, S0, o, S_T, stream=None,
                 train=False, keep_states=True):
@@ -680,17 +684,19 @@ class Layer:
                     self.chunk_offsets, S0, o, S_T,
                     self.saved_states if (keep_states or train) else None,
                     self.ws_bwd if train else self.ws_fwd, stream,
-                    GDN_FLAG_KEEP_FOR_BACKWARD if train else 0)
+                    (GDN_FLAG_KEEP_FOR_BACKWARD if train else 0) |
+                    (GDN_FLAG_BF16_SAVED_STATES if self.bf16_states else 0))
 
     def backward(self, q, k, v, alpha, beta_raw, a_log, dt_bias, S0, dO, dS_T, dq, dk, dv,
                  dalpha, dbeta_raw, da_log, ddt_bias, dS0, stream=None, train=False):
         gdn_backward(self.shape, q, k, v, alpha, beta_raw, a_log, dt_bias, self.cu_seqlens,
                      self.chunk_offsets, S0, dO, dS_T, self.saved_states, dq, dk, dv, dalpha,
                      dbeta_raw, da_log, ddt_bias, dS0, self.ws_bwd, stream,
-                     GDN_FLAG_REUSE_FORWARD if train else 0)
+                     (GDN_FLAG_REUSE_FORWARD if train else 0) |
+                     (GDN_FLAG_BF16_SAVED_STATES if self.bf16_states else 0))
 
 
 __all__ = list(EXPORTED) + ["gdn_profile", "gdn_shape", "make_shape", "Layer", "GdnError", "LIB_PATH", "CHUNK",
                             "GDN_DTYPE_F32", "GDN_DTYPE_BF16", "GDN_FLAG_KEEP_FOR_BACKWARD",
-                            "GDN_FLAG_REUSE_FORWARD", "GDN_ERR_NOT_KEPT",
+                            "GDN_FLAG_REUSE_FORWARD", "GDN_FLAG_BF16_SAVED_STATES", "GDN_ERR_NOT_KEPT",
                             "GDN_HEAD_MAP_CONSECUTIVE", "GDN_HEAD_MAP_MODULO"]

@@ -60,6 +60,14 @@ int check_vec(const void* p, bool required) {
   return GDN_OK;
 }
 
+// An fp32 per-head vector (a_log, dt_bias and their gradients): read and written one
+// element at a time, so 4-byte alignment (a sub-vector of one rank's heads passes).
+int check_head_vec(const void* p) {
+  if (!p) return GDN_ERR_INVALID_ARG;
+  if (((uintptr_t)p & 3u) != 0) return GDN_ERR_MISALIGNED;
+  return GDN_OK;
+}
+
 // Byte ranges of two [rows, ld] matrices (width used columns) intersect.
 bool overlaps(const void* a, int64_t a_ld, const void* b, int64_t b_ld, int64_t rows,
               int64_t width, size_t esize) {
@@ -178,6 +186,7 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
       p.Tb = (uint8_t*)(base + L.Tb);
       p.dSb = (uint8_t*)(base + L.dSb);
       p.dDb = (uint8_t*)(base + L.dDb);
+      p.Stb = (uint8_t*)(base + L.Stb);
     }
   }
 }
@@ -193,8 +202,8 @@ int check_inputs(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
   GDN_TRY(check_matrix(v, v_ld, (int64_t)s->Hv * s->Dv, es, T));
   GDN_TRY(check_gate_matrix(alpha, alpha_ld, s->Hv, T));
   GDN_TRY(check_gate_matrix(beta_raw, beta_ld, s->Hv, T));
-  GDN_TRY(check_vec(a_log, true));
-  GDN_TRY(check_vec(dt_bias, true));
+  GDN_TRY(check_head_vec(a_log));
+  GDN_TRY(check_head_vec(dt_bias));
   if (!cu || !coff) return GDN_ERR_INVALID_ARG;
   if (((uintptr_t)cu & 3u) || ((uintptr_t)coff & 3u)) return GDN_ERR_MISALIGNED;
   GDN_TRY(check_vec(S0, false));
@@ -384,10 +393,23 @@ int gdn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t* chunk_offs
 
 size_t gdn_saved_state_bytes(const gdn_shape* s) {
   if (check_shape(s) != GDN_OK) return 0;
-  if (s->dtype == GDN_DTYPE_BF16)
-    return (size_t)s->total_chunks * s->Hv * gdn::state_tile_bytes(s->Dk, s->Dv);
   return (size_t)s->total_chunks * s->Hv * s->Dk * s->Dv * sizeof(float);
 }
+
+namespace {
+// GDN_FLAG_BF16_SAVED_STATES: bf16 inputs with Dk, Dv >= 64 (so that the bf16 tiles,
+// padded to 64 rows and columns, fit in the fp32 buffer's bytes).
+int check_bf16_states(const gdn_shape* s, uint32_t flags, int* on) {
+  *on = (flags & GDN_FLAG_BF16_SAVED_STATES) != 0;
+  if (*on && (s->dtype != GDN_DTYPE_BF16 || s->Dk < 64 || s->Dv < 64)) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+// The shape tag a keeping forward leaves and a reusing backward checks, covering the
+// saved states' format too.
+uint32_t keep_tag(const gdn_shape* s, int bf16_states) {
+  return bf16_states ? (shape_tag(s) ^ 0x5bd1e994u) | 1u : shape_tag(s);
+}
+}  // namespace
 
 size_t gdn_workspace_bytes(const gdn_shape* s, int is_backward) {
   if (check_shape(s) != GDN_OK) return 0;
@@ -401,8 +423,11 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
                 const float* S0, void* o, int64_t o_ld, float* S_T, void* saved_states,
                 void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
   GDN_TRY(check_shape(s));
-  if (flags & ~(uint32_t)GDN_FLAG_KEEP_FOR_BACKWARD) return GDN_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)(GDN_FLAG_KEEP_FOR_BACKWARD | GDN_FLAG_BF16_SAVED_STATES))
+    return GDN_ERR_INVALID_ARG;
   const bool keep = (flags & GDN_FLAG_KEEP_FOR_BACKWARD) != 0;
+  int bf16_states = 0;
+  GDN_TRY(check_bf16_states(s, flags, &bf16_states));
   GDN_TRY(check_inputs(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
                        dt_bias, cu_seqlens, chunk_offsets, S0));
   const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
@@ -418,7 +443,8 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
   fill_common(p, s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
               dt_bias, cu_seqlens, chunk_offsets, S0, workspace, keep);
   p.keep = keep ? 1 : 0;
-  p.tag = shape_tag(s);
+  p.bf16_states = bf16_states;
+  p.tag = keep_tag(s, bf16_states);
   p.o = o;
   p.o_ld = o_ld;
   p.S_T = S_T;
@@ -463,7 +489,10 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
                  int64_t dbeta_ld, float* da_log, float* ddt_bias, float* dS0, void* workspace,
                  size_t workspace_bytes, uint32_t flags, void* stream) {
   GDN_TRY(check_shape(s));
-  if (flags & ~(uint32_t)GDN_FLAG_REUSE_FORWARD) return GDN_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)(GDN_FLAG_REUSE_FORWARD | GDN_FLAG_BF16_SAVED_STATES))
+    return GDN_ERR_INVALID_ARG;
+  int bf16_states = 0;
+  GDN_TRY(check_bf16_states(s, flags, &bf16_states));
   GDN_TRY(check_inputs(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
                        dt_bias, cu_seqlens, chunk_offsets, S0));
   const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
@@ -476,8 +505,8 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
   GDN_TRY(check_matrix(dv, dv_ld, (int64_t)s->Hv * s->Dv, es, T));
   GDN_TRY(check_gate_matrix(dalpha, dalpha_ld, s->Hv, T));
   GDN_TRY(check_gate_matrix(dbeta_raw, dbeta_ld, s->Hv, T));
-  GDN_TRY(check_vec(da_log, true));
-  GDN_TRY(check_vec(ddt_bias, true));
+  GDN_TRY(check_head_vec(da_log));
+  GDN_TRY(check_head_vec(ddt_bias));
   GDN_TRY(check_vec(dS0, false));
   GDN_TRY(check_workspace(s, workspace, workspace_bytes, true));
   cudaStream_t st = (cudaStream_t)stream;
@@ -503,7 +532,8 @@ int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
   p.dS0 = dS0;
   // with no chunk there is nothing to reuse: the flag is then a no-op
   p.reuse = (flags & GDN_FLAG_REUSE_FORWARD) != 0 && s->total_chunks > 0 ? 1 : 0;
-  p.tag = shape_tag(s);
+  p.bf16_states = bf16_states;
+  p.tag = keep_tag(s, bf16_states);
   (void)cudaGetLastError();  // report only errors of this call's own launches
   g_last_error[0] = 0;
   // status block and the fused backward's flags; a reusing backward keeps the
@@ -556,8 +586,8 @@ int gdn_decode_step(const gdn_shape* s, const void* q, int64_t q_ld, const void*
   GDN_TRY(check_matrix(o, o_ld, (int64_t)s->Hv * s->Dv, es, N));
   GDN_TRY(check_gate_matrix(alpha, alpha_ld, s->Hv, N));
   GDN_TRY(check_gate_matrix(beta_raw, beta_ld, s->Hv, N));
-  GDN_TRY(check_vec(a_log, true));
-  GDN_TRY(check_vec(dt_bias, true));
+  GDN_TRY(check_head_vec(a_log));
+  GDN_TRY(check_head_vec(dt_bias));
   GDN_TRY(check_vec(S_in, false));
   GDN_TRY(check_vec(S_out, N > 0));
   if (N == 0) return GDN_OK;

@@ -69,6 +69,8 @@ struct WsLayout {
   size_t Tb;      // [NC][Hv] 2 x [C][C]: T, T diag(b e^G) (backward)
   size_t dSb;     // [NC][Hv] [MV][Dk] dS^T: state adjoint at each chunk end (backward)
   size_t dDb;     // [NC][Hv] [C][MV]  -d Delta (backward); MV = max(Dv, 64)
+  size_t Stb;     // [NC][Hv] [MV][Dk] S^T: chunk-start states as the backward's bf16 operand
+                  // tiles, kept by a keeping forward (with fp32 saved states)
   size_t total;
 };
 
@@ -127,6 +129,7 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
       L.Tb = take(NC * Hv * 2 * tile_CxD(64));
       L.dSb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
       L.dDb = take(NC * Hv * tile_CxD(s.Dv));
+      L.Stb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
     }
   }
   L.total = off;
@@ -176,6 +179,8 @@ struct Params {
   uint32_t* bready;  // fused backward: [NC][Hv] state-walk chunk done
   uint32_t tag;  // shape tag (see shape_tag); written by a keeping forward, checked by a reusing backward
   int keep;      // forward: leave the backward's chunk operands in the workspace
+  int bf16_states;  // chunk-start states as bf16 S^T tiles (GDN_FLAG_BF16_SAVED_STATES)
+                    // instead of fp32 [NC][Hv][Dk][Dv]
   int reuse;     // backward: read them from the workspace instead of recomputing them
   float* Qn;
   float* Kn;
@@ -201,6 +206,7 @@ struct Params {
   uint8_t* Tb;
   uint8_t* dSb;
   uint8_t* dDb;
+  uint8_t* Stb;
 };
 
 // Key head of value head h, and the j-th (j < r) value head of key head kh: value

@@ -24,7 +24,7 @@ __device__ __forceinline__ int col_group() { return (int)(threadIdx.x >> 7); }
 // mbarriers and the TMEM address, at the same place whatever role the CTA plays.
 constexpr uint32_t kCtlBytes = 1024;
 struct CtaCtl {
-  uint64_t bar[4];
+  uint64_t bar[8];
   uint32_t tmem;
 };
 // All threads: nbar mbarriers (arrival count 1) and ncols TMEM columns.

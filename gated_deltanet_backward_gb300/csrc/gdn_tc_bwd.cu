@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_state_tc(Params p,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
-  cta_setup(ctl, 3, 512);
+  cta_setup(ctl, 4, 512);
   bwd_state_unit<DK>(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
   cta_teardown(ctl, 512);
 }
@@ -277,8 +277,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_state_tc(Params p,
 // grads_tc_smem bytes; `tmem`: 512 columns; bars[0] / bars[1]: MMA and loads with
 // their running phases).  In a fused launch (p.bready set) it first waits until the
 // reverse walks of the key head's value heads have published chunk c.
+// The bf16 S^T tiles of the chunk-start states the backward reads, if there are any: the
+// saved states (GDN_FLAG_BF16_SAVED_STATES) or the copy kept by the forward of a
+// training step; null when the fp32 saved states are converted instead.
+__device__ __forceinline__ const uint8_t* st_tile_source(const Params& p) {
+  return p.bf16_states ? (const uint8_t*)p.saved_in : (p.reuse ? p.Stb : nullptr);
+}
+
+// Thread 0: the fp32 chunk-start states of unit (c, kh)'s value heads into the L2 (heads
+// from `first` on), so that their conversion to the S^T tile does not wait on HBM.
+__device__ __forceinline__ void prefetch_unit_states(const Params& p, int c, int kh, int first) {
+  if (st_tile_source(p) || c < 0) return;
+  const uint32_t bytes = (uint32_t)p.Dk * p.Dv * 4u;
+  for (int hh = first; hh < p.r; ++hh) {
+    const float* s = p.saved_in + ((size_t)c * p.Hv + value_head(p, kh, hh)) * (size_t)p.Dk * p.Dv;
+    for (uint32_t off = 0; off < bytes; off += 16384u)
+      tc::bulk_prefetch_l2((const uint8_t*)s + off, bytes - off < 16384u ? bytes - off : 16384u);
+  }
+}
+
 __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, uint8_t* sm,
-                           uint32_t tmem, uint64_t* bars, uint32_t& mphase, uint32_t& lphase) {
+                           uint32_t tmem, uint64_t* bars, uint32_t& mphase, uint32_t& lphase,
+                           int next_c = -1, int next_kh = 0) {
   int n;
   int64_t t0;
   int len;
@@ -362,10 +382,15 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   // -dDelta rows (bulk) are the walk's and wait for its flag.  All land in one phase
   // of bars[1] of phase_a_bytes.
   const int nbv = (Dv + 63) / 64;
-  const uint32_t phase_a_bytes = sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u + bSt;
+  // the S^T tile is a bulk copy of a bf16 state tile: the saved state itself
+  // (GDN_FLAG_BF16_SAVED_STATES) or the copy a keeping forward left for a reusing
+  // backward; otherwise the whole CTA converts the fp32 saved state (load_state_f32)
+  const uint8_t* st_tiles = st_tile_source(p);
+  const uint32_t phase_a_bytes =
+      sCK + (uint32_t)Dv * C * 2 + 3u * nbv * 8192u + (st_tiles ? bSt : 0u);
   auto issue_phase_a_inputs = [&](int h) {
     const size_t ch = (size_t)c * p.Hv + h;
-    tc::bulk_g2s(tSt, (const uint8_t*)p.saved_in + ch * bSt, bSt, &bars[1]);
+    if (st_tiles) tc::bulk_g2s(tSt, st_tiles + ch * bSt, bSt, &bars[1]);
     tc::bulk_g2s(tW, p.Wsw + ch * sCK, sCK, &bars[1]);
     tc::bulk_g2s(sU, p.Utb + ch * Dv * C, (uint32_t)Dv * C * 2, &bars[1]);
     for (int b = 0; b < nbv; ++b) {
@@ -393,6 +418,61 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
   };
 
+  // The chunk-start state of value head h as the bf16 S^T tile tSt (rows v, columns k),
+  // converted by the whole CTA from the fp32 saved state.  Items (k pair kp, block of 8
+  // value columns v8), consecutive lanes on consecutive kp so that the 4-byte (k, k + 1)
+  // stores of a warp fall in distinct banks.  The tile then also goes to the workspace
+  // (Stb), from where phase B reads it back for <S, dS> exactly as it reads a kept tile.
+  const int nkp = Dk / 2, n_items = (Dk / 2) * (Dv / 8);
+  constexpr int kItems = 2;   // items per thread: Dk * Dv / 16 <= 2 * kTcThreads
+  auto load_state_f32 = [&](int h) {
+    const size_t ch = (size_t)c * p.Hv + h;
+    const float* Sf = p.saved_in + ch * (size_t)Dk * Dv;
+    if (Dv < 64 || Dk < 64) {   // the tile's padding rows / columns read as zero
+      for (int i = tid; i < (int)bSt / 16; i += kTcThreads) ((uint4*)tSt)[i] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+    }
+    float4 x[kItems][4];
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int i = tid + u * kTcThreads, kp = i % nkp, v0 = (i / nkp) * 8;
+      if (i < n_items) {
+        const float* r0 = Sf + (size_t)(2 * kp) * Dv + v0;
+        x[u][0] = *(const float4*)r0;
+        x[u][1] = *(const float4*)(r0 + 4);
+        x[u][2] = *(const float4*)(r0 + Dv);
+        x[u][3] = *(const float4*)(r0 + Dv + 4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int i = tid + u * kTcThreads, kp = i % nkp, v0 = (i / nkp) * 8;
+      if (i < n_items) {
+        const float a[8] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w,
+                            x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
+        const float b[8] = {x[u][2].x, x[u][2].y, x[u][2].z, x[u][2].w,
+                            x[u][3].x, x[u][3].y, x[u][3].z, x[u][3].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          __nv_bfloat162 pr = __floats2bfloat162_rn(a[j], b[j]);
+          *(__nv_bfloat162*)(tSt + tc::sw128_offset(v0 + j, 2 * kp, MV)) = pr;
+        }
+      }
+    }
+    tc::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc::bulk_s2g(p.Stb + ch * bSt, tSt, bSt);
+      tc::bulk_commit();
+    }
+  };
+
+  // fp32 states: this unit's later value heads and the next unit's into the L2 (the
+  // first head's conversion follows at once)
+  if (tid == 0) {
+    prefetch_unit_states(p, c, kh, 1);
+    prefetch_unit_states(p, next_c, next_kh, 0);
+  }
   // K, Q of the key head and the first value head's phase-A tiles in one phase of
   // bars[1]; the copies that need no walk start before the flags are read
   if (tid == 0) {
@@ -423,7 +503,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     const int h = value_head(p, kh, hh);
     const size_t ch = (size_t)c * p.Hv + h;
     const uint32_t acc_first = hh > 0 ? 1u : 0u;
-    const uint8_t* Sg = (const uint8_t*)p.saved_in + ch * bSt;   // S^T tile
+    // S^T tile in global memory for <S, dS>: the kept / saved tile, or the converted one
+    const uint8_t* Sg = (st_tiles ? st_tiles : p.Stb) + ch * bSt;
     // this head's vectors (prefetched), then the next head's prefetch
     tc::cp_async_wait_all();
     if (tid < C) {
@@ -445,6 +526,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
     __syncthreads();
     // ---- phase A: S^T, [dO; -dDelta], scale e^G dO
+    if (!st_tiles) load_state_f32(h);
     {
       const bool lok = tc::mbar_wait(&bars[1], lphase);
       lphase ^= 1u;
@@ -468,6 +550,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
+      // a converted tile's store to the workspace has read tSt before epilogue A reuses it
+      if (!st_tiles) tc::bulk_wait_read<0>();
       tc::mma_tile_p(tmp, tc::smem_u32(tSt), sVC, MV, tc::smem_u32(tW), 64u * 128u, C, Dk,
                      0u);                                                                // S^T W^T
       tc::mma_tile_x(tmp + 128, tc::smem_u32(tA2), false, 128u * 128u, 128, tc::smem_u32(tSt),
@@ -522,7 +606,16 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       tc::mbar_arrive_expect_tx(&bars[1], sCC);
       tc::bulk_g2s(tP, p.Psw + ch * sCC, sCC, &bars[1]);
     }
-    // S^T again, from global memory (L2), for <S, dS>: the shared copy is gone
+    // S^T again, from global memory (L2), for <S, dS>: the shared copy is gone.  A tile
+    // converted here was stored by this unit's bulk copy: it has landed and is visible
+    // to the generic loads once thread 0 has waited for it, fenced and met the others
+    if (!st_tiles) {
+      if (tid == 0) {
+        tc::bulk_wait<0>();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      __syncthreads();
+    }
     constexpr int kSraw = 32768 / 16 / kTcThreads;   // 16-byte pieces per thread (32 KB tile max)
     uint4 sraw[kSraw];
 #pragma unroll
@@ -912,14 +1005,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_fused_tc(Params p,
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
   __shared__ int s_unit;
-  cta_setup(ctl, 3, 512);
+  cta_setup(ctl, 4, 512);
   const int walks = p.n_seqs * p.Hv;
   if ((int)blockIdx.x < walks) {
     bwd_state_unit<DK>(p, maps, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes,
                        ctl->tmem, ctl->bar);
     // fresh mbarriers for the gradient role
     if (threadIdx.x == 0) {
-      for (int i = 0; i < 3; ++i) {
+      for (int i = 0; i < 4; ++i) {
         tc::mbar_inval(&ctl->bar[i]);
         tc::mbar_init(&ctl->bar[i], 1);
       }
@@ -938,8 +1031,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_fused_tc(Params p,
     __syncthreads();
     if (u >= units) break;
     if (threadIdx.x == 0) next = (int)atomicAdd(p.bwork, 1u);
+    // thread 0 knows the next unit (the others pass a placeholder they do not use)
+    const int nc = threadIdx.x == 0 && next < units ? p.NC - 1 - next / p.Hk : -1;
     grads_unit(p, maps, p.NC - 1 - u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem, ctl->bar,
-               mphase, lphase);
+               mphase, lphase, nc, threadIdx.x == 0 && next < units ? next % p.Hk : 0);
   }
   cta_teardown(ctl, 512);
 }

@@ -661,8 +661,10 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       // the chunk-start state S^T goes to the saved states as it is, by one bulk store
       // issued behind the product (the two would contend for the tile's reads); a
       // forward that keeps no states skips it
-      if (p.saved) {
-        tc::bulk_s2g((uint8_t*)p.saved + ((size_t)cc * p.Hv + h) * bSt, tSt, bSt);
+      uint8_t* tile_dst = p.saved && p.bf16_states ? (uint8_t*)p.saved
+                          : (p.keep && p.saved ? p.Stb : nullptr);
+      if (tile_dst) {
+        tc::bulk_s2g(tile_dst + ((size_t)cc * p.Hv + h) * bSt, tSt, bSt);
         tc::bulk_commit();
       }
     }, &bars[0]);
@@ -706,6 +708,20 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       }
     }
     tc::fence_async_smem();
+    // fp32 saved state of chunk c [chunk][head][Dk][Dv] from the registers (the chunk's
+    // start state): each thread stores its column v of S (a warp's lanes hold
+    // consecutive v, so every store of a warp is one 128-byte row piece), after the fence
+    // above and before the products' wait, so that they drain under the products
+    if (p.saved && !p.bf16_states && vok) {
+      float* dst = p.saved + ((size_t)c * p.Hv + h) * SZ + vrow;
+#pragma unroll
+      for (int ii = 0; ii < NKC; ++ii) {
+        const int k0 = grp * 16 + 16 * kGroups * ii;
+        if (k0 < DK)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[(size_t)(k0 + j) * Dv] = S[ii][j];
+      }
+    }
     // state update first (the next chunk waits on it), then the output products
     ok = mma_run([&] {
       tc::bulk_wait_read<0>();   // the saved-state store has read S^T: the update may rewrite it

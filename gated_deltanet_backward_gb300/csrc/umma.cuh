@@ -309,6 +309,12 @@ __device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, u
                "r"(smem_u32(smem_src)), "r"(bytes)
                : "memory");
 }
+// One thread: asks for `bytes` (multiple of 16; 16-byte aligned address) of global
+// memory to be brought into the L2 cache ahead of their use; no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gmem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem_src), "r"(bytes)
+               : "memory");
+}
 // Closes the issuing thread's current bulk group.
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");

@@ -52,9 +52,12 @@
  *  - Every argument is checked on the host before anything is launched: on a
  *    failed check the call returns a negative gdn_status and launches nothing.
  *    Supported: Dk, Dv in {16, 32, 64, 128}; Hv a multiple of Hk; device
- *    buffers 16-byte aligned; row strides of q, k, v, o, dO, dq, dk, dv whose
- *    byte size is a multiple of 16; fp32 row strides of alpha, beta_raw,
- *    d alpha, d beta_raw of at least Hv; workspace at least
+ *    buffers 16-byte aligned, except the fp32 per-head gate matrices alpha,
+ *    beta_raw, d alpha, d beta_raw and vectors a_log, dt_bias, d a_log,
+ *    d dt_bias, which need 4-byte alignment (so that a column slice of them, one
+ *    rank's heads, can be passed as it is); row strides of q, k, v, o, dO, dq,
+ *    dk, dv whose byte size is a multiple of 16; fp32 row strides of alpha,
+ *    beta_raw, d alpha, d beta_raw of at least Hv; workspace at least
  *    gdn_workspace_bytes() and 256-byte aligned.
  *  - Errors found on the device (a cu_seqlens / chunk_offsets pair that does
  *    not match the shape, a bounded wait that ran out) do not trap: the kernels
@@ -103,8 +106,24 @@ typedef enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
  * error and is not detected. */
 typedef enum {
   GDN_FLAG_KEEP_FOR_BACKWARD = 1, /* gdn_forward only */
-  GDN_FLAG_REUSE_FORWARD = 2      /* gdn_backward only */
+  GDN_FLAG_REUSE_FORWARD = 2,     /* gdn_backward only */
+  GDN_FLAG_BF16_SAVED_STATES = 4  /* gdn_forward and gdn_backward; see below */
 } gdn_flag;
+
+/* GDN_FLAG_BF16_SAVED_STATES (a measured option of this library; the default is the
+ * fp32 layout below).  For bf16 inputs with Dk, Dv >= 64 the forward may keep the
+ * chunk-start states in bf16, the precision every tensor-core product that reads them
+ * rounds them to anyway, as one tile of S^T per (chunk, value head): max(Dv, 64) rows
+ * (value index) by Dk columns (key index), each 64-column block stored as 128-byte rows
+ * whose 16-byte pieces are XOR-permuted by row % 8 (the K-major 128-byte-swizzled
+ * operand layout of the tensor cores): element (v, k) at byte
+ *   (k / 64) * max(Dv, 64) * 128 + v * 128 + (((k % 64) / 8) ^ (v % 8)) * 16 + (k % 8) * 2
+ * of the tile, tiles ceil(Dk / 64) * max(Dv, 64) * 128 bytes apart in (chunk, value
+ * head) order.  That halves the largest byte stream of a training step; the gradients
+ * are the same bits as with fp32 states (the backward rounds the fp32 states to the
+ * same bf16 values).  The backward must be given the same flag as the forward that
+ * wrote the buffer.  With fp32 inputs or a head size below 64 the flag returns
+ * GDN_ERR_UNSUPPORTED. */
 
 /* Key head of value head h (v_repeat = Hv / Hk value heads share each key head).
  * GDN_HEAD_MAP_CONSECUTIVE: kh = h / v_repeat (value heads kh*v_repeat ..
@@ -136,9 +155,12 @@ typedef struct {
 int gdn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t* chunk_offsets_host,
              int32_t* total_chunks);
 
-/* Bytes of the saved-state buffer: total_chunks * Hv * Dk * Dv * 4 for fp32
- * inputs, total_chunks * Hv * ceil(Dk / 64) * max(Dv, 64) * 128 for bf16.
- * Returns 0 for an invalid shape. */
+/* Bytes of the saved-state buffer: total_chunks * Hv * Dk * Dv * 4.  It holds the
+ * state S at the start of every chunk, fp32 [total_chunks, Hv, Dk, Dv] row-major
+ * (chunk c of sequence n at index chunk_offsets[n] + c; S[i][j] at i * Dv + j, i over
+ * the key index), for both input dtypes; GDN_FLAG_BF16_SAVED_STATES stores bf16 tiles
+ * in the first part of the same buffer instead (Dk, Dv >= 64).  Returns 0 for an
+ * invalid shape. */
 size_t gdn_saved_state_bytes(const gdn_shape* shape);
 
 /* Bytes of device scratch the forward (is_backward = 0) or the backward
@@ -155,13 +177,13 @@ size_t gdn_workspace_bytes(const gdn_shape* shape, int is_backward);
  *   S0        device, [n_seqs, Hv, Dk, Dv] fp32, or NULL for a zero state
  *   o         device, [total_tokens, o_ld] dtype (written)
  *   S_T       device, [n_seqs, Hv, Dk, Dv] fp32 final states, or NULL
- *   saved_states device, gdn_saved_state_bytes() bytes (written; the backward
- *             reads it), or NULL for a forward no backward will read (prefill,
- *             inference: the chunk-start states are then not stored); required
- *             with GDN_FLAG_KEEP_FOR_BACKWARD
+ *   saved_states device, gdn_saved_state_bytes() bytes (written: the fp32 state
+ *             at the start of every chunk, which the backward reads), or NULL for a
+ *             forward no backward will read (prefill, inference: the chunk-start
+ *             states are then not stored); required with GDN_FLAG_KEEP_FOR_BACKWARD
  *   workspace device scratch, gdn_workspace_bytes(shape, 0) bytes
  *             (gdn_workspace_bytes(shape, 1) with GDN_FLAG_KEEP_FOR_BACKWARD)
- *   flags     0 or GDN_FLAG_KEEP_FOR_BACKWARD
+ *   flags     0, or GDN_FLAG_KEEP_FOR_BACKWARD and / or GDN_FLAG_BF16_SAVED_STATES
  * Returns a gdn_status. */
 int gdn_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
                 int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
@@ -174,7 +196,8 @@ int gdn_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void*
 /* Backward (reverse chunk walk with a dS carry).  Inputs as gdn_forward, plus
  *   dO        device, [total_tokens, dO_ld] dtype: dL/do
  *   dS_T      device, [n_seqs, Hv, Dk, Dv] fp32: dL/dS_T, or NULL for zero
- *   saved_states device, as written by gdn_forward on the same inputs
+ *   saved_states device, as written by gdn_forward on the same inputs (with the
+ *             same GDN_FLAG_BF16_SAVED_STATES setting)
  * Outputs (all written, none accumulated):
  *   dq, dk    device, [total_tokens, *_ld] dtype: dL/dq, dL/dk of the RAW
  *             (un-normalised) q and k, summed over the value heads of each key head
@@ -185,7 +208,7 @@ int gdn_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const void*
  *   dS0       device, [n_seqs, Hv, Dk, Dv] fp32: dL/dS_0, or NULL to skip
  *   workspace device scratch, gdn_workspace_bytes(shape, 1) bytes; with
  *             GDN_FLAG_REUSE_FORWARD, the workspace of the kept forward
- *   flags     0 or GDN_FLAG_REUSE_FORWARD
+ *   flags     0, or GDN_FLAG_REUSE_FORWARD and / or GDN_FLAG_BF16_SAVED_STATES
  * Returns a gdn_status. */
 int gdn_backward(const gdn_shape* shape, const void* q, int64_t q_ld, const void* k,
                  int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,

@@ -33,7 +33,7 @@ class DeviceRun:
     each call compute everything itself."""
 
     def __init__(self, inp: W.Inputs, device="cuda", dense=False, run_backward=True,
-                 train=True):
+                 train=True, bf16_states=False):
         import torch
         import gated_deltanet_backward_gb300 as gdn
         self.inp = inp
@@ -58,7 +58,8 @@ class DeviceRun:
         self.dO = dev(inp.dO, self.tdtype)
         self.dS_T = None if inp.dS_T is None else dev(inp.dS_T)
         self.layer = gdn.Layer.create(Hk, Hv, Dk, Dv, inp.cu_seqlens, wl.dtype,
-                                      wl.scale_value(), device=device, head_map=wl.head_map)
+                                      wl.scale_value(), device=device, head_map=wl.head_map,
+                                      bf16_states=bf16_states)
         N = wl.n_seqs
         self.o = torch.full((T, Hv * Dv), float("nan"), device=device, dtype=self.tdtype)
         self.S_T = torch.full((N, Hv, Dk, Dv), float("nan"), device=device)
@@ -116,21 +117,23 @@ class DeviceRun:
         import torch
         torch.cuda.synchronize()
         out = dict(o=self.o.double().cpu().numpy(), S_T=self.S_T.double().cpu().numpy())
-        out["saved"] = saved_states_dense(self.layer.saved_states, self.inp.wl)
+        out["saved"] = saved_states_dense(self.layer.saved_states, self.inp.wl,
+                                          self.layer.bf16_states)
         if self.grads is not None:
             for k, v in self.grads.items():
                 out[k] = v.double().cpu().numpy()
         return out
 
 
-def saved_states_dense(saved, wl: W.Workload) -> np.ndarray:
+def saved_states_dense(saved, wl: W.Workload, bf16_states=False) -> np.ndarray:
     """The saved chunk-start states as [total_chunks, Hv, Dk, Dv] f64, decoded from the
-    buffer's documented format (include/gdn.h): fp32 blocks, or for bf16 inputs bf16
-    S^T tiles of max(Dv, 64) rows in the 128-byte-swizzled K-major layout."""
+    buffer's documented format (include/gdn.h): fp32 blocks, or with
+    GDN_FLAG_BF16_SAVED_STATES bf16 S^T tiles of max(Dv, 64) rows in the
+    128-byte-swizzled K-major layout."""
     import torch
     NC, Hv, Dk, Dv = wl.total_chunks, wl.Hv, wl.Dk, wl.Dv
     raw = saved.detach().reshape(-1).view(torch.uint8).cpu().numpy()
-    if wl.dtype != "bf16":
+    if not bf16_states:
         return raw[:NC * Hv * Dk * Dv * 4].view(np.float32).astype(np.float64).reshape(
             NC, Hv, Dk, Dv)
     MV = max(Dv, 64)

@@ -56,12 +56,17 @@ def test_plan(gdn):
 
 def test_sizes(gdn):
     s = gdn.make_shape(16, 48, 128, 128, 1, 64, 4096, "bf16")
-    # bf16: one bf16 S^T tile per (chunk, value head); fp32: the dense fp32 states
-    assert gdn.gdn_saved_state_bytes(s) == 64 * 48 * 128 * 128 * 2
+    # the fp32 chunk-start states [total_chunks, Hv, Dk, Dv] for both input dtypes
+    assert gdn.gdn_saved_state_bytes(s) == 64 * 48 * 128 * 128 * 4
     assert gdn.gdn_saved_state_bytes(gdn.make_shape(2, 4, 16, 32, 1, 3, 150, "bf16")) == \
-        3 * 4 * 1 * 64 * 128                 # Dk 16 -> one 64-column block; Dv 32 -> 64 rows
+        3 * 4 * 16 * 32 * 4
     assert gdn.gdn_saved_state_bytes(gdn.make_shape(2, 4, 16, 32, 1, 3, 150, "f32")) == \
         3 * 4 * 16 * 32 * 4
+    # the bf16 tiles of GDN_FLAG_BF16_SAVED_STATES (Dk, Dv >= 64) fit in the same buffer
+    for Dk in (64, 128):
+        for Dv in (64, 128):
+            tile = -(-Dk // 64) * max(Dv, 64) * 128
+            assert tile <= Dk * Dv * 4, (Dk, Dv)
     f, b = gdn.gdn_workspace_bytes(s, False), gdn.gdn_workspace_bytes(s, True)
     assert 256 < f < b and f % 256 == 0 and b % 256 == 0
     bad = gdn.make_shape(16, 48, 96, 128, 1, 64, 4096, "bf16")
@@ -115,7 +120,10 @@ def test_forward_rejects_bad_arguments_before_launching(gdn):
     assert lib.gdn_forward(None, *_fwd_args(gdn, s, ws_bytes=ws)[1:]) == -1
     # unknown flags, a backward-only flag, and a keeping forward whose workspace has
     # only the forward's size
-    assert lib.gdn_forward(*_fwd_args(gdn, s, ws_bytes=ws, flags=4)) == -1
+    assert lib.gdn_forward(*_fwd_args(gdn, s, ws_bytes=ws, flags=8)) == -1
+    # bf16 saved states with fp32 inputs
+    assert lib.gdn_forward(*_fwd_args(gdn, s, ws_bytes=ws,
+                                      flags=gdn.GDN_FLAG_BF16_SAVED_STATES)) == -2
     assert lib.gdn_forward(*_fwd_args(gdn, s, ws_bytes=ws, flags=gdn.GDN_FLAG_REUSE_FORWARD)) == -1
     assert lib.gdn_forward(*_fwd_args(gdn, s, ws_bytes=ws,
                                       flags=gdn.GDN_FLAG_KEEP_FOR_BACKWARD)) == -6
@@ -176,6 +184,6 @@ int main(void) {
                     "-Wl,-rpath," + libdir], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
     assert out[0] == "plan 0 1 1 4 5 total 5"
-    assert out[1] == "saved %d" % (64 * 48 * 128 * 128 * 2)
+    assert out[1] == "saved %d" % (64 * 48 * 128 * 128 * 4)
     assert out[2] == "ws 1"
     assert out[3] == "forward -1 GDN_ERR_INVALID_ARG"

@@ -64,6 +64,13 @@ def test_backward_checks(gdn):
              dS0=None, ws=f(), ws_bytes=ws, flags=0, stream=None)
     run = lambda **o: _call(gdn._lib.gdn_backward, BWD_ORDER, a, **o)
     assert run(flags=gdn.GDN_FLAG_KEEP_FOR_BACKWARD) == INVALID      # a forward-only flag
+    assert run(flags=8) == INVALID                                    # no such flag
+    # bf16 saved states: bf16 inputs with Dk, Dv >= 64 only
+    assert run(flags=gdn.GDN_FLAG_BF16_SAVED_STATES) == UNSUPPORTED   # fp32 inputs
+    s16 = gdn.make_shape(2, 6, 64, 32, 1, 2, 100, "bf16")
+    assert run(shape=ctypes.byref(s16), flags=gdn.GDN_FLAG_BF16_SAVED_STATES,
+               ws_bytes=gdn.gdn_workspace_bytes(s16, True), dO_ld=6 * 32,
+               dv_ld=6 * 32, v_ld=6 * 32) == UNSUPPORTED
     assert run(saved=None) == INVALID                                 # chunks need states
     assert run(ws_bytes=gdn.gdn_workspace_bytes(s, False)) == WORKSPACE
     assert run(dO_ld=wv - 8) == INVALID

@@ -114,6 +114,31 @@ def test_l27b_batch_training_steps_are_byte_identical():
     _five_training_steps_are_byte_identical(W.generate(W.get("l27b_batch_bf16")))
 
 
+@pytest.mark.parametrize("name", ["small", "l27b_bf16"])
+def test_bf16_saved_states_give_the_same_bits(name):
+    """GDN_FLAG_BF16_SAVED_STATES keeps the chunk-start states as bf16 S^T tiles instead of
+    fp32.  Every tensor-core product of the backward rounds the fp32 states to the same
+    bf16 values, so o, S_T and every gradient are the same bits either way, and the tiles
+    hold the fp32 states rounded to bf16."""
+    import torch
+    wl = W.get(name) if name != "small" else W.custom(
+        dtype="bf16", Hk=2, Hv=6, Dk=128, Dv=64, seqlens=(300, 77), seed=41, S0_std=0.1,
+        dST_std=0.05, dt_bias_std=0.1)
+    inp = W.generate(wl)
+    a = DeviceRun(inp)
+    A = a.host()
+    del a
+    b = DeviceRun(inp, bf16_states=True)
+    assert b.status() == 0 and b.status(backward=True) == 0
+    B = b.host()
+    del b
+    for key in A:
+        if key != "saved":
+            assert np.array_equal(A[key], B[key]), key
+    rounded = torch.from_numpy(A["saved"]).float().bfloat16().double().numpy()
+    assert np.array_equal(B["saved"], rounded)
+
+
 def test_strided_and_dense_inputs_give_identical_bits():
     inp = W.generate(W.custom(dtype="bf16", Hk=2, Hv=6, Dk=64, Dv=64, seqlens=(300, 77), seed=3,
                               S0_std=0.1, dST_std=0.1))
