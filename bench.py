@@ -120,7 +120,7 @@ def path_model(wl: W.Workload):
 # The kernels of each pass: a pass's algorithmic work (path_model) is what its kernels
 # do between them; a fused pass is one launch.
 FWD_KERNELS = ("gdn_fwd_fused_tc", "gdn_prep_tc", "gdn_prep_tc_full", "gdn_fwd_state_tc",
-               "gdn_prep", "gdn_fwd_state")
+               "gdn_fwd_out_tc", "gdn_prep", "gdn_fwd_state")
 BWD_KERNELS = ("gdn_bwd_fused_tc", "gdn_bwd_state_tc", "gdn_bwd_grads_tc", "gdn_bwd_state",
                "gdn_bwd_grads", "gdn_bwd_qk", "gdn_bwd_gates")
 
@@ -183,7 +183,11 @@ def kernel_models(wl: W.Workload):
                           4 * C * Dk * Dv + 2 * C * C * Dv + 2 * C * C * (Dv + Dk) +
                           4 * C * C * Dk + 2 * C * C * Dv + 4 * C ** 3 + 4 * C * C * Dk +
                           2 * C * C * Dk)
+    # output pass: Q tiles, the walk's S^T and Delta^T tiles, P and G in, o out
+    out_tc_b = (NC * Hk * sKC + NC * Hv * (sST + MV * 128 + sCC + C * 4) + T * Hv * Dv * es)
+    out_tc_f = NC * Hv * (2 * C * Dk * Dv + 2 * C * C * Dv)
     return {
+        "gdn_fwd_out_tc": (out_tc_b, out_tc_f, "tensor"),
         "gdn_fwd_fused_tc": (tc_prep_bwd_b + fst_tc_b, tc_prep_f + fst_tc_f, "tensor"),
         "gdn_bwd_fused_tc": (bst_tc_b + bgr_tc_b, bst_tc_f + bgr_tc_f, "tensor"),
         "gdn_prep_tc": (tc_prep_b, tc_prep_f, "tensor"),

@@ -181,12 +181,13 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
     p.Wsw = (uint8_t*)(base + L.Wsw);
     p.Psw = (uint8_t*)(base + L.Psw);
     p.Utb = (__nv_bfloat16*)(base + L.Utb);
+    p.Stb = (uint8_t*)(base + L.Stb);
+    p.Dtb = (uint8_t*)(base + L.Dtb);
     if (bwd) {
       p.KKf = (float*)(base + L.KKf);
       p.Tb = (uint8_t*)(base + L.Tb);
       p.dSb = (uint8_t*)(base + L.dSb);
       p.dDb = (uint8_t*)(base + L.dDb);
-      p.Stb = (uint8_t*)(base + L.Stb);
     }
   }
 }
@@ -369,6 +370,7 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_COMPOSE: return "gdn_state_compose";
     case gdn::KID_KDA_FWD: return "gdn_kda_fwd";
     case gdn::KID_KDA_BWD: return "gdn_kda_bwd";
+    case gdn::KID_FWD_OUT_TC: return "gdn_fwd_out_tc";
     default: return "?";
   }
 }

@@ -228,10 +228,14 @@ cudaError_t launch_forward(const Params& p, const TmaMaps* maps, cudaStream_t st
     // bf16 inputs: tensor-core chunk preparation and state walk
     bool fused = false;
     cudaError_t e = launch_fwd_fused_tc(p, *maps, st, &fused);
-    if (e != cudaSuccess || fused) return e;
-    e = launch_prep_tc(p, *maps, p.keep != 0, st);
     if (e != cudaSuccess) return e;
-    return launch_fwd_state_tc(p, st);
+    if (!fused) {
+      e = launch_prep_tc(p, *maps, p.keep != 0, st);
+      if (e == cudaSuccess) e = launch_fwd_state_tc(p, st);
+      if (e != cudaSuccess) return e;
+    }
+    // the output from the walks' state and Delta tiles
+    return launch_fwd_out_tc(p, st);
   }
   cudaError_t e = launch_prep(p, bf16, p.keep != 0, st);
   if (e != cudaSuccess || p.n_seqs == 0) return e;

@@ -69,8 +69,9 @@ struct WsLayout {
   size_t Tb;      // [NC][Hv] 2 x [C][C]: T, T diag(b e^G) (backward)
   size_t dSb;     // [NC][Hv] [MV][Dk] dS^T: state adjoint at each chunk end (backward)
   size_t dDb;     // [NC][Hv] [C][MV]  -d Delta (backward); MV = max(Dv, 64)
-  size_t Stb;     // [NC][Hv] [MV][Dk] S^T: chunk-start states as the backward's bf16 operand
-                  // tiles, kept by a keeping forward (with fp32 saved states)
+  size_t Stb;     // [NC][Hv] [MV][Dk] S^T: chunk-start states as bf16 operand tiles, written
+                  // by the walk for the output pass (and kept for a reusing backward)
+  size_t Dtb;     // [NC][Hv] [MV][C] Delta^T, written by the walk for the output pass
   size_t total;
 };
 
@@ -124,12 +125,13 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
     L.Wsw = take(NC * Hv * tile_CxD(s.Dk));
     L.Psw = take(NC * Hv * tile_CxD(64));
     L.Utb = take(NC * Hv * Dv * C * 2);
+    L.Stb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
+    L.Dtb = take(NC * Hv * (size_t)(Dv < 64 ? 64 : Dv) * 128);
     if (bwd) {
       L.KKf = take(NC * Hk * C * C * 4);
       L.Tb = take(NC * Hv * 2 * tile_CxD(64));
       L.dSb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
       L.dDb = take(NC * Hv * tile_CxD(s.Dv));
-      L.Stb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
     }
   }
   L.total = off;
@@ -207,6 +209,7 @@ struct Params {
   uint8_t* dSb;
   uint8_t* dDb;
   uint8_t* Stb;
+  uint8_t* Dtb;
 };
 
 // Key head of value head h, and the j-th (j < r) value head of key head kh: value
@@ -243,7 +246,8 @@ enum KernelId {
   KID_COMPOSE = 19,
   KID_KDA_FWD = 20,
   KID_KDA_BWD = 21,
-  KID_COUNT = 22
+  KID_FWD_OUT_TC = 22,
+  KID_COUNT = 23
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
@@ -271,6 +275,8 @@ int sm_count();
 cudaError_t launch_fwd_fused_tc(const Params& p, const TmaMaps& maps, cudaStream_t st,
                                 bool* launched);
 cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st);
+// The output pass of the bf16 forward: O from the walk's state and Delta tiles.
+cudaError_t launch_fwd_out_tc(const Params& p, cudaStream_t st);
 cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st);
 
 // One decode step (gdn_decode_step): arguments validated by the caller.

@@ -545,7 +545,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
 // The chunk walk of sequence n, value head h on a whole CTA (`sm`: 1024-aligned,
 // fwd_state_tc_smem bytes; `tmem`: 512 columns; bars[0..2]: MMA and the two load
 // buffers).  In a fused launch (p.fready set) chunk c's tiles are read only after the
-// preparation unit (c, key head) has published them.
+// preparation unit (c, key head) has published them.  The walk carries only the state:
+// per chunk it writes the chunk-start state (fp32, and as a bf16 S^T tile) and the
+// Delta^T tile, from which the output pass (out_unit) forms O.
 template <int DK>
 __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint32_t tmem,
                                uint64_t* bars) {
@@ -560,30 +562,28 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read K MN-major
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const int tid = threadIdx.x, grp = col_group();
-  const uint32_t bW = (uint32_t)tileCD(DK), bP = 8192;
+  const uint32_t bW = (uint32_t)tileCD(DK);
   const uint32_t bU = (uint32_t)Dv * C * 2, bG = C * 4;
   const uint32_t bSt = tc::sw128_bytes(MV, DK);       // one saved S^T tile
   uint8_t* tSt = sm;                                  // [MV][DK]
   uint8_t* buf0 = tSt + tc::sw128_bytes(MV, DK);
-  const uint32_t bufsz = bW * 3 + bP + ((bU + bG + 1023) & ~1023u);
-  uint8_t* tDt = buf0 + 2 * bufsz;                    // [MV][C] Delta^T, then O rows
+  const uint32_t bufsz = bW * 2 + ((bU + bG + 1023) & ~1023u);
+  uint8_t* tDt = buf0 + 2 * bufsz;                    // [MV][C] Delta^T
   uint8_t* tDct = tDt + MV * 128;                     // [MV][C] Delta^T diag(c)
   float* evb = (float*)(tDct + MV * 128);             // [2][C] e^G, by chunk parity
   float* cvb = evb + 2 * C;                           // [2][C] e^{G_last - G}
   auto tW = [&](int b) { return buf0 + b * bufsz; };
-  auto tQ = [&](int b) { return buf0 + b * bufsz + bW; };
-  auto tK = [&](int b) { return buf0 + b * bufsz + 2 * bW; };
-  auto tP = [&](int b) { return buf0 + b * bufsz + 3 * bW; };
-  auto sU = [&](int b) { return (const __nv_bfloat16*)(buf0 + b * bufsz + 3 * bW + bP); };
-  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + 3 * bW + bP + bU); };
+  auto tK = [&](int b) { return buf0 + b * bufsz + bW; };
+  auto sU = [&](int b) { return (const __nv_bfloat16*)(buf0 + b * bufsz + 2 * bW); };
+  auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + 2 * bW + bU); };
+  const uint32_t bDt = (uint32_t)MV * 128;            // one Delta^T tile
 
   for (int i = tid; i < (int)(tc::sw128_bytes(MV, DK) / 16); i += kTcThreads)
     ((uint4*)tSt)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < MV * 128 * 2 / 16; i += kTcThreads) ((uint4*)tDt)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  // TMEM: X = S^T W^T @0, state update @64, and the output in token rows (M = 64):
-  // Q S @256, P Delta @384 (they survive into the next chunk's first product)
-  const uint32_t tX = tmem, tS = tmem + 64, tO1 = tmem + 256, tO2 = tmem + 384;
+  // TMEM: X = S^T W^T @0, state update @64
+  const uint32_t tX = tmem, tS = tmem + 64;
   uint32_t mphase = 0, lph[2] = {0, 0};
   const int vrow = acc_row(MV);
   const bool vok = vrow >= 0 && vrow < Dv;
@@ -607,11 +607,9 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
     const size_t chh = (size_t)cc * p.Hv + h, ckk = (size_t)cc * p.Hk + kh;
-    tc::mbar_arrive_expect_tx(lb, 3 * bW + bP + bU + bG);
+    tc::mbar_arrive_expect_tx(lb, 2 * bW + bU + bG);
     tc::bulk_g2s(tW(b), p.Wsw + chh * bW, bW, lb);
-    tc::bulk_g2s(tQ(b), p.Qsw + ckk * bW, bW, lb);
     tc::bulk_g2s(tK(b), p.Ksw + ckk * bW, bW, lb);
-    tc::bulk_g2s(tP(b), p.Psw + chh * bP, bP, lb);
     tc::bulk_g2s((void*)sU(b), p.Utb + chh * Dv * C, bU, lb);
     tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
   };
@@ -657,16 +655,16 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       cvb[b * C + tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
     }
     mma_issue([&] {
+      // the previous chunk's Delta^T store has read its tile (the epilogue after this
+      // product rewrites it)
+      tc::bulk_wait_read<0>();
       tc::mma_tile(tX, tc::smem_u32(tSt), MV, tc::smem_u32(tW(b)), C, DK, 0u);
-      // the chunk-start state S^T goes to the saved states as it is, by one bulk store
-      // issued behind the product (the two would contend for the tile's reads); a
-      // forward that keeps no states skips it
-      uint8_t* tile_dst = p.saved && p.bf16_states ? (uint8_t*)p.saved
-                          : (p.keep && p.saved ? p.Stb : nullptr);
-      if (tile_dst) {
-        tc::bulk_s2g(tile_dst + ((size_t)cc * p.Hv + h) * bSt, tSt, bSt);
-        tc::bulk_commit();
-      }
+      // the chunk-start state as a bf16 S^T tile, for the output pass and the backward:
+      // the saved state itself (GDN_FLAG_BF16_SAVED_STATES) or the workspace copy; one
+      // bulk store issued behind the product (the two would contend for the tile's reads)
+      uint8_t* tile_dst = p.saved && p.bf16_states ? (uint8_t*)p.saved : p.Stb;
+      tc::bulk_s2g(tile_dst + ((size_t)cc * p.Hv + h) * bSt, tSt, bSt);
+      tc::bulk_commit();
     }, &bars[0]);
     return true;
   };
@@ -681,7 +679,6 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   }
   for (int c = c0; c < c1 && ok; ++c) {
     const int i = c - c0, b = i & 1;
-    const int64_t t0 = s0 + (int64_t)i * C;
     const int len = chunk_len(c);
     const float* ev = evb + b * C;
     const float* cv = cvb + b * C;
@@ -722,16 +719,14 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
           for (int j = 0; j < 16; ++j) dst[(size_t)(k0 + j) * Dv] = S[ii][j];
       }
     }
-    // state update first (the next chunk waits on it), then the output products
+    // the state update; the Delta^T tile goes out for the output pass
     ok = mma_run([&] {
-      tc::bulk_wait_read<0>();   // the saved-state store has read S^T: the update may rewrite it
+      tc::bulk_wait_read<0>();   // the state tile's store has read S^T: the update may rewrite it
       // K^T read MN-major from the natural K tile
       tc::mma_tile_x(tS, tc::smem_u32(tDct), false, (uint32_t)MV * 128u, MV, tc::smem_u32(tK(b)),
                      true, 8192u, NKF, C, 0u);
-      // O in token rows: Q S (B = the S^T tile) and P Delta (B = the Delta^T tile)
-      tc::mma_tile_p(tO1, tc::smem_u32(tQ(b)), 8192u, 64, tc::smem_u32(tSt), (uint32_t)MV * 128u,
-                     Dv, DK, 0u);
-      tc::mma_tile(tO2, tc::smem_u32(tP(b)), 64, tc::smem_u32(tDt), Dv, C, 0u);
+      tc::bulk_s2g(p.Dtb + ((size_t)c * p.Hv + h) * bDt, tDt, bDt);
+      tc::bulk_commit();
       // while the tensor core works: is chunk c + 2 prepared (flag read ahead)?
       if (p.fready && c + 2 < c1 && issued == c + 1 &&
           flag_ready(p.fready + (size_t)(c + 2) * p.Hk + kh))
@@ -760,35 +755,9 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       }
     }
     tc::fence_async_smem();
-    // the next chunk's first product runs while this chunk's output is formed
     if (c + 1 < c1 && !start_chunk(c + 1)) {
       ok = false;
       break;
-    }
-    // O = scale (e^G Q S + P Delta), token row r of the chunk per accumulator lane:
-    // each thread stores 16 consecutive values of its row
-    {
-      // M = 64 accumulators, two 16-column pieces per load (x2_row / x2_half)
-      const int r = x2_row();
-      __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + r) * p.o_ld + (int64_t)h * Dv;
-      for (int c0 = grp * 16; c0 < Dv; c0 += 32 * kGroups) {
-        float o1[16], o2[16];
-        tc::tmem_ld16_x2<16 * kGroups>(tO1 + lane_quarter() + c0, o1);
-        tc::tmem_ld16_x2<16 * kGroups>(tO2 + lane_quarter() + c0, o2);
-        tc::tmem_ld_wait();
-        const int col = c0 + x2_half() * 16 * kGroups;
-        if (r < len && col < Dv) {
-          const float e = p.scale * ev[r];
-          __align__(16) __nv_bfloat162 pk[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            pk[j] = __floats2bfloat162_rn(fmaf(e, o1[2 * j], p.scale * o2[2 * j]),
-                                          fmaf(e, o1[2 * j + 1], p.scale * o2[2 * j + 1]));
-          uint4* dst = (uint4*)(orow + col);
-          dst[0] = ((const uint4*)pk)[0];
-          dst[1] = ((const uint4*)pk)[1];
-        }
-      }
     }
   }
   if (ok && p.S_T && vok)
@@ -800,6 +769,90 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
           p.S_T[((size_t)n * p.Hv + h) * SZ + (size_t)(grp * 16 + 16 * kGroups * ii + j) * Dv +
                 vrow] = S[ii][j];
   if (tid == 0) tc::bulk_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
+// The output of one (chunk c, value head h) on a whole CTA (`sm`: 1024-aligned,
+// out_tc_smem bytes; `tmem`: 256 columns; bars[0..1]: the tiles and the products):
+//   O = scale (diag(e^G) Q S + P Delta)
+// in token rows, from the normalised Q tile of the key head, the chunk-start state's
+// S^T tile and the Delta^T tile the walk left, and P.  Small enough (about 73 KB of
+// shared memory, 256 TMEM columns, 64 registers) for two CTAs per SM, so that one
+// CTA's loads and products run under the other's epilogue.
+__device__ void out_unit(const Params& p, int c, int h, uint8_t* sm, uint32_t tmem,
+                         uint64_t* bars) {
+  int n;
+  int64_t t0;
+  int len;
+  if (!chunk_info(p, c, &n, &t0, &len)) {
+    if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
+    return;
+  }
+  const int Dk = p.Dk, Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
+  const int tid = threadIdx.x, grp = col_group();
+  const uint32_t bQ = (uint32_t)tileCD(Dk), bSt = tc::sw128_bytes(MV, Dk);
+  const uint32_t bDt = (uint32_t)MV * 128, bP = 8192, bG = C * 4;
+  uint8_t* tQ = sm;                  // [C][Dk] normalised Q of the key head
+  uint8_t* tS = tQ + bQ;             // [MV][Dk] S^T
+  uint8_t* tD = tS + bSt;            // [MV][C] Delta^T
+  uint8_t* tP = tD + bDt;            // [C][C] P
+  float* sG = (float*)(tP + bP);     // [C] G
+  float* ev = sG + C;                // [C] scale e^G
+  const uint32_t tO1 = tmem, tO2 = tmem + 128;   // Q S and P Delta (M = 64)
+  const uint8_t* tiles = p.saved && p.bf16_states ? (const uint8_t*)p.saved : p.Stb;
+  const size_t ch = (size_t)c * p.Hv + h;
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bars[0], bQ + bSt + bDt + bP + bG);
+    tc::bulk_g2s(tQ, p.Qsw + ((size_t)c * p.Hk + key_head(p, h)) * bQ, bQ, &bars[0]);
+    tc::bulk_g2s(tS, tiles + ch * bSt, bSt, &bars[0]);
+    tc::bulk_g2s(tD, p.Dtb + ch * bDt, bDt, &bars[0]);
+    tc::bulk_g2s(tP, p.Psw + ch * bP, bP, &bars[0]);
+    tc::bulk_g2s(sG, p.G + ch * C, bG, &bars[0]);
+  }
+  uint32_t ph = 0, mph = 0;
+  const bool lok = tc::mbar_wait(&bars[0], ph);
+  if (__syncthreads_or(lok ? 0 : 1)) {
+    if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+    return;
+  }
+  if (tid < C) ev[tid] = p.scale * expf(sG[tid]);
+  // O1 = Q S (B = the S^T tile), O2 = P Delta (B = the Delta^T tile)
+  const bool ok = mma_run([&] {
+    tc::mma_tile_p(tO1, tc::smem_u32(tQ), 8192u, 64, tc::smem_u32(tS), (uint32_t)MV * 128u, Dv,
+                   Dk, 0u);
+    tc::mma_tile(tO2, tc::smem_u32(tP), 64, tc::smem_u32(tD), Dv, C, 0u);
+  }, &bars[1], mph, p.status, c);
+  if (!ok) return;
+  // token row r of the chunk per accumulator lane, 16 consecutive values per thread
+  const int r = x2_row();
+  __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + r) * p.o_ld + (int64_t)h * Dv;
+  for (int c0 = grp * 16; c0 < Dv; c0 += 32 * kGroups) {
+    float o1[16], o2[16];
+    tc::tmem_ld16_x2<16 * kGroups>(tO1 + lane_quarter() + c0, o1);
+    tc::tmem_ld16_x2<16 * kGroups>(tO2 + lane_quarter() + c0, o2);
+    tc::tmem_ld_wait();
+    const int col = c0 + x2_half() * 16 * kGroups;
+    if (r < len && col < Dv) {
+      const float e = ev[r];
+      __align__(16) __nv_bfloat162 pk[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        pk[j] = __floats2bfloat162_rn(fmaf(e, o1[2 * j], p.scale * o2[2 * j]),
+                                      fmaf(e, o1[2 * j + 1], p.scale * o2[2 * j + 1]));
+      uint4* dst = (uint4*)(orow + col);
+      dst[0] = ((const uint4*)pk)[0];
+      dst[1] = ((const uint4*)pk)[1];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 2) k_fwd_out_tc(Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  CtaCtl* ctl = (CtaCtl*)base;
+  cta_setup(ctl, 2, 256);
+  out_unit(p, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
+  cta_teardown(ctl, 256);
 }
 
 template <int DK>
@@ -876,12 +929,28 @@ static size_t prep_tc_smem(const Params& p) {
   return b + kCtlBytes + 1024;
 }
 
+static size_t out_tc_smem(const Params& p) {
+  const int Dk = p.Dk, Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
+  return tc::sw128_bytes(64, Dk) + tc::sw128_bytes(MV, Dk) + (size_t)MV * 128 + 8192 +
+         2 * C * 4 + kCtlBytes + 1024;
+}
+
+cudaError_t launch_fwd_out_tc(const Params& p, cudaStream_t st) {
+  if (p.NC == 0) return cudaSuccess;
+  const size_t smem = out_tc_smem(p);
+  cudaFuncSetAttribute(k_fwd_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  profile_pre(st, KID_FWD_OUT_TC);
+  k_fwd_out_tc<<<dim3(p.NC, p.Hv), kTcThreads, smem, st>>>(p);
+  profile_post(st);
+  return cudaGetLastError();
+}
+
 template <int DK>
 static size_t fwd_state_tc_smem(const Params& p) {
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
-  const size_t bW = tc::sw128_bytes(64, DK), bP = 8192;
+  const size_t bW = tc::sw128_bytes(64, DK);
   const size_t bU = (size_t)Dv * C * 2, bG = C * 4;
-  const size_t bufsz = bW * 3 + bP + ((bU + bG + 1023) & ~(size_t)1023);
+  const size_t bufsz = bW * 2 + ((bU + bG + 1023) & ~(size_t)1023);
   return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 4 * C * 4 + kCtlBytes +
          1024;
 }
