@@ -183,6 +183,7 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
     p.Utb = (__nv_bfloat16*)(base + L.Utb);
     p.Stb = (uint8_t*)(base + L.Stb);
     p.Dtb = (uint8_t*)(base + L.Dtb);
+    p.Kcw = (uint8_t*)(base + L.Kcw);
     if (bwd) {
       p.KKf = (float*)(base + L.KKf);
       p.Tb = (uint8_t*)(base + L.Tb);

@@ -72,6 +72,7 @@ struct WsLayout {
   size_t Stb;     // [NC][Hv] [MV][Dk] S^T: chunk-start states as bf16 operand tiles, written
                   // by the walk for the output pass (and kept for a reusing backward)
   size_t Dtb;     // [NC][Hv] [MV][C] Delta^T, written by the walk for the output pass
+  size_t Kcw;     // [NC][Hv] [C][Dk]   diag(e^{G_last - G}) K, the state update's operand
   size_t total;
 };
 
@@ -127,6 +128,7 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
     L.Utb = take(NC * Hv * Dv * C * 2);
     L.Stb = take(NC * Hv * state_tile_bytes(s.Dk, s.Dv));
     L.Dtb = take(NC * Hv * (size_t)(Dv < 64 ? 64 : Dv) * 128);
+    L.Kcw = take(NC * Hv * tile_CxD(s.Dk));
     if (bwd) {
       L.KKf = take(NC * Hk * C * C * 4);
       L.Tb = take(NC * Hv * 2 * tile_CxD(64));
@@ -210,6 +212,7 @@ struct Params {
   uint8_t* dDb;
   uint8_t* Stb;
   uint8_t* Dtb;
+  uint8_t* Kcw;
 };
 
 // Key head of value head h, and the j-th (j < r) value head of key head kh: value

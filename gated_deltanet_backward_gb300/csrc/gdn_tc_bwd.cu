@@ -122,11 +122,12 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
       break;
     }
     if (tid == 0) {
-      // every fourth chunk, before this chunk's first store: all but the last two
-      // store groups (the previous chunk's) have landed, so the chunks down to c + 2
-      // are published (the gradient units trail the walk; waiting only for old stores
-      // keeps the wait short)
-      if (p.bready && i > 1 && (i & 3) == 0) {
+      // every fourth chunk (every chunk at first, when gradient units are waiting for
+      // the walk), before this chunk's first store: all but the last two store groups
+      // (the previous chunk's) have landed, so the chunks down to c + 2 are published
+      // (later the gradient units trail the walk; waiting only for old stores keeps the
+      // wait short)
+      if (p.bready && i > 1 && (i < 8 || (i & 3) == 0)) {
         tc::bulk_wait<2>();
         publish_down_to(c + 2);
       }

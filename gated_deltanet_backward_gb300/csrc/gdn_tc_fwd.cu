@@ -246,7 +246,8 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   uint8_t* tP = tTB + 8192;                             // [C][C] P
   uint8_t* tT = tP + 8192;                              // [C][C] T (backward)
   uint8_t* tW = tT + 8192;                              // [C][Dk] W
-  float* KK = (float*)(tW + bKC);                       // [C][C]
+  uint8_t* tKc = tW + bKC;                              // [C][Dk] diag(c) K of one head
+  float* KK = (float*)(tKc + bKC);                      // [C][C]
   float* QK = KK + C * C;                               // [C][C]
   float* Tm = QK + C * C;                               // [RB][C][TS]
   float* Mt = Tm + RB * C * TS;                         // [RB][1024] scratch of the inverse
@@ -418,10 +419,12 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
         const float* g = gv + hh * C;
         const float br = bv[hh * C + r], gr = g[r];
         const float4 kk = *(const float4*)(KK + r * C + s0);
-        a.x = br * expf(gr - g[s0]) * kk.x;
-        if (s0 + 1 < r) a.y = br * expf(gr - g[s0 + 1]) * kk.y;
-        if (s0 + 2 < r) a.z = br * expf(gr - g[s0 + 2]) * kk.z;
-        if (s0 + 3 < r) a.w = br * expf(gr - g[s0 + 3]) * kk.w;
+        // the exponent is at most 0: the intrinsic's error (a few ulp) is far below the
+        // bf16 rounding every product operand takes later
+        a.x = br * __expf(gr - g[s0]) * kk.x;
+        if (s0 + 1 < r) a.y = br * __expf(gr - g[s0 + 1]) * kk.y;
+        if (s0 + 2 < r) a.z = br * __expf(gr - g[s0 + 2]) * kk.z;
+        if (s0 + 3 < r) a.w = br * __expf(gr - g[s0 + 3]) * kk.w;
       }
       *(float4*)(Tm + hh * C * TS + r * TS + s0) = a;
     }
@@ -460,8 +463,8 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
           const int s = s8 + 2 * u;
           pw[u] = __floats2bfloat162_rn(tv[2 * u] * w[s], tv[2 * u + 1] * w[s + 1]);
           pb[u] = __floats2bfloat162_rn(tv[2 * u] * bb[s], tv[2 * u + 1] * bb[s + 1]);
-          pp[u] = __floats2bfloat162_rn(s <= r ? expf(G[r] - G[s]) * qv[2 * u] : 0.f,
-                                        s + 1 <= r ? expf(G[r] - G[s + 1]) * qv[2 * u + 1] : 0.f);
+          pp[u] = __floats2bfloat162_rn(s <= r ? __expf(G[r] - G[s]) * qv[2 * u] : 0.f,
+                                        s + 1 <= r ? __expf(G[r] - G[s + 1]) * qv[2 * u + 1] : 0.f);
           pt[u] = __floats2bfloat162_rn(tv[2 * u], tv[2 * u + 1]);
         }
         const uint32_t off = tc::sw128_offset(r, s8, C);
@@ -485,6 +488,21 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
           const int b2 = idx / ((C - len) * 8), rem = idx % ((C - len) * 8);
           ((uint4*)(sV + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
         }
+      // diag(c) K with c_s = e^{G_last - G_s} (zero past the chunk): the walk's state
+      // update S <- e^{G_last} S + (diag(c) K)^T Delta takes it as its operand
+      for (int idx = tid; idx < C * (NK / 8); idx += kTcThreads) {
+        const int s = idx % C, k8 = (idx / C) * 8;
+        const uint4 raw = *(const uint4*)(tAQK + tc::sw128_offset(s, k8, 128));
+        const __nv_bfloat162* e = (const __nv_bfloat162*)&raw;
+        const float cs = s < len ? __expf(G[len - 1] - G[s]) : 0.f;
+        __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(e[q]);
+          pk[q] = __floats2bfloat162_rn(f.x * cs, f.y * cs);
+        }
+        *(uint4*)(tKc + tc::sw128_offset(s, k8, C)) = *(const uint4*)pk;
+      }
       tc::fence_async_smem();
       ok = mma_run([&] {
         // W = (T diag(w)) K: B is K read MN-major from the rows of the [K; Q] tile
@@ -510,6 +528,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       __syncthreads();
       if (tid == 0) {
         tc::bulk_s2g(p.Wsw + ch * bKC, tW, bKC);
+        tc::bulk_s2g(p.Kcw + ch * bKC, tKc, bKC);
         tc::bulk_s2g(p.Psw + ch * 8192, tP, 8192);
         if (bwd) {
           tc::bulk_s2g(p.Tb + ch * 16384, tT, 8192);
@@ -547,7 +566,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
 // buffers).  In a fused launch (p.fready set) chunk c's tiles are read only after the
 // preparation unit (c, key head) has published them.  The walk carries only the state:
 // per chunk it writes the chunk-start state (fp32, and as a bf16 S^T tile) and the
-// Delta^T tile, from which the output pass (out_unit) forms O.
+// Delta^T tile, from which the output pass (out_unit) forms O.  Every one of these
+// leaves by a bulk store from shared memory (the fp32 state through two staging
+// buffers): global stores issued by the threads themselves would hold up their next
+// proxy fence until they drain.
 template <int DK>
 __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint32_t tmem,
                                uint64_t* bars) {
@@ -569,11 +591,12 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   uint8_t* buf0 = tSt + tc::sw128_bytes(MV, DK);
   const uint32_t bufsz = bW * 2 + ((bU + bG + 1023) & ~1023u);
   uint8_t* tDt = buf0 + 2 * bufsz;                    // [MV][C] Delta^T
-  uint8_t* tDct = tDt + MV * 128;                     // [MV][C] Delta^T diag(c)
-  float* evb = (float*)(tDct + MV * 128);             // [2][C] e^G, by chunk parity
-  float* cvb = evb + 2 * C;                           // [2][C] e^{G_last - G}
+  const uint32_t bHalf = (uint32_t)(DK / 2) * Dv * 4; // half an fp32 state
+  float* stg0 = (float*)(tDt + MV * 128);             // [DK / 2][Dv] fp32 staging, rows
+  float* stg1 = (float*)((uint8_t*)stg0 + ((bHalf + 1023) & ~1023u));   // 0.. and DK/2..
+  float* evb = (float*)((uint8_t*)stg1 + ((bHalf + 1023) & ~1023u));   // [2][C] e^G
   auto tW = [&](int b) { return buf0 + b * bufsz; };
-  auto tK = [&](int b) { return buf0 + b * bufsz + bW; };
+  auto tK = [&](int b) { return buf0 + b * bufsz + bW; };   // diag(c) K of the value head
   auto sU = [&](int b) { return (const __nv_bfloat16*)(buf0 + b * bufsz + 2 * bW); };
   auto sG = [&](int b) { return (const float*)(buf0 + b * bufsz + 2 * bW + bU); };
   const uint32_t bDt = (uint32_t)MV * 128;            // one Delta^T tile
@@ -585,6 +608,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   // TMEM: X = S^T W^T @0, state update @64
   const uint32_t tX = tmem, tS = tmem + 64;
   uint32_t mphase = 0, lph[2] = {0, 0};
+  const bool f32_states = p.saved && !p.bf16_states;
   const int vrow = acc_row(MV);
   const bool vok = vrow >= 0 && vrow < Dv;
   const size_t SZ = (size_t)DK * Dv;
@@ -606,10 +630,10 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
 
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
-    const size_t chh = (size_t)cc * p.Hv + h, ckk = (size_t)cc * p.Hk + kh;
+    const size_t chh = (size_t)cc * p.Hv + h;
     tc::mbar_arrive_expect_tx(lb, 2 * bW + bU + bG);
     tc::bulk_g2s(tW(b), p.Wsw + chh * bW, bW, lb);
-    tc::bulk_g2s(tK(b), p.Ksw + ckk * bW, bW, lb);
+    tc::bulk_g2s(tK(b), p.Kcw + chh * bW, bW, lb);
     tc::bulk_g2s((void*)sU(b), p.Utb + chh * Dv * C, bU, lb);
     tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
   };
@@ -650,14 +674,12 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       return false;
     }
     const float* G = sG(b);
-    if (tid < C) {
-      evb[b * C + tid] = expf(G[tid]);
-      cvb[b * C + tid] = tid < len ? expf(G[len - 1] - G[tid]) : 0.f;
-    }
+    if (tid == 0) evb[b * C] = expf(G[len - 1]);
     mma_issue([&] {
       // the previous chunk's Delta^T store has read its tile (the epilogue after this
-      // product rewrites it)
-      tc::bulk_wait_read<0>();
+      // product rewrites it); its two fp32 halves, stored after it, may still be read
+      if (f32_states) tc::bulk_wait_read<2>();
+      else tc::bulk_wait_read<0>();
       tc::mma_tile(tX, tc::smem_u32(tSt), MV, tc::smem_u32(tW(b)), C, DK, 0u);
       // the chunk-start state as a bf16 S^T tile, for the output pass and the backward:
       // the saved state itself (GDN_FLAG_BF16_SAVED_STATES) or the workspace copy; one
@@ -677,14 +699,31 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
     }
     ok = start_chunk(c0);
   }
+  // Half `half` (rows k of S in [half DK/2, half DK/2 + DK/2)) of the fp32 state in the
+  // registers into its staging buffer [DK/2][Dv] (a warp's lanes write consecutive v)
+  auto stage_halves = [&]() {
+    if (!vok) return;
+#pragma unroll
+    for (int ii = 0; ii < NKC; ++ii) {
+      const int k0 = grp * 16 + 16 * kGroups * ii;
+      if (k0 < DK)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int k = k0 + j;
+          float* dst = k < DK / 2 ? stg0 + (size_t)k * Dv : stg1 + (size_t)(k - DK / 2) * Dv;
+          dst[vrow] = S[ii][j];
+        }
+    }
+  };
   for (int c = c0; c < c1 && ok; ++c) {
     const int i = c - c0, b = i & 1;
     const int len = chunk_len(c);
-    const float* ev = evb + b * C;
-    const float* cv = cvb + b * C;
+    // the staging buffers' last stores have read them (the barrier below orders this
+    // before the next writes); the state tile's store may still be reading
+    if (tid == 0 && f32_states) tc::bulk_wait_read<1>();
     ok = mma_wait(&bars[0], mphase, p.status, c);
     if (!ok) break;
-    // Delta^T = U^T - X^T and Delta^T diag(c)
+    // Delta^T = U^T - X^T
     const uint8_t* U = (const uint8_t*)sU(b);
 #pragma unroll
     for (int q = 0; q < C / (16 * kGroups); ++q) {
@@ -693,40 +732,31 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       tc::tmem_ld16(tX + lane_quarter() + col0, x);
       tc::tmem_ld_wait();
       if (vok) {
-        float u[16], dc[16];
+        float u[16];
         tile_get16(U, Dv, vrow, col0, u);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          x[j] = u[j] - x[j];
-          dc[j] = x[j] * cv[col0 + j];
-        }
+        for (int j = 0; j < 16; ++j) x[j] = u[j] - x[j];
         tile_put16(tDt, MV, vrow, col0, x);
-        tile_put16(tDct, MV, vrow, col0, dc);
       }
     }
+    // the chunk's fp32 start state, still in the registers, into the staging buffers
+    if (f32_states) stage_halves();
     tc::fence_async_smem();
-    // fp32 saved state of chunk c [chunk][head][Dk][Dv] from the registers (the chunk's
-    // start state): each thread stores its column v of S (a warp's lanes hold
-    // consecutive v, so every store of a warp is one 128-byte row piece), after the fence
-    // above and before the products' wait, so that they drain under the products
-    if (p.saved && !p.bf16_states && vok) {
-      float* dst = p.saved + ((size_t)c * p.Hv + h) * SZ + vrow;
-#pragma unroll
-      for (int ii = 0; ii < NKC; ++ii) {
-        const int k0 = grp * 16 + 16 * kGroups * ii;
-        if (k0 < DK)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) dst[(size_t)(k0 + j) * Dv] = S[ii][j];
-      }
-    }
-    // the state update; the Delta^T tile goes out for the output pass
+    // the state update; the Delta^T tile and the fp32 state go out
     ok = mma_run([&] {
       tc::bulk_wait_read<0>();   // the state tile's store has read S^T: the update may rewrite it
-      // K^T read MN-major from the natural K tile
-      tc::mma_tile_x(tS, tc::smem_u32(tDct), false, (uint32_t)MV * 128u, MV, tc::smem_u32(tK(b)),
+      // (diag(c) K)^T read MN-major from the natural tile
+      tc::mma_tile_x(tS, tc::smem_u32(tDt), false, (uint32_t)MV * 128u, MV, tc::smem_u32(tK(b)),
                      true, 8192u, NKF, C, 0u);
       tc::bulk_s2g(p.Dtb + ((size_t)c * p.Hv + h) * bDt, tDt, bDt);
       tc::bulk_commit();
+      if (f32_states) {
+        float* dst = p.saved + ((size_t)c * p.Hv + h) * SZ;
+        tc::bulk_s2g(dst, stg0, bHalf);
+        tc::bulk_commit();
+        tc::bulk_s2g(dst + (size_t)(DK / 2) * Dv, stg1, bHalf);
+        tc::bulk_commit();
+      }
       // while the tensor core works: is chunk c + 2 prepared (flag read ahead)?
       if (p.fready && c + 2 < c1 && issued == c + 1 &&
           flag_ready(p.fready + (size_t)(c + 2) * p.Hk + kh))
@@ -739,7 +769,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       try_issue(c + 2, false);
     }
     // S^T <- e^{G_last} S^T + Delta^T diag(c) K
-    const float eC = ev[len - 1];
+    const float eC = evb[b * C];
 #pragma unroll
     for (int ii = 0; ii < NKC; ++ii) {
       const int col0 = grp * 16 + 16 * kGroups * ii;
@@ -907,6 +937,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
           publish_flag(p.fready + link.pending);
         }
         link.pending = u;
+        // the first chunk's units are published at once: every walk starts with them
+        if (u < p.Hk) {
+          tc::bulk_wait<0>();
+          publish_flag(p.fready + u);
+          link.pending = -1;
+        }
       }
       if (!ok) break;
     }
@@ -924,7 +960,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
 static size_t prep_tc_smem(const Params& p) {
   const int Dk = p.Dk, Dv = p.Dv;
   size_t b = (size_t)((Dk + 63) / 64) * 128 * 128 + (size_t)((Dv + 63) / 64) * 8192 + 4 * 8192 +
-             tc::sw128_bytes(64, Dk);
+             2 * tc::sw128_bytes(64, Dk);
   b += sizeof(float) * ((size_t)2 * C * C + (size_t)RB * C * TS + RB * 1024 + 3 * RB * C);
   return b + kCtlBytes + 1024;
 }
@@ -951,8 +987,9 @@ static size_t fwd_state_tc_smem(const Params& p) {
   const size_t bW = tc::sw128_bytes(64, DK);
   const size_t bU = (size_t)Dv * C * 2, bG = C * 4;
   const size_t bufsz = bW * 2 + ((bU + bG + 1023) & ~(size_t)1023);
-  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 * 2 + 4 * C * 4 + kCtlBytes +
-         1024;
+  const size_t bHalf = ((size_t)(DK / 2) * Dv * 4 + 1023) & ~(size_t)1023;
+  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 + 2 * bHalf + 2 * C * 4 +
+         kCtlBytes + 1024;
 }
 
 cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st) {
