@@ -68,6 +68,12 @@ _u32 = ctypes.c_uint32
 _lib.gdn_forward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] +
                              [_vp, _vp, _vp, _sz, _u32, _vp])
 _lib.gdn_forward.restype = ctypes.c_int
+# as gdn_forward with z (+ld), gamma, eps, y (+ld) between saved_states and the workspace
+_lib.gdn_forward_gated_rmsnorm.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] +
+                                           [_vp, _vp] + [_vp, _i64, _vp, ctypes.c_float,
+                                                         _vp, _i64] +
+                                           [_vp, _sz, _u32, _vp])
+_lib.gdn_forward_gated_rmsnorm.restype = ctypes.c_int
 # shape; q,k,v,alpha,beta_raw (+ld); a_log, dt_bias, cu, coff, S0; dO (+ld); dS_T, saved;
 # dq,dk,dv,dalpha,dbeta_raw (+ld); da_log, ddt_bias, dS0, ws, ws bytes, flags, stream
 _lib.gdn_backward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64] + [_vp, _vp] +
@@ -129,7 +135,7 @@ EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_for
             "gdn_conv1d_silu_backward", "gdn_gated_rmsnorm_forward",
             "gdn_gated_rmsnorm_workspace_bytes", "gdn_gated_rmsnorm_backward",
             "gdn_state_compose", "gdn_kda_forward", "gdn_kda_backward_workspace_bytes",
-            "gdn_kda_backward")
+            "gdn_kda_backward", "gdn_forward_gated_rmsnorm")
 
 
 class GdnError(RuntimeError):
@@ -355,6 +361,33 @@ def gdn_forward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, chu
     c.ready()
     args.append(_stream(stream))
     _check(_lib.gdn_forward(*args), "gdn_forward")
+
+
+def gdn_forward_gated_rmsnorm(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens,
+                              chunk_offsets, S0, o, S_T, saved_states, z, gamma, eps, y,
+                              workspace, stream=None, flags=0) -> None:
+    """Calls gdn_forward_gated_rmsnorm: gdn_forward, and y = the gated RMSNorm of o with z,
+    gamma [Dv] and eps over each (token, value head) row (fused into the forward's output
+    pass for bf16)."""
+    c = _Call("gdn_forward_gated_rmsnorm")
+    tok = c.token_dtype(shape)
+    T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
+    wv = int(shape.Hv) * int(shape.Dv)
+    args = [ctypes.byref(shape)]
+    args += _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, dt_bias, T,
+                               int(shape.Hv), tok)
+    args += [c.vec(cu_seqlens, "cu_seqlens", N + 1, I32),
+             c.vec(chunk_offsets, "chunk_offsets", N + 1, I32), c.vec(S0, "S0", ns, F32)]
+    args += c.mat(o, "o", T, wv, tok)
+    args += [c.vec(S_T, "S_T", ns, F32),
+             c.buf(saved_states, "saved_states", gdn_saved_state_bytes(shape))]
+    args += c.mat(z, "z", T, wv, tok)
+    args += [c.vec(gamma, "gamma", int(shape.Dv), F32), float(eps)]
+    args += c.mat(y, "y", T, wv, tok)
+    args += [c.buf(workspace, "workspace"), _nbytes(workspace), int(flags)]
+    c.ready()
+    args.append(_stream(stream))
+    _check(_lib.gdn_forward_gated_rmsnorm(*args), "gdn_forward_gated_rmsnorm")
 
 
 def gdn_backward(shape, q, k, v, alpha, beta_raw, a_log, dt_bias, cu_seqlens, chunk_offsets, S0,

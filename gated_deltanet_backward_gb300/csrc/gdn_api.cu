@@ -419,12 +419,23 @@ size_t gdn_workspace_bytes(const gdn_shape* s, int is_backward) {
   return gdn::ws_layout(*s, is_backward != 0).total;
 }
 
-int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, int64_t k_ld,
-                const void* v, int64_t v_ld, const float* alpha, int64_t alpha_ld,
-                const float* beta_raw, int64_t beta_ld, const float* a_log,
-                const float* dt_bias, const int32_t* cu_seqlens, const int32_t* chunk_offsets,
-                const float* S0, void* o, int64_t o_ld, float* S_T, void* saved_states,
-                void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+// The gated RMSNorm that a forward may apply to its own output (y null: none).
+struct FwdNorm {
+  const void* z = nullptr;
+  int64_t z_ld = 0;
+  const float* gamma = nullptr;
+  float eps = 0.f;
+  void* y = nullptr;
+  int64_t y_ld = 0;
+};
+
+static int forward_impl(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                        int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                        int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                        const float* a_log, const float* dt_bias, const int32_t* cu_seqlens,
+                        const int32_t* chunk_offsets, const float* S0, void* o, int64_t o_ld,
+                        float* S_T, void* saved_states, void* workspace, size_t workspace_bytes,
+                        uint32_t flags, const FwdNorm& nm, void* stream) {
   GDN_TRY(check_shape(s));
   if (flags & ~(uint32_t)(GDN_FLAG_KEEP_FOR_BACKWARD | GDN_FLAG_BF16_SAVED_STATES))
     return GDN_ERR_INVALID_ARG;
@@ -435,6 +446,16 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
                        dt_bias, cu_seqlens, chunk_offsets, S0));
   const size_t es = s->dtype == GDN_DTYPE_BF16 ? 2 : 4;
   GDN_TRY(check_matrix(o, o_ld, (int64_t)s->Hv * s->Dv, es, s->total_tokens));
+  if (nm.y) {
+    const int64_t T = s->total_tokens, W = (int64_t)s->Hv * s->Dv;
+    size_t nes = 0;
+    GDN_TRY(check_norm(s->dtype, T, s->Hv, s->Dv, nm.eps, nm.gamma, &nes));
+    GDN_TRY(check_matrix(nm.z, nm.z_ld, W, es, T));
+    GDN_TRY(check_matrix(nm.y, nm.y_ld, W, es, T));
+    if (overlaps(o, o_ld, nm.y, nm.y_ld, T, W, es) || overlaps(nm.z, nm.z_ld, nm.y, nm.y_ld, T, W, es) ||
+        overlaps(o, o_ld, nm.z, nm.z_ld, T, W, es))
+      return GDN_ERR_INVALID_ARG;
+  }
   GDN_TRY(check_vec(S_T, false));
   // a forward that no backward reads (prefill, inference) may skip the saved states
   GDN_TRY(check_vec(saved_states, keep && s->total_chunks > 0));
@@ -477,9 +498,58 @@ int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, 
       return GDN_ERR_CUDA;
     }
   }
+  if (nm.y && bf16) {
+    // bf16: the output pass normalises the rows it forms
+    p.nz = nm.z;
+    p.nz_ld = nm.z_ld;
+    p.ngamma = nm.gamma;
+    p.neps = nm.eps;
+    p.ny = nm.y;
+    p.ny_ld = nm.y_ld;
+  }
   e = gdn::launch_forward(p, bf16 ? &maps : nullptr, st);
   if (e != cudaSuccess) return cuda_fail("gdn_forward: kernel launch", e);
+  if (nm.y && !bf16 && s->total_tokens > 0) {
+    e = gdn::launch_gated_rmsnorm(false, s->dtype, s->total_tokens, s->Hv, s->Dv, nm.eps, o, o_ld,
+                                  nm.z, nm.z_ld, nm.gamma, nullptr, 0, nm.y, nm.y_ld, nullptr, 0,
+                                  nullptr, nullptr, st);
+    if (e != cudaSuccess) return cuda_fail("gdn_forward_gated_rmsnorm: norm launch", e);
+  }
   return GDN_OK;
+}
+
+int gdn_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, int64_t k_ld,
+                const void* v, int64_t v_ld, const float* alpha, int64_t alpha_ld,
+                const float* beta_raw, int64_t beta_ld, const float* a_log,
+                const float* dt_bias, const int32_t* cu_seqlens, const int32_t* chunk_offsets,
+                const float* S0, void* o, int64_t o_ld, float* S_T, void* saved_states,
+                void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+  return forward_impl(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
+                      dt_bias, cu_seqlens, chunk_offsets, S0, o, o_ld, S_T, saved_states,
+                      workspace, workspace_bytes, flags, FwdNorm(), stream);
+}
+
+int gdn_forward_gated_rmsnorm(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                              int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                              int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                              const float* a_log, const float* dt_bias,
+                              const int32_t* cu_seqlens, const int32_t* chunk_offsets,
+                              const float* S0, void* o, int64_t o_ld, float* S_T,
+                              void* saved_states, const void* z, int64_t z_ld,
+                              const float* gamma, float eps, void* y, int64_t y_ld,
+                              void* workspace, size_t workspace_bytes, uint32_t flags,
+                              void* stream) {
+  if (!y) return GDN_ERR_INVALID_ARG;
+  FwdNorm nm;
+  nm.z = z;
+  nm.z_ld = z_ld;
+  nm.gamma = gamma;
+  nm.eps = eps;
+  nm.y = y;
+  nm.y_ld = y_ld;
+  return forward_impl(s, q, q_ld, k, k_ld, v, v_ld, alpha, alpha_ld, beta_raw, beta_ld, a_log,
+                      dt_bias, cu_seqlens, chunk_offsets, S0, o, o_ld, S_T, saved_states,
+                      workspace, workspace_bytes, flags, nm, stream);
 }
 
 int gdn_backward(const gdn_shape* s, const void* q, int64_t q_ld, const void* k, int64_t k_ld,

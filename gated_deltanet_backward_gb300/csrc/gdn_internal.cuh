@@ -182,6 +182,14 @@ struct Params {
   uint32_t* bwork;   // fused backward: next gradient unit
   uint32_t* bready;  // fused backward: [NC][Hv] state-walk chunk done
   uint32_t tag;  // shape tag (see shape_tag); written by a keeping forward, checked by a reusing backward
+  // forward with the gated RMSNorm of o fused into its output pass (ny null: none):
+  // y = (o / sqrt(mean o^2 + neps)) * ngamma * SiLU(z) per (token, value head) row
+  const void* nz;
+  int64_t nz_ld;
+  const float* ngamma;
+  float neps;
+  void* ny;
+  int64_t ny_ld;
   int keep;      // forward: leave the backward's chunk operands in the workspace
   int bf16_states;  // chunk-start states as bf16 S^T tiles (GDN_FLAG_BF16_SAVED_STATES)
                     // instead of fp32 [NC][Hv][Dk][Dv]

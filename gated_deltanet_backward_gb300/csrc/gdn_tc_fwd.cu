@@ -853,25 +853,64 @@ __device__ void out_unit(const Params& p, int c, int h, uint8_t* sm, uint32_t tm
     tc::mma_tile(tO2, tc::smem_u32(tP), 64, tc::smem_u32(tD), Dv, C, 0u);
   }, &bars[1], mph, p.status, c);
   if (!ok) return;
-  // token row r of the chunk per accumulator lane, 16 consecutive values per thread
+  // token row r of the chunk per accumulator lane, 16 consecutive values per thread (Dv
+  // <= 128: one piece per thread; a row's pieces sit in the 8 threads of its lane pair in
+  // the kGroups warps of its lane quarter)
   const int r = x2_row();
+  const int col = grp * 16 + x2_half() * 16 * kGroups;
+  const bool mine = r < len && col < Dv;
   __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + r) * p.o_ld + (int64_t)h * Dv;
-  for (int c0 = grp * 16; c0 < Dv; c0 += 32 * kGroups) {
-    float o1[16], o2[16];
-    tc::tmem_ld16_x2<16 * kGroups>(tO1 + lane_quarter() + c0, o1);
-    tc::tmem_ld16_x2<16 * kGroups>(tO2 + lane_quarter() + c0, o2);
-    tc::tmem_ld_wait();
-    const int col = c0 + x2_half() * 16 * kGroups;
-    if (r < len && col < Dv) {
-      const float e = ev[r];
-      __align__(16) __nv_bfloat162 pk[8];
+  float o1[16], o2[16];
+  tc::tmem_ld16_x2<16 * kGroups>(tO1 + lane_quarter() + grp * 16, o1);
+  tc::tmem_ld16_x2<16 * kGroups>(tO2 + lane_quarter() + grp * 16, o2);
+  tc::tmem_ld_wait();
+  __align__(16) __nv_bfloat162 pk[8];
+  {
+    const float e = ev[r];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        pk[j] = __floats2bfloat162_rn(fmaf(e, o1[2 * j], p.scale * o2[2 * j]),
-                                      fmaf(e, o1[2 * j + 1], p.scale * o2[2 * j + 1]));
-      uint4* dst = (uint4*)(orow + col);
-      dst[0] = ((const uint4*)pk)[0];
-      dst[1] = ((const uint4*)pk)[1];
+    for (int j = 0; j < 8; ++j)
+      pk[j] = __floats2bfloat162_rn(fmaf(e, o1[2 * j], p.scale * o2[2 * j]),
+                                    fmaf(e, o1[2 * j + 1], p.scale * o2[2 * j + 1]));
+  }
+  if (mine) {
+    uint4* dst = (uint4*)(orow + col);
+    dst[0] = ((const uint4*)pk)[0];
+    dst[1] = ((const uint4*)pk)[1];
+  }
+  if (p.ny) {
+    // gated RMSNorm of the row of o as stored (bf16): the sum of squares over the row's
+    // pieces (lane pair, then the kGroups warps in a fixed order through shared memory)
+    float* red = ev + C;   // [kGroups][C]
+    float ss = 0.f;
+    if (mine)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 f = __bfloat1622float2(pk[j]);
+        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+      }
+    ss = x2_pair_sum(ss);
+    if (x2_half() == 0) red[grp * C + r] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) tot += red[g * C + r];
+    if (mine) {
+      const float inv = rsqrtf(fmaf(tot, 1.f / (float)Dv, p.neps));
+      const __nv_bfloat16* zrow = (const __nv_bfloat16*)p.nz + (t0 + r) * p.nz_ld + (int64_t)h * Dv;
+      const uint4 za = *(const uint4*)(zrow + col), zb = *(const uint4*)(zrow + col + 8);
+      const __nv_bfloat162* z2[2] = {(const __nv_bfloat162*)&za, (const __nv_bfloat162*)&zb};
+      __align__(16) __nv_bfloat162 yk[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 f = __bfloat1622float2(pk[j]);
+        const float2 z = __bfloat1622float2(z2[j >> 2][j & 3]);
+        const float g0 = p.ngamma[col + 2 * j], g1 = p.ngamma[col + 2 * j + 1];
+        yk[j] = __floats2bfloat162_rn(f.x * inv * g0 * (z.x * sigmoid_f(z.x)),
+                                      f.y * inv * g1 * (z.y * sigmoid_f(z.y)));
+      }
+      uint4* ydst = (uint4*)((__nv_bfloat16*)p.ny + (t0 + r) * p.ny_ld + (int64_t)h * Dv + col);
+      ydst[0] = ((const uint4*)yk)[0];
+      ydst[1] = ((const uint4*)yk)[1];
     }
   }
 }
@@ -881,7 +920,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_fwd_out_tc(Params p) {
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
   cta_setup(ctl, 2, 256);
-  out_unit(p, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
+  // value heads of one chunk are consecutive CTAs: they share the key head's Q tile
+  // through the L2 while it is there
+  out_unit(p, (int)(blockIdx.x / p.Hv), (int)(blockIdx.x % p.Hv), base + kCtlBytes, ctl->tmem,
+           ctl->bar);
   cta_teardown(ctl, 256);
 }
 
@@ -968,7 +1010,7 @@ static size_t prep_tc_smem(const Params& p) {
 static size_t out_tc_smem(const Params& p) {
   const int Dk = p.Dk, Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   return tc::sw128_bytes(64, Dk) + tc::sw128_bytes(MV, Dk) + (size_t)MV * 128 + 8192 +
-         2 * C * 4 + kCtlBytes + 1024;
+         (2 + kGroups) * C * 4 + kCtlBytes + 1024;
 }
 
 cudaError_t launch_fwd_out_tc(const Params& p, cudaStream_t st) {
@@ -976,7 +1018,7 @@ cudaError_t launch_fwd_out_tc(const Params& p, cudaStream_t st) {
   const size_t smem = out_tc_smem(p);
   cudaFuncSetAttribute(k_fwd_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_FWD_OUT_TC);
-  k_fwd_out_tc<<<dim3(p.NC, p.Hv), kTcThreads, smem, st>>>(p);
+  k_fwd_out_tc<<<(unsigned)p.NC * p.Hv, kTcThreads, smem, st>>>(p);
   profile_post(st);
   return cudaGetLastError();
 }

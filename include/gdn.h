@@ -351,6 +351,32 @@ int gdn_gated_rmsnorm_forward(int32_t dtype, int64_t total_tokens, int32_t n_hea
                               const void* z, int64_t z_ld, const float* gamma, void* y,
                               int64_t y_ld, void* stream);
 size_t gdn_gated_rmsnorm_workspace_bytes(int32_t head_dim);
+
+/* gdn_forward followed by gdn_gated_rmsnorm_forward of its output over the Hv value heads
+ * (n_heads = Hv, head_dim = Dv): o as gdn_forward writes it, and y = the gated RMSNorm of
+ * each (token, value head) row of o with z, gamma and eps, the norm taken over o as stored
+ * (its element type).  With bf16 inputs the norm runs in the epilogue of the forward's
+ * output pass, which holds each row's Dv values when it stores them, so y costs one read
+ * of z and one write of y instead of a further pass over o; with fp32 inputs it is the
+ * separate norm kernel after the forward.  o is still written: the norm's backward reads
+ * it.  Arguments as gdn_forward and gdn_gated_rmsnorm_forward:
+ *   z, z_ld   device, [total_tokens, z_ld] of the shape's dtype, Hv*Dv used columns
+ *   gamma     device, fp32 [Dv];  eps >= 0, finite
+ *   y, y_ld   device, [total_tokens, y_ld] of the shape's dtype (written)
+ * y must not overlap o or z, and o must not overlap z (GDN_ERR_INVALID_ARG); y NULL is
+ * GDN_ERR_INVALID_ARG.  The rows agree with gdn_gated_rmsnorm_forward on this o to within
+ * the rounding of the sum of squares (the two sum the row in different orders).
+ * Returns a gdn_status. */
+int gdn_forward_gated_rmsnorm(const gdn_shape* shape, const void* q, int64_t q_ld,
+                              const void* k, int64_t k_ld, const void* v, int64_t v_ld,
+                              const float* alpha, int64_t alpha_ld, const float* beta_raw,
+                              int64_t beta_ld, const float* a_log, const float* dt_bias,
+                              const int32_t* cu_seqlens, const int32_t* chunk_offsets,
+                              const float* S0, void* o, int64_t o_ld, float* S_T,
+                              void* saved_states, const void* z, int64_t z_ld,
+                              const float* gamma, float eps, void* y, int64_t y_ld,
+                              void* workspace, size_t workspace_bytes, uint32_t flags,
+                              void* stream);
 int gdn_gated_rmsnorm_backward(int32_t dtype, int64_t total_tokens, int32_t n_heads,
                                int32_t head_dim, float eps, const void* o, int64_t o_ld,
                                const void* z, int64_t z_ld, const float* gamma, const void* dy,

@@ -247,3 +247,32 @@ def test_kda_checks(gdn):
     assert runb(shape=ctypes.byref(narrow)) == UNSUPPORTED    # 32-column state slices
     many = gdn.make_shape(Hk, Hv, Dk, Dv, 65536, 0, 65536, "bf16")
     assert runb(shape=ctypes.byref(many)) == UNSUPPORTED
+
+
+# --- gdn_forward_gated_rmsnorm -----------------------------------------------------------
+
+FWDN_ORDER = ["shape", "q", "q_ld", "k", "k_ld", "v", "v_ld", "alpha", "alpha_ld", "beta",
+              "beta_ld", "a_log", "dt", "cu", "coff", "S0", "o", "o_ld", "S_T", "saved", "z",
+              "z_ld", "gamma", "eps", "y", "y_ld", "ws", "ws_bytes", "flags", "stream"]
+
+
+def test_forward_gated_rmsnorm_checks(gdn):
+    f = Fake()
+    s = gdn.make_shape(2, 6, 64, 64, 1, 2, 100, "bf16")
+    ws = gdn.gdn_workspace_bytes(s, False)
+    wq, wv = 2 * 64, 6 * 64
+    a = dict(shape=ctypes.byref(s), q=f(), q_ld=wq, k=f(), k_ld=wq, v=f(), v_ld=wv, alpha=f(),
+             alpha_ld=6, beta=f(), beta_ld=6, a_log=f(), dt=f(), cu=f(), coff=f(), S0=None,
+             o=f(), o_ld=wv, S_T=None, saved=None, z=f(), z_ld=wv, gamma=f(), eps=1e-6, y=f(),
+             y_ld=wv, ws=f(), ws_bytes=ws, flags=0, stream=None)
+    run = lambda **o: _call(gdn._lib.gdn_forward_gated_rmsnorm, FWDN_ORDER, a, **o)
+    assert run(y=None) == INVALID
+    assert run(gamma=None) == INVALID
+    assert run(z=None) == INVALID
+    assert run(eps=-1.0) == INVALID and run(eps=float("nan")) == INVALID
+    assert run(y=a["o"]) == INVALID and run(y=a["z"]) == INVALID and run(z=a["o"]) == INVALID
+    assert run(z_ld=wv + 1) == MISALIGNED and run(y=a["y"] + 2) == MISALIGNED
+    assert run(y_ld=wv - 8) == INVALID
+    # the recurrence's own checks come first, as in gdn_forward
+    assert run(q=None) == INVALID
+    assert run(ws_bytes=ws - 1) == WORKSPACE
