@@ -44,23 +44,29 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-
 // Locates global chunk c: its sequence n, first token t0 and length len.
 // Returns false (and the caller records GDN_ERR_DEVICE_BOUNDS) when
 // cu_seqlens / chunk_offsets do not describe chunk c consistently.
-__device__ __forceinline__ bool chunk_info(const Params& p, int c, int* n_out, int64_t* t0,
-                                           int* len) {
-  if (p.n_seqs <= 0 || c < 0 || c >= p.NC) return false;
-  int lo = 0, hi = p.n_seqs - 1;
+__device__ __forceinline__ bool chunk_info_at(const int32_t* cu, const int32_t* coff, int n_seqs,
+                                              int NC, int64_t T, int c, int* n_out, int64_t* t0,
+                                              int* len) {
+  if (n_seqs <= 0 || c < 0 || c >= NC) return false;
+  int lo = 0, hi = n_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.coff[mid] <= c) lo = mid; else hi = mid - 1;
+    if (coff[mid] <= c) lo = mid; else hi = mid - 1;
   }
   const int n = lo;
-  const int j = c - p.coff[n];
-  const int64_t s = p.cu[n], e = p.cu[n + 1];
+  const int j = c - coff[n];
+  const int64_t s = cu[n], e = cu[n + 1];
   const int64_t start = s + (int64_t)j * kChunk;
-  if (j < 0 || c >= p.coff[n + 1] || s < 0 || e < s || e > p.T || start >= e) return false;
+  if (j < 0 || c >= coff[n + 1] || s < 0 || e < s || e > T || start >= e) return false;
   *n_out = n;
   *t0 = start;
   *len = (int)((e - start) < kChunk ? (e - start) : kChunk);
   return true;
+}
+// chunk_info_at on the batch's own cu_seqlens / chunk_offsets (global memory)
+__device__ __forceinline__ bool chunk_info(const Params& p, int c, int* n_out, int64_t* t0,
+                                           int* len) {
+  return chunk_info_at(p.cu, p.coff, p.n_seqs, p.NC, p.T, c, n_out, t0, len);
 }
 
 // Checks that sequence n's chunk range matches its token range.

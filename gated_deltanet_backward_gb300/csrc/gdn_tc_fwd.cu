@@ -194,42 +194,93 @@ struct PrepLink {
   int pending;     // the previous unit, whose tile stores may still be in flight and whose
                    // flag is unpublished; -1 if none
   int next;        // the unit this CTA takes next, or -1
-  bool kq_issued;  // this unit's raw k / q tiles were issued by the previous unit
+  bool kq_issued;  // this unit's raw k / q tiles and its first value head's V tile were
+                   // issued by the previous unit
 };
 
-// Thread 0: the raw k and q rows of unit (c, kh) as TMA boxes into the [K; Q] tile,
-// on one phase of `bar`.  False (nothing issued) for a chunk outside the batch.
-__device__ bool issue_kq(const Params& p, const TmaMaps& maps, int c, int kh, uint8_t* tAQK,
-                         uint64_t* bar) {
-  int n, len;
-  int64_t t0;
-  if (!chunk_info(p, c, &n, &t0, &len)) return false;
+// Bytes of prep_unit's buffers (the sequence table follows them).
+__host__ __device__ __forceinline__ size_t prep_buffers_bytes(int Dk, int Dv) {
+  const size_t b = (size_t)((Dk + 63) / 64) * 128 * 128 + (size_t)((Dv + 63) / 64) * 8192 +
+                   2 * 8192;
+  return b + sizeof(float) * ((size_t)C * C + (size_t)C * TS + (size_t)RB * C * TS + RB * 1024 +
+                              3 * RB * C);
+}
+
+// The batch's cu_seqlens and chunk offsets copied into shared memory for the
+// preparation's chunk lookups (each a global round trip otherwise, on the path of the
+// thread that issues the copies), for batches of fewer than kSeqCache sequences.
+constexpr int kSeqCache = 1024;
+struct SeqTab {
+  const int32_t* cu;
+  const int32_t* coff;
+};
+// All threads, then a CTA barrier: fills the cache at `sm` (2 kSeqCache int32) if the
+// batch fits, and returns the table to read.
+__device__ SeqTab seq_tab(const Params& p, int32_t* sm) {
+  const int m = p.n_seqs + 1;
+  const bool fits = m <= kSeqCache;
+  if (fits)
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+      sm[i] = p.cu[i];
+      sm[kSeqCache + i] = p.coff[i];
+    }
+  __syncthreads();
+  return fits ? SeqTab{sm, sm + kSeqCache} : SeqTab{p.cu, p.coff};
+}
+__device__ __forceinline__ bool chunk_info(const Params& p, const SeqTab& tab, int c, int* n,
+                                           int64_t* t0, int* len) {
+  return chunk_info_at(tab.cu, tab.coff, p.n_seqs, p.NC, p.T, c, n, t0, len);
+}
+
+// Thread 0: the raw k and q rows of key head kh of the chunk starting at token t0 as TMA
+// boxes into the [K; Q] tile, on one phase of `bar`.
+__device__ void issue_kq(const Params& p, const TmaMaps& maps, int64_t t0, int kh,
+                         uint8_t* tAQK, uint64_t* bar) {
   const int nbk = (p.Dk + 63) / 64;
   tc::mbar_arrive_expect_tx(bar, 2u * nbk * 8192u);
   for (int b = 0; b < nbk; ++b) {
     tc::tma_load_2d(tAQK + b * 128 * 128, &maps.k, kh * p.Dk + 64 * b, (int)t0, bar);
     tc::tma_load_2d(tAQK + b * 128 * 128 + 8192, &maps.q, kh * p.Dk + 64 * b, (int)t0, bar);
   }
-  return true;
+}
+
+// Thread 0: the natural V tile of value head j of key head kh (chunk at token t0) into
+// `dst`, on one phase of `bar`.
+__device__ void issue_v(const Params& p, const TmaMaps& maps, int64_t t0, int kh, int j,
+                        uint8_t* dst, uint64_t* bar) {
+  const int nbv = (p.Dv + 63) / 64, h = value_head(p, kh, j);
+  tc::mbar_arrive_expect_tx(bar, (uint32_t)nbv * 8192u);
+  for (int b = 0; b < nbv; ++b)
+    tc::tma_load_2d(dst + b * 8192, &maps.v, h * p.Dv + 64 * b, (int)t0, bar);
 }
 
 // One (chunk c, key head kh) unit of the preparation on a whole CTA.  `sm` is its
-// shared memory (1024-aligned, prep_tc_smem bytes), `tmem` 256 TMEM columns, bar[0] /
-// bar[1] the MMA and load mbarriers with their running phases.  Without `link` every
-// write of the unit has completed when it returns.  With it (fused forward) the unit
-// publishes link->pending's flag once that unit's stores are done, before issuing its
-// own, returns with its own stores possibly in flight, and issues link->next's k / q
-// tiles once its last product has read its own (setting link->kq_issued).  False
-// after a timed-out wait.
-__device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, int kh,
-                          uint8_t* sm, uint32_t tmem, uint64_t* bar, uint32_t& phase,
-                          uint32_t& lphase, PrepLink* link) {
+// shared memory (1024-aligned, prep_tc_smem bytes, ending in the sequence table `tab`
+// may point to), `tmem` 256 TMEM columns, bar[0] /
+// bar[1] the MMA and k / q load mbarriers with their running phases, bar[2] / bar[3] the
+// two V buffers' (phases in bits 0 / 1 of vphase).  The value heads' V tiles land ahead
+// of use: head 0's with the k / q rows, the next head's in the second buffer (the K K^T
+// region, free once A is formed; only when the unit's heads form one group) and the
+// head after that as soon as the product of the head before it has read the buffer.
+// Every workspace tile leaves by plain stores from the threads that form it (the
+// natural K / Q tiles at the normalisation, K K^T at the Gram epilogue, diag(c) K, P and
+// the backward's T tiles while a head's products run, W and U^T at its epilogue): no
+// bulk store, so the copy engine serves the loads alone.  Without `link` the unit's
+// writes are done when the kernel ends.  With it (fused forward) the unit publishes
+// link->pending's flag (that unit's writes all came before this unit's CTA barriers)
+// once the inverse's inputs are formed, and issues link->next's k / q tiles and first V
+// tile once its last product has read its own (setting link->kq_issued; link->next is
+// the raw work-counter value, a unit index only below NC Hk).  False after a timed-out
+// wait.
+__device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& tab, int bwd,
+                          int c, int kh, uint8_t* sm, uint32_t tmem, uint64_t* bar,
+                          uint32_t& phase, uint32_t& lphase, uint32_t& vphase, PrepLink* link) {
   int n;
   int64_t t0;
   int len;
   const bool kq_issued = link != nullptr && link->kq_issued;
   if (link != nullptr && threadIdx.x == 0) link->kq_issued = false;
-  if (!chunk_info(p, c, &n, &t0, &len)) {
+  if (!chunk_info(p, tab, c, &n, &t0, &len)) {
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
     return true;
   }
@@ -243,43 +294,38 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
   uint8_t* sV = tAQK + nbk * aqk_pitch;                 // [C][Dv] natural V of one head (TMA)
   uint8_t* tTW = sV + nbv * 8192;                       // [C][C] T diag(b e^G)
   uint8_t* tTB = tTW + 8192;                            // [C][C] T diag(b)
-  uint8_t* tP = tTB + 8192;                             // [C][C] P
-  uint8_t* tT = tP + 8192;                              // [C][C] T (backward)
-  uint8_t* tW = tT + 8192;                              // [C][Dk] W
-  uint8_t* tKc = tW + bKC;                              // [C][Dk] diag(c) K of one head
-  float* KK = (float*)(tKc + bKC);                      // [C][C]
-  float* QK = KK + C * C;                               // [C][C]
-  float* Tm = QK + C * C;                               // [RB][C][TS]
+  float* KK = (float*)(tTB + 8192);                     // [C][C]
+  float* QK = KK + C * C;                               // [C][TS]
+  float* Tm = QK + C * TS;                              // [RB][C][TS]
   float* Mt = Tm + RB * C * TS;                         // [RB][1024] scratch of the inverse
   float* gv = Mt + RB * 1024;                           // [RB][C]
   float* bv = gv + RB * C;                              // [RB][C]
   float* wv = bv + RB * C;                              // [RB][C]
 
-  // W's padding columns (Dk < 64) stay zero: the epilogue writes only columns < Dk (once
-  // the previous unit's W store has read the tile)
-  if (Dk < 64) {
-    if (tid == 0) tc::bulk_wait_read<0>();
-    __syncthreads();
-    for (int i = tid; i < (int)bKC / 16; i += kTcThreads) ((uint4*)tW)[i] = make_uint4(0, 0, 0, 0);
-  }
   __syncthreads();
   // TMEM columns: [0, 64) the Gram products, [64, 64 + NK) W, [192, 256) U^T
   const uint32_t tAccW = tmem + 64, tAccU = tmem + 192;
   bool ok = true;
   // the first head group's raw gate inputs, loaded while the q/k tiles are in flight
-  float pre_beta = 0.f, pre_x = 0.f;
+  float pre_beta = 0.f, pre_x = 0.f, pre_al = 0.f;
   {
     const int nh0 = p.r < RB ? p.r : RB;
     if (tid < nh0 * C && tid % C < len) {
       const int t = tid % C, h = value_head(p, kh, tid / C);
       pre_beta = p.beta_raw[(t0 + t) * p.beta_ld + h];
       pre_x = p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
+      pre_al = p.a_log[h];
     }
   }
   const size_t ckk = (size_t)c * p.Hk + kh, ck = ckk * C;
   // raw k and q rows of the chunk: TMA boxes straight into the [K; Q] operand tile
   // (issued by the previous unit when it could)
-  if (tid == 0 && !kq_issued) issue_kq(p, maps, c, kh, tAQK, &bar[1]);
+  if (tid == 0 && !kq_issued) {
+    issue_kq(p, maps, t0, kh, tAQK, &bar[1]);
+    issue_v(p, maps, t0, kh, 0, sV, &bar[2]);
+  }
+  // the unit's value heads form one group of at most RB: odd heads take the second buffer
+  const bool two_v = p.r <= RB;
   {
     const bool lok = tc::mbar_wait(&bar[1], lphase);
     lphase ^= 1u;
@@ -325,6 +371,9 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
           pk[q] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
         }
         *(uint4*)(tAQK + tc::sw128_offset(row, (part * cpt + j) * 8, 128)) = *(const uint4*)pk;
+        // the natural K or Q tile of the key head in the workspace, row by row
+        *(uint4*)((isq ? p.Qsw : p.Ksw) + ckk * bKC +
+                  tc::sw128_offset(t, (part * cpt + j) * 8, 64)) = *(const uint4*)pk;
       }
     if (bwd && part == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
     // Dk < 64: the box's columns past Dk (a neighbouring head) become zero padding
@@ -333,45 +382,32 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       for (int idx = tid; idx < 2 * C * padc; idx += kTcThreads) {
         const int row = idx / padc, c0 = (Dk / 8 + idx % padc) * 8;
         *(uint4*)(tAQK + tc::sw128_offset(row, c0, 128)) = make_uint4(0, 0, 0, 0);
+        *(uint4*)((row >= C ? p.Qsw : p.Ksw) + ckk * bKC + tc::sw128_offset(row & (C - 1), c0, 64)) =
+            make_uint4(0, 0, 0, 0);
       }
     }
   }
   tc::fence_async_smem();
   __syncthreads();
-  // the natural K and Q tiles of this key head go to the workspace as they are; first
-  // the previous unit's stores are waited for and its flag published
-  if (tid == 0) {
-    if (link != nullptr && link->pending >= 0) {
-      tc::bulk_wait<0>();
-      publish_flag(p.fready + link->pending);
-      link->pending = -1;
-    }
-    for (int b = 0; b < nbk; ++b) {
-      tc::bulk_s2g(p.Ksw + ckk * bKC + b * 8192, tAQK + b * aqk_pitch, 8192);
-      tc::bulk_s2g(p.Qsw + ckk * bKC + b * 8192, tAQK + b * aqk_pitch + 8192, 8192);
-    }
-    tc::bulk_commit();
-  }
   // 2. [K; Q] K^T -> TMEM columns [0, 64): lanes 0-63 K K^T, lanes 64-127 Q K^T.
   ok = mma_run([&] { tc::mma_tile_p(tmem, tc::smem_u32(tAQK), aqk_pitch, 128, tc::smem_u32(tAQK),
                                      aqk_pitch, 64, Dk, 0u); },
                &bar[0], phase, p.status, c);
   if (!ok) goto done;
   acc_walk(tmem, 128, 64, 128, [&](int row, int col0, const float* v) {
-    float* dst = row < C ? KK + row * C : QK + (row - C) * C;
+    float* dst = row < C ? KK + row * C : QK + (row - C) * TS;
     *(float4*)(dst + col0) = make_float4(v[0], v[1], v[2], v[3]);
     *(float4*)(dst + col0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
     *(float4*)(dst + col0 + 8) = make_float4(v[8], v[9], v[10], v[11]);
     *(float4*)(dst + col0 + 12) = make_float4(v[12], v[13], v[14], v[15]);
-  });
-  if (bwd) {
-    tc::fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {   // K K^T (fp32, row-major) for the gradient kernel
-      tc::bulk_s2g(p.KKf + ck * C, KK, C * C * 4);
-      tc::bulk_commit();
+    if (bwd && row < C) {   // K K^T (fp32, row-major) for the gradient kernel
+      float* g = p.KKf + (ck + row) * C + col0;
+      *(float4*)(g) = make_float4(v[0], v[1], v[2], v[3]);
+      *(float4*)(g + 4) = make_float4(v[4], v[5], v[6], v[7]);
+      *(float4*)(g + 8) = make_float4(v[8], v[9], v[10], v[11]);
+      *(float4*)(g + 12) = make_float4(v[12], v[13], v[14], v[15]);
     }
-  }
+  });
   __syncthreads();
 
   for (int g0 = 0; g0 < p.r; g0 += RB) {
@@ -384,7 +420,7 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
         const float braw = g0 == 0 ? pre_beta : p.beta_raw[(t0 + t) * p.beta_ld + h];
         const float x = g0 == 0 ? pre_x : p.alpha[(t0 + t) * p.alpha_ld + h] + p.dt_bias[h];
         b = sigmoid_f(braw);
-        l = -expf(p.a_log[h]) * softplus_f(x);
+        l = -expf(g0 == 0 ? pre_al : p.a_log[h]) * softplus_f(x);
       }
       gv[hh * C + t] = l;
       bv[hh * C + t] = b;
@@ -428,7 +464,16 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       }
       *(float4*)(Tm + hh * C * TS + r * TS + s0) = a;
     }
+    tc::fence_async_smem();   // the K K^T reads come before the V tile that replaces it
     __syncthreads();
+    if (g0 == 0 && tid == 0) {
+      // every write of the previous unit came before this CTA's barriers: publish it
+      if (link != nullptr && link->pending >= 0) {
+        publish_flag(p.fready + link->pending);
+        link->pending = -1;
+      }
+      if (two_v && p.r > 1) issue_v(p, maps, t0, kh, 1, (uint8_t*)KK, &bar[3]);
+    }
     // 4. T = (I + A)^-1 for the nh heads at once
     tri_inverse(Tm, nh, Mt);
     // 5. per head: W = T diag(w) K, U^T = V^T (T diag(b))^T, P
@@ -436,46 +481,85 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       const int h = value_head(p, kh, g0 + hh);
       const size_t ch = (size_t)c * p.Hv + h;
       const float* T = Tm + hh * C * TS;
+      const int j = g0 + hh;
+      const bool odd = two_v && (j & 1);
+      uint8_t* vb = odd ? (uint8_t*)KK : sV;   // this head's V tile
       if (tid == 0) {
-        // the previous head's tile stores have read their sources
-        tc::bulk_wait_read<0>();
-        // this head's V rows, landing while the T tiles are staged
-        tc::mbar_arrive_expect_tx(&bar[1], (uint32_t)nbv * 8192u);
-        for (int b = 0; b < nbv; ++b)
-          tc::tma_load_2d(sV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bar[1]);
+        // the maps of the loads this head issues after its products
+        tc::prefetch_tensormap(&maps.v);
+        if (j + 1 == p.r) {
+          tc::prefetch_tensormap(&maps.k);
+          tc::prefetch_tensormap(&maps.q);
+        }
       }
       __syncthreads();
       const float* w = wv + hh * C;
       const float* bb = bv + hh * C;
       const float* G = gv + hh * C;
-      // T diag(w), T diag(b), P and (backward) T: one pass over 8-column pieces
-      for (int idx = tid; idx < C * (C / 8); idx += kTcThreads) {
-        const int r = idx % C, s8 = (idx / C) * 8;
+      // T diag(w) and T diag(b) into the product tiles; P, and for the backward T and
+      // T diag(w), stay in registers and go to the workspace while the products run.
+      // Thread tid takes row r = tid / 8, columns [s8, s8 + 8) with s8 = 8 (tid % 8), so
+      // eight threads fill a row of each tile (one 128-byte line of the workspace copy).
+      static_assert(C * C / 8 == kTcThreads, "one 8-column piece of the C x C tiles a thread");
+      uint4 rp, rt, rw;
+      uint32_t toff;
+      {
+        const int r = tid >> 3, s8 = (tid & 7) * 8;
         const float4 ta = *(const float4*)(T + r * TS + s8);
         const float4 tb = *(const float4*)(T + r * TS + s8 + 4);
-        const float4 qa = *(const float4*)(QK + r * C + s8);
-        const float4 qb = *(const float4*)(QK + r * C + s8 + 4);
+        const float4 qa = *(const float4*)(QK + r * TS + s8);
+        const float4 qb = *(const float4*)(QK + r * TS + s8 + 4);
         const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
         const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const float gr = G[r];
         __align__(16) __nv_bfloat162 pw[4], pb[4], pp[4], pt[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int s = s8 + 2 * u;
           pw[u] = __floats2bfloat162_rn(tv[2 * u] * w[s], tv[2 * u + 1] * w[s + 1]);
           pb[u] = __floats2bfloat162_rn(tv[2 * u] * bb[s], tv[2 * u + 1] * bb[s + 1]);
-          pp[u] = __floats2bfloat162_rn(s <= r ? __expf(G[r] - G[s]) * qv[2 * u] : 0.f,
-                                        s + 1 <= r ? __expf(G[r] - G[s + 1]) * qv[2 * u + 1] : 0.f);
+          pp[u] = __floats2bfloat162_rn(s <= r ? __expf(gr - G[s]) * qv[2 * u] : 0.f,
+                                        s + 1 <= r ? __expf(gr - G[s + 1]) * qv[2 * u + 1] : 0.f);
           pt[u] = __floats2bfloat162_rn(tv[2 * u], tv[2 * u + 1]);
         }
-        const uint32_t off = tc::sw128_offset(r, s8, C);
-        *(uint4*)(tTW + off) = *(const uint4*)pw;
-        *(uint4*)(tTB + off) = *(const uint4*)pb;
-        *(uint4*)(tP + off) = *(const uint4*)pp;
-        if (bwd) *(uint4*)(tT + off) = *(const uint4*)pt;
+        toff = tc::sw128_offset(r, s8, C);
+        *(uint4*)(tTW + toff) = *(const uint4*)pw;
+        *(uint4*)(tTB + toff) = *(const uint4*)pb;
+        rp = *(const uint4*)pp;
+        rt = *(const uint4*)pt;
+        rw = *(const uint4*)pw;
+      }
+      // diag(c) K with c_s = e^{G_last - G_s} (zero past the chunk): the walk's state
+      // update S <- e^{G_last} S + (diag(c) K)^T Delta takes it as its operand.  Kept in
+      // registers for the store: NK / 8 threads per row.
+      constexpr int kKcMax = C * 16 / kTcThreads;   // pieces per thread at NK = 128
+      const int nkc = C * (NK / 8) / kTcThreads;
+      uint4 rk[kKcMax];
+      uint32_t koff[kKcMax];
+#pragma unroll
+      for (int i = 0; i < kKcMax; ++i) {
+        rk[i] = make_uint4(0, 0, 0, 0);
+        koff[i] = 0;
+        if (i < nkc) {
+          const int idx = tid + i * kTcThreads;
+          const int s = idx / (NK / 8), k8 = (idx % (NK / 8)) * 8;
+          const uint4 raw = *(const uint4*)(tAQK + tc::sw128_offset(s, k8, 128));
+          const __nv_bfloat162* e = (const __nv_bfloat162*)&raw;
+          const float cs = s < len ? __expf(G[len - 1] - G[s]) : 0.f;
+          __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(e[q]);
+            pk[q] = __floats2bfloat162_rn(f.x * cs, f.y * cs);
+          }
+          rk[i] = *(const uint4*)pk;
+          koff[i] = tc::sw128_offset(s, k8, C);
+        }
       }
       {
-        const bool lok = tc::mbar_wait(&bar[1], lphase);
-        lphase ^= 1u;
+        const uint32_t bit = odd ? 2u : 1u;
+        const bool lok = tc::mbar_wait(odd ? &bar[3] : &bar[2], (vphase & bit) ? 1u : 0u);
+        vphase ^= bit;
         if (__syncthreads_or(lok ? 0 : 1)) {
           if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
           ok = false;
@@ -486,56 +570,58 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, int bwd, int c, 
       if (len < C)
         for (int idx = tid; idx < nbv * (C - len) * 8; idx += kTcThreads) {
           const int b2 = idx / ((C - len) * 8), rem = idx % ((C - len) * 8);
-          ((uint4*)(sV + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
+          ((uint4*)(vb + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
         }
-      // diag(c) K with c_s = e^{G_last - G_s} (zero past the chunk): the walk's state
-      // update S <- e^{G_last} S + (diag(c) K)^T Delta takes it as its operand
-      for (int idx = tid; idx < C * (NK / 8); idx += kTcThreads) {
-        const int s = idx % C, k8 = (idx / C) * 8;
-        const uint4 raw = *(const uint4*)(tAQK + tc::sw128_offset(s, k8, 128));
-        const __nv_bfloat162* e = (const __nv_bfloat162*)&raw;
-        const float cs = s < len ? __expf(G[len - 1] - G[s]) : 0.f;
-        __align__(16) __nv_bfloat162 pk[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(e[q]);
-          pk[q] = __floats2bfloat162_rn(f.x * cs, f.y * cs);
-        }
-        *(uint4*)(tKc + tc::sw128_offset(s, k8, C)) = *(const uint4*)pk;
-      }
       tc::fence_async_smem();
-      ok = mma_run([&] {
+      mma_issue([&] {
         // W = (T diag(w)) K: B is K read MN-major from the rows of the [K; Q] tile
         tc::mma_tile_x(tAccW, tc::smem_u32(tTW), false, 8192u, 64, tc::smem_u32(tAQK), true,
                        aqk_pitch, NK, C, 0u);
         // U^T = V^T (T diag(b))^T: A is V^T read MN-major from the natural V tile
-        tc::mma_tile_x(tAccU, tc::smem_u32(sV), true, 8192u, MV, tc::smem_u32(tTB), false,
+        tc::mma_tile_x(tAccU, tc::smem_u32(vb), true, 8192u, MV, tc::smem_u32(tTB), false,
                        8192u, C, C, 0u);
-      }, &bar[0], phase, p.status, c);
+      }, &bar[0]);
+      // the tiles that only the workspace takes leave while the products run (after the
+      // proxy fence above, which therefore never waits for them)
+      *(uint4*)(p.Psw + ch * 8192 + toff) = rp;
+      if (bwd) {
+        *(uint4*)(p.Tb + ch * 16384 + toff) = rt;
+        *(uint4*)(p.Tb + ch * 16384 + 8192 + toff) = rw;
+      }
+#pragma unroll
+      for (int i = 0; i < kKcMax; ++i)
+        if (i < nkc) *(uint4*)(p.Kcw + ch * bKC + koff[i]) = rk[i];
+      ok = mma_wait(&bar[0], phase, p.status, c);
       if (!ok) goto done;
-      // the unit's last product has read the [K; Q] tile: the next unit's rows may land
-      if (tid == 0 && link != nullptr && link->next >= 0 && g0 + nh == p.r && hh + 1 == nh)
-        link->kq_issued =
-            issue_kq(p, maps, link->next / p.Hk, link->next % p.Hk, tAQK, &bar[1]);
+      if (tid == 0) {
+        // this head's V buffer is free again: the next head that uses it may land
+        const int jn = two_v ? j + 2 : j + 1;
+        if (!odd && jn < p.r) issue_v(p, maps, t0, kh, jn, sV, &bar[2]);
+        // the unit's last product has read the [K; Q] tile and the V tiles: the next
+        // unit's rows and first V tile may land
+        if (link != nullptr && j + 1 == p.r && link->next >= 0 && link->next < p.NC * p.Hk) {
+          const int cn = link->next / p.Hk, khn = link->next % p.Hk;
+          int nn, nlen;
+          int64_t nt0;
+          if (chunk_info(p, tab, cn, &nn, &nt0, &nlen)) {
+            issue_kq(p, maps, nt0, khn, tAQK, &bar[1]);
+            issue_v(p, maps, nt0, khn, 0, sV, &bar[2]);
+            link->kq_issued = true;
+          }
+        }
+      }
       acc_walk64(tAccW, Dk, C, [&](int s, int col0, const float* v) {
-        tile_put16(tW, C, s, col0, v);
+        tile_put16(p.Wsw + ch * bKC, C, s, col0, v);
       });
+      if (Dk < 64)   // the W tile's padding columns
+        for (int idx = tid; idx < C * (8 - Dk / 8); idx += kTcThreads) {
+          const int s = idx / (8 - Dk / 8), c0 = (Dk / 8 + idx % (8 - Dk / 8)) * 8;
+          *(uint4*)(p.Wsw + ch * bKC + tc::sw128_offset(s, c0, C)) = make_uint4(0, 0, 0, 0);
+        }
       acc_walk(tAccU, MV, 64, Dv, [&](int vv, int col0, const float* v) {
         // U^T as a [Dv][C] SW128 tile, so that row reads by the state walks are conflict-free
         tile_put16((uint8_t*)(p.Utb + ch * Dv * C), Dv, vv, col0, v);
       });
-      tc::fence_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        tc::bulk_s2g(p.Wsw + ch * bKC, tW, bKC);
-        tc::bulk_s2g(p.Kcw + ch * bKC, tKc, bKC);
-        tc::bulk_s2g(p.Psw + ch * 8192, tP, 8192);
-        if (bwd) {
-          tc::bulk_s2g(p.Tb + ch * 16384, tT, 8192);
-          tc::bulk_s2g(p.Tb + ch * 16384 + 8192, tTW, 8192);
-        }
-        tc::bulk_commit();
-      }
     }
   }
 done:
@@ -553,10 +639,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
-  cta_setup(ctl, 2, 256);
-  uint32_t phase = 0, lphase = 0;
-  prep_unit(p, maps, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar, phase,
-            lphase, nullptr);
+  cta_setup(ctl, 4, 256);
+  uint32_t phase = 0, lphase = 0, vphase = 0;
+  const SeqTab tab = seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)));
+  prep_unit(p, maps, tab, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar,
+            phase, lphase, vphase, nullptr);
   cta_teardown(ctl, 256);
 }
 
@@ -956,9 +1043,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
     fwd_state_unit<DK>(p, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes, ctl->tmem,
                        ctl->bar);
   } else {
-    uint32_t phase = 0, lphase = 0;
+    uint32_t phase = 0, lphase = 0, vphase = 0;
     const int units = p.NC * p.Hk;
-    // the next unit is taken while the current one runs (thread 0's view)
+    const SeqTab tab =
+        seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)));
+    // the next unit is taken while the current one runs (thread 0's view); its value is
+    // first read at the unit's last head, so the atomic's round trip stalls nobody
     PrepLink link{-1, -1, false};
     int next = threadIdx.x == 0 ? (int)atomicAdd(p.fwork, 1u) : 0;
     for (;;) {
@@ -969,10 +1059,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
       if (u >= units) break;
       if (threadIdx.x == 0) {
         next = (int)atomicAdd(p.fwork, 1u);
-        link.next = next < units ? next : -1;
+        link.next = next;
       }
-      const bool ok = prep_unit(p, maps, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
-                                ctl->bar, phase, lphase, &link);
+      const bool ok = prep_unit(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes,
+                                ctl->tmem, ctl->bar, phase, lphase, vphase, &link);
       if (threadIdx.x == 0) {
         if (link.pending >= 0) {   // a unit that stopped before its stores
           tc::bulk_wait<0>();
@@ -990,7 +1080,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
     }
     if (threadIdx.x == 0) {
       // the last unit's stores, and k / q rows issued for a unit that will not run
-      if (link.kq_issued) tc::mbar_wait(&ctl->bar[1], lphase);
+      if (link.kq_issued) {
+        tc::mbar_wait(&ctl->bar[1], lphase);
+        tc::mbar_wait(&ctl->bar[2], vphase & 1u);
+      }
       tc::bulk_wait<0>();
       if (link.pending >= 0) publish_flag(p.fready + link.pending);
     }
@@ -1000,11 +1093,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
 
 // ---------------------------------------------------------------------------
 static size_t prep_tc_smem(const Params& p) {
-  const int Dk = p.Dk, Dv = p.Dv;
-  size_t b = (size_t)((Dk + 63) / 64) * 128 * 128 + (size_t)((Dv + 63) / 64) * 8192 + 4 * 8192 +
-             2 * tc::sw128_bytes(64, Dk);
-  b += sizeof(float) * ((size_t)2 * C * C + (size_t)RB * C * TS + RB * 1024 + 3 * RB * C);
-  return b + kCtlBytes + 1024;
+  return prep_buffers_bytes(p.Dk, p.Dv) + 2 * kSeqCache * sizeof(int32_t) + kCtlBytes + 1024;
 }
 
 static size_t out_tc_smem(const Params& p) {

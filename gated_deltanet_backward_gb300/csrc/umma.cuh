@@ -278,6 +278,11 @@ __host__ __device__ __forceinline__ uint32_t sw128_bytes(int rows, int cols) {
 // row) of the 2-D tensor map into shared memory; completion is signalled on
 // `bar` through its transaction count.  The map lives in kernel-parameter
 // space (__grid_constant__).
+// Brings a tensor map (the generic address of a __grid_constant__ kernel parameter) into
+// the descriptor cache ahead of the copies that use it.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tmap) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int x, int y,
                                             uint64_t* bar) {
   asm volatile(
