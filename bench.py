@@ -387,7 +387,10 @@ def run_ours(args):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device, dt)
 
     qkv = dev(inp.qkv, tdt)
-    q, k, v = qkv[:, :Hk * Dk], qkv[:, Hk * Dk:2 * Hk * Dk], qkv[:, 2 * Hk * Dk:]
+    if qkv is not None:   # packed projection rows: q, k, v are strided views
+        q, k, v = qkv[:, :Hk * Dk], qkv[:, Hk * Dk:2 * Hk * Dk], qkv[:, 2 * Hk * Dk:]
+    else:
+        q, k, v = dev(inp.q, tdt), dev(inp.k, tdt), dev(inp.v, tdt)
     alpha, beta_raw = dev(inp.alpha), dev(inp.beta_raw)
     a_log, dt_bias = dev(inp.a_log), dev(inp.dt_bias)
     S0, dS_T, dO = dev(inp.S0), dev(inp.dS_T), dev(inp.dO, tdt)
@@ -819,7 +822,9 @@ def run_e2e(args, inp, layer, device, tdt, world):
     def pin(a, dt=torch.float32):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dt).pin_memory()
 
-    h_in = dict(qkv=pin(inp.qkv, tdt), alpha=pin(inp.alpha), beta_raw=pin(inp.beta_raw),
+    packed = inp.qkv is not None
+    qkv_rows = inp.qkv if packed else np.concatenate([inp.q, inp.k, inp.v], axis=1)
+    h_in = dict(qkv=pin(qkv_rows, tdt), alpha=pin(inp.alpha), beta_raw=pin(inp.beta_raw),
                 a_log=pin(inp.a_log), dt_bias=pin(inp.dt_bias), dO=pin(inp.dO, tdt),
                 S0=pin(inp.S0), dS_T=pin(inp.dS_T))
     outs = dict(o=(T, Hv * Dv, tdt), dq=(T, Hk * Dk, tdt), dk=(T, Hk * Dk, tdt),

@@ -48,6 +48,31 @@ __device__ __forceinline__ void cta_teardown(CtaCtl* ctl, uint32_t ncols) {
   if ((threadIdx.x >> 5) == 0) tc::tmem_dealloc(ctl->tmem, ncols);
 }
 
+// A batch's cu_seqlens and chunk offsets copied into shared memory for a CTA's chunk
+// lookups (each a global round trip otherwise, on the path of the thread that issues
+// the copies), when the batch has fewer than `cap` sequences.
+struct SeqTab {
+  const int32_t* cu;
+  const int32_t* coff;
+};
+// All threads, then a CTA barrier: fills the cache at `sm` (2 cap int32) if the batch
+// fits, and returns the table to read.
+__device__ __forceinline__ SeqTab seq_tab(const Params& p, int32_t* sm, int cap) {
+  const int m = p.n_seqs + 1;
+  const bool fits = m <= cap;
+  if (fits)
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+      sm[i] = p.cu[i];
+      sm[cap + i] = p.coff[i];
+    }
+  __syncthreads();
+  return fits ? SeqTab{sm, sm + cap} : SeqTab{p.cu, p.coff};
+}
+__device__ __forceinline__ bool chunk_info(const Params& p, const SeqTab& tab, int c, int* n,
+                                           int64_t* t0, int* len) {
+  return chunk_info_at(tab.cu, tab.coff, p.n_seqs, p.NC, p.T, c, n, t0, len);
+}
+
 // Readiness flags between the CTAs of one cooperative launch (all co-resident).
 // The producer publishes after every write of the unit has completed (its bulk
 // stores waited for, a CTA barrier, then this call on one thread); the consumer

@@ -23,6 +23,7 @@ namespace gdn {
 namespace {
 
 constexpr int C = kChunk;
+constexpr int kSeqCache = 1024;   // sequences + 1 whose tables the preparation caches
 constexpr int RB = 3;  // value heads prepared together (triangular solves in parallel)
 
 __device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64) * 64 * 128; }
@@ -204,32 +205,6 @@ __host__ __device__ __forceinline__ size_t prep_buffers_bytes(int Dk, int Dv) {
                    2 * 8192;
   return b + sizeof(float) * ((size_t)C * C + (size_t)C * TS + (size_t)RB * C * TS + RB * 1024 +
                               3 * RB * C);
-}
-
-// The batch's cu_seqlens and chunk offsets copied into shared memory for the
-// preparation's chunk lookups (each a global round trip otherwise, on the path of the
-// thread that issues the copies), for batches of fewer than kSeqCache sequences.
-constexpr int kSeqCache = 1024;
-struct SeqTab {
-  const int32_t* cu;
-  const int32_t* coff;
-};
-// All threads, then a CTA barrier: fills the cache at `sm` (2 kSeqCache int32) if the
-// batch fits, and returns the table to read.
-__device__ SeqTab seq_tab(const Params& p, int32_t* sm) {
-  const int m = p.n_seqs + 1;
-  const bool fits = m <= kSeqCache;
-  if (fits)
-    for (int i = threadIdx.x; i < m; i += blockDim.x) {
-      sm[i] = p.cu[i];
-      sm[kSeqCache + i] = p.coff[i];
-    }
-  __syncthreads();
-  return fits ? SeqTab{sm, sm + kSeqCache} : SeqTab{p.cu, p.coff};
-}
-__device__ __forceinline__ bool chunk_info(const Params& p, const SeqTab& tab, int c, int* n,
-                                           int64_t* t0, int* len) {
-  return chunk_info_at(tab.cu, tab.coff, p.n_seqs, p.NC, p.T, c, n, t0, len);
 }
 
 // Thread 0: the raw k and q rows of key head kh of the chunk starting at token t0 as TMA
@@ -641,7 +616,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
   CtaCtl* ctl = (CtaCtl*)base;
   cta_setup(ctl, 4, 256);
   uint32_t phase = 0, lphase = 0, vphase = 0;
-  const SeqTab tab = seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)));
+  const SeqTab tab =
+      seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)), kSeqCache);
   prep_unit(p, maps, tab, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar,
             phase, lphase, vphase, nullptr);
   cta_teardown(ctl, 256);
@@ -1046,7 +1022,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
     uint32_t phase = 0, lphase = 0, vphase = 0;
     const int units = p.NC * p.Hk;
     const SeqTab tab =
-        seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)));
+        seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)), kSeqCache);
     // the next unit is taken while the current one runs (thread 0's view); its value is
     // first read at the unit's last head, so the atomic's round trip stalls nobody
     PrepLink link{-1, -1, false};
