@@ -461,7 +461,7 @@ cudaError_t launch_backward(const Params& p, const TmaMaps* maps, cudaStream_t s
     return launch_bwd_tc(p, *maps, st);
   }
   if (!p.reuse) {
-    cudaError_t e = launch_prep(p, bf16, true, st);
+    cudaError_t e = launch_prep(p, true, st);
     if (e != cudaSuccess) return e;
   }
   return launch_backward_t<float>(p, st);

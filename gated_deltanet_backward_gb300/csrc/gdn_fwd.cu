@@ -206,18 +206,14 @@ static size_t prep_smem(const Params& p) {
   return sizeof(float) * ((size_t)kChunk * p.Dk + 3 * kChunk * kChunk + 3 * kChunk);
 }
 
-cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t st) {
+// fp32 inputs only: bf16 inputs take the tensor-core preparation (launch_prep_tc)
+cudaError_t launch_prep(const Params& p, bool write_T, cudaStream_t st) {
   if (p.NC == 0) return cudaSuccess;
   const size_t smem = prep_smem(p);
   dim3 grid(p.NC, p.Hk);
   profile_pre(st, KID_PREP);
-  if (bf16) {
-    cudaFuncSetAttribute(k_prep<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_prep<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, write_T ? 1 : 0);
-  } else {
-    cudaFuncSetAttribute(k_prep<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_prep<float><<<grid, kThreads, smem, st>>>(p, write_T ? 1 : 0);
-  }
+  cudaFuncSetAttribute(k_prep<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  k_prep<float><<<grid, kThreads, smem, st>>>(p, write_T ? 1 : 0);
   profile_post(st);
   return cudaGetLastError();
 }
@@ -237,20 +233,15 @@ cudaError_t launch_forward(const Params& p, const TmaMaps* maps, cudaStream_t st
     // the output from the walks' state and Delta tiles
     return launch_fwd_out_tc(p, st);
   }
-  cudaError_t e = launch_prep(p, bf16, p.keep != 0, st);
+  cudaError_t e = launch_prep(p, p.keep != 0, st);
   if (e != cudaSuccess || p.n_seqs == 0) return e;
   const int DVS = p.Dv < 32 ? p.Dv : 32;
   const size_t smem = sizeof(float) * ((size_t)p.Dk * DVS + (size_t)kChunk * DVS +
                                        kChunk * kChunk + 3 * kChunk);
   dim3 grid(p.n_seqs, p.Hv, p.Dv / DVS);
   profile_pre(st, KID_FWD_STATE);
-  if (bf16) {
-    cudaFuncSetAttribute(k_fwd_state<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_fwd_state<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, DVS);
-  } else {
-    cudaFuncSetAttribute(k_fwd_state<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_fwd_state<float><<<grid, kThreads, smem, st>>>(p, DVS);
-  }
+  cudaFuncSetAttribute(k_fwd_state<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  k_fwd_state<float><<<grid, kThreads, smem, st>>>(p, DVS);
   profile_post(st);
   return cudaGetLastError();
 }

@@ -334,7 +334,7 @@ cudaError_t launch_decode(const gdn_shape* s, const void* q, int64_t q_ld, const
                           float* S_out, void* o, int64_t o_ld, cudaStream_t st);
 
 // Launchers (return a cudaError_t from the launch).
-cudaError_t launch_prep(const Params& p, bool bf16, bool write_T, cudaStream_t st);
+cudaError_t launch_prep(const Params& p, bool write_T, cudaStream_t st);
 cudaError_t launch_forward(const Params& p, const TmaMaps* maps, cudaStream_t st);
 cudaError_t launch_backward(const Params& p, const TmaMaps* maps, cudaStream_t st);
 
