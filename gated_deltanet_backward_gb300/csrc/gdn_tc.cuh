@@ -82,6 +82,17 @@ __device__ __forceinline__ void publish_flag(uint32_t* flag) {
   __threadfence();
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
 }
+// publish_flag for several units whose writes are all done: one fence for all of them,
+// then a relaxed store per flag (the fence and a later store form the release), at
+// flags + i * stride for i < count.
+__device__ __forceinline__ void publish_flags(uint32_t* flags, size_t stride, int count) {
+  if (count <= 0) return;
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  for (int i = 0; i < count; ++i)
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flags + (size_t)i * stride), "r"(1u)
+                 : "memory");
+}
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* flag) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");

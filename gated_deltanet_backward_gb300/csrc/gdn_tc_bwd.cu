@@ -69,8 +69,10 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
   // the walk goes down, so every chunk >= published is)
   int published = c1;
   auto publish_down_to = [&](int cc) {
-    for (; published > cc; --published)
-      publish_flag(p.bready + ((size_t)(published - 1) * p.Hv + h));
+    if (published > cc) {
+      publish_flags(p.bready + ((size_t)cc * p.Hv + h), (size_t)p.Hv, published - cc);
+      published = cc;
+    }
   };
   // TMEM: dS^T update (rows v) @0; in token rows (M = 64): P^T dO @128, K dS @256
   const uint32_t tA3 = tmem, tA1 = tmem + 128, tA2 = tmem + 256;
