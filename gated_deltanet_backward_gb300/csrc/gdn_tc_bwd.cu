@@ -781,7 +781,12 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       tc::mma_tile_x(tmp + 128, T_, true, sCC, 64, tc::smem_u32(tdT), true, sCC, C, C, 0u); // Y = T^T dT
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
-    // epilogue C: dv = b dBv, db += rowsum(dBv * V), Y tile
+    // epilogue C: dv = b dBv, db += rowsum(dBv * V), Y tile.  A thread holds at most
+    // one 16-column piece of dv (Dv <= 32 kGroups), kept in registers and stored once
+    // the next products are issued (plain global stores just before the proxy fence
+    // would stall it until they drain)
+    uint4 dv_lo = make_uint4(0, 0, 0, 0), dv_hi = dv_lo;
+    uint4* dv_dst = nullptr;
     {
       __nv_bfloat16* dvc = (__nv_bfloat16*)p.dv + t0 * p.dv_ld + (int64_t)h * Dv;
       float rs = 0.f;
@@ -796,9 +801,9 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           pk[j] = __floats2bfloat162_rn(bv[s] * x[2 * j], bv[s] * x[2 * j + 1]);
-        uint4* dst = (uint4*)(dvc + (int64_t)s * p.dv_ld + col0);
-        dst[0] = ((const uint4*)pk)[0];
-        dst[1] = ((const uint4*)pk)[1];
+        dv_dst = (uint4*)(dvc + (int64_t)s * p.dv_ld + col0);
+        dv_lo = ((const uint4*)pk)[0];
+        dv_hi = ((const uint4*)pk)[1];
       });
       rs = x2_pair_sum(rs);
       if (x2_half() == 0) part[grp * C + x2_row()] = rs;
@@ -809,13 +814,18 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     __syncthreads();
     if (tid < C) db[tid] += rsum_g(part, tid);
     tc::fence_async_smem();
-    ok = mma_run([&] {
+    mma_issue([&] {
       tc::mma_tile_x(tmp, tc::smem_u32(tT), true, sCC, 64, tc::smem_u32(tdW), true, 8192u, NK, C,
                      0u);                                                         // dBk = T^T dW
       tc::mma_tile_x(tdK, tc::smem_u32(tTW), true, sCC, 64, tc::smem_u32(tdW), true, 8192u, NK,
                      C, 1u);                                                      // dK += b e^G dBk
       tc::mma_tile(tmp + 128, tc::smem_u32(tY), 64, tc::smem_u32(tT), C, C, 0u);  // Y T^T
-    }, &bars[0], mphase, p.status, c);
+    }, &bars[0]);
+    if (dv_dst != nullptr) {   // this head's dv piece, while the products run
+      dv_dst[0] = dv_lo;
+      dv_dst[1] = dv_hi;
+    }
+    ok = mma_wait(&bars[0], mphase, p.status, c);
     if (!ok) break;
     // epilogue D: t_s = rowsum(dBk * K); dA = -(Y T^T) strictly lower.  With
     // A[r][s] = b_r E_rs KK_rs (s < r) and q = dA E KK: db_r += sum_s q[r][s],

@@ -346,9 +346,6 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& ta
           pk[q] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
         }
         *(uint4*)(tAQK + tc::sw128_offset(row, (part * cpt + j) * 8, 128)) = *(const uint4*)pk;
-        // the natural K or Q tile of the key head in the workspace, row by row
-        *(uint4*)((isq ? p.Qsw : p.Ksw) + ckk * bKC +
-                  tc::sw128_offset(t, (part * cpt + j) * 8, 64)) = *(const uint4*)pk;
       }
     if (bwd && part == 0) (isq ? p.nq : p.nk)[ck + t] = nrm;
     // Dk < 64: the box's columns past Dk (a neighbouring head) become zero padding
@@ -365,9 +362,25 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& ta
   tc::fence_async_smem();
   __syncthreads();
   // 2. [K; Q] K^T -> TMEM columns [0, 64): lanes 0-63 K K^T, lanes 64-127 Q K^T.
-  ok = mma_run([&] { tc::mma_tile_p(tmem, tc::smem_u32(tAQK), aqk_pitch, 128, tc::smem_u32(tAQK),
-                                     aqk_pitch, 64, Dk, 0u); },
-               &bar[0], phase, p.status, c);
+  mma_issue([&] { tc::mma_tile_p(tmem, tc::smem_u32(tAQK), aqk_pitch, 128, tc::smem_u32(tAQK),
+                                 aqk_pitch, 64, Dk, 0u); },
+            &bar[0]);
+  {
+    // the natural K and Q tiles of the key head into the workspace while the product
+    // runs (plain stores issued before the proxy fence above would have stalled it):
+    // each thread copies the pieces it normalised
+    const int row = tid >> 2, part = tid & 3;
+    const int nch = Dk / 8, tpr = nch < 4 ? nch : 4, cpt = part < tpr ? nch / tpr : 0;
+    uint8_t* dst = (row >= C ? p.Qsw : p.Ksw) + ckk * bKC;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < cpt) {
+        const int k8 = (part * cpt + j) * 8;
+        *(uint4*)(dst + tc::sw128_offset(row & (C - 1), k8, 64)) =
+            *(const uint4*)(tAQK + tc::sw128_offset(row, k8, 128));
+      }
+  }
+  ok = mma_wait(&bar[0], phase, p.status, c);
   if (!ok) goto done;
   acc_walk(tmem, 128, 64, 128, [&](int row, int col0, const float* v) {
     float* dst = row < C ? KK + row * C : QK + (row - C) * TS;
