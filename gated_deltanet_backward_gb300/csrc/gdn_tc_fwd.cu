@@ -878,14 +878,16 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
 }
 
 // ---------------------------------------------------------------------------
-// The output of one (chunk c, value head h) on a whole CTA (`sm`: 1024-aligned,
-// out_tc_smem bytes; `tmem`: 256 columns; bars[0..1]: the tiles and the products):
+// The output of chunk c for the value heads of key head kh on a whole CTA (`sm`:
+// 1024-aligned, out_tc_smem bytes; `tmem`: 256 columns; bars[0..1]: the tiles and the
+// products), value head by value head:
 //   O = scale (diag(e^G) Q S + P Delta)
-// in token rows, from the normalised Q tile of the key head, the chunk-start state's
-// S^T tile and the Delta^T tile the walk left, and P.  Small enough (about 73 KB of
-// shared memory, 256 TMEM columns, 64 registers) for two CTAs per SM, so that one
-// CTA's loads and products run under the other's epilogue.
-__device__ void out_unit(const Params& p, int c, int h, uint8_t* sm, uint32_t tmem,
+// in token rows, from the normalised Q tile of the key head (loaded once), the
+// chunk-start state's S^T tile and the Delta^T tile the walk left, and P.  A head's tiles
+// land while the previous head's epilogue runs.  Small enough (about 73 KB of shared
+// memory, 256 TMEM columns, 48 registers) for two CTAs per SM, so that one CTA's loads
+// and products also run under the other's epilogue.
+__device__ void out_unit(const Params& p, int c, int kh, uint8_t* sm, uint32_t tmem,
                          uint64_t* bars) {
   int n;
   int64_t t0;
@@ -906,87 +908,97 @@ __device__ void out_unit(const Params& p, int c, int h, uint8_t* sm, uint32_t tm
   float* ev = sG + C;                // [C] scale e^G
   const uint32_t tO1 = tmem, tO2 = tmem + 128;   // Q S and P Delta (M = 64)
   const uint8_t* tiles = p.saved && p.bf16_states ? (const uint8_t*)p.saved : p.Stb;
-  const size_t ch = (size_t)c * p.Hv + h;
-  if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&bars[0], bQ + bSt + bDt + bP + bG);
-    tc::bulk_g2s(tQ, p.Qsw + ((size_t)c * p.Hk + key_head(p, h)) * bQ, bQ, &bars[0]);
+  // thread 0: value head j's S^T, Delta^T, P and G tiles on one phase of bars[0]
+  auto issue_head = [&](int j, uint32_t extra) {
+    const size_t ch = (size_t)c * p.Hv + value_head(p, kh, j);
+    tc::mbar_arrive_expect_tx(&bars[0], extra + bSt + bDt + bP + bG);
     tc::bulk_g2s(tS, tiles + ch * bSt, bSt, &bars[0]);
     tc::bulk_g2s(tD, p.Dtb + ch * bDt, bDt, &bars[0]);
     tc::bulk_g2s(tP, p.Psw + ch * bP, bP, &bars[0]);
     tc::bulk_g2s(sG, p.G + ch * C, bG, &bars[0]);
+  };
+  if (tid == 0) {
+    issue_head(0, bQ);
+    tc::bulk_g2s(tQ, p.Qsw + ((size_t)c * p.Hk + kh) * bQ, bQ, &bars[0]);
   }
   uint32_t ph = 0, mph = 0;
-  const bool lok = tc::mbar_wait(&bars[0], ph);
-  if (__syncthreads_or(lok ? 0 : 1)) {
-    if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
-    return;
-  }
-  if (tid < C) ev[tid] = p.scale * expf(sG[tid]);
-  // O1 = Q S (B = the S^T tile), O2 = P Delta (B = the Delta^T tile)
-  const bool ok = mma_run([&] {
-    tc::mma_tile_p(tO1, tc::smem_u32(tQ), 8192u, 64, tc::smem_u32(tS), (uint32_t)MV * 128u, Dv,
-                   Dk, 0u);
-    tc::mma_tile(tO2, tc::smem_u32(tP), 64, tc::smem_u32(tD), Dv, C, 0u);
-  }, &bars[1], mph, p.status, c);
-  if (!ok) return;
-  // token row r of the chunk per accumulator lane, 16 consecutive values per thread (Dv
-  // <= 128: one piece per thread; a row's pieces sit in the 8 threads of its lane pair in
-  // the kGroups warps of its lane quarter)
-  const int r = x2_row();
-  const int col = grp * 16 + x2_half() * 16 * kGroups;
-  const bool mine = r < len && col < Dv;
-  __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + r) * p.o_ld + (int64_t)h * Dv;
-  float o1[16], o2[16];
-  tc::tmem_ld16_x2<16 * kGroups>(tO1 + lane_quarter() + grp * 16, o1);
-  tc::tmem_ld16_x2<16 * kGroups>(tO2 + lane_quarter() + grp * 16, o2);
-  tc::tmem_ld_wait();
-  __align__(16) __nv_bfloat162 pk[8];
-  {
-    const float e = ev[r];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      pk[j] = __floats2bfloat162_rn(fmaf(e, o1[2 * j], p.scale * o2[2 * j]),
-                                    fmaf(e, o1[2 * j + 1], p.scale * o2[2 * j + 1]));
-  }
-  if (mine) {
-    uint4* dst = (uint4*)(orow + col);
-    dst[0] = ((const uint4*)pk)[0];
-    dst[1] = ((const uint4*)pk)[1];
-  }
-  if (p.ny) {
-    // gated RMSNorm of the row of o as stored (bf16): the sum of squares over the row's
-    // pieces (lane pair, then the kGroups warps in a fixed order through shared memory)
-    float* red = ev + C;   // [kGroups][C]
-    float ss = 0.f;
-    if (mine)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float2 f = __bfloat1622float2(pk[j]);
-        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-      }
-    ss = x2_pair_sum(ss);
-    if (x2_half() == 0) red[grp * C + r] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) tot += red[g * C + r];
+  for (int j = 0; j < p.r; ++j) {
+    const int h = value_head(p, kh, j);
+    const bool lok = tc::mbar_wait(&bars[0], ph);
+    ph ^= 1u;
+    if (__syncthreads_or(lok ? 0 : 1)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+      return;
+    }
+    if (tid < C) ev[tid] = p.scale * expf(sG[tid]);
+    // O1 = Q S (B = the S^T tile), O2 = P Delta (B = the Delta^T tile)
+    const bool ok = mma_run([&] {
+      tc::mma_tile_p(tO1, tc::smem_u32(tQ), 8192u, 64, tc::smem_u32(tS), (uint32_t)MV * 128u, Dv,
+                     Dk, 0u);
+      tc::mma_tile(tO2, tc::smem_u32(tP), 64, tc::smem_u32(tD), Dv, C, 0u);
+    }, &bars[1], mph, p.status, c);
+    if (!ok) return;
+    // the products have read this head's tiles: the next head's land under the epilogue
+    if (tid == 0 && j + 1 < p.r) issue_head(j + 1, 0u);
+    // token row r of the chunk per accumulator lane, 16 consecutive values per thread (Dv
+    // <= 128: one piece per thread; a row's pieces sit in the 8 threads of its lane pair in
+    // the kGroups warps of its lane quarter)
+    const int r = x2_row();
+    const int col = grp * 16 + x2_half() * 16 * kGroups;
+    const bool mine = r < len && col < Dv;
+    __nv_bfloat16* orow = (__nv_bfloat16*)p.o + (t0 + r) * p.o_ld + (int64_t)h * Dv;
+    float o1[16], o2[16];
+    tc::tmem_ld16_x2<16 * kGroups>(tO1 + lane_quarter() + grp * 16, o1);
+    tc::tmem_ld16_x2<16 * kGroups>(tO2 + lane_quarter() + grp * 16, o2);
+    tc::tmem_ld_wait();
+    __align__(16) __nv_bfloat162 pk[8];
+    {
+      const float e = ev[r];
+  #pragma unroll
+      for (int j = 0; j < 8; ++j)
+        pk[j] = __floats2bfloat162_rn(fmaf(e, o1[2 * j], p.scale * o2[2 * j]),
+                                      fmaf(e, o1[2 * j + 1], p.scale * o2[2 * j + 1]));
+    }
     if (mine) {
-      const float inv = rsqrtf(fmaf(tot, 1.f / (float)Dv, p.neps));
-      const __nv_bfloat16* zrow = (const __nv_bfloat16*)p.nz + (t0 + r) * p.nz_ld + (int64_t)h * Dv;
-      const uint4 za = *(const uint4*)(zrow + col), zb = *(const uint4*)(zrow + col + 8);
-      const __nv_bfloat162* z2[2] = {(const __nv_bfloat162*)&za, (const __nv_bfloat162*)&zb};
-      __align__(16) __nv_bfloat162 yk[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float2 f = __bfloat1622float2(pk[j]);
-        const float2 z = __bfloat1622float2(z2[j >> 2][j & 3]);
-        const float g0 = p.ngamma[col + 2 * j], g1 = p.ngamma[col + 2 * j + 1];
-        yk[j] = __floats2bfloat162_rn(f.x * inv * g0 * (z.x * sigmoid_f(z.x)),
-                                      f.y * inv * g1 * (z.y * sigmoid_f(z.y)));
+      uint4* dst = (uint4*)(orow + col);
+      dst[0] = ((const uint4*)pk)[0];
+      dst[1] = ((const uint4*)pk)[1];
+    }
+    if (p.ny) {
+      // gated RMSNorm of the row of o as stored (bf16): the sum of squares over the row's
+      // pieces (lane pair, then the kGroups warps in a fixed order through shared memory)
+      float* red = ev + C;   // [kGroups][C]
+      float ss = 0.f;
+      if (mine)
+  #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 f = __bfloat1622float2(pk[j]);
+          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+        }
+      ss = x2_pair_sum(ss);
+      if (x2_half() == 0) red[grp * C + r] = ss;
+      __syncthreads();
+      float tot = 0.f;
+  #pragma unroll
+      for (int g = 0; g < kGroups; ++g) tot += red[g * C + r];
+      if (mine) {
+        const float inv = rsqrtf(fmaf(tot, 1.f / (float)Dv, p.neps));
+        const __nv_bfloat16* zrow = (const __nv_bfloat16*)p.nz + (t0 + r) * p.nz_ld + (int64_t)h * Dv;
+        const uint4 za = *(const uint4*)(zrow + col), zb = *(const uint4*)(zrow + col + 8);
+        const __nv_bfloat162* z2[2] = {(const __nv_bfloat162*)&za, (const __nv_bfloat162*)&zb};
+        __align__(16) __nv_bfloat162 yk[8];
+  #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 f = __bfloat1622float2(pk[j]);
+          const float2 z = __bfloat1622float2(z2[j >> 2][j & 3]);
+          const float g0 = p.ngamma[col + 2 * j], g1 = p.ngamma[col + 2 * j + 1];
+          yk[j] = __floats2bfloat162_rn(f.x * inv * g0 * (z.x * sigmoid_f(z.x)),
+                                        f.y * inv * g1 * (z.y * sigmoid_f(z.y)));
+        }
+        uint4* ydst = (uint4*)((__nv_bfloat16*)p.ny + (t0 + r) * p.ny_ld + (int64_t)h * Dv + col);
+        ydst[0] = ((const uint4*)yk)[0];
+        ydst[1] = ((const uint4*)yk)[1];
       }
-      uint4* ydst = (uint4*)((__nv_bfloat16*)p.ny + (t0 + r) * p.ny_ld + (int64_t)h * Dv + col);
-      ydst[0] = ((const uint4*)yk)[0];
-      ydst[1] = ((const uint4*)yk)[1];
     }
   }
 }
@@ -996,9 +1008,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_fwd_out_tc(Params p) {
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
   cta_setup(ctl, 2, 256);
-  // value heads of one chunk are consecutive CTAs: they share the key head's Q tile
-  // through the L2 while it is there
-  out_unit(p, (int)(blockIdx.x / p.Hv), (int)(blockIdx.x % p.Hv), base + kCtlBytes, ctl->tmem,
+  // one CTA per (chunk, key head): the Q tile is loaded once for the group's value heads
+  out_unit(p, (int)(blockIdx.x / p.Hk), (int)(blockIdx.x % p.Hk), base + kCtlBytes, ctl->tmem,
            ctl->bar);
   cta_teardown(ctl, 256);
 }
@@ -1096,7 +1107,7 @@ cudaError_t launch_fwd_out_tc(const Params& p, cudaStream_t st) {
   const size_t smem = out_tc_smem(p);
   cudaFuncSetAttribute(k_fwd_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_FWD_OUT_TC);
-  k_fwd_out_tc<<<(unsigned)p.NC * p.Hv, kTcThreads, smem, st>>>(p);
+  k_fwd_out_tc<<<(unsigned)p.NC * p.Hk, kTcThreads, smem, st>>>(p);
   profile_post(st);
   return cudaGetLastError();
 }
