@@ -123,6 +123,9 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
       ok = false;
       break;
     }
+    // the next chunk's tiles into the other buffer (every read of it by the last chunk
+    // is done, its in-place writes fenced), by another thread than the products' issuer
+    if (tid == 32 && c - 1 >= c0) issue_load(c - 1, b ^ 1);
     if (tid == 0) {
       // every fourth chunk (every chunk at first, when gradient units are waiting for
       // the walk), before this chunk's first store: all but the last two store groups
@@ -176,9 +179,6 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
       // rows v: dO^T (scale e^G Q), dO^T read MN-major
       tc::mma_tile_x(tA3, tc::smem_u32(sdO(b)), true, 8192u, MV, tc::smem_u32(tQ(b)), true,
                      8192u, NKF, C, 0u);
-      // the next chunk's tiles into the other buffer (its last chunk's products are
-      // done), issued while these products finish
-      if (c - 1 >= c0) issue_load(c - 1, b ^ 1);
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
     // dDelta = scale P^T dO + diag(c) K dS, stored negated in token rows (the A
