@@ -153,6 +153,7 @@ void fill_common(Params& p, const gdn_shape* s, const void* q, int64_t q_ld, con
   // flag arrays are handed to the kernels only by the fused launchers
   p.fwork = (uint32_t*)(base + L.fsync);
   p.fready = nullptr;
+  p.oready = nullptr;
   p.bwork = (uint32_t*)(base + L.bsync);
   p.bready = nullptr;
   p.nq = (float*)(base + L.nq);

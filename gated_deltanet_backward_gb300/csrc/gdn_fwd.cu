@@ -230,7 +230,8 @@ cudaError_t launch_forward(const Params& p, const TmaMaps* maps, cudaStream_t st
       if (e == cudaSuccess) e = launch_fwd_state_tc(p, st);
       if (e != cudaSuccess) return e;
     }
-    // the output from the walks' state and Delta tiles
+    // the output from the walks' state and Delta tiles: every unit, or those the fused
+    // launch left
     return launch_fwd_out_tc(p, st);
   }
   cudaError_t e = launch_prep(p, p.keep != 0, st);

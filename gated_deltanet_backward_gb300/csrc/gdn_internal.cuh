@@ -40,7 +40,8 @@ struct DeviceStatus {
 // shared memory by the next.
 struct WsLayout {
   size_t status;  // DeviceStatus, 256 B
-  size_t fsync;   // forward fused launch: work counter + (chunk, key head) flags
+  size_t fsync;   // forward fused launch: work counters + (chunk, key head) and (chunk,
+                  // value head) flags
   size_t bsync;   // backward fused launch: work counter + (chunk, value head) flags
   size_t nq;      // [NC][Hk][C] query norms sqrt(|q|^2 + 1e-6)
   size_t nk;      // [NC][Hk][C] key norms
@@ -96,9 +97,9 @@ inline WsLayout ws_layout(const gdn_shape& s, bool bwd) {
   };
   L.status = take(256);
   // readiness flags of the fused launches, right after the status block so that one
-  // memset clears both: forward [256 B work counter | NC*Hk flags], backward
-  // [256 B work counter | NC*Hv flags]
-  L.fsync = take(256 + NC * Hk * 4);
+  // memset clears both: forward [256 B: preparation and output work counters | NC*Hk
+  // preparation flags | NC*Hv walk flags], backward [256 B work counter | NC*Hv flags]
+  L.fsync = take(256 + NC * Hk * 4 + NC * Hv * 4);
   L.bsync = take(256 + NC * Hv * 4);
   L.nq = take(NC * Hk * C * 4);
   L.nk = take(NC * Hk * C * 4);
@@ -177,8 +178,10 @@ struct Params {
   float* ddt_bias;
   float* dS0;
   DeviceStatus* status;
-  uint32_t* fwork;   // fused forward: next preparation unit
+  uint32_t* fwork;   // fused forward: next preparation unit; fwork[1]: next output unit
   uint32_t* fready;  // fused forward: [NC][Hk] preparation unit done
+  uint32_t* oready;  // fused forward: [NC][Hv] the walk's S^T and Delta^T tiles of the
+                     // chunk stored (the output units read them); null: no output units
   uint32_t* bwork;   // fused backward: next gradient unit
   uint32_t* bready;  // fused backward: [NC][Hv] state-walk chunk done
   uint32_t tag;  // shape tag (see shape_tag); written by a keeping forward, checked by a reusing backward

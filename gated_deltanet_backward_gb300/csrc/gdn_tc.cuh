@@ -93,6 +93,12 @@ __device__ __forceinline__ void publish_flags(uint32_t* flags, size_t stride, in
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flags + (size_t)i * stride), "r"(1u)
                  : "memory");
 }
+// A relaxed read of a counter or flag (no ordering: for heuristics only).
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* flag) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* flag) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");

@@ -716,6 +716,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   // Thread 0 issues chunk loads in order; a fused launch first needs the preparation
   // unit's flag (blocking only when the walk cannot go on without the chunk).
   int issued = c0 - 1, acquired = c0 - 1;   // acquired: the flag was already read set
+  int opub = c0;   // thread 0: chunks [c0, opub) are published for the output units
   auto try_issue = [&](int cc, bool block) {
     if (cc >= c1 || cc != issued + 1) return;
     if (p.fready && cc == acquired) {
@@ -797,6 +798,17 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
     // the staging buffers' last stores have read them (the barrier below orders this
     // before the next writes); the state tile's store may still be reading
     if (tid == 0 && f32_states) tc::bulk_wait_read<1>();
+    // fused launch, every eighth chunk: the groups older than the last chunk's (its
+    // Delta^T tile and fp32 halves) and this chunk's state tile have landed, so chunks
+    // up to c - 2 are complete for the output units: one fence for the run
+    if (tid == 0 && p.oready && i > 1 && (i & 7) == 0) {
+      if (f32_states)
+        tc::bulk_wait<4>();
+      else
+        tc::bulk_wait<2>();
+      publish_flags(p.oready + (size_t)opub * p.Hv + h, (size_t)p.Hv, c - 1 - opub);
+      opub = c - 1;
+    }
     ok = mma_wait(&bars[0], mphase, p.status, c);
     if (!ok) break;
     // Delta^T = U^T - X^T
@@ -874,13 +886,17 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
         for (int j = 0; j < 16; ++j)
           p.S_T[((size_t)n * p.Hv + h) * SZ + (size_t)(grp * 16 + 16 * kGroups * ii + j) * Dv +
                 vrow] = S[ii][j];
-  if (tid == 0) tc::bulk_wait<0>();
+  if (tid == 0) {
+    tc::bulk_wait<0>();
+    // the rest (also after an error: the status word then holds it)
+    if (p.oready) publish_flags(p.oready + (size_t)opub * p.Hv + h, (size_t)p.Hv, c1 - opub);
+  }
 }
 
 // ---------------------------------------------------------------------------
 // The output of chunk c for the value heads of key head kh on a whole CTA (`sm`:
-// 1024-aligned, out_tc_smem bytes; `tmem`: 256 columns; bars[0..1]: the tiles and the
-// products), value head by value head:
+// 1024-aligned, out_tc_smem bytes; `tmem`: 256 columns; lbar / mbar: the tiles' and the
+// products' mbarriers with their running phases), value head by value head:
 //   O = scale (diag(e^G) Q S + P Delta)
 // in token rows, from the normalised Q tile of the key head (loaded once), the
 // chunk-start state's S^T tile and the Delta^T tile the walk left, and P.  A head's tiles
@@ -888,7 +904,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
 // memory, 256 TMEM columns, 48 registers) for two CTAs per SM, so that one CTA's loads
 // and products also run under the other's epilogue.
 __device__ void out_unit(const Params& p, int c, int kh, uint8_t* sm, uint32_t tmem,
-                         uint64_t* bars) {
+                         uint64_t* lbar, uint32_t& ph, uint64_t* mbar, uint32_t& mph) {
   int n;
   int64_t t0;
   int len;
@@ -911,20 +927,19 @@ __device__ void out_unit(const Params& p, int c, int kh, uint8_t* sm, uint32_t t
   // thread 0: value head j's S^T, Delta^T, P and G tiles on one phase of bars[0]
   auto issue_head = [&](int j, uint32_t extra) {
     const size_t ch = (size_t)c * p.Hv + value_head(p, kh, j);
-    tc::mbar_arrive_expect_tx(&bars[0], extra + bSt + bDt + bP + bG);
-    tc::bulk_g2s(tS, tiles + ch * bSt, bSt, &bars[0]);
-    tc::bulk_g2s(tD, p.Dtb + ch * bDt, bDt, &bars[0]);
-    tc::bulk_g2s(tP, p.Psw + ch * bP, bP, &bars[0]);
-    tc::bulk_g2s(sG, p.G + ch * C, bG, &bars[0]);
+    tc::mbar_arrive_expect_tx(lbar, extra + bSt + bDt + bP + bG);
+    tc::bulk_g2s(tS, tiles + ch * bSt, bSt, lbar);
+    tc::bulk_g2s(tD, p.Dtb + ch * bDt, bDt, lbar);
+    tc::bulk_g2s(tP, p.Psw + ch * bP, bP, lbar);
+    tc::bulk_g2s(sG, p.G + ch * C, bG, lbar);
   };
   if (tid == 0) {
     issue_head(0, bQ);
-    tc::bulk_g2s(tQ, p.Qsw + ((size_t)c * p.Hk + kh) * bQ, bQ, &bars[0]);
+    tc::bulk_g2s(tQ, p.Qsw + ((size_t)c * p.Hk + kh) * bQ, bQ, lbar);
   }
-  uint32_t ph = 0, mph = 0;
   for (int j = 0; j < p.r; ++j) {
     const int h = value_head(p, kh, j);
-    const bool lok = tc::mbar_wait(&bars[0], ph);
+    const bool lok = tc::mbar_wait(lbar, ph);
     ph ^= 1u;
     if (__syncthreads_or(lok ? 0 : 1)) {
       if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
@@ -936,7 +951,7 @@ __device__ void out_unit(const Params& p, int c, int kh, uint8_t* sm, uint32_t t
       tc::mma_tile_p(tO1, tc::smem_u32(tQ), 8192u, 64, tc::smem_u32(tS), (uint32_t)MV * 128u, Dv,
                      Dk, 0u);
       tc::mma_tile(tO2, tc::smem_u32(tP), 64, tc::smem_u32(tD), Dv, C, 0u);
-    }, &bars[1], mph, p.status, c);
+    }, mbar, mph, p.status, c);
     if (!ok) return;
     // the products have read this head's tiles: the next head's land under the epilogue
     if (tid == 0 && j + 1 < p.r) issue_head(j + 1, 0u);
@@ -1003,14 +1018,28 @@ __device__ void out_unit(const Params& p, int c, int kh, uint8_t* sm, uint32_t t
   }
 }
 
+// The output pass: persistent CTAs (two per SM) take (chunk, key head) units from the
+// output counter fwork[1] in chunk order; after a fused forward only the units it left.
 __global__ void __launch_bounds__(kTcThreads, 2) k_fwd_out_tc(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
+  __shared__ int s_unit;
   cta_setup(ctl, 2, 256);
-  // one CTA per (chunk, key head): the Q tile is loaded once for the group's value heads
-  out_unit(p, (int)(blockIdx.x / p.Hk), (int)(blockIdx.x % p.Hk), base + kCtlBytes, ctl->tmem,
-           ctl->bar);
+  const int ounits = p.NC * p.Hk;
+  uint32_t lph = 0, mph = 0;
+  int next = threadIdx.x == 0 ? (int)atomicAdd(p.fwork + 1, 1u) : 0;
+  for (;;) {
+    if (threadIdx.x == 0) s_unit = next;
+    __syncthreads();
+    const int u = s_unit;
+    __syncthreads();
+    if (u >= ounits) break;
+    if (threadIdx.x == 0) next = (int)atomicAdd(p.fwork + 1, 1u);
+    // one unit per (chunk, key head): the Q tile is loaded once for the group's heads
+    out_unit(p, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem, &ctl->bar[0], lph, &ctl->bar[1],
+             mph);
+  }
   cta_teardown(ctl, 256);
 }
 
@@ -1037,11 +1066,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
   __shared__ int s_unit;
-  cta_setup(ctl, 4, 512);
+  cta_setup(ctl, 6, 512);
   const int walks = p.n_seqs * p.Hv;
+  // Output units (chunk, key head) in chunk order from the second counter (fwork[1]),
+  // each once its value heads' walks have published the chunk: the preparation CTAs take
+  // them once the preparation is handed out, until the first walk finishes (fwork[2]
+  // counts the finished walks; they finish within microseconds of each other), so that
+  // the launch ends about when its walks do.  bar[4] / bar[5] serve them; neither role
+  // used them before.  The output pass launched after this kernel takes the units left
+  // (o and y are written by exactly one of them per unit).
+  auto run_outputs = [&]() {
+    const int ounits = p.oready ? p.NC * p.Hk : 0;
+    uint32_t olph = 0, omph = 0;
+    for (;;) {
+      if (threadIdx.x == 0)
+        s_unit = ld_relaxed(p.fwork + 2) == 0u ? (int)atomicAdd(p.fwork + 1, 1u) : ounits;
+      __syncthreads();
+      const int u = s_unit;
+      __syncthreads();
+      if (u >= ounits) break;
+      const int c = u / p.Hk, kh = u % p.Hk;
+      int bad = 0;
+      for (int j = threadIdx.x; j < p.r; j += blockDim.x)
+        if (!wait_flag(p.oready + (size_t)c * p.Hv + value_head(p, kh, j))) {
+          set_status(p.status, GDN_ERR_TIMEOUT, c);
+          bad = 1;
+        }
+      if (__syncthreads_or(bad)) break;
+      if (threadIdx.x == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+      out_unit(p, c, kh, base + kCtlBytes, ctl->tmem, &ctl->bar[4], olph, &ctl->bar[5], omph);
+    }
+  };
   if ((int)blockIdx.x < walks) {
     fwd_state_unit<DK>(p, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes, ctl->tmem,
                        ctl->bar);
+    if (threadIdx.x == 0 && p.oready) atomicAdd(p.fwork + 2, 1u);
   } else {
     uint32_t phase = 0, lphase = 0, vphase = 0;
     const int units = p.NC * p.Hk;
@@ -1087,6 +1146,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
       tc::bulk_wait<0>();
       if (link.pending >= 0) publish_flag(p.fready + link.pending);
     }
+    run_outputs();
   }
   cta_teardown(ctl, 512);
 }
@@ -1107,7 +1167,9 @@ cudaError_t launch_fwd_out_tc(const Params& p, cudaStream_t st) {
   const size_t smem = out_tc_smem(p);
   cudaFuncSetAttribute(k_fwd_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_FWD_OUT_TC);
-  k_fwd_out_tc<<<(unsigned)p.NC * p.Hk, kTcThreads, smem, st>>>(p);
+  const int sms = sm_count();
+  const int units = p.NC * p.Hk, grid = sms > 0 && 2 * sms < units ? 2 * sms : units;
+  k_fwd_out_tc<<<(unsigned)grid, kTcThreads, smem, st>>>(p);
   profile_post(st);
   return cudaGetLastError();
 }
@@ -1172,7 +1234,8 @@ static cudaError_t launch_fwd_fused_t(const Params& p, const TmaMaps& maps, cuda
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_fused_tc<DK>, kTcThreads, smem);
   if (e != cudaSuccess || per_sm < 1) return cudaSuccess;
   Params pp = p;
-  pp.fready = p.fwork + 64;   // the work counter's 256-byte slot, then the flags
+  pp.fready = p.fwork + 64;             // the work counters' 256-byte slot, then the flags
+  pp.oready = pp.fready + p.NC * p.Hk;  // the walks' chunk flags: the launch forms O too
   TmaMaps mm = maps;
   void* args[] = {&pp, &mm};
   profile_pre(st, KID_FWD_FUSED_TC);
