@@ -1098,6 +1098,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
     }
   };
   if ((int)blockIdx.x < walks) {
+    // One preparation unit first: the walk cannot start before the first chunk's units
+    // are done anyway, so its CTA adds to the preparation's first wave.
+    {
+      const SeqTab tab =
+          seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)), kSeqCache);
+      if (threadIdx.x == 0) s_unit = (int)atomicAdd(p.fwork, 1u);
+      __syncthreads();
+      const int u = s_unit;
+      if (u < p.NC * p.Hk) {
+        uint32_t phase = 0, lphase = 0, vphase = 0;
+        // every load and product of the unit has completed when it returns, and every
+        // write came before its last barrier
+        prep_unit(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
+                  ctl->bar, phase, lphase, vphase, nullptr);
+        if (threadIdx.x == 0) {
+          publish_flag(p.fready + u);
+          // fresh mbarriers for the walk
+          for (int i = 0; i < 4; ++i) {
+            tc::mbar_inval(&ctl->bar[i]);
+            tc::mbar_init(&ctl->bar[i], 1);
+          }
+          tc::fence_mbar_init();
+        }
+        __syncthreads();
+      }
+    }
     fwd_state_unit<DK>(p, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes, ctl->tmem,
                        ctl->bar);
     if (threadIdx.x == 0 && p.oready) atomicAdd(p.fwork + 2, 1u);
