@@ -602,7 +602,20 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
       }
       if (row < C) part[grp * C + row] = rs;
     }
+    // phase B's products that need no dS^T (dO Delta^T and -dDelta V^T) are issued now,
+    // once epilogue A's tiles and TMEM reads are done, and run under the -e^G K pass and
+    // the dS^T load; the rest follow behind them and one commit covers all five
+    const uint32_t dvp = (uint32_t)Dv * 128u;   // Delta^T tiles read MN-major
+    tc::fence_async_smem();
+    tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_tile_x(tmp + 128, tc::smem_u32(tA2), false, 128u * 128u, 64, tc::smem_u32(tDl), true,
+                     dvp, C, Dv, 0u);                                                    // dO Delta^T
+      tc::mma_tile_p(tmp + 192, tc::smem_u32(tA2) + 64u * 128u, 128u * 128u, 64,
+                     tc::smem_u32(tV), (uint32_t)C * 128u, C, Dv, 0u);                  // -dDelta V^T
+    }
     if (tid < C) dG[tid] += p.scale * ev[tid] * rsum_g(part, tid);
     // ---- phase B: dS tile, P tile (bulk), e^G K from K^T, <S, dS>
     if (tid == 0) {
@@ -672,15 +685,10 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     }
     tc::fence_async_smem();
     ok = mma_run([&] {
-      const uint32_t dvp = (uint32_t)Dv * 128u;   // Delta^T tiles read MN-major
       tc::mma_tile_x(tmp, tc::smem_u32(tDlc), true, dvp, 64, tc::smem_u32(tdS), true, sVC, NK, Dv,
                      0u);                                                                // c Delta dS^T
       tc::mma_tile_x(tdK, tc::smem_u32(tDlc), true, dvp, 64, tc::smem_u32(tdS), true, sVC, NK, Dv,
                      acc_first);                                                         // dK +=
-      tc::mma_tile_x(tmp + 128, tc::smem_u32(tA2), false, 128u * 128u, 64, tc::smem_u32(tDl), true,
-                     dvp, C, Dv, 0u);                                                    // dO Delta^T
-      tc::mma_tile_p(tmp + 192, tc::smem_u32(tA2) + 64u * 128u, 128u * 128u, 64,
-                     tc::smem_u32(tV), (uint32_t)C * 128u, C, Dv, 0u);                  // -dDelta V^T
       tc::mma_tile(tmp + 192, tc::smem_u32(tdW), 64, tc::smem_u32(tKe), C, Dk, 1u);     // - dW (e^G K)^T
     }, &bars[0], mphase, p.status, c);
     if (!ok) break;
