@@ -806,6 +806,29 @@ def run_kda(wl, device, pk, n_seqs=64, prefill_tokens=1024, steps=20, warmup=3):
             ms = e0.elapsed_time(e1) / 2
             entry["training_step_ms"] = ms
             entry["training_tokens_per_s"] = T / (ms * 1e-3)
+            # the same prefill chunked on the tensor cores (gdn_kda_forward_chunked)
+            if wl.dtype == "bf16" and Dk in (64, 128) and Dv in (64, 128):
+                off, NC = gdn.gdn_plan(np.array([0, T], dtype=np.int32))
+                shape_c = gdn.make_shape(Hk, Hv, Dk, Dv, N, NC, T, wl.dtype, 0.0)
+                coff = torch.from_numpy(off).to(device)
+                wsc = torch.empty(gdn.gdn_kda_forward_chunked_workspace_bytes(shape_c),
+                                  dtype=torch.uint8, device=device)
+
+                def chunked():
+                    gdn.gdn_kda_forward_chunked(shape_c, q, k, v, alpha, beta, a_log, b_alpha, cu,
+                                                coff, S0, S_T, o, wsc)
+
+                chunked()
+                torch.cuda.synchronize()
+                e0.record()
+                for _ in range(steps):
+                    chunked()
+                e1.record()
+                torch.cuda.synchronize()
+                us_c = 1e3 * e0.elapsed_time(e1) / steps
+                entry["chunked"] = {"us_per_call": us_c, "tokens_per_s": T / (us_c * 1e-6),
+                                    "note": "gdn_kda_forward_chunked: the chunk algebra, "
+                                            "products, walk and output on the tensor cores"}
         out[name] = entry
     return out
 

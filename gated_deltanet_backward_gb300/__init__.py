@@ -110,6 +110,13 @@ _lib.gdn_state_compose.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int3
 _lib.gdn_state_compose.restype = ctypes.c_int
 _lib.gdn_kda_forward.argtypes = [_SP] + [_vp, _i64] * 5 + [_vp] * 5 + [_vp, _i64, _vp]
 _lib.gdn_kda_forward.restype = ctypes.c_int
+# shape; q,k,v,alpha,beta_raw (+ld); a_log, b_alpha, cu, coff, S_in, S_out; o (+ld); ws,
+# ws bytes, stream
+_lib.gdn_kda_forward_chunked.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 6 + [_vp, _i64] +
+                                         [_vp, _sz, _vp])
+_lib.gdn_kda_forward_chunked.restype = ctypes.c_int
+_lib.gdn_kda_forward_chunked_workspace_bytes.argtypes = [_SP]
+_lib.gdn_kda_forward_chunked_workspace_bytes.restype = _sz
 _lib.gdn_kda_backward_workspace_bytes.argtypes = [_SP]
 _lib.gdn_kda_backward_workspace_bytes.restype = _sz
 _lib.gdn_kda_backward.argtypes = ([_SP] + [_vp, _i64] * 5 + [_vp] * 4 + [_vp, _i64] + [_vp] +
@@ -135,7 +142,8 @@ EXPORTED = ("gdn_plan", "gdn_saved_state_bytes", "gdn_workspace_bytes", "gdn_for
             "gdn_conv1d_silu_backward", "gdn_gated_rmsnorm_forward",
             "gdn_gated_rmsnorm_workspace_bytes", "gdn_gated_rmsnorm_backward",
             "gdn_state_compose", "gdn_kda_forward", "gdn_kda_backward_workspace_bytes",
-            "gdn_kda_backward", "gdn_forward_gated_rmsnorm")
+            "gdn_kda_backward", "gdn_forward_gated_rmsnorm", "gdn_kda_forward_chunked",
+            "gdn_kda_forward_chunked_workspace_bytes")
 
 
 class GdnError(RuntimeError):
@@ -595,6 +603,32 @@ def gdn_kda_forward(shape, q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens,
     c.ready()
     args.append(_stream(stream))
     _check(_lib.gdn_kda_forward(*args), "gdn_kda_forward")
+
+
+def gdn_kda_forward_chunked_workspace_bytes(shape) -> int:
+    return int(_lib.gdn_kda_forward_chunked_workspace_bytes(ctypes.byref(shape)))
+
+
+def gdn_kda_forward_chunked(shape, q, k, v, alpha, beta_raw, a_log, b_alpha, cu_seqlens,
+                            chunk_offsets, S_in, S_out, o, workspace, stream=None) -> None:
+    """Calls gdn_kda_forward_chunked: gdn_kda_forward as a chunked prefill on the tensor
+    cores (bf16, Dk and Dv in {64, 128}); shape.total_chunks and chunk_offsets from
+    gdn_plan; workspace of gdn_kda_forward_chunked_workspace_bytes(shape) bytes."""
+    c = _Call("gdn_kda_forward_chunked")
+    tok = c.token_dtype(shape)
+    T, N, ns = int(shape.total_tokens), int(shape.n_seqs), _state_elems(shape)
+    args = [ctypes.byref(shape)]
+    args += _recurrence_inputs(c, shape, q, k, v, alpha, beta_raw, a_log, b_alpha, T,
+                               int(shape.Hv) * int(shape.Dk), tok)
+    args += [c.vec(cu_seqlens, "cu_seqlens", N + 1, I32),
+             c.vec(chunk_offsets, "chunk_offsets", N + 1, I32), c.vec(S_in, "S_in", ns, F32),
+             c.vec(S_out, "S_out", ns, F32)]
+    args += c.mat(o, "o", T, int(shape.Hv) * int(shape.Dv), tok)
+    args += [c.buf(workspace, "workspace", gdn_kda_forward_chunked_workspace_bytes(shape)),
+             _nbytes(workspace)]
+    c.ready()
+    args.append(_stream(stream))
+    _check(_lib.gdn_kda_forward_chunked(*args), "gdn_kda_forward_chunked")
 
 
 def gdn_kda_backward_workspace_bytes(shape) -> int:

@@ -373,6 +373,7 @@ const char* gdn_kernel_name(int32_t id) {
     case gdn::KID_KDA_FWD: return "gdn_kda_fwd";
     case gdn::KID_KDA_BWD: return "gdn_kda_bwd";
     case gdn::KID_FWD_OUT_TC: return "gdn_fwd_out_tc";
+    case gdn::KID_KDA_PREP_TC: return "gdn_kda_prep_tc";
     default: return "?";
   }
 }
@@ -852,6 +853,144 @@ int gdn_kda_forward(const gdn_shape* s, const void* q, int64_t q_ld, const void*
                                                 beta_raw, beta_ld, a_log, b_alpha, cu_seqlens,
                                                 S_in, S_out, o, o_ld, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail("gdn_kda_forward: kernel launch", e);
+  return GDN_OK;
+}
+
+// Workspace of the chunked KDA forward: status block and work counters, then per (chunk,
+// value head) the preparation's tiles (W, K e^{G_last - G}, Q e^G, U^T, P), e^{G_last}
+// and the walk's S^T and Delta^T tiles for the output pass.
+struct KdaChunkedLayout {
+  size_t status, sync, Wsw, Kcw, Qgw, Utb, Psw, Gl, Stb, Dtb, total;
+};
+static KdaChunkedLayout kda_chunked_layout(const gdn_shape& s) {
+  KdaChunkedLayout L{};
+  const size_t NCH = (size_t)s.total_chunks * s.Hv, C = gdn::kChunk;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = gdn::align256(off + bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.sync = take(256);
+  L.Wsw = take(NCH * gdn::tile_CxD(s.Dk));
+  L.Kcw = take(NCH * gdn::tile_CxD(s.Dk));
+  L.Qgw = take(NCH * gdn::tile_CxD(s.Dk));
+  L.Utb = take(NCH * (size_t)s.Dv * C * 2);
+  L.Psw = take(NCH * 8192);
+  L.Gl = take(NCH * (size_t)s.Dk * 4);
+  L.Stb = take(NCH * gdn::state_tile_bytes(s.Dk, s.Dv));
+  L.Dtb = take(NCH * (size_t)s.Dv * 128);
+  L.total = off;
+  return L;
+}
+
+static bool kda_chunked_shape_ok(const gdn_shape* s) {
+  return s->dtype == GDN_DTYPE_BF16 && (s->Dk == 64 || s->Dk == 128) &&
+         (s->Dv == 64 || s->Dv == 128);
+}
+
+size_t gdn_kda_forward_chunked_workspace_bytes(const gdn_shape* s) {
+  if (!s || check_shape(s) != GDN_OK || !kda_chunked_shape_ok(s)) return 0;
+  return kda_chunked_layout(*s).total;
+}
+
+int gdn_kda_forward_chunked(const gdn_shape* s, const void* q, int64_t q_ld, const void* k,
+                            int64_t k_ld, const void* v, int64_t v_ld, const float* alpha,
+                            int64_t alpha_ld, const float* beta_raw, int64_t beta_ld,
+                            const float* a_log, const float* b_alpha,
+                            const int32_t* cu_seqlens, const int32_t* chunk_offsets,
+                            const float* S_in, float* S_out, void* o, int64_t o_ld,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  GDN_TRY(check_shape(s));
+  if (!kda_chunked_shape_ok(s)) return GDN_ERR_UNSUPPORTED;
+  const int64_t T = s->total_tokens;
+  if (T > ((int64_t)1 << 31) - 1) return GDN_ERR_UNSUPPORTED;
+  GDN_TRY(check_matrix(q, q_ld, (int64_t)s->Hk * s->Dk, 2, T));
+  GDN_TRY(check_matrix(k, k_ld, (int64_t)s->Hk * s->Dk, 2, T));
+  GDN_TRY(check_matrix(v, v_ld, (int64_t)s->Hv * s->Dv, 2, T));
+  GDN_TRY(check_matrix(o, o_ld, (int64_t)s->Hv * s->Dv, 2, T));
+  GDN_TRY(check_gate_matrix(alpha, alpha_ld, (int64_t)s->Hv * s->Dk, T));
+  GDN_TRY(check_gate_matrix(beta_raw, beta_ld, s->Hv, T));
+  GDN_TRY(check_vec(a_log, true));
+  GDN_TRY(check_vec(b_alpha, true));
+  GDN_TRY(check_vec(S_in, false));
+  GDN_TRY(check_vec(S_out, s->n_seqs > 0));
+  if (s->n_seqs > 0) {
+    if (!cu_seqlens || !chunk_offsets) return GDN_ERR_INVALID_ARG;
+    if (((uintptr_t)cu_seqlens & 3u) != 0 || ((uintptr_t)chunk_offsets & 3u) != 0)
+      return GDN_ERR_MISALIGNED;
+  }
+  const KdaChunkedLayout L = kda_chunked_layout(*s);
+  if (!workspace || ((uintptr_t)workspace & 255u) != 0 || workspace_bytes < L.total)
+    return GDN_ERR_WORKSPACE;
+  if (s->n_seqs == 0) return GDN_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  (void)cudaGetLastError();
+  g_last_error[0] = 0;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, L.Wsw, st);   // status and counters
+  if (e != cudaSuccess) return cuda_fail("gdn_kda_forward_chunked: clearing the status word", e);
+  if (s->total_chunks == 0) {   // every sequence is empty: S_out = S_in
+    const size_t bytes = (size_t)s->n_seqs * s->Hv * s->Dk * s->Dv * sizeof(float);
+    e = S_in ? (S_in == S_out ? cudaSuccess
+                              : cudaMemcpyAsync(S_out, S_in, bytes, cudaMemcpyDeviceToDevice, st))
+             : cudaMemsetAsync(S_out, 0, bytes, st);
+    return e == cudaSuccess ? GDN_OK : cuda_fail("gdn_kda_forward_chunked: empty sequences", e);
+  }
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.Hk = s->Hk;
+  p.Hv = s->Hv;
+  p.Dk = s->Dk;
+  p.Dv = s->Dv;
+  p.r = s->Hv / s->Hk;
+  p.head_map = s->head_map;
+  p.n_seqs = s->n_seqs;
+  p.NC = s->total_chunks;
+  p.T = T;
+  p.scale = s->scale > 0.f ? s->scale : 1.0f / std::sqrt((float)s->Dk);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.q_ld = q_ld;
+  p.k_ld = k_ld;
+  p.v_ld = v_ld;
+  p.alpha = alpha;
+  p.alpha_ld = alpha_ld;
+  p.beta_raw = beta_raw;
+  p.beta_ld = beta_ld;
+  p.a_log = a_log;
+  p.b_alpha = b_alpha;
+  p.cu = cu_seqlens;
+  p.coff = chunk_offsets;
+  p.S0 = S_in;
+  p.S_T = S_out;
+  p.o = o;
+  p.o_ld = o_ld;
+  p.kda = 1;
+  char* base = (char*)workspace;
+  p.status = (gdn::DeviceStatus*)(base + L.status);
+  p.fwork = (uint32_t*)(base + L.sync);
+  p.Wsw = (uint8_t*)(base + L.Wsw);
+  p.Kcw = (uint8_t*)(base + L.Kcw);
+  p.Qgw = (uint8_t*)(base + L.Qgw);
+  p.Utb = (__nv_bfloat16*)(base + L.Utb);
+  p.Psw = (uint8_t*)(base + L.Psw);
+  p.Gl = (float*)(base + L.Gl);
+  p.Stb = (uint8_t*)(base + L.Stb);
+  p.Dtb = (uint8_t*)(base + L.Dtb);
+  gdn::TmaMaps maps;
+  if (!gdn::encode_tma_2d(&maps.q, q, (int64_t)s->Hk * s->Dk, T, q_ld) ||
+      !gdn::encode_tma_2d(&maps.k, k, (int64_t)s->Hk * s->Dk, T, k_ld) ||
+      !gdn::encode_tma_2d(&maps.v, v, (int64_t)s->Hv * s->Dv, T, v_ld)) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "gdn_kda_forward_chunked: cuTensorMapEncodeTiled failed");
+    return GDN_ERR_CUDA;
+  }
+  e = gdn::launch_kda_prep_tc(p, maps, st);
+  if (e == cudaSuccess) e = gdn::launch_fwd_state_tc(p, st);
+  if (e == cudaSuccess) e = gdn::launch_fwd_out_tc(p, st);
+  if (e != cudaSuccess) return cuda_fail("gdn_kda_forward_chunked: kernel launch", e);
   return GDN_OK;
 }
 

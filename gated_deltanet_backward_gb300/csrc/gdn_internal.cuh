@@ -224,6 +224,14 @@ struct Params {
   uint8_t* Stb;
   uint8_t* Dtb;
   uint8_t* Kcw;
+  // chunked KDA forward (a decay gate per key channel): kda set, the gates from alpha
+  // [T, Hv*Dk] and b_alpha [Hv*Dk]; its preparation leaves per (chunk, value head) the
+  // tile Q * e^G (Qgw, [C][Dk], the output's operand) and e^{G_last} (Gl, [Dk], the
+  // walk's per-channel decay); the walk and the output pass read those instead of G
+  int kda;
+  const float* b_alpha;
+  uint8_t* Qgw;
+  float* Gl;
 };
 
 // Key head of value head h, and the j-th (j < r) value head of key head kh: value
@@ -261,7 +269,8 @@ enum KernelId {
   KID_KDA_FWD = 20,
   KID_KDA_BWD = 21,
   KID_FWD_OUT_TC = 22,
-  KID_COUNT = 23
+  KID_KDA_PREP_TC = 23,
+  KID_COUNT = 24
 };
 
 // Bracket one launch with the caller's profiling events (no-op when none are
@@ -291,6 +300,7 @@ cudaError_t launch_fwd_fused_tc(const Params& p, const TmaMaps& maps, cudaStream
 cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st);
 // The output pass of the bf16 forward: O from the walk's state and Delta tiles.
 cudaError_t launch_fwd_out_tc(const Params& p, cudaStream_t st);
+cudaError_t launch_kda_prep_tc(const Params& p, const TmaMaps& maps, cudaStream_t st);
 cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st);
 
 // One decode step (gdn_decode_step): arguments validated by the caller.

@@ -620,6 +620,263 @@ done:
   return ok;
 }
 
+// ---------------------------------------------------------------------------
+// KDA variant (a decay gate per key channel, the KDA work log's module gate): one (chunk
+// c, value head h) preparation unit on a whole CTA (`sm`: 1024-aligned, kda_prep_bytes;
+// `tmem`: 256 columns; bar[0..2]: products, k / q rows, V rows).  The chunk algebra of
+// the per-channel recurrence, per value head (its gates differ from head to head):
+//   l[r][i] = -e^{a_log[h]} softplus(alpha[t][h Dk + i] + b_alpha[h Dk + i]),
+//   G = inclusive cumsum of l over the chunk's rows, channel by channel,
+//   A[r][s] = b_r sum_i K[r][i] K[s][i] e^{G[r][i] - G[s][i]}   (s < r),
+//   P[r][s] =     sum_i Q[r][i] K[s][i] e^{G[r][i] - G[s][i]}   (s <= r),
+// each pair summed over the channels on CUDA cores (G does not increase along the rows,
+// so every exponent is <= 0 and nothing overflows however fast the gates decay); then
+// T = (I + A)^-1, W = T diag(b) (K e^G) and U^T = V^T (T diag(b))^T on the tensor core,
+// and the operands of the walk and the output: K e^{G_last - G} (the state update),
+// Q e^G (the output's inter-chunk term), e^{G_last} (the walk's per-channel decay) and
+// P.  Rows past the chunk are zero and take no decay.  Dk, Dv in {64, 128}.
+constexpr int kGS = 128 + 4;   // row stride (floats) of the fp32 [C][Dk] gate matrix
+
+__host__ __device__ __forceinline__ size_t kda_prep_bytes(int Dk, int Dv) {
+  const size_t nbk = (size_t)(Dk + 63) / 64, nbv = (size_t)(Dv + 63) / 64;
+  return nbk * 128 * 128 + nbv * 8192 + 2 * 8192 + nbk * 8192 +
+         sizeof(float) * ((size_t)C * kGS + (size_t)C * TS + 1024 + C);
+}
+
+__device__ void kda_prep_unit(const Params& p, const TmaMaps& maps, int c, int h, uint8_t* sm,
+                              uint32_t tmem, uint64_t* bar) {
+  int n;
+  int64_t t0;
+  int len;
+  if (!chunk_info(p, c, &n, &t0, &len)) {
+    if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
+    return;
+  }
+  const int Dk = p.Dk, Dv = p.Dv, MV = Dv, NK = Dk;
+  const int tid = threadIdx.x, kh = key_head(p, h);
+  const int nbk = (Dk + 63) / 64, nbv = (Dv + 63) / 64;
+  const uint32_t aqk_pitch = 128u * 128u, bKC = tc::sw128_bytes(64, Dk);
+  uint8_t* tAQK = sm;                          // [128][Dk]: rows 0-63 K, 64-127 Q
+  uint8_t* sV = tAQK + nbk * aqk_pitch;        // [C][Dv] natural V (TMA)
+  uint8_t* tTB = sV + nbv * 8192;              // [C][C] T diag(b)
+  uint8_t* tP = tTB + 8192;                    // [C][C] P
+  uint8_t* tKg = tP + 8192;                    // [C][Dk] K e^G
+  float* Gf = (float*)(tKg + bKC);             // [C][kGS] G
+  float* Tm = Gf + C * kGS;                    // [C][TS] A, then T
+  float* Mt = Tm + C * TS;                     // [1024] scratch of the inverse
+  float* bv = Mt + 1024;                       // [C] beta
+  const uint32_t tAccW = tmem, tAccU = tmem + 128;
+  const size_t ch = (size_t)c * p.Hv + h;
+  uint32_t phase = 0, lphase = 0, vphase = 0;
+  if (tid == 0) {
+    issue_kq(p, maps, t0, kh, tAQK, &bar[1]);
+    tc::mbar_arrive_expect_tx(&bar[2], (uint32_t)nbv * 8192u);
+    for (int b = 0; b < nbv; ++b)
+      tc::tma_load_2d(sV + b * 8192, &maps.v, h * Dv + 64 * b, (int)t0, &bar[2]);
+  }
+  // 1. gates while the rows land: l, then the cumsum over the rows (four threads per
+  // channel, 16 rows each, combined by shuffles); beta; A and P start at zero
+  {
+    const float ea = expf(p.a_log[h]);
+    const float* arow = p.alpha + (size_t)h * Dk;
+    const float* barow = p.b_alpha + (size_t)h * Dk;
+    for (int idx = tid; idx < C * Dk; idx += kTcThreads) {
+      const int r = idx / Dk, i = idx % Dk;
+      Gf[r * kGS + i] = r < len ? -ea * softplus_f(arow[(t0 + r) * p.alpha_ld + i] + barow[i])
+                                : 0.f;
+    }
+    if (tid < C) bv[tid] = tid < len ? sigmoid_f(p.beta_raw[(t0 + tid) * p.beta_ld + h]) : 0.f;
+    for (int i = tid; i < C * TS; i += kTcThreads) Tm[i] = 0.f;
+    for (int i = tid; i < 8192 / 16; i += kTcThreads) ((uint4*)tP)[i] = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  if (tid < 4 * Dk) {
+    const int i = tid >> 2, part = tid & 3, r0 = part * 16;
+    float vals[16], run = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      vals[j] = Gf[(r0 + j) * kGS + i];
+      run += vals[j];
+    }
+    float inc = run;
+#pragma unroll
+    for (int d = 1; d < 4; d <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, d, 4);
+      if (part >= d) inc += y;
+    }
+    float acc = inc - run;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      acc += vals[j];
+      Gf[(r0 + j) * kGS + i] = acc;
+    }
+  }
+  // 2. L2 normalisation of the k / q rows in place (four threads per row), rows past the
+  // chunk zero
+  {
+    const bool lok = tc::mbar_wait(&bar[1], lphase);
+    lphase ^= 1u;
+    if (__syncthreads_or(lok ? 0 : 1)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+      return;
+    }
+  }
+  {
+    const int row = tid >> 2, part = tid & 3, t = row & (C - 1);
+    const int nch = Dk / 8, cpt = nch / 4;
+    uint4 raw[4];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < cpt) {
+        raw[j] = *(const uint4*)(tAQK + tc::sw128_offset(row, (part * cpt + j) * 8, 128));
+        const __nv_bfloat162* e = (const __nv_bfloat162*)&raw[j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(e[q]);
+          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+        }
+      }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float inv = t < len ? 1.f / sqrtf(ss + 1e-6f) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < cpt) {
+        const __nv_bfloat162* e = (const __nv_bfloat162*)&raw[j];
+        __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(e[q]);
+          pk[q] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+        }
+        *(uint4*)(tAQK + tc::sw128_offset(row, (part * cpt + j) * 8, 128)) = *(const uint4*)pk;
+      }
+  }
+  __syncthreads();
+  // 3. A and P, pair by pair over the channels (pairs s <= r in row-major order)
+  for (int idx = tid; idx < C * (C + 1) / 2; idx += kTcThreads) {
+    int r = (int)((sqrtf(8.f * (float)idx + 1.f) - 1.f) * 0.5f);
+    while ((r + 1) * (r + 2) / 2 <= idx) ++r;
+    while (r * (r + 1) / 2 > idx) --r;
+    const int s = idx - r * (r + 1) / 2;
+    float a = 0.f, pp = 0.f;
+    if (r < len) {
+      const float* gr = Gf + r * kGS;
+      const float* gs = Gf + s * kGS;
+      for (int k8 = 0; k8 < Dk; k8 += 8) {
+        const uint4 kr = *(const uint4*)(tAQK + tc::sw128_offset(r, k8, 128));
+        const uint4 ks = *(const uint4*)(tAQK + tc::sw128_offset(s, k8, 128));
+        const uint4 qr = *(const uint4*)(tAQK + tc::sw128_offset(C + r, k8, 128));
+        const float4 ga = *(const float4*)(gr + k8), gb = *(const float4*)(gr + k8 + 4);
+        const float4 ha = *(const float4*)(gs + k8), hb = *(const float4*)(gs + k8 + 4);
+        const float e[8] = {__expf(ga.x - ha.x), __expf(ga.y - ha.y), __expf(ga.z - ha.z),
+                            __expf(ga.w - ha.w), __expf(gb.x - hb.x), __expf(gb.y - hb.y),
+                            __expf(gb.z - hb.z), __expf(gb.w - hb.w)};
+        const __nv_bfloat162* k2r = (const __nv_bfloat162*)&kr;
+        const __nv_bfloat162* k2s = (const __nv_bfloat162*)&ks;
+        const __nv_bfloat162* q2r = (const __nv_bfloat162*)&qr;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 fr = __bfloat1622float2(k2r[q]), fs = __bfloat1622float2(k2s[q]);
+          const float2 fq = __bfloat1622float2(q2r[q]);
+          const float k0 = fs.x * e[2 * q], k1 = fs.y * e[2 * q + 1];
+          a = fmaf(fr.x, k0, fmaf(fr.y, k1, a));
+          pp = fmaf(fq.x, k0, fmaf(fq.y, k1, pp));
+        }
+      }
+    }
+    if (s < r) Tm[r * TS + s] = bv[r] * a;
+    *(__nv_bfloat16*)(tP + tc::sw128_offset(r, s, C)) = __float2bfloat16_rn(pp);
+  }
+  __syncthreads();
+  // 4. T = (I + A)^-1
+  tri_inverse(Tm, 1, Mt);
+  // 5. T diag(b) and K e^G into the product tiles; Q e^G, K e^{G_last - G}, e^{G_last}
+  // and P into the workspace
+  {
+    const int r = tid >> 3, s8 = (tid & 7) * 8;   // one 8-column piece of T a thread
+    __align__(16) __nv_bfloat162 pb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      pb[u] = __floats2bfloat162_rn(Tm[r * TS + s8 + 2 * u] * bv[s8 + 2 * u],
+                                    Tm[r * TS + s8 + 2 * u + 1] * bv[s8 + 2 * u + 1]);
+    *(uint4*)(tTB + tc::sw128_offset(r, s8, C)) = *(const uint4*)pb;
+    *(uint4*)(p.Psw + ch * 8192 + tc::sw128_offset(r, s8, C)) =
+        *(const uint4*)(tP + tc::sw128_offset(r, s8, C));
+  }
+  {
+    const float* gl = Gf + (len - 1) * kGS;
+    for (int idx = tid; idx < C * (NK / 8); idx += kTcThreads) {
+      const int s = idx / (NK / 8), k8 = (idx % (NK / 8)) * 8;
+      const uint4 kraw = *(const uint4*)(tAQK + tc::sw128_offset(s, k8, 128));
+      const uint4 qraw = *(const uint4*)(tAQK + tc::sw128_offset(C + s, k8, 128));
+      const __nv_bfloat162* k2 = (const __nv_bfloat162*)&kraw;
+      const __nv_bfloat162* q2 = (const __nv_bfloat162*)&qraw;
+      const float* g = Gf + s * kGS + k8;
+      __align__(16) __nv_bfloat162 kg[4], qg[4], kc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 fk = __bfloat1622float2(k2[q]), fq = __bfloat1622float2(q2[q]);
+        const float e0 = __expf(g[2 * q]), e1 = __expf(g[2 * q + 1]);
+        const float c0 = s < len ? __expf(gl[k8 + 2 * q] - g[2 * q]) : 0.f;
+        const float c1 = s < len ? __expf(gl[k8 + 2 * q + 1] - g[2 * q + 1]) : 0.f;
+        kg[q] = __floats2bfloat162_rn(fk.x * e0, fk.y * e1);
+        qg[q] = __floats2bfloat162_rn(fq.x * e0, fq.y * e1);
+        kc[q] = __floats2bfloat162_rn(fk.x * c0, fk.y * c1);
+      }
+      const uint32_t off = tc::sw128_offset(s, k8, C);
+      *(uint4*)(tKg + off) = *(const uint4*)kg;
+      *(uint4*)(p.Qgw + ch * bKC + off) = *(const uint4*)qg;
+      *(uint4*)(p.Kcw + ch * bKC + off) = *(const uint4*)kc;
+    }
+    if (tid < Dk) p.Gl[ch * Dk + tid] = expf(gl[tid]);
+  }
+  // 6. V rows (past the chunk zero), then W = T diag(b) (K e^G) and U^T = V^T (T diag(b))^T
+  {
+    const bool lok = tc::mbar_wait(&bar[2], vphase & 1u);
+    vphase ^= 1u;
+    if (__syncthreads_or(lok ? 0 : 1)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
+      return;
+    }
+  }
+  if (len < C)
+    for (int idx = tid; idx < nbv * (C - len) * 8; idx += kTcThreads) {
+      const int b2 = idx / ((C - len) * 8), rem = idx % ((C - len) * 8);
+      ((uint4*)(sV + b2 * 8192 + (len + rem / 8) * 128))[rem % 8] = make_uint4(0, 0, 0, 0);
+    }
+  tc::fence_async_smem();
+  const bool ok = mma_run([&] {
+    // W = (T diag(b)) (K e^G): B is K e^G read MN-major from its natural tile
+    tc::mma_tile_x(tAccW, tc::smem_u32(tTB), false, 8192u, 64, tc::smem_u32(tKg), true, 8192u,
+                   NK, C, 0u);
+    // U^T = V^T (T diag(b))^T: A is V^T read MN-major from the natural V tile
+    tc::mma_tile_x(tAccU, tc::smem_u32(sV), true, 8192u, MV, tc::smem_u32(tTB), false, 8192u, C,
+                   C, 0u);
+  }, &bar[0], phase, p.status, c);
+  if (!ok) return;
+  acc_walk64(tAccW, Dk, C, [&](int s, int col0, const float* v) {
+    tile_put16(p.Wsw + ch * bKC, C, s, col0, v);
+  });
+  acc_walk(tAccU, MV, 64, Dv, [&](int vv, int col0, const float* v) {
+    tile_put16((uint8_t*)(p.Utb + ch * Dv * C), Dv, vv, col0, v);
+  });
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) k_kda_prep_tc(Params p,
+                                                              const __grid_constant__ TmaMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  CtaCtl* ctl = (CtaCtl*)base;
+  cta_setup(ctl, 3, 256);
+  kda_prep_unit(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
+  cta_teardown(ctl, 256);
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
                                                           const __grid_constant__ TmaMaps maps,
                                                           int bwd) {
@@ -661,7 +918,9 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const int tid = threadIdx.x, grp = col_group();
   const uint32_t bW = (uint32_t)tileCD(DK);
-  const uint32_t bU = (uint32_t)Dv * C * 2, bG = C * 4;
+  // G slot: the chunk's G (C floats), or e^{G_last} per channel for KDA (DK floats)
+  constexpr int EVS = DK > C ? DK : C;
+  const uint32_t bU = (uint32_t)Dv * C * 2, bG = EVS * 4, gbytes = (p.kda ? DK : C) * 4;
   const uint32_t bSt = tc::sw128_bytes(MV, DK);       // one saved S^T tile
   uint8_t* tSt = sm;                                  // [MV][DK]
   uint8_t* buf0 = tSt + tc::sw128_bytes(MV, DK);
@@ -670,7 +929,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   const uint32_t bHalf = (uint32_t)(DK / 2) * Dv * 4; // half an fp32 state
   float* stg0 = (float*)(tDt + MV * 128);             // [DK / 2][Dv] fp32 staging, rows
   float* stg1 = (float*)((uint8_t*)stg0 + ((bHalf + 1023) & ~1023u));   // 0.. and DK/2..
-  float* evb = (float*)((uint8_t*)stg1 + ((bHalf + 1023) & ~1023u));   // [2][C] e^G
+  float* evb = (float*)((uint8_t*)stg1 + ((bHalf + 1023) & ~1023u));   // [2][EVS] decay
   auto tW = [&](int b) { return buf0 + b * bufsz; };
   auto tK = [&](int b) { return buf0 + b * bufsz + bW; };   // diag(c) K of the value head
   auto sU = [&](int b) { return (const __nv_bfloat16*)(buf0 + b * bufsz + 2 * bW); };
@@ -707,11 +966,14 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   auto issue_load = [&](int cc, int b) {
     uint64_t* lb = &bars[1 + b];
     const size_t chh = (size_t)cc * p.Hv + h;
-    tc::mbar_arrive_expect_tx(lb, 2 * bW + bU + bG);
+    tc::mbar_arrive_expect_tx(lb, 2 * bW + bU + gbytes);
     tc::bulk_g2s(tW(b), p.Wsw + chh * bW, bW, lb);
     tc::bulk_g2s(tK(b), p.Kcw + chh * bW, bW, lb);
     tc::bulk_g2s((void*)sU(b), p.Utb + chh * Dv * C, bU, lb);
-    tc::bulk_g2s((void*)sG(b), p.G + chh * C, bG, lb);
+    if (p.kda)
+      tc::bulk_g2s((void*)sG(b), p.Gl + chh * DK, gbytes, lb);
+    else
+      tc::bulk_g2s((void*)sG(b), p.G + chh * C, gbytes, lb);
   };
   // Thread 0 issues chunk loads in order; a fused launch first needs the preparation
   // unit's flag (blocking only when the walk cannot go on without the chunk).
@@ -751,7 +1013,12 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       return false;
     }
     const float* G = sG(b);
-    if (tid == 0) evb[b * C] = expf(G[len - 1]);
+    // the state's decay over the chunk: e^{G_last} (or, for KDA, per channel)
+    if (p.kda) {
+      if (tid < DK) evb[b * EVS + tid] = G[tid];
+    } else if (tid == 0) {
+      evb[b * EVS] = expf(G[len - 1]);
+    }
     mma_issue([&] {
       // the previous chunk's Delta^T store has read its tile (the epilogue after this
       // product rewrites it); its two fp32 halves, stored after it, may still be read
@@ -857,7 +1124,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
       try_issue(c + 2, false);
     }
     // S^T <- e^{G_last} S^T + Delta^T diag(c) K
-    const float eC = evb[b * C];
+    const float eC = evb[b * EVS];
 #pragma unroll
     for (int ii = 0; ii < NKC; ++ii) {
       const int col0 = grp * 16 + 16 * kGroups * ii;
@@ -866,8 +1133,13 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
         tc::tmem_ld16(tS + lane_quarter() + col0, x);
         tc::tmem_ld_wait();
         if (vok) {
+          if (p.kda) {   // row k of S decays by its own channel's gate
 #pragma unroll
-          for (int j = 0; j < 16; ++j) S[ii][j] = fmaf(eC, S[ii][j], x[j]);
+            for (int j = 0; j < 16; ++j) S[ii][j] = fmaf(evb[b * EVS + col0 + j], S[ii][j], x[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) S[ii][j] = fmaf(eC, S[ii][j], x[j]);
+          }
           tile_put16(tSt, MV, vrow, col0, S[ii]);
         }
       }
@@ -924,18 +1196,27 @@ __device__ void out_unit(const Params& p, int c, int kh, uint8_t* sm, uint32_t t
   float* ev = sG + C;                // [C] scale e^G
   const uint32_t tO1 = tmem, tO2 = tmem + 128;   // Q S and P Delta (M = 64)
   const uint8_t* tiles = p.saved && p.bf16_states ? (const uint8_t*)p.saved : p.Stb;
-  // thread 0: value head j's S^T, Delta^T, P and G tiles on one phase of bars[0]
+  // thread 0: value head j's S^T, Delta^T, P and G tiles on one phase of bars[0]; for
+  // KDA its own Q e^G tile instead of G (the key head's Q tile and e^G scaling serve the
+  // scalar gate)
   auto issue_head = [&](int j, uint32_t extra) {
     const size_t ch = (size_t)c * p.Hv + value_head(p, kh, j);
-    tc::mbar_arrive_expect_tx(lbar, extra + bSt + bDt + bP + bG);
+    tc::mbar_arrive_expect_tx(lbar, extra + bSt + bDt + bP + (p.kda ? bQ : bG));
     tc::bulk_g2s(tS, tiles + ch * bSt, bSt, lbar);
     tc::bulk_g2s(tD, p.Dtb + ch * bDt, bDt, lbar);
     tc::bulk_g2s(tP, p.Psw + ch * bP, bP, lbar);
-    tc::bulk_g2s(sG, p.G + ch * C, bG, lbar);
+    if (p.kda)
+      tc::bulk_g2s(tQ, p.Qgw + ch * bQ, bQ, lbar);
+    else
+      tc::bulk_g2s(sG, p.G + ch * C, bG, lbar);
   };
   if (tid == 0) {
-    issue_head(0, bQ);
-    tc::bulk_g2s(tQ, p.Qsw + ((size_t)c * p.Hk + kh) * bQ, bQ, lbar);
+    if (p.kda) {
+      issue_head(0, 0u);
+    } else {
+      issue_head(0, bQ);
+      tc::bulk_g2s(tQ, p.Qsw + ((size_t)c * p.Hk + kh) * bQ, bQ, lbar);
+    }
   }
   for (int j = 0; j < p.r; ++j) {
     const int h = value_head(p, kh, j);
@@ -945,7 +1226,7 @@ __device__ void out_unit(const Params& p, int c, int kh, uint8_t* sm, uint32_t t
       if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT, c);
       return;
     }
-    if (tid < C) ev[tid] = p.scale * expf(sG[tid]);
+    if (tid < C) ev[tid] = p.kda ? p.scale : p.scale * expf(sG[tid]);
     // O1 = Q S (B = the S^T tile), O2 = P Delta (B = the Delta^T tile)
     const bool ok = mma_run([&] {
       tc::mma_tile_p(tO1, tc::smem_u32(tQ), 8192u, 64, tc::smem_u32(tS), (uint32_t)MV * 128u, Dv,
@@ -1204,11 +1485,22 @@ template <int DK>
 static size_t fwd_state_tc_smem(const Params& p) {
   const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
   const size_t bW = tc::sw128_bytes(64, DK);
-  const size_t bU = (size_t)Dv * C * 2, bG = C * 4;
+  constexpr size_t EVS = DK > C ? DK : C;
+  const size_t bU = (size_t)Dv * C * 2, bG = EVS * 4;
   const size_t bufsz = bW * 2 + ((bU + bG + 1023) & ~(size_t)1023);
   const size_t bHalf = ((size_t)(DK / 2) * Dv * 4 + 1023) & ~(size_t)1023;
-  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 + 2 * bHalf + 2 * C * 4 +
+  return tc::sw128_bytes(MV, DK) + 2 * bufsz + (size_t)MV * 128 + 2 * bHalf + 2 * EVS * 4 +
          kCtlBytes + 1024;
+}
+
+cudaError_t launch_kda_prep_tc(const Params& p, const TmaMaps& maps, cudaStream_t st) {
+  if (p.NC == 0) return cudaSuccess;
+  const size_t smem = kda_prep_bytes(p.Dk, p.Dv) + kCtlBytes + 1024;
+  cudaFuncSetAttribute(k_kda_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  profile_pre(st, KID_KDA_PREP_TC);
+  k_kda_prep_tc<<<dim3(p.NC, p.Hv), kTcThreads, smem, st>>>(p, maps);
+  profile_post(st);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st) {

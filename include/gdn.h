@@ -431,6 +431,31 @@ int gdn_kda_forward(const gdn_shape* shape, const void* q, int64_t q_ld, const v
                     const float* b_alpha, const int32_t* cu_seqlens, const float* S_in,
                     float* S_out, void* o, int64_t o_ld, void* stream);
 
+/* gdn_kda_forward as a chunked prefill on the tensor cores (bf16 inputs, Dk and Dv in
+ * {64, 128}): the same recurrence and outputs (o, S_out), formed chunk by chunk (C = 64
+ * tokens) from the per-channel chunk algebra.  Per (chunk, value head), with l the
+ * per-channel log gates and G their inclusive cumsum over the chunk's rows:
+ *   A[r][s] = b_r sum_i k_r[i] k_s[i] e^{G_r[i] - G_s[i]} (s < r),  T = (I + A)^-1,
+ *   P[r][s] = sum_i q_r[i] k_s[i] e^{G_r[i] - G_s[i]} (s <= r),
+ *   W = T diag(b) (K e^G),  U = T diag(b) V,  Delta = U - W S,
+ *   O = scale ((Q e^G) S + P Delta),  S' = diag(e^{G_last}) S + (K e^{G_last - G})^T Delta.
+ * A and P are summed pair by pair over the channels on CUDA cores, so every exponent is
+ * <= 0 however fast the gates decay; T, the products, the chunk walk and the output run
+ * on the tensor cores (the walk carries S in fp32).
+ * shape: as for gdn_forward (total_chunks and chunk_offsets from gdn_plan).
+ * Arguments as gdn_kda_forward, plus chunk_offsets (device, int32 [n_seqs + 1]) and a
+ * workspace of gdn_kda_forward_chunked_workspace_bytes(shape) bytes (256-byte aligned;
+ * 0 for an unsupported shape).  Returns GDN_ERR_UNSUPPORTED for fp32 inputs or other head
+ * sizes (use gdn_kda_forward), otherwise as gdn_forward. */
+size_t gdn_kda_forward_chunked_workspace_bytes(const gdn_shape* shape);
+int gdn_kda_forward_chunked(const gdn_shape* shape, const void* q, int64_t q_ld,
+                            const void* k, int64_t k_ld, const void* v, int64_t v_ld,
+                            const float* alpha, int64_t alpha_ld, const float* beta_raw,
+                            int64_t beta_ld, const float* a_log, const float* b_alpha,
+                            const int32_t* cu_seqlens, const int32_t* chunk_offsets,
+                            const float* S_in, float* S_out, void* o, int64_t o_ld,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* Reverse mode of gdn_kda_forward, in token form: given dO and dS_T (NULL = zero) it
  * returns dq, dk (summed over the value heads that share a key head), dv, d alpha
  * [total_tokens, Hv*Dk], d beta_raw, d a_log [Hv], d b_alpha [Hv*Dk] (sums over every

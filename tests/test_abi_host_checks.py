@@ -276,3 +276,35 @@ def test_forward_gated_rmsnorm_checks(gdn):
     # the recurrence's own checks come first, as in gdn_forward
     assert run(q=None) == INVALID
     assert run(ws_bytes=ws - 1) == WORKSPACE
+
+
+# --- gdn_kda_forward_chunked -----------------------------------------------------------
+
+KDAC_ORDER = ["shape", "q", "q_ld", "k", "k_ld", "v", "v_ld", "alpha", "alpha_ld", "beta",
+              "beta_ld", "a_log", "b_alpha", "cu", "coff", "S_in", "S_out", "o", "o_ld", "ws",
+              "ws_bytes", "stream"]
+
+
+def test_kda_forward_chunked_checks(gdn):
+    f = Fake()
+    s = gdn.make_shape(2, 6, 128, 128, 1, 2, 100, "bf16")
+    ws = gdn.gdn_kda_forward_chunked_workspace_bytes(s)
+    assert ws > 0
+    wq, wv = 2 * 128, 6 * 128
+    a = dict(shape=ctypes.byref(s), q=f(), q_ld=wq, k=f(), k_ld=wq, v=f(), v_ld=wv, alpha=f(),
+             alpha_ld=6 * 128, beta=f(), beta_ld=6, a_log=f(), b_alpha=f(), cu=f(), coff=f(),
+             S_in=None, S_out=f(), o=f(), o_ld=wv, ws=f(), ws_bytes=ws, stream=None)
+    run = lambda **o: _call(gdn._lib.gdn_kda_forward_chunked, KDAC_ORDER, a, **o)
+    assert run(alpha_ld=6 * 128 - 1) == INVALID          # one gate column per key channel
+    assert run(b_alpha=None) == INVALID and run(a_log=None) == INVALID
+    assert run(coff=None) == INVALID and run(cu=None) == INVALID
+    assert run(coff=a["coff"] + 2) == MISALIGNED
+    assert run(S_out=None) == INVALID
+    assert run(ws_bytes=ws - 1) == WORKSPACE and run(ws=a["ws"] + 16) == WORKSPACE
+    assert run(q_ld=wq + 1) == MISALIGNED
+    for dt, Dk, Dv in (("f32", 128, 128), ("bf16", 32, 128), ("bf16", 128, 16)):
+        s2 = gdn.make_shape(2, 6, Dk, Dv, 1, 2, 100, dt)
+        assert gdn.gdn_kda_forward_chunked_workspace_bytes(s2) == 0
+        assert run(shape=ctypes.byref(s2)) == UNSUPPORTED
+    s3 = gdn.make_shape(2, 6, 128, 128, 0, 0, 0, "bf16")
+    assert run(shape=ctypes.byref(s3), cu=None, coff=None, S_out=None) == OK
