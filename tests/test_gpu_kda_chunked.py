@@ -4,8 +4,9 @@ the oracle's KDA recurrence and against the token-form kernel (gdn_kda_forward):
 * o and S_out on ragged varlen batches (several chunks, ragged tails, one-token and empty
   sequences), both head sizes (64, 128, Dk != Dv), key heads shared by value heads
   under both head maps, a start state and in-place state;
-* gates that decay fast (large a_log), where a chunk's cumulative decay underflows: the
-  pairwise Gram sums keep every exponent <= 0, so nothing overflows;
+* gates that decay fast (large a_log), where a chunk's cumulative decay underflows and
+  every 16-row block's own pairs are summed channel by channel; and chunks where only
+  some blocks decay that fast, so both ways of forming a block's pairs meet in one A;
 * unsupported shapes are refused before anything runs.
 """
 import numpy as np
@@ -116,6 +117,25 @@ def test_fast_decaying_gates_stay_finite_and_match(torch_cuda):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
     assert rel_err(o, o_ref) <= TOL["bf16"]
     assert rel_err(S, S_ref) <= TOL["bf16"]
+
+
+def test_blocks_with_fast_and_slow_gates_mix(torch_cuda):
+    """alpha raised by 12 on rows 16-31 of every chunk: those blocks decay by more than
+    e^60 over their 16 rows (their own pairs are summed channel by channel), the others
+    go through the block products whole."""
+    torch = torch_cuda
+    import gated_deltanet_backward_gb300 as gdn
+    wl, inp, alpha, b_alpha, a_log = _case(2, 4, 128, 128, (200, 70, 33), seed=13)
+    cu = inp.cu_seqlens
+    for n in range(len(cu) - 1):
+        rows = np.arange(cu[n], cu[n + 1])
+        band = rows[((rows - cu[n]) % 64 >= 16) & ((rows - cu[n]) % 64 < 32)]
+        alpha[band] += np.float32(12.0)
+    o, S = _run_chunked(torch, gdn, wl, inp, alpha, b_alpha, a_log)
+    o_ref, S_ref = _ref(wl, inp, alpha, b_alpha, a_log)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    assert rel_err(o, o_ref) <= TOL["bf16"], rel_err(o, o_ref)
+    assert rel_err(S, S_ref) <= TOL["bf16"], rel_err(S, S_ref)
 
 
 def test_in_place_state(torch_cuda):
