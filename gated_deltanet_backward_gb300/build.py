@@ -17,8 +17,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libgdn.so")
 OBJ = os.path.join(HERE, "_build")
-SOURCES = ["gdn_api.cu", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_tc_fwd.cu", "gdn_tc_bwd.cu", "gdn_noalloc.cu",
-           "gdn_decode.cu", "gdn_neighbours.cu", "gdn_context.cu", "gdn_kda.cu"]
+SOURCES = ["gdn_api.cu", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_tc_fwd.cu", "gdn_tc_bwd.cu",
+           "gdn_tc_kda.cu", "gdn_noalloc.cu", "gdn_decode.cu", "gdn_neighbours.cu",
+           "gdn_context.cu", "gdn_kda.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
