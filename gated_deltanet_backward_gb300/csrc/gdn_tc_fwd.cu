@@ -37,9 +37,14 @@ constexpr int TS = C + 4;   // row stride (floats) of the fp32 [C][C] matrices o
 //   32x32 diagonal blocks: lower-left 16x16 = -D_1 A_10 D_0
 //   64x64: lower-left 32x32 = -T_B A_BA T_A (T_A, T_B the 32x32 diagonal inverses)
 // The 32x32 level runs 1 x 4 register tiles (one row, four columns per thread), the
-// 64x64 level 4 x 4 tiles on 2 nh warps.  Scratch M: nh * 1024 floats.
+// 64x64 level 4 x 4 tiles on 2 nh warps.  Scratch M: nh * 1024 floats.  Threads
+// 0 .. kTriThreads - 1 call it (all it uses for nh <= RB) and meet on named barrier 1;
+// the other warps stay free for work that does not need T.
+constexpr int kTriThreads = 128 * RB;
+static_assert(kTriThreads % 32 == 0 && kTriThreads < kTcThreads, "warps left beside the inverse");
 __device__ void tri_inverse(float* Tm, int nh, float* M) {
   const int tid = threadIdx.x;
+  const auto tri_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kTriThreads) : "memory"); };
   // 16x16 diagonal blocks: 16 threads per (head, block), thread j solves column j
   {
     const int unit = tid >> 4, j = tid & 15;
@@ -59,11 +64,11 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
         x[i] = a0 + a1;
       }
     }
-    __syncthreads();
+    tri_sync();
     if (act)
 #pragma unroll
       for (int i = 0; i < 16; ++i) B[i * TS + j] = x[i];
-    __syncthreads();
+    tri_sync();
   }
   // 32x32 diagonal blocks (two per head): M = A_10 D_0, then L = -D_1 M.  A thread
   // runs all its 1 x 4 tiles together over the whole k range (the zero triangles
@@ -98,7 +103,7 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
       const int it = tid + j * kTcThreads;
       if (it < n1) *(float4*)(M + (it >> 6) * 256 + ((it >> 2) & 15) * 16 + (it & 3) * 4) = acc[j];
     }
-    __syncthreads();
+    tri_sync();
 #pragma unroll
     for (int j = 0; j < kMax; ++j) {
       const int it = tid + j * kTcThreads;
@@ -129,7 +134,7 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
             make_float4(-acc[j].x, -acc[j].y, -acc[j].z, -acc[j].w);
       }
     }
-    __syncthreads();
+    tri_sync();
   }
   // 64x64: M = A_BA T_A, then lower-left = -T_B M.  Warp w < 2 nh owns a 32 x 16
   // piece of head w / 2 (columns 16 (w % 2) ...); a thread holds the 4 x 4 tile of rows
@@ -161,7 +166,7 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) *(float4*)(Mh + (rg + 8 * i) * 32 + cb) = acc[i];
     }
-    __syncthreads();
+    tri_sync();
     if (act) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -182,7 +187,7 @@ __device__ void tri_inverse(float* Tm, int nh, float* M) {
         *(float4*)(Tm + hh * C * TS + (32 + rg + 8 * i) * TS + cb) =
             make_float4(-acc[i].x, -acc[i].y, -acc[i].z, -acc[i].w);
     }
-    __syncthreads();
+    tri_sync();
   }
 }
 
@@ -435,20 +440,25 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& ta
       p.G[ch * C + t] = gv[hh * C + t];
       p.b[ch * C + t] = bv[hh * C + t];
     }
-    // A = diag(b) (E * K K^T), strictly lower, four columns per step
-    for (int idx = tid; idx < nh * C * (C / 4); idx += kTcThreads) {
+    // A = diag(b) (E * K K^T), strictly lower, four columns per step (C * C / 4 pieces a
+    // head: two passes of the CTA)
+    static_assert(C * C / 4 == 2 * kTcThreads, "two passes a head");
+#pragma unroll 2
+    for (int it = 0; it < 2 * nh; ++it) {
+      const int idx = tid + it * kTcThreads;
       const int hh = idx / (C * C / 4), e4 = idx % (C * C / 4), r = e4 / (C / 4), s0 = (e4 % (C / 4)) * 4;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
       if (s0 < r) {
         const float* g = gv + hh * C;
         const float br = bv[hh * C + r], gr = g[r];
         const float4 kk = *(const float4*)(KK + r * C + s0);
+        const float4 gs = *(const float4*)(g + s0);
         // the exponent is at most 0: the intrinsic's error (a few ulp) is far below the
         // bf16 rounding every product operand takes later
-        a.x = br * __expf(gr - g[s0]) * kk.x;
-        if (s0 + 1 < r) a.y = br * __expf(gr - g[s0 + 1]) * kk.y;
-        if (s0 + 2 < r) a.z = br * __expf(gr - g[s0 + 2]) * kk.z;
-        if (s0 + 3 < r) a.w = br * __expf(gr - g[s0 + 3]) * kk.w;
+        a.x = br * __expf(gr - gs.x) * kk.x;
+        if (s0 + 1 < r) a.y = br * __expf(gr - gs.y) * kk.y;
+        if (s0 + 2 < r) a.z = br * __expf(gr - gs.z) * kk.z;
+        if (s0 + 3 < r) a.w = br * __expf(gr - gs.w) * kk.w;
       }
       *(float4*)(Tm + hh * C * TS + r * TS + s0) = a;
     }
@@ -462,8 +472,34 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& ta
       }
       if (two_v && p.r > 1) issue_v(p, maps, t0, kh, 1, (uint8_t*)KK, &bar[3]);
     }
-    // 4. T = (I + A)^-1 for the nh heads at once
-    tri_inverse(Tm, nh, Mt);
+    // 4. T = (I + A)^-1 for the nh heads at once, while warps 12-15 write every head's
+    // diag(c) K with c_s = e^{G_last - G_s} (zero past the chunk), the operand the walk's
+    // state update S <- e^{G_last} S + (diag(c) K)^T Delta takes
+    if (tid < kTriThreads) {
+      tri_inverse(Tm, nh, Mt);
+    } else {
+      constexpr int nt = kTcThreads - kTriThreads;
+      const int t3 = tid - kTriThreads, c8n = NK / 8;
+      for (int hh = 0; hh < nh; ++hh) {
+        const float* G = gv + hh * C;
+        const float gl = G[len - 1];
+        uint8_t* dst = p.Kcw + ((size_t)c * p.Hv + value_head(p, kh, g0 + hh)) * bKC;
+        for (int idx = t3; idx < C * c8n; idx += nt) {
+          const int s = idx / c8n, k8 = (idx % c8n) * 8;
+          const uint4 raw = *(const uint4*)(tAQK + tc::sw128_offset(s, k8, 128));
+          const __nv_bfloat162* e = (const __nv_bfloat162*)&raw;
+          const float cs = s < len ? __expf(gl - G[s]) : 0.f;
+          __align__(16) __nv_bfloat162 pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(e[q]);
+            pk[q] = __floats2bfloat162_rn(f.x * cs, f.y * cs);
+          }
+          *(uint4*)(dst + tc::sw128_offset(s, k8, C)) = *(const uint4*)pk;
+        }
+      }
+    }
+    __syncthreads();
     // 5. per head: W = T diag(w) K, U^T = V^T (T diag(b))^T, P
     for (int hh = 0; hh < nh; ++hh) {
       const int h = value_head(p, kh, g0 + hh);
@@ -517,33 +553,6 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& ta
         rt = *(const uint4*)pt;
         rw = *(const uint4*)pw;
       }
-      // diag(c) K with c_s = e^{G_last - G_s} (zero past the chunk): the walk's state
-      // update S <- e^{G_last} S + (diag(c) K)^T Delta takes it as its operand.  Kept in
-      // registers for the store: NK / 8 threads per row.
-      constexpr int kKcMax = C * 16 / kTcThreads;   // pieces per thread at NK = 128
-      const int nkc = C * (NK / 8) / kTcThreads;
-      uint4 rk[kKcMax];
-      uint32_t koff[kKcMax];
-#pragma unroll
-      for (int i = 0; i < kKcMax; ++i) {
-        rk[i] = make_uint4(0, 0, 0, 0);
-        koff[i] = 0;
-        if (i < nkc) {
-          const int idx = tid + i * kTcThreads;
-          const int s = idx / (NK / 8), k8 = (idx % (NK / 8)) * 8;
-          const uint4 raw = *(const uint4*)(tAQK + tc::sw128_offset(s, k8, 128));
-          const __nv_bfloat162* e = (const __nv_bfloat162*)&raw;
-          const float cs = s < len ? __expf(G[len - 1] - G[s]) : 0.f;
-          __align__(16) __nv_bfloat162 pk[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 f = __bfloat1622float2(e[q]);
-            pk[q] = __floats2bfloat162_rn(f.x * cs, f.y * cs);
-          }
-          rk[i] = *(const uint4*)pk;
-          koff[i] = tc::sw128_offset(s, k8, C);
-        }
-      }
       {
         const uint32_t bit = odd ? 2u : 1u;
         const bool lok = tc::mbar_wait(odd ? &bar[3] : &bar[2], (vphase & bit) ? 1u : 0u);
@@ -576,9 +585,6 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& ta
         *(uint4*)(p.Tb + ch * 16384 + toff) = rt;
         *(uint4*)(p.Tb + ch * 16384 + 8192 + toff) = rw;
       }
-#pragma unroll
-      for (int i = 0; i < kKcMax; ++i)
-        if (i < nkc) *(uint4*)(p.Kcw + ch * bKC + koff[i]) = rk[i];
       ok = mma_wait(&bar[0], phase, p.status, c);
       if (!ok) goto done;
       if (tid == 0) {
