@@ -252,20 +252,24 @@ __device__ void issue_v(const Params& p, const TmaMaps& maps, int64_t t0, int kh
 // tile once its last product has read its own (setting link->kq_issued; link->next is
 // the raw work-counter value, a unit index only below NC Hk).  False after a timed-out
 // wait.
+template <int DK>
 __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& tab, int bwd,
                           int c, int kh, uint8_t* sm, uint32_t tmem, uint64_t* bar,
                           uint32_t& phase, uint32_t& lphase, uint32_t& vphase, PrepLink* link) {
   int n;
   int64_t t0;
   int len;
+  __shared__ int s_publish;   // the previous unit, handed from thread 0 to its publisher
   const bool kq_issued = link != nullptr && link->kq_issued;
   if (link != nullptr && threadIdx.x == 0) link->kq_issued = false;
   if (!chunk_info(p, tab, c, &n, &t0, &len)) {
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
     return true;
   }
-  const int Dk = p.Dk, Dv = p.Dv;
-  const int MV = Dv < 64 ? 64 : Dv, NK = Dk < 64 ? 64 : Dk;
+  constexpr int Dk = DK;   // the head size p.Dk, fixed by the instantiation
+  const int Dv = p.Dv;
+  const int MV = Dv < 64 ? 64 : Dv;
+  constexpr int NK = Dk < 64 ? 64 : Dk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nbk = (Dk + 63) / 64, nbv = (Dv + 63) / 64;
   const uint32_t aqk_pitch = 128u * 128u;               // 64-column blocks of the [K; Q] tile
@@ -462,14 +466,18 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& ta
       }
       *(float4*)(Tm + hh * C * TS + r * TS + s0) = a;
     }
+    // the previous unit goes for its publication to the inverse's last thread, which its
+    // first (16x16) phase leaves idle, so that the fence holds up no one
+    if (g0 == 0 && tid == 0) {
+      s_publish = link != nullptr ? link->pending : -1;
+      if (link != nullptr) link->pending = -1;
+    }
     tc::fence_async_smem();   // the K K^T reads come before the V tile that replaces it
     __syncthreads();
-    if (g0 == 0 && tid == 0) {
+    static_assert(kTriThreads - 1 >= 64 * RB, "the publisher sits out the 16x16 phase");
+    if (g0 == 0 && tid == kTriThreads - 1) {
       // every write of the previous unit came before this CTA's barriers: publish it
-      if (link != nullptr && link->pending >= 0) {
-        publish_flag(p.fready + link->pending);
-        link->pending = -1;
-      }
+      if (s_publish >= 0) publish_flag(p.fready + s_publish);
       if (two_v && p.r > 1) issue_v(p, maps, t0, kh, 1, (uint8_t*)KK, &bar[3]);
     }
     // 4. T = (I + A)^-1 for the nh heads at once, while warps 12-15 write every head's
@@ -626,6 +634,7 @@ done:
   return ok;
 }
 
+template <int DK>
 __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
                                                           const __grid_constant__ TmaMaps maps,
                                                           int bwd) {
@@ -637,8 +646,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
   uint32_t phase = 0, lphase = 0, vphase = 0;
   const SeqTab tab =
       seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)), kSeqCache);
-  prep_unit(p, maps, tab, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar,
-            phase, lphase, vphase, nullptr);
+  prep_unit<DK>(p, maps, tab, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem,
+                ctl->bar, phase, lphase, vphase, nullptr);
   cta_teardown(ctl, 256);
 }
 
@@ -1140,7 +1149,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
         uint32_t phase = 0, lphase = 0, vphase = 0;
         // every load and product of the unit has completed when it returns, and every
         // write came before its last barrier
-        prep_unit(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
+        prep_unit<DK>(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
                   ctl->bar, phase, lphase, vphase, nullptr);
         if (threadIdx.x == 0) {
           publish_flag(p.fready + u);
@@ -1176,7 +1185,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
         next = (int)atomicAdd(p.fwork, 1u);
         link.next = next;
       }
-      const bool ok = prep_unit(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes,
+      const bool ok = prep_unit<DK>(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes,
                                 ctl->tmem, ctl->bar, phase, lphase, vphase, &link);
       if (threadIdx.x == 0) {
         if (link.pending >= 0) {   // a unit that stopped before its stores
@@ -1245,9 +1254,13 @@ static size_t fwd_state_tc_smem(const Params& p) {
 cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st) {
   if (p.NC == 0) return cudaSuccess;
   const size_t smem = prep_tc_smem(p);
-  cudaFuncSetAttribute(k_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = p.Dk == 128 ? k_prep_tc<128>
+              : p.Dk == 64 ? k_prep_tc<64>
+              : p.Dk == 32 ? k_prep_tc<32>
+                           : k_prep_tc<16>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, bwd ? KID_PREP_TC_FULL : KID_PREP_TC);
-  k_prep_tc<<<dim3(p.NC, p.Hk), kTcThreads, smem, st>>>(p, maps, bwd ? 1 : 0);
+  kern<<<dim3(p.NC, p.Hk), kTcThreads, smem, st>>>(p, maps, bwd ? 1 : 0);
   profile_post(st);
   return cudaGetLastError();
 }
