@@ -299,6 +299,7 @@ __device__ __forceinline__ void prefetch_unit_states(const Params& p, int c, int
   }
 }
 
+template <int DK>
 __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, uint8_t* sm,
                            uint32_t tmem, uint64_t* bars, uint32_t& mphase, uint32_t& lphase,
                            int next_c = -1, int next_kh = 0) {
@@ -309,14 +310,16 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
     return;
   }
-  const int Dk = p.Dk, Dv = p.Dv;
+  constexpr int Dk = DK;   // the head size p.Dk, fixed by the instantiation
+  const int Dv = p.Dv;
   const int tid = threadIdx.x, warp = tid >> 5, grp = col_group();
   const uint32_t sCK = tc::sw128_bytes(C, Dk), sCV = tc::sw128_bytes(C, Dv);
   const uint32_t sCC = 8192;
   // tiles handed over by the state kernels: S^T and dS^T [MV][Dk], -dDelta^T [MV][C],
   // -dDelta [C][MV] (MV = Dv rounded up to 64); MMAs whose N is Dk read S / dS
   // MN-major with N rounded up to 64 (the tiles' padding columns are zero)
-  const int MV = Dv < 64 ? 64 : Dv, NK = Dk < 64 ? 64 : Dk;
+  const int MV = Dv < 64 ? 64 : Dv;
+  constexpr int NK = Dk < 64 ? 64 : Dk;
   const uint32_t bSt = tc::sw128_bytes(MV, Dk), sVC = (uint32_t)MV * 128;
   uint8_t* R1 = sm;
   uint8_t* R2 = R1 + 66560;
@@ -999,6 +1002,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   tc::fence_after_sync();
 }
 
+template <int DK>
 __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_grads_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   if (kept_operands_missing(p)) return;
@@ -1007,8 +1011,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_grads_tc(Params p,
   CtaCtl* ctl = (CtaCtl*)base;
   cta_setup(ctl, 2, 512);
   uint32_t mphase = 0, lphase = 0;
-  grads_unit(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar, mphase,
-             lphase);
+  grads_unit<DK>(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar, mphase,
+                 lphase);
   cta_teardown(ctl, 512);
 }
 
@@ -1054,8 +1058,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_fused_tc(Params p,
     if (threadIdx.x == 0) next = (int)atomicAdd(p.bwork, 1u);
     // thread 0 knows the next unit (the others pass a placeholder they do not use)
     const int nc = threadIdx.x == 0 && next < units ? p.NC - 1 - next / p.Hk : -1;
-    grads_unit(p, maps, p.NC - 1 - u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem, ctl->bar,
-               mphase, lphase, nc, threadIdx.x == 0 && next < units ? next % p.Hk : 0);
+    grads_unit<DK>(p, maps, p.NC - 1 - u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
+                   ctl->bar, mphase, lphase, nc, threadIdx.x == 0 && next < units ? next % p.Hk : 0);
   }
   cta_teardown(ctl, 512);
 }
@@ -1156,9 +1160,13 @@ cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st)
       if (e != cudaSuccess) return e;
     }
     const size_t smem = grads_tc_smem();
-    cudaFuncSetAttribute(k_bwd_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = p.Dk == 128 ? k_bwd_grads_tc<128>
+                : p.Dk == 64 ? k_bwd_grads_tc<64>
+                : p.Dk == 32 ? k_bwd_grads_tc<32>
+                             : k_bwd_grads_tc<16>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     profile_pre(st, KID_BWD_GRADS_TC);
-    k_bwd_grads_tc<<<dim3(p.NC, p.Hk), kTcThreads, smem, st>>>(p, maps);
+    kern<<<dim3(p.NC, p.Hk), kTcThreads, smem, st>>>(p, maps);
     profile_post(st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
