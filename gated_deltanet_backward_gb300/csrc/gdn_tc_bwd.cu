@@ -299,7 +299,7 @@ __device__ __forceinline__ void prefetch_unit_states(const Params& p, int c, int
   }
 }
 
-template <int DK>
+template <int DK, int DV>   // DV: the value head size when fixed, else 0 (p.Dv)
 __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, uint8_t* sm,
                            uint32_t tmem, uint64_t* bars, uint32_t& mphase, uint32_t& lphase,
                            int next_c = -1, int next_kh = 0) {
@@ -310,8 +310,8 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
     return;
   }
-  constexpr int Dk = DK;   // the head size p.Dk, fixed by the instantiation
-  const int Dv = p.Dv;
+  constexpr int Dk = DK;   // the head sizes p.Dk, p.Dv, fixed by the instantiation where it can
+  const int Dv = DV > 0 ? DV : p.Dv;
   const int tid = threadIdx.x, warp = tid >> 5, grp = col_group();
   const uint32_t sCK = tc::sw128_bytes(C, Dk), sCV = tc::sw128_bytes(C, Dv);
   const uint32_t sCC = 8192;
@@ -1002,7 +1002,7 @@ __device__ void grads_unit(const Params& p, const TmaMaps& maps, int c, int kh, 
   tc::fence_after_sync();
 }
 
-template <int DK>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_grads_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   if (kept_operands_missing(p)) return;
@@ -1011,7 +1011,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_grads_tc(Params p,
   CtaCtl* ctl = (CtaCtl*)base;
   cta_setup(ctl, 2, 512);
   uint32_t mphase = 0, lphase = 0;
-  grads_unit<DK>(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar, mphase,
+  grads_unit<DK, DV>(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar, mphase,
                  lphase);
   cta_teardown(ctl, 512);
 }
@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_grads_tc(Params p,
 // units in descending chunk order from a work counter, each waiting for its chunk's
 // flags, and every walk joins them when it is done.  Walks never wait on gradient
 // units, so the launch always finishes.
-template <int DK>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_fused_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   if (kept_operands_missing(p)) return;
@@ -1058,7 +1058,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_fused_tc(Params p,
     if (threadIdx.x == 0) next = (int)atomicAdd(p.bwork, 1u);
     // thread 0 knows the next unit (the others pass a placeholder they do not use)
     const int nc = threadIdx.x == 0 && next < units ? p.NC - 1 - next / p.Hk : -1;
-    grads_unit<DK>(p, maps, p.NC - 1 - u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
+    grads_unit<DK, DV>(p, maps, p.NC - 1 - u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
                    ctl->bar, mphase, lphase, nc, threadIdx.x == 0 && next < units ? next % p.Hk : 0);
   }
   cta_teardown(ctl, 512);
@@ -1112,7 +1112,7 @@ static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, c
 
 // The fused backward (k_bwd_fused_tc) under the same conditions as the fused forward;
 // *launched = false otherwise.
-template <int DK>
+template <int DK, int DV>
 static cudaError_t launch_bwd_fused_t(const Params& p, const TmaMaps& maps, cudaStream_t st,
                                       bool* launched) {
   *launched = false;
@@ -1121,32 +1121,44 @@ static cudaError_t launch_bwd_fused_t(const Params& p, const TmaMaps& maps, cuda
   if (sms <= 0 || walks + kMinProducers > sms || p.NC == 0) return cudaSuccess;
   const size_t a = bwd_state_tc_smem<DK>(p), b = grads_tc_smem();
   const size_t smem = (a > b ? a : b) + 64;
-  cudaError_t e = cudaFuncSetAttribute(k_bwd_fused_tc<DK>,
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_fused_tc<DK, DV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bwd_fused_tc<DK>, kTcThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bwd_fused_tc<DK, DV>, kTcThreads, smem);
   if (e != cudaSuccess || per_sm < 1) return cudaSuccess;
   Params pp = p;
   pp.bready = p.bwork + 64;   // the work counter's 256-byte slot, then the flags
   TmaMaps mm = maps;
   void* args[] = {&pp, &mm};
   profile_pre(st, KID_BWD_FUSED_TC);
-  e = cudaLaunchCooperativeKernel((const void*)k_bwd_fused_tc<DK>, dim3(sms), dim3(kTcThreads), args,
+  e = cudaLaunchCooperativeKernel((const void*)k_bwd_fused_tc<DK, DV>, dim3(sms), dim3(kTcThreads), args,
                                   smem, st);
   profile_post(st);
   if (e == cudaSuccess) *launched = true;
   return e;
 }
 
+// The instantiation with the value head size fixed when it equals the key head size.
+template <int DK>
+static cudaError_t launch_bwd_fused_dk(const Params& p, const TmaMaps& maps, cudaStream_t st,
+                                       bool* launched) {
+  return p.Dv == DK ? launch_bwd_fused_t<DK, DK>(p, maps, st, launched)
+                    : launch_bwd_fused_t<DK, 0>(p, maps, st, launched);
+}
+template <int DK>
+static void (*grads_kernel(const Params& p))(Params, TmaMaps) {
+  return p.Dv == DK ? k_bwd_grads_tc<DK, DK> : k_bwd_grads_tc<DK, 0>;
+}
+
 cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   bool fused = false;
   switch (p.Dk) {
-    case 16: e = launch_bwd_fused_t<16>(p, maps, st, &fused); break;
-    case 32: e = launch_bwd_fused_t<32>(p, maps, st, &fused); break;
-    case 64: e = launch_bwd_fused_t<64>(p, maps, st, &fused); break;
-    default: e = launch_bwd_fused_t<128>(p, maps, st, &fused); break;
+    case 16: e = launch_bwd_fused_dk<16>(p, maps, st, &fused); break;
+    case 32: e = launch_bwd_fused_dk<32>(p, maps, st, &fused); break;
+    case 64: e = launch_bwd_fused_dk<64>(p, maps, st, &fused); break;
+    default: e = launch_bwd_fused_dk<128>(p, maps, st, &fused); break;
   }
   if (e != cudaSuccess) return e;
   if (!fused) {
@@ -1160,10 +1172,10 @@ cudaError_t launch_bwd_tc(const Params& p, const TmaMaps& maps, cudaStream_t st)
       if (e != cudaSuccess) return e;
     }
     const size_t smem = grads_tc_smem();
-    auto kern = p.Dk == 128 ? k_bwd_grads_tc<128>
-                : p.Dk == 64 ? k_bwd_grads_tc<64>
-                : p.Dk == 32 ? k_bwd_grads_tc<32>
-                             : k_bwd_grads_tc<16>;
+    auto kern = p.Dk == 128 ? grads_kernel<128>(p)
+                : p.Dk == 64 ? grads_kernel<64>(p)
+                : p.Dk == 32 ? grads_kernel<32>(p)
+                             : grads_kernel<16>(p);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     profile_pre(st, KID_BWD_GRADS_TC);
     kern<<<dim3(p.NC, p.Hk), kTcThreads, smem, st>>>(p, maps);
