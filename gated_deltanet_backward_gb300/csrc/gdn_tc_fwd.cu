@@ -252,7 +252,7 @@ __device__ void issue_v(const Params& p, const TmaMaps& maps, int64_t t0, int kh
 // tile once its last product has read its own (setting link->kq_issued; link->next is
 // the raw work-counter value, a unit index only below NC Hk).  False after a timed-out
 // wait.
-template <int DK>
+template <int DK, int DV>   // DV: the value head size when fixed, else 0 (p.Dv)
 __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& tab, int bwd,
                           int c, int kh, uint8_t* sm, uint32_t tmem, uint64_t* bar,
                           uint32_t& phase, uint32_t& lphase, uint32_t& vphase, PrepLink* link) {
@@ -266,8 +266,8 @@ __device__ bool prep_unit(const Params& p, const TmaMaps& maps, const SeqTab& ta
     if (threadIdx.x == 0) set_status(p.status, GDN_ERR_DEVICE_BOUNDS, c);
     return true;
   }
-  constexpr int Dk = DK;   // the head size p.Dk, fixed by the instantiation
-  const int Dv = p.Dv;
+  constexpr int Dk = DK;   // the head sizes p.Dk, p.Dv, fixed by the instantiation where it can
+  const int Dv = DV > 0 ? DV : p.Dv;
   const int MV = Dv < 64 ? 64 : Dv;
   constexpr int NK = Dk < 64 ? 64 : Dk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -634,7 +634,7 @@ done:
   return ok;
 }
 
-template <int DK>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
                                                           const __grid_constant__ TmaMaps maps,
                                                           int bwd) {
@@ -646,7 +646,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
   uint32_t phase = 0, lphase = 0, vphase = 0;
   const SeqTab tab =
       seq_tab(p, (int32_t*)(base + kCtlBytes + prep_buffers_bytes(p.Dk, p.Dv)), kSeqCache);
-  prep_unit<DK>(p, maps, tab, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem,
+  prep_unit<DK, DV>(p, maps, tab, bwd, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem,
                 ctl->bar, phase, lphase, vphase, nullptr);
   cta_teardown(ctl, 256);
 }
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_prep_tc(Params p,
 // leaves by a bulk store from shared memory (the fp32 state through two staging
 // buffers): global stores issued by the threads themselves would hold up their next
 // proxy fence until they drain.
-template <int DK>
+template <int DK, int DV>   // DV: the value head size when fixed, else 0 (p.Dv)
 __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint32_t tmem,
                                uint64_t* bars) {
   const int kh = key_head(p, h);
@@ -673,7 +673,7 @@ __device__ void fwd_state_unit(const Params& p, int n, int h, uint8_t* sm, uint3
   }
   constexpr int NKC = (DK + 16 * kGroups - 1) / (16 * kGroups);   // S^T pieces per thread
   constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read K MN-major
-  const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
+  const int Dv = DV > 0 ? DV : p.Dv, MV = Dv < 64 ? 64 : Dv;
   const int tid = threadIdx.x, grp = col_group();
   const uint32_t bW = (uint32_t)tileCD(DK);
   // G slot: the chunk's G (C floats), or e^{G_last} per channel for KDA (DK floats)
@@ -1082,13 +1082,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_fwd_out_tc(Params p) {
   cta_teardown(ctl, 256);
 }
 
-template <int DK>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_state_tc(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
   cta_setup(ctl, 4, 512);
-  fwd_state_unit<DK>(p, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
+  fwd_state_unit<DK, DV>(p, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
   cta_teardown(ctl, 512);
 }
 
@@ -1097,7 +1097,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_state_tc(Params p) {
 // the others prepare (chunk, key head) units in chunk order, taken from a work
 // counter, and publish each one's flag; a walk waits for the flag of the chunk it
 // needs next.  Walks never block the preparation, so the launch always finishes.
-template <int DK>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   stamp_kept_operands(p);
@@ -1149,7 +1149,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
         uint32_t phase = 0, lphase = 0, vphase = 0;
         // every load and product of the unit has completed when it returns, and every
         // write came before its last barrier
-        prep_unit<DK>(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
+        prep_unit<DK, DV>(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes, ctl->tmem,
                   ctl->bar, phase, lphase, vphase, nullptr);
         if (threadIdx.x == 0) {
           publish_flag(p.fready + u);
@@ -1163,7 +1163,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
         __syncthreads();
       }
     }
-    fwd_state_unit<DK>(p, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes, ctl->tmem,
+    fwd_state_unit<DK, DV>(p, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes, ctl->tmem,
                        ctl->bar);
     if (threadIdx.x == 0 && p.oready) atomicAdd(p.fwork + 2, 1u);
   } else {
@@ -1185,7 +1185,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fwd_fused_tc(Params p,
         next = (int)atomicAdd(p.fwork, 1u);
         link.next = next;
       }
-      const bool ok = prep_unit<DK>(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes,
+      const bool ok = prep_unit<DK, DV>(p, maps, tab, p.keep, u / p.Hk, u % p.Hk, base + kCtlBytes,
                                 ctl->tmem, ctl->bar, phase, lphase, vphase, &link);
       if (threadIdx.x == 0) {
         if (link.pending >= 0) {   // a unit that stopped before its stores
@@ -1251,13 +1251,19 @@ static size_t fwd_state_tc_smem(const Params& p) {
          kCtlBytes + 1024;
 }
 
+// The instantiations with the value head size fixed when it equals the key head size.
+template <int DK>
+static void (*prep_kernel(const Params& p))(Params, TmaMaps, int) {
+  return p.Dv == DK ? k_prep_tc<DK, DK> : k_prep_tc<DK, 0>;
+}
+
 cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaStream_t st) {
   if (p.NC == 0) return cudaSuccess;
   const size_t smem = prep_tc_smem(p);
-  auto kern = p.Dk == 128 ? k_prep_tc<128>
-              : p.Dk == 64 ? k_prep_tc<64>
-              : p.Dk == 32 ? k_prep_tc<32>
-                           : k_prep_tc<16>;
+  auto kern = p.Dk == 128 ? prep_kernel<128>(p)
+              : p.Dk == 64 ? prep_kernel<64>(p)
+              : p.Dk == 32 ? prep_kernel<32>(p)
+                           : prep_kernel<16>(p);
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, bwd ? KID_PREP_TC_FULL : KID_PREP_TC);
   kern<<<dim3(p.NC, p.Hk), kTcThreads, smem, st>>>(p, maps, bwd ? 1 : 0);
@@ -1268,9 +1274,10 @@ cudaError_t launch_prep_tc(const Params& p, const TmaMaps& maps, bool bwd, cudaS
 template <int DK>
 static cudaError_t launch_fwd_state_tc_t(const Params& p, cudaStream_t st) {
   const size_t smem = fwd_state_tc_smem<DK>(p);
-  cudaFuncSetAttribute(k_fwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = p.Dv == DK ? k_fwd_state_tc<DK, DK> : k_fwd_state_tc<DK, 0>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_FWD_STATE_TC);
-  k_fwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kTcThreads, smem, st>>>(p);
+  kern<<<dim3(p.n_seqs, p.Hv), kTcThreads, smem, st>>>(p);
   profile_post(st);
   return cudaGetLastError();
 }
@@ -1288,7 +1295,7 @@ cudaError_t launch_fwd_state_tc(const Params& p, cudaStream_t st) {
 // The fused forward (k_fwd_fused_tc) when the walks leave at least kMinProducers SMs
 // to the preparation and one CTA fits per SM; *launched = false otherwise (the caller
 // then runs the preparation and the walk as two launches).
-template <int DK>
+template <int DK, int DV>
 static cudaError_t launch_fwd_fused_t(const Params& p, const TmaMaps& maps, cudaStream_t st,
                                       bool* launched) {
   *launched = false;
@@ -1297,11 +1304,11 @@ static cudaError_t launch_fwd_fused_t(const Params& p, const TmaMaps& maps, cuda
   if (sms <= 0 || walks + kMinProducers > sms || p.NC == 0) return cudaSuccess;
   const size_t a = prep_tc_smem(p), b = fwd_state_tc_smem<DK>(p);
   const size_t smem = (a > b ? a : b) + 64;
-  cudaError_t e = cudaFuncSetAttribute(k_fwd_fused_tc<DK>,
+  cudaError_t e = cudaFuncSetAttribute(k_fwd_fused_tc<DK, DV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_fused_tc<DK>, kTcThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_fused_tc<DK, DV>, kTcThreads, smem);
   if (e != cudaSuccess || per_sm < 1) return cudaSuccess;
   Params pp = p;
   pp.fready = p.fwork + 64;             // the work counters' 256-byte slot, then the flags
@@ -1309,20 +1316,27 @@ static cudaError_t launch_fwd_fused_t(const Params& p, const TmaMaps& maps, cuda
   TmaMaps mm = maps;
   void* args[] = {&pp, &mm};
   profile_pre(st, KID_FWD_FUSED_TC);
-  e = cudaLaunchCooperativeKernel((const void*)k_fwd_fused_tc<DK>, dim3(sms), dim3(kTcThreads), args,
+  e = cudaLaunchCooperativeKernel((const void*)k_fwd_fused_tc<DK, DV>, dim3(sms), dim3(kTcThreads), args,
                                   smem, st);
   profile_post(st);
   if (e == cudaSuccess) *launched = true;
   return e;
 }
 
+template <int DK>
+static cudaError_t launch_fwd_fused_dk(const Params& p, const TmaMaps& maps, cudaStream_t st,
+                                       bool* launched) {
+  return p.Dv == DK ? launch_fwd_fused_t<DK, DK>(p, maps, st, launched)
+                    : launch_fwd_fused_t<DK, 0>(p, maps, st, launched);
+}
+
 cudaError_t launch_fwd_fused_tc(const Params& p, const TmaMaps& maps, cudaStream_t st,
                                 bool* launched) {
   switch (p.Dk) {
-    case 16: return launch_fwd_fused_t<16>(p, maps, st, launched);
-    case 32: return launch_fwd_fused_t<32>(p, maps, st, launched);
-    case 64: return launch_fwd_fused_t<64>(p, maps, st, launched);
-    default: return launch_fwd_fused_t<128>(p, maps, st, launched);
+    case 16: return launch_fwd_fused_dk<16>(p, maps, st, launched);
+    case 32: return launch_fwd_fused_dk<32>(p, maps, st, launched);
+    case 64: return launch_fwd_fused_dk<64>(p, maps, st, launched);
+    default: return launch_fwd_fused_dk<128>(p, maps, st, launched);
   }
 }
 
