@@ -28,7 +28,7 @@ __device__ __forceinline__ size_t tileCD(int D) { return (size_t)((D + 63) / 64)
 // bwd_state_tc_smem bytes; `tmem`: 512 columns; bars[0..2]: MMA and the two load
 // buffers).  In a fused launch (p.bready set) chunk c's flag is published once its dS^T
 // and -dDelta tiles have reached global memory.
-template <int DK>
+template <int DK, int DV>   // DV: the value head size when fixed, else 0 (p.Dv)
 __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int h, uint8_t* sm,
                                uint32_t tmem, uint64_t* bars) {
   const int kh = key_head(p, h);
@@ -39,7 +39,7 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
     return;
   }
   constexpr int NKC = (DK + 16 * kGroups - 1) / (16 * kGroups);   // dS^T pieces per thread
-  const int Dv = p.Dv, MV = Dv < 64 ? 64 : Dv;
+  const int Dv = DV > 0 ? DV : p.Dv, MV = Dv < 64 ? 64 : Dv;
   const int tid = threadIdx.x, grp = col_group();
   constexpr int NKF = DK < 64 ? 64 : DK;        // N of products read Q / W MN-major
   const uint32_t bK = (uint32_t)tileCD(DK), bP = 8192, bG = C * 4;
@@ -249,7 +249,7 @@ __device__ void bwd_state_unit(const Params& p, const TmaMaps& maps, int n, int 
   __syncthreads();
 }
 
-template <int DK>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_state_tc(Params p,
                                                                const __grid_constant__ TmaMaps maps) {
   if (kept_operands_missing(p)) return;
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_state_tc(Params p,
   uint8_t* base = align1024(smem_raw);
   CtaCtl* ctl = (CtaCtl*)base;
   cta_setup(ctl, 4, 512);
-  bwd_state_unit<DK>(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
+  bwd_state_unit<DK, DV>(p, maps, blockIdx.x, blockIdx.y, base + kCtlBytes, ctl->tmem, ctl->bar);
   cta_teardown(ctl, 512);
 }
 
@@ -1033,7 +1033,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bwd_fused_tc(Params p,
   cta_setup(ctl, 4, 512);
   const int walks = p.n_seqs * p.Hv;
   if ((int)blockIdx.x < walks) {
-    bwd_state_unit<DK>(p, maps, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes,
+    bwd_state_unit<DK, DV>(p, maps, blockIdx.x / p.Hv, blockIdx.x % p.Hv, base + kCtlBytes,
                        ctl->tmem, ctl->bar);
     // fresh mbarriers for the gradient role
     if (threadIdx.x == 0) {
@@ -1103,9 +1103,10 @@ static size_t grads_tc_smem() {
 template <int DK>
 static cudaError_t launch_bwd_state_tc_t(const Params& p, const TmaMaps& maps, cudaStream_t st) {
   const size_t smem = bwd_state_tc_smem<DK>(p);
-  cudaFuncSetAttribute(k_bwd_state_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = p.Dv == DK ? k_bwd_state_tc<DK, DK> : k_bwd_state_tc<DK, 0>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   profile_pre(st, KID_BWD_STATE_TC);
-  k_bwd_state_tc<DK><<<dim3(p.n_seqs, p.Hv), kTcThreads, smem, st>>>(p, maps);
+  kern<<<dim3(p.n_seqs, p.Hv), kTcThreads, smem, st>>>(p, maps);
   profile_post(st);
   return cudaGetLastError();
 }
