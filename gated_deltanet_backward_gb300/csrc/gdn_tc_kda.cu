@@ -143,8 +143,9 @@ __device__ void tri_inverse_one_head(float* Tm, float* M) {
 // G[16 j] - G[16 j + 15], so the block's own pairs come from the product only where
 // that stays below kKdaWide for every channel (e^60 keeps the operand, and the masked
 // entries above the diagonal, far from overflow and the block's own factor
-// e^{G[r] - G[16 j]} far from underflow).  A block whose gates decay faster zeroes those rows of the operand and sums its
-// 136 pairs channel by channel on CUDA cores, eight threads a pair, every exponent <= 0.
+// e^{G[r] - G[16 j]} far from underflow).  A block whose gates decay faster zeroes those
+// rows of the operand and sums its 136 pairs channel by channel on CUDA cores, eight
+// threads a pair, every exponent <= 0.
 // Then T = (I + A)^-1, W = T diag(b) (K e^G) and U^T = V^T (T diag(b))^T on the tensor
 // core, and the operands of the walk and the output: K e^{G_last - G} (the state
 // update), Q e^G (the output's inter-chunk term), e^{G_last} (the walk's per-channel
@@ -190,10 +191,12 @@ __device__ void kda_prep_unit(const Params& p, const TmaMaps& maps, int c, int h
   // [128][Dk] block-scaled K; Q rows of the intra-chunk products, over tTB .. tKg (which
   // are written only after those products)
   uint8_t* tXs = tTB;
-  uint8_t* tKn = tKg + bKC;                    // [160][Dk] block-scaled K: block j's rows from 8 j (j+1) on
+  uint8_t* tKn = tKg + bKC;                    // [160][Dk] block-scaled K (block j from row
+                                               // 8 j (j + 1) on)
   float* Gf = (float*)(tKn + nbk * 160 * 128); // [C][kGS] G
   float* Tm = Gf + C * kGS;                    // [C][TS] A, then T
-  float* Mt = Tm + C * TS;                     // [1024] diagonal blocks of P, then scratch of the inverse
+  float* Mt = Tm + C * TS;                     // [1024] diagonal blocks of P, then the
+                                               // inverse's scratch
   float* bv = Mt + 1024;                       // [C] beta
   int* wide = (int*)(bv + C);                  // [4] block decays faster than kKdaWide
   const uint32_t tAccW = tmem, tAccU = tmem + 128;
