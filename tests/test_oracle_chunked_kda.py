@@ -12,7 +12,10 @@ token-by-token KDA oracle, in f64:
   restatement (oracle/chunked.py), which is pinned on its own;
 * a design check for a tensor-core kernel: computed in fp32 with bf16 operands in every
   product, the blocked form stays within 1e-2 (about 5e-3 measured) of the token oracle,
-  inside the 2e-2 bar of bf16 outputs.
+  inside the 2e-2 bar of bf16 outputs;
+* the same with a block's own pairs also formed as a bf16 product through the block's
+  first row, wherever the block decays by at most e^60 (the kernel's choice), for gates
+  whose blocks sit just below and just above that bound.
 """
 import numpy as np
 import pytest
@@ -123,11 +126,16 @@ def _bf16(x):
     return u.astype(np.uint32).view(np.float32)
 
 
-def _blocked_forward_bf16_operands(d, cu, kw, chunk=64, sub=16):
+def _blocked_forward_bf16_operands(d, cu, kw, chunk=64, sub=16, diag_product=False,
+                                   wide=60.0, stats=None):
     """The blocked chunked forward with the arithmetic a tensor-core kernel would use: fp32
     throughout, and every product (the off-diagonal Gram blocks, U, W, W S, Qg S, P Delta
     and the state update) fed bf16-rounded operands with fp32 accumulation.  The
-    diagonal Gram blocks and the triangular solve stay fp32."""
+    triangular solve stays fp32.  The diagonal Gram blocks are fp32 pairwise sums, or,
+    with diag_product, products of bf16 operands through the block's first row as well
+    (X e^{G - G[a0]} against K e^{G[a0] - G}, masked to the lower triangle) wherever the
+    block's own decay (the sum of its rows' log gates) stays below `wide` on every
+    channel; `stats` (a list) then collects each such block's decay."""
     f = lambda a: np.asarray(a, np.float32)
 
     def gram(X, K, G, strict):
@@ -135,9 +143,18 @@ def _blocked_forward_bf16_operands(d, cu, kw, chunk=64, sub=16):
         out = np.zeros((c, c), np.float32)
         for a0 in range(0, c, sub):
             a1 = min(a0 + sub, c)
-            for r in range(a0, a1):
-                for s in range(a0, r + (0 if strict else 1)):
-                    out[r, s] = (X[r] * K[s] * np.exp(G[r] - G[s])).sum(dtype=np.float32)
+            decay = float(((G[a0 - 1] if a0 > 0 else 0.0) - G[a1 - 1]).max())
+            if diag_product and decay <= wide:
+                full = _bf16(X[a0:a1] * np.exp(G[a0:a1] - G[a0])) @ \
+                    _bf16(K[a0:a1] * np.exp(G[a0] - G[a0:a1])).T
+                assert np.isfinite(full).all()   # the masked entries above the diagonal too
+                out[a0:a1, a0:a1] = np.tril(full, -1 if strict else 0)
+                if stats is not None:
+                    stats.append(decay)
+            else:
+                for r in range(a0, a1):
+                    for s in range(a0, r + (0 if strict else 1)):
+                        out[r, s] = (X[r] * K[s] * np.exp(G[r] - G[s])).sum(dtype=np.float32)
             if a0 > 0:
                 out[a0:a1, :a0] = _bf16(X[a0:a1] * np.exp(G[a0:a1] - G[a0])) @ \
                     _bf16(K[:a0] * np.exp(G[a0] - G[:a0])).T
@@ -184,3 +201,34 @@ def test_blocked_form_with_bf16_operands_stays_inside_the_bf16_bar(strong):
     oc, Sc = _blocked_forward_bf16_operands(d, cu, kw)
     assert np.isfinite(oc).all() and np.isfinite(Sc).all()
     assert _rel(oc, o) < 1e-2 and _rel(Sc, S_T) < 1e-2
+
+
+@pytest.mark.parametrize("gates", ["typical", "near_e60", "strong"])
+def test_diagonal_blocks_through_the_product_stay_inside_the_bf16_bar(gates):
+    """Design check of the tensor-core kernel's own choice: a 16-row block's own pairs also
+    go through the bf16 product, referenced to the block's first row, wherever the block
+    decays by at most e^60 on every channel (the operand factor K e^{G[a0] - G} then
+    reaches e^60, and the masked entries above the diagonal stay finite in fp32); faster
+    blocks keep the pairwise sums.  With typical gates, with half the channels losing
+    ~3.7 nats a token (blocks just below and above e^60) and with 12 nats a token, the
+    forward stays inside the bf16 bar of the f64 token oracle."""
+    d, cu, kw = _inputs(13, seqlens=(150, 41), Hk=1, Hv=2, Dk=32, Dv=32,
+                        strong=gates == "strong")
+    if gates == "near_e60":
+        rng = np.random.default_rng(5)
+        d["a_log"][:] = 0.0
+        d["b_alpha"][:] = 0.0
+        x = d["alpha"].reshape(int(cu[-1]), kw["Hv"], kw["Dk"])
+        x[:, :, 0::2] = 3.7 + 0.05 * rng.standard_normal(x[:, :, 0::2].shape)
+    o, S_T = _token_fwd(d, cu, kw)
+    stats = []
+    oc, Sc = _blocked_forward_bf16_operands(d, cu, kw, diag_product=True, stats=stats)
+    assert np.isfinite(oc).all() and np.isfinite(Sc).all()
+    assert _rel(oc, o) < 1e-2 and _rel(Sc, S_T) < 1e-2
+    if gates == "typical":
+        assert stats and max(stats) < 60.0
+    if gates == "near_e60":
+        assert stats and max(stats) > 55.0     # factors near e^60 were exercised
+    if gates == "strong":
+        assert not stats                       # every block decays past e^60
+
